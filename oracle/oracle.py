@@ -1,0 +1,171 @@
+"""Python front end of the CPU oracle (fp64, plain loops in C).
+
+TEST INFRASTRUCTURE ONLY: the tests, the package smoke check and the
+benchmark's CPU-baseline leg use it.  It never imports the product package's
+compiled library and the product never imports this module.
+
+``build()`` compiles ``lora_oracle.c`` with gcc (OpenMP when available) into
+``oracle/_build/liboracle.so``.  The functions below marshal CPU torch tensors
+into the C calls; every arithmetic step happens in the C file.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import List, Optional, Sequence
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lora_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle; returns the path of the shared object."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", _SRC, "-o", tmp]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       stdout=subprocess.PIPE, stderr=subprocess.PIPE)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        p, i64, i32, dbl = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_double
+        lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_build_segments.restype = ctypes.c_int
+        lib.oracle_build_segments.argtypes = [p, i64, i32, p, p, p, p, p, p, p, p]
+        lib.oracle_lora_linear_rows.restype = None
+        lib.oracle_lora_linear_rows.argtypes = [p, i64, i64, p, i64, p, p, i32, p, p, p, dbl,
+                                                p, i64, p]
+        lib.oracle_shrink_rows.restype = None
+        lib.oracle_shrink_rows.argtypes = [p, i64, i64, p, i32, p, p, p, i64, i64, p]
+        lib.oracle_expand_rows.restype = None
+        lib.oracle_expand_rows.argtypes = [p, i64, p, i64, p, i32, p, p, dbl, p, i64, p]
+        _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers (no arithmetic)
+# ---------------------------------------------------------------------------
+
+def _bits(t: Optional[torch.Tensor]) -> Optional[np.ndarray]:
+    """bf16 tensor -> contiguous uint16 numpy array of its raw bits."""
+    if t is None:
+        return None
+    assert t.dtype == torch.bfloat16
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _concat(mats: List[torch.Tensor], K_or_N: int) -> np.ndarray:
+    if not mats:
+        return np.zeros(1, dtype=np.uint16)
+    return _bits(torch.cat([m.reshape(-1) for m in mats]).contiguous())
+
+
+def _rows_arg(rows, M):
+    if rows is None:
+        return None, M
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    assert r.ndim == 1 and (r.size == 0 or (r.min() >= 0 and r.max() < M))
+    return r, r.size
+
+
+# ---------------------------------------------------------------------------
+# public oracle calls
+# ---------------------------------------------------------------------------
+
+def build_segments(ids, num_adapters: int, true_ranks: Sequence[int]):
+    """Segment table of "vLLM-Ascend dynamic LoRA" §2.3 (stable sort by id).
+
+    Returns a dict of numpy int32 arrays: perm, bucket_offsets, seg_id,
+    seg_start, seg_len, seg_rank (padded), plus num_segments and invalid.
+    """
+    lib = _load()
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    M = ids.size
+    A = int(num_adapters)
+    rk = np.ascontiguousarray(np.asarray(list(true_ranks) or [0], dtype=np.int32))
+    perm = np.zeros(max(M, 1), np.int32)
+    off = np.zeros(A + 2, np.int32)
+    sid, sst, sln, srk = (np.zeros(max(A, 1), np.int32) for _ in range(4))
+    ns = np.zeros(1, np.int32)
+    invalid = lib.oracle_build_segments(_ptr(ids), M, A, _ptr(rk), _ptr(perm), _ptr(off),
+                                        _ptr(sid), _ptr(sst), _ptr(sln), _ptr(srk), _ptr(ns))
+    n = int(ns[0])
+    return dict(perm=perm[:M], bucket_offsets=off, seg_id=sid[:n], seg_start=sst[:n],
+                seg_len=sln[:n], seg_rank=srk[:n], num_segments=n, invalid=int(invalid))
+
+
+def lora_linear(wl, rows=None, scale: Optional[float] = None) -> np.ndarray:
+    """fp64 layer output for a Workload-like object (fields x, W, bias, ids,
+    ranks, A, B, scale).  ``rows`` selects output rows; returns [len(rows), N]."""
+    lib = _load()
+    x, W, bias = _bits(wl.x), _bits(wl.W), _bits(wl.bias)
+    ids = np.ascontiguousarray(wl.ids.numpy().astype(np.int32))
+    rk = np.ascontiguousarray(np.asarray(list(wl.ranks) or [0], dtype=np.int32))
+    a_cat, b_cat = _concat(wl.A, wl.K), _concat(wl.B, wl.N)
+    r, nrows = _rows_arg(rows, wl.M)
+    y = np.zeros((nrows, wl.N), dtype=np.float64)
+    s = wl.scale if scale is None else scale
+    lib.oracle_lora_linear_rows(_ptr(x), wl.M, wl.K, _ptr(W), wl.N, _ptr(bias), _ptr(ids),
+                                len(wl.ranks), _ptr(rk), _ptr(a_cat), _ptr(b_cat), float(s),
+                                _ptr(r), nrows, _ptr(y))
+    return y
+
+
+def shrink(wl, s_cols: int, rows=None) -> np.ndarray:
+    """fp64 S = x A_id^T, [len(rows), s_cols], zero outside each row's rank."""
+    lib = _load()
+    x = _bits(wl.x)
+    ids = np.ascontiguousarray(wl.ids.numpy().astype(np.int32))
+    rk = np.ascontiguousarray(np.asarray(list(wl.ranks) or [0], dtype=np.int32))
+    a_cat = _concat(wl.A, wl.K)
+    r, nrows = _rows_arg(rows, wl.M)
+    S = np.zeros((nrows, s_cols), dtype=np.float64)
+    lib.oracle_shrink_rows(_ptr(x), wl.M, wl.K, _ptr(ids), len(wl.ranks), _ptr(rk),
+                           _ptr(a_cat), _ptr(r), nrows, s_cols, _ptr(S))
+    return S
+
+
+def expand(wl, S: torch.Tensor, y_in: torch.Tensor, scale: Optional[float] = None,
+           rows=None) -> np.ndarray:
+    """fp64 y_in + scale * S B_id^T for the given fp32 S [M, s_cols] and bf16 y_in [M, N]."""
+    lib = _load()
+    S_np = np.ascontiguousarray(S.detach().cpu().float().numpy())
+    yin = _bits(y_in)
+    ids = np.ascontiguousarray(wl.ids.numpy().astype(np.int32))
+    rk = np.ascontiguousarray(np.asarray(list(wl.ranks) or [0], dtype=np.int32))
+    b_cat = _concat(wl.B, wl.N)
+    r, nrows = _rows_arg(rows, wl.M)
+    y = np.zeros((nrows, wl.N), dtype=np.float64)
+    s = wl.scale if scale is None else scale
+    lib.oracle_expand_rows(_ptr(S_np), S_np.shape[1], _ptr(yin), wl.N, _ptr(ids),
+                           len(wl.ranks), _ptr(rk), _ptr(b_cat), float(s), _ptr(r), nrows,
+                           _ptr(y))
+    return y

@@ -1,0 +1,230 @@
+"""Seeded synthetic workloads for the multi-LoRA linear layer.
+
+This module only draws inputs; it holds none of the layer's arithmetic, so the
+CPU oracle and the CUDA path can both consume it without sharing any of the
+computation.  Everything is drawn on the CPU with a ``torch.Generator`` seeded
+per workload, in fp32, and rounded to bf16 exactly once.
+
+Shapes and value distributions follow the five benchmark configurations of
+this project (tiny / decode / prefill / merged-QKV / MLP-down).  The weight
+shapes follow "vLLM-Ascend dynamic LoRA" (pptc.cn/news/149022) §1.1: A_i is
+[r_i, K], B_i is [N, r_i], W is [N, K] (torch ``nn.Linear`` convention), and
+``lora_id_map`` has one int32 per token with -1 meaning "no adapter" (§2.1).
+
+Notation: ``N(0, s)`` means a normal distribution with standard deviation s.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import List, Optional
+
+import torch
+
+CONFIG_NAMES = ("tiny", "decode", "prefill", "qkv", "mlp_down")
+
+
+@dataclass
+class Workload:
+    """One seeded instance of the layer's inputs (all CPU tensors)."""
+
+    name: str
+    M: int
+    K: int
+    N: int
+    ranks: List[int]                 # true rank r_i of each adapter
+    ids: torch.Tensor                # int32 [M], -1 = base only
+    x: torch.Tensor                  # bf16 [M, K]
+    W: torch.Tensor                  # bf16 [N, K]
+    bias: Optional[torch.Tensor]     # bf16 [N] or None
+    A: List[torch.Tensor]            # bf16 [r_i, K] per adapter
+    B: List[torch.Tensor]            # bf16 [N, r_i] per adapter
+    scale: float
+    seed: int = 0
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def num_adapters(self) -> int:
+        return len(self.ranks)
+
+    def describe(self) -> str:
+        nz = int((self.ids >= 0).sum())
+        return (f"{self.name}: M={self.M} K={self.K} N={self.N} adapters={self.num_adapters} "
+                f"lora_tokens={nz} scale={self.scale}")
+
+
+# --------------------------------------------------------------------------
+# id-structure generators (structure only, no layer arithmetic)
+# --------------------------------------------------------------------------
+
+def _zipf_probs(n: int, s: float) -> torch.Tensor:
+    k = torch.arange(1, n + 1, dtype=torch.float64)
+    p = k.pow(-s)
+    return p / p.sum()
+
+
+def _renormalise_lengths(lengths: List[int], total: int) -> List[int]:
+    """Scale request lengths so they sum to ``total`` exactly.
+
+    floor(L_j * total / sum L) (at least 1), then the remainder is handed out
+    +1 at a time to the largest fractional parts, ties broken by lower j.
+    """
+    s = sum(lengths)
+    exact = [L * total / s for L in lengths]
+    out = [max(1, int(math.floor(e))) for e in exact]
+    rem = total - sum(out)
+    order = sorted(range(len(lengths)), key=lambda j: (-(exact[j] - math.floor(exact[j])), j))
+    i = 0
+    while rem > 0:
+        out[order[i % len(order)]] += 1
+        rem -= 1
+        i += 1
+    while rem < 0:  # only possible when many lengths were clamped up to 1
+        j = max(range(len(out)), key=lambda q: (out[q], -q))
+        out[j] -= 1
+        rem += 1
+    return out
+
+
+def _draw_values(g: torch.Generator, M, K, N, ranks, w_std, a_std, b_std, bias_std, with_bias=True):
+    x = torch.randn(M, K, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    W = (torch.randn(N, K, generator=g, dtype=torch.float32) * w_std).to(torch.bfloat16)
+    bias = None
+    if with_bias:
+        bias = (torch.randn(N, generator=g, dtype=torch.float32) * bias_std).to(torch.bfloat16)
+    A, B = [], []
+    for r in ranks:
+        A.append((torch.randn(r, K, generator=g, dtype=torch.float32) * a_std).to(torch.bfloat16))
+        B.append((torch.randn(N, r, generator=g, dtype=torch.float32) * b_std).to(torch.bfloat16))
+    return x, W, bias, A, B
+
+
+def make_config(name_or_index, seed: Optional[int] = None) -> Workload:
+    """Build one of the five benchmark configurations.
+
+    ``seed`` defaults to 1234 + the configuration index.
+    """
+    if isinstance(name_or_index, int):
+        idx = name_or_index
+        name = CONFIG_NAMES[idx]
+    else:
+        name = name_or_index
+        idx = CONFIG_NAMES.index(name)
+    if seed is None:
+        seed = 1234 + idx
+    g = torch.Generator().manual_seed(seed)
+    meta = {}
+
+    if name == "tiny":
+        M, K, N = 64, 256, 256
+        ranks = [8, 8, 16, 16]
+        ids = torch.randint(-1, 4, (M,), generator=g, dtype=torch.int64)
+        w_std, bias_std, b_std, scale = 0.02, 0.01, 0.02, 2.0
+
+    elif name == "decode":
+        M, K, N = 32, 4096, 4096
+        nA = 20
+        choices = torch.tensor([16, 32, 64])
+        ranks = choices[torch.randint(0, 3, (nA,), generator=g)].tolist()
+        ids = torch.randint(0, nA, (M,), generator=g, dtype=torch.int64)
+        drop = torch.rand(M, generator=g) < 0.10
+        ids[drop] = -1
+        w_std, bias_std, b_std, scale = 0.02, 0.01, 0.02, 2.0
+
+    elif name == "prefill":
+        M, K, N = 1024, 4096, 4096
+        nA, nreq = 40, 16
+        choices = torch.tensor([16, 32, 64])
+        ranks = choices[torch.randint(0, 3, (nA,), generator=g)].tolist()
+        lengths = torch.randint(16, 129, (nreq,), generator=g).tolist()
+        lengths = _renormalise_lengths(lengths, M)
+        req_ids = torch.randint(0, nA, (nreq,), generator=g).tolist()
+        base_only = (torch.rand(nreq, generator=g) < 0.05).tolist()
+        parts = []
+        for L, a, b in zip(lengths, req_ids, base_only):
+            parts.append(torch.full((L,), -1 if b else a, dtype=torch.int64))
+        ids = torch.cat(parts)
+        meta["request_lengths"] = lengths
+        w_std, bias_std, b_std, scale = 0.02, 0.01, 0.02, 2.0
+
+    elif name == "qkv":
+        M, K, N = 2048, 4096, 6144
+        nA = 8
+        ranks = [64] * nA
+        p = _zipf_probs(nA, 1.1)
+        ids = torch.multinomial(p, M, replacement=True, generator=g).to(torch.int64)
+        drop = torch.rand(M, generator=g) < 0.20
+        ids[drop] = -1
+        w_std, bias_std, b_std, scale = 0.02, 0.01, 0.02, 2.0
+
+    elif name == "mlp_down":
+        M, K, N = 8192, 12288, 4096
+        nA = 32
+        choices = torch.tensor([16, 32, 64])
+        ranks = choices[torch.randint(0, 3, (nA,), generator=g)].tolist()
+        p = _zipf_probs(nA, 1.1)
+        lengths, total = [], 0
+        while total < M:
+            L = int(torch.randint(64, 513, (1,), generator=g))
+            L = min(L, M - total)
+            lengths.append(L)
+            total += L
+        nreq = len(lengths)
+        req_ids = torch.multinomial(p, nreq, replacement=True, generator=g).tolist()
+        base_only = (torch.rand(nreq, generator=g) < 0.20).tolist()
+        parts = []
+        for L, a, b in zip(lengths, req_ids, base_only):
+            parts.append(torch.full((L,), -1 if b else a, dtype=torch.int64))
+        ids = torch.cat(parts)
+        meta["request_lengths"] = lengths
+        w_std, bias_std, b_std, scale = 0.01, 0.01, 0.02, 1.0
+    else:
+        raise ValueError(f"unknown config {name!r}")
+
+    a_std = 1.0 / math.sqrt(K)
+    x, W, bias, A, B = _draw_values(g, M, K, N, ranks, w_std, a_std, b_std, bias_std)
+    return Workload(name=name, M=M, K=K, N=N, ranks=list(ranks), ids=ids.to(torch.int32),
+                    x=x, W=W, bias=bias, A=A, B=B, scale=scale, seed=seed, meta=meta)
+
+
+def make_custom(M: int, K: int, N: int, ranks: List[int], seed: int, ids=None,
+                id_mode: str = "uniform", p_base: float = 0.1, scale: float = 2.0,
+                with_bias: bool = True, w_std: float = 0.02) -> Workload:
+    """A free-form workload for edge cases.
+
+    ``ids`` may be given explicitly; otherwise ``id_mode`` picks the structure:
+    "uniform" (i.i.d. over adapters, then -1 with probability p_base),
+    "runs" (contiguous runs of random length), "all_base" (every id -1),
+    "single" (every token uses adapter 0).
+    """
+    g = torch.Generator().manual_seed(seed)
+    nA = len(ranks)
+    if ids is not None:
+        ids = torch.as_tensor(ids, dtype=torch.int64)
+    elif id_mode == "all_base" or nA == 0:
+        ids = torch.full((M,), -1, dtype=torch.int64)
+    elif id_mode == "single":
+        ids = torch.zeros(M, dtype=torch.int64)
+    elif id_mode == "uniform":
+        ids = torch.randint(0, nA, (M,), generator=g, dtype=torch.int64)
+        ids[torch.rand(M, generator=g) < p_base] = -1
+    elif id_mode == "runs":
+        parts, total = [], 0
+        while total < M:
+            L = min(int(torch.randint(1, 200, (1,), generator=g)), M - total)
+            a = int(torch.randint(-1, nA, (1,), generator=g))
+            parts.append(torch.full((L,), a, dtype=torch.int64))
+            total += L
+        ids = torch.cat(parts) if parts else torch.zeros(0, dtype=torch.int64)
+    else:
+        raise ValueError(id_mode)
+    a_std = 1.0 / math.sqrt(K)
+    x, W, bias, A, B = _draw_values(g, M, K, N, ranks, w_std, a_std, 0.02, 0.01, with_bias)
+    return Workload(name=f"custom_M{M}_K{K}_N{N}", M=M, K=K, N=N, ranks=list(ranks),
+                    ids=ids.to(torch.int32), x=x, W=W, bias=bias, A=A, B=B, scale=scale, seed=seed)
+
+
+def random_fp32(shape, seed: int, std: float = 1.0) -> torch.Tensor:
+    """A seeded fp32 tensor (used as the given S input of the expand step)."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(*shape, generator=g, dtype=torch.float32) * std

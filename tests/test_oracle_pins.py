@@ -1,0 +1,239 @@
+"""Pins of the CPU oracle to facts fixed by the pages and by mathematics.
+
+None of these re-types the oracle's own loops: each compares it with an
+independent route (a library matmul on a special case, a closed-form identity,
+a brute-force Python loop on tiny inputs, a worked example printed on the
+page, or an invariant).  Source: "vLLM-Ascend dynamic LoRA"
+(pptc.cn/news/149022), sections cited per test.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle
+from segmented_gemm_gb300 import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def f64(t):
+    return t.to(torch.float64).numpy()
+
+
+def _rel_close(a, b, rtol=1e-11):
+    scale = np.maximum(1.0, np.abs(b))
+    return np.max(np.abs(a - b) / scale) <= rtol
+
+
+# ----------------------------------------------------------------------------
+# segment table (§2.3)
+# ----------------------------------------------------------------------------
+
+def test_segments_page_example():
+    """§2.3 worked example: ids [0, 2, 0, 1] -> same-id tokens contiguous."""
+    g = json.load(open(os.path.join(GOLDEN, "segments_p5_example.json")))
+    s = oracle.build_segments(g["ids"], g["num_adapters"], g["true_ranks"])
+    assert s["perm"].tolist() == g["perm"]
+    assert s["bucket_offsets"].tolist() == g["bucket_offsets"]
+    got = [dict(id=int(i), start=int(a), len=int(b), rank=int(r))
+           for i, a, b, r in zip(s["seg_id"], s["seg_start"], s["seg_len"], s["seg_rank"])]
+    assert got == g["segments"]
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_segments_brute_force(seed):
+    """Stable sort by (id+1, t) computed by Python's sorted() on tiny inputs."""
+    rng = np.random.default_rng(seed)
+    A = int(rng.integers(1, 9))
+    M = int(rng.integers(0, 70))
+    ranks = [int(r) for r in rng.choice([8, 16, 20, 32, 64], size=A)]
+    ids = rng.integers(-1, A, size=M).astype(np.int32)
+    s = oracle.build_segments(ids, A, ranks)
+    want = sorted(range(M), key=lambda t: (int(ids[t]) + 1, t))
+    assert s["perm"].tolist() == want
+    # invariants: permutation, offsets sum to M, each segment one id and contiguous
+    assert sorted(s["perm"].tolist()) == list(range(M))
+    assert s["bucket_offsets"][-1] == M
+    for i, st, ln, rk in zip(s["seg_id"], s["seg_start"], s["seg_len"], s["seg_rank"]):
+        toks = s["perm"][st:st + ln]
+        assert ln > 0 and all(ids[t] == i for t in toks)
+        assert rk % 16 == 0 and rk >= ranks[i] and rk - ranks[i] < 16   # §4.3 padding
+    assert list(s["seg_id"]) == sorted(set(int(v) for v in ids if v >= 0))
+
+
+def test_segments_invalid_ids_are_base_only():
+    s = oracle.build_segments([3, -1, 7, -5, 0], 2, [16, 16])
+    assert s["invalid"] == 3
+    assert s["perm"].tolist() == [0, 1, 2, 3, 4]   # 3, 7, -5 all sorted as -1
+    assert s["seg_id"].tolist() == [0]
+
+
+def test_segments_empty_and_all_base():
+    s = oracle.build_segments([], 3, [16, 16, 16])
+    assert s["num_segments"] == 0 and s["bucket_offsets"].tolist() == [0, 0, 0, 0, 0]
+    s = oracle.build_segments([-1] * 9, 3, [16, 16, 16])
+    assert s["num_segments"] == 0 and s["perm"].tolist() == list(range(9))
+
+
+# ----------------------------------------------------------------------------
+# layer output (§1.1, §2.1, §2.2, §3.4)
+# ----------------------------------------------------------------------------
+
+def test_all_base_equals_library_gemm():
+    """§4.3 / §3.3: with every id -1 the layer is the plain linear x W^T + bias."""
+    wl = workloads.make_custom(40, 96, 72, [16, 32], seed=3, id_mode="all_base")
+    y = oracle.lora_linear(wl)
+    ref = f64(wl.x) @ f64(wl.W).T + f64(wl.bias)[None, :]
+    assert _rel_close(y, ref)
+    wl.bias = None
+    assert _rel_close(oracle.lora_linear(wl), f64(wl.x) @ f64(wl.W).T)
+
+
+@pytest.mark.parametrize("which", [0, 1, 2])
+def test_single_adapter_equals_merged_weight(which):
+    """§1.1: a batch where every token uses adapter i equals the merged linear
+    x (W + scale * B_i A_i)^T + bias; the other adapters sit in the pool too,
+    so a wrong adapter offset or a transposed operand fails here."""
+    wl = workloads.make_custom(24, 80, 56, [8, 32, 16], seed=11 + which, id_mode="single",
+                               scale=1.75)
+    wl.ids[:] = which
+    y = oracle.lora_linear(wl)
+    Wm = f64(wl.W) + wl.scale * f64(wl.B[which]) @ f64(wl.A[which])
+    ref = f64(wl.x) @ Wm.T + f64(wl.bias)[None, :]
+    assert _rel_close(y, ref, 1e-10)
+
+
+def _brute(wl):
+    """Per-token loop written out in Python, for tiny shapes only."""
+    x, W, b = f64(wl.x), f64(wl.W), f64(wl.bias) if wl.bias is not None else None
+    out = np.zeros((wl.M, wl.N))
+    for t in range(wl.M):
+        for n in range(wl.N):
+            v = sum(x[t, k] * W[n, k] for k in range(wl.K))
+            if b is not None:
+                v += b[n]
+            i = int(wl.ids[t])
+            if 0 <= i < len(wl.ranks):
+                A, B = f64(wl.A[i]), f64(wl.B[i])
+                S = [sum(x[t, k] * A[j, k] for k in range(wl.K)) for j in range(wl.ranks[i])]
+                v += wl.scale * sum(S[j] * B[n, j] for j in range(wl.ranks[i]))
+            out[t, n] = v
+    return out
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_per_token_brute_force(seed):
+    """§2.1 / §3.4: each token gets its own base row plus only its own adapter."""
+    wl = workloads.make_custom(8, 24, 16, [8, 16, 4], seed=seed, id_mode="uniform", p_base=0.3,
+                               scale=0.5 + seed)
+    wl.ids[0] = -1
+    wl.ids[1] = 2
+    wl.ids[2] = 9          # names no adapter: treated as base only
+    assert _rel_close(oracle.lora_linear(wl), _brute(wl))
+
+
+def test_row_independence():
+    """A mixed batch's row t equals row t of a batch where every token uses id[t]."""
+    wl = workloads.make_custom(30, 64, 48, [16, 8, 32, 16], seed=5, id_mode="uniform",
+                               p_base=0.25)
+    y = oracle.lora_linear(wl)
+    for i in [-1, 0, 1, 2, 3]:
+        ids = wl.ids.clone()
+        wl2 = workloads.Workload(**{**wl.__dict__, "ids": torch.full_like(ids, i)})
+        yi = oracle.lora_linear(wl2)
+        sel = (ids == i).numpy()
+        assert np.array_equal(y[sel], yi[sel])
+
+
+def test_rank_padding_is_exact():
+    """§4.3: zero rows in A and zero columns in B leave the result unchanged."""
+    wl = workloads.make_custom(12, 48, 40, [8, 20], seed=9, id_mode="uniform", p_base=0.0)
+    y = oracle.lora_linear(wl)
+    A2 = [torch.cat([a, torch.zeros(16 * ((a.shape[0] + 15) // 16) - a.shape[0], a.shape[1],
+                                    dtype=a.dtype)]) for a in wl.A]
+    B2 = [torch.cat([b, torch.zeros(b.shape[0], a.shape[0] - b.shape[1], dtype=b.dtype)], 1)
+          for a, b in zip(A2, wl.B)]
+    wl2 = workloads.Workload(**{**wl.__dict__, "A": A2, "B": B2,
+                                "ranks": [a.shape[0] for a in A2]})
+    assert np.array_equal(y, oracle.lora_linear(wl2))
+
+
+def test_rows_subset_matches_full():
+    wl = workloads.make_custom(20, 32, 24, [16, 16], seed=4)
+    full = oracle.lora_linear(wl)
+    rows = [19, 0, 7, 7, 3]
+    assert np.array_equal(oracle.lora_linear(wl, rows=rows), full[rows])
+
+
+def test_decode_walkthrough_shapes():
+    """§3.4 walk-through: ids [0, 2, -1], K 4096, merged QKV N 12288, ranks 16 / 32.
+    The page prints no values; it pins the -1 passthrough and per-row adapters."""
+    g = json.load(open(os.path.join(GOLDEN, "decode_walkthrough_p5.json")))
+    ranks = [g["ranks"]["0"], 16, g["ranks"]["2"]]
+    wl = workloads.make_custom(g["M"], g["K"], g["N"], ranks, seed=34, ids=g["ids"])
+    y = oracle.lora_linear(wl)
+    x, W, b = f64(wl.x), f64(wl.W), f64(wl.bias)
+    base = x @ W.T + b
+    assert _rel_close(y[2], base[2])                       # id -1 row passes through
+    for row, i in [(0, 0), (1, 2)]:
+        lora = wl.scale * (x[row] @ f64(wl.A[i]).T) @ f64(wl.B[i]).T
+        assert _rel_close(y[row], base[row] + lora, 1e-10)
+        assert not _rel_close(y[row], base[row], 1e-6)     # the LoRA term is really there
+
+
+# ----------------------------------------------------------------------------
+# the two steps alone (§2.2)
+# ----------------------------------------------------------------------------
+
+def test_shrink_matches_library_gemm():
+    wl = workloads.make_custom(26, 72, 40, [16, 48, 8], seed=21, id_mode="uniform", p_base=0.2)
+    S = oracle.shrink(wl, 64)
+    x = f64(wl.x)
+    for t in range(wl.M):
+        i = int(wl.ids[t])
+        want = np.zeros(64)
+        if i >= 0:
+            want[:wl.ranks[i]] = x[t] @ f64(wl.A[i]).T
+        assert _rel_close(S[t], want)
+
+
+def test_expand_matches_library_gemm():
+    wl = workloads.make_custom(18, 40, 56, [16, 32], seed=22, id_mode="uniform", p_base=0.3)
+    S = workloads.random_fp32((wl.M, 32), seed=5)
+    y_in = workloads.random_fp32((wl.M, wl.N), seed=6).to(torch.bfloat16)
+    y = oracle.expand(wl, S, y_in, scale=1.5)
+    for t in range(wl.M):
+        i = int(wl.ids[t])
+        want = f64(y_in[t])
+        if i >= 0:
+            want = want + 1.5 * S[t, :wl.ranks[i]].double().numpy() @ f64(wl.B[i]).T
+        assert _rel_close(y[t], want)
+
+
+def test_linear_is_shrink_then_expand():
+    """§2.2: y = base + scale * (x A^T) B^T, via the two separate steps in fp64."""
+    wl = workloads.make_custom(16, 64, 32, [16, 32, 64], seed=30, id_mode="uniform", p_base=0.2)
+    y = oracle.lora_linear(wl)
+    S = oracle.shrink(wl, 64)
+    base = f64(wl.x) @ f64(wl.W).T + f64(wl.bias)
+    for t in range(wl.M):
+        i = int(wl.ids[t])
+        want = base[t] if i < 0 else base[t] + wl.scale * S[t, :wl.ranks[i]] @ f64(wl.B[i]).T
+        assert _rel_close(y[t], want)
+
+
+def test_config_generators_shapes():
+    for name in workloads.CONFIG_NAMES[:3]:
+        wl = workloads.make_config(name)
+        assert wl.x.shape == (wl.M, wl.K) and wl.W.shape == (wl.N, wl.K)
+        assert wl.ids.shape == (wl.M,) and wl.ids.dtype == torch.int32
+        assert int(wl.ids.min()) >= -1 and int(wl.ids.max()) < wl.num_adapters
+        for a, b, r in zip(wl.A, wl.B, wl.ranks):
+            assert a.shape == (r, wl.K) and b.shape == (wl.N, r)
+    wl = workloads.make_config("prefill")
+    assert sum(wl.meta["request_lengths"]) == 1024 and len(wl.meta["request_lengths"]) == 16
+    # seeded: same seed -> identical draw
+    assert torch.equal(workloads.make_config("tiny").x, workloads.make_config("tiny").x)
