@@ -1,0 +1,225 @@
+/*
+ * lora.h — C ABI of the GB300 (sm_103a) fused dynamic multi-LoRA linear layer.
+ *
+ * The layer (page "vLLM-Ascend dynamic LoRA", pptc.cn/news/149022, §1.1, §2.1):
+ *
+ *     y[t,:] = x[t,:] W^T + bias + (id[t] >= 0 ? scale * (x[t,:] A_id^T) B_id^T : 0)
+ *
+ * x is hidden_states [M, K], W the base weight [N, K] (nn.Linear layout), bias [N]
+ * or none, lora_id_map [M] int32 with -1 meaning "base only" (§2.1), A_i [r_i, K]
+ * and B_i [N, r_i] the adapter factors (§1.1), and the result is [M, N].
+ * `scale` is one fp32 scalar per call (the page's formula has scale 1).
+ *
+ * Conventions for every entry point
+ *   - Pointers named "device" are CUDA device pointers; "host" ones are host
+ *     memory.  Every buffer is owned by the caller; the library never
+ *     allocates, frees, synchronises (except lora_get_status) or copies
+ *     device->host on the compute entry points.
+ *   - bf16 tensors are passed as raw 16-bit patterns (lora_bf16_t), row-major,
+ *     16-byte aligned, with K and N multiples of 8 (rows are TMA-addressable).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). All device
+ *     work of a call is enqueued on it, in order.
+ *   - Return value: LORA_OK, or one of the LORA_ERR_* codes for problems that
+ *     are visible on the host (checked before anything is enqueued, so nothing
+ *     runs).  Problems found on the device (an id outside [-1, num_adapters),
+ *     a bounded wait that gave up) never trap: the kernels finish, treat the
+ *     offending token as base-only, and set bits of a status word inside the
+ *     workspace that lora_get_status returns.
+ *   - Concurrency: two calls that share a workspace must not run at the same
+ *     time on the GPU; weights and the pool must not change while a call that
+ *     reads them is in flight (§4.3, concurrent adapter replacement).
+ */
+#ifndef LORA_GB300_LORA_H
+#define LORA_GB300_LORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t lora_bf16_t;   /* raw bfloat16 bits */
+typedef void *lora_stream_t;    /* cudaStream_t */
+
+/* Host-side status codes (return values). */
+enum {
+    LORA_OK = 0,
+    LORA_ERR_NULL = 1,          /* a required pointer is NULL */
+    LORA_ERR_SHAPE = 2,         /* negative M, K or N not positive multiples of 8, too many adapters */
+    LORA_ERR_ALIGN = 3,         /* a tensor base address is not 16-byte aligned */
+    LORA_ERR_RANK = 4,          /* a rank outside [1, 64], or max_rank not a padded rank */
+    LORA_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than lora_workspace_size() */
+    LORA_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch error, bad device) */
+    LORA_ERR_UNSUPPORTED = 7,   /* device is not sm_103 / sm_100 family or similar */
+    LORA_ERR_SEGMENTS = 8       /* a prebuilt segment table does not match this call */
+};
+
+/* Device-side status bits (returned through lora_get_status). */
+enum {
+    LORA_DEV_BAD_ID = 1 << 0,   /* some id was < -1 or >= num_adapters (treated as -1) */
+    LORA_DEV_TIMEOUT = 1 << 1   /* a bounded wait gave up; that call's output is invalid */
+};
+
+#define LORA_MAX_RANK 64        /* largest padded rank */
+#define LORA_RANK_ALIGN 16      /* ranks are padded to a multiple of this (§4.3) */
+#define LORA_MAX_ADAPTERS 1024  /* largest num_adapters in one pool */
+
+/*
+ * Rank-grouped adapter pool (§2.1: all adapters of one rank stored in one
+ * contiguous region, each adapter's start found by a table lookup on its id;
+ * §2.2: B arranged at load time in the form the second product consumes;
+ * §4.3: ranks padded to a multiple of 16 with zero rows of A / columns of B).
+ *
+ *   A_i  at a_pool + a_offset[i]: [rank[i], K] row-major bf16
+ *        (rows >= true rank are zero).  a_offset[i] is a multiple of K.
+ *   B_i  at b_pool + b_offset[i]: rank[i]/16 column panels, panel p being the
+ *        [N, 16] row-major block B_i[:, 16p : 16p+16]; element (n, j) of B_i
+ *        sits at b_offset[i] + (j/16)*N*16 + n*16 + j%16 (columns >= true rank
+ *        are zero).  b_offset[i] is a multiple of 16.
+ * a_pool, b_pool, a_offset, b_offset, rank: DEVICE pointers, caller-owned.
+ * a_elems / b_elems (host values) are the total element counts of the pools;
+ * num_adapters, max_rank (largest rank[i]), K and N are host values.
+ * lora_pool_layout() computes offsets, padded ranks and sizes for a set of
+ * true ranks; filling the pool is the caller's (adapter loader's) job.
+ */
+typedef struct {
+    const lora_bf16_t *a_pool;
+    const lora_bf16_t *b_pool;
+    const int64_t *a_offset;
+    const int64_t *b_offset;
+    const int32_t *rank;
+    int64_t a_elems;
+    int64_t b_elems;
+    int32_t num_adapters;
+    int32_t max_rank;
+    int32_t K;
+    int32_t N;
+} lora_pool_t;
+
+/*
+ * Segment table (§2.3): a stable bucket sort of the tokens by lora_id.
+ * Filled by lora_build_segments with DEVICE pointers into the workspace.
+ *   perm[M]            permuted position p -> original token index
+ *                      (bucket order: id -1 first, then ascending id; within a
+ *                      bucket, ascending token index)
+ *   bucket_offsets[A+2] exclusive scan of the bucket counts (bucket 0 = id -1,
+ *                      bucket i+1 = adapter i); bucket_offsets[A+1] = M
+ *   seg_id/seg_start/seg_len/seg_rank[A]: one entry per adapter present, in
+ *                      ascending id: its id, first permuted position, token
+ *                      count and padded rank.  Only the first *num_segments
+ *                      entries are defined.  Id -1 tokens form no segment.
+ *   num_segments[1]
+ * The remaining fields are the library's own bookkeeping (the tile work lists
+ * that the fused kernels consume); callers pass the struct back unchanged.
+ */
+typedef struct {
+    int32_t *perm;
+    int32_t *bucket_offsets;
+    int32_t *seg_id;
+    int32_t *seg_start;
+    int32_t *seg_len;
+    int32_t *seg_rank;
+    int32_t *num_segments;
+    void *plan;                 /* internal: tile / chunk work lists */
+    int64_t M;
+    int32_t num_adapters;
+    int32_t reserved;
+} lora_segments_t;
+
+/*
+ * Host helper: rank-grouped pool layout for `num_adapters` adapters with true
+ * ranks `true_rank[i]` (host array, each in [1, 64]).  Adapters are grouped by
+ * padded rank (16, 32, 48, 64) in that order, keeping id order inside a
+ * group.  Writes (host arrays of num_adapters entries) a_offset, b_offset,
+ * rank_padded, and *a_elems / *b_elems.  Returns LORA_ERR_RANK / _SHAPE / _NULL.
+ */
+int lora_pool_layout(int32_t num_adapters, const int32_t *true_rank, int32_t K, int32_t N,
+                     int64_t *a_offset, int64_t *b_offset, int32_t *rank_padded,
+                     int64_t *a_elems, int64_t *b_elems);
+
+/*
+ * Bytes of device workspace needed by every call below for M tokens, output
+ * width N and a pool of num_adapters adapters.  The workspace holds the
+ * segment table, the tile work lists, the bf16 S scratch, split-K partial sums
+ * and a status / counter block.  It must be zero-filled once before its
+ * first use (lora_workspace_init does that); every call leaves the counter
+ * block zeroed again.
+ */
+size_t lora_workspace_size(int64_t M, int32_t N, int32_t num_adapters);
+
+/* Zero-fill a fresh workspace (enqueued on `stream`). ws: DEVICE pointer. */
+int lora_workspace_init(void *ws, size_t ws_bytes, lora_stream_t stream);
+
+/*
+ * §2.3 / §3.2: build the segment table for one step's lora_id_map (DEVICE
+ * int32 [M]) against `pool` (its ranks).  One small kernel; the result can be
+ * reused by every LoRA layer of the step that shares ids and ranks, as long
+ * as the same workspace is passed to those calls.  *out (HOST struct) receives
+ * device pointers into ws.
+ */
+int lora_build_segments(const int32_t *lora_id_map, int64_t M, const lora_pool_t *pool,
+                        lora_segments_t *out, void *ws, size_t ws_bytes, lora_stream_t stream);
+
+/*
+ * §2.2 first product alone: S[t, j] = sum_k x[t,k] A_{id[t]}[j,k] for
+ * j < rank[id[t]]; S[t, j] = 0 for j >= rank[id[t]] and for id -1 rows.
+ * x: DEVICE bf16 [M, pool->K].  S: DEVICE fp32 [M, s_cols], original token
+ * order, s_cols >= pool->max_rank (extra columns are zeroed).  segs: a table
+ * built for lora_id_map, or NULL to build one in ws first.
+ */
+int lora_shrink(const lora_bf16_t *x, int64_t M, const int32_t *lora_id_map,
+                const lora_pool_t *pool, const lora_segments_t *segs, float *S, int32_t s_cols,
+                void *ws, size_t ws_bytes, lora_stream_t stream);
+
+/*
+ * §2.2 second product alone, added into the output rows (§2.3):
+ * y[t, :] += scale * S[t, :rank] B_{id[t]}^T for id >= 0; id -1 rows untouched.
+ * S: DEVICE fp32 [M, s_cols] (s_cols >= pool->max_rank), original order.
+ * y: DEVICE bf16 [M, pool->N], read and written (rounded once to bf16).
+ */
+int lora_expand(const float *S, int32_t s_cols, int64_t M, const int32_t *lora_id_map,
+                const lora_pool_t *pool, const lora_segments_t *segs, float scale,
+                lora_bf16_t *y, void *ws, size_t ws_bytes, lora_stream_t stream);
+
+/*
+ * The fused layer (§2.1 operator contract, §2.3 one dispatch for all
+ * segments): y = x W^T + bias + scale * (x A_id^T) B_id^T per token.
+ * x: DEVICE bf16 [M, K]; W: DEVICE bf16 [N, K]; bias: DEVICE bf16 [N] or NULL;
+ * lora_id_map: DEVICE int32 [M]; y: DEVICE bf16 [M, N] (written, never read).
+ * K and N are taken from the pool.  segs: a table built for lora_id_map and
+ * this pool's ranks, or NULL to build one in ws first.  Accumulation is fp32;
+ * S is rounded to bf16 once after scaling, the output once at the end.
+ * M == 0 is a no-op.  A call whose ids are all -1 runs the base GEMM only.
+ */
+int lora_linear(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
+                const int32_t *lora_id_map, const lora_pool_t *pool, float scale,
+                const lora_segments_t *segs, lora_bf16_t *y, void *ws, size_t ws_bytes,
+                lora_stream_t stream);
+
+/* Schedules of lora_linear_ex (the automatic choice picks by M). */
+enum {
+    LORA_PATH_AUTO = 0,
+    LORA_PATH_TILED = 1,        /* token-tile x output-tile persistent schedule */
+    LORA_PATH_SPLITK = 2        /* weight-streaming split-K schedule, M <= 128 */
+};
+
+/* lora_linear with an explicit schedule (for tests and tuning). */
+int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
+                   const int32_t *lora_id_map, const lora_pool_t *pool, float scale,
+                   const lora_segments_t *segs, lora_bf16_t *y, void *ws, size_t ws_bytes,
+                   lora_stream_t stream, int32_t path);
+
+/*
+ * Synchronise `stream`, then read and clear the device status word of ws
+ * into *status (a bitwise OR of LORA_DEV_* since the last read).
+ */
+int lora_get_status(void *ws, lora_stream_t stream, int32_t *status);
+
+/* Static text for a LORA_ERR_* code. */
+const char *lora_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LORA_GB300_LORA_H */

@@ -1,0 +1,418 @@
+// Tiled schedule of the fused multi-LoRA linear layer on tcgen05.
+//
+// Page "vLLM-Ascend dynamic LoRA" (pptc.cn/news/149022): §2.3 (tokens grouped
+// by adapter into segments, every segment consumed inside ONE operator
+// launch), §2.2 (S = x A^T first, then S B^T; never pre-multiplied), §2.4
+// (tile M first, then the rank), §4.2 #1 (S accumulated in fp32), §3.4 / §4.1
+// (output rows back in the original token order, -1 rows = base only).
+//
+// Work is a list of jobs executed by a persistent grid (one CTA per SM):
+//   shrink job (tile m, chunks c0..c1):  D[128, 16*(c1-c0)] = x_perm[m] A_cat^T
+//       over the full K; the epilogue masks every row to its own segment's
+//       rank panels, multiplies by scale, rounds to bf16 and parks the panels
+//       in an L2-resident scratch, then bumps the tile's ready counter.
+//   output job (tile m, tile n):  D[128, 256] = x_perm[m] W[n]^T over K, then
+//       extra K-steps  D += S_panel[m, c] B_panel[c, n]^T  for the tile's
+//       chunks (S read back through TMA once the ready counter is complete),
+//       then + bias, round to bf16, rows scattered to y[perm[row]].
+// Shrink jobs come first in the list, so no CTA ever waits on a job that is
+// queued behind a waiting job: the grid cannot deadlock (every wait is also
+// bounded).
+//
+// Roles inside a CTA (192 threads):
+//   warp 0      TMA producer: x rows by tile::gather4 (4 permuted rows per
+//               instruction), W / A / B / S boxes by 2-D tiled loads
+//   warp 1      TMEM allocator and MMA issuer (one thread)
+//   warps 2..5  epilogue: tcgen05.ld -> registers -> global
+// Smem: 4 stages x (16 KB x-slot + 32 KB w-slot), 128-byte swizzle for the
+// K-blocks of 64, 32-byte swizzle for the 16-wide rank panels.  TMEM: two
+// 256-column fp32 accumulators so the epilogue of job j overlaps the
+// mainloop of job j+1.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "lora.h"
+#include "ptx.cuh"
+
+namespace lora {
+
+constexpr int kStages = 4;
+constexpr int kXSlot = kBM * kBK * 2;         // 16 KB
+constexpr int kWSlot = kBN * kBK * 2;         // 32 KB
+constexpr int kStageBytes = kXSlot + kWSlot;
+constexpr int kSPanelBytes = kBM * kChunk * 2;   // 4 KB  (128 rows x 16)
+constexpr int kBPanelBytes = kBN * kChunk * 2;   // 8 KB  (256 rows x 16)
+constexpr int kAPanelBytes = kChunk * kBK * 2;   // 2 KB  (16 rows x 64)
+constexpr int kPanelsPerStage = 4;
+constexpr int kTcThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr int kAccCols = 256;
+constexpr size_t kTcSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+
+struct Job {
+    int kind;   // 0 shrink, 1 output
+    int m, n, c0, c1;
+};
+
+__device__ __forceinline__ Job decode_job(int j, int n_sjobs, const TcParams &p)
+{
+    Job jb;
+    if (j < n_sjobs) {
+        jb.kind = 0;
+        jb.m = p.sjob_tile[j];
+        jb.n = 0;
+        jb.c0 = p.sjob_c0[j];
+        jb.c1 = p.sjob_c1[j];
+        return jb;
+    }
+    const int t = j - n_sjobs;
+    const int per_group = p.group_m * p.num_ntiles;
+    const int g = t / per_group, r = t - g * per_group;
+    const int m0 = g * p.group_m;
+    const int gm = min(p.group_m, p.num_mtiles - m0);
+    jb.kind = 1;
+    jb.m = m0 + r % gm;
+    jb.n = r / gm;
+    jb.c0 = p.tile_chunk_off[jb.m];
+    jb.c1 = p.tile_chunk_off[jb.m + 1];
+    return jb;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    lora_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                   const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                   const __grid_constant__ CUtensorMap tm_s, const TcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *acc_full = empty + kStages;
+    uint64_t *acc_empty = acc_full + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *last_flag = const_cast<int *>(abort_flag) + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int32_t *status = p.counters + CNT_STATUS;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], 128);
+        }
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tm_x);
+        tma_prefetch_map(&tm_w);
+        tma_prefetch_map(&tm_a);
+        tma_prefetch_map(&tm_b);
+        tma_prefetch_map(&tm_s);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int n_sjobs = (p.mode == kModeExpand) ? 0 : p.hdr[HDR_NSJOBS];
+    const int n_out = (p.mode == kModeShrink) ? 0 : p.num_mtiles * p.num_ntiles;
+    const int total = n_sjobs + n_out;
+    const int kblocks = (p.mode == kModeExpand) ? 0 : p.kblocks;
+
+    if (warp == 0) {
+        // ===================== TMA producer ==================================
+        uint32_t it = 0;
+        for (int j = blockIdx.x; j < total; j += gridDim.x) {
+            const Job jb = decode_job(j, n_sjobs, p);
+            int rows[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                int64_t pp = static_cast<int64_t>(jb.m) * kBM + 4 * lane + q;
+                if (pp >= p.M) pp = p.M - 1;
+                rows[q] = p.perm[pp];
+            }
+            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int s = it % kStages;
+                const uint32_t round = it / kStages;
+                if (lane == 0 && round > 0) mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                __syncwarp();
+                uint8_t *xs = smem + s * kStageBytes;
+                uint8_t *wsl = xs + kXSlot;
+                const uint32_t bytes =
+                    kXSlot + (jb.kind == 0 ? (jb.c1 - jb.c0) * kAPanelBytes : kWSlot);
+                if (lane == 0) mbar_expect_tx(&full[s], bytes);
+                __syncwarp();
+                tma_gather4(xs + lane * 512, &tm_x, &full[s], kb * kBK, rows[0], rows[1], rows[2], rows[3]);
+                if (jb.kind == 1) {
+                    if (lane == 0) tma_load_2d(wsl, &tm_w, &full[s], kb * kBK, jb.n * kBN);
+                } else {
+                    for (int c = jb.c0 + lane; c < jb.c1; c += 32)
+                        tma_load_2d(wsl + (c - jb.c0) * kAPanelBytes, &tm_a, &full[s], kb * kBK, p.chunk_arow[c]);
+                }
+            }
+            if (jb.kind == 1 && jb.c1 > jb.c0) {
+                if (p.mode == kModeLinear) {
+                    if (lane == 0) {
+                        wait_flag_geq(p.counters + CNT_FIXED + jb.m, p.tile_njobs[jb.m], abort_flag, status,
+                                      LORA_DEV_TIMEOUT);
+                        fence_proxy_async_global();
+                    }
+                    __syncwarp();
+                }
+                for (int cg = jb.c0; cg < jb.c1; cg += kPanelsPerStage, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t round = it / kStages;
+                    if (lane == 0 && round > 0) mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                    __syncwarp();
+                    uint8_t *xs = smem + s * kStageBytes;
+                    uint8_t *wsl = xs + kXSlot;
+                    const int nc = min(kPanelsPerStage, jb.c1 - cg);
+                    if (lane == 0) mbar_expect_tx(&full[s], nc * (kSPanelBytes + kBPanelBytes));
+                    __syncwarp();
+                    if (lane < nc) {
+                        const int c = cg + lane;
+                        tma_load_2d(xs + lane * kSPanelBytes, &tm_s, &full[s], 0, c * kBM);
+                        tma_load_2d(wsl + lane * kBPanelBytes, &tm_b, &full[s], 0, p.chunk_brow[c] + jb.n * kBN);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ===================== MMA issuer ====================================
+        uint32_t it = 0, q = 0;
+        for (int j = blockIdx.x; j < total; j += gridDim.x, ++q) {
+            const Job jb = decode_job(j, n_sjobs, p);
+            const uint32_t slot = q & 1, use = q >> 1;
+            if (use > 0) mbar_wait(&acc_empty[slot], (use - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+            tc_fence_after();
+            const uint32_t d = tmem_base + slot * kAccCols;
+            const int n_mma = jb.kind == 0 ? (jb.c1 - jb.c0) * kChunk : kBN;
+            const uint32_t idesc = umma_idesc_bf16(kBM, n_mma);
+            uint32_t acc = 0;
+            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int s = it % kStages;
+                mbar_wait(&full[s], (it / kStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t xa = smem_u32(smem + s * kStageBytes);
+                    const uint32_t wa = xa + kXSlot;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        umma_bf16(d, umma_sdesc(xa + kk * 32, 1024, kSwizzle128),
+                                  umma_sdesc(wa + kk * 32, 1024, kSwizzle128), idesc, acc);
+                        acc = 1;
+                    }
+                    umma_commit(&empty[s]);
+                }
+                __syncwarp();
+            }
+            if (jb.kind == 1 && jb.c1 > jb.c0) {
+                const uint32_t idesc_e = umma_idesc_bf16(kBM, kBN);
+                for (int cg = jb.c0; cg < jb.c1; cg += kPanelsPerStage, ++it) {
+                    const int s = it % kStages;
+                    mbar_wait(&full[s], (it / kStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t xa = smem_u32(smem + s * kStageBytes);
+                        const uint32_t wa = xa + kXSlot;
+                        const int nc = min(kPanelsPerStage, jb.c1 - cg);
+                        for (int i = 0; i < nc; ++i) {
+                            umma_bf16(d, umma_sdesc(xa + i * kSPanelBytes, 256, kSwizzle32),
+                                      umma_sdesc(wa + i * kBPanelBytes, 256, kSwizzle32), idesc_e, acc);
+                            acc = 1;
+                        }
+                        umma_commit(&empty[s]);
+                    }
+                    __syncwarp();
+                }
+            }
+            if (lane == 0) umma_commit(&acc_full[slot]);
+            __syncwarp();
+        }
+    } else {
+        // ===================== epilogue (warps 2..5) =========================
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int et = threadIdx.x - 64;   // 0..127
+        uint32_t q = 0;
+        for (int j = blockIdx.x; j < total; j += gridDim.x, ++q) {
+            const Job jb = decode_job(j, n_sjobs, p);
+            const uint32_t slot = q & 1, use = q >> 1;
+            mbar_wait(&acc_full[slot], use & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + slot * kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
+            const int64_t pp = static_cast<int64_t>(jb.m) * kBM + row;
+            const bool valid = pp < p.M;
+            const int tok = valid ? p.perm[pp] : 0;
+
+            if (jb.kind == 0) {
+                // ---- S panels: mask to the row's own segment, scale, bf16 ----
+                for (int c = jb.c0; c < jb.c1; ++c) {
+                    uint32_t r[16];
+                    tmem_ld16(tbase + (c - jb.c0) * kChunk, r);
+                    tmem_ld_wait16(r);
+                    const int32_t rng = p.chunk_rng[c];
+                    const bool keep = valid && row >= rng_lo(rng) && row < rng_hi(rng);
+                    if (p.mode == kModeLinear) {
+                        uint4 o0, o1;
+                        const float sc = keep ? p.scale : 0.f;
+                        o0.x = pack_bf16x2(__uint_as_float(r[0]) * sc, __uint_as_float(r[1]) * sc);
+                        o0.y = pack_bf16x2(__uint_as_float(r[2]) * sc, __uint_as_float(r[3]) * sc);
+                        o0.z = pack_bf16x2(__uint_as_float(r[4]) * sc, __uint_as_float(r[5]) * sc);
+                        o0.w = pack_bf16x2(__uint_as_float(r[6]) * sc, __uint_as_float(r[7]) * sc);
+                        o1.x = pack_bf16x2(__uint_as_float(r[8]) * sc, __uint_as_float(r[9]) * sc);
+                        o1.y = pack_bf16x2(__uint_as_float(r[10]) * sc, __uint_as_float(r[11]) * sc);
+                        o1.z = pack_bf16x2(__uint_as_float(r[12]) * sc, __uint_as_float(r[13]) * sc);
+                        o1.w = pack_bf16x2(__uint_as_float(r[14]) * sc, __uint_as_float(r[15]) * sc);
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.s_panels + (static_cast<int64_t>(c) * kBM + row) * kChunk);
+                        dst[0] = o0;
+                        dst[1] = o1;
+                    } else if (keep) {
+                        // standalone shrink: fp32, unscaled, original row, panel columns
+                        float4 *dst = reinterpret_cast<float4 *>(p.s_out + static_cast<int64_t>(tok) * p.s_cols +
+                                                                 rng_panel(rng) * kChunk);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                                 __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&acc_empty[slot]);
+                if (p.mode == kModeLinear) {
+                    fence_proxy_async_global();
+                    __threadfence();
+                    named_bar_sync(1, 128);
+                    if (et == 0) red_release_gpu_add(p.counters + CNT_FIXED + jb.m, 1);
+                }
+            } else {
+                // ---- output tile: + bias, bf16, scatter to the original row ----
+                const int n0 = jb.n * kBN;
+                const bool lora_row = p.mode != kModeExpand || pp >= p.offsets[1];
+                for (int cc = 0; cc < kBN / 16; ++cc) {
+                    uint32_t r[16];
+                    tmem_ld16(tbase + cc * 16, r);
+                    tmem_ld_wait16(r);
+                    if (cc == kBN / 16 - 1) {
+                        tc_fence_before();
+                        mbar_arrive(&acc_empty[slot]);
+                    }
+                    const int col = n0 + cc * 16;
+                    if (!valid || col >= p.N || !lora_row) continue;
+                    uint16_t *dst = p.y + static_cast<int64_t>(tok) * p.N + col;
+                    float v[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
+                    if (p.mode == kModeExpand) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(dst);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            if (col + 8 * h >= p.N) break;
+                            const uint4 u = src[h];
+                            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                v[8 * h + 2 * e] += bf16_lo(w4[e]);
+                                v[8 * h + 2 * e + 1] += bf16_hi(w4[e]);
+                            }
+                        }
+                    } else if (p.bias) {
+                        const uint4 *bsrc = reinterpret_cast<const uint4 *>(p.bias + col);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            if (col + 8 * h >= p.N) break;
+                            const uint4 u = __ldg(bsrc + h);
+                            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                v[8 * h + 2 * e] += bf16_lo(w4[e]);
+                                v[8 * h + 2 * e + 1] += bf16_hi(w4[e]);
+                            }
+                        }
+                    }
+                    uint4 *o = reinterpret_cast<uint4 *>(dst);
+                    o[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                      pack_bf16x2(v[6], v[7]));
+                    if (col + 8 < p.N)
+                        o[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]),
+                                          pack_bf16x2(v[12], v[13]), pack_bf16x2(v[14], v[15]));
+                }
+            }
+        }
+    }
+
+    // ---- teardown ---------------------------------------------------------
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+    if (p.mode == kModeLinear) {
+        // the last CTA to finish clears the per-tile ready counters
+        if (threadIdx.x == 0) {
+            __threadfence();
+            *last_flag = (atom_acq_rel_gpu_add(p.counters + CNT_CTAS_DONE, 1) == static_cast<int>(gridDim.x) - 1);
+        }
+        __syncthreads();
+        if (*last_flag) {
+            for (int m = threadIdx.x; m < p.num_mtiles; m += blockDim.x) p.counters[CNT_FIXED + m] = 0;
+            if (threadIdx.x == 0) p.counters[CNT_CTAS_DONE] = 0;
+        }
+    }
+}
+
+// Standalone expand: turn the caller's fp32 S [M, s_cols] (original token
+// order) into the kernel's bf16 S panels (permuted tile rows, each row masked
+// to its own segment's rank panels, multiplied by scale).  One CTA per token
+// tile, one thread per tile row.
+__global__ void __launch_bounds__(kBM) s_prep_kernel(const float *S, int32_t s_cols, float scale, TcParams p)
+{
+    const int m = blockIdx.x, row = threadIdx.x;
+    const int64_t pp = static_cast<int64_t>(m) * kBM + row;
+    const bool valid = pp < p.M;
+    const int tok = valid ? p.perm[pp] : 0;
+    for (int c = p.tile_chunk_off[m]; c < p.tile_chunk_off[m + 1]; ++c) {
+        const int32_t rng = p.chunk_rng[c];
+        const bool keep = valid && row >= rng_lo(rng) && row < rng_hi(rng);
+        const float *src = S + static_cast<int64_t>(tok) * s_cols + rng_panel(rng) * kChunk;
+        uint32_t w[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            w[e] = keep ? pack_bf16x2(src[2 * e] * scale, src[2 * e + 1] * scale) : 0u;
+        uint4 *dst = reinterpret_cast<uint4 *>(p.s_panels + (static_cast<int64_t>(c) * kBM + row) * kChunk);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
+cudaError_t launch_s_prep(const float *S, int32_t s_cols, float scale, const TcParams &p, cudaStream_t stream)
+{
+    s_prep_kernel<<<p.num_mtiles, kBM, 0, stream>>>(S, s_cols, scale, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cudaStream_t stream)
+{
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(lora_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kTcSmemBytes));
+        if (e != cudaSuccess) return e;
+        configured[dev] = 1;
+    }
+    lora_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, stream>>>(maps.x, maps.w, maps.a, maps.b, maps.s, p);
+    return cudaGetLastError();
+}
+
+}  // namespace lora

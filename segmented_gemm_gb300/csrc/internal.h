@@ -1,0 +1,136 @@
+// Internal declarations shared by the host API and the kernels of liblora.
+//
+// Workspace layout (all offsets 256-byte aligned), for M tokens, N outputs and
+// A adapters:
+//   counters   status word, grid counters, per-token-tile S-ready flags,
+//              per-output-tile split-K arrival counters   (zero at rest)
+//   segments   perm[M], bucket_offsets[A+2], seg_{id,start,len,rank}[A],
+//              num_segments[1]                             (the §2.3 table)
+//   plan       header, per-tile chunk lists, shrink-job list, split-K chunk
+//              list                                        (kernel work lists)
+//   s_scratch  bf16 S panels (scaled, masked), [chunks][rows][16]
+//   partials   fp32 split-K partial tiles
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace lora {
+
+// ---- tiled (token-tile x output-tile) schedule -----------------------------
+constexpr int kBM = 128;          // permuted tokens per tile (UMMA M)
+constexpr int kBN = 256;          // output features per tile (UMMA N)
+constexpr int kBK = 64;           // K per stage (one 128-byte swizzle row)
+constexpr int kChunk = 16;        // rank columns per chunk (one UMMA K step)
+constexpr int kMaxShrinkChunks = 16;   // chunks per shrink job -> N <= 256
+
+// ---- split-K (weight streaming) schedule ----------------------------------
+constexpr int kSplitMaxTokens = 128;   // largest M served by the split-K path
+constexpr int kSplitBN = 128;          // output features per tile (UMMA M)
+constexpr int kSplitMaxCtas = 1024;    // upper bound on the persistent grid
+
+// plan header entries
+enum PlanHdr {
+    HDR_NCHUNKS = 0,      // chunks of the tiled schedule (all tiles)
+    HDR_NSJOBS = 1,       // shrink jobs of the tiled schedule
+    HDR_DCHUNKS = 2,      // chunks of the split-K schedule (adapters present)
+    HDR_NSEG = 3,         // number of segments
+    HDR_WORDS = 16
+};
+
+// counter block entries (int32), zero between calls
+enum Counters {
+    CNT_STATUS = 0,       // LORA_DEV_* bits
+    CNT_CTAS_DONE = 1,    // tiled schedule: CTAs finished
+    CNT_SPLIT_DONE = 2,   // split-K: CTAs finished
+    CNT_SPLIT_SREADY = 3, // split-K: shrink row tiles reduced
+    CNT_FIXED = 8         // first per-tile counter
+};
+
+struct WsLayout {
+    int64_t M;
+    int32_t N, A;
+    int32_t num_mtiles;       // ceil(M / kBM)
+    int32_t max_chunks;       // tiled-schedule chunk capacity
+    int32_t max_sjobs;        // shrink-job capacity
+    int32_t max_dchunks;      // split-K chunk capacity
+    int32_t split_tiles;      // split-K output + shrink tiles (counter slots)
+    int64_t split_slots;      // split-K partial slots
+    size_t counters, n_counters;
+    size_t perm, offsets, seg_id, seg_start, seg_len, seg_rank, num_segments;
+    size_t hdr, tile_chunk_off, chunk_arow, chunk_brow, chunk_rng;
+    size_t sjob_tile, sjob_c0, sjob_c1, tile_njobs;
+    size_t dchunk_arow, dchunk_brow, dchunk_adapter;
+    size_t s_scratch, s_scratch_bytes;
+    size_t partials, partials_bytes;
+    size_t total;
+};
+
+// Host+device: compute the layout for (M, N, A).
+WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A);
+
+// chunk_rng packing: rows [lo, hi) of the tile, rank panel p of the segment
+__host__ __device__ inline int32_t pack_rng(int lo, int hi, int p) { return lo | (hi << 8) | (p << 16); }
+__host__ __device__ inline int rng_lo(int32_t v) { return v & 0xFF; }
+__host__ __device__ inline int rng_hi(int32_t v) { return (v >> 8) & 0xFF; }
+__host__ __device__ inline int rng_panel(int32_t v) { return (v >> 16) & 0xFF; }
+
+// ---- kernel parameter blocks ----------------------------------------------
+enum TcMode { kModeLinear = 0, kModeShrink = 1, kModeExpand = 2 };
+
+struct TcMaps {
+    CUtensorMap x, w, a, b, s;
+};
+
+struct TcParams {
+    int64_t M;
+    int32_t N, K, kblocks, num_mtiles, num_ntiles, group_m, mode, s_cols;
+    float scale;
+    const uint16_t *bias;      // bf16 [N] or null
+    uint16_t *y;               // bf16 [M, N]
+    uint16_t *s_panels;        // bf16 [chunks][128][16]
+    float *s_out;              // fp32 [M, s_cols] (shrink mode)
+    const int32_t *perm, *offsets, *hdr;
+    const int32_t *tile_chunk_off, *chunk_arow, *chunk_brow, *chunk_rng;
+    const int32_t *sjob_tile, *sjob_c0, *sjob_c1, *tile_njobs;
+    int32_t *counters;
+};
+
+struct SplitParams {
+    int64_t M;
+    int32_t N, K, T_pad, kblocks, NT, stages, tmem_cols, R1, R2, R3, A;
+    float scale;
+    const uint16_t *bias;
+    uint16_t *y;
+    const int32_t *ids, *hdr, *dchunk_arow, *dchunk_brow, *dchunk_adapter;
+    uint16_t *s_panels;        // bf16 [chunks][T_pad][16]
+    float *partials;           // fp32 [slots][128][T_pad]
+    int32_t *counters;
+};
+
+struct SegParams {
+    const int32_t *ids;
+    int64_t M;
+    int32_t A, K, N, num_mtiles;
+    const int32_t *rank;
+    const int64_t *a_offset;
+    const int64_t *b_offset;
+    int32_t *perm, *offsets, *seg_id, *seg_start, *seg_len, *seg_rank, *num_segments;
+    int32_t *hdr, *tile_chunk_off, *chunk_arow, *chunk_brow, *chunk_rng;
+    int32_t *sjob_tile, *sjob_c0, *sjob_c1, *tile_njobs;
+    int32_t *dchunk_arow, *dchunk_brow, *dchunk_adapter;
+    int32_t *counters;
+    int32_t n_counters;
+};
+
+// ---- launchers (enqueue only; return the launch status) --------------------
+cudaError_t launch_seg_build(const SegParams &p, cudaStream_t stream);
+cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cudaStream_t stream);
+cudaError_t launch_s_prep(const float *S, int32_t s_cols, float scale, const TcParams &p, cudaStream_t stream);
+cudaError_t launch_splitk(const TcMaps &maps, const SplitParams &p, int grid, cudaStream_t stream);
+int splitk_stages(int T_pad);
+int num_sms_current_device();
+
+}  // namespace lora

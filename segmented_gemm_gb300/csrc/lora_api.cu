@@ -1,0 +1,533 @@
+// Host side of the C ABI declared in include/lora.h: argument validation,
+// workspace carving, TMA tensor-map encoding and kernel dispatch.  Nothing
+// here allocates device memory, synchronises or copies device->host except
+// lora_get_status.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+#include "lora.h"
+
+namespace lora {
+
+// ---------------------------------------------------------------------------
+// device queries and the tensor-map encoder (driver entry point, no -lcuda)
+// ---------------------------------------------------------------------------
+int num_sms_current_device()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev < 64 && cache[dev]) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    if (dev < 64) cache[dev] = n;
+    return n;
+}
+
+static bool device_supported()
+{
+    static int cache[64] = {0};   // 0 unknown, 1 yes, 2 no
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (dev < 64 && cache[dev]) return cache[dev] == 1;
+    int major = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    int minor = 0;
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    const bool ok = (major == 10 && minor == 3);
+    if (dev < 64) cache[dev] = ok ? 1 : 2;
+    return ok;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encoder()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 map: `inner` elements per row, `rows` rows, row pitch in bytes.
+static bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t pitch,
+                      uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw)
+{
+    EncodeTiledFn fn = encoder();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, rows < 1 ? 1 : rows};
+    cuuint64_t strides[1] = {pitch};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// workspace layout
+// ---------------------------------------------------------------------------
+static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+static int split_tpad(int64_t M) { return static_cast<int>(((M + 15) / 16) * 16); }
+
+WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
+{
+    WsLayout L;
+    std::memset(&L, 0, sizeof L);
+    L.M = M;
+    L.N = N;
+    L.A = A;
+    L.num_mtiles = static_cast<int32_t>((M + kBM - 1) / kBM);
+    L.max_chunks = 4 * (A + L.num_mtiles) + 4;
+    L.max_sjobs = L.num_mtiles + L.max_chunks / kMaxShrinkChunks + 1;
+    const int64_t present = std::min<int64_t>(A, M);
+    L.max_dchunks = static_cast<int32_t>(4 * present + 4);
+    const int NT = (N + kSplitBN - 1) / kSplitBN;
+    const int RTmax = (L.max_dchunks + 7) / 8;
+    L.split_tiles = NT + RTmax;
+    size_t split_s = 0;
+    if (M <= kSplitMaxTokens) {
+        const int G = num_sms_current_device();
+        const int T = split_tpad(M);
+        const int R1 = (RTmax + G - 1) / G + 3, R2 = (NT + G - 1) / G + 3, R3 = R2;
+        L.split_slots = static_cast<int64_t>(G) * (R1 + R2 + R3);
+        L.partials_bytes = static_cast<size_t>(L.split_slots) * kSplitBN * T * 4;
+        split_s = static_cast<size_t>(L.max_dchunks) * T * kChunk * 2;
+    }
+    L.n_counters = CNT_FIXED + std::max<size_t>(L.num_mtiles, L.split_tiles) + 8;
+    const size_t tiled_s = static_cast<size_t>(L.max_chunks) * kBM * kChunk * 2;
+    L.s_scratch_bytes = std::max(tiled_s, split_s);
+
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align256(o + bytes);
+        return at;
+    };
+    L.counters = take(L.n_counters * 4);
+    L.perm = take(static_cast<size_t>(std::max<int64_t>(M, 1)) * 4);
+    L.offsets = take(static_cast<size_t>(A + 2) * 4);
+    L.seg_id = take(static_cast<size_t>(std::max(A, 1)) * 4);
+    L.seg_start = take(static_cast<size_t>(std::max(A, 1)) * 4);
+    L.seg_len = take(static_cast<size_t>(std::max(A, 1)) * 4);
+    L.seg_rank = take(static_cast<size_t>(std::max(A, 1)) * 4);
+    L.num_segments = take(4);
+    L.hdr = take(HDR_WORDS * 4);
+    L.tile_chunk_off = take(static_cast<size_t>(L.num_mtiles + 1) * 4);
+    L.chunk_arow = take(static_cast<size_t>(L.max_chunks) * 4);
+    L.chunk_brow = take(static_cast<size_t>(L.max_chunks) * 4);
+    L.chunk_rng = take(static_cast<size_t>(L.max_chunks) * 4);
+    L.sjob_tile = take(static_cast<size_t>(L.max_sjobs) * 4);
+    L.sjob_c0 = take(static_cast<size_t>(L.max_sjobs) * 4);
+    L.sjob_c1 = take(static_cast<size_t>(L.max_sjobs) * 4);
+    L.tile_njobs = take(static_cast<size_t>(L.num_mtiles) * 4);
+    L.dchunk_arow = take(static_cast<size_t>(L.max_dchunks) * 4);
+    L.dchunk_brow = take(static_cast<size_t>(L.max_dchunks) * 4);
+    L.dchunk_adapter = take(static_cast<size_t>(L.max_dchunks) * 4);
+    o = (o + 1023) & ~size_t(1023);
+    L.s_scratch = take(L.s_scratch_bytes);
+    L.partials = take(std::max<size_t>(L.partials_bytes, 16));
+    L.total = o;
+    return L;
+}
+
+template <typename T>
+static T *at(void *ws, size_t off)
+{
+    return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+static int check_pool(const lora_pool_t *pool)
+{
+    if (!pool) return LORA_ERR_NULL;
+    if (pool->K <= 0 || pool->N <= 0 || (pool->K % 8) || (pool->N % 8)) return LORA_ERR_SHAPE;
+    if (pool->num_adapters < 0 || pool->num_adapters > LORA_MAX_ADAPTERS) return LORA_ERR_SHAPE;
+    if (pool->num_adapters > 0) {
+        if (!pool->a_pool || !pool->b_pool || !pool->a_offset || !pool->b_offset || !pool->rank) return LORA_ERR_NULL;
+        if (!aligned16(pool->a_pool) || !aligned16(pool->b_pool)) return LORA_ERR_ALIGN;
+        if (pool->max_rank < LORA_RANK_ALIGN || pool->max_rank > LORA_MAX_RANK || (pool->max_rank % LORA_RANK_ALIGN))
+            return LORA_ERR_RANK;
+        if (pool->a_elems <= 0 || pool->b_elems <= 0 || (pool->a_elems % pool->K) || (pool->b_elems % kChunk))
+            return LORA_ERR_SHAPE;
+    }
+    return LORA_OK;
+}
+
+struct Carve {
+    WsLayout L;
+    int32_t *counters;
+};
+
+static void fill_segments(void *ws, const WsLayout &L, int64_t M, int32_t A, lora_segments_t *out)
+{
+    out->perm = at<int32_t>(ws, L.perm);
+    out->bucket_offsets = at<int32_t>(ws, L.offsets);
+    out->seg_id = at<int32_t>(ws, L.seg_id);
+    out->seg_start = at<int32_t>(ws, L.seg_start);
+    out->seg_len = at<int32_t>(ws, L.seg_len);
+    out->seg_rank = at<int32_t>(ws, L.seg_rank);
+    out->num_segments = at<int32_t>(ws, L.num_segments);
+    out->plan = ws;
+    out->M = M;
+    out->num_adapters = A;
+    out->reserved = 0;
+}
+
+static int enqueue_segments(const int32_t *ids, int64_t M, const lora_pool_t *pool, const WsLayout &L, void *ws,
+                            cudaStream_t stream)
+{
+    SegParams p;
+    p.ids = ids;
+    p.M = M;
+    p.A = pool->num_adapters;
+    p.K = pool->K;
+    p.N = pool->N;
+    p.num_mtiles = L.num_mtiles;
+    p.rank = pool->rank;
+    p.a_offset = pool->a_offset;
+    p.b_offset = pool->b_offset;
+    p.perm = at<int32_t>(ws, L.perm);
+    p.offsets = at<int32_t>(ws, L.offsets);
+    p.seg_id = at<int32_t>(ws, L.seg_id);
+    p.seg_start = at<int32_t>(ws, L.seg_start);
+    p.seg_len = at<int32_t>(ws, L.seg_len);
+    p.seg_rank = at<int32_t>(ws, L.seg_rank);
+    p.num_segments = at<int32_t>(ws, L.num_segments);
+    p.hdr = at<int32_t>(ws, L.hdr);
+    p.tile_chunk_off = at<int32_t>(ws, L.tile_chunk_off);
+    p.chunk_arow = at<int32_t>(ws, L.chunk_arow);
+    p.chunk_brow = at<int32_t>(ws, L.chunk_brow);
+    p.chunk_rng = at<int32_t>(ws, L.chunk_rng);
+    p.sjob_tile = at<int32_t>(ws, L.sjob_tile);
+    p.sjob_c0 = at<int32_t>(ws, L.sjob_c0);
+    p.sjob_c1 = at<int32_t>(ws, L.sjob_c1);
+    p.tile_njobs = at<int32_t>(ws, L.tile_njobs);
+    p.dchunk_arow = at<int32_t>(ws, L.dchunk_arow);
+    p.dchunk_brow = at<int32_t>(ws, L.dchunk_brow);
+    p.dchunk_adapter = at<int32_t>(ws, L.dchunk_adapter);
+    p.counters = at<int32_t>(ws, L.counters);
+    p.n_counters = static_cast<int32_t>(L.n_counters);
+    return launch_seg_build(p, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
+// Validate the common arguments and make sure a segment table exists in ws.
+static int prepare(const int32_t *ids, int64_t M, const lora_pool_t *pool, const lora_segments_t *segs, void *ws,
+                   size_t ws_bytes, cudaStream_t stream, WsLayout *L)
+{
+    int rc = check_pool(pool);
+    if (rc) return rc;
+    if (M < 0) return LORA_ERR_SHAPE;
+    if (M > (int64_t(1) << 31) - kBM) return LORA_ERR_SHAPE;
+    if (!ws) return LORA_ERR_WORKSPACE;
+    if (!device_supported()) return LORA_ERR_UNSUPPORTED;
+    *L = make_ws_layout(M, pool->N, pool->num_adapters);
+    if (ws_bytes < L->total) return LORA_ERR_WORKSPACE;
+    if (segs) {
+        if (segs->plan != ws || segs->M != M || segs->num_adapters != pool->num_adapters) return LORA_ERR_SEGMENTS;
+        return LORA_OK;
+    }
+    if (!ids) return LORA_ERR_NULL;
+    return enqueue_segments(ids, M, pool, *L, ws, stream);
+}
+
+static void fill_tc_params(TcParams &p, const WsLayout &L, void *ws, const lora_pool_t *pool, int64_t M)
+{
+    std::memset(&p, 0, sizeof p);
+    p.M = M;
+    p.N = pool->N;
+    p.K = pool->K;
+    p.kblocks = (pool->K + kBK - 1) / kBK;
+    p.num_mtiles = L.num_mtiles;
+    p.num_ntiles = (pool->N + kBN - 1) / kBN;
+    p.group_m = 8;
+    p.s_panels = at<uint16_t>(ws, L.s_scratch);
+    p.perm = at<int32_t>(ws, L.perm);
+    p.offsets = at<int32_t>(ws, L.offsets);
+    p.hdr = at<int32_t>(ws, L.hdr);
+    p.tile_chunk_off = at<int32_t>(ws, L.tile_chunk_off);
+    p.chunk_arow = at<int32_t>(ws, L.chunk_arow);
+    p.chunk_brow = at<int32_t>(ws, L.chunk_brow);
+    p.chunk_rng = at<int32_t>(ws, L.chunk_rng);
+    p.sjob_tile = at<int32_t>(ws, L.sjob_tile);
+    p.sjob_c0 = at<int32_t>(ws, L.sjob_c0);
+    p.sjob_c1 = at<int32_t>(ws, L.sjob_c1);
+    p.tile_njobs = at<int32_t>(ws, L.tile_njobs);
+    p.counters = at<int32_t>(ws, L.counters);
+}
+
+// Maps shared by the schedules: A pool (16-row boxes), B pool (16-col panels).
+static bool encode_pool_maps(TcMaps &m, const lora_pool_t *pool, const void *dummy, uint32_t b_rows_box)
+{
+    const uint64_t K = pool->K;
+    if (pool->num_adapters > 0) {
+        if (!encode_2d(&m.a, pool->a_pool, K, pool->a_elems / K, K * 2, kBK, kChunk, CU_TENSOR_MAP_SWIZZLE_128B))
+            return false;
+        if (!encode_2d(&m.b, pool->b_pool, kChunk, pool->b_elems / kChunk, kChunk * 2, kChunk, b_rows_box,
+                       CU_TENSOR_MAP_SWIZZLE_32B))
+            return false;
+    } else {
+        if (!encode_2d(&m.a, dummy, K, 1, K * 2, kBK, kChunk, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
+        if (!encode_2d(&m.b, dummy, kChunk, 1, kChunk * 2, kChunk, b_rows_box, CU_TENSOR_MAP_SWIZZLE_32B))
+            return false;
+    }
+    return true;
+}
+
+static int run_tiled(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
+                     const lora_pool_t *pool, float scale, lora_bf16_t *y, void *ws, const WsLayout &L, int mode,
+                     float *s_out, int32_t s_cols, const float *s_in, cudaStream_t stream)
+{
+    TcParams p;
+    fill_tc_params(p, L, ws, pool, M);
+    p.mode = mode;
+    p.scale = scale;
+    p.bias = bias;
+    p.y = y;
+    p.s_out = s_out;
+    p.s_cols = s_cols;
+    const uint64_t K = pool->K, N = pool->N;
+    TcMaps m;
+    const void *xsrc = x ? static_cast<const void *>(x) : static_cast<const void *>(p.s_panels);
+    const uint64_t xrows = x ? static_cast<uint64_t>(M) : 1;
+    if (!encode_2d(&m.x, xsrc, K, xrows, K * 2, kBK, 1, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ERR_CUDA;
+    const void *wsrc = W ? static_cast<const void *>(W) : xsrc;
+    if (!encode_2d(&m.w, wsrc, K, W ? N : 1, K * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ERR_CUDA;
+    if (!encode_pool_maps(m, pool, p.s_panels, kBN)) return LORA_ERR_CUDA;
+    if (!encode_2d(&m.s, p.s_panels, kChunk, static_cast<uint64_t>(L.max_chunks) * kBM, kChunk * 2, kChunk, kBM,
+                   CU_TENSOR_MAP_SWIZZLE_32B))
+        return LORA_ERR_CUDA;
+    if (mode == kModeExpand) {
+        if (launch_s_prep(s_in, s_cols, scale, p, stream) != cudaSuccess) return LORA_ERR_CUDA;
+    }
+    const int sms = num_sms_current_device();
+    int64_t jobs = 0;
+    if (mode != kModeShrink) jobs += static_cast<int64_t>(p.num_mtiles) * p.num_ntiles;
+    if (mode != kModeExpand) jobs += L.max_sjobs;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, jobs)));
+    return launch_tc(m, p, grid, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
+static int run_splitk(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
+                      const int32_t *ids, const lora_pool_t *pool, float scale, lora_bf16_t *y, void *ws,
+                      const WsLayout &L, cudaStream_t stream)
+{
+    SplitParams p;
+    std::memset(&p, 0, sizeof p);
+    const int G = num_sms_current_device();
+    const int T = split_tpad(M);
+    p.M = M;
+    p.N = pool->N;
+    p.K = pool->K;
+    p.T_pad = T;
+    p.kblocks = (pool->K + kBK - 1) / kBK;
+    p.NT = (pool->N + kSplitBN - 1) / kSplitBN;
+    p.stages = splitk_stages(T);
+    int tc = 32;
+    while (tc < 2 * T) tc <<= 1;
+    p.tmem_cols = tc;
+    const int RTmax = (L.max_dchunks + 7) / 8;
+    p.R1 = (RTmax + G - 1) / G + 3;
+    p.R2 = (p.NT + G - 1) / G + 3;
+    p.R3 = p.R2;
+    if (static_cast<int64_t>(G) * (p.R1 + p.R2 + p.R3) > L.split_slots) return LORA_ERR_WORKSPACE;
+    p.A = pool->num_adapters;
+    p.scale = scale;
+    p.bias = bias;
+    p.y = y;
+    p.ids = ids;
+    p.hdr = at<int32_t>(ws, L.hdr);
+    p.dchunk_arow = at<int32_t>(ws, L.dchunk_arow);
+    p.dchunk_brow = at<int32_t>(ws, L.dchunk_brow);
+    p.dchunk_adapter = at<int32_t>(ws, L.dchunk_adapter);
+    p.s_panels = at<uint16_t>(ws, L.s_scratch);
+    p.partials = at<float>(ws, L.partials);
+    p.counters = at<int32_t>(ws, L.counters);
+    const uint64_t K = pool->K, N = pool->N;
+    TcMaps m;
+    if (!encode_2d(&m.x, x, K, static_cast<uint64_t>(M), K * 2, kBK, T, CU_TENSOR_MAP_SWIZZLE_128B))
+        return LORA_ERR_CUDA;
+    if (!encode_2d(&m.w, W, K, N, K * 2, kBK, kSplitBN, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ERR_CUDA;
+    if (!encode_pool_maps(m, pool, p.s_panels, kSplitBN)) return LORA_ERR_CUDA;
+    if (!encode_2d(&m.s, p.s_panels, kChunk, static_cast<uint64_t>(L.max_dchunks) * T, kChunk * 2, kChunk, T,
+                   CU_TENSOR_MAP_SWIZZLE_32B))
+        return LORA_ERR_CUDA;
+    return launch_splitk(m, p, G, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
+}  // namespace lora
+
+using namespace lora;
+
+extern "C" {
+
+int lora_pool_layout(int32_t num_adapters, const int32_t *true_rank, int32_t K, int32_t N, int64_t *a_offset,
+                     int64_t *b_offset, int32_t *rank_padded, int64_t *a_elems, int64_t *b_elems)
+{
+    if (num_adapters < 0 || num_adapters > LORA_MAX_ADAPTERS) return LORA_ERR_SHAPE;
+    if (K <= 0 || N <= 0 || (K % 8) || (N % 8)) return LORA_ERR_SHAPE;
+    if (!a_elems || !b_elems) return LORA_ERR_NULL;
+    if (num_adapters > 0 && (!true_rank || !a_offset || !b_offset || !rank_padded)) return LORA_ERR_NULL;
+    for (int i = 0; i < num_adapters; ++i)
+        if (true_rank[i] < 1 || true_rank[i] > LORA_MAX_RANK) return LORA_ERR_RANK;
+    // rank-grouped: padded rank 16, 32, 48, 64 in that order, id order inside
+    std::vector<int> order(num_adapters);
+    for (int i = 0; i < num_adapters; ++i) order[i] = i;
+    auto rp = [&](int i) { return ((true_rank[i] + LORA_RANK_ALIGN - 1) / LORA_RANK_ALIGN) * LORA_RANK_ALIGN; };
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return rp(a) < rp(b); });
+    int64_t a = 0, b = 0;
+    for (int i : order) {
+        rank_padded[i] = rp(i);
+        a_offset[i] = a;
+        b_offset[i] = b;
+        a += static_cast<int64_t>(rp(i)) * K;
+        b += static_cast<int64_t>(rp(i)) * N;
+    }
+    *a_elems = a;
+    *b_elems = b;
+    return LORA_OK;
+}
+
+size_t lora_workspace_size(int64_t M, int32_t N, int32_t num_adapters)
+{
+    if (M < 0 || N <= 0 || num_adapters < 0) return 0;
+    return make_ws_layout(M, N, num_adapters).total;
+}
+
+int lora_workspace_init(void *ws, size_t ws_bytes, lora_stream_t stream)
+{
+    if (!ws) return LORA_ERR_WORKSPACE;
+    return cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LORA_OK
+                                                                                                : LORA_ERR_CUDA;
+}
+
+int lora_build_segments(const int32_t *lora_id_map, int64_t M, const lora_pool_t *pool, lora_segments_t *out,
+                        void *ws, size_t ws_bytes, lora_stream_t stream)
+{
+    if (!out) return LORA_ERR_NULL;
+    WsLayout L;
+    if (M == 0) {
+        int rc = check_pool(pool);
+        if (rc) return rc;
+        L = make_ws_layout(0, pool->N, pool->num_adapters);
+        if (!ws || ws_bytes < L.total) return LORA_ERR_WORKSPACE;
+        fill_segments(ws, L, 0, pool->num_adapters, out);
+        return LORA_OK;
+    }
+    int rc = prepare(lora_id_map, M, pool, nullptr, ws, ws_bytes, static_cast<cudaStream_t>(stream), &L);
+    if (rc) return rc;
+    fill_segments(ws, L, M, pool->num_adapters, out);
+    return LORA_OK;
+}
+
+int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
+                   const int32_t *lora_id_map, const lora_pool_t *pool, float scale, const lora_segments_t *segs,
+                   lora_bf16_t *y, void *ws, size_t ws_bytes, lora_stream_t stream, int32_t path)
+{
+    if (M < 0) return LORA_ERR_SHAPE;
+    if (M == 0) return check_pool(pool);
+    if (!x || !W || !y) return LORA_ERR_NULL;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (bias && !aligned16(bias))) return LORA_ERR_ALIGN;
+    if (path < LORA_PATH_AUTO || path > LORA_PATH_SPLITK) return LORA_ERR_SHAPE;
+    if (path == LORA_PATH_SPLITK && M > kSplitMaxTokens) return LORA_ERR_SHAPE;
+    if (path == LORA_PATH_SPLITK && !lora_id_map) return LORA_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsLayout L;
+    int rc = prepare(lora_id_map, M, pool, segs, ws, ws_bytes, s, &L);
+    if (rc) return rc;
+    const bool splitk = path == LORA_PATH_SPLITK || (path == LORA_PATH_AUTO && M <= kSplitMaxTokens);
+    if (splitk) return run_splitk(x, M, W, bias, lora_id_map, pool, scale, y, ws, L, s);
+    return run_tiled(x, M, W, bias, pool, scale, y, ws, L, kModeLinear, nullptr, 0, nullptr, s);
+}
+
+int lora_linear(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
+                const int32_t *lora_id_map, const lora_pool_t *pool, float scale, const lora_segments_t *segs,
+                lora_bf16_t *y, void *ws, size_t ws_bytes, lora_stream_t stream)
+{
+    return lora_linear_ex(x, M, W, bias, lora_id_map, pool, scale, segs, y, ws, ws_bytes, stream, LORA_PATH_AUTO);
+}
+
+int lora_shrink(const lora_bf16_t *x, int64_t M, const int32_t *lora_id_map, const lora_pool_t *pool,
+                const lora_segments_t *segs, float *S, int32_t s_cols, void *ws, size_t ws_bytes,
+                lora_stream_t stream)
+{
+    if (M < 0) return LORA_ERR_SHAPE;
+    if (M == 0) return check_pool(pool);
+    if (!x || !S) return LORA_ERR_NULL;
+    if (!pool) return LORA_ERR_NULL;
+    if (!aligned16(x) || !aligned16(S)) return LORA_ERR_ALIGN;
+    if (s_cols < std::max(pool->max_rank, 1) || (s_cols % 4)) return LORA_ERR_SHAPE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsLayout L;
+    int rc = prepare(lora_id_map, M, pool, segs, ws, ws_bytes, s, &L);
+    if (rc) return rc;
+    if (cudaMemsetAsync(S, 0, static_cast<size_t>(M) * s_cols * sizeof(float), s) != cudaSuccess)
+        return LORA_ERR_CUDA;
+    if (pool->num_adapters == 0) return LORA_OK;
+    return run_tiled(x, M, nullptr, nullptr, pool, 1.0f, nullptr, ws, L, kModeShrink, S, s_cols, nullptr, s);
+}
+
+int lora_expand(const float *S, int32_t s_cols, int64_t M, const int32_t *lora_id_map, const lora_pool_t *pool,
+                const lora_segments_t *segs, float scale, lora_bf16_t *y, void *ws, size_t ws_bytes,
+                lora_stream_t stream)
+{
+    if (M < 0) return LORA_ERR_SHAPE;
+    if (M == 0) return check_pool(pool);
+    if (!S || !y || !pool) return LORA_ERR_NULL;
+    if (!aligned16(S) || !aligned16(y)) return LORA_ERR_ALIGN;
+    if (s_cols < std::max(pool->max_rank, 1)) return LORA_ERR_SHAPE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsLayout L;
+    int rc = prepare(lora_id_map, M, pool, segs, ws, ws_bytes, s, &L);
+    if (rc) return rc;
+    if (pool->num_adapters == 0) return LORA_OK;
+    return run_tiled(nullptr, M, nullptr, nullptr, pool, scale, y, ws, L, kModeExpand, nullptr, s_cols, S, s);
+}
+
+int lora_get_status(void *ws, lora_stream_t stream, int32_t *status)
+{
+    if (!ws || !status) return LORA_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return LORA_ERR_CUDA;
+    int32_t v = 0;
+    int32_t *word = at<int32_t>(ws, 0) + CNT_STATUS;
+    if (cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return LORA_ERR_CUDA;
+    if (cudaMemset(word, 0, sizeof v) != cudaSuccess) return LORA_ERR_CUDA;
+    *status = v;
+    return LORA_OK;
+}
+
+const char *lora_status_string(int code)
+{
+    switch (code) {
+    case LORA_OK: return "ok";
+    case LORA_ERR_NULL: return "a required pointer is NULL";
+    case LORA_ERR_SHAPE: return "invalid shape (M < 0, K or N not a positive multiple of 8, too many adapters)";
+    case LORA_ERR_ALIGN: return "a tensor base address is not 16-byte aligned";
+    case LORA_ERR_RANK: return "a rank outside [1, 64] or max_rank not a multiple of 16";
+    case LORA_ERR_WORKSPACE: return "workspace missing or smaller than lora_workspace_size()";
+    case LORA_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case LORA_ERR_UNSUPPORTED: return "the current device is not an sm_103 (GB300-class) GPU";
+    case LORA_ERR_SEGMENTS: return "the segment table was built for another call (M, pool or workspace differ)";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

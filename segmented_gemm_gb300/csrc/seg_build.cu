@@ -1,0 +1,252 @@
+// Segment builder ("vLLM-Ascend dynamic LoRA", §2.3): bucket the tokens by
+// lora_id so that tokens of one adapter become contiguous, and derive the
+// work lists the fused kernels consume (§2.4: which token block a core
+// handles, which segment it belongs to and its rank are decided before the
+// GEMM launches, not by branching inside it).
+//
+// One CTA of 1024 threads.  Each warp owns a contiguous range of tokens:
+//   pass 1  warp-aggregated histogram (__match_any_sync peers, leader adds
+//           popc) into a per-warp row of a [32][A+1] shared table
+//   scan    bucket totals -> exclusive scan -> per-warp running bases
+//   pass 2  stable scatter: rank inside a 32-token step = popc of the peers
+//           below the lane, plus the warp's running base for the bucket
+// Bucket 0 holds id -1, bucket i+1 adapter i; ids outside [-1, A) are
+// counted as -1 and flagged in the status word.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "lora.h"
+#include "ptx.cuh"
+
+namespace lora {
+
+
+constexpr int kSegThreads = 1024;
+
+// Exclusive scan of one int per thread over the 1024-thread block.
+__device__ int block_exclusive_scan(int v, int *wsum, int *total)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int s = wsum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        wsum[lane] = s;
+    }
+    __syncthreads();
+    const int excl = x - v + (w > 0 ? wsum[w - 1] : 0);
+    *total = wsum[31];
+    __syncthreads();
+    return excl;
+}
+
+__global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
+{
+    extern __shared__ int sm[];
+    const int nb = p.A + 1;
+    int *whist = sm;                 // [32][nb]
+    int *bsum = whist + 32 * nb;     // [nb + 1]
+    int *wsum = bsum + nb + 1;       // [32]
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    int32_t *status = p.counters + CNT_STATUS;
+
+    for (int i = tid; i < p.n_counters; i += kSegThreads)
+        if (i != CNT_STATUS) p.counters[i] = 0;
+    for (int i = tid; i < 32 * nb; i += kSegThreads) whist[i] = 0;
+    __syncthreads();
+
+    const int64_t per = (p.M + 31) / 32;
+    const int64_t t_begin = w * per;
+    const int64_t t_end = t_begin + per < p.M ? t_begin + per : p.M;
+
+    // ---- pass 1: per-warp histograms --------------------------------------
+    int bad = 0;
+    for (int64_t base = t_begin; base < t_end; base += 32) {
+        const int64_t t = base + lane;
+        const bool act = t < t_end;
+        const unsigned amask = __ballot_sync(0xffffffffu, act);
+        if (act) {
+            const int id = p.ids[t];
+            const int e = (id >= 0 && id < p.A) ? id : -1;
+            bad |= (e != id);
+            const int b = e + 1;
+            const unsigned peers = __match_any_sync(amask, b);
+            if (lane == __ffs(peers) - 1) whist[w * nb + b] += __popc(peers);
+        }
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(status, LORA_DEV_BAD_ID);
+    __syncthreads();
+
+    // ---- bucket totals, exclusive scan, per-warp running bases ------------
+    int carry = 0;
+    for (int b0 = 0; b0 < nb; b0 += kSegThreads) {
+        const int b = b0 + tid;
+        int tot = 0;
+        if (b < nb)
+            for (int ww = 0; ww < 32; ++ww) tot += whist[ww * nb + b];
+        int total;
+        const int ex = block_exclusive_scan(tot, wsum, &total);
+        if (b < nb) {
+            int run = carry + ex;
+            bsum[b] = run;
+            for (int ww = 0; ww < 32; ++ww) {
+                const int c = whist[ww * nb + b];
+                whist[ww * nb + b] = run;
+                run += c;
+            }
+        }
+        carry += total;
+    }
+    if (tid == 0) bsum[nb] = carry;
+    __syncthreads();
+    for (int b = tid; b <= nb; b += kSegThreads) p.offsets[b] = bsum[b];
+
+    // ---- pass 2: stable scatter -------------------------------------------
+    for (int64_t base = t_begin; base < t_end; base += 32) {
+        const int64_t t = base + lane;
+        const bool act = t < t_end;
+        const unsigned amask = __ballot_sync(0xffffffffu, act);
+        unsigned peers = 0;
+        int b = 0;
+        if (act) {
+            const int id = p.ids[t];
+            b = ((id >= 0 && id < p.A) ? id : -1) + 1;
+            peers = __match_any_sync(amask, b);
+            const int below = __popc(peers & ((1u << lane) - 1u));
+            p.perm[whist[w * nb + b] + below] = static_cast<int32_t>(t);
+        }
+        __syncwarp();
+        if (act && lane == __ffs(peers) - 1) whist[w * nb + b] += __popc(peers);
+        __syncwarp();
+    }
+
+    // ---- segments: one per non-empty adapter bucket, ascending id ---------
+    carry = 0;
+    for (int i0 = 0; i0 < p.A; i0 += kSegThreads) {
+        const int i = i0 + tid;
+        const int cnt = i < p.A ? bsum[i + 2] - bsum[i + 1] : 0;
+        const int flag = cnt > 0;
+        int total;
+        const int ex = block_exclusive_scan(flag, wsum, &total);
+        if (flag) {
+            const int s = carry + ex;
+            p.seg_id[s] = i;
+            p.seg_start[s] = bsum[i + 1];
+            p.seg_len[s] = cnt;
+            p.seg_rank[s] = p.rank[i];
+        }
+        carry += total;
+    }
+    const int nseg = carry;
+    if (tid == 0) {
+        *p.num_segments = nseg;
+        p.hdr[HDR_NSEG] = nseg;
+    }
+    __syncthreads();
+
+    // ---- split-K chunk list: every rank panel of every adapter present ----
+    carry = 0;
+    for (int s0 = 0; s0 < nseg; s0 += kSegThreads) {
+        const int s = s0 + tid;
+        const int nc = s < nseg ? p.seg_rank[s] / kChunk : 0;
+        int total;
+        const int ex = block_exclusive_scan(nc, wsum, &total);
+        if (s < nseg) {
+            const int i = p.seg_id[s];
+            const int c = carry + ex;
+            for (int q = 0; q < nc; ++q) {
+                p.dchunk_arow[c + q] = static_cast<int32_t>(p.a_offset[i] / p.K) + kChunk * q;
+                p.dchunk_brow[c + q] = static_cast<int32_t>(p.b_offset[i] / kChunk) + q * p.N;
+                p.dchunk_adapter[c + q] = i;
+            }
+        }
+        carry += total;
+    }
+    if (tid == 0) p.hdr[HDR_DCHUNKS] = carry;
+
+    // ---- tiled schedule: per 128-token tile of the permuted order, the
+    //      rank panels of the segments it intersects, and its shrink jobs ---
+    int carry_c = 0, carry_j = 0;
+    for (int m0 = 0; m0 < p.num_mtiles; m0 += kSegThreads) {
+        const int m = m0 + tid;
+        int nch = 0, sfirst = 0;
+        int64_t lo = 0, hi = 0;
+        if (m < p.num_mtiles) {
+            lo = static_cast<int64_t>(m) * kBM;
+            hi = lo + kBM < p.M ? lo + kBM : p.M;
+            int L = 0, R = nseg;   // first segment whose end is past lo
+            while (L < R) {
+                const int mid = (L + R) >> 1;
+                if (p.seg_start[mid] + p.seg_len[mid] > lo) R = mid; else L = mid + 1;
+            }
+            sfirst = L;
+            for (int s = sfirst; s < nseg && p.seg_start[s] < hi; ++s) nch += p.seg_rank[s] / kChunk;
+        }
+        int totc, totj;
+        const int exc = block_exclusive_scan(nch, wsum, &totc);
+        const int nj = (nch + kMaxShrinkChunks - 1) / kMaxShrinkChunks;
+        const int exj = block_exclusive_scan(nj, wsum, &totj);
+        if (m < p.num_mtiles) {
+            int c = carry_c + exc;
+            const int cfirst = c;
+            p.tile_chunk_off[m] = c;
+            p.tile_njobs[m] = nj;
+            for (int s = sfirst; s < nseg && p.seg_start[s] < hi; ++s) {
+                const int64_t s0 = p.seg_start[s], s1 = s0 + p.seg_len[s];
+                const int rlo = static_cast<int>((s0 > lo ? s0 : lo) - lo);
+                const int rhi = static_cast<int>((s1 < hi ? s1 : hi) - lo);
+                const int i = p.seg_id[s];
+                for (int q = 0; q < p.seg_rank[s] / kChunk; ++q, ++c) {
+                    p.chunk_arow[c] = static_cast<int32_t>(p.a_offset[i] / p.K) + kChunk * q;
+                    p.chunk_brow[c] = static_cast<int32_t>(p.b_offset[i] / kChunk) + q * p.N;
+                    p.chunk_rng[c] = pack_rng(rlo, rhi, q);
+                }
+            }
+            const int j = carry_j + exj;
+            for (int q = 0; q < nj; ++q) {
+                p.sjob_tile[j + q] = m;
+                p.sjob_c0[j + q] = cfirst + kMaxShrinkChunks * q;
+                const int c1 = cfirst + kMaxShrinkChunks * (q + 1);
+                p.sjob_c1[j + q] = c1 < cfirst + nch ? c1 : cfirst + nch;
+            }
+        }
+        carry_c += totc;
+        carry_j += totj;
+    }
+    if (tid == 0) {
+        p.tile_chunk_off[p.num_mtiles] = carry_c;
+        p.hdr[HDR_NCHUNKS] = carry_c;
+        p.hdr[HDR_NSJOBS] = carry_j;
+    }
+}
+
+size_t seg_build_smem_bytes(int32_t A) { return static_cast<size_t>(32 * (A + 1) + (A + 2) + 32) * 4; }
+
+cudaError_t launch_seg_build(const SegParams &p, cudaStream_t stream)
+{
+    const size_t smem = seg_build_smem_bytes(p.A);
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (smem > 48 * 1024 && (dev >= 64 || !configured[dev])) {
+        cudaError_t e = cudaFuncSetAttribute(seg_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(seg_build_smem_bytes(LORA_MAX_ADAPTERS)));
+        if (e != cudaSuccess) return e;
+        if (dev < 64) configured[dev] = 1;
+    }
+    seg_build_kernel<<<1, kSegThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace lora

@@ -1,0 +1,261 @@
+"""Python binding of liblora (include/lora.h), argument marshalling only.
+
+Every entry point keeps the C name and forwards device pointers, sizes and
+the current CUDA stream of PyTorch; all arithmetic runs in the library's CUDA
+kernels.  PyTorch only provides device memory and streams.  There is no CPU
+fallback: if the compiled library is missing, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblora.so")
+
+LORA_OK = 0
+LORA_ERR_NULL, LORA_ERR_SHAPE, LORA_ERR_ALIGN, LORA_ERR_RANK = 1, 2, 3, 4
+LORA_ERR_WORKSPACE, LORA_ERR_CUDA, LORA_ERR_UNSUPPORTED, LORA_ERR_SEGMENTS = 5, 6, 7, 8
+LORA_DEV_BAD_ID, LORA_DEV_TIMEOUT = 1, 2
+LORA_PATH_AUTO, LORA_PATH_TILED, LORA_PATH_SPLITK = 0, 1, 2
+LORA_MAX_RANK, LORA_RANK_ALIGN, LORA_MAX_ADAPTERS = 64, 16, 1024
+
+EXPORTS = ("lora_pool_layout", "lora_workspace_size", "lora_workspace_init", "lora_build_segments",
+           "lora_shrink", "lora_expand", "lora_linear", "lora_linear_ex", "lora_get_status",
+           "lora_status_string")
+
+
+class lora_pool_t(ctypes.Structure):
+    _fields_ = [("a_pool", ctypes.c_void_p), ("b_pool", ctypes.c_void_p),
+                ("a_offset", ctypes.c_void_p), ("b_offset", ctypes.c_void_p),
+                ("rank", ctypes.c_void_p), ("a_elems", ctypes.c_int64), ("b_elems", ctypes.c_int64),
+                ("num_adapters", ctypes.c_int32), ("max_rank", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("N", ctypes.c_int32)]
+
+
+class lora_segments_t(ctypes.Structure):
+    _fields_ = [("perm", ctypes.c_void_p), ("bucket_offsets", ctypes.c_void_p),
+                ("seg_id", ctypes.c_void_p), ("seg_start", ctypes.c_void_p),
+                ("seg_len", ctypes.c_void_p), ("seg_rank", ctypes.c_void_p),
+                ("num_segments", ctypes.c_void_p), ("plan", ctypes.c_void_p),
+                ("M", ctypes.c_int64), ("num_adapters", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class LoraError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {status_string(code)} (code {code})")
+        self.code = code
+
+
+_lib = None
+
+
+def load_library():
+    """Load liblora.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"liblora.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    PP = ctypes.POINTER(lora_pool_t)
+    PS = ctypes.POINTER(lora_segments_t)
+    sig = {
+        "lora_pool_layout": (ctypes.c_int, [I32, P, I32, I32, P, P, P, P, P]),
+        "lora_workspace_size": (SZ, [I64, I32, I32]),
+        "lora_workspace_init": (ctypes.c_int, [P, SZ, P]),
+        "lora_build_segments": (ctypes.c_int, [P, I64, PP, PS, P, SZ, P]),
+        "lora_shrink": (ctypes.c_int, [P, I64, P, PP, PS, P, I32, P, SZ, P]),
+        "lora_expand": (ctypes.c_int, [P, I32, I64, P, PP, PS, F32, P, P, SZ, P]),
+        "lora_linear": (ctypes.c_int, [P, I64, P, P, P, PP, F32, PS, P, P, SZ, P]),
+        "lora_linear_ex": (ctypes.c_int, [P, I64, P, P, P, PP, F32, PS, P, P, SZ, P, I32]),
+        "lora_get_status": (ctypes.c_int, [P, P, P]),
+        "lora_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().lora_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str):
+    if code != LORA_OK:
+        raise LoraError(code, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ---------------------------------------------------------------------------
+# adapter pool (load-time arrangement; not part of the per-step path)
+# ---------------------------------------------------------------------------
+
+def lora_pool_layout(true_ranks: Sequence[int], K: int, N: int):
+    """Rank-grouped offsets: returns (a_offset, b_offset, rank_padded, a_elems, b_elems)."""
+    lib = load_library()
+    n = len(true_ranks)
+    rk = (ctypes.c_int32 * max(n, 1))(*true_ranks)
+    ao = (ctypes.c_int64 * max(n, 1))()
+    bo = (ctypes.c_int64 * max(n, 1))()
+    rp = (ctypes.c_int32 * max(n, 1))()
+    ae, be = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib.lora_pool_layout(n, rk, K, N, ao, bo, rp, ctypes.byref(ae), ctypes.byref(be)),
+           "lora_pool_layout")
+    return list(ao)[:n], list(bo)[:n], list(rp)[:n], ae.value, be.value
+
+
+@dataclass
+class LoraPool:
+    """Device-resident rank-grouped adapter pool and its C descriptor."""
+    a_pool: torch.Tensor
+    b_pool: torch.Tensor
+    a_offset: torch.Tensor
+    b_offset: torch.Tensor
+    rank: torch.Tensor
+    desc: lora_pool_t
+    true_ranks: List[int]
+    padded_ranks: List[int]
+
+    @property
+    def num_adapters(self):
+        return self.desc.num_adapters
+
+
+def build_pool(A: List[torch.Tensor], B: List[torch.Tensor], K: int, N: int, device="cuda") -> LoraPool:
+    """Arrange adapters A_i [r_i, K], B_i [N, r_i] into the pool layout of
+    include/lora.h (rank-grouped; A rows and B panels zero-padded to 16)."""
+    ranks = [int(a.shape[0]) for a in A]
+    a_off, b_off, rpad, a_elems, b_elems = lora_pool_layout(ranks, K, N)
+    bf = torch.bfloat16
+    a_pool = torch.zeros(max(a_elems, 8), dtype=bf, device=device)
+    b_pool = torch.zeros(max(b_elems, 8), dtype=bf, device=device)
+    for i, (a, b) in enumerate(zip(A, B)):
+        r, rp = ranks[i], rpad[i]
+        assert a.shape == (r, K) and b.shape == (N, r)
+        a_pool[a_off[i]:a_off[i] + r * K] = a.to(device=device, dtype=bf).reshape(-1)
+        bp = torch.zeros(N, rp, dtype=bf, device=device)
+        bp[:, :r] = b.to(device=device, dtype=bf)
+        panels = bp.reshape(N, rp // 16, 16).permute(1, 0, 2).contiguous()   # [rp/16, N, 16]
+        b_pool[b_off[i]:b_off[i] + rp * N] = panels.reshape(-1)
+    a_offset = torch.tensor(a_off or [0], dtype=torch.int64, device=device)
+    b_offset = torch.tensor(b_off or [0], dtype=torch.int64, device=device)
+    rank = torch.tensor(rpad or [0], dtype=torch.int32, device=device)
+    desc = lora_pool_t(a_pool.data_ptr(), b_pool.data_ptr(), a_offset.data_ptr(), b_offset.data_ptr(),
+                       rank.data_ptr(), a_elems, b_elems, len(A), max(rpad) if rpad else 0, K, N)
+    return LoraPool(a_pool, b_pool, a_offset, b_offset, rank, desc, ranks, rpad)
+
+
+# ---------------------------------------------------------------------------
+# workspace and segments
+# ---------------------------------------------------------------------------
+
+def lora_workspace_size(M: int, N: int, num_adapters: int) -> int:
+    return int(load_library().lora_workspace_size(M, N, num_adapters))
+
+
+class Workspace:
+    """A zero-initialised device workspace sized for (M, N, num_adapters)."""
+
+    def __init__(self, M: int, N: int, num_adapters: int, device="cuda"):
+        self.nbytes = lora_workspace_size(M, N, num_adapters)
+        self.buf = torch.zeros(max(self.nbytes, 256), dtype=torch.uint8, device=device)
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.buf.data_ptr())
+
+
+def lora_workspace_init(ws: Workspace, stream=None):
+    _check(load_library().lora_workspace_init(ws.ptr, ws.nbytes, _stream(stream)), "lora_workspace_init")
+
+
+def lora_build_segments(ids: torch.Tensor, pool: LoraPool, ws: Workspace, stream=None) -> lora_segments_t:
+    out = lora_segments_t()
+    _check(load_library().lora_build_segments(_ptr(ids), ids.numel(), ctypes.byref(pool.desc),
+                                              ctypes.byref(out), ws.ptr, ws.nbytes, _stream(stream)),
+           "lora_build_segments")
+    return out
+
+
+def segments_to_host(segs: lora_segments_t, ws: Workspace, M: int, num_adapters: int) -> dict:
+    """Copy a device segment table (it lives inside ws) into CPU int32 tensors."""
+    base = ws.buf.data_ptr()
+
+    def grab(ptr, n):
+        off = int(ptr) - base
+        assert 0 <= off and off + 4 * n <= ws.buf.numel()
+        return ws.buf[off:off + 4 * n].view(torch.int32).cpu()
+
+    ns = int(grab(segs.num_segments, 1)[0])
+    return dict(perm=grab(segs.perm, M), bucket_offsets=grab(segs.bucket_offsets, num_adapters + 2),
+                seg_id=grab(segs.seg_id, ns), seg_start=grab(segs.seg_start, ns),
+                seg_len=grab(segs.seg_len, ns), seg_rank=grab(segs.seg_rank, ns), num_segments=ns)
+
+
+# ---------------------------------------------------------------------------
+# compute entry points
+# ---------------------------------------------------------------------------
+
+def lora_linear(x: torch.Tensor, W: torch.Tensor, bias: Optional[torch.Tensor], ids: torch.Tensor,
+                pool: LoraPool, scale: float, ws: Workspace, y: Optional[torch.Tensor] = None,
+                segs: Optional[lora_segments_t] = None, path: int = LORA_PATH_AUTO,
+                stream=None) -> torch.Tensor:
+    """y = x W^T + bias + scale * (x A_id^T) B_id^T per token (id -1: base only)."""
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty(M, W.shape[0], dtype=torch.bfloat16, device=x.device)
+    _check(load_library().lora_linear_ex(
+        _ptr(x), M, _ptr(W), _ptr(bias), _ptr(ids), ctypes.byref(pool.desc), float(scale),
+        ctypes.byref(segs) if segs is not None else None, _ptr(y), ws.ptr, ws.nbytes,
+        _stream(stream), int(path)), "lora_linear")
+    return y
+
+
+def lora_shrink(x: torch.Tensor, ids: torch.Tensor, pool: LoraPool, ws: Workspace,
+                S: Optional[torch.Tensor] = None, s_cols: Optional[int] = None,
+                segs: Optional[lora_segments_t] = None, stream=None) -> torch.Tensor:
+    """S = x A_id^T (fp32, [M, s_cols], zero past each row's rank and on -1 rows)."""
+    M = x.shape[0]
+    s_cols = s_cols or max(pool.desc.max_rank, 16)
+    if S is None:
+        S = torch.empty(M, s_cols, dtype=torch.float32, device=x.device)
+    _check(load_library().lora_shrink(
+        _ptr(x), M, _ptr(ids), ctypes.byref(pool.desc),
+        ctypes.byref(segs) if segs is not None else None, _ptr(S), s_cols, ws.ptr, ws.nbytes,
+        _stream(stream)), "lora_shrink")
+    return S
+
+
+def lora_expand(S: torch.Tensor, ids: torch.Tensor, pool: LoraPool, scale: float, y: torch.Tensor,
+                ws: Workspace, segs: Optional[lora_segments_t] = None, stream=None) -> torch.Tensor:
+    """y += scale * S B_id^T in place (bf16 y, id -1 rows untouched)."""
+    M = S.shape[0]
+    _check(load_library().lora_expand(
+        _ptr(S), S.shape[1], M, _ptr(ids), ctypes.byref(pool.desc),
+        ctypes.byref(segs) if segs is not None else None, float(scale), _ptr(y), ws.ptr, ws.nbytes,
+        _stream(stream)), "lora_expand")
+    return y
+
+
+def lora_get_status(ws: Workspace, stream=None) -> int:
+    v = ctypes.c_int32()
+    _check(load_library().lora_get_status(ws.ptr, _stream(stream), ctypes.byref(v)), "lora_get_status")
+    return v.value

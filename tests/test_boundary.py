@@ -1,0 +1,78 @@
+"""CPU checks of the C ABI boundary: the library loads, exports every symbol
+that include/lora.h declares, and its host-only helpers behave.  No compute
+call runs here (no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from segmented_gemm_gb300 import lora as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "lora.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(lora_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(L.LIB_PATH):
+        from segmented_gemm_gb300 import build
+        build.build()
+    return L.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(L.EXPORTS)
+
+
+def test_pool_layout_rank_grouped(lib):
+    a_off, b_off, rpad, ae, be = L.lora_pool_layout([8, 64, 16, 33, 20], 4096, 1024)
+    assert rpad == [16, 64, 16, 48, 32]
+    # grouped by padded rank: 16s (ids 0, 2), then 32 (id 4), 48 (id 3), 64 (id 1)
+    order = sorted(range(5), key=lambda i: a_off[i])
+    assert order == [0, 2, 4, 3, 1]
+    assert all(a_off[i] % 4096 == 0 and b_off[i] % 16 == 0 for i in range(5))
+    assert ae == sum(rpad) * 4096 and be == sum(rpad) * 1024
+    # contiguous, non-overlapping
+    for x, y in zip(order, order[1:]):
+        assert a_off[y] == a_off[x] + rpad[x] * 4096
+        assert b_off[y] == b_off[x] + rpad[x] * 1024
+
+
+@pytest.mark.parametrize("ranks,K,N,code", [([0], 64, 64, L.LORA_ERR_RANK), ([65], 64, 64, L.LORA_ERR_RANK),
+                                            ([16], 60, 64, L.LORA_ERR_SHAPE),
+                                            ([16], 64, 0, L.LORA_ERR_SHAPE)])
+def test_pool_layout_errors(lib, ranks, K, N, code):
+    with pytest.raises(L.LoraError) as e:
+        L.lora_pool_layout(ranks, K, N)
+    assert e.value.code == code
+
+
+def test_workspace_size_monotone(lib):
+    a = L.lora_workspace_size(1024, 4096, 40)
+    b = L.lora_workspace_size(8192, 4096, 40)
+    assert 0 < a < b
+    assert L.lora_workspace_size(-1, 64, 1) == 0
+
+
+def test_status_strings(lib):
+    for c in range(9):
+        assert L.status_string(c)
+    assert "unknown" in L.status_string(99)
+
+
+def test_null_arguments_rejected_without_gpu(lib):
+    # host-side validation runs before anything touches the device
+    rc = lib.lora_linear_ex(None, 4, None, None, None, None, ctypes.c_float(1.0), None, None, None, 0, None, 0)
+    assert rc == L.LORA_ERR_NULL
+    rc = lib.lora_linear_ex(None, -1, None, None, None, None, ctypes.c_float(1.0), None, None, None, 0, None, 0)
+    assert rc == L.LORA_ERR_SHAPE

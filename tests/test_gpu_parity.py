@@ -1,0 +1,275 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
+
+Bar: segment tables and permutations bit-exact; outputs within
+|gpu - oracle| <= 2e-2 * (1 + |oracle|) per element (bf16 output, fp32
+accumulation, S rounded once to bf16 before the second product).
+Every output buffer is pre-filled with NaN so an element the kernels never
+write fails the comparison.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle
+from segmented_gemm_gb300 import lora as L
+from segmented_gemm_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+
+
+def to_dev(wl):
+    d = "cuda"
+    return dict(x=wl.x.to(d), W=wl.W.to(d), bias=None if wl.bias is None else wl.bias.to(d),
+                ids=wl.ids.to(d), pool=L.build_pool(wl.A, wl.B, wl.K, wl.N, d))
+
+
+def rel_err(gpu, ref):
+    g = gpu.detach().float().cpu().double().numpy()
+    return np.abs(g - ref) / (1.0 + np.abs(ref))
+
+
+def assert_close(gpu, ref, tol=TOL, what=""):
+    e = rel_err(gpu, ref)
+    bad = ~(e <= tol)
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements out of tolerance, max err {np.nanmax(e):.3e}"
+
+
+def run_linear(wl, dev, path=L.LORA_PATH_AUTO, prebuilt=False):
+    ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
+    y = torch.full((wl.M, wl.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    segs = L.lora_build_segments(dev["ids"], dev["pool"], ws) if prebuilt else None
+    L.lora_linear(dev["x"], dev["W"], dev["bias"], dev["ids"], dev["pool"], wl.scale, ws, y=y,
+                  segs=segs, path=path)
+    status = L.lora_get_status(ws)
+    return y, ws, status
+
+
+def sample_rows(M, per_tile=3, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = set([0, M - 1])
+    for t0 in range(0, M, 128):
+        hi = min(M, t0 + 128)
+        rows.update(int(r) for r in rng.integers(t0, hi, size=min(per_tile, hi - t0)))
+    return sorted(rows)
+
+
+def check_segments(wl, dev, ws, segs):
+    got = L.segments_to_host(segs, ws, wl.M, wl.num_adapters)
+    want = oracle.build_segments(wl.ids.numpy(), wl.num_adapters, wl.ranks)
+    assert np.array_equal(got["perm"].numpy(), want["perm"])
+    assert np.array_equal(got["bucket_offsets"].numpy(), want["bucket_offsets"])
+    assert got["num_segments"] == want["num_segments"]
+    for k in ("seg_id", "seg_start", "seg_len", "seg_rank"):
+        assert np.array_equal(got[k].numpy(), want[k]), k
+
+
+# ---------------------------------------------------------------------------
+# segment builder: bit-exact
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", workloads.CONFIG_NAMES)
+def test_segments_configs(name):
+    wl = workloads.make_config(name)
+    dev = to_dev(wl)
+    ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
+    segs = L.lora_build_segments(dev["ids"], dev["pool"], ws)
+    check_segments(wl, dev, ws, segs)
+    assert L.lora_get_status(ws) == 0
+
+
+@pytest.mark.parametrize("M,A,mode", [(1, 3, "uniform"), (33, 1, "single"), (1000, 7, "runs"),
+                                      (4097, 200, "uniform"), (300, 5, "all_base"),
+                                      (20000, 1024, "uniform")])
+def test_segments_edge(M, A, mode):
+    ranks = [16 * (1 + (i % 4)) for i in range(A)]
+    ids = None
+    if A == 1024:
+        g = torch.Generator().manual_seed(3)
+        ids = torch.randint(-1, A, (M,), generator=g)
+    wl = workloads.make_custom(M, 64, 64, ranks, seed=M + A, ids=ids, id_mode=mode)
+    dev = to_dev(wl)
+    ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
+    segs = L.lora_build_segments(dev["ids"], dev["pool"], ws)
+    check_segments(wl, dev, ws, segs)
+
+
+def test_segments_invalid_ids_flagged():
+    wl = workloads.make_custom(50, 64, 64, [16, 32], seed=1, id_mode="uniform")
+    wl.ids[3] = 7
+    wl.ids[9] = -4
+    dev = to_dev(wl)
+    ws = L.Workspace(wl.M, wl.N, 2)
+    segs = L.lora_build_segments(dev["ids"], dev["pool"], ws)
+    check_segments(wl, dev, ws, segs)      # oracle also sorts them as -1
+    assert L.lora_get_status(ws) & L.LORA_DEV_BAD_ID
+    assert L.lora_get_status(ws) == 0       # reading clears the word
+
+
+# ---------------------------------------------------------------------------
+# the fused layer
+# ---------------------------------------------------------------------------
+
+def test_tiny_config_all_rows_both_paths():
+    wl = workloads.make_config("tiny")
+    dev = to_dev(wl)
+    ref = oracle.lora_linear(wl)
+    for path in (L.LORA_PATH_AUTO, L.LORA_PATH_TILED, L.LORA_PATH_SPLITK):
+        y, ws, status = run_linear(wl, dev, path)
+        assert status == 0
+        assert_close(y, ref, what=f"tiny path={path}")
+
+
+@pytest.mark.parametrize("path", [L.LORA_PATH_TILED, L.LORA_PATH_SPLITK])
+@pytest.mark.parametrize("M,K,N,ranks,mode", [
+    (1, 64, 64, [16], "single"),
+    (7, 200, 136, [8, 40, 64], "uniform"),          # K not a multiple of 64, N ragged
+    (100, 320, 520, [16, 32, 48, 64, 20], "uniform"),
+    (128, 256, 256, [64] * 6, "uniform"),
+    (61, 512, 384, [16] * 40, "uniform"),            # many segments in one tile
+])
+def test_linear_small_shapes(path, M, K, N, ranks, mode):
+    wl = workloads.make_custom(M, K, N, ranks, seed=M * 7 + K, id_mode=mode, p_base=0.15, scale=1.5)
+    dev = to_dev(wl)
+    y, ws, status = run_linear(wl, dev, path)
+    assert status == 0
+    assert_close(y, oracle.lora_linear(wl), what=f"M{M} K{K} N{N} path={path}")
+
+
+@pytest.mark.parametrize("M,K,N,ranks,mode", [
+    (300, 320, 520, [16, 32, 48, 64], "runs"),       # several tiles, ragged M tail
+    (640, 256, 768, [64] * 5 + [16] * 5, "uniform"),
+    (257, 128, 264, [64] * 20, "uniform"),           # > 16 rank panels in a tile: 2 shrink jobs
+    (1000, 192, 512, [16, 32], "all_base"),          # base GEMM only
+    (513, 256, 256, [32], "single"),
+])
+def test_linear_tiled_multi_tile(M, K, N, ranks, mode):
+    wl = workloads.make_custom(M, K, N, ranks, seed=M + N, id_mode=mode, p_base=0.2, scale=0.75)
+    dev = to_dev(wl)
+    y, ws, status = run_linear(wl, dev)
+    assert status == 0
+    assert_close(y, oracle.lora_linear(wl), what=f"M{M} K{K} N{N}")
+
+
+def test_linear_no_bias_and_prebuilt_segments():
+    wl = workloads.make_custom(200, 256, 320, [16, 64, 32], seed=77, with_bias=False)
+    dev = to_dev(wl)
+    ref = oracle.lora_linear(wl)
+    for path in (L.LORA_PATH_AUTO, L.LORA_PATH_TILED):
+        y, ws, status = run_linear(wl, dev, path, prebuilt=True)
+        assert status == 0
+        assert_close(y, ref, what=f"no-bias path={path}")
+
+
+def test_linear_repeated_calls_reuse_workspace():
+    """Counters are left zeroed: the same workspace serves call after call."""
+    wl = workloads.make_custom(96, 256, 512, [16, 32, 64], seed=5, scale=2.0)
+    dev = to_dev(wl)
+    ref = oracle.lora_linear(wl)
+    for path in (L.LORA_PATH_TILED, L.LORA_PATH_SPLITK):
+        ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
+        segs = L.lora_build_segments(dev["ids"], dev["pool"], ws)
+        for _ in range(4):
+            y = torch.full((wl.M, wl.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+            L.lora_linear(dev["x"], dev["W"], dev["bias"], dev["ids"], dev["pool"], wl.scale, ws, y=y,
+                          segs=segs, path=path)
+            assert_close(y, ref, what=f"repeat path={path}")
+        assert L.lora_get_status(ws) == 0
+
+
+def test_decode_walkthrough_shapes():
+    """Page's decode walk-through: ids [0, 2, -1], K 4096, N 12288, ranks 16 / 32."""
+    wl = workloads.make_custom(3, 4096, 12288, [16, 16, 32], seed=34, ids=[0, 2, -1])
+    dev = to_dev(wl)
+    ref = oracle.lora_linear(wl)
+    for path in (L.LORA_PATH_SPLITK, L.LORA_PATH_TILED):
+        y, ws, status = run_linear(wl, dev, path)
+        assert status == 0
+        assert_close(y, ref, what=f"walkthrough path={path}")
+
+
+def test_invalid_ids_are_base_only_and_flagged():
+    wl = workloads.make_custom(40, 128, 256, [16, 16], seed=8)
+    wl.ids[0] = 5
+    wl.ids[1] = -3
+    dev = to_dev(wl)
+    ref = oracle.lora_linear(wl)      # oracle treats them as -1 too
+    for path in (L.LORA_PATH_TILED, L.LORA_PATH_SPLITK):
+        y, ws, status = run_linear(wl, dev, path)
+        assert status & L.LORA_DEV_BAD_ID
+        assert_close(y, ref, what=f"invalid ids path={path}")
+
+
+def test_empty_batch_is_noop():
+    wl = workloads.make_custom(4, 64, 64, [16], seed=2)
+    dev = to_dev(wl)
+    ws = L.Workspace(0, 64, 1)
+    x = dev["x"][:0]
+    y = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    L.lora_linear(x, dev["W"], dev["bias"], dev["ids"][:0], dev["pool"], 1.0, ws, y=y)
+
+
+def test_host_errors():
+    wl = workloads.make_custom(16, 64, 64, [16], seed=2)
+    dev = to_dev(wl)
+    ws = L.Workspace(16, 64, 1)
+    small = L.Workspace(1, 8, 0)
+    with pytest.raises(L.LoraError) as e:
+        L.lora_linear(dev["x"], dev["W"], None, dev["ids"], dev["pool"], 1.0, small)
+    assert e.value.code == L.LORA_ERR_WORKSPACE
+    with pytest.raises(L.LoraError) as e:
+        L.lora_linear(dev["x"], dev["W"], None, dev["ids"], dev["pool"], 1.0, ws,
+                      y=torch.empty(16, 64, dtype=torch.bfloat16, device="cuda"), path=7)
+    assert e.value.code == L.LORA_ERR_SHAPE
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads: sampled rows against the oracle
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["decode", "prefill", "qkv", "mlp_down"])
+def test_config_full_size_sampled(name):
+    wl = workloads.make_config(name)
+    dev = to_dev(wl)
+    ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
+    segs = L.lora_build_segments(dev["ids"], dev["pool"], ws)
+    y = torch.full((wl.M, wl.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    L.lora_linear(dev["x"], dev["W"], dev["bias"], dev["ids"], dev["pool"], wl.scale, ws, y=y, segs=segs)
+    assert L.lora_get_status(ws) == 0
+    assert not torch.isnan(y).any()
+    rows = sample_rows(wl.M, per_tile=2 if wl.M > 2048 else 3)
+    ref = oracle.lora_linear(wl, rows=rows)
+    assert_close(y[rows], ref, what=name)
+
+
+# ---------------------------------------------------------------------------
+# the two products alone
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,K,ranks,mode", [(64, 256, [8, 8, 16, 16], "uniform"),
+                                            (300, 320, [16, 48, 64, 32], "runs"),
+                                            (257, 128, [64] * 20, "uniform")])
+def test_shrink(M, K, ranks, mode):
+    wl = workloads.make_custom(M, K, 64, ranks, seed=M, id_mode=mode, p_base=0.2)
+    dev = to_dev(wl)
+    ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
+    S = torch.full((M, 64), float("nan"), dtype=torch.float32, device="cuda")
+    L.lora_shrink(dev["x"], dev["ids"], dev["pool"], ws, S=S, s_cols=64)
+    ref = oracle.shrink(wl, 64)
+    assert_close(S, ref, tol=1e-3, what="shrink")
+
+
+@pytest.mark.parametrize("M,N,ranks,mode", [(64, 256, [8, 8, 16, 16], "uniform"),
+                                            (300, 520, [16, 48, 64, 32], "runs")])
+def test_expand(M, N, ranks, mode):
+    wl = workloads.make_custom(M, 64, N, ranks, seed=N, id_mode=mode, p_base=0.2)
+    dev = to_dev(wl)
+    ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
+    S = workloads.random_fp32((M, 64), seed=11)
+    y0 = workloads.random_fp32((M, N), seed=12).to(torch.bfloat16)
+    y = y0.to("cuda")
+    L.lora_expand(S.to("cuda"), dev["ids"], dev["pool"], 1.25, y, ws)
+    ref = oracle.expand(wl, S, y0, scale=1.25)
+    assert_close(y, ref, what="expand")
+    base_rows = (wl.ids < 0).nonzero().flatten()
+    assert torch.equal(y[base_rows.to('cuda')].cpu(), y0[base_rows])    # -1 rows untouched
