@@ -1,0 +1,499 @@
+"""Benchmark of the fused dynamic multi-LoRA linear layer on GB300.
+
+One step = one pass of the whole hot path over one batch: the segment build
+(bucket sort of lora_id_map + work lists) and the fused layer
+y = x W^T + bias + scale * (x A_id^T) B_id^T, both through the C ABI.
+
+Default workload: the decode step (M=32 tokens, K=N=4096, 20 adapters of
+rank 16/32/64, 10% base-only tokens), seeded synthetic data.  Prints ONE JSON
+line on rank 0.  Under torchrun each rank runs its own replica on its own GPU
+(independent batches, no collective on the data path): weak scaling.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config decode|tiny|prefill|qkv|mlp_down] [--no-sweep] [--no-cpu]
+
+--impl reference times the CPU fp64 oracle (the reference arm of this
+project): rank 0 only, each step a bounded element sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from segmented_gemm_gb300 import workloads  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "multi-LoRA linear tokens/s; % of HBM / bf16 tensor roofline, M=32..8192"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CONFIG_TEXT = {
+    "tiny": "tiny: M=64, K=256, N=256, 4 adapters ranks {8,8,16,16}, ids uniform over {-1..3}",
+    "decode": "decode step: M=32 tokens, K=4096, N=4096, 20 adapters ranks U{16,32,64}, 10% base-only",
+    "prefill": "prefill: M=1024 from 16 requests (contiguous runs), K=N=4096, 40 adapters, 5% base-only requests",
+    "qkv": "merged QKV: M=2048, K=4096, N=6144, 8 adapters rank 64, Zipf(1.1) ids shuffled, 20% base-only",
+    "mlp_down": "MLP down: M=8192, K=12288, N=4096, 32 adapters U{16,32,64}, Zipf(1.1) requests, 20% base-only",
+}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work of one step (counts only)
+# ---------------------------------------------------------------------------
+
+def algorithmic_work(wl):
+    """Bytes: W, x, y, bias, ids and the A_i / B_i of distinct adapters
+    present at true rank.  Flops: 2MKN + sum over LoRA tokens 2 r (K + N)."""
+    ids = wl.ids
+    present = sorted(set(int(i) for i in ids.tolist() if 0 <= i < wl.num_adapters))
+    adapter_elems = sum(wl.ranks[i] * (wl.K + wl.N) for i in present)
+    nbytes = 2 * (wl.N * wl.K + wl.M * wl.K + wl.M * wl.N + (wl.N if wl.bias is not None else 0)
+                  + adapter_elems) + 4 * wl.M
+    lora_flops = sum(2 * wl.ranks[int(i)] * (wl.K + wl.N) for i in ids.tolist() if 0 <= i < wl.num_adapters)
+    flops = 2 * wl.M * wl.K * wl.N + lora_flops
+    return nbytes, flops, len(present)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "segmented_gemm_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"source_hash:\s*([0-9a-f]+)", txt)
+    if not m or not h or h.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.t0 = self.t1 = None
+        ident = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = ["--id=" + (uuid if uuid.startswith("GPU-") else "GPU-" + uuid)]
+        except Exception:
+            ident = []
+        self.cmd = ["nvidia-smi", *ident, "--query-gpu=timestamp," + self.FIELDS,
+                    "--format=csv,noheader,nounits", "-lms", "50"]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append(dict(ts=ts, sm=float(parts[1]), smmax=float(parts[2]), power=float(parts[3]),
+                                 active=parts[4], hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except (ValueError, IndexError):
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        pmax = max(r["power"] for r in rows)
+        window = "timed region"
+        load = []
+        if self.t0 is not None and self.t1 is not None:
+            load = [r for r in rows if self.t0 - 0.06 <= r["ts"] <= self.t1 + 0.06]
+        if not load:   # timed region shorter than the sampling interval: samples under load
+            window = "under load around the timed region"
+            load = [r for r in rows if r["power"] >= 0.5 * pmax] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": max(r["smmax"] for r in load),
+                "reasons": sorted(reasons), "samples": len(load), "window": window,
+                "power_w_max": max(r["power"] for r in load)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+class InputSet:
+    def __init__(self, wl, L, device):
+        self.x = wl.x.to(device)
+        self.W = wl.W.to(device)
+        self.bias = None if wl.bias is None else wl.bias.to(device)
+        self.ids = wl.ids.to(device)
+        self.pool = L.build_pool(wl.A, wl.B, wl.K, wl.N, device)
+        self.y = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device=device)
+        self.ws = L.Workspace(wl.M, wl.N, wl.num_adapters, device)
+        self.segs = None
+
+    def nbytes(self):
+        p = self.pool
+        t = [self.x, self.W, self.y, self.ids, p.a_pool, p.b_pool] + ([self.bias] if self.bias is not None else [])
+        return sum(a.numel() * a.element_size() for a in t)
+
+
+def build_sets(wl, L, device, min_bytes=4 * L2_BYTES, max_sets=16):
+    first = InputSet(wl, L, device)
+    n = 1 if first.nbytes() >= min_bytes else min(max_sets, math.ceil(min_bytes / first.nbytes()))
+    sets = [first] + [InputSet(wl, L, device) for _ in range(n - 1)]
+    return sets
+
+
+def graph_of(fn, n_steps, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n_steps):
+                fn(i)
+    return g
+
+
+def time_steps(fn, steps, warmup, stream, chunk=None, sampler=None, dist_barrier=None):
+    """Replay `fn(i)` for exactly `steps` steps inside CUDA graphs, timed with
+    CUDA events on `stream`.  Returns total milliseconds."""
+    chunk = chunk or min(steps, 200)
+    for i in range(warmup):
+        with torch.cuda.stream(stream):
+            fn(i)
+    torch.cuda.synchronize()
+    full, rem = divmod(steps, chunk)
+    g_full = graph_of(fn, chunk, stream) if full else None
+    g_rem = graph_of(fn, rem, stream) if rem else None
+    for g in (g_full, g_rem):          # graph warm-up
+        if g is not None:
+            g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist_barrier:
+        dist_barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t0")
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(full):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t1")
+    if dist_barrier:
+        dist_barrier()
+    return e0.elapsed_time(e1)
+
+
+def run_config(name, L, device, steps, warmup, stream, sampler=None, dist_barrier=None, e2e=True):
+    wl = workloads.make_config(name)
+    nbytes, flops, n_present = algorithmic_work(wl)
+    sets = build_sets(wl, L, device)
+    ns = len(sets)
+
+    def full_step(i):
+        s = sets[i % ns]
+        L.lora_linear(s.x, s.W, s.bias, s.ids, s.pool, wl.scale, s.ws, y=s.y)
+
+    for s in sets:                          # prebuilt tables for the kernel-only timing
+        s.segs = L.lora_build_segments(s.ids, s.pool, s.ws)
+
+    def kernel_step(i):
+        s = sets[i % ns]
+        L.lora_linear(s.x, s.W, s.bias, s.ids, s.pool, wl.scale, s.ws, y=s.y, segs=s.segs)
+
+    # the fused kernel alone (segment tables prebuilt): dominant-kernel duration
+    kern_ms = time_steps(kernel_step, steps, warmup, stream) / steps
+    if sampler:
+        sampler.start()
+    total_ms = time_steps(full_step, steps, warmup, stream, sampler=sampler, dist_barrier=dist_barrier)
+    clocks = sampler.stop() if sampler else None
+    for s in sets:                          # the timed step also rebuilds its table
+        s.segs = None
+    status = L.lora_get_status(sets[0].ws)
+    res = dict(name=name, wl=wl, ms_per_step=total_ms / steps, kernel_ms=kern_ms, bytes=nbytes, flops=flops,
+               n_present=n_present, n_sets=ns, set_bytes=sets[0].nbytes(), status=status, clocks=clocks)
+    if e2e:
+        res["e2e"] = run_e2e(wl, sets[0], L, device, min(steps, 5000), max(3, min(warmup, 50)), stream)
+    return res
+
+
+def run_e2e(wl, s, L, device, steps, warmup, stream):
+    """Same metric through the public API with host buffers: every step copies
+    x and lora_id_map host->device (pinned) and reads y back."""
+    hx = wl.x.pin_memory()
+    hids = wl.ids.pin_memory()
+    hy = torch.empty(wl.M, wl.N, dtype=torch.bfloat16).pin_memory()
+    dx, dids = torch.empty_like(s.x), torch.empty_like(s.ids)
+
+    def step():
+        dx.copy_(hx, non_blocking=True)
+        dids.copy_(hids, non_blocking=True)
+        L.lora_linear(dx, s.W, s.bias, dids, s.pool, wl.scale, s.ws, y=s.y)
+        hy.copy_(s.y, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    h2d = hx.numel() * hx.element_size() + hids.numel() * hids.element_size()
+    d2h = hy.numel() * hy.element_size()
+    return {"value": wl.M / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+
+
+def cpu_baseline(name, budget_s=8.0):
+    """The CPU oracle as it stands, on whole rows of the same workload."""
+    from oracle import oracle
+    wl = workloads.make_config(name)
+    prep = oracle.Prepared(wl)
+    rows_done, t_used, reps = 0, 0.0, 0
+    rng = np.random.default_rng(0)
+    per_call = min(wl.M, max(1, oracle.num_threads()))
+    while t_used < budget_s and reps < 1000:
+        rows = rng.integers(0, wl.M, per_call) if per_call < wl.M else np.arange(wl.M)
+        t0 = time.perf_counter()
+        oracle.lora_linear_rows_prepared(prep, rows)
+        t_used += time.perf_counter() - t0
+        rows_done += len(rows)
+        reps += 1
+    return {"value": rows_done / t_used, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{rows_done} whole output rows of the {name} workload ({reps} calls of {per_call} rows), "
+                      f"{t_used:.1f} s of CPU time, fp64 plain loops, OpenMP over rows"}
+
+
+def ours(args):
+    from segmented_gemm_gb300 import lora as L
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    L.load_library()
+    stream = torch.cuda.Stream(device)
+    barrier = (lambda: dist.barrier()) if dist else None
+    peaks, peak_kind = load_peaks()
+
+    sampler = ClockSampler(local)
+    r = run_config(args.config, L, device, args.steps, args.warmup, stream, sampler=sampler,
+                   dist_barrier=barrier)
+    wl = r["wl"]
+    ms = r["ms_per_step"]
+    if dist:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * wl.M / (ms * 1e-3)
+
+    # roofline of the dominant kernel (the fused layer)
+    kern_s = r["kernel_ms"] * 1e-3
+    hbm_bound = wl.M <= 128
+    kname = "lora_splitk_kernel" if hbm_bound else "lora_tc_kernel"
+    if hbm_bound:
+        achieved = r["bytes"] / kern_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    else:
+        achieved = r["flops"] / kern_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4)}
+    roof["traffic"] = profiled_traffic(kname, args.config)
+    roof["kernel"] = kname
+    roof["kernel_us"] = round(r["kernel_ms"] * 1e3, 3)
+    roof["algorithmic_bytes"] = r["bytes"]
+    roof["algorithmic_flops"] = r["flops"]
+    roof["peak_source"] = f"{peak_kind} ({'MEASURED_PEAKS.json' if peak_kind == 'measured' else 'recipe fallback'})"
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, bf16-rounded N(0,s) draws)",
+        "config": {"workload": CONFIG_TEXT[args.config], "M": wl.M, "K": wl.K, "N": wl.N,
+                   "num_adapters": wl.num_adapters, "adapters_present": r["n_present"],
+                   "parallelism": f"replicas x{world} (independent batches)",
+                   "l2": f"rotating {r['n_sets']} input sets of {r['set_bytes'] / 1e6:.1f} MB "
+                         f"({r['n_sets'] * r['set_bytes'] / 1e6:.0f} MB > L2)" if r["n_sets"] > 1 else
+                         f"inputs {r['set_bytes'] / 1e6:.0f} MB > 4x L2",
+                   "timing": "CUDA graphs of whole steps (segment build + fused layer), CUDA events"},
+        "roofline": roof,
+        "tflops": round(r["flops"] / (ms * 1e-3) / 1e12, 2),
+        "e2e": {k: r["e2e"][k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
+        "gpu_launches": 2 * args.steps,
+        "clocks": r["clocks"],
+        "device_status": r["status"],
+    }
+    if world == 1 and rank == 0 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline(args.config)
+    if not args.no_sweep and rank == 0:
+        sweep = {}
+        for name in ("prefill", "qkv", "mlp_down"):
+            if name == args.config:
+                continue
+            s = run_config(name, L, device, 30 if name == "mlp_down" else 100, 5, stream, e2e=False)
+            kt = s["kernel_ms"] * 1e-3
+            sweep[name] = {
+                "M": s["wl"].M, "tokens_per_s": round(s["wl"].M / (s["ms_per_step"] * 1e-3), 1),
+                "ms_per_step": round(s["ms_per_step"], 5), "kernel_us": round(s["kernel_ms"] * 1e3, 2),
+                "kernel_tflops": round(s["flops"] / kt / 1e12, 1),
+                "tensor_frac": round(s["flops"] / kt / 1e12 / peaks["bf16_tflops"], 4),
+                "hbm_gbs": round(s["bytes"] / kt / 1e9, 1), "device_status": s["status"]}
+            del s
+            torch.cuda.empty_cache()
+        out["sweep"] = sweep
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+
+def reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import oracle
+    wl = workloads.make_config(args.config)
+    prep = oracle.Prepared(wl)
+    rng = np.random.default_rng(0)
+    # size each step's sample so the whole run takes about a minute: whole
+    # rows (the oracle's row routine) when a step can afford a batch of rows,
+    # else single output elements
+    budget = 60.0
+    per_step = budget / max(1, args.steps + args.warmup)
+    threads = oracle.num_threads()
+    row_batch = min(wl.M, threads)
+    t0 = time.perf_counter()
+    oracle.lora_linear_rows_prepared(prep, rng.integers(0, wl.M, row_batch))
+    t_rows = time.perf_counter() - t0
+    if t_rows <= per_step:
+        nb = max(1, int(per_step / t_rows))
+        n_rows = min(wl.M, row_batch * nb)
+
+        def step():
+            oracle.lora_linear_rows_prepared(prep, rng.integers(0, wl.M, n_rows))
+        per_step_tokens = float(n_rows)
+        sample = f"each step: {n_rows} random whole output rows of the {args.config} workload"
+    else:
+        probe_n = 256
+        t0 = time.perf_counter()
+        oracle.lora_linear_elems(prep, rng.integers(0, wl.M, probe_n), rng.integers(0, wl.N, probe_n))
+        per_elem = (time.perf_counter() - t0) / probe_n
+        n = int(max(1, min(wl.M * wl.N, per_step / per_elem)))
+
+        def step():
+            oracle.lora_linear_elems(prep, rng.integers(0, wl.M, n), rng.integers(0, wl.N, n))
+        per_step_tokens = n / wl.N
+        sample = (f"each step: {n} random output elements of the {args.config} workload "
+                  f"(N elements count as one token)")
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = args.steps * per_step_tokens / dt
+    ms = dt * 1e3 / args.steps
+    cores = oracle.num_threads()
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": 0,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+           "config": {"workload": CONFIG_TEXT[args.config], "M": wl.M, "K": wl.K, "N": wl.N,
+                      "num_adapters": wl.num_adapters},
+           "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=list(CONFIG_TEXT), default="decode")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        reference(args)
+    else:
+        ours(args)
+
+
+if __name__ == "__main__":
+    main()

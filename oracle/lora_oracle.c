@@ -227,3 +227,37 @@ void oracle_expand_rows(const float *S, int64_t s_cols, const uint16_t *y_in, in
         }
     }
 }
+
+/*
+ * Selected single elements y[rows[q], cols[q]] of the layer (same definition
+ * as oracle_lora_linear_rows, evaluated element by element; S is recomputed
+ * for every element).  Used for bounded samples of large workloads.
+ */
+void oracle_lora_linear_elems(const uint16_t *x, int64_t K, const uint16_t *W, int64_t N,
+                              const uint16_t *bias, const int32_t *ids, int32_t num_adapters,
+                              const int32_t *rank, const uint16_t *a_cat, const uint16_t *b_cat,
+                              double scale, const int64_t *rows, const int64_t *cols, int64_t n,
+                              double *y)
+{
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t q = 0; q < n; ++q) {
+        int64_t t = rows[q], c = cols[q];
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k) acc += bf16_to_f64(x[t * K + k]) * bf16_to_f64(W[c * K + k]);
+        if (bias) acc += bf16_to_f64(bias[c]);
+        int32_t i = effective_id(ids[t], num_adapters);
+        if (i >= 0) {
+            int64_t r = rank[i];
+            const uint16_t *Ai = a_cat + a_start(rank, i, K);
+            const uint16_t *Bi = b_cat + b_start(rank, i, N);
+            double lora = 0.0;
+            for (int64_t j = 0; j < r; ++j) {
+                double s = 0.0;
+                for (int64_t k = 0; k < K; ++k) s += bf16_to_f64(x[t * K + k]) * bf16_to_f64(Ai[j * K + k]);
+                lora += s * bf16_to_f64(Bi[c * r + j]);
+            }
+            acc += scale * lora;
+        }
+        y[q] = acc;
+    }
+}

@@ -56,6 +56,8 @@ def _load():
                                                 p, i64, p]
         lib.oracle_shrink_rows.restype = None
         lib.oracle_shrink_rows.argtypes = [p, i64, i64, p, i32, p, p, p, i64, i64, p]
+        lib.oracle_lora_linear_elems.restype = None
+        lib.oracle_lora_linear_elems.argtypes = [p, i64, p, i64, p, p, i32, p, p, p, dbl, p, p, i64, p]
         lib.oracle_expand_rows.restype = None
         lib.oracle_expand_rows.argtypes = [p, i64, p, i64, p, i32, p, p, dbl, p, i64, p]
         _lib = lib
@@ -136,6 +138,46 @@ def lora_linear(wl, rows=None, scale: Optional[float] = None) -> np.ndarray:
     lib.oracle_lora_linear_rows(_ptr(x), wl.M, wl.K, _ptr(W), wl.N, _ptr(bias), _ptr(ids),
                                 len(wl.ranks), _ptr(rk), _ptr(a_cat), _ptr(b_cat), float(s),
                                 _ptr(r), nrows, _ptr(y))
+    return y
+
+
+class Prepared:
+    """Inputs of one workload marshalled once (bits + concatenated adapters),
+    so repeated oracle calls on samples do not re-marshal the whole workload."""
+
+    def __init__(self, wl):
+        self.wl = wl
+        self.x, self.W, self.bias = _bits(wl.x), _bits(wl.W), _bits(wl.bias)
+        self.ids = np.ascontiguousarray(wl.ids.numpy().astype(np.int32))
+        self.rk = np.ascontiguousarray(np.asarray(list(wl.ranks) or [0], dtype=np.int32))
+        self.a_cat, self.b_cat = _concat(wl.A, wl.K), _concat(wl.B, wl.N)
+
+
+def lora_linear_elems(prep: "Prepared", rows, cols, scale: Optional[float] = None) -> np.ndarray:
+    """fp64 y[rows[q], cols[q]] for q = 0..n-1 (element samples)."""
+    lib = _load()
+    wl = prep.wl
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    c = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+    assert r.shape == c.shape and r.ndim == 1
+    assert r.size == 0 or (r.min() >= 0 and r.max() < wl.M and c.min() >= 0 and c.max() < wl.N)
+    y = np.zeros(r.size, dtype=np.float64)
+    s = wl.scale if scale is None else scale
+    lib.oracle_lora_linear_elems(_ptr(prep.x), wl.K, _ptr(prep.W), wl.N, _ptr(prep.bias),
+                                 _ptr(prep.ids), len(wl.ranks), _ptr(prep.rk), _ptr(prep.a_cat),
+                                 _ptr(prep.b_cat), float(s), _ptr(r), _ptr(c), r.size, _ptr(y))
+    return y
+
+
+def lora_linear_rows_prepared(prep: "Prepared", rows) -> np.ndarray:
+    """Like lora_linear(wl, rows) but reusing marshalled inputs."""
+    lib = _load()
+    wl = prep.wl
+    r, nrows = _rows_arg(rows, wl.M)
+    y = np.zeros((nrows, wl.N), dtype=np.float64)
+    lib.oracle_lora_linear_rows(_ptr(prep.x), wl.M, wl.K, _ptr(prep.W), wl.N, _ptr(prep.bias),
+                                _ptr(prep.ids), len(wl.ranks), _ptr(prep.rk), _ptr(prep.a_cat),
+                                _ptr(prep.b_cat), float(wl.scale), _ptr(r), nrows, _ptr(y))
     return y
 
 

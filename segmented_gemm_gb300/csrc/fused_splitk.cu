@@ -9,20 +9,23 @@
 // At this size the layer is bound by streaming W (and the A/B panels of the
 // adapters present) from HBM once, so the MMA is swapped: the 128-row UMMA
 // operand is a weight tile and the tokens form the N side (16..128), which
-// keeps the tensor core's M dimension full.  Three lists of units, each unit
-// one 64-wide K block (or four 16-wide rank panels):
-//   L1 shrink : tile = 128 rows of the concatenated A panels of all adapters
-//               present;  D[a_row, t] += A_cat[a_row, k] x[t, k]
-//   L2 base   : tile = 128 output features;  D[n, t] += W[n, k] x[t, k]
-//   L3 expand : tile = 128 output features;  D[n, t] += B_cat[n, r] S[t, r]
-// Every CTA of the persistent grid takes an equal contiguous slice of L1,
-// then of L2, then of L3, so the shrink is finished grid-wide long before
-// any CTA reaches its expand units.  Each run of units that share a tile is
-// accumulated in TMEM and written as an fp32 partial; the CTA whose arrival
-// completes a tile's count sums the partials in a fixed order (deterministic
-// for any timing) and finishes it:
+// keeps the tensor core's M dimension full.  Units of work (one 64-wide K
+// block, or four 16-wide rank panels) come in two lists:
+//   shrink list : tile = 128 rows of the concatenated A panels of all adapters
+//                 present;  D[a_row, t] += A_cat[a_row, k] x[t, k]
+//   output list : tile = 128 output features; its units are the K blocks of
+//                 the base product  D[n, t] += W[n, k] x[t, k]  followed by
+//                 the expand steps  D[n, t] += B_cat[n, r] S[t, r]
+// Every CTA of the persistent grid takes an equal contiguous slice of the
+// shrink list, then of the output list, so the shrink is finished grid-wide
+// long before the expand steps need it; a run of a slice whose first unit is
+// an expand step is moved behind the CTA's other runs.  Each run (units of
+// one tile) is accumulated in TMEM and added with fp32 vector atomics into a
+// per-tile accumulator in L2; the CTA whose arrival completes the tile's
+// count reads it once and finishes it:
 //   shrink tile -> mask each token to its own adapter, * scale, bf16 S panels
 //   output tile -> + bias, bf16, y[t, n]
+// and zeroes the accumulator and counter for the next call.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -32,20 +35,17 @@
 namespace lora {
 
 constexpr int kSkThreads = 192;
-constexpr int kSkASlot = kSplitBN * kBK * 2;   // 16 KB: W / A_cat K-block or 4 B panels
-constexpr int kSkAPanel = kChunk * kBK * 2;    // 2 KB: 16 rows of A x 64
+constexpr int kSkASlot = kSplitBN * kBK * 2;       // 16 KB: W / A_cat K-block or 4 B panels
+constexpr int kSkAPanel = kChunk * kBK * 2;        // 2 KB: 16 rows of A x 64
 constexpr int kSkBPanel = kSplitBN * kChunk * 2;   // 4 KB: 128 rows of B x 16
+constexpr int kMaxRuns = 64;
 
 struct ListGeo {
     int64_t U;   // units
     int TL;      // units per tile
-    int tiles;
 };
 
-__device__ __forceinline__ int64_t slice_begin(const ListGeo &g, int c, int G)
-{
-    return (g.U * c) / G;
-}
+__device__ __forceinline__ int64_t slice_begin(const ListGeo &g, int c, int G) { return (g.U * c) / G; }
 
 // CTA whose slice holds unit u (slices are monotone; empty ones are skipped).
 __device__ __forceinline__ int owner_of(const ListGeo &g, int64_t u, int G)
@@ -53,32 +53,7 @@ __device__ __forceinline__ int owner_of(const ListGeo &g, int64_t u, int G)
     return static_cast<int>(((u + 1) * G - 1) / g.U);
 }
 
-__device__ __forceinline__ int64_t slot_of(const ListGeo &g, int list_base, int R, int c, int tile, int G)
-{
-    const int first_tile = static_cast<int>(slice_begin(g, c, G) / g.TL);
-    return static_cast<int64_t>(list_base) + static_cast<int64_t>(c) * R + (tile - first_tile);
-}
-
-struct Geos {
-    ListGeo l[3];
-    int D;       // chunks (16-row A panels / 16-col B panels) of adapters present
-    int RT;      // shrink tiles
-};
-
-__device__ __forceinline__ Geos make_geos(const SplitParams &p)
-{
-    Geos g;
-    g.D = p.hdr[HDR_DCHUNKS];
-    g.RT = (g.D + 7) / 8;
-    const int EU = (g.D + 3) / 4;
-    g.l[0] = {static_cast<int64_t>(g.RT) * p.kblocks, p.kblocks, g.RT};
-    g.l[1] = {static_cast<int64_t>(p.NT) * p.kblocks, p.kblocks, p.NT};
-    g.l[2] = {static_cast<int64_t>(p.NT) * EU, EU > 0 ? EU : 1, EU > 0 ? p.NT : 0};
-    if (EU == 0) g.l[2].U = 0;
-    return g;
-}
-
-// Number of CTAs with a non-empty slice intersecting `tile` of list g.
+// Number of CTAs with a non-empty slice intersecting `tile`.
 __device__ __forceinline__ int contributors(const ListGeo &g, int tile, int G)
 {
     if (g.U == 0) return 0;
@@ -90,10 +65,18 @@ __device__ __forceinline__ int contributors(const ListGeo &g, int tile, int G)
     return n;
 }
 
+struct Run {
+    int list;       // 0 shrink, 1 output
+    int tile;
+    int u0, u1;     // unit range inside the tile: [u0, u1)
+};
+
 __global__ void __launch_bounds__(kSkThreads, 1)
     lora_splitk_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                        const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                       const __grid_constant__ CUtensorMap tm_s, const SplitParams p)
+                       const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_a32,
+                       const __grid_constant__ CUtensorMap tm_a48, const __grid_constant__ CUtensorMap tm_a64,
+                       const SplitParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -105,10 +88,18 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *bcast = const_cast<int *>(abort_flag) + 1;
+    int *n_runs = bcast + 1;
+    Run *runs = reinterpret_cast<Run *>(n_runs + 3);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, cta = blockIdx.x;
     int32_t *status = p.counters + CNT_STATUS;
+
+    const int D = p.hdr[HDR_DCHUNKS];               // rank panels of the adapters present
+    const int RT = (D + 7) / 8;                     // shrink tiles (8 panels = 128 rows)
+    const int EU = (D + 3) / 4;                     // expand units per output tile
+    const ListGeo g_shr = {static_cast<int64_t>(RT) * p.kblocks, p.kblocks};
+    const ListGeo g_out = {static_cast<int64_t>(p.NT) * (p.kblocks + EU), p.kblocks + EU};
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -121,11 +112,36 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         }
         *abort_flag = 0;
         fence_mbarrier_init();
+        // this CTA's runs: shrink slice, then output slice
+        int n = 0;
+        const ListGeo *gs[2] = {&g_shr, &g_out};
+        int first_out = -1;
+        for (int L = 0; L < 2; ++L) {
+            const ListGeo &g = *gs[L];
+            if (g.U == 0) continue;
+            const int64_t u1 = slice_begin(g, cta + 1, G);
+            for (int64_t u = slice_begin(g, cta, G); u < u1 && n < kMaxRuns;) {
+                const int tile = static_cast<int>(u / g.TL);
+                const int64_t e = min(u1, static_cast<int64_t>(tile + 1) * g.TL);
+                if (L == 1 && first_out < 0) first_out = n;
+                runs[n++] = {L, tile, static_cast<int>(u - static_cast<int64_t>(tile) * g.TL),
+                             static_cast<int>(e - static_cast<int64_t>(tile) * g.TL)};
+                u = e;
+            }
+        }
+        // an output run that starts with expand steps goes last
+        if (first_out >= 0 && n - first_out > 1 && runs[first_out].u0 >= p.kblocks) {
+            const Run r = runs[first_out];
+            for (int i = first_out; i < n - 1; ++i) runs[i] = runs[i + 1];
+            runs[n - 1] = r;
+        }
+        *n_runs = n;
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tm_x);
         tma_prefetch_map(&tm_w);
         tma_prefetch_map(&tm_a);
+        tma_prefetch_map(&tm_a64);
         tma_prefetch_map(&tm_b);
         tma_prefetch_map(&tm_s);
     }
@@ -137,52 +153,57 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const Geos geo = make_geos(p);
-    const int list_base[3] = {0, G * p.R1, G * (p.R1 + p.R2)};
-    const int list_R[3] = {p.R1, p.R2, p.R3};
+    const int nr = *n_runs;
 
     if (warp == 0) {
         // ===================== TMA producer ==================================
         uint32_t it = 0;
-        for (int L = 0; L < 3; ++L) {
-            const ListGeo &g = geo.l[L];
-            if (g.U == 0) continue;
-            const int64_t u0 = slice_begin(g, cta, G), u1 = slice_begin(g, cta + 1, G);
-            if (L == 2 && u1 > u0) {
-                if (lane == 0) {
-                    wait_flag_geq(p.counters + CNT_SPLIT_SREADY, geo.RT, abort_flag, status, LORA_DEV_TIMEOUT);
-                    fence_proxy_async_global();
+        bool s_ready = false;
+        for (int ri = 0; ri < nr; ++ri) {
+            const Run r = runs[ri];
+            for (int k = r.u0; k < r.u1; ++k, ++it) {
+                const bool expand = r.list == 1 && k >= p.kblocks;
+                if (expand && !s_ready) {
+                    if (lane == 0) {
+                        wait_flag_geq(p.counters + CNT_SPLIT_SREADY, RT, abort_flag, status, LORA_DEV_TIMEOUT);
+                        fence_proxy_async_global();
+                    }
+                    __syncwarp();
+                    s_ready = true;
                 }
-                __syncwarp();
-            }
-            for (int64_t u = u0; u < u1; ++u, ++it) {
-                const int tile = static_cast<int>(u / g.TL), k = static_cast<int>(u % g.TL);
                 const int s = it % p.stages;
                 const uint32_t round = it / p.stages;
                 if (lane == 0 && round > 0) mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
                 __syncwarp();
                 uint8_t *as = smem + s * stage_bytes;
                 uint8_t *bs = as + kSkASlot;
-                if (L == 0) {
-                    const int g0 = tile * 8, nch = min(8, geo.D - g0);
+                if (r.list == 0) {
+                    const int g0 = r.tile * 8, g1 = min(g0 + 8, D);
                     if (lane == 0) {
-                        mbar_expect_tx(&full[s], nch * kSkAPanel + p.T_pad * kBK * 2);
+                        mbar_expect_tx(&full[s], (g1 - g0) * kSkAPanel + p.T_pad * kBK * 2);
                         tma_load_2d(bs, &tm_x, &full[s], k * kBK, 0);
+                        // consecutive panels of one adapter: one box of 16..64 rows
+                        for (int g = g0; g < g1;) {
+                            const int r0 = p.dchunk_arow[g];
+                            int len = 1;
+                            while (len < 4 && g + len < g1 && p.dchunk_arow[g + len] == r0 + kChunk * len) ++len;
+                            const CUtensorMap *m = len == 1 ? &tm_a : len == 2 ? &tm_a32 : len == 3 ? &tm_a48 : &tm_a64;
+                            tma_load_2d(as + (g - g0) * kSkAPanel, m, &full[s], k * kBK, r0);
+                            g += len;
+                        }
                     }
-                    __syncwarp();
-                    if (lane < nch) tma_load_2d(as + lane * kSkAPanel, &tm_a, &full[s], k * kBK, p.dchunk_arow[g0 + lane]);
-                } else if (L == 1) {
+                } else if (!expand) {
                     if (lane == 0) {
                         mbar_expect_tx(&full[s], kSkASlot + p.T_pad * kBK * 2);
-                        tma_load_2d(as, &tm_w, &full[s], k * kBK, tile * kSplitBN);
+                        tma_load_2d(as, &tm_w, &full[s], k * kBK, r.tile * kSplitBN);
                         tma_load_2d(bs, &tm_x, &full[s], k * kBK, 0);
                     }
                 } else {
-                    const int g0 = k * 4, nch = min(4, geo.D - g0);
+                    const int g0 = (k - p.kblocks) * 4, nch = min(4, D - g0);
                     if (lane == 0) mbar_expect_tx(&full[s], nch * (kSkBPanel + p.T_pad * kChunk * 2));
                     __syncwarp();
                     if (lane < nch) {
-                        tma_load_2d(as + lane * kSkBPanel, &tm_b, &full[s], 0, p.dchunk_brow[g0 + lane] + tile * kSplitBN);
+                        tma_load_2d(as + lane * kSkBPanel, &tm_b, &full[s], 0, p.dchunk_brow[g0 + lane] + r.tile * kSplitBN);
                         tma_load_2d(bs + lane * p.T_pad * kChunk * 2, &tm_s, &full[s], 0, (g0 + lane) * p.T_pad);
                     }
                 }
@@ -191,167 +212,128 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         }
     } else if (warp == 1) {
         // ===================== MMA issuer ====================================
-        uint32_t it = 0, q = 0;
+        uint32_t it = 0;
         const uint32_t idesc = umma_idesc_bf16(kSplitBN, p.T_pad);
-        for (int L = 0; L < 3; ++L) {
-            const ListGeo &g = geo.l[L];
-            if (g.U == 0) continue;
-            const int64_t u0 = slice_begin(g, cta, G), u1 = slice_begin(g, cta + 1, G);
-            int64_t u = u0;
-            while (u < u1) {
-                const int tile = static_cast<int>(u / g.TL);
-                const int64_t run_end = min(u1, static_cast<int64_t>(tile + 1) * g.TL);
-                const uint32_t slot = q & 1, use = q >> 1;
-                if (use > 0) mbar_wait(&acc_empty[slot], (use - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+        for (int ri = 0; ri < nr; ++ri) {
+            const Run r = runs[ri];
+            const uint32_t slot = ri & 1, use = ri >> 1;
+            if (use > 0) mbar_wait(&acc_empty[slot], (use - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+            tc_fence_after();
+            const uint32_t d = tmem_base + slot * p.T_pad;
+            uint32_t acc = 0;
+            for (int k = r.u0; k < r.u1; ++k, ++it) {
+                const bool expand = r.list == 1 && k >= p.kblocks;
+                const int s = it % p.stages;
+                mbar_wait(&full[s], (it / p.stages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
                 tc_fence_after();
-                const uint32_t d = tmem_base + slot * p.T_pad;
-                uint32_t acc = 0;
-                for (; u < run_end; ++u, ++it) {
-                    const int k = static_cast<int>(u % g.TL);
-                    const int s = it % p.stages;
-                    mbar_wait(&full[s], (it / p.stages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t aa = smem_u32(smem + s * stage_bytes);
-                        const uint32_t ba = aa + kSkASlot;
-                        if (L < 2) {
+                if (lane == 0) {
+                    const uint32_t aa = smem_u32(smem + s * stage_bytes);
+                    const uint32_t ba = aa + kSkASlot;
+                    if (!expand) {
 #pragma unroll
-                            for (int kk = 0; kk < kBK / 16; ++kk) {
-                                umma_bf16(d, umma_sdesc(aa + kk * 32, 1024, kSwizzle128),
-                                          umma_sdesc(ba + kk * 32, 1024, kSwizzle128), idesc, acc);
-                                acc = 1;
-                            }
-                        } else {
-                            const int nch = min(4, geo.D - k * 4);
-                            for (int i = 0; i < nch; ++i) {
-                                umma_bf16(d, umma_sdesc(aa + i * kSkBPanel, 256, kSwizzle32),
-                                          umma_sdesc(ba + i * p.T_pad * kChunk * 2, 256, kSwizzle32), idesc, acc);
-                                acc = 1;
-                            }
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            umma_bf16(d, umma_sdesc(aa + kk * 32, 1024, kSwizzle128),
+                                      umma_sdesc(ba + kk * 32, 1024, kSwizzle128), idesc, acc);
+                            acc = 1;
                         }
-                        umma_commit(&empty[s]);
+                    } else {
+                        const int nch = min(4, D - (k - p.kblocks) * 4);
+                        for (int i = 0; i < nch; ++i) {
+                            umma_bf16(d, umma_sdesc(aa + i * kSkBPanel, 256, kSwizzle32),
+                                      umma_sdesc(ba + i * p.T_pad * kChunk * 2, 256, kSwizzle32), idesc, acc);
+                            acc = 1;
+                        }
                     }
-                    __syncwarp();
+                    umma_commit(&empty[s]);
                 }
-                if (lane == 0) umma_commit(&acc_full[slot]);
                 __syncwarp();
-                ++q;
             }
+            if (lane == 0) umma_commit(&acc_full[slot]);
+            __syncwarp();
         }
     } else {
-        // ===================== epilogue: partials + reductions ===============
+        // ===================== epilogue: accumulate, finish tiles =============
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int et = threadIdx.x - 64;
         const int T = p.T_pad;
-        uint32_t q = 0;
-        for (int L = 0; L < 3; ++L) {
-            const ListGeo &g = geo.l[L];
-            if (g.U == 0) continue;
-            const int64_t u0 = slice_begin(g, cta, G), u1 = slice_begin(g, cta + 1, G);
-            int64_t u = u0;
-            while (u < u1) {
-                const int tile = static_cast<int>(u / g.TL);
-                u = min(u1, static_cast<int64_t>(tile + 1) * g.TL);
-                const uint32_t slot = q & 1, use = q >> 1;
-                ++q;
-                mbar_wait(&acc_full[slot], use & 1, abort_flag, status, LORA_DEV_TIMEOUT);
-                tc_fence_after();
-                const uint32_t tbase = tmem_base + slot * T + (static_cast<uint32_t>(quad * 32) << 16);
-                float *mine = p.partials + slot_of(g, list_base[L], list_R[L], cta, tile, G) * (kSplitBN * T) +
-                              static_cast<int64_t>(row) * T;
-                for (int c = 0; c < T; c += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(tbase + c, r);
-                    tmem_ld_wait16(r);
-                    float4 *dst = reinterpret_cast<float4 *>(mine + c);
+        for (int ri = 0; ri < nr; ++ri) {
+            const Run r = runs[ri];
+            const uint32_t slot = ri & 1, use = ri >> 1;
+            mbar_wait(&acc_full[slot], use & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + slot * T + (static_cast<uint32_t>(quad * 32) << 16);
+            const bool is_out = r.list == 1;
+            float *accum = (is_out ? p.acc_out : p.acc_shr) + (static_cast<int64_t>(r.tile) * kSplitBN + row) * T;
+            for (int c = 0; c < T; c += 16) {
+                uint32_t v[16];
+                tmem_ld16(tbase + c, v);
+                tmem_ld_wait16(v);
+                float4 *dst = reinterpret_cast<float4 *>(accum + c);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                             __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                for (int q = 0; q < 4; ++q)
+                    atomicAdd(dst + q, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                   __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
+            }
+            tc_fence_before();
+            mbar_arrive(&acc_empty[slot]);
+            __threadfence();
+            named_bar_sync(1, 128);
+            int32_t *cnt = p.counters + CNT_FIXED + (is_out ? r.tile : p.NT + r.tile);
+            if (et == 0) {
+                const int expect = contributors(is_out ? g_out : g_shr, r.tile, G);
+                *bcast = (atom_acq_rel_gpu_add(cnt, 1) == expect - 1);
+            }
+            named_bar_sync(1, 128);
+            if (!*bcast) continue;
+            __threadfence();
+            // ---- last arrival: the tile's sum is complete in `accum` ----------
+            const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c = 0; c < T; c += 16) {
+                float a[16];
+                float4 *src = reinterpret_cast<float4 *>(accum + c);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 f = __ldcg(src + q);
+                    a[4 * q] = f.x;
+                    a[4 * q + 1] = f.y;
+                    a[4 * q + 2] = f.z;
+                    a[4 * q + 3] = f.w;
+                    __stcg(src + q, zero4);
                 }
-                tc_fence_before();
-                mbar_arrive(&acc_empty[slot]);
-                __threadfence();
-                named_bar_sync(1, 128);
-                const bool is_out = (L != 0);
-                int32_t *cnt = p.counters + CNT_FIXED + (is_out ? tile : p.NT + tile);
-                if (et == 0) {
-                    const int expect = is_out ? contributors(geo.l[1], tile, G) + contributors(geo.l[2], tile, G)
-                                              : contributors(geo.l[0], tile, G);
-                    *bcast = (atom_acq_rel_gpu_add(cnt, 1) == expect - 1);
-                }
-                named_bar_sync(1, 128);
-                if (!*bcast) continue;
-                __threadfence();
-                // ---- this CTA completes the tile: fixed-order sum of partials
-                const int lists[2] = {is_out ? 1 : 0, is_out ? 2 : -1};
-                for (int c = 0; c < T; c += 16) {
-                    float acc16[16];
+                if (is_out) {
+                    const int n = r.tile * kSplitBN + row;
+                    if (n < p.N) {
+                        const float b = p.bias ? __uint_as_float(static_cast<uint32_t>(p.bias[n]) << 16) : 0.f;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) acc16[e] = 0.f;
-                    for (int li = 0; li < 2; ++li) {
-                        const int LL = lists[li];
-                        if (LL < 0) continue;
-                        const ListGeo &gg = geo.l[LL];
-                        if (gg.U == 0) continue;
-                        const int64_t a = static_cast<int64_t>(tile) * gg.TL;
-                        const int cfirst = owner_of(gg, a, G), clast = owner_of(gg, a + gg.TL - 1, G);
-                        for (int cc = cfirst; cc <= clast; ++cc) {
-                            if (slice_begin(gg, cc + 1, G) <= slice_begin(gg, cc, G)) continue;
-                            const float4 *src = reinterpret_cast<const float4 *>(
-                                p.partials + slot_of(gg, list_base[LL], list_R[LL], cc, tile, G) * (kSplitBN * T) +
-                                static_cast<int64_t>(row) * T + c);
-#pragma unroll
-                            for (int v = 0; v < 4; ++v) {
-                                const float4 f = __ldcg(src + v);
-                                acc16[4 * v] += f.x;
-                                acc16[4 * v + 1] += f.y;
-                                acc16[4 * v + 2] += f.z;
-                                acc16[4 * v + 3] += f.w;
-                            }
+                        for (int e = 0; e < 16; ++e) {
+                            const int t = c + e;
+                            if (t < p.M)
+                                p.y[static_cast<int64_t>(t) * p.N + n] =
+                                    static_cast<uint16_t>(pack_bf16x2(a[e] + b, 0.f) & 0xFFFF);
                         }
                     }
-                    if (is_out) {
-                        const int n = tile * kSplitBN + row;
-                        if (n < p.N) {
-                            const float b = p.bias ? __uint_as_float(static_cast<uint32_t>(p.bias[n]) << 16) : 0.f;
-                            for (int e = 0; e < 16; ++e) {
-                                const int t = c + e;
-                                if (t < p.M) {
-                                    const uint32_t h = pack_bf16x2(acc16[e] + b, 0.f);
-                                    p.y[static_cast<int64_t>(t) * p.N + n] = static_cast<uint16_t>(h & 0xFFFF);
-                                }
-                            }
-                        }
-                    } else {
-                        const int arow = tile * kSplitBN + row;
-                        const int gch = arow / kChunk;
-                        if (gch < geo.D) {
-                            const int adapter = p.dchunk_adapter[gch];
-                            uint16_t *dst = p.s_panels + (static_cast<int64_t>(gch) * T) * kChunk + (arow % kChunk);
-                            for (int e = 0; e < 16; ++e) {
-                                const int t = c + e;
-                                float v = 0.f;
-                                if (t < p.M) {
-                                    const int id = p.ids[t];
-                                    if (id == adapter) v = acc16[e] * p.scale;
-                                }
-                                const uint32_t h = pack_bf16x2(v, 0.f);
-                                dst[static_cast<int64_t>(t) * kChunk] = static_cast<uint16_t>(h & 0xFFFF);
-                            }
+                } else {
+                    const int arow = r.tile * kSplitBN + row;
+                    const int gch = arow / kChunk;
+                    if (gch < D) {
+                        const int adapter = p.dchunk_adapter[gch];
+                        uint16_t *dst = p.s_panels + static_cast<int64_t>(gch) * T * kChunk + (arow % kChunk);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int t = c + e;
+                            const float v = (t < p.M && p.ids[t] == adapter) ? a[e] * p.scale : 0.f;
+                            dst[static_cast<int64_t>(t) * kChunk] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFF);
                         }
                     }
                 }
-                if (!is_out) {
-                    fence_proxy_async_global();
-                    __threadfence();
-                }
-                named_bar_sync(1, 128);
-                if (et == 0) {
-                    *cnt = 0;
-                    if (!is_out) red_release_gpu_add(p.counters + CNT_SPLIT_SREADY, 1);
-                }
+            }
+            if (!is_out) fence_proxy_async_global();
+            __threadfence();
+            named_bar_sync(1, 128);
+            if (et == 0) {
+                *cnt = 0;
+                if (!is_out) red_release_gpu_add(p.counters + CNT_SPLIT_SREADY, 1);
             }
         }
     }
@@ -372,7 +354,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 
 size_t splitk_smem_bytes(int T_pad, int stages)
 {
-    return static_cast<size_t>(stages) * (kSkASlot + T_pad * kBK * 2) + 1024 + 256;
+    return static_cast<size_t>(stages) * (kSkASlot + T_pad * kBK * 2) + 1024 + 256 + kMaxRuns * sizeof(Run);
 }
 
 int splitk_stages(int T_pad)
@@ -382,19 +364,22 @@ int splitk_stages(int T_pad)
     return s > 12 ? 12 : s;
 }
 
+int splitk_max_runs() { return kMaxRuns; }
+
 cudaError_t launch_splitk(const TcMaps &maps, const SplitParams &p, int grid, cudaStream_t stream)
 {
     static int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     const size_t smem = splitk_smem_bytes(p.T_pad, p.stages);
-    if (dev < 64 && !configured[dev]) {
+    if (dev >= 64 || !configured[dev]) {
         cudaError_t e = cudaFuncSetAttribute(lora_splitk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              220 * 1024);
         if (e != cudaSuccess) return e;
-        configured[dev] = 1;
+        if (dev < 64) configured[dev] = 1;
     }
-    lora_splitk_kernel<<<grid, kSkThreads, smem, stream>>>(maps.x, maps.w, maps.a, maps.b, maps.s, p);
+    lora_splitk_kernel<<<grid, kSkThreads, smem, stream>>>(maps.x, maps.w, maps.a, maps.b, maps.s, maps.a32, maps.a48,
+                                                           maps.a64, p);
     return cudaGetLastError();
 }
 

@@ -20,10 +20,14 @@
 // bounded).
 //
 // Roles inside a CTA (192 threads):
-//   warp 0      TMA producer: x rows by tile::gather4 (4 permuted rows per
-//               instruction), W / A / B / S boxes by 2-D tiled loads
+//   warp 0      TMA producer: W / A / B / S boxes by 2-D tiled loads
 //   warp 1      TMEM allocator and MMA issuer (one thread)
 //   warps 2..5  epilogue: tcgen05.ld -> registers -> global
+//   warps 6..9  x loaders: the tile's permuted token rows, 16 bytes per
+//               thread by cp.async into the swizzled layout (a row gather
+//               costs one LSU request per 16 bytes instead of one TMA
+//               instruction per four rows, which the TMA unit issues too
+//               slowly to feed the tensor core)
 // Smem: 4 stages x (16 KB x-slot + 32 KB w-slot), 128-byte swizzle for the
 // K-blocks of 64, 32-byte swizzle for the 16-wide rank panels.  TMEM: two
 // 256-column fp32 accumulators so the epilogue of job j overlaps the
@@ -36,18 +40,18 @@
 
 namespace lora {
 
-constexpr int kStages = 4;
+constexpr int kXStages = 6;                   // x ring (cp.async row gathers)
+constexpr int kWStages = 4;                   // W ring (TMA: W, A panels, S / B panels)
 constexpr int kXSlot = kBM * kBK * 2;         // 16 KB
 constexpr int kWSlot = kBN * kBK * 2;         // 32 KB
-constexpr int kStageBytes = kXSlot + kWSlot;
 constexpr int kSPanelBytes = kBM * kChunk * 2;   // 4 KB  (128 rows x 16)
 constexpr int kBPanelBytes = kBN * kChunk * 2;   // 8 KB  (256 rows x 16)
 constexpr int kAPanelBytes = kChunk * kBK * 2;   // 2 KB  (16 rows x 64)
-constexpr int kPanelsPerStage = 4;
-constexpr int kTcThreads = 192;
+constexpr int kPanelsPerStage = 2;               // expand step: 2 x (S 4 KB + B 8 KB) in one W slot
+constexpr int kTcThreads = 320;   // 10 warps: TMA, MMA, 4 epilogue, 4 x loaders
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 256;
-constexpr size_t kTcSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr size_t kTcSmemBytes = kXStages * kXSlot + kWStages * kWSlot + 1024 /*align*/ + 256 /*barriers*/;
 
 struct Job {
     int kind;   // 0 shrink, 1 output
@@ -81,13 +85,19 @@ __device__ __forceinline__ Job decode_job(int j, int n_sjobs, const TcParams &p)
 __global__ void __launch_bounds__(kTcThreads, 1)
     lora_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                    const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   const __grid_constant__ CUtensorMap tm_s, const TcParams p)
+                   const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_a32,
+                   const __grid_constant__ CUtensorMap tm_a48, const __grid_constant__ CUtensorMap tm_a64,
+                   const TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
-    uint64_t *empty = full + kStages;
-    uint64_t *acc_full = empty + kStages;
+    uint8_t *xring = smem;                                  // kXStages x 16 KB
+    uint8_t *wring = smem + kXStages * kXSlot;              // kWStages x 32 KB
+    uint64_t *fullx = reinterpret_cast<uint64_t *>(wring + kWStages * kWSlot);
+    uint64_t *emptyx = fullx + kXStages;
+    uint64_t *fullw = emptyx + kXStages;
+    uint64_t *emptyw = fullw + kWStages;
+    uint64_t *acc_full = emptyw + kWStages;
     uint64_t *acc_empty = acc_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -97,9 +107,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int32_t *status = p.counters + CNT_STATUS;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < kXStages; ++s) {
+            mbar_init(&fullx[s], 128);    // one cp.async-completion arrive per loader thread
+            mbar_init(&emptyx[s], 1);
+        }
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(&fullw[s], 1);      // the producer's expect_tx arrive
+            mbar_init(&emptyw[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
@@ -109,7 +123,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_mbarrier_init();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&tm_x);
         tma_prefetch_map(&tm_w);
         tma_prefetch_map(&tm_a);
         tma_prefetch_map(&tm_b);
@@ -130,35 +143,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int kblocks = (p.mode == kModeExpand) ? 0 : p.kblocks;
 
     if (warp == 0) {
-        // ===================== TMA producer ==================================
-        uint32_t it = 0;
+        // ===================== TMA producer: W ring (W, A panels, S / B panels)
+        uint32_t iw = 0;
         for (int j = blockIdx.x; j < total; j += gridDim.x) {
             const Job jb = decode_job(j, n_sjobs, p);
-            int rows[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                int64_t pp = static_cast<int64_t>(jb.m) * kBM + 4 * lane + q;
-                if (pp >= p.M) pp = p.M - 1;
-                rows[q] = p.perm[pp];
-            }
-            for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                const int s = it % kStages;
-                const uint32_t round = it / kStages;
-                if (lane == 0 && round > 0) mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
-                __syncwarp();
-                uint8_t *xs = smem + s * kStageBytes;
-                uint8_t *wsl = xs + kXSlot;
-                const uint32_t bytes =
-                    kXSlot + (jb.kind == 0 ? (jb.c1 - jb.c0) * kAPanelBytes : kWSlot);
-                if (lane == 0) mbar_expect_tx(&full[s], bytes);
-                __syncwarp();
-                tma_gather4(xs + lane * 512, &tm_x, &full[s], kb * kBK, rows[0], rows[1], rows[2], rows[3]);
-                if (jb.kind == 1) {
-                    if (lane == 0) tma_load_2d(wsl, &tm_w, &full[s], kb * kBK, jb.n * kBN);
-                } else {
-                    for (int c = jb.c0 + lane; c < jb.c1; c += 32)
-                        tma_load_2d(wsl + (c - jb.c0) * kAPanelBytes, &tm_a, &full[s], kb * kBK, p.chunk_arow[c]);
+            for (int kb = 0; kb < kblocks; ++kb, ++iw) {
+                const int s = iw % kWStages;
+                const uint32_t round = iw / kWStages;
+                if (lane == 0) {
+                    if (round > 0) mbar_wait(&emptyw[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                    uint8_t *wsl = wring + s * kWSlot;
+                    if (jb.kind == 1) {
+                        mbar_expect_tx(&fullw[s], kWSlot);
+                        tma_load_2d(wsl, &tm_w, &fullw[s], kb * kBK, jb.n * kBN);
+                    } else {
+                        mbar_expect_tx(&fullw[s], (jb.c1 - jb.c0) * kAPanelBytes);
+                        // consecutive rank panels of one adapter are consecutive
+                        // pool rows: one box of 16..64 rows per run
+                        for (int c = jb.c0; c < jb.c1;) {
+                            const int r0 = p.chunk_arow[c];
+                            int len = 1;
+                            while (len < 4 && c + len < jb.c1 && p.chunk_arow[c + len] == r0 + kChunk * len) ++len;
+                            const CUtensorMap *m = len == 1 ? &tm_a : len == 2 ? &tm_a32 : len == 3 ? &tm_a48 : &tm_a64;
+                            tma_load_2d(wsl + (c - jb.c0) * kAPanelBytes, m, &fullw[s], kb * kBK, r0);
+                            c += len;
+                        }
+                    }
                 }
+                __syncwarp();
             }
             if (jb.kind == 1 && jb.c1 > jb.c0) {
                 if (p.mode == kModeLinear) {
@@ -169,27 +181,62 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     __syncwarp();
                 }
-                for (int cg = jb.c0; cg < jb.c1; cg += kPanelsPerStage, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t round = it / kStages;
-                    if (lane == 0 && round > 0) mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                for (int cg = jb.c0; cg < jb.c1; cg += kPanelsPerStage, ++iw) {
+                    const int s = iw % kWStages;
+                    const uint32_t round = iw / kWStages;
+                    if (lane == 0 && round > 0) mbar_wait(&emptyw[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
                     __syncwarp();
-                    uint8_t *xs = smem + s * kStageBytes;
-                    uint8_t *wsl = xs + kXSlot;
+                    uint8_t *wsl = wring + s * kWSlot;   // [S panels | B panels]
                     const int nc = min(kPanelsPerStage, jb.c1 - cg);
-                    if (lane == 0) mbar_expect_tx(&full[s], nc * (kSPanelBytes + kBPanelBytes));
+                    if (lane == 0) mbar_expect_tx(&fullw[s], nc * (kSPanelBytes + kBPanelBytes));
                     __syncwarp();
                     if (lane < nc) {
                         const int c = cg + lane;
-                        tma_load_2d(xs + lane * kSPanelBytes, &tm_s, &full[s], 0, c * kBM);
-                        tma_load_2d(wsl + lane * kBPanelBytes, &tm_b, &full[s], 0, p.chunk_brow[c] + jb.n * kBN);
+                        tma_load_2d(wsl + lane * kSPanelBytes, &tm_s, &fullw[s], 0, c * kBM);
+                        tma_load_2d(wsl + kPanelsPerStage * kSPanelBytes + lane * kBPanelBytes, &tm_b, &fullw[s], 0,
+                                    p.chunk_brow[c] + jb.n * kBN);
                     }
+                    __syncwarp();
                 }
             }
         }
+    } else if (warp >= 6) {
+        // ===================== x loaders: permuted-row gather (cp.async) =====
+        // Thread lt copies 16-byte chunk (lt % 8) of rows lt/8 + 16q, q < 8,
+        // into the 128-byte-swizzled x slot; a warp instruction covers four
+        // whole 128-byte row segments.  Completion is tracked by the hardware
+        // (cp.async.mbarrier.arrive.noinc), so all kXStages slots stay in
+        // flight; the MMA thread fences the generic-proxy writes for the
+        // tensor core's async-proxy reads after its wait.
+        const int lt = threadIdx.x - 192;
+        const int chunk = lt & 7, rb = lt >> 3;
+        const uint32_t swz = static_cast<uint32_t>((chunk ^ (rb & 7)) << 4);
+        uint32_t ix = 0;
+        for (int j = blockIdx.x; j < total && kblocks > 0; j += gridDim.x) {
+            const Job jb = decode_job(j, n_sjobs, p);
+            const uint16_t *src[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                int64_t pp = static_cast<int64_t>(jb.m) * kBM + rb + 16 * q;
+                if (pp >= p.M) pp = p.M - 1;
+                src[q] = p.x + static_cast<int64_t>(p.perm[pp]) * p.K + chunk * 8;
+            }
+            for (int kb = 0; kb < kblocks; ++kb, ++ix) {
+                const int s = ix % kXStages;
+                const uint32_t round = ix / kXStages;
+                if (lane == 0 && round > 0) mbar_wait(&emptyx[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                __syncwarp();
+                uint8_t *xs = xring + s * kXSlot + swz;
+                const uint32_t nbytes = (kb * kBK + chunk * 8 < p.K) ? 16u : 0u;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) cp_async16(xs + (rb + 16 * q) * 128, src[q] + kb * kBK, nbytes);
+                cp_async_mbar_arrive_noinc(&fullx[s]);
+            }
+        }
+        cp_async_wait_all();
     } else if (warp == 1) {
         // ===================== MMA issuer ====================================
-        uint32_t it = 0, q = 0;
+        uint32_t iw = 0, ix = 0, q = 0;
         for (int j = blockIdx.x; j < total; j += gridDim.x, ++q) {
             const Job jb = decode_job(j, n_sjobs, p);
             const uint32_t slot = q & 1, use = q >> 1;
@@ -199,39 +246,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int n_mma = jb.kind == 0 ? (jb.c1 - jb.c0) * kChunk : kBN;
             const uint32_t idesc = umma_idesc_bf16(kBM, n_mma);
             uint32_t acc = 0;
-            for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                const int s = it % kStages;
-                mbar_wait(&full[s], (it / kStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+            for (int kb = 0; kb < kblocks; ++kb, ++iw, ++ix) {
+                const int sw = iw % kWStages, sx = ix % kXStages;
+                mbar_wait(&fullx[sx], (ix / kXStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                mbar_wait(&fullw[sw], (iw / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                fence_proxy_async_smem();   // x arrived through the generic proxy (cp.async)
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t xa = smem_u32(smem + s * kStageBytes);
-                    const uint32_t wa = xa + kXSlot;
+                    const uint32_t xa = smem_u32(xring + sx * kXSlot);
+                    const uint32_t wa = smem_u32(wring + sw * kWSlot);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         umma_bf16(d, umma_sdesc(xa + kk * 32, 1024, kSwizzle128),
                                   umma_sdesc(wa + kk * 32, 1024, kSwizzle128), idesc, acc);
                         acc = 1;
                     }
-                    umma_commit(&empty[s]);
+                    umma_commit(&emptyx[sx]);
+                    umma_commit(&emptyw[sw]);
                 }
                 __syncwarp();
             }
             if (jb.kind == 1 && jb.c1 > jb.c0) {
                 const uint32_t idesc_e = umma_idesc_bf16(kBM, kBN);
-                for (int cg = jb.c0; cg < jb.c1; cg += kPanelsPerStage, ++it) {
-                    const int s = it % kStages;
-                    mbar_wait(&full[s], (it / kStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                for (int cg = jb.c0; cg < jb.c1; cg += kPanelsPerStage, ++iw) {
+                    const int sw = iw % kWStages;
+                    mbar_wait(&fullw[sw], (iw / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t xa = smem_u32(smem + s * kStageBytes);
-                        const uint32_t wa = xa + kXSlot;
+                        const uint32_t sa = smem_u32(wring + sw * kWSlot);
+                        const uint32_t ba = sa + kPanelsPerStage * kSPanelBytes;
                         const int nc = min(kPanelsPerStage, jb.c1 - cg);
                         for (int i = 0; i < nc; ++i) {
-                            umma_bf16(d, umma_sdesc(xa + i * kSPanelBytes, 256, kSwizzle32),
-                                      umma_sdesc(wa + i * kBPanelBytes, 256, kSwizzle32), idesc_e, acc);
+                            umma_bf16(d, umma_sdesc(sa + i * kSPanelBytes, 256, kSwizzle32),
+                                      umma_sdesc(ba + i * kBPanelBytes, 256, kSwizzle32), idesc_e, acc);
                             acc = 1;
                         }
-                        umma_commit(&empty[s]);
+                        umma_commit(&emptyw[sw]);
                     }
                     __syncwarp();
                 }
@@ -239,7 +289,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) umma_commit(&acc_full[slot]);
             __syncwarp();
         }
-    } else {
+    } else if (warp >= 2) {
         // ===================== epilogue (warps 2..5) =========================
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
@@ -411,7 +461,8 @@ cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cudaStrea
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
-    lora_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, stream>>>(maps.x, maps.w, maps.a, maps.b, maps.s, p);
+    lora_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, stream>>>(maps.x, maps.w, maps.a, maps.b, maps.s, maps.a32,
+                                                               maps.a48, maps.a64, p);
     return cudaGetLastError();
 }
 

@@ -9,7 +9,7 @@
 //   plan       header, per-tile chunk lists, shrink-job list, split-K chunk
 //              list                                        (kernel work lists)
 //   s_scratch  bf16 S panels (scaled, masked), [chunks][rows][16]
-//   partials   fp32 split-K partial tiles
+//   acc        fp32 split-K tile accumulators (zero at rest)
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -57,14 +57,13 @@ struct WsLayout {
     int32_t max_sjobs;        // shrink-job capacity
     int32_t max_dchunks;      // split-K chunk capacity
     int32_t split_tiles;      // split-K output + shrink tiles (counter slots)
-    int64_t split_slots;      // split-K partial slots
     size_t counters, n_counters;
     size_t perm, offsets, seg_id, seg_start, seg_len, seg_rank, num_segments;
     size_t hdr, tile_chunk_off, chunk_arow, chunk_brow, chunk_rng;
     size_t sjob_tile, sjob_c0, sjob_c1, tile_njobs;
     size_t dchunk_arow, dchunk_brow, dchunk_adapter;
     size_t s_scratch, s_scratch_bytes;
-    size_t partials, partials_bytes;
+    size_t acc_out, acc_out_bytes, acc_shr, acc_shr_bytes;
     size_t total;
 };
 
@@ -82,6 +81,7 @@ enum TcMode { kModeLinear = 0, kModeShrink = 1, kModeExpand = 2 };
 
 struct TcMaps {
     CUtensorMap x, w, a, b, s;
+    CUtensorMap a32, a48, a64;   // A pool with 32 / 48 / 64-row boxes (a: 16 rows)
 };
 
 struct TcParams {
@@ -89,6 +89,7 @@ struct TcParams {
     int32_t N, K, kblocks, num_mtiles, num_ntiles, group_m, mode, s_cols;
     float scale;
     const uint16_t *bias;      // bf16 [N] or null
+    const uint16_t *x;         // bf16 [M, K] (rows gathered by the loader warps)
     uint16_t *y;               // bf16 [M, N]
     uint16_t *s_panels;        // bf16 [chunks][128][16]
     float *s_out;              // fp32 [M, s_cols] (shrink mode)
@@ -100,13 +101,14 @@ struct TcParams {
 
 struct SplitParams {
     int64_t M;
-    int32_t N, K, T_pad, kblocks, NT, stages, tmem_cols, R1, R2, R3, A;
+    int32_t N, K, T_pad, kblocks, NT, stages, tmem_cols, A;
     float scale;
     const uint16_t *bias;
     uint16_t *y;
     const int32_t *ids, *hdr, *dchunk_arow, *dchunk_brow, *dchunk_adapter;
     uint16_t *s_panels;        // bf16 [chunks][T_pad][16]
-    float *partials;           // fp32 [slots][128][T_pad]
+    float *acc_out;            // fp32 [NT][128][T_pad], zero at rest
+    float *acc_shr;            // fp32 [shrink tiles][128][T_pad], zero at rest
     int32_t *counters;
 };
 
@@ -131,6 +133,7 @@ cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cudaStrea
 cudaError_t launch_s_prep(const float *S, int32_t s_cols, float scale, const TcParams &p, cudaStream_t stream);
 cudaError_t launch_splitk(const TcMaps &maps, const SplitParams &p, int grid, cudaStream_t stream);
 int splitk_stages(int T_pad);
+int splitk_max_runs();
 int num_sms_current_device();
 
 }  // namespace lora

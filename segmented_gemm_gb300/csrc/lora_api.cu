@@ -103,11 +103,9 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
     L.split_tiles = NT + RTmax;
     size_t split_s = 0;
     if (M <= kSplitMaxTokens) {
-        const int G = num_sms_current_device();
         const int T = split_tpad(M);
-        const int R1 = (RTmax + G - 1) / G + 3, R2 = (NT + G - 1) / G + 3, R3 = R2;
-        L.split_slots = static_cast<int64_t>(G) * (R1 + R2 + R3);
-        L.partials_bytes = static_cast<size_t>(L.split_slots) * kSplitBN * T * 4;
+        L.acc_out_bytes = static_cast<size_t>(NT) * kSplitBN * T * 4;
+        L.acc_shr_bytes = static_cast<size_t>(RTmax) * kSplitBN * T * 4;
         split_s = static_cast<size_t>(L.max_dchunks) * T * kChunk * 2;
     }
     L.n_counters = CNT_FIXED + std::max<size_t>(L.num_mtiles, L.split_tiles) + 8;
@@ -142,7 +140,8 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
     L.dchunk_adapter = take(static_cast<size_t>(L.max_dchunks) * 4);
     o = (o + 1023) & ~size_t(1023);
     L.s_scratch = take(L.s_scratch_bytes);
-    L.partials = take(std::max<size_t>(L.partials_bytes, 16));
+    L.acc_out = take(std::max<size_t>(L.acc_out_bytes, 16));
+    L.acc_shr = take(std::max<size_t>(L.acc_shr_bytes, 16));
     L.total = o;
     return L;
 }
@@ -280,11 +279,18 @@ static bool encode_pool_maps(TcMaps &m, const lora_pool_t *pool, const void *dum
     if (pool->num_adapters > 0) {
         if (!encode_2d(&m.a, pool->a_pool, K, pool->a_elems / K, K * 2, kBK, kChunk, CU_TENSOR_MAP_SWIZZLE_128B))
             return false;
+        if (!encode_2d(&m.a32, pool->a_pool, K, pool->a_elems / K, K * 2, kBK, 2 * kChunk, CU_TENSOR_MAP_SWIZZLE_128B))
+            return false;
+        if (!encode_2d(&m.a48, pool->a_pool, K, pool->a_elems / K, K * 2, kBK, 3 * kChunk, CU_TENSOR_MAP_SWIZZLE_128B))
+            return false;
+        if (!encode_2d(&m.a64, pool->a_pool, K, pool->a_elems / K, K * 2, kBK, 4 * kChunk, CU_TENSOR_MAP_SWIZZLE_128B))
+            return false;
         if (!encode_2d(&m.b, pool->b_pool, kChunk, pool->b_elems / kChunk, kChunk * 2, kChunk, b_rows_box,
                        CU_TENSOR_MAP_SWIZZLE_32B))
             return false;
     } else {
         if (!encode_2d(&m.a, dummy, K, 1, K * 2, kBK, kChunk, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
+        m.a32 = m.a48 = m.a64 = m.a;
         if (!encode_2d(&m.b, dummy, kChunk, 1, kChunk * 2, kChunk, b_rows_box, CU_TENSOR_MAP_SWIZZLE_32B))
             return false;
     }
@@ -300,6 +306,7 @@ static int run_tiled(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, cons
     p.mode = mode;
     p.scale = scale;
     p.bias = bias;
+    p.x = x;
     p.y = y;
     p.s_out = s_out;
     p.s_cols = s_cols;
@@ -344,10 +351,7 @@ static int run_splitk(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, con
     while (tc < 2 * T) tc <<= 1;
     p.tmem_cols = tc;
     const int RTmax = (L.max_dchunks + 7) / 8;
-    p.R1 = (RTmax + G - 1) / G + 3;
-    p.R2 = (p.NT + G - 1) / G + 3;
-    p.R3 = p.R2;
-    if (static_cast<int64_t>(G) * (p.R1 + p.R2 + p.R3) > L.split_slots) return LORA_ERR_WORKSPACE;
+    if ((RTmax + G - 1) / G + 2 + (p.NT + G - 1) / G + 2 > splitk_max_runs()) return LORA_ERR_SHAPE;
     p.A = pool->num_adapters;
     p.scale = scale;
     p.bias = bias;
@@ -358,7 +362,8 @@ static int run_splitk(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, con
     p.dchunk_brow = at<int32_t>(ws, L.dchunk_brow);
     p.dchunk_adapter = at<int32_t>(ws, L.dchunk_adapter);
     p.s_panels = at<uint16_t>(ws, L.s_scratch);
-    p.partials = at<float>(ws, L.partials);
+    p.acc_out = at<float>(ws, L.acc_out);
+    p.acc_shr = at<float>(ws, L.acc_shr);
     p.counters = at<int32_t>(ws, L.counters);
     const uint64_t K = pool->K, N = pool->N;
     TcMaps m;

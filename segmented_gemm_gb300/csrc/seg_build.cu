@@ -58,12 +58,21 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
     int *whist = sm;                 // [32][nb]
     int *bsum = whist + 32 * nb;     // [nb + 1]
     int *wsum = bsum + nb + 1;       // [32]
+    // the segment table and per-adapter pool rows, kept on chip for the
+    // per-tile loops below (A entries each)
+    int *s_id = wsum + 32, *s_start = s_id + p.A, *s_len = s_start + p.A, *s_rank = s_len + p.A;
+    int *s_arow = s_rank + p.A;      // a_offset / K
+    int *s_brow = s_arow + p.A;      // b_offset / 16
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     int32_t *status = p.counters + CNT_STATUS;
 
     for (int i = tid; i < p.n_counters; i += kSegThreads)
         if (i != CNT_STATUS) p.counters[i] = 0;
     for (int i = tid; i < 32 * nb; i += kSegThreads) whist[i] = 0;
+    for (int i = tid; i < p.A; i += kSegThreads) {
+        s_arow[i] = static_cast<int>(p.a_offset[i] / p.K);
+        s_brow[i] = static_cast<int>(p.b_offset[i] / kChunk);
+    }
     __syncthreads();
 
     const int64_t per = (p.M + 31) / 32;
@@ -141,10 +150,15 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
         const int ex = block_exclusive_scan(flag, wsum, &total);
         if (flag) {
             const int s = carry + ex;
+            const int rk = p.rank[i];
             p.seg_id[s] = i;
             p.seg_start[s] = bsum[i + 1];
             p.seg_len[s] = cnt;
-            p.seg_rank[s] = p.rank[i];
+            p.seg_rank[s] = rk;
+            s_id[s] = i;
+            s_start[s] = bsum[i + 1];
+            s_len[s] = cnt;
+            s_rank[s] = rk;
         }
         carry += total;
     }
@@ -159,15 +173,15 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
     carry = 0;
     for (int s0 = 0; s0 < nseg; s0 += kSegThreads) {
         const int s = s0 + tid;
-        const int nc = s < nseg ? p.seg_rank[s] / kChunk : 0;
+        const int nc = s < nseg ? s_rank[s] / kChunk : 0;
         int total;
         const int ex = block_exclusive_scan(nc, wsum, &total);
         if (s < nseg) {
-            const int i = p.seg_id[s];
+            const int i = s_id[s];
             const int c = carry + ex;
             for (int q = 0; q < nc; ++q) {
-                p.dchunk_arow[c + q] = static_cast<int32_t>(p.a_offset[i] / p.K) + kChunk * q;
-                p.dchunk_brow[c + q] = static_cast<int32_t>(p.b_offset[i] / kChunk) + q * p.N;
+                p.dchunk_arow[c + q] = s_arow[i] + kChunk * q;
+                p.dchunk_brow[c + q] = s_brow[i] + q * p.N;
                 p.dchunk_adapter[c + q] = i;
             }
         }
@@ -188,10 +202,10 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
             int L = 0, R = nseg;   // first segment whose end is past lo
             while (L < R) {
                 const int mid = (L + R) >> 1;
-                if (p.seg_start[mid] + p.seg_len[mid] > lo) R = mid; else L = mid + 1;
+                if (s_start[mid] + s_len[mid] > lo) R = mid; else L = mid + 1;
             }
             sfirst = L;
-            for (int s = sfirst; s < nseg && p.seg_start[s] < hi; ++s) nch += p.seg_rank[s] / kChunk;
+            for (int s = sfirst; s < nseg && s_start[s] < hi; ++s) nch += s_rank[s] / kChunk;
         }
         int totc, totj;
         const int exc = block_exclusive_scan(nch, wsum, &totc);
@@ -202,14 +216,14 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
             const int cfirst = c;
             p.tile_chunk_off[m] = c;
             p.tile_njobs[m] = nj;
-            for (int s = sfirst; s < nseg && p.seg_start[s] < hi; ++s) {
-                const int64_t s0 = p.seg_start[s], s1 = s0 + p.seg_len[s];
+            for (int s = sfirst; s < nseg && s_start[s] < hi; ++s) {
+                const int64_t s0 = s_start[s], s1 = s0 + s_len[s];
                 const int rlo = static_cast<int>((s0 > lo ? s0 : lo) - lo);
                 const int rhi = static_cast<int>((s1 < hi ? s1 : hi) - lo);
-                const int i = p.seg_id[s];
-                for (int q = 0; q < p.seg_rank[s] / kChunk; ++q, ++c) {
-                    p.chunk_arow[c] = static_cast<int32_t>(p.a_offset[i] / p.K) + kChunk * q;
-                    p.chunk_brow[c] = static_cast<int32_t>(p.b_offset[i] / kChunk) + q * p.N;
+                const int i = s_id[s];
+                for (int q = 0; q < s_rank[s] / kChunk; ++q, ++c) {
+                    p.chunk_arow[c] = s_arow[i] + kChunk * q;
+                    p.chunk_brow[c] = s_brow[i] + q * p.N;
                     p.chunk_rng[c] = pack_rng(rlo, rhi, q);
                 }
             }
@@ -231,7 +245,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
     }
 }
 
-size_t seg_build_smem_bytes(int32_t A) { return static_cast<size_t>(32 * (A + 1) + (A + 2) + 32) * 4; }
+size_t seg_build_smem_bytes(int32_t A) { return static_cast<size_t>(32 * (A + 1) + (A + 2) + 32 + 6 * A) * 4; }
 
 cudaError_t launch_seg_build(const SegParams &p, cudaStream_t stream)
 {

@@ -237,3 +237,23 @@ def test_config_generators_shapes():
     assert sum(wl.meta["request_lengths"]) == 1024 and len(wl.meta["request_lengths"]) == 16
     # seeded: same seed -> identical draw
     assert torch.equal(workloads.make_config("tiny").x, workloads.make_config("tiny").x)
+
+
+def test_element_samples_match_rows():
+    """Element sampling evaluates the same definition as the row routine,
+    pinned independently against a library GEMM on a mixed batch."""
+    wl = workloads.make_custom(21, 48, 40, [16, 8, 32], seed=41, id_mode="uniform", p_base=0.3)
+    prep = oracle.Prepared(wl)
+    rng = np.random.default_rng(0)
+    rows = rng.integers(0, wl.M, 60)
+    cols = rng.integers(0, wl.N, 60)
+    e = oracle.lora_linear_elems(prep, rows, cols)
+    x, W, b = f64(wl.x), f64(wl.W), f64(wl.bias)
+    for q, (t, c) in enumerate(zip(rows, cols)):
+        want = x[t] @ W[c] + b[c]
+        i = int(wl.ids[t])
+        if i >= 0:
+            want += wl.scale * (x[t] @ f64(wl.A[i]).T) @ f64(wl.B[i])[c]
+        assert abs(e[q] - want) <= 1e-11 * max(1.0, abs(want))
+    full = oracle.lora_linear_rows_prepared(prep, list(range(wl.M)))
+    assert np.allclose(e, full[rows, cols], rtol=1e-12, atol=1e-12)
