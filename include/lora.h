@@ -201,7 +201,8 @@ int lora_linear(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lor
 enum {
     LORA_PATH_AUTO = 0,
     LORA_PATH_TILED = 1,        /* token-tile x output-tile persistent schedule */
-    LORA_PATH_SPLITK = 2        /* weight-streaming split-K schedule, M <= 128 */
+    LORA_PATH_SPLITK = 2,       /* weight-streaming split-K schedule, M <= 128 */
+    LORA_PATH_STREAM = 3        /* weight-streaming cluster schedule, M <= 64, K % 64 == 0 */
 };
 
 /* lora_linear with an explicit schedule (for tests and tuning). */

@@ -30,6 +30,7 @@ constexpr int kMaxShrinkChunks = 16;   // chunks per shrink job -> N <= 256
 constexpr int kSplitMaxTokens = 128;   // largest M served by the split-K path
 constexpr int kSplitBN = 128;          // output features per tile (UMMA M)
 constexpr int kSplitMaxCtas = 1024;    // upper bound on the persistent grid
+constexpr int kStreamMaxTokens = 64;    // largest M served by the weight-streaming schedule
 
 // plan header entries
 enum PlanHdr {
@@ -37,6 +38,8 @@ enum PlanHdr {
     HDR_NSJOBS = 1,       // shrink jobs of the tiled schedule
     HDR_DCHUNKS = 2,      // chunks of the split-K schedule (adapters present)
     HDR_NSEG = 3,         // number of segments
+    HDR_DGROUPS = 4,      // stream schedule: groups of <= 2 panels of one adapter
+    HDR_NWIN = 5,         // stream schedule: 8-panel windows of the B pool holding present panels
     HDR_WORDS = 16
 };
 
@@ -46,6 +49,7 @@ enum Counters {
     CNT_CTAS_DONE = 1,    // tiled schedule: CTAs finished
     CNT_SPLIT_DONE = 2,   // split-K: CTAs finished
     CNT_SPLIT_SREADY = 3, // split-K: shrink row tiles reduced
+    CNT_EPOCH = 4,        // stream schedule: call parity of the double-buffered accumulators
     CNT_FIXED = 8         // first per-tile counter
 };
 
@@ -62,6 +66,10 @@ struct WsLayout {
     size_t hdr, tile_chunk_off, chunk_arow, chunk_brow, chunk_rng;
     size_t sjob_tile, sjob_c0, sjob_c1, tile_njobs;
     size_t dchunk_arow, dchunk_brow, dchunk_adapter;
+    size_t dgrp_first, dgrp_len, dseg_first, dgrp_arow, dgrp_adapter, dseg_group;
+    size_t ewin_first, pinfo, acc_str, acc_str_bytes, gcnt;
+    int32_t max_dgroups;      // stream-schedule shrink groups capacity
+    int32_t max_win;          // stream-schedule expand windows capacity
     size_t s_scratch, s_scratch_bytes;
     size_t acc_out, acc_out_bytes, acc_shr, acc_shr_bytes;
     size_t total;
@@ -112,6 +120,23 @@ struct SplitParams {
     int32_t *counters;
 };
 
+struct ClusterMaps {
+    CUtensorMap w3, a3_16, a3_32, b3;
+};
+
+struct ClusterParams {
+    int64_t M;
+    int32_t N, K, T_pad, C, NT, kblocks, stages, tmem_cols, max_regions, max_groups;
+    float scale;
+    const uint16_t *bias;
+    const uint16_t *x;         // bf16 [M, K] (read by the loader warps)
+    uint16_t *y;
+    const int32_t *ids, *hdr, *dgrp_arow, *dgrp_len, *dgrp_adapter, *ewin_first, *pinfo;
+    float *acc;                // fp32 [2][groups][T_pad][32]: per-epoch group sums of S
+    int32_t *gcnt;             // [2][groups]: per-epoch group arrival counts
+    int32_t *counters;
+};
+
 struct SegParams {
     const int32_t *ids;
     int64_t M;
@@ -123,6 +148,9 @@ struct SegParams {
     int32_t *hdr, *tile_chunk_off, *chunk_arow, *chunk_brow, *chunk_rng;
     int32_t *sjob_tile, *sjob_c0, *sjob_c1, *tile_njobs;
     int32_t *dchunk_arow, *dchunk_brow, *dchunk_adapter;
+    int32_t *dgrp_first, *dgrp_len, *dseg_first, *dgrp_arow, *dgrp_adapter, *dseg_group;
+    int32_t *ewin_first, *pinfo;
+    int32_t P;                 // panels in the B pool (b_elems / (16 N))
     int32_t *counters;
     int32_t n_counters;
 };
@@ -133,6 +161,11 @@ cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cudaStrea
 cudaError_t launch_s_prep(const float *S, int32_t s_cols, float scale, const TcParams &p, cudaStream_t stream);
 cudaError_t launch_splitk(const TcMaps &maps, const SplitParams &p, int grid, cudaStream_t stream);
 int splitk_stages(int T_pad);
+cudaError_t launch_cluster(const ClusterMaps &m, const ClusterParams &p, cudaStream_t stream);
+int cluster_pick_size(int NT, int T_pad, int sms);
+int cluster_stages(int T_pad);
+int cluster_max_regions();
+int cluster_win();
 int splitk_max_runs();
 int num_sms_current_device();
 

@@ -79,6 +79,21 @@ static bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map: dims {d0, d1, d2}, byte strides of dims 1 and 2.
+static bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+                      uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle sw)
+{
+    EncodeTiledFn fn = encoder();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d0, d1 < 1 ? 1 : d1, d2 < 1 ? 1 : d2};
+    cuuint64_t strides[2] = {s1, s2};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------------------
 // workspace layout
 // ---------------------------------------------------------------------------
@@ -100,12 +115,13 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
     L.max_dchunks = static_cast<int32_t>(4 * present + 4);
     const int NT = (N + kSplitBN - 1) / kSplitBN;
     const int RTmax = (L.max_dchunks + 7) / 8;
-    L.split_tiles = NT + RTmax;
+    L.split_tiles = NT + std::max<int>(RTmax, static_cast<int>(2 * present + 2));
     size_t split_s = 0;
     if (M <= kSplitMaxTokens) {
         const int T = split_tpad(M);
         L.acc_out_bytes = static_cast<size_t>(NT) * kSplitBN * T * 4;
-        L.acc_shr_bytes = static_cast<size_t>(RTmax) * kSplitBN * T * 4;
+        L.acc_shr_bytes = std::max<size_t>(static_cast<size_t>(RTmax) * kSplitBN,
+                                           static_cast<size_t>(2 * present + 2) * 32) * T * 4;
         split_s = static_cast<size_t>(L.max_dchunks) * T * kChunk * 2;
     }
     L.n_counters = CNT_FIXED + std::max<size_t>(L.num_mtiles, L.split_tiles) + 8;
@@ -138,6 +154,20 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
     L.dchunk_arow = take(static_cast<size_t>(L.max_dchunks) * 4);
     L.dchunk_brow = take(static_cast<size_t>(L.max_dchunks) * 4);
     L.dchunk_adapter = take(static_cast<size_t>(L.max_dchunks) * 4);
+    L.max_dgroups = static_cast<int32_t>(2 * present + 2);
+    L.dgrp_first = take(static_cast<size_t>(L.max_dgroups) * 4);
+    L.dgrp_len = take(static_cast<size_t>(L.max_dgroups) * 4);
+    L.dseg_first = take(static_cast<size_t>(std::max(A, 1)) * 4);
+    L.dgrp_arow = take(static_cast<size_t>(L.max_dgroups) * 4);
+    L.dgrp_adapter = take(static_cast<size_t>(L.max_dgroups) * 4);
+    L.dseg_group = take(static_cast<size_t>(std::max(A, 1)) * 4);
+    L.max_win = (4 * A + 7) / 8 + 1;
+    L.ewin_first = take(static_cast<size_t>(L.max_win) * 4);
+    L.pinfo = take(static_cast<size_t>(L.max_win) * 8 * 4);
+    L.gcnt = take(static_cast<size_t>(2 * L.max_dgroups) * 4);
+    L.acc_str_bytes = M <= kStreamMaxTokens
+                          ? static_cast<size_t>(2) * L.max_dgroups * split_tpad(M) * 32 * 4 : 16;
+    L.acc_str = take(L.acc_str_bytes);
     o = (o + 1023) & ~size_t(1023);
     L.s_scratch = take(L.s_scratch_bytes);
     L.acc_out = take(std::max<size_t>(L.acc_out_bytes, 16));
@@ -222,6 +252,15 @@ static int enqueue_segments(const int32_t *ids, int64_t M, const lora_pool_t *po
     p.dchunk_arow = at<int32_t>(ws, L.dchunk_arow);
     p.dchunk_brow = at<int32_t>(ws, L.dchunk_brow);
     p.dchunk_adapter = at<int32_t>(ws, L.dchunk_adapter);
+    p.dgrp_first = at<int32_t>(ws, L.dgrp_first);
+    p.dgrp_len = at<int32_t>(ws, L.dgrp_len);
+    p.dseg_first = at<int32_t>(ws, L.dseg_first);
+    p.dgrp_arow = at<int32_t>(ws, L.dgrp_arow);
+    p.dgrp_adapter = at<int32_t>(ws, L.dgrp_adapter);
+    p.dseg_group = at<int32_t>(ws, L.dseg_group);
+    p.ewin_first = at<int32_t>(ws, L.ewin_first);
+    p.pinfo = at<int32_t>(ws, L.pinfo);
+    p.P = pool->num_adapters ? static_cast<int32_t>(pool->b_elems / (static_cast<int64_t>(kChunk) * pool->N)) : 0;
     p.counters = at<int32_t>(ws, L.counters);
     p.n_counters = static_cast<int32_t>(L.n_counters);
     return launch_seg_build(p, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
@@ -377,6 +416,85 @@ static int run_splitk(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, con
     return launch_splitk(m, p, G, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
+// Weight-streaming schedule (M <= 64, K a multiple of 64): one cluster of C
+// CTAs per 128-feature output tile.  Returns -1 when this device / shape
+// cannot host it, so the caller falls back to split-K.
+static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
+                       const int32_t *ids, const lora_pool_t *pool, float scale, lora_bf16_t *y, void *ws,
+                       const WsLayout &L, cudaStream_t stream)
+{
+    if (M > kStreamMaxTokens || (pool->K % kBK) != 0) return -1;
+    const int T = split_tpad(M);
+    const int NT = (pool->N + kSplitBN - 1) / kSplitBN;
+    const int sms = num_sms_current_device();
+    // one cached choice of C per (device, NT, T)
+    struct Pick {
+        int dev, NT, T, C;
+    };
+    static Pick cache[32];
+    static int ncache = 0;
+    static std::mutex mu;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int C = -1;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        for (int i = 0; i < ncache; ++i)
+            if (cache[i].dev == dev && cache[i].NT == NT && cache[i].T == T) C = cache[i].C;
+        if (C < 0) {
+            C = cluster_pick_size(NT, T, sms);
+            cache[ncache % 32] = {dev, NT, T, C};
+            ncache = ncache < 32 ? ncache + 1 : 32;
+        }
+    }
+    if (C <= 0) return -1;
+    const int grid = C * NT;
+    const int max_regions = std::min(cluster_max_regions(), 512 / T);
+    // shrink runs of one CTA (each needs its own TMEM region) stay below the cap
+    if ((L.max_dgroups + grid - 1) / grid + 2 > max_regions - 1) return -1;
+    ClusterParams p;
+    std::memset(&p, 0, sizeof p);
+    p.M = M;
+    p.N = pool->N;
+    p.K = pool->K;
+    p.T_pad = T;
+    p.C = C;
+    p.NT = NT;
+    p.kblocks = pool->K / kBK;
+    p.stages = cluster_stages(T);
+    p.tmem_cols = 512;
+    p.max_regions = max_regions;
+    p.max_groups = L.max_dgroups;
+    p.scale = scale;
+    p.bias = bias;
+    p.x = x;
+    p.y = y;
+    p.ids = ids;
+    p.hdr = at<int32_t>(ws, L.hdr);
+    p.dgrp_arow = at<int32_t>(ws, L.dgrp_arow);
+    p.dgrp_len = at<int32_t>(ws, L.dgrp_len);
+    p.dgrp_adapter = at<int32_t>(ws, L.dgrp_adapter);
+    p.ewin_first = at<int32_t>(ws, L.ewin_first);
+    p.pinfo = at<int32_t>(ws, L.pinfo);
+    p.acc = at<float>(ws, L.acc_str);
+    p.gcnt = at<int32_t>(ws, L.gcnt);
+    p.counters = at<int32_t>(ws, L.counters);
+    const uint64_t K = pool->K, N = pool->N, KB = pool->K / kBK;
+    ClusterMaps m;
+    const CUtensorMapSwizzle s128 = CU_TENSOR_MAP_SWIZZLE_128B, s32 = CU_TENSOR_MAP_SWIZZLE_32B;
+    if (!encode_3d(&m.w3, W, kBK, N, KB, K * 2, kBK * 2, kBK, kSplitBN, 2, s128)) return LORA_ERR_CUDA;
+    const void *apool = pool->num_adapters ? static_cast<const void *>(pool->a_pool) : static_cast<const void *>(W);
+    const uint64_t arows = pool->num_adapters ? static_cast<uint64_t>(pool->a_elems / pool->K) : 1;
+    if (!encode_3d(&m.a3_16, apool, kBK, arows, KB, K * 2, kBK * 2, kBK, kChunk, 4, s128)) return LORA_ERR_CUDA;
+    if (!encode_3d(&m.a3_32, apool, kBK, arows, KB, K * 2, kBK * 2, kBK, 2 * kChunk, 4, s128)) return LORA_ERR_CUDA;
+    const void *bpool = pool->num_adapters ? static_cast<const void *>(pool->b_pool) : static_cast<const void *>(W);
+    const uint64_t panels =
+        pool->num_adapters ? static_cast<uint64_t>(pool->b_elems / (static_cast<int64_t>(kChunk) * N)) : 1;
+    if (!encode_3d(&m.b3, bpool, kChunk, N, panels, kChunk * 2, N * kChunk * 2, kChunk, kSplitBN, cluster_win(), s32))
+        return LORA_ERR_CUDA;
+    return launch_cluster(m, p, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
 }  // namespace lora
 
 using namespace lora;
@@ -450,14 +568,20 @@ int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const 
     if (M == 0) return check_pool(pool);
     if (!x || !W || !y) return LORA_ERR_NULL;
     if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (bias && !aligned16(bias))) return LORA_ERR_ALIGN;
-    if (path < LORA_PATH_AUTO || path > LORA_PATH_SPLITK) return LORA_ERR_SHAPE;
+    if (path < LORA_PATH_AUTO || path > LORA_PATH_STREAM) return LORA_ERR_SHAPE;
     if (path == LORA_PATH_SPLITK && M > kSplitMaxTokens) return LORA_ERR_SHAPE;
-    if (path == LORA_PATH_SPLITK && !lora_id_map) return LORA_ERR_NULL;
+    if (path == LORA_PATH_STREAM && (M > kStreamMaxTokens || (pool && (pool->K % kBK)))) return LORA_ERR_SHAPE;
+    if ((path == LORA_PATH_SPLITK || path == LORA_PATH_STREAM) && !lora_id_map) return LORA_ERR_NULL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     WsLayout L;
     int rc = prepare(lora_id_map, M, pool, segs, ws, ws_bytes, s, &L);
     if (rc) return rc;
-    const bool splitk = path == LORA_PATH_SPLITK || (path == LORA_PATH_AUTO && M <= kSplitMaxTokens);
+    if (path == LORA_PATH_STREAM || (path == LORA_PATH_AUTO && M <= kStreamMaxTokens && lora_id_map)) {
+        const int rc2 = run_cluster(x, M, W, bias, lora_id_map, pool, scale, y, ws, L, s);
+        if (rc2 >= 0) return rc2;
+        if (path == LORA_PATH_STREAM) return LORA_ERR_UNSUPPORTED;
+    }
+    const bool splitk = path == LORA_PATH_SPLITK || (path == LORA_PATH_AUTO && M <= kSplitMaxTokens && lora_id_map);
     if (splitk) return run_splitk(x, M, W, bias, lora_id_map, pool, scale, y, ws, L, s);
     return run_tiled(x, M, W, bias, pool, scale, y, ws, L, kModeLinear, nullptr, 0, nullptr, s);
 }

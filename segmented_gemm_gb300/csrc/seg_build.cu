@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
     int32_t *status = p.counters + CNT_STATUS;
 
     for (int i = tid; i < p.n_counters; i += kSegThreads)
-        if (i != CNT_STATUS) p.counters[i] = 0;
+        if (i != CNT_STATUS && i != CNT_EPOCH) p.counters[i] = 0;
     for (int i = tid; i < 32 * nb; i += kSegThreads) whist[i] = 0;
     for (int i = tid; i < p.A; i += kSegThreads) {
         s_arow[i] = static_cast<int>(p.a_offset[i] / p.K);
@@ -189,6 +189,67 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
     }
     if (tid == 0) p.hdr[HDR_DCHUNKS] = carry;
 
+    // ---- cluster schedule: each adapter's panels in groups of <= 2, and
+    //      the first panel of every segment -----------------------------------
+    carry = 0;
+    int carry_c2 = 0;
+    for (int s0 = 0; s0 < nseg; s0 += kSegThreads) {
+        const int s = s0 + tid;
+        const int nc = s < nseg ? s_rank[s] / kChunk : 0;
+        const int ng = (nc + 1) / 2;
+        int total, total_c;
+        const int exg = block_exclusive_scan(ng, wsum, &total);
+        const int exc = block_exclusive_scan(nc, wsum, &total_c);
+        if (s < nseg) {
+            const int c = carry_c2 + exc;
+            const int i = s_id[s];
+            p.dseg_first[s] = c;
+            p.dseg_group[s] = carry + exg;
+            for (int q = 0; q < ng; ++q) {
+                p.dgrp_first[carry + exg + q] = c + 2 * q;
+                p.dgrp_len[carry + exg + q] = min(2, nc - 2 * q);
+                p.dgrp_arow[carry + exg + q] = s_arow[i] + 2 * q * kChunk;
+                p.dgrp_adapter[carry + exg + q] = i;
+            }
+        }
+        carry += total;
+        carry_c2 += total_c;
+    }
+    if (tid == 0) p.hdr[HDR_DGROUPS] = carry;
+    __syncthreads();
+
+    // ---- stream schedule: which panels of the B pool belong to adapters
+    //      present, in 8-panel windows (pool order).  ppinfo[p] = 2 * group +
+    //      half for a present panel p, -1 otherwise ----------------------------
+    int *ppinfo = whist;   // the histogram space is free again
+    for (int pp = tid; pp < p.P; pp += kSegThreads) ppinfo[pp] = -1;
+    __syncthreads();
+    for (int s = tid; s < nseg; s += kSegThreads) {
+        const int i = s_id[s];
+        const int pp0 = s_brow[i] / p.N;        // first pool panel of adapter i
+        const int np = s_rank[s] / kChunk;
+        const int g0 = p.dseg_group[s];
+        for (int j = 0; j < np; ++j) ppinfo[pp0 + j] = 2 * (g0 + j / 2) + (j & 1);
+    }
+    __syncthreads();
+    carry = 0;
+    const int nwin_all = (p.P + 7) / 8;
+    for (int w0 = 0; w0 < nwin_all; w0 += kSegThreads) {
+        const int w = w0 + tid;
+        int any = 0;
+        if (w < nwin_all)
+            for (int j = 0; j < 8 && 8 * w + j < p.P; ++j) any |= ppinfo[8 * w + j] >= 0;
+        int total;
+        const int ex = block_exclusive_scan(any, wsum, &total);
+        if (any) {
+            const int k = carry + ex;
+            p.ewin_first[k] = 8 * w;
+            for (int j = 0; j < 8; ++j) p.pinfo[8 * k + j] = 8 * w + j < p.P ? ppinfo[8 * w + j] : -1;
+        }
+        carry += total;
+    }
+    if (tid == 0) p.hdr[HDR_NWIN] = carry;
+
     // ---- tiled schedule: per 128-token tile of the permuted order, the
     //      rank panels of the segments it intersects, and its shrink jobs ---
     int carry_c = 0, carry_j = 0;
@@ -245,7 +306,11 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
     }
 }
 
-size_t seg_build_smem_bytes(int32_t A) { return static_cast<size_t>(32 * (A + 1) + (A + 2) + 32 + 6 * A) * 4; }
+size_t seg_build_smem_bytes(int32_t A)
+{
+    // the [32][A+1] histogram space is reused for the pool panel table (<= 4 A entries)
+    return static_cast<size_t>(32 * (A + 1) + (A + 2) + 32 + 6 * A) * 4;
+}
 
 cudaError_t launch_seg_build(const SegParams &p, cudaStream_t stream)
 {

@@ -21,7 +21,7 @@ LORA_OK = 0
 LORA_ERR_NULL, LORA_ERR_SHAPE, LORA_ERR_ALIGN, LORA_ERR_RANK = 1, 2, 3, 4
 LORA_ERR_WORKSPACE, LORA_ERR_CUDA, LORA_ERR_UNSUPPORTED, LORA_ERR_SEGMENTS = 5, 6, 7, 8
 LORA_DEV_BAD_ID, LORA_DEV_TIMEOUT = 1, 2
-LORA_PATH_AUTO, LORA_PATH_TILED, LORA_PATH_SPLITK = 0, 1, 2
+LORA_PATH_AUTO, LORA_PATH_TILED, LORA_PATH_SPLITK, LORA_PATH_STREAM = 0, 1, 2, 3
 LORA_MAX_RANK, LORA_RANK_ALIGN, LORA_MAX_ADAPTERS = 64, 16, 1024
 
 EXPORTS = ("lora_pool_layout", "lora_workspace_size", "lora_workspace_init", "lora_build_segments",

@@ -114,21 +114,28 @@ def test_tiny_config_all_rows_both_paths():
     wl = workloads.make_config("tiny")
     dev = to_dev(wl)
     ref = oracle.lora_linear(wl)
-    for path in (L.LORA_PATH_AUTO, L.LORA_PATH_TILED, L.LORA_PATH_SPLITK):
+    for path in (L.LORA_PATH_AUTO, L.LORA_PATH_TILED, L.LORA_PATH_SPLITK, L.LORA_PATH_STREAM):
         y, ws, status = run_linear(wl, dev, path)
         assert status == 0
         assert_close(y, ref, what=f"tiny path={path}")
 
 
-@pytest.mark.parametrize("path", [L.LORA_PATH_TILED, L.LORA_PATH_SPLITK])
+@pytest.mark.parametrize("path", [L.LORA_PATH_TILED, L.LORA_PATH_SPLITK, L.LORA_PATH_STREAM])
 @pytest.mark.parametrize("M,K,N,ranks,mode", [
     (1, 64, 64, [16], "single"),
     (7, 200, 136, [8, 40, 64], "uniform"),          # K not a multiple of 64, N ragged
     (100, 320, 520, [16, 32, 48, 64, 20], "uniform"),
     (128, 256, 256, [64] * 6, "uniform"),
     (61, 512, 384, [16] * 40, "uniform"),            # many segments in one tile
+    (33, 640, 1032, [48, 16, 64, 32], "uniform"),    # odd number of K blocks, 9 output tiles
+    (64, 1024, 2048, [64] * 12 + [16] * 12, "uniform"),
+    (16, 4096, 4096, [16, 32, 64] * 7, "uniform"),  # decode shapes, 21 adapters
 ])
 def test_linear_small_shapes(path, M, K, N, ranks, mode):
+    if path == L.LORA_PATH_STREAM and (M > 64 or K % 64):
+        pytest.skip("streaming schedule serves M <= 64 with K a multiple of 64")
+    if path == L.LORA_PATH_SPLITK and M > 128:
+        pytest.skip("split-K schedule serves M <= 128")
     wl = workloads.make_custom(M, K, N, ranks, seed=M * 7 + K, id_mode=mode, p_base=0.15, scale=1.5)
     dev = to_dev(wl)
     y, ws, status = run_linear(wl, dev, path)
@@ -163,10 +170,10 @@ def test_linear_no_bias_and_prebuilt_segments():
 
 def test_linear_repeated_calls_reuse_workspace():
     """Counters are left zeroed: the same workspace serves call after call."""
-    wl = workloads.make_custom(96, 256, 512, [16, 32, 64], seed=5, scale=2.0)
+    wl = workloads.make_custom(60, 256, 512, [16, 32, 64], seed=5, scale=2.0)
     dev = to_dev(wl)
     ref = oracle.lora_linear(wl)
-    for path in (L.LORA_PATH_TILED, L.LORA_PATH_SPLITK):
+    for path in (L.LORA_PATH_TILED, L.LORA_PATH_SPLITK, L.LORA_PATH_STREAM):
         ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
         segs = L.lora_build_segments(dev["ids"], dev["pool"], ws)
         for _ in range(4):
@@ -182,7 +189,7 @@ def test_decode_walkthrough_shapes():
     wl = workloads.make_custom(3, 4096, 12288, [16, 16, 32], seed=34, ids=[0, 2, -1])
     dev = to_dev(wl)
     ref = oracle.lora_linear(wl)
-    for path in (L.LORA_PATH_SPLITK, L.LORA_PATH_TILED):
+    for path in (L.LORA_PATH_STREAM, L.LORA_PATH_SPLITK, L.LORA_PATH_TILED):
         y, ws, status = run_linear(wl, dev, path)
         assert status == 0
         assert_close(y, ref, what=f"walkthrough path={path}")
@@ -194,7 +201,7 @@ def test_invalid_ids_are_base_only_and_flagged():
     wl.ids[1] = -3
     dev = to_dev(wl)
     ref = oracle.lora_linear(wl)      # oracle treats them as -1 too
-    for path in (L.LORA_PATH_TILED, L.LORA_PATH_SPLITK):
+    for path in (L.LORA_PATH_TILED, L.LORA_PATH_SPLITK, L.LORA_PATH_STREAM):
         y, ws, status = run_linear(wl, dev, path)
         assert status & L.LORA_DEV_BAD_ID
         assert_close(y, ref, what=f"invalid ids path={path}")
