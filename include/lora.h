@@ -52,7 +52,8 @@ enum {
     LORA_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than lora_workspace_size() */
     LORA_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch error, bad device) */
     LORA_ERR_UNSUPPORTED = 7,   /* device is not sm_103 / sm_100 family or similar */
-    LORA_ERR_SEGMENTS = 8       /* a prebuilt segment table does not match this call */
+    LORA_ERR_SEGMENTS = 8,      /* a prebuilt segment table does not match this call */
+    LORA_ERR_CAPACITY = 9       /* the problem needs more scratch than lora_linear_noalloc holds */
 };
 
 /* Device-side status bits (returned through lora_get_status). */
@@ -210,6 +211,34 @@ int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const 
                    const int32_t *lora_id_map, const lora_pool_t *pool, float scale,
                    const lora_segments_t *segs, lora_bf16_t *y, void *ws, size_t ws_bytes,
                    lora_stream_t stream, int32_t path);
+
+/*
+ * lora_linear without a workspace, for callers that cannot allocate device
+ * memory: an inference-engine hook or plugin that is handed no workspace and
+ * may not call cudaMalloc while it runs, for example.  (The paper has no
+ * counterpart; this is a convenience of this library.)
+ *
+ * Same arguments, layouts and result as lora_linear (segments are always
+ * built internally).  The scratch is a file-scope device array of
+ * LORA_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that
+ * loads the library holds until the process exits; nothing is allocated or
+ * freed.  A call whose lora_workspace_size(M, N, num_adapters) exceeds that
+ * size returns LORA_ERR_CAPACITY and enqueues nothing.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array, which keeps the previous call's
+ * contents: each call first clears (with cudaMemsetAsync on `stream`) the
+ * parts that must start at zero.  Calls whose execution overlaps on the GPU
+ * (other streams, other host threads) race on the array and must be avoided.
+ * Device-detected problems (bad ids) are handled as in lora_linear, but the
+ * status word is cleared by the next call and cannot be read through this
+ * entry point.
+ */
+#define LORA_NOALLOC_SCRATCH_BYTES (8u << 20)   /* 8 MiB */
+int lora_linear_noalloc(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
+                        const int32_t *lora_id_map, const lora_pool_t *pool, float scale, lora_bf16_t *y,
+                        lora_stream_t stream);
 
 /*
  * Synchronise `stream`, then read and clear the device status word of ws

@@ -20,13 +20,15 @@ LIB_PATH = os.path.join(_PKG, "liblora.so")
 LORA_OK = 0
 LORA_ERR_NULL, LORA_ERR_SHAPE, LORA_ERR_ALIGN, LORA_ERR_RANK = 1, 2, 3, 4
 LORA_ERR_WORKSPACE, LORA_ERR_CUDA, LORA_ERR_UNSUPPORTED, LORA_ERR_SEGMENTS = 5, 6, 7, 8
+LORA_ERR_CAPACITY = 9
+LORA_NOALLOC_SCRATCH_BYTES = 8 << 20
 LORA_DEV_BAD_ID, LORA_DEV_TIMEOUT = 1, 2
 LORA_PATH_AUTO, LORA_PATH_TILED, LORA_PATH_SPLITK, LORA_PATH_STREAM = 0, 1, 2, 3
 LORA_MAX_RANK, LORA_RANK_ALIGN, LORA_MAX_ADAPTERS = 64, 16, 1024
 
 EXPORTS = ("lora_pool_layout", "lora_workspace_size", "lora_workspace_init", "lora_build_segments",
            "lora_shrink", "lora_expand", "lora_linear", "lora_linear_ex", "lora_get_status",
-           "lora_status_string")
+           "lora_status_string", "lora_linear_noalloc")
 
 
 class lora_pool_t(ctypes.Structure):
@@ -75,6 +77,7 @@ def load_library():
         "lora_linear": (ctypes.c_int, [P, I64, P, P, P, PP, F32, PS, P, P, SZ, P]),
         "lora_linear_ex": (ctypes.c_int, [P, I64, P, P, P, PP, F32, PS, P, P, SZ, P, I32]),
         "lora_get_status": (ctypes.c_int, [P, P, P]),
+        "lora_linear_noalloc": (ctypes.c_int, [P, I64, P, P, P, PP, F32, P, P]),
         "lora_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
@@ -252,6 +255,20 @@ def lora_expand(S: torch.Tensor, ids: torch.Tensor, pool: LoraPool, scale: float
         _ptr(S), S.shape[1], M, _ptr(ids), ctypes.byref(pool.desc),
         ctypes.byref(segs) if segs is not None else None, float(scale), _ptr(y), ws.ptr, ws.nbytes,
         _stream(stream)), "lora_expand")
+    return y
+
+
+def lora_linear_noalloc(x: torch.Tensor, W: torch.Tensor, bias: Optional[torch.Tensor], ids: torch.Tensor,
+                        pool: LoraPool, scale: float, y: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+    """lora_linear for callers that cannot allocate device memory: the
+    library's own static scratch array is used instead of a workspace."""
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty(M, W.shape[0], dtype=torch.bfloat16, device=x.device)
+    _check(load_library().lora_linear_noalloc(
+        _ptr(x), M, _ptr(W), _ptr(bias), _ptr(ids), ctypes.byref(pool.desc), float(scale), _ptr(y),
+        _stream(stream)), "lora_linear_noalloc")
     return y
 
 

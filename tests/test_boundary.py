@@ -65,7 +65,7 @@ def test_workspace_size_monotone(lib):
 
 
 def test_status_strings(lib):
-    for c in range(9):
+    for c in range(10):
         assert L.status_string(c)
     assert "unknown" in L.status_string(99)
 
