@@ -38,6 +38,7 @@ import torch  # noqa: E402
 from segmented_gemm_gb300 import workloads  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
+MAX_SETS = None          # --max-sets: cap the rotating input sets (small profiler captures)
 METRIC = "multi-LoRA linear tokens/s; % of HBM / bf16 tensor roofline, M=32..8192"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 CONFIG_TEXT = {
@@ -68,6 +69,16 @@ def algorithmic_work(wl):
     lora_flops = sum(2 * wl.ranks[int(i)] * (wl.K + wl.N) for i in ids.tolist() if 0 <= i < wl.num_adapters)
     flops = 2 * wl.M * wl.K * wl.N + lora_flops
     return nbytes, flops, len(present)
+
+
+def dominant_kernel(wl):
+    """The kernel lora_linear's automatic schedule choice launches for this
+    shape (the same rule as the library's dispatch)."""
+    if wl.M <= 64 and wl.K % 64 == 0:
+        return "lora_cluster_kernel"
+    if wl.M <= 128:
+        return "lora_splitk_kernel"
+    return "lora_tc_kernel"
 
 
 def load_peaks():
@@ -193,6 +204,7 @@ class InputSet:
 
 
 def build_sets(wl, L, device, min_bytes=4 * L2_BYTES, max_sets=16):
+    max_sets = MAX_SETS or max_sets
     first = InputSet(wl, L, device)
     n = 1 if first.nbytes() >= min_bytes else min(max_sets, math.ceil(min_bytes / first.nbytes()))
     sets = [first] + [InputSet(wl, L, device) for _ in range(n - 1)]
@@ -358,7 +370,7 @@ def ours(args):
     # roofline of the dominant kernel (the fused layer)
     kern_s = r["kernel_ms"] * 1e-3
     hbm_bound = wl.M <= 128
-    kname = "lora_splitk_kernel" if hbm_bound else "lora_tc_kernel"
+    kname = dominant_kernel(wl)
     if hbm_bound:
         achieved = r["bytes"] / kern_s / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -487,7 +499,11 @@ def main():
     ap.add_argument("--config", choices=list(CONFIG_TEXT), default="decode")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--max-sets", type=int, default=None,
+                    help="cap the rotating input sets (for small ncu captures; the L2 note in config says so)")
     args = ap.parse_args()
+    global MAX_SETS
+    MAX_SETS = args.max_sets
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         reference(args)
