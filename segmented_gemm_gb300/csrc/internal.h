@@ -8,6 +8,8 @@
 //              num_segments[1]                             (the §2.3 table)
 //   plan       header, per-tile chunk lists, shrink-job list, split-K chunk
 //              list                                        (kernel work lists)
+//   windows    stream schedule: window list, per-window arrival and consumer
+//              counters (zero at rest), fp32 window sums of S (zero at rest)
 //   s_scratch  bf16 S panels (scaled, masked), [chunks][rows][16]
 //   acc        fp32 split-K tile accumulators (zero at rest)
 #pragma once
@@ -31,6 +33,7 @@ constexpr int kSplitMaxTokens = 128;   // largest M served by the split-K path
 constexpr int kSplitBN = 128;          // output features per tile (UMMA M)
 constexpr int kSplitMaxCtas = 1024;    // upper bound on the persistent grid
 constexpr int kStreamMaxTokens = 64;    // largest M served by the weight-streaming schedule
+constexpr int kWinCntStride = 32;       // ints per window counter pair (one 128-byte line)
 
 // plan header entries
 enum PlanHdr {
@@ -38,8 +41,7 @@ enum PlanHdr {
     HDR_NSJOBS = 1,       // shrink jobs of the tiled schedule
     HDR_DCHUNKS = 2,      // chunks of the split-K schedule (adapters present)
     HDR_NSEG = 3,         // number of segments
-    HDR_DGROUPS = 4,      // stream schedule: groups of <= 2 panels of one adapter
-    HDR_NWIN = 5,         // stream schedule: 8-panel windows of the B pool holding present panels
+    HDR_NWIN = 5,         // stream schedule: 128-row windows of the pools holding panels of adapters present
     HDR_WORDS = 16
 };
 
@@ -49,7 +51,6 @@ enum Counters {
     CNT_CTAS_DONE = 1,    // tiled schedule: CTAs finished
     CNT_SPLIT_DONE = 2,   // split-K: CTAs finished
     CNT_SPLIT_SREADY = 3, // split-K: shrink row tiles reduced
-    CNT_EPOCH = 4,        // stream schedule: call parity of the double-buffered accumulators
     CNT_FIXED = 8         // first per-tile counter
 };
 
@@ -66,10 +67,9 @@ struct WsLayout {
     size_t hdr, tile_chunk_off, chunk_arow, chunk_brow, chunk_rng;
     size_t sjob_tile, sjob_c0, sjob_c1, tile_njobs;
     size_t dchunk_arow, dchunk_brow, dchunk_adapter;
-    size_t dgrp_first, dgrp_len, dseg_first, dgrp_arow, dgrp_adapter, dseg_group;
-    size_t ewin_first, pinfo, acc_str, acc_str_bytes, gcnt;
-    int32_t max_dgroups;      // stream-schedule shrink groups capacity
-    int32_t max_win;          // stream-schedule expand windows capacity
+    size_t ewin_first, pinfo, wcnt, acc_str, acc_str_bytes;
+    int32_t max_win;          // window-list capacity (all windows of the pool)
+    int32_t max_win_str;      // windows the stream schedule's sums can hold (M <= 64)
     size_t s_scratch, s_scratch_bytes;
     size_t acc_out, acc_out_bytes, acc_shr, acc_shr_bytes;
     size_t total;
@@ -121,19 +121,20 @@ struct SplitParams {
 };
 
 struct ClusterMaps {
-    CUtensorMap w3, a3_16, a3_32, b3;
+    CUtensorMap w3, a3, b3;    // W, A pool: {64, 128 rows, 2 K blocks}; B pool: {16, 128 rows, 8 panels}
 };
 
 struct ClusterParams {
     int64_t M;
-    int32_t N, K, T_pad, C, NT, kblocks, stages, tmem_cols, max_regions, max_groups;
+    int32_t N, K, T_pad, C, NT, kblocks, stages, max_regions, max_win_str;
     float scale;
     const uint16_t *bias;
     const uint16_t *x;         // bf16 [M, K] (read by the loader warps)
     uint16_t *y;
-    const int32_t *ids, *hdr, *dgrp_arow, *dgrp_len, *dgrp_adapter, *ewin_first, *pinfo;
-    float *acc;                // fp32 [2][groups][T_pad][32]: per-epoch group sums of S
-    int32_t *gcnt;             // [2][groups]: per-epoch group arrival counts
+    const int32_t *ids, *hdr, *ewin_first, *pinfo;
+    float *acc;                // fp32 [windows][T_pad][128]: per-window sums of S (zero at rest)
+    int32_t *wcnt;             // [windows][kWinCntStride]: shrink arrivals at 0, consumer CTAs at 16 (zero at rest)
+    int32_t max_win;
     int32_t *counters;
 };
 
@@ -148,9 +149,10 @@ struct SegParams {
     int32_t *hdr, *tile_chunk_off, *chunk_arow, *chunk_brow, *chunk_rng;
     int32_t *sjob_tile, *sjob_c0, *sjob_c1, *tile_njobs;
     int32_t *dchunk_arow, *dchunk_brow, *dchunk_adapter;
-    int32_t *dgrp_first, *dgrp_len, *dseg_first, *dgrp_arow, *dgrp_adapter, *dseg_group;
     int32_t *ewin_first, *pinfo;
-    int32_t P;                 // panels in the B pool (b_elems / (16 N))
+    int32_t P;                 // panels in the pools (b_elems / (16 N))
+    int32_t max_win;           // window-list capacity
+    int32_t *wcnt;             // [max_win][kWinCntStride] stream-schedule window counters, zeroed here
     int32_t *counters;
     int32_t n_counters;
 };
@@ -161,10 +163,12 @@ cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cudaStrea
 cudaError_t launch_s_prep(const float *S, int32_t s_cols, float scale, const TcParams &p, cudaStream_t stream);
 cudaError_t launch_splitk(const TcMaps &maps, const SplitParams &p, int grid, cudaStream_t stream);
 int splitk_stages(int T_pad);
-cudaError_t launch_cluster(const ClusterMaps &m, const ClusterParams &p, cudaStream_t stream);
+cudaError_t launch_cluster(const ClusterMaps &m, const ClusterParams &p, bool pdl, cudaStream_t stream);
 int cluster_pick_size(int NT, int T_pad, int sms);
 int cluster_stages(int T_pad);
 int cluster_max_regions();
+int cluster_max_runs();
+int cluster_max_win_cta();
 int cluster_win();
 int splitk_max_runs();
 int num_sms_current_device();

@@ -154,19 +154,15 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
     L.dchunk_arow = take(static_cast<size_t>(L.max_dchunks) * 4);
     L.dchunk_brow = take(static_cast<size_t>(L.max_dchunks) * 4);
     L.dchunk_adapter = take(static_cast<size_t>(L.max_dchunks) * 4);
-    L.max_dgroups = static_cast<int32_t>(2 * present + 2);
-    L.dgrp_first = take(static_cast<size_t>(L.max_dgroups) * 4);
-    L.dgrp_len = take(static_cast<size_t>(L.max_dgroups) * 4);
-    L.dseg_first = take(static_cast<size_t>(std::max(A, 1)) * 4);
-    L.dgrp_arow = take(static_cast<size_t>(L.max_dgroups) * 4);
-    L.dgrp_adapter = take(static_cast<size_t>(L.max_dgroups) * 4);
-    L.dseg_group = take(static_cast<size_t>(std::max(A, 1)) * 4);
+    // stream schedule: windows of 8 pool panels.  An adapter's <= 4 panels
+    // span at most 2 windows, so a batch touches <= 2 * min(A, M) of them.
     L.max_win = (4 * A + 7) / 8 + 1;
+    L.max_win_str = static_cast<int32_t>(std::min<int64_t>(L.max_win, 2 * present));
     L.ewin_first = take(static_cast<size_t>(L.max_win) * 4);
     L.pinfo = take(static_cast<size_t>(L.max_win) * 8 * 4);
-    L.gcnt = take(static_cast<size_t>(2 * L.max_dgroups) * 4);
+    L.wcnt = take(static_cast<size_t>(L.max_win) * kWinCntStride * 4);
     L.acc_str_bytes = M <= kStreamMaxTokens
-                          ? static_cast<size_t>(2) * L.max_dgroups * split_tpad(M) * 32 * 4 : 16;
+                          ? static_cast<size_t>(std::max(L.max_win_str, 1)) * split_tpad(M) * kSplitBN * 4 : 16;
     L.acc_str = take(L.acc_str_bytes);
     o = (o + 1023) & ~size_t(1023);
     L.s_scratch = take(L.s_scratch_bytes);
@@ -252,15 +248,11 @@ static int enqueue_segments(const int32_t *ids, int64_t M, const lora_pool_t *po
     p.dchunk_arow = at<int32_t>(ws, L.dchunk_arow);
     p.dchunk_brow = at<int32_t>(ws, L.dchunk_brow);
     p.dchunk_adapter = at<int32_t>(ws, L.dchunk_adapter);
-    p.dgrp_first = at<int32_t>(ws, L.dgrp_first);
-    p.dgrp_len = at<int32_t>(ws, L.dgrp_len);
-    p.dseg_first = at<int32_t>(ws, L.dseg_first);
-    p.dgrp_arow = at<int32_t>(ws, L.dgrp_arow);
-    p.dgrp_adapter = at<int32_t>(ws, L.dgrp_adapter);
-    p.dseg_group = at<int32_t>(ws, L.dseg_group);
     p.ewin_first = at<int32_t>(ws, L.ewin_first);
     p.pinfo = at<int32_t>(ws, L.pinfo);
     p.P = pool->num_adapters ? static_cast<int32_t>(pool->b_elems / (static_cast<int64_t>(kChunk) * pool->N)) : 0;
+    p.max_win = L.max_win;
+    p.wcnt = at<int32_t>(ws, L.wcnt);
     p.counters = at<int32_t>(ws, L.counters);
     p.n_counters = static_cast<int32_t>(L.n_counters);
     return launch_seg_build(p, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
@@ -418,10 +410,11 @@ static int run_splitk(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, con
 
 // Weight-streaming schedule (M <= 64, K a multiple of 64): one cluster of C
 // CTAs per 128-feature output tile.  Returns -1 when this device / shape
-// cannot host it, so the caller falls back to split-K.
+// cannot host it, so the caller falls back to split-K.  pdl: the segment
+// builder was enqueued right before this launch on the same stream.
 static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
                        const int32_t *ids, const lora_pool_t *pool, float scale, lora_bf16_t *y, void *ws,
-                       const WsLayout &L, cudaStream_t stream)
+                       const WsLayout &L, bool pdl, cudaStream_t stream)
 {
     if (M > kStreamMaxTokens || (pool->K % kBK) != 0) return -1;
     const int T = split_tpad(M);
@@ -449,9 +442,14 @@ static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, co
     }
     if (C <= 0) return -1;
     const int grid = C * NT;
+    const int kblocks = pool->K / kBK;
+    const int64_t KU2 = (kblocks + 1) / 2;
     const int max_regions = std::min(cluster_max_regions(), 512 / T);
-    // shrink runs of one CTA (each needs its own TMEM region) stay below the cap
-    if ((L.max_dgroups + grid - 1) / grid + 2 > max_regions - 1) return -1;
+    // the shrink runs and expand windows of one CTA fit its on-chip tables
+    const int64_t u_cta = (static_cast<int64_t>(L.max_win_str) * KU2 + grid - 1) / grid;
+    const int64_t runs = (u_cta + KU2 - 1) / KU2 + 1;
+    if (runs > cluster_max_runs() || runs + 1 > max_regions) return -1;
+    if ((L.max_win_str + C - 1) / C > cluster_max_win_cta()) return -1;
     ClusterParams p;
     std::memset(&p, 0, sizeof p);
     p.M = M;
@@ -460,39 +458,35 @@ static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, co
     p.T_pad = T;
     p.C = C;
     p.NT = NT;
-    p.kblocks = pool->K / kBK;
+    p.kblocks = kblocks;
     p.stages = cluster_stages(T);
-    p.tmem_cols = 512;
     p.max_regions = max_regions;
-    p.max_groups = L.max_dgroups;
+    p.max_win_str = L.max_win_str;
+    p.max_win = L.max_win;
     p.scale = scale;
     p.bias = bias;
     p.x = x;
     p.y = y;
     p.ids = ids;
     p.hdr = at<int32_t>(ws, L.hdr);
-    p.dgrp_arow = at<int32_t>(ws, L.dgrp_arow);
-    p.dgrp_len = at<int32_t>(ws, L.dgrp_len);
-    p.dgrp_adapter = at<int32_t>(ws, L.dgrp_adapter);
     p.ewin_first = at<int32_t>(ws, L.ewin_first);
     p.pinfo = at<int32_t>(ws, L.pinfo);
     p.acc = at<float>(ws, L.acc_str);
-    p.gcnt = at<int32_t>(ws, L.gcnt);
+    p.wcnt = at<int32_t>(ws, L.wcnt);
     p.counters = at<int32_t>(ws, L.counters);
-    const uint64_t K = pool->K, N = pool->N, KB = pool->K / kBK;
+    const uint64_t K = pool->K, N = pool->N, KB = kblocks;
     ClusterMaps m;
     const CUtensorMapSwizzle s128 = CU_TENSOR_MAP_SWIZZLE_128B, s32 = CU_TENSOR_MAP_SWIZZLE_32B;
     if (!encode_3d(&m.w3, W, kBK, N, KB, K * 2, kBK * 2, kBK, kSplitBN, 2, s128)) return LORA_ERR_CUDA;
     const void *apool = pool->num_adapters ? static_cast<const void *>(pool->a_pool) : static_cast<const void *>(W);
     const uint64_t arows = pool->num_adapters ? static_cast<uint64_t>(pool->a_elems / pool->K) : 1;
-    if (!encode_3d(&m.a3_16, apool, kBK, arows, KB, K * 2, kBK * 2, kBK, kChunk, 4, s128)) return LORA_ERR_CUDA;
-    if (!encode_3d(&m.a3_32, apool, kBK, arows, KB, K * 2, kBK * 2, kBK, 2 * kChunk, 4, s128)) return LORA_ERR_CUDA;
+    if (!encode_3d(&m.a3, apool, kBK, arows, KB, K * 2, kBK * 2, kBK, kSplitBN, 2, s128)) return LORA_ERR_CUDA;
     const void *bpool = pool->num_adapters ? static_cast<const void *>(pool->b_pool) : static_cast<const void *>(W);
     const uint64_t panels =
         pool->num_adapters ? static_cast<uint64_t>(pool->b_elems / (static_cast<int64_t>(kChunk) * N)) : 1;
     if (!encode_3d(&m.b3, bpool, kChunk, N, panels, kChunk * 2, N * kChunk * 2, kChunk, kSplitBN, cluster_win(), s32))
         return LORA_ERR_CUDA;
-    return launch_cluster(m, p, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+    return launch_cluster(m, p, pdl, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
 }  // namespace lora
@@ -577,7 +571,7 @@ int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const 
     int rc = prepare(lora_id_map, M, pool, segs, ws, ws_bytes, s, &L);
     if (rc) return rc;
     if (path == LORA_PATH_STREAM || (path == LORA_PATH_AUTO && M <= kStreamMaxTokens && lora_id_map)) {
-        const int rc2 = run_cluster(x, M, W, bias, lora_id_map, pool, scale, y, ws, L, s);
+        const int rc2 = run_cluster(x, M, W, bias, lora_id_map, pool, scale, y, ws, L, segs == nullptr, s);
         if (rc2 >= 0) return rc2;
         if (path == LORA_PATH_STREAM) return LORA_ERR_UNSUPPORTED;
     }

@@ -4,12 +4,24 @@
 // handles, which segment it belongs to and its rank are decided before the
 // GEMM launches, not by branching inside it).
 //
-// One CTA of 1024 threads.  Each warp owns a contiguous range of tokens:
-//   pass 1  warp-aggregated histogram (__match_any_sync peers, leader adds
-//           popc) into a per-warp row of a [32][A+1] shared table
-//   scan    bucket totals -> exclusive scan -> per-warp running bases
-//   pass 2  stable scatter: rank inside a 32-token step = popc of the peers
-//           below the lane, plus the warp's running base for the bucket
+// One CTA of 512 threads (16 warps), three block-wide barriers:
+//   phase 0  zero the counter block, stage ranks and pool offsets on chip
+//   phase 1  each warp owns a contiguous range of tokens and builds its own
+//            histogram row (__match_any_sync peers, the leader adds popc)
+//   phase 2  bucket totals -> exclusive scan -> per-warp running bases
+//   phase 3  every warp scatters its own tokens (stable: the rank inside a
+//            32-token step is the popc of the peers below the lane plus the
+//            warp's running base), then the warps build one list each, in
+//            parallel and without further block barriers:
+//              warp 0       the segment table (one segment per non-empty
+//                           adapter bucket, ascending id)
+//              warp 1       split-K chunk list (rank panels of adapters present)
+//              warp 2       stream-schedule windows: 128-row windows of the
+//                           adapter pools that hold panels of adapters present
+//              warps 3..15  tiled-schedule chunk lists and shrink jobs: one
+//                           warp per 128-token tile (a lane per adapter
+//                           bucket) when there are at most 13 tiles, else
+//                           one thread per tile
 // Bucket 0 holds id -1, bucket i+1 adapter i; ids outside [-1, A) are
 // counted as -1 and flagged in the status word.
 #include <cuda_runtime.h>
@@ -20,96 +32,138 @@
 
 namespace lora {
 
+constexpr int kSegThreads = 512;
+constexpr int kSegWarps = kSegThreads / 32;
+constexpr int kTileWarp0 = 3;                       // first warp of the tile-list group
+constexpr int kTileWarps = kSegWarps - kTileWarp0;
+constexpr int kTileBar = 1;                         // named barrier of the tile-list group
 
-constexpr int kSegThreads = 1024;
+// Bucket of a token id: 0 for -1 and for ids outside [-1, A), else id + 1.
+__device__ __forceinline__ int id_bucket(int id, int A) { return (id >= 0 && id < A) ? id + 1 : 0; }
 
-// Exclusive scan of one int per thread over the 1024-thread block.
+__device__ __forceinline__ int warp_incl_scan(int v, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+    }
+    return v;
+}
+
+// Exclusive scan of one int per thread over the whole block.
 __device__ int block_exclusive_scan(int v, int *wsum, int *total)
 {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
+    const int x = warp_incl_scan(v, lane);
     if (lane == 31) wsum[w] = x;
     __syncthreads();
     if (w == 0) {
-        int s = wsum[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int y = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += y;
-        }
-        wsum[lane] = s;
+        int s = lane < kSegWarps ? wsum[lane] : 0;
+        s = warp_incl_scan(s, lane);
+        if (lane < kSegWarps) wsum[lane] = s;
     }
     __syncthreads();
     const int excl = x - v + (w > 0 ? wsum[w - 1] : 0);
-    *total = wsum[31];
+    *total = wsum[kSegWarps - 1];
     __syncthreads();
     return excl;
 }
 
+// Exclusive scan of two ints per thread over the tile-list warps only.
+__device__ void tile_group_scan(int a, int b, int *ws2, int *ea, int *eb, int *ta, int *tb)
+{
+    const int lane = threadIdx.x & 31, gw = (threadIdx.x >> 5) - kTileWarp0;
+    const int xa = warp_incl_scan(a, lane), xb = warp_incl_scan(b, lane);
+    if (lane == 31) {
+        ws2[2 * gw] = xa;
+        ws2[2 * gw + 1] = xb;
+    }
+    named_bar_sync(kTileBar, kTileWarps * 32);
+    if (gw == 0) {
+        int sa = lane < kTileWarps ? ws2[2 * lane] : 0, sb = lane < kTileWarps ? ws2[2 * lane + 1] : 0;
+        sa = warp_incl_scan(sa, lane);
+        sb = warp_incl_scan(sb, lane);
+        if (lane < kTileWarps) {
+            ws2[2 * lane] = sa;
+            ws2[2 * lane + 1] = sb;
+        }
+    }
+    named_bar_sync(kTileBar, kTileWarps * 32);
+    *ea = xa - a + (gw > 0 ? ws2[2 * (gw - 1)] : 0);
+    *eb = xb - b + (gw > 0 ? ws2[2 * (gw - 1) + 1] : 0);
+    *ta = ws2[2 * (kTileWarps - 1)];
+    *tb = ws2[2 * (kTileWarps - 1) + 1];
+    named_bar_sync(kTileBar, kTileWarps * 32);
+}
+
 __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
 {
+    // the fused kernel that follows may start its prologue and its weight
+    // stream now; it waits for this grid before reading anything built here
+    pdl_launch_dependents();
+
     extern __shared__ int sm[];
-    const int nb = p.A + 1;
-    int *whist = sm;                 // [32][nb]
-    int *bsum = whist + 32 * nb;     // [nb + 1]
-    int *wsum = bsum + nb + 1;       // [32]
-    // the segment table and per-adapter pool rows, kept on chip for the
-    // per-tile loops below (A entries each)
-    int *s_id = wsum + 32, *s_start = s_id + p.A, *s_len = s_start + p.A, *s_rank = s_len + p.A;
-    int *s_arow = s_rank + p.A;      // a_offset / K
-    int *s_brow = s_arow + p.A;      // b_offset / 16
+    const int A = p.A, nb = A + 1;
+    int *whist = sm;                          // [kSegWarps][nb]
+    int *bsum = whist + kSegWarps * nb;       // [nb + 1] bucket offsets
+    int *wsum = bsum + nb + 1;                // [32] scan scratch
+    int *s_rank = wsum + 32;                  // [A] padded ranks
+    int *s_arow = s_rank + A;                 // [A] first A pool row (a_offset / K)
+    int *s_brow = s_arow + A;                 // [A] b_offset / 16
+    int *ptab = s_brow + A;                   // [P] pool panel -> adapter present owning it, else -1
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     int32_t *status = p.counters + CNT_STATUS;
 
-    for (int i = tid; i < p.n_counters; i += kSegThreads)
-        if (i != CNT_STATUS && i != CNT_EPOCH) p.counters[i] = 0;
-    for (int i = tid; i < 32 * nb; i += kSegThreads) whist[i] = 0;
-    for (int i = tid; i < p.A; i += kSegThreads) {
-        s_arow[i] = static_cast<int>(p.a_offset[i] / p.K);
-        s_brow[i] = static_cast<int>(p.b_offset[i] / kChunk);
-    }
-    __syncthreads();
-
-    const int64_t per = (p.M + 31) / 32;
+    const int64_t per = (p.M + kSegWarps - 1) / kSegWarps;
     const int64_t t_begin = w * per;
     const int64_t t_end = t_begin + per < p.M ? t_begin + per : p.M;
 
-    // ---- pass 1: per-warp histograms --------------------------------------
+    // ---- phase 0 -------------------------------------------------------------
+    for (int i = tid; i < p.n_counters; i += kSegThreads)
+        if (i != CNT_STATUS) p.counters[i] = 0;
+    for (int i = tid; i < p.max_win * kWinCntStride; i += kSegThreads) p.wcnt[i] = 0;
+    for (int i = tid; i < kSegWarps * nb; i += kSegThreads) whist[i] = 0;
+    for (int i = tid; i < A; i += kSegThreads) {
+        s_rank[i] = p.rank[i];
+        s_arow[i] = static_cast<int>(p.a_offset[i] / p.K);
+        s_brow[i] = static_cast<int>(p.b_offset[i] / kChunk);
+    }
+    for (int i = tid; i < p.P; i += kSegThreads) ptab[i] = -1;
+    __syncthreads();
+
+    // ---- phase 1: per-warp histograms ----------------------------------------
     int bad = 0;
-    for (int64_t base = t_begin; base < t_end; base += 32) {
-        const int64_t t = base + lane;
+    auto hist_step = [&](int64_t t, int id) {
         const bool act = t < t_end;
         const unsigned amask = __ballot_sync(0xffffffffu, act);
         if (act) {
-            const int id = p.ids[t];
-            const int e = (id >= 0 && id < p.A) ? id : -1;
-            bad |= (e != id);
-            const int b = e + 1;
+            const int b = id_bucket(id, A);
+            bad |= (b == 0 && id != -1);
             const unsigned peers = __match_any_sync(amask, b);
             if (lane == __ffs(peers) - 1) whist[w * nb + b] += __popc(peers);
         }
+    };
+    for (int64_t base = t_begin; base < t_end; base += 32) {
+        const int64_t t = base + lane;
+        hist_step(t, t < t_end ? p.ids[t] : 0);
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(status, LORA_DEV_BAD_ID);
     __syncthreads();
 
-    // ---- bucket totals, exclusive scan, per-warp running bases ------------
+    // ---- phase 2: bucket totals, exclusive scan, per-warp running bases ------
     int carry = 0;
     for (int b0 = 0; b0 < nb; b0 += kSegThreads) {
         const int b = b0 + tid;
         int tot = 0;
         if (b < nb)
-            for (int ww = 0; ww < 32; ++ww) tot += whist[ww * nb + b];
+            for (int ww = 0; ww < kSegWarps; ++ww) tot += whist[ww * nb + b];
         int total;
         const int ex = block_exclusive_scan(tot, wsum, &total);
         if (b < nb) {
             int run = carry + ex;
             bsum[b] = run;
-            for (int ww = 0; ww < 32; ++ww) {
+            for (int ww = 0; ww < kSegWarps; ++ww) {
                 const int c = whist[ww * nb + b];
                 whist[ww * nb + b] = run;
                 run += c;
@@ -121,16 +175,14 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
     __syncthreads();
     for (int b = tid; b <= nb; b += kSegThreads) p.offsets[b] = bsum[b];
 
-    // ---- pass 2: stable scatter -------------------------------------------
-    for (int64_t base = t_begin; base < t_end; base += 32) {
-        const int64_t t = base + lane;
+    // ---- phase 3a: stable scatter (every warp, its own tokens in order) ------
+    auto scatter_step = [&](int64_t t, int id) {
         const bool act = t < t_end;
         const unsigned amask = __ballot_sync(0xffffffffu, act);
         unsigned peers = 0;
         int b = 0;
         if (act) {
-            const int id = p.ids[t];
-            b = ((id >= 0 && id < p.A) ? id : -1) + 1;
+            b = id_bucket(id, A);
             peers = __match_any_sync(amask, b);
             const int below = __popc(peers & ((1u << lane) - 1u));
             p.perm[whist[w * nb + b] + below] = static_cast<int32_t>(t);
@@ -138,178 +190,221 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
         __syncwarp();
         if (act && lane == __ffs(peers) - 1) whist[w * nb + b] += __popc(peers);
         __syncwarp();
+    };
+    for (int64_t base = t_begin; base < t_end; base += 32) {
+        const int64_t t = base + lane;
+        scatter_step(t, t < t_end ? p.ids[t] : 0);
     }
 
-    // ---- segments: one per non-empty adapter bucket, ascending id ---------
-    carry = 0;
-    for (int i0 = 0; i0 < p.A; i0 += kSegThreads) {
-        const int i = i0 + tid;
-        const int cnt = i < p.A ? bsum[i + 2] - bsum[i + 1] : 0;
-        const int flag = cnt > 0;
-        int total;
-        const int ex = block_exclusive_scan(flag, wsum, &total);
-        if (flag) {
-            const int s = carry + ex;
-            const int rk = p.rank[i];
-            p.seg_id[s] = i;
-            p.seg_start[s] = bsum[i + 1];
-            p.seg_len[s] = cnt;
-            p.seg_rank[s] = rk;
-            s_id[s] = i;
-            s_start[s] = bsum[i + 1];
-            s_len[s] = cnt;
-            s_rank[s] = rk;
+    // ---- phase 3b: one list per warp (group) ---------------------------------
+    const unsigned lt_mask = (1u << lane) - 1u;
+    if (w == 0) {
+        // the segment table
+        int n = 0;
+        for (int i0 = 0; i0 < A; i0 += 32) {
+            const int i = i0 + lane;
+            const int cnt = i < A ? bsum[i + 2] - bsum[i + 1] : 0;
+            const unsigned m = __ballot_sync(0xffffffffu, cnt > 0);
+            if (cnt > 0) {
+                const int s = n + __popc(m & lt_mask);
+                p.seg_id[s] = i;
+                p.seg_start[s] = bsum[i + 1];
+                p.seg_len[s] = cnt;
+                p.seg_rank[s] = s_rank[i];
+            }
+            n += __popc(m);
         }
-        carry += total;
-    }
-    const int nseg = carry;
-    if (tid == 0) {
-        *p.num_segments = nseg;
-        p.hdr[HDR_NSEG] = nseg;
-    }
-    __syncthreads();
-
-    // ---- split-K chunk list: every rank panel of every adapter present ----
-    carry = 0;
-    for (int s0 = 0; s0 < nseg; s0 += kSegThreads) {
-        const int s = s0 + tid;
-        const int nc = s < nseg ? s_rank[s] / kChunk : 0;
-        int total;
-        const int ex = block_exclusive_scan(nc, wsum, &total);
-        if (s < nseg) {
-            const int i = s_id[s];
-            const int c = carry + ex;
+        if (lane == 0) {
+            *p.num_segments = n;
+            p.hdr[HDR_NSEG] = n;
+        }
+    } else if (w == 1) {
+        // split-K chunk list: every rank panel of every adapter present
+        int n = 0;
+        for (int i0 = 0; i0 < A; i0 += 32) {
+            const int i = i0 + lane;
+            const int nc = (i < A && bsum[i + 2] > bsum[i + 1]) ? s_rank[i] / kChunk : 0;
+            const int incl = warp_incl_scan(nc, lane);
+            const int c = n + incl - nc;
             for (int q = 0; q < nc; ++q) {
                 p.dchunk_arow[c + q] = s_arow[i] + kChunk * q;
                 p.dchunk_brow[c + q] = s_brow[i] + q * p.N;
                 p.dchunk_adapter[c + q] = i;
             }
+            n += __shfl_sync(0xffffffffu, incl, 31);
         }
-        carry += total;
-    }
-    if (tid == 0) p.hdr[HDR_DCHUNKS] = carry;
-
-    // ---- cluster schedule: each adapter's panels in groups of <= 2, and
-    //      the first panel of every segment -----------------------------------
-    carry = 0;
-    int carry_c2 = 0;
-    for (int s0 = 0; s0 < nseg; s0 += kSegThreads) {
-        const int s = s0 + tid;
-        const int nc = s < nseg ? s_rank[s] / kChunk : 0;
-        const int ng = (nc + 1) / 2;
-        int total, total_c;
-        const int exg = block_exclusive_scan(ng, wsum, &total);
-        const int exc = block_exclusive_scan(nc, wsum, &total_c);
-        if (s < nseg) {
-            const int c = carry_c2 + exc;
-            const int i = s_id[s];
-            p.dseg_first[s] = c;
-            p.dseg_group[s] = carry + exg;
-            for (int q = 0; q < ng; ++q) {
-                p.dgrp_first[carry + exg + q] = c + 2 * q;
-                p.dgrp_len[carry + exg + q] = min(2, nc - 2 * q);
-                p.dgrp_arow[carry + exg + q] = s_arow[i] + 2 * q * kChunk;
-                p.dgrp_adapter[carry + exg + q] = i;
+        if (lane == 0) p.hdr[HDR_DCHUNKS] = n;
+    } else if (w == 2) {
+        // stream schedule: windows of 8 pool panels (128 A rows / 128 B
+        // columns) that hold a panel of an adapter present; pinfo gives the
+        // adapter of each panel of a window, -1 where none is present
+        for (int i = lane; i < A; i += 32)
+            if (bsum[i + 2] > bsum[i + 1]) {
+                const int pp0 = s_brow[i] / p.N, np = s_rank[i] / kChunk;
+                for (int j = 0; j < np && pp0 + j < p.P; ++j) ptab[pp0 + j] = i;
             }
+        __syncwarp();
+        const int nwin_all = (p.P + 7) / 8;
+        int n = 0;
+        for (int w0 = 0; w0 < nwin_all; w0 += 32) {
+            const int wi = w0 + lane;
+            bool any = false;
+            if (wi < nwin_all)
+                for (int j = 0; j < 8; ++j) any |= (8 * wi + j < p.P) && ptab[8 * wi + j] >= 0;
+            const unsigned m = __ballot_sync(0xffffffffu, any);
+            if (any) {
+                const int k = n + __popc(m & lt_mask);
+                if (k < p.max_win) {
+                    p.ewin_first[k] = 8 * wi;
+                    for (int j = 0; j < 8; ++j) p.pinfo[8 * k + j] = 8 * wi + j < p.P ? ptab[8 * wi + j] : -1;
+                }
+            }
+            n += __popc(m);
         }
-        carry += total;
-        carry_c2 += total_c;
-    }
-    if (tid == 0) p.hdr[HDR_DGROUPS] = carry;
-    __syncthreads();
-
-    // ---- stream schedule: which panels of the B pool belong to adapters
-    //      present, in 8-panel windows (pool order).  ppinfo[p] = 2 * group +
-    //      half for a present panel p, -1 otherwise ----------------------------
-    int *ppinfo = whist;   // the histogram space is free again
-    for (int pp = tid; pp < p.P; pp += kSegThreads) ppinfo[pp] = -1;
-    __syncthreads();
-    for (int s = tid; s < nseg; s += kSegThreads) {
-        const int i = s_id[s];
-        const int pp0 = s_brow[i] / p.N;        // first pool panel of adapter i
-        const int np = s_rank[s] / kChunk;
-        const int g0 = p.dseg_group[s];
-        for (int j = 0; j < np; ++j) ppinfo[pp0 + j] = 2 * (g0 + j / 2) + (j & 1);
-    }
-    __syncthreads();
-    carry = 0;
-    const int nwin_all = (p.P + 7) / 8;
-    for (int w0 = 0; w0 < nwin_all; w0 += kSegThreads) {
-        const int w = w0 + tid;
-        int any = 0;
-        if (w < nwin_all)
-            for (int j = 0; j < 8 && 8 * w + j < p.P; ++j) any |= ppinfo[8 * w + j] >= 0;
-        int total;
-        const int ex = block_exclusive_scan(any, wsum, &total);
-        if (any) {
-            const int k = carry + ex;
-            p.ewin_first[k] = 8 * w;
-            for (int j = 0; j < 8; ++j) p.pinfo[8 * k + j] = 8 * w + j < p.P ? ppinfo[8 * w + j] : -1;
-        }
-        carry += total;
-    }
-    if (tid == 0) p.hdr[HDR_NWIN] = carry;
-
-    // ---- tiled schedule: per 128-token tile of the permuted order, the
-    //      rank panels of the segments it intersects, and its shrink jobs ---
-    int carry_c = 0, carry_j = 0;
-    for (int m0 = 0; m0 < p.num_mtiles; m0 += kSegThreads) {
-        const int m = m0 + tid;
-        int nch = 0, sfirst = 0;
+        if (lane == 0) p.hdr[HDR_NWIN] = n < p.max_win ? n : p.max_win;
+    } else if (p.num_mtiles <= kTileWarps) {
+        // tiled schedule, few tiles: warp (w - 3) builds tile m's chunk list,
+        // one lane per adapter bucket
+        const int m = w - kTileWarp0;
+        int *t_nch = wsum, *t_nj = wsum + 16;     // per-tile counts (<= 13 tiles)
         int64_t lo = 0, hi = 0;
+        int bfirst = A + 1, nch = 0;
         if (m < p.num_mtiles) {
             lo = static_cast<int64_t>(m) * kBM;
             hi = lo + kBM < p.M ? lo + kBM : p.M;
-            int L = 0, R = nseg;   // first segment whose end is past lo
+            int L = 1, R = A + 1;   // first adapter bucket that ends past lo
             while (L < R) {
                 const int mid = (L + R) >> 1;
-                if (s_start[mid] + s_len[mid] > lo) R = mid; else L = mid + 1;
+                if (bsum[mid + 1] > lo) R = mid; else L = mid + 1;
             }
-            sfirst = L;
-            for (int s = sfirst; s < nseg && s_start[s] < hi; ++s) nch += s_rank[s] / kChunk;
+            bfirst = L;
+            for (int b0 = bfirst; b0 <= A; b0 += 32) {
+                const int b = b0 + lane;
+                const bool in = b <= A && bsum[b] < hi;
+                int nc = (in && bsum[b + 1] > bsum[b]) ? s_rank[b - 1] / kChunk : 0;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) nc += __shfl_xor_sync(0xffffffffu, nc, o);
+                nch += nc;
+                if (__ballot_sync(0xffffffffu, in) != 0xffffffffu) break;
+            }
+            if (lane == 0) {
+                t_nch[m] = nch;
+                t_nj[m] = (nch + kMaxShrinkChunks - 1) / kMaxShrinkChunks;
+            }
         }
-        int totc, totj;
-        const int exc = block_exclusive_scan(nch, wsum, &totc);
-        const int nj = (nch + kMaxShrinkChunks - 1) / kMaxShrinkChunks;
-        const int exj = block_exclusive_scan(nj, wsum, &totj);
+        named_bar_sync(kTileBar, kTileWarps * 32);
         if (m < p.num_mtiles) {
-            int c = carry_c + exc;
-            const int cfirst = c;
-            p.tile_chunk_off[m] = c;
-            p.tile_njobs[m] = nj;
-            for (int s = sfirst; s < nseg && s_start[s] < hi; ++s) {
-                const int64_t s0 = s_start[s], s1 = s0 + s_len[s];
-                const int rlo = static_cast<int>((s0 > lo ? s0 : lo) - lo);
-                const int rhi = static_cast<int>((s1 < hi ? s1 : hi) - lo);
-                const int i = s_id[s];
-                for (int q = 0; q < s_rank[s] / kChunk; ++q, ++c) {
-                    p.chunk_arow[c] = s_arow[i] + kChunk * q;
-                    p.chunk_brow[c] = s_brow[i] + q * p.N;
-                    p.chunk_rng[c] = pack_rng(rlo, rhi, q);
+            int cbase = 0, jbase = 0;
+            for (int k = 0; k < m; ++k) {
+                cbase += t_nch[k];
+                jbase += t_nj[k];
+            }
+            int c = cbase;
+            for (int b0 = bfirst; b0 <= A; b0 += 32) {
+                const int b = b0 + lane;
+                const bool in = b <= A && bsum[b] < hi;
+                const bool live = in && bsum[b + 1] > bsum[b];
+                const int nc = live ? s_rank[b - 1] / kChunk : 0;
+                const int incl = warp_incl_scan(nc, lane);
+                if (live) {
+                    const int64_t s0 = bsum[b], s1 = bsum[b + 1];
+                    const int rlo = static_cast<int>((s0 > lo ? s0 : lo) - lo);
+                    const int rhi = static_cast<int>((s1 < hi ? s1 : hi) - lo);
+                    const int i = b - 1;
+                    for (int q = 0; q < nc; ++q) {
+                        const int cc = c + incl - nc + q;
+                        p.chunk_arow[cc] = s_arow[i] + kChunk * q;
+                        p.chunk_brow[cc] = s_brow[i] + q * p.N;
+                        p.chunk_rng[cc] = pack_rng(rlo, rhi, q);
+                    }
+                }
+                c += __shfl_sync(0xffffffffu, incl, 31);
+                if (__ballot_sync(0xffffffffu, in) != 0xffffffffu) break;
+            }
+            const int nj = t_nj[m];
+            if (lane == 0) {
+                p.tile_chunk_off[m] = cbase;
+                p.tile_njobs[m] = nj;
+            }
+            for (int q = lane; q < nj; q += 32) {
+                p.sjob_tile[jbase + q] = m;
+                p.sjob_c0[jbase + q] = cbase + kMaxShrinkChunks * q;
+                const int c1 = cbase + kMaxShrinkChunks * (q + 1);
+                p.sjob_c1[jbase + q] = c1 < cbase + nch ? c1 : cbase + nch;
+            }
+            if (m == p.num_mtiles - 1 && lane == 0) {
+                p.tile_chunk_off[p.num_mtiles] = cbase + nch;
+                p.hdr[HDR_NCHUNKS] = cbase + nch;
+                p.hdr[HDR_NSJOBS] = jbase + nj;
+            }
+        }
+    } else {
+        // tiled schedule, many tiles: per 128-token tile of the permuted
+        // order (one thread each), the rank panels of the segments it
+        // intersects (ascending adapter), and its shrink jobs of
+        // <= kMaxShrinkChunks panels
+        const int gt = tid - kTileWarp0 * 32;
+        int carry_c = 0, carry_j = 0;
+        for (int m0 = 0; m0 < p.num_mtiles; m0 += kTileWarps * 32) {
+            const int m = m0 + gt;
+            int nch = 0, bfirst = 1;
+            int64_t lo = 0, hi = 0;
+            if (m < p.num_mtiles) {
+                lo = static_cast<int64_t>(m) * kBM;
+                hi = lo + kBM < p.M ? lo + kBM : p.M;
+                int L = 1, R = A + 1;   // first adapter bucket that ends past lo
+                while (L < R) {
+                    const int mid = (L + R) >> 1;
+                    if (bsum[mid + 1] > lo) R = mid; else L = mid + 1;
+                }
+                bfirst = L;
+                for (int b = bfirst; b <= A && bsum[b] < hi; ++b)
+                    if (bsum[b + 1] > bsum[b]) nch += s_rank[b - 1] / kChunk;
+            }
+            const int nj = (nch + kMaxShrinkChunks - 1) / kMaxShrinkChunks;
+            int exc, exj, totc, totj;
+            tile_group_scan(nch, nj, wsum, &exc, &exj, &totc, &totj);
+            if (m < p.num_mtiles) {
+                int c = carry_c + exc;
+                const int cfirst = c;
+                p.tile_chunk_off[m] = c;
+                p.tile_njobs[m] = nj;
+                for (int b = bfirst; b <= A && bsum[b] < hi; ++b) {
+                    const int64_t s0 = bsum[b], s1 = bsum[b + 1];
+                    if (s1 == s0) continue;
+                    const int rlo = static_cast<int>((s0 > lo ? s0 : lo) - lo);
+                    const int rhi = static_cast<int>((s1 < hi ? s1 : hi) - lo);
+                    const int i = b - 1;
+                    for (int q = 0; q < s_rank[i] / kChunk; ++q, ++c) {
+                        p.chunk_arow[c] = s_arow[i] + kChunk * q;
+                        p.chunk_brow[c] = s_brow[i] + q * p.N;
+                        p.chunk_rng[c] = pack_rng(rlo, rhi, q);
+                    }
+                }
+                const int j = carry_j + exj;
+                for (int q = 0; q < nj; ++q) {
+                    p.sjob_tile[j + q] = m;
+                    p.sjob_c0[j + q] = cfirst + kMaxShrinkChunks * q;
+                    const int c1 = cfirst + kMaxShrinkChunks * (q + 1);
+                    p.sjob_c1[j + q] = c1 < cfirst + nch ? c1 : cfirst + nch;
                 }
             }
-            const int j = carry_j + exj;
-            for (int q = 0; q < nj; ++q) {
-                p.sjob_tile[j + q] = m;
-                p.sjob_c0[j + q] = cfirst + kMaxShrinkChunks * q;
-                const int c1 = cfirst + kMaxShrinkChunks * (q + 1);
-                p.sjob_c1[j + q] = c1 < cfirst + nch ? c1 : cfirst + nch;
-            }
+            carry_c += totc;
+            carry_j += totj;
         }
-        carry_c += totc;
-        carry_j += totj;
-    }
-    if (tid == 0) {
-        p.tile_chunk_off[p.num_mtiles] = carry_c;
-        p.hdr[HDR_NCHUNKS] = carry_c;
-        p.hdr[HDR_NSJOBS] = carry_j;
+        if (gt == 0) {
+            p.tile_chunk_off[p.num_mtiles] = carry_c;
+            p.hdr[HDR_NCHUNKS] = carry_c;
+            p.hdr[HDR_NSJOBS] = carry_j;
+        }
     }
 }
 
 size_t seg_build_smem_bytes(int32_t A)
 {
-    // the [32][A+1] histogram space is reused for the pool panel table (<= 4 A entries)
-    return static_cast<size_t>(32 * (A + 1) + (A + 2) + 32 + 6 * A) * 4;
+    // histograms, bucket offsets, scan scratch, three per-adapter tables and
+    // the pool panel table (<= 4 panels per adapter)
+    return static_cast<size_t>(kSegWarps * (A + 1) + (A + 2) + 32 + 3 * A + 4 * A) * 4;
 }
 
 cudaError_t launch_seg_build(const SegParams &p, cudaStream_t stream)
