@@ -320,6 +320,13 @@ def run_e2e(wl, s, L, device, steps, warmup, stream):
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
 
 
+def aggregate(ms_local: float, tokens_per_rank: int, world: int, all_reduce_max):
+    """Whole-job numbers of `world` independent replicas: the step time is the
+    slowest rank's, the throughput counts every rank's tokens."""
+    ms = all_reduce_max(ms_local)
+    return ms, world * tokens_per_rank / (ms * 1e-3)
+
+
 def cpu_baseline(name, budget_s=8.0):
     """The CPU oracle as it stands, on whole rows of the same workload."""
     from oracle import oracle
@@ -360,12 +367,14 @@ def ours(args):
     r = run_config(args.config, L, device, args.steps, args.warmup, stream, sampler=sampler,
                    dist_barrier=barrier)
     wl = r["wl"]
-    ms = r["ms_per_step"]
-    if dist:
-        t = torch.tensor([ms], device=device)
+    def all_reduce_max(v):
+        if not dist:
+            return v
+        t = torch.tensor([v], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * wl.M / (ms * 1e-3)
+        return float(t.item())
+
+    ms, value = aggregate(r["ms_per_step"], wl.M, world, all_reduce_max)
 
     # roofline of the dominant kernel (the fused layer)
     kern_s = r["kernel_ms"] * 1e-3

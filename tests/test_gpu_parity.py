@@ -130,6 +130,8 @@ def test_tiny_config_all_rows_both_paths():
     (33, 640, 1032, [48, 16, 64, 32], "uniform"),    # odd number of K blocks, 9 output tiles
     (64, 1024, 2048, [64] * 12 + [16] * 12, "uniform"),
     (16, 4096, 4096, [16, 32, 64] * 7, "uniform"),  # decode shapes, 21 adapters
+    (48, 192, 392, [16, 64, 32], "uniform"),         # 3 K blocks (half K unit), N ragged
+    (64, 512, 256, [16] * 64, "uniform"),            # ~40 adapters present: shrink slices span 3-4 windows
 ])
 def test_linear_small_shapes(path, M, K, N, ranks, mode):
     if path == L.LORA_PATH_STREAM and (M > 64 or K % 64):
