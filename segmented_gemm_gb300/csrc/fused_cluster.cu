@@ -30,11 +30,11 @@
 // The C partial tiles are then pushed with st.async into the CTA that owns
 // each 128/C-row slice (distributed shared memory, mbarrier byte counting);
 // the owner sums them, adds the bias and writes y.
-// Roles (320 threads): warp 0 TMA producer, warp 1 TMEM allocator + MMA
-// issuer, warps 2..5 epilogue (warp 2 also reads the metadata), warps 6..9
-// loaders of the token-side operands (x by cp.async, S by
-// load-convert-store).  All waits are bounded; the host only launches the
-// grid when every cluster can be resident at once.
+// Roles (320 threads): warp 0 TMA producer (the weight box and the x box of
+// each unit, B windows), warp 1 TMEM allocator + MMA issuer, warps 2..5
+// epilogue (warp 2 also derives the metadata), warps 6..9 stage the S
+// operand of the expand units (load-convert-store).  All waits are bounded;
+// the host only launches the grid when every cluster can be resident at once.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -45,7 +45,9 @@ namespace lora {
 
 constexpr int kClThreads = 320;
 constexpr int kClWArea = 32 * 1024;        // one W / A / B box
-constexpr int kClMisc = 4096;              // barriers, segment list, window tables, bias
+constexpr int kClMisc = 5120;              // barriers, segment list, window tables, bias
+constexpr int kStMaxWinAll = 512;          // windows of the pool (bitmap of 16 words)
+constexpr int kStMaxWinList = 2 * kStreamMaxTokens;   // windows a batch can touch
 constexpr int kClMaxStages = 8;
 constexpr int kStMaxSegs = 8;
 constexpr int kStMaxRegions = 16;
@@ -56,6 +58,10 @@ constexpr int kBarMeta = 1;                // named barrier: metadata ready (eve
 constexpr int kBarMma = 2;                 // named barrier: metadata ready (MMA issuer + warp 2)
 constexpr int kBarLoad = 3;                // named barrier: the four loader warps
 constexpr int kBarEpi = 4;                 // named barrier: the four epilogue warps
+constexpr int kBarInit = 5;                // named barrier: ring barriers initialised (warp 0 -> loaders)
+constexpr int kBarTmem = 6;                // named barrier: TMEM allocated (warps 0..5; the loaders never read it)
+constexpr int kBarTables = 7;              // named barrier: panel tables ready (warp 2 -> every warp but the MMA issuer)
+constexpr int kStFirst = 3;                // K units issued before the metadata is known
 constexpr int kMetaThreads = kClThreads - 32;
 
 enum StKind { kStBase = 0, kStShrink = 1, kStExpand = 2 };
@@ -102,31 +108,16 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
     return r;
 }
 
-// x K blocks kb0, kb0 + 1 of all T token rows into a slot: [kb][T rows][64],
-// 128-byte swizzle (chunk c of row r at r*128 + (c ^ (r & 7))*16); rows >= M
-// and K blocks past K are zero.  `lt` is the thread's index among the 128
-// loader threads.
-__device__ __forceinline__ void load_x_unit(uint8_t *xa, const ClusterParams &p, int T, int kb0, int lt)
-{
-    const int pieces = 2 * T * 8;
-    for (int pc = lt; pc < pieces; pc += 128) {
-        const int j = pc / (T * 8), rem = pc - j * T * 8;
-        const int row = rem >> 3, c = rem & 7;
-        const int kb = kb0 + j;
-        const bool ok = row < p.M && kb < p.kblocks;
-        const uint16_t *src = p.x + (ok ? static_cast<int64_t>(row) * p.K + kb * kBK + c * 8 : 0);
-        cp_async16(xa + j * T * 128 + row * 128 + ((c ^ (row & 7)) << 4), src, ok ? 16u : 0u);
-    }
-}
-
 __global__ void __launch_bounds__(kClThreads, 1)
     lora_cluster_kernel(const __grid_constant__ CUtensorMap tm_w3, const __grid_constant__ CUtensorMap tm_a3,
-                        const __grid_constant__ CUtensorMap tm_b3, const ClusterParams p)
+                        const __grid_constant__ CUtensorMap tm_b3, const __grid_constant__ CUtensorMap tm_x3,
+                        const ClusterParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int T = p.T_pad;
     const int slot_bytes = kClWArea + T * 256;    // [W / A / B box | token operand]
+    const uint32_t unit_tx = kClWArea + T * 256;   // a base / shrink unit: weight box + x box
     float *red = reinterpret_cast<float *>(smem + p.stages * slot_bytes);   // [C][128/C][T]
     uint64_t *full = reinterpret_cast<uint64_t *>(red + kSplitBN * T);
     uint64_t *empty = full + kClMaxStages;
@@ -144,6 +135,9 @@ __global__ void __launch_bounds__(kClThreads, 1)
     int *s_win_info = s_win_panel + kStMaxWinCta;      // [kStMaxWinCta][8] adapter of each panel, -1 if absent
     int *s_run_info = s_win_info + kStMaxWinCta * kStWin;   // [kStMaxRuns][8] the same for my shrink windows
     int *s_zero = s_run_info + kStMaxRuns * kStWin;    // [kStMaxWinCta] I am the window's last consumer
+    unsigned *s_wbits = reinterpret_cast<unsigned *>(s_zero + kStMaxWinCta);   // [16] windows touched
+    int *s_wpre = reinterpret_cast<int *>(s_wbits + kStMaxWinAll / 32);       // [16] popcount prefix
+    int *s_wlist = s_wpre + kStMaxWinAll / 32;         // [kStMaxWinList] windows touched, ascending
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, cta = blockIdx.x;
@@ -153,7 +147,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     int32_t *status = p.counters + CNT_STATUS;
     const int KU2 = (p.kblocks + 1) / 2;          // K units of 2 K blocks
     const int b0 = (KU2 * q) / C, b1 = (KU2 * (q + 1)) / C;
-    const int nfirst = min(p.stages, b1 - b0);
+    const int nfirst = min(min(p.stages, kStFirst), b1 - b0);
     const int rpo = kSplitBN / C;                 // output rows owned by each CTA of the cluster
     // window k's arrival counter is wcnt[k * kWinCntStride], its consumer
     // counter sits in the other half of the same 128-byte line
@@ -161,7 +155,12 @@ __global__ void __launch_bounds__(kClThreads, 1)
     int32_t *wcnt = p.wcnt;
     int32_t *ccnt = p.wcnt + kCntStride / 2;
 
-    // ---- prologue: nothing here depends on the segment builder ----------------
+    // ---- prologue: nothing in this kernel depends on the segment builder ------
+    int id0 = -1, id1 = -1;   // warp 2: the ids of tokens lane, lane + 32 (inputs; loaded first)
+    if (warp == 2) {
+        id0 = lane < p.M ? p.ids[lane] : -2;
+        id1 = lane + 32 < p.M ? p.ids[lane + 32] : -2;
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&full[s], 1 + 128);   // producer's expect_tx arrive + one arrive per loader thread
@@ -172,9 +171,16 @@ __global__ void __launch_bounds__(kClThreads, 1)
         *abort_flag = 0;
         mbar_expect_tx(red_full, static_cast<uint32_t>(kSplitBN * T * 4));   // the C partials of my rows
         fence_mbarrier_init();
+    }
+    if (warp == 0) {
+        __syncwarp();
+        named_bar_arrive(kBarInit, 160);   // the loaders may arrive on the ring barriers now
+    }
+    if (threadIdx.x == 0) {
         for (int i = 0; i < nfirst; ++i) {
-            mbar_expect_tx(&full[i], kClWArea);
+            mbar_expect_tx(&full[i], unit_tx);
             tma_load_3d_st(smem + i * slot_bytes, &tm_w3, &full[i], 0, n0, 2 * (b0 + i));
+            tma_load_3d_st(smem + i * slot_bytes + kClWArea, &tm_x3, &full[i], 0, 0, 2 * (b0 + i));
         }
         tma_prefetch_map(&tm_a3);
         tma_prefetch_map(&tm_b3);
@@ -183,61 +189,68 @@ __global__ void __launch_bounds__(kClThreads, 1)
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
-    if (threadIdx.x >= 64 && threadIdx.x < 128) {   // token ids
-        const int t = threadIdx.x - 64;
-        s_ids[t] = t < p.M ? p.ids[t] : -2;
+    if (warp >= 6) {   // the first units need no token-side staging
+        named_bar_sync(kBarInit, 160);
+        for (int i = 0; i < nfirst; ++i) mbar_arrive(&full[i]);
     }
-    if (threadIdx.x >= 128 && threadIdx.x < 128 + rpo / 8) {   // bias of the rows this CTA finishes
-        const int k = threadIdx.x - 128;
-        const int n = n0 + q * rpo + 8 * k;
-        uint4 b = make_uint4(0u, 0u, 0u, 0u);
-        if (p.bias && n < p.N) b = __ldg(reinterpret_cast<const uint4 *>(p.bias + n));
-        reinterpret_cast<uint4 *>(s_bias)[k] = b;
+    if (warp < 6) {
+        tc_fence_before();
+        named_bar_sync(kBarTmem, 192);
+        tc_fence_after();
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+    pdl_launch_dependents();   // a dependent launch may start its prologue on the idle SMs
     cluster_arrive();          // my barriers are initialised; peers wait for this before any st.async
-    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tmem_base = warp < 6 ? *tmem_slot : 0u;
 
     if (warp == 0) {
         // ===================== TMA producer: W, A and B boxes ================
         named_bar_sync(kBarMeta, kMetaThreads);
         const int ns = *n_segs;
         uint32_t it = nfirst;
+        bool tables = false;
         for (int si = 1; si < ns; ++si) {
             const StSeg sg = segs[si];
+            if (sg.kind == kStExpand && !tables) {
+                named_bar_sync(kBarTables, kMetaThreads);   // s_win_panel
+                tables = true;
+            }
             for (int u = sg.a; u < sg.b; ++u, ++it) {
                 const int s = it % p.stages;
                 const uint32_t round = it / p.stages;
                 if (lane == 0) {
                     if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
                     uint8_t *wa = smem + s * slot_bytes;
-                    mbar_expect_tx(&full[s], kClWArea);
-                    if (sg.kind == kStShrink) tma_load_3d_st(wa, &tm_a3, &full[s], 0, sg.arow, 2 * u);
-                    else if (sg.kind == kStBase) tma_load_3d_st(wa, &tm_w3, &full[s], 0, n0, 2 * u);
-                    else tma_load_3d_st(wa, &tm_b3, &full[s], 0, n0, s_win_panel[u - sg.a]);
+                    if (sg.kind == kStExpand) {
+                        mbar_expect_tx(&full[s], kClWArea);
+                        tma_load_3d_st(wa, &tm_b3, &full[s], 0, n0, s_win_panel[u - sg.a]);
+                    } else {
+                        mbar_expect_tx(&full[s], unit_tx);
+                        if (sg.kind == kStShrink) tma_load_3d_st(wa, &tm_a3, &full[s], 0, sg.arow, 2 * u);
+                        else tma_load_3d_st(wa, &tm_w3, &full[s], 0, n0, 2 * u);
+                        tma_load_3d_st(wa + kClWArea, &tm_x3, &full[s], 0, 0, 2 * u);
+                    }
                 }
                 __syncwarp();
             }
         }
+        if (!tables) named_bar_sync(kBarTables, kMetaThreads);
     } else if (warp >= 6) {
         // ===================== loaders: token-side operands ==================
         const int lt = threadIdx.x - 192;
-        for (int i = 0; i < nfirst; ++i) {      // x of the first units: inputs only
-            load_x_unit(smem + i * slot_bytes + kClWArea, p, T, 2 * (b0 + i), lt);
-            cp_async_mbar_arrive_noinc(&full[i]);
-        }
-        pdl_wait();
         named_bar_sync(kBarMeta, kMetaThreads);
         const int ns = *n_segs;
+        int ew0 = 0, ew1 = 0;   // my expand windows
+        if (ns > 1 && segs[ns - 1].kind == kStExpand) {
+            ew0 = segs[ns - 1].a;
+            ew1 = segs[ns - 1].b;
+        }
         uint32_t it = nfirst;
-        int ew0 = 0, ew1 = 0;
+        bool tables = false;
         for (int si = 1; si < ns; ++si) {
             const StSeg sg = segs[si];
             if (sg.kind == kStExpand) {
-                ew0 = sg.a;
-                ew1 = sg.b;
+                named_bar_sync(kBarTables, kMetaThreads);   // s_win_info
+                tables = true;
                 // every window of my share must be complete: one lane per
                 // window waits, so the checks overlap
                 for (int k = sg.a + lane; k < sg.b; k += 32)
@@ -251,8 +264,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 __syncwarp();
                 uint8_t *xa = smem + s * slot_bytes + kClWArea;
                 if (sg.kind != kStExpand) {
-                    load_x_unit(xa, p, T, 2 * u, lt);
-                    cp_async_mbar_arrive_noinc(&full[s]);
+                    mbar_arrive(&full[s]);   // x arrives by TMA with the weight box
                 } else {
                     // S panels [8][T rows][16], 32-byte swizzle (chunk c of
                     // row t at t*32 + (c ^ ((t >> 2) & 1))*16)
@@ -295,7 +307,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 }
             }
         }
-        cp_async_wait_all();
+        if (!tables) named_bar_sync(kBarTables, kMetaThreads);
         if (ew1 > ew0) {
             // my reads of the window sums are done: count myself as a
             // consumer; the last of the NT consumers of a window clears it
@@ -382,56 +394,118 @@ __global__ void __launch_bounds__(kClThreads, 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int et = threadIdx.x - 64;
-        pdl_wait();
+        if (threadIdx.x >= 160 && threadIdx.x < 160 + rpo / 8) {   // bias of the rows this CTA finishes
+            const int k = threadIdx.x - 160;
+            const int n = n0 + q * rpo + 8 * k;
+            uint4 b = make_uint4(0u, 0u, 0u, 0u);
+            if (p.bias && n < p.N) b = __ldg(reinterpret_cast<const uint4 *>(p.bias + n));
+            reinterpret_cast<uint4 *>(s_bias)[k] = b;
+        }
         if (warp == 2) {
-            // ---- metadata: the segment list of this CTA ----------------------
-            int NW = p.hdr[HDR_NWIN];
-            if (NW > p.max_win_str) {     // cannot happen for a table built for this call
-                if (lane == 0) atomicOr(status, LORA_DEV_TIMEOUT);
-                NW = p.max_win_str;
+            // ---- metadata: the pool windows this batch touches, from
+            // lora_id_map and the pool table (one more round of loads) -------
+            const bool v0 = id0 >= 0 && id0 < p.A, v1 = id1 >= 0 && id1 < p.A;
+            const int64_t ao0 = v0 ? p.a_offset[id0] : 0, ao1 = v1 ? p.a_offset[id1] : 0;
+            const int rk0 = v0 ? p.rank[id0] : 0, rk1 = v1 ? p.rank[id1] : 0;
+            s_ids[lane] = id0;
+            s_ids[lane + 32] = id1;
+            if (lane < kStMaxWinAll / 32) s_wbits[lane] = 0u;
+            __syncwarp();
+            // token's adapter: pool panels [pa, pa + np), in windows pa/8 .. (pa+np-1)/8
+            const int pa0 = static_cast<int>(ao0 / p.K) / kChunk, np0 = min(rk0 / kChunk, LORA_MAX_RANK / kChunk);
+            const int pa1 = static_cast<int>(ao1 / p.K) / kChunk, np1 = min(rk1 / kChunk, LORA_MAX_RANK / kChunk);
+            auto mark = [&](int pa, int np) {
+                if (np <= 0) return;
+                for (int wv = pa / kStWin; wv <= (pa + np - 1) / kStWin && wv < p.windows_all; ++wv)
+                    atomicOr(&s_wbits[wv >> 5], 1u << (wv & 31));
+            };
+            mark(pa0, np0);
+            mark(pa1, np1);
+            __syncwarp();
+            const unsigned bits = lane < kStMaxWinAll / 32 ? s_wbits[lane] : 0u;
+            const int cnt = __popc(bits);
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
             }
+            const int NW = __shfl_sync(0xffffffffu, incl, 31);   // <= 2 windows per token
+            if (lane < kStMaxWinAll / 32) s_wpre[lane] = incl - cnt;
+            for (unsigned b = bits, k = incl - cnt; b; b &= b - 1, ++k) s_wlist[k] = 32 * lane + __ffs(b) - 1;
+            __syncwarp();
+            // ---- the segment list of this CTA ---------------------------------
+            // (32-bit: the host bounds windows x K units x grid below 2^31)
             const int w0 = (NW * q) / C, w1 = (NW * (q + 1)) / C;
-            if (lane == 0) {
-                int n = 0, region = 1, run = 0;
-                segs[n++] = {kStBase, b0, b0 + nfirst, 0, 0, 0};
-                const int64_t U = static_cast<int64_t>(NW) * KU2;
-                for (int64_t u = (U * cta) / G, u1 = (U * (cta + 1)) / G; u < u1;) {
-                    const int wi = static_cast<int>(u / KU2);
-                    const int64_t e = min(u1, static_cast<int64_t>(wi + 1) * KU2);
-                    if (run >= kStMaxRuns || region >= p.max_regions) {   // the host rules this out
+            const int wend = min(w1, w0 + kStMaxWinCta);
+            int n = 0, region = 1, run = 0;
+            int run_w[kStMaxRuns] = {-1, -1, -1, -1};
+            if (lane == 0) segs[0] = {kStBase, b0, b0 + nfirst, 0, 0, 0};
+            ++n;
+            const int U = NW * KU2;
+            for (int u = (U * cta) / G, u1 = (U * (cta + 1)) / G; u < u1;) {
+                const int wi = u / KU2;
+                const int e = min(u1, (wi + 1) * KU2);
+                if (run >= kStMaxRuns || region >= p.max_regions) {   // the host rules this out
+                    if (lane == 0) {
                         atomicOr(status, LORA_DEV_TIMEOUT);
                         *abort_flag = 1;
-                        break;
                     }
-                    segs[n++] = {kStShrink, static_cast<int>(u - static_cast<int64_t>(wi) * KU2),
-                                 static_cast<int>(e - static_cast<int64_t>(wi) * KU2), wi, region++,
-                                 kChunk * p.ewin_first[wi]};
-                    ++run;
-                    u = e;
+                    break;
                 }
-                if (b1 > b0 + nfirst) segs[n++] = {kStBase, b0 + nfirst, b1, 0, 0, 0};
-                if (w1 - w0 > kStMaxWinCta) {   // the host rules this out
-                    atomicOr(status, LORA_DEV_TIMEOUT);
-                    *abort_flag = 1;
-                }
-                if (w1 > w0) segs[n++] = {kStExpand, w0, min(w1, w0 + kStMaxWinCta), 0, 0, 0};
+                if (lane == 0) segs[n] = {kStShrink, u - wi * KU2, e - wi * KU2, wi, region, kChunk * kStWin * s_wlist[wi]};
+                run_w[run] = wi;
+                ++n;
+                ++region;
+                ++run;
+                u = e;
+            }
+            if (b1 > b0 + nfirst) {
+                if (lane == 0) segs[n] = {kStBase, b0 + nfirst, b1, 0, 0, 0};
+                ++n;
+            }
+            if (w1 - w0 > kStMaxWinCta && lane == 0) {   // the host rules this out
+                atomicOr(status, LORA_DEV_TIMEOUT);
+                *abort_flag = 1;
+            }
+            if (w1 > w0) {
+                if (lane == 0) segs[n] = {kStExpand, w0, wend, 0, 0, 0};
+                ++n;
+            }
+            if (lane == 0) {
                 *n_segs = n;
                 *out_empty = (b1 == b0 && w1 == w0);
             }
             __syncwarp();
-            // window tables, one lane per entry
-            for (int k = lane; k < min(w1 - w0, kStMaxWinCta); k += 32) s_win_panel[k] = p.ewin_first[w0 + k];
-            for (int k = lane; k < min(w1 - w0, kStMaxWinCta) * kStWin; k += 32)
-                s_win_info[k] = p.pinfo[w0 * kStWin + k];
-            const int nseg = *n_segs;
-            for (int k = lane; k < kStMaxRuns * kStWin; k += 32) {
-                const int si = 1 + k / kStWin;
-                s_run_info[k] = (si < nseg && segs[si].kind == kStShrink) ? p.pinfo[segs[si].w * kStWin + k % kStWin] : -1;
-            }
-            __syncwarp();
             named_bar_arrive(kBarMma, 64);
+            named_bar_arrive(kBarMeta, kMetaThreads);   // the producer may issue the shrink boxes now
+            // ---- panel tables (needed at the shrink epilogue and the expand) ---
+            for (int k = w0 + lane; k < wend; k += 32) s_win_panel[k - w0] = kStWin * s_wlist[k];
+            for (int k = lane; k < (wend - w0) * kStWin; k += 32) s_win_info[k] = -1;
+            s_run_info[lane] = -1;   // kStMaxRuns x kStWin = 32 entries
+            __syncwarp();
+            // the adapter owning each panel of my windows (absent panels stay -1)
+            auto fill = [&](int id, int pa, int np) {
+                if (np <= 0) return;
+                for (int wv = pa / kStWin; wv <= (pa + np - 1) / kStWin && wv < p.windows_all; ++wv) {
+                    const int pos = s_wpre[wv >> 5] + __popc(s_wbits[wv >> 5] & ((1u << (wv & 31)) - 1u));
+                    const int lo = max(pa, kStWin * wv), hi = min(pa + np, kStWin * wv + kStWin);
+                    if (pos >= w0 && pos < wend)
+                        for (int pp = lo; pp < hi; ++pp) s_win_info[(pos - w0) * kStWin + pp - kStWin * wv] = id;
+                    for (int r = 0; r < kStMaxRuns; ++r)
+                        if (run_w[r] == pos)
+                            for (int pp = lo; pp < hi; ++pp) s_run_info[r * kStWin + pp - kStWin * wv] = id;
+                }
+            };
+            fill(id0, pa0, np0);
+            fill(id1, pa1, np1);
+            __syncwarp();
+            named_bar_arrive(kBarTables, kMetaThreads);
         }
-        named_bar_sync(kBarMeta, kMetaThreads);
+        if (warp != 2) {
+            named_bar_sync(kBarMeta, kMetaThreads);
+            named_bar_sync(kBarTables, kMetaThreads);   // s_run_info
+        }
         const int ns = *n_segs;
         // ---- shrink runs: add my partial window sums, then release ------------
         for (int si = 1, run = 0; si < ns; ++si) {
@@ -517,6 +591,9 @@ __global__ void __launch_bounds__(kClThreads, 1)
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, 512);
     cluster_wait();            // no CTA leaves while a peer may still touch its shared memory
+    // when launched right after the segment builder as a programmatic
+    // dependent, finish only after it (stream order for what follows)
+    if (threadIdx.x == 0) pdl_wait();
 }
 
 int cluster_max_regions() { return kStMaxRegions; }
@@ -595,7 +672,7 @@ cudaError_t launch_cluster(const ClusterMaps &m, const ClusterParams &p, bool pd
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, lora_cluster_kernel, m.w3, m.a3, m.b3, p);
+    return cudaLaunchKernelEx(&cfg, lora_cluster_kernel, m.w3, m.a3, m.b3, m.x3, p);
 }
 
 }  // namespace lora

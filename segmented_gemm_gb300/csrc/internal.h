@@ -41,7 +41,6 @@ enum PlanHdr {
     HDR_NSJOBS = 1,       // shrink jobs of the tiled schedule
     HDR_DCHUNKS = 2,      // chunks of the split-K schedule (adapters present)
     HDR_NSEG = 3,         // number of segments
-    HDR_NWIN = 5,         // stream schedule: 128-row windows of the pools holding panels of adapters present
     HDR_WORDS = 16
 };
 
@@ -67,9 +66,8 @@ struct WsLayout {
     size_t hdr, tile_chunk_off, chunk_arow, chunk_brow, chunk_rng;
     size_t sjob_tile, sjob_c0, sjob_c1, tile_njobs;
     size_t dchunk_arow, dchunk_brow, dchunk_adapter;
-    size_t ewin_first, pinfo, wcnt, acc_str, acc_str_bytes;
-    int32_t max_win;          // window-list capacity (all windows of the pool)
-    int32_t max_win_str;      // windows the stream schedule's sums can hold (M <= 64)
+    size_t wcnt, acc_str, acc_str_bytes;
+    int32_t max_win_str;      // windows the stream schedule's sums and counters can hold (M <= 64)
     size_t s_scratch, s_scratch_bytes;
     size_t acc_out, acc_out_bytes, acc_shr, acc_shr_bytes;
     size_t total;
@@ -122,6 +120,7 @@ struct SplitParams {
 
 struct ClusterMaps {
     CUtensorMap w3, a3, b3;    // W, A pool: {64, 128 rows, 2 K blocks}; B pool: {16, 128 rows, 8 panels}
+    CUtensorMap x3;            // x: {64, T rows, 2 K blocks} (rows past M read as zeros)
 };
 
 struct ClusterParams {
@@ -129,12 +128,14 @@ struct ClusterParams {
     int32_t N, K, T_pad, C, NT, kblocks, stages, max_regions, max_win_str;
     float scale;
     const uint16_t *bias;
-    const uint16_t *x;         // bf16 [M, K] (read by the loader warps)
+    const uint16_t *x;         // bf16 [M, K] (read through the x tensor map)
     uint16_t *y;
-    const int32_t *ids, *hdr, *ewin_first, *pinfo;
+    const int32_t *ids;
+    const int64_t *a_offset;   // the pool table (device): first A pool element of each adapter
+    const int32_t *rank;       // padded rank of each adapter
+    int32_t A, windows_all;    // adapters; 128-row windows in the pool
     float *acc;                // fp32 [windows][T_pad][128]: per-window sums of S (zero at rest)
     int32_t *wcnt;             // [windows][kWinCntStride]: shrink arrivals at 0, consumer CTAs at 16 (zero at rest)
-    int32_t max_win;
     int32_t *counters;
 };
 
@@ -149,10 +150,6 @@ struct SegParams {
     int32_t *hdr, *tile_chunk_off, *chunk_arow, *chunk_brow, *chunk_rng;
     int32_t *sjob_tile, *sjob_c0, *sjob_c1, *tile_njobs;
     int32_t *dchunk_arow, *dchunk_brow, *dchunk_adapter;
-    int32_t *ewin_first, *pinfo;
-    int32_t P;                 // panels in the pools (b_elems / (16 N))
-    int32_t max_win;           // window-list capacity
-    int32_t *wcnt;             // [max_win][kWinCntStride] stream-schedule window counters, zeroed here
     int32_t *counters;
     int32_t n_counters;
 };

@@ -156,11 +156,9 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
     L.dchunk_adapter = take(static_cast<size_t>(L.max_dchunks) * 4);
     // stream schedule: windows of 8 pool panels.  An adapter's <= 4 panels
     // span at most 2 windows, so a batch touches <= 2 * min(A, M) of them.
-    L.max_win = (4 * A + 7) / 8 + 1;
-    L.max_win_str = static_cast<int32_t>(std::min<int64_t>(L.max_win, 2 * present));
-    L.ewin_first = take(static_cast<size_t>(L.max_win) * 4);
-    L.pinfo = take(static_cast<size_t>(L.max_win) * 8 * 4);
-    L.wcnt = take(static_cast<size_t>(L.max_win) * kWinCntStride * 4);
+    L.max_win_str = M <= kStreamMaxTokens
+                        ? static_cast<int32_t>(std::min<int64_t>((4 * A + 7) / 8, 2 * present)) : 0;
+    L.wcnt = take(static_cast<size_t>(std::max(L.max_win_str, 1)) * kWinCntStride * 4);
     L.acc_str_bytes = M <= kStreamMaxTokens
                           ? static_cast<size_t>(std::max(L.max_win_str, 1)) * split_tpad(M) * kSplitBN * 4 : 16;
     L.acc_str = take(L.acc_str_bytes);
@@ -248,11 +246,6 @@ static int enqueue_segments(const int32_t *ids, int64_t M, const lora_pool_t *po
     p.dchunk_arow = at<int32_t>(ws, L.dchunk_arow);
     p.dchunk_brow = at<int32_t>(ws, L.dchunk_brow);
     p.dchunk_adapter = at<int32_t>(ws, L.dchunk_adapter);
-    p.ewin_first = at<int32_t>(ws, L.ewin_first);
-    p.pinfo = at<int32_t>(ws, L.pinfo);
-    p.P = pool->num_adapters ? static_cast<int32_t>(pool->b_elems / (static_cast<int64_t>(kChunk) * pool->N)) : 0;
-    p.max_win = L.max_win;
-    p.wcnt = at<int32_t>(ws, L.wcnt);
     p.counters = at<int32_t>(ws, L.counters);
     p.n_counters = static_cast<int32_t>(L.n_counters);
     return launch_seg_build(p, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
@@ -450,6 +443,10 @@ static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, co
     const int64_t runs = (u_cta + KU2 - 1) / KU2 + 1;
     if (runs > cluster_max_runs() || runs + 1 > max_regions) return -1;
     if ((L.max_win_str + C - 1) / C > cluster_max_win_cta()) return -1;
+    if (static_cast<int64_t>(std::max(L.max_win_str, 1)) * KU2 * grid >= (int64_t(1) << 31)) return -1;   // 32-bit slicing
+    const uint64_t panels =
+        pool->num_adapters ? static_cast<uint64_t>(pool->b_elems / (static_cast<int64_t>(kChunk) * pool->N)) : 1;
+    if ((panels + cluster_win() - 1) / cluster_win() > 512) return -1;   // the kernel's window bitmap
     ClusterParams p;
     std::memset(&p, 0, sizeof p);
     p.M = M;
@@ -462,15 +459,15 @@ static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, co
     p.stages = cluster_stages(T);
     p.max_regions = max_regions;
     p.max_win_str = L.max_win_str;
-    p.max_win = L.max_win;
+    p.A = pool->num_adapters;
+    p.a_offset = pool->a_offset;
+    p.rank = pool->rank;
+    p.windows_all = static_cast<int32_t>((panels + cluster_win() - 1) / cluster_win());
     p.scale = scale;
     p.bias = bias;
     p.x = x;
     p.y = y;
     p.ids = ids;
-    p.hdr = at<int32_t>(ws, L.hdr);
-    p.ewin_first = at<int32_t>(ws, L.ewin_first);
-    p.pinfo = at<int32_t>(ws, L.pinfo);
     p.acc = at<float>(ws, L.acc_str);
     p.wcnt = at<int32_t>(ws, L.wcnt);
     p.counters = at<int32_t>(ws, L.counters);
@@ -478,12 +475,13 @@ static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, co
     ClusterMaps m;
     const CUtensorMapSwizzle s128 = CU_TENSOR_MAP_SWIZZLE_128B, s32 = CU_TENSOR_MAP_SWIZZLE_32B;
     if (!encode_3d(&m.w3, W, kBK, N, KB, K * 2, kBK * 2, kBK, kSplitBN, 2, s128)) return LORA_ERR_CUDA;
+    if (!encode_3d(&m.x3, x, kBK, static_cast<uint64_t>(M), KB, K * 2, kBK * 2, kBK, static_cast<uint32_t>(T), 2, s128))
+        return LORA_ERR_CUDA;
     const void *apool = pool->num_adapters ? static_cast<const void *>(pool->a_pool) : static_cast<const void *>(W);
     const uint64_t arows = pool->num_adapters ? static_cast<uint64_t>(pool->a_elems / pool->K) : 1;
     if (!encode_3d(&m.a3, apool, kBK, arows, KB, K * 2, kBK * 2, kBK, kSplitBN, 2, s128)) return LORA_ERR_CUDA;
     const void *bpool = pool->num_adapters ? static_cast<const void *>(pool->b_pool) : static_cast<const void *>(W);
-    const uint64_t panels =
-        pool->num_adapters ? static_cast<uint64_t>(pool->b_elems / (static_cast<int64_t>(kChunk) * N)) : 1;
+
     if (!encode_3d(&m.b3, bpool, kChunk, N, panels, kChunk * 2, N * kChunk * 2, kChunk, kSplitBN, cluster_win(), s32))
         return LORA_ERR_CUDA;
     return launch_cluster(m, p, pdl, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;

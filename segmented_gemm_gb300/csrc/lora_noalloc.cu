@@ -64,7 +64,7 @@ extern "C" int lora_linear_noalloc(const lora_bf16_t *x, int64_t M, const lora_b
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *base = static_cast<char *>(ws);
     const size_t zero_regions[][2] = {{L.counters, L.n_counters * 4},
-                                      {L.wcnt, static_cast<size_t>(L.max_win) * kWinCntStride * 4},
+                                      {L.wcnt, static_cast<size_t>(L.max_win_str) * kWinCntStride * 4},
                                       {L.acc_str, L.acc_str_bytes},
                                       {L.acc_out, L.acc_out_bytes},
                                       {L.acc_shr, L.acc_shr_bytes}};

@@ -16,11 +16,9 @@
 //              warp 0       the segment table (one segment per non-empty
 //                           adapter bucket, ascending id)
 //              warp 1       split-K chunk list (rank panels of adapters present)
-//              warp 2       stream-schedule windows: 128-row windows of the
-//                           adapter pools that hold panels of adapters present
-//              warps 3..15  tiled-schedule chunk lists and shrink jobs: one
+//              warps 2..15  tiled-schedule chunk lists and shrink jobs: one
 //                           warp per 128-token tile (a lane per adapter
-//                           bucket) when there are at most 13 tiles, else
+//                           bucket) when there are at most 14 tiles, else
 //                           one thread per tile
 // Bucket 0 holds id -1, bucket i+1 adapter i; ids outside [-1, A) are
 // counted as -1 and flagged in the status word.
@@ -34,9 +32,10 @@ namespace lora {
 
 constexpr int kSegThreads = 512;
 constexpr int kSegWarps = kSegThreads / 32;
-constexpr int kTileWarp0 = 3;                       // first warp of the tile-list group
+constexpr int kTileWarp0 = 2;                       // first warp of the tile-list group
 constexpr int kTileWarps = kSegWarps - kTileWarp0;
 constexpr int kTileBar = 1;                         // named barrier of the tile-list group
+static_assert(2 * kTileWarps <= 32 && kTileWarps <= 16, "tile-list scan scratch lives in the 32-int wsum");
 
 // Bucket of a token id: 0 for -1 and for ids outside [-1, A), else id + 1.
 __device__ __forceinline__ int id_bucket(int id, int A) { return (id >= 0 && id < A) ? id + 1 : 0; }
@@ -99,8 +98,11 @@ __device__ void tile_group_scan(int a, int b, int *ws2, int *ea, int *eb, int *t
 
 __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
 {
-    // the fused kernel that follows may start its prologue and its weight
-    // stream now; it waits for this grid before reading anything built here
+    // Let the fused kernel that follows start its prologue and weight stream
+    // now; it waits for this grid before reading anything built here.  (The
+    // wait is a no-op for an ordinary launch; it keeps the kernel correct
+    // should it ever be launched as a programmatic dependent itself.)
+    pdl_wait();
     pdl_launch_dependents();
 
     extern __shared__ int sm[];
@@ -111,7 +113,6 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
     int *s_rank = wsum + 32;                  // [A] padded ranks
     int *s_arow = s_rank + A;                 // [A] first A pool row (a_offset / K)
     int *s_brow = s_arow + A;                 // [A] b_offset / 16
-    int *ptab = s_brow + A;                   // [P] pool panel -> adapter present owning it, else -1
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     int32_t *status = p.counters + CNT_STATUS;
 
@@ -122,14 +123,12 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
     // ---- phase 0 -------------------------------------------------------------
     for (int i = tid; i < p.n_counters; i += kSegThreads)
         if (i != CNT_STATUS) p.counters[i] = 0;
-    for (int i = tid; i < p.max_win * kWinCntStride; i += kSegThreads) p.wcnt[i] = 0;
     for (int i = tid; i < kSegWarps * nb; i += kSegThreads) whist[i] = 0;
     for (int i = tid; i < A; i += kSegThreads) {
         s_rank[i] = p.rank[i];
         s_arow[i] = static_cast<int>(p.a_offset[i] / p.K);
         s_brow[i] = static_cast<int>(p.b_offset[i] / kChunk);
     }
-    for (int i = tid; i < p.P; i += kSegThreads) ptab[i] = -1;
     __syncthreads();
 
     // ---- phase 1: per-warp histograms ----------------------------------------
@@ -234,39 +233,11 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
             n += __shfl_sync(0xffffffffu, incl, 31);
         }
         if (lane == 0) p.hdr[HDR_DCHUNKS] = n;
-    } else if (w == 2) {
-        // stream schedule: windows of 8 pool panels (128 A rows / 128 B
-        // columns) that hold a panel of an adapter present; pinfo gives the
-        // adapter of each panel of a window, -1 where none is present
-        for (int i = lane; i < A; i += 32)
-            if (bsum[i + 2] > bsum[i + 1]) {
-                const int pp0 = s_brow[i] / p.N, np = s_rank[i] / kChunk;
-                for (int j = 0; j < np && pp0 + j < p.P; ++j) ptab[pp0 + j] = i;
-            }
-        __syncwarp();
-        const int nwin_all = (p.P + 7) / 8;
-        int n = 0;
-        for (int w0 = 0; w0 < nwin_all; w0 += 32) {
-            const int wi = w0 + lane;
-            bool any = false;
-            if (wi < nwin_all)
-                for (int j = 0; j < 8; ++j) any |= (8 * wi + j < p.P) && ptab[8 * wi + j] >= 0;
-            const unsigned m = __ballot_sync(0xffffffffu, any);
-            if (any) {
-                const int k = n + __popc(m & lt_mask);
-                if (k < p.max_win) {
-                    p.ewin_first[k] = 8 * wi;
-                    for (int j = 0; j < 8; ++j) p.pinfo[8 * k + j] = 8 * wi + j < p.P ? ptab[8 * wi + j] : -1;
-                }
-            }
-            n += __popc(m);
-        }
-        if (lane == 0) p.hdr[HDR_NWIN] = n < p.max_win ? n : p.max_win;
     } else if (p.num_mtiles <= kTileWarps) {
-        // tiled schedule, few tiles: warp (w - 3) builds tile m's chunk list,
+        // tiled schedule, few tiles: warp (w - 2) builds tile m's chunk list,
         // one lane per adapter bucket
         const int m = w - kTileWarp0;
-        int *t_nch = wsum, *t_nj = wsum + 16;     // per-tile counts (<= 13 tiles)
+        int *t_nch = wsum, *t_nj = wsum + 16;     // per-tile counts (<= 14 tiles)
         int64_t lo = 0, hi = 0;
         int bfirst = A + 1, nch = 0;
         if (m < p.num_mtiles) {
@@ -402,9 +373,8 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
 
 size_t seg_build_smem_bytes(int32_t A)
 {
-    // histograms, bucket offsets, scan scratch, three per-adapter tables and
-    // the pool panel table (<= 4 panels per adapter)
-    return static_cast<size_t>(kSegWarps * (A + 1) + (A + 2) + 32 + 3 * A + 4 * A) * 4;
+    // histograms, bucket offsets, scan scratch and three per-adapter tables
+    return static_cast<size_t>(kSegWarps * (A + 1) + (A + 2) + 32 + 3 * A) * 4;
 }
 
 cudaError_t launch_seg_build(const SegParams &p, cudaStream_t stream)
@@ -419,6 +389,8 @@ cudaError_t launch_seg_build(const SegParams &p, cudaStream_t stream)
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[dev] = 1;
     }
+    // an ordinary launch: measured faster than a programmatic dependent one
+    // here, whose waiting block delays the fused kernel's clusters
     seg_build_kernel<<<1, kSegThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
