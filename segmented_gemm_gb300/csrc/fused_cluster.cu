@@ -60,7 +60,9 @@ constexpr int kBarLoad = 3;                // named barrier: the four loader war
 constexpr int kBarEpi = 4;                 // named barrier: the four epilogue warps
 constexpr int kBarInit = 5;                // named barrier: ring barriers initialised (warp 0 -> loaders)
 constexpr int kBarTmem = 6;                // named barrier: TMEM allocated (warps 0..5; the loaders never read it)
-constexpr int kBarTables = 7;              // named barrier: panel tables ready (warp 2 -> every warp but the MMA issuer)
+constexpr int kBarTables = 7;              // named barrier: panel tables ready (warp 2 -> producer, MMA, loaders)
+constexpr int kBarTablesEpi = 8;           // named barrier: panel tables ready (warp 2 -> the other epilogue warps)
+constexpr int kTablesThreads = kClThreads - 96;   // warp 2 + warps 0, 1, 6..9
 constexpr int kStFirst = 3;                // K units issued before the metadata is known
 constexpr int kMetaThreads = kClThreads - 32;
 
@@ -99,12 +101,71 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint
 }
 
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+// Arrive without release semantics: used once the barriers a peer will
+// touch have been published with fence.mbarrier_init (a release arrive
+// would also wait for this thread's outstanding memory operations).
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Unit list of one CTA before its expand windows.  Shrink runs are the
+// CTA's slice of the (window, K unit) list of the whole grid; a shrunk
+// window is named by its index w in the list of windows shrunk (s_wlist
+// maps it to a pool window, identity when every window is shrunk).  With
+// shrink_first the order is [shrink runs][base], else [first base units]
+// [shrink runs][rest of base].  Written to segs when write.
+struct SegPlan {
+    int n, nruns;
+    int run_w[kStMaxRuns];
+    bool ok;
+};
+
+__device__ __forceinline__ SegPlan plan_segments(StSeg *segs, bool write, int NW, int KU2, int G, int cta, int b0,
+                                                 int b1, int nbase_first, int max_regions, const int *s_wlist,
+                                                 bool shrink_first)
+{
+    SegPlan r;
+    int n = 0, region = 1;
+    r.nruns = 0;
+    r.ok = true;
+    for (int i = 0; i < kStMaxRuns; ++i) r.run_w[i] = -1;
+    if (!shrink_first) {
+        if (write) segs[n] = {kStBase, b0, b0 + nbase_first, 0, 0, 0};
+        ++n;
+    }
+    const int U = NW * KU2;   // the host keeps NW x KU2 x G below 2^31
+    for (int u = (U * cta) / G, u1 = (U * (cta + 1)) / G; u < u1;) {
+        const int wi = u / KU2;
+        const int e = min(u1, (wi + 1) * KU2);
+        if (r.nruns >= kStMaxRuns || region >= max_regions) {   // the host rules this out
+            r.ok = false;
+            break;
+        }
+        const int win = s_wlist ? s_wlist[wi] : wi;
+        if (write) segs[n] = {kStShrink, u - wi * KU2, e - wi * KU2, wi, region, kChunk * kStWin * win};
+#pragma unroll
+        for (int i = 0; i < kStMaxRuns; ++i)
+            if (i == r.nruns) r.run_w[i] = wi;   // constant indices: stays in registers
+        ++r.nruns;
+        ++n;
+        ++region;
+        u = e;
+    }
+    const int bb = shrink_first ? b0 : b0 + nbase_first;
+    if (b1 > bb) {
+        if (write) segs[n] = {kStBase, bb, b1, 0, 0, 0};
+        ++n;
+    }
+    r.n = n;
     return r;
 }
 
@@ -126,13 +187,15 @@ __global__ void __launch_bounds__(kClThreads, 1)
     int *ivars = reinterpret_cast<int *>(red_full + 1);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ivars);
     volatile int *abort_flag = ivars + 1;
-    int *n_segs = ivars + 2;
+    int *n_segs = ivars + 2;       // segments before the expand
     int *out_empty = ivars + 3;
+    int *n_exp = ivars + 4;        // 1: segs[*n_segs] is my expand segment
     uint16_t *s_bias = reinterpret_cast<uint16_t *>(ivars + 10);   // [128] my output rows' bias (16-byte aligned)
     int *s_ids = reinterpret_cast<int *>(s_bias + kSplitBN);         // [64] token ids (-2 past M)
     StSeg *segs = reinterpret_cast<StSeg *>(s_ids + 64);
     int *s_win_panel = reinterpret_cast<int *>(segs + kStMaxSegs);   // [kStMaxWinCta] first panel of my windows
-    int *s_win_info = s_win_panel + kStMaxWinCta;      // [kStMaxWinCta][8] adapter of each panel, -1 if absent
+    int *s_win_acc = s_win_panel + kStMaxWinCta;       // [kStMaxWinCta] window-sum / counter index of my windows
+    int *s_win_info = s_win_acc + kStMaxWinCta;        // [kStMaxWinCta][8] adapter of each panel, -1 if absent
     int *s_run_info = s_win_info + kStMaxWinCta * kStWin;   // [kStMaxRuns][8] the same for my shrink windows
     int *s_zero = s_run_info + kStMaxRuns * kStWin;    // [kStMaxWinCta] I am the window's last consumer
     unsigned *s_wbits = reinterpret_cast<unsigned *>(s_zero + kStMaxWinCta);   // [16] windows touched
@@ -147,8 +210,19 @@ __global__ void __launch_bounds__(kClThreads, 1)
     int32_t *status = p.counters + CNT_STATUS;
     const int KU2 = (p.kblocks + 1) / 2;          // K units of 2 K blocks
     const int b0 = (KU2 * q) / C, b1 = (KU2 * (q + 1)) / C;
-    const int nfirst = min(min(p.stages, kStFirst), b1 - b0);
     const int rpo = kSplitBN / C;                 // output rows owned by each CTA of the cluster
+    // all_windows: every window of the pool is processed, so the unit list
+    // is known at launch and the shrink goes first; otherwise warp 2 finds
+    // the windows the batch touches and the first units are base units
+    const bool allw = p.all_windows != 0;
+    int nfirst;   // units issued in the prologue (no metadata needed)
+    if (allw) {
+        const int U = p.windows_all * KU2;
+        const int nsh = (U * (cta + 1)) / G - (U * cta) / G;
+        nfirst = min(p.stages, nsh + (b1 - b0));
+    } else {
+        nfirst = min(min(p.stages, kStFirst), b1 - b0);
+    }
     // window k's arrival counter is wcnt[k * kWinCntStride], its consumer
     // counter sits in the other half of the same 128-byte line
     constexpr int kCntStride = kWinCntStride;
@@ -161,29 +235,54 @@ __global__ void __launch_bounds__(kClThreads, 1)
         id0 = lane < p.M ? p.ids[lane] : -2;
         id1 = lane + 32 < p.M ? p.ids[lane + 32] : -2;
     }
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < p.stages; ++s) {
-            mbar_init(&full[s], 1 + 128);   // producer's expect_tx arrive + one arrive per loader thread
-            mbar_init(&empty[s], 1);
-        }
-        for (int a = 0; a < kStMaxRegions; ++a) mbar_init(&acc_full[a], 1);
-        mbar_init(red_full, 1);
-        *abort_flag = 0;
-        mbar_expect_tx(red_full, static_cast<uint32_t>(kSplitBN * T * 4));   // the C partials of my rows
-        fence_mbarrier_init();
-    }
     if (warp == 0) {
+        // one barrier per lane
+        if (lane < p.stages) {
+            mbar_init(&full[lane], 1 + 128);   // producer's expect_tx arrive + one arrive per loader thread
+            mbar_init(&empty[lane], 1);
+        }
+        if (lane < kStMaxRegions) mbar_init(&acc_full[lane], 1);
+        if (lane == 0) {
+            mbar_init(red_full, 1);
+            *abort_flag = 0;
+            mbar_expect_tx(red_full, static_cast<uint32_t>(kSplitBN * T * 4));   // the C partials of my rows
+        }
+        fence_mbarrier_init();
         __syncwarp();
         named_bar_arrive(kBarInit, 160);   // the loaders may arrive on the ring barriers now
-    }
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < nfirst; ++i) {
-            mbar_expect_tx(&full[i], unit_tx);
-            tma_load_3d_st(smem + i * slot_bytes, &tm_w3, &full[i], 0, n0, 2 * (b0 + i));
-            tma_load_3d_st(smem + i * slot_bytes + kClWArea, &tm_x3, &full[i], 0, 0, 2 * (b0 + i));
+        if (lane == 0) {
+            if (allw) {
+                // the first units: my shrink units (window, K unit), then base
+                const int U = p.windows_all * KU2;
+                const int u0 = (U * cta) / G, u1 = (U * (cta + 1)) / G;
+                int wi = u0 / KU2, ku = u0 - wi * KU2;
+                for (int i = 0; i < nfirst; ++i) {
+                    uint8_t *wa = smem + i * slot_bytes;
+                    mbar_expect_tx(&full[i], unit_tx);
+                    int kb;
+                    if (u0 + i < u1) {
+                        kb = 2 * ku;
+                        tma_load_3d_st(wa, &tm_a3, &full[i], 0, kChunk * kStWin * wi, kb);
+                        if (++ku == KU2) {
+                            ku = 0;
+                            ++wi;
+                        }
+                    } else {
+                        kb = 2 * (b0 + (u0 + i - u1));
+                        tma_load_3d_st(wa, &tm_w3, &full[i], 0, n0, kb);
+                    }
+                    tma_load_3d_st(wa + kClWArea, &tm_x3, &full[i], 0, 0, kb);
+                }
+            } else {
+                for (int i = 0; i < nfirst; ++i) {
+                    mbar_expect_tx(&full[i], unit_tx);
+                    tma_load_3d_st(smem + i * slot_bytes, &tm_w3, &full[i], 0, n0, 2 * (b0 + i));
+                    tma_load_3d_st(smem + i * slot_bytes + kClWArea, &tm_x3, &full[i], 0, 0, 2 * (b0 + i));
+                }
+            }
+            tma_prefetch_map(&tm_a3);
+            tma_prefetch_map(&tm_b3);
         }
-        tma_prefetch_map(&tm_a3);
-        tma_prefetch_map(&tm_b3);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
@@ -199,22 +298,22 @@ __global__ void __launch_bounds__(kClThreads, 1)
         tc_fence_after();
     }
     pdl_launch_dependents();   // a dependent launch may start its prologue on the idle SMs
-    cluster_arrive();          // my barriers are initialised; peers wait for this before any st.async
+    cluster_arrive_relaxed();  // my barriers are initialised; peers wait for this before any st.async
     const uint32_t tmem_base = warp < 6 ? *tmem_slot : 0u;
 
     if (warp == 0) {
         // ===================== TMA producer: W, A and B boxes ================
         named_bar_sync(kBarMeta, kMetaThreads);
-        const int ns = *n_segs;
-        uint32_t it = nfirst;
-        bool tables = false;
-        for (int si = 1; si < ns; ++si) {
-            const StSeg sg = segs[si];
-            if (sg.kind == kStExpand && !tables) {
-                named_bar_sync(kBarTables, kMetaThreads);   // s_win_panel
-                tables = true;
+        const int nk = *n_segs;
+        uint32_t it = 0;
+        for (int si = 0; si <= nk; ++si) {
+            if (si == nk) {   // the expand windows, once the tables are ready
+                named_bar_sync(kBarTables, kTablesThreads);
+                if (!*n_exp) break;
             }
+            const StSeg sg = segs[si];
             for (int u = sg.a; u < sg.b; ++u, ++it) {
+                if (it < static_cast<uint32_t>(nfirst)) continue;   // issued in the prologue
                 const int s = it % p.stages;
                 const uint32_t round = it / p.stages;
                 if (lane == 0) {
@@ -233,31 +332,28 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 __syncwarp();
             }
         }
-        if (!tables) named_bar_sync(kBarTables, kMetaThreads);
     } else if (warp >= 6) {
-        // ===================== loaders: token-side operands ==================
+        // ===================== loaders: the S operand of the expand ==========
         const int lt = threadIdx.x - 192;
         named_bar_sync(kBarMeta, kMetaThreads);
-        const int ns = *n_segs;
+        const int nk = *n_segs;
         int ew0 = 0, ew1 = 0;   // my expand windows
-        if (ns > 1 && segs[ns - 1].kind == kStExpand) {
-            ew0 = segs[ns - 1].a;
-            ew1 = segs[ns - 1].b;
-        }
-        uint32_t it = nfirst;
-        bool tables = false;
-        for (int si = 1; si < ns; ++si) {
-            const StSeg sg = segs[si];
-            if (sg.kind == kStExpand) {
-                named_bar_sync(kBarTables, kMetaThreads);   // s_win_info
-                tables = true;
+        uint32_t it = 0;
+        for (int si = 0; si <= nk; ++si) {
+            if (si == nk) {   // the expand windows, once the tables are ready
+                named_bar_sync(kBarTables, kTablesThreads);   // s_win_*, s_ids
+                if (!*n_exp) break;
+                ew0 = segs[si].a;
+                ew1 = segs[si].b;
                 // every window of my share must be complete: one lane per
                 // window waits, so the checks overlap
-                for (int k = sg.a + lane; k < sg.b; k += 32)
-                    wait_flag_geq(wcnt + k * kCntStride, KU2, abort_flag, status, LORA_DEV_TIMEOUT);
+                for (int k = ew0 + lane; k < ew1; k += 32)
+                    wait_flag_geq(wcnt + s_win_acc[k - ew0] * kCntStride, KU2, abort_flag, status, LORA_DEV_TIMEOUT);
                 __syncwarp();
             }
+            const StSeg sg = segs[si];
             for (int u = sg.a; u < sg.b; ++u, ++it) {
+                if (it < static_cast<uint32_t>(nfirst)) continue;   // arrived in the prologue
                 const int s = it % p.stages;
                 const uint32_t round = it / p.stages;
                 if (lane == 0 && round > 0) mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
@@ -267,11 +363,11 @@ __global__ void __launch_bounds__(kClThreads, 1)
                     mbar_arrive(&full[s]);   // x arrives by TMA with the weight box
                 } else {
                     // S panels [8][T rows][16], 32-byte swizzle (chunk c of
-                    // row t at t*32 + (c ^ ((t >> 2) & 1))*16)
-                    // pieces of 8 ranks: (panel j, token t, half c); all loads of
-                    // a thread are issued before the first conversion
+                    // row t at t*32 + (c ^ ((t >> 2) & 1))*16); pieces of 8
+                    // ranks (panel j, token t, half c); all loads of a thread
+                    // are issued before the first conversion
                     const int *info = s_win_info + (u - sg.a) * kStWin;
-                    const float *wsum = p.acc + static_cast<int64_t>(u) * T * kSplitBN;
+                    const float *wsum = p.acc + static_cast<int64_t>(s_win_acc[u - sg.a]) * T * kSplitBN;
                     const int pieces = kStWin * T * 2;           // <= 1024 for T <= 64
                     constexpr int kMaxPer = kStWin * kStreamMaxTokens * 2 / 128;
                     float4 f[kMaxPer][2];
@@ -307,22 +403,22 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 }
             }
         }
-        if (!tables) named_bar_sync(kBarTables, kMetaThreads);
         if (ew1 > ew0) {
             // my reads of the window sums are done: count myself as a
             // consumer; the last of the NT consumers of a window clears it
             named_bar_sync(kBarLoad, 128);
             if (lt == 0)
                 for (int k = ew0; k < ew1; ++k)
-                    s_zero[k - ew0] = atom_acq_rel_gpu_add(ccnt + k * kCntStride, 1) == p.NT - 1;
+                    s_zero[k - ew0] = atom_acq_rel_gpu_add(ccnt + s_win_acc[k - ew0] * kCntStride, 1) == p.NT - 1;
             named_bar_sync(kBarLoad, 128);
             for (int k = ew0; k < ew1; ++k) {
                 if (!s_zero[k - ew0]) continue;
-                float4 *wsum = reinterpret_cast<float4 *>(p.acc + static_cast<int64_t>(k) * T * kSplitBN);
+                const int ai = s_win_acc[k - ew0];
+                float4 *wsum = reinterpret_cast<float4 *>(p.acc + static_cast<int64_t>(ai) * T * kSplitBN);
                 for (int i = lt; i < T * kSplitBN / 4; i += 128) wsum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (lt == 0) {
-                    wcnt[k * kCntStride] = 0;
-                    ccnt[k * kCntStride] = 0;
+                    wcnt[ai * kCntStride] = 0;
+                    ccnt[ai * kCntStride] = 0;
                 }
             }
         }
@@ -333,7 +429,6 @@ __global__ void __launch_bounds__(kClThreads, 1)
         auto mma_kunit = [&](uint32_t it, uint32_t d, int region) {
             const int s = it % p.stages;
             mbar_wait(&full[s], (it / p.stages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
-            fence_proxy_async_smem();   // token operands arrived through the generic proxy
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t wa = smem_u32(smem + s * slot_bytes);
@@ -353,10 +448,18 @@ __global__ void __launch_bounds__(kClThreads, 1)
             __syncwarp();
         };
         uint32_t it = 0;
-        for (; it < static_cast<uint32_t>(nfirst); ++it) mma_kunit(it, tmem_base, 0);
+        int si0 = 0;
+        if (!allw) {   // the first base units are known before the metadata
+            for (; it < static_cast<uint32_t>(nfirst); ++it) mma_kunit(it, tmem_base, 0);
+            si0 = 1;
+        }
         named_bar_sync(kBarMma, 64);
-        const int ns = *n_segs;
-        for (int si = 1; si < ns; ++si) {
+        const int nk = *n_segs;
+        for (int si = si0; si <= nk; ++si) {
+            if (si == nk) {   // the expand windows, once the tables are ready
+                named_bar_sync(kBarTables, kTablesThreads);
+                if (!*n_exp) break;
+            }
             const StSeg sg = segs[si];
             const uint32_t d = tmem_base + sg.region * T;
             for (int u = sg.a; u < sg.b; ++u, ++it) {
@@ -366,7 +469,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 }
                 const int s = it % p.stages;
                 mbar_wait(&full[s], (it / p.stages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
-                fence_proxy_async_smem();
+                fence_proxy_async_smem();   // the S operand arrived through the generic proxy
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t wa = smem_u32(smem + s * slot_bytes);
@@ -402,18 +505,28 @@ __global__ void __launch_bounds__(kClThreads, 1)
             reinterpret_cast<uint4 *>(s_bias)[k] = b;
         }
         if (warp == 2) {
-            // ---- metadata: the pool windows this batch touches, from
-            // lora_id_map and the pool table (one more round of loads) -------
+            // ---- metadata --------------------------------------------------
+            SegPlan pl;
+            if (allw) {
+                // every window is shrunk: the list before the expand is known now
+                pl = plan_segments(segs, lane == 0, p.windows_all, KU2, G, cta, b0, b1, 0, p.max_regions, nullptr,
+                                   true);
+                if (lane == 0) *n_segs = pl.n;
+                __syncwarp();
+                named_bar_arrive(kBarMma, 64);
+                named_bar_arrive(kBarMeta, kMetaThreads);
+            }
+            // tokens' adapters: pool panels [pa, pa + np), windows pa/8 ..
             const bool v0 = id0 >= 0 && id0 < p.A, v1 = id1 >= 0 && id1 < p.A;
             const int64_t ao0 = v0 ? p.a_offset[id0] : 0, ao1 = v1 ? p.a_offset[id1] : 0;
             const int rk0 = v0 ? p.rank[id0] : 0, rk1 = v1 ? p.rank[id1] : 0;
             s_ids[lane] = id0;
             s_ids[lane + 32] = id1;
+            const int pa0 = static_cast<int>(ao0 / p.K) / kChunk, np0 = v0 ? min(rk0 / kChunk, LORA_MAX_RANK / kChunk) : 0;
+            const int pa1 = static_cast<int>(ao1 / p.K) / kChunk, np1 = v1 ? min(rk1 / kChunk, LORA_MAX_RANK / kChunk) : 0;
+            // the windows the batch touches, ascending (s_wlist)
             if (lane < kStMaxWinAll / 32) s_wbits[lane] = 0u;
             __syncwarp();
-            // token's adapter: pool panels [pa, pa + np), in windows pa/8 .. (pa+np-1)/8
-            const int pa0 = static_cast<int>(ao0 / p.K) / kChunk, np0 = min(rk0 / kChunk, LORA_MAX_RANK / kChunk);
-            const int pa1 = static_cast<int>(ao1 / p.K) / kChunk, np1 = min(rk1 / kChunk, LORA_MAX_RANK / kChunk);
             auto mark = [&](int pa, int np) {
                 if (np <= 0) return;
                 for (int wv = pa / kStWin; wv <= (pa + np - 1) / kStWin && wv < p.windows_all; ++wv)
@@ -430,59 +543,40 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 const int y = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += y;
             }
-            const int NW = __shfl_sync(0xffffffffu, incl, 31);   // <= 2 windows per token
+            const int NT_ = __shfl_sync(0xffffffffu, incl, 31);   // windows touched (<= 2 per token)
             if (lane < kStMaxWinAll / 32) s_wpre[lane] = incl - cnt;
             for (unsigned b = bits, k = incl - cnt; b; b &= b - 1, ++k) s_wlist[k] = 32 * lane + __ffs(b) - 1;
             __syncwarp();
-            // ---- the segment list of this CTA ---------------------------------
-            // (32-bit: the host bounds windows x K units x grid below 2^31)
-            const int w0 = (NW * q) / C, w1 = (NW * (q + 1)) / C;
-            const int wend = min(w1, w0 + kStMaxWinCta);
-            int n = 0, region = 1, run = 0;
-            int run_w[kStMaxRuns] = {-1, -1, -1, -1};
-            if (lane == 0) segs[0] = {kStBase, b0, b0 + nfirst, 0, 0, 0};
-            ++n;
-            const int U = NW * KU2;
-            for (int u = (U * cta) / G, u1 = (U * (cta + 1)) / G; u < u1;) {
-                const int wi = u / KU2;
-                const int e = min(u1, (wi + 1) * KU2);
-                if (run >= kStMaxRuns || region >= p.max_regions) {   // the host rules this out
-                    if (lane == 0) {
-                        atomicOr(status, LORA_DEV_TIMEOUT);
-                        *abort_flag = 1;
-                    }
-                    break;
-                }
-                if (lane == 0) segs[n] = {kStShrink, u - wi * KU2, e - wi * KU2, wi, region, kChunk * kStWin * s_wlist[wi]};
-                run_w[run] = wi;
-                ++n;
-                ++region;
-                ++run;
-                u = e;
+            if (!allw) {
+                // only the touched windows are shrunk, named by their list index
+                pl = plan_segments(segs, lane == 0, NT_, KU2, G, cta, b0, b1, nfirst, p.max_regions, s_wlist, false);
+                if (lane == 0) *n_segs = pl.n;
+                __syncwarp();
+                named_bar_arrive(kBarMma, 64);
+                named_bar_arrive(kBarMeta, kMetaThreads);   // the producer may issue the shrink boxes now
             }
-            if (b1 > b0 + nfirst) {
-                if (lane == 0) segs[n] = {kStBase, b0 + nfirst, b1, 0, 0, 0};
-                ++n;
+            if (!pl.ok && lane == 0) {
+                atomicOr(status, LORA_DEV_TIMEOUT);
+                *abort_flag = 1;
             }
+            // ---- my expand windows: a share of the touched windows ------------
+            const int w0 = (NT_ * q) / C, w1 = (NT_ * (q + 1)) / C;
             if (w1 - w0 > kStMaxWinCta && lane == 0) {   // the host rules this out
                 atomicOr(status, LORA_DEV_TIMEOUT);
                 *abort_flag = 1;
             }
-            if (w1 > w0) {
-                if (lane == 0) segs[n] = {kStExpand, w0, wend, 0, 0, 0};
-                ++n;
+            const int wend = min(w1, w0 + kStMaxWinCta);
+            for (int k = w0 + lane; k < wend; k += 32) {
+                s_win_panel[k - w0] = kStWin * s_wlist[k];
+                s_win_acc[k - w0] = allw ? s_wlist[k] : k;   // sums are kept per shrunk window
             }
-            if (lane == 0) {
-                *n_segs = n;
-                *out_empty = (b1 == b0 && w1 == w0);
-            }
-            __syncwarp();
-            named_bar_arrive(kBarMma, 64);
-            named_bar_arrive(kBarMeta, kMetaThreads);   // the producer may issue the shrink boxes now
-            // ---- panel tables (needed at the shrink epilogue and the expand) ---
-            for (int k = w0 + lane; k < wend; k += 32) s_win_panel[k - w0] = kStWin * s_wlist[k];
             for (int k = lane; k < (wend - w0) * kStWin; k += 32) s_win_info[k] = -1;
             s_run_info[lane] = -1;   // kStMaxRuns x kStWin = 32 entries
+            if (lane == 0) {
+                segs[pl.n] = {kStExpand, w0, wend, 0, 0, 0};
+                *n_exp = w1 > w0;
+                *out_empty = (b1 == b0 && w1 == w0);
+            }
             __syncwarp();
             // the adapter owning each panel of my windows (absent panels stay -1)
             auto fill = [&](int id, int pa, int np) {
@@ -492,23 +586,25 @@ __global__ void __launch_bounds__(kClThreads, 1)
                     const int lo = max(pa, kStWin * wv), hi = min(pa + np, kStWin * wv + kStWin);
                     if (pos >= w0 && pos < wend)
                         for (int pp = lo; pp < hi; ++pp) s_win_info[(pos - w0) * kStWin + pp - kStWin * wv] = id;
+                    const int rw = allw ? wv : pos;   // how shrink runs name this window
+#pragma unroll
                     for (int r = 0; r < kStMaxRuns; ++r)
-                        if (run_w[r] == pos)
+                        if (pl.run_w[r] == rw)
                             for (int pp = lo; pp < hi; ++pp) s_run_info[r * kStWin + pp - kStWin * wv] = id;
                 }
             };
             fill(id0, pa0, np0);
             fill(id1, pa1, np1);
             __syncwarp();
-            named_bar_arrive(kBarTables, kMetaThreads);
-        }
-        if (warp != 2) {
+            named_bar_arrive(kBarTablesEpi, 128);
+            named_bar_arrive(kBarTables, kTablesThreads);
+        } else {
             named_bar_sync(kBarMeta, kMetaThreads);
-            named_bar_sync(kBarTables, kMetaThreads);   // s_run_info
+            named_bar_sync(kBarTablesEpi, 128);   // s_run_info, s_wbits
         }
         const int ns = *n_segs;
         // ---- shrink runs: add my partial window sums, then release ------------
-        for (int si = 1, run = 0; si < ns; ++si) {
+        for (int si = 0, run = 0; si < ns; ++si) {
             const StSeg sg = segs[si];
             if (sg.kind != kStShrink) continue;
             mbar_wait(&acc_full[sg.region], 0, abort_flag, status, LORA_DEV_TIMEOUT);
@@ -526,9 +622,13 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 }
             }
             // one release for the whole run, after all four warps' additions:
-            // the window is complete once its KU2 units have arrived
+            // the window is complete once its KU2 units have arrived.  A
+            // window no token touches (shrunk only because every window is)
+            // keeps its sum and counter at zero.
             named_bar_sync(kBarEpi, 128);
-            if (et == 0) red_release_gpu_add(wcnt + sg.w * kCntStride, sg.b - sg.a);
+            const int pw = allw ? sg.w : s_wlist[sg.w];
+            const bool touched = (s_wbits[pw >> 5] >> (pw & 31)) & 1u;
+            if (et == 0 && touched) red_release_gpu_add(wcnt + sg.w * kCntStride, sg.b - sg.a);
             ++run;
         }
         // ---- output tile: push my partial rows to their owners ----------------

@@ -134,6 +134,7 @@ struct ClusterParams {
     const int64_t *a_offset;   // the pool table (device): first A pool element of each adapter
     const int32_t *rank;       // padded rank of each adapter
     int32_t A, windows_all;    // adapters; 128-row windows in the pool
+    int32_t all_windows;       // process every window (known at launch) instead of the ones the batch touches
     float *acc;                // fp32 [windows][T_pad][128]: per-window sums of S (zero at rest)
     int32_t *wcnt;             // [windows][kWinCntStride]: shrink arrivals at 0, consumer CTAs at 16 (zero at rest)
     int32_t *counters;

@@ -462,7 +462,10 @@ static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, co
     p.A = pool->num_adapters;
     p.a_offset = pool->a_offset;
     p.rank = pool->rank;
-    p.windows_all = static_cast<int32_t>((panels + cluster_win() - 1) / cluster_win());
+    p.windows_all = pool->num_adapters ? static_cast<int32_t>((panels + cluster_win() - 1) / cluster_win()) : 0;
+    // a pool no larger than what one batch could touch is processed whole:
+    // the unit list is then known at launch and the shrink can go first
+    p.all_windows = p.windows_all <= L.max_win_str ? 1 : 0;
     p.scale = scale;
     p.bias = bias;
     p.x = x;
