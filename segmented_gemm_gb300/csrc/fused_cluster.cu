@@ -655,7 +655,10 @@ __global__ void __launch_bounds__(kClThreads, 1)
         }
         // ---- owner: sum the C partials of my rows, bias, bf16, y ---------------
         mbar_wait(red_full, 0, abort_flag, status, LORA_DEV_TIMEOUT);
-        cluster_arrive();      // done with distributed shared memory
+        // done with distributed shared memory: every peer's bytes have landed
+        // here (red_full) and nothing here touches a peer's shared memory
+        // any more, so the arrive needs no release ordering
+        cluster_arrive_relaxed();
         const int groups = rpo / 8;
         for (int w = et; w < T * groups; w += 128) {
             const int t = w / groups, gq = w % groups;
