@@ -147,27 +147,61 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t iw = 0;
         for (int j = blockIdx.x; j < total; j += gridDim.x) {
             const Job jb = decode_job(j, n_sjobs, p);
+            // shrink job: consecutive rank panels of one adapter are
+            // consecutive pool rows, loaded as one box of 16..64 rows per run.
+            // The runs are found once per job, one lane per chunk: lane c
+            // starts a run of run_len panels at pool row run_row, else 0.
+            int run_row = 0, run_len = 0;
+            // output job: the B-pool row of each of the tile's first 32
+            // chunks, one lane per chunk, loaded now for the expand steps
+            const int brow_l = (jb.kind == 1 && jb.c0 + lane < jb.c1) ? p.chunk_brow[jb.c0 + lane] : 0;
+            if (jb.kind == 0) {
+                const int c = jb.c0 + lane;
+                const bool in = c < jb.c1;
+                const int r = in ? p.chunk_arow[c] : -1;
+                const int prev = __shfl_up_sync(0xffffffffu, r, 1);
+                const bool start = in && (lane == 0 || prev != r - kChunk);
+                const unsigned starts = __ballot_sync(0xffffffffu, start);
+                if (start) {
+                    // up to the next start or the end of the job, at most 4 panels
+                    const unsigned later = starts & ~((2u << lane) - 1u);
+                    const int next = later ? __ffs(later) - 1 : jb.c1 - jb.c0;
+                    run_row = r;
+                    run_len = next - lane;
+                }
+                // runs longer than 4 panels are split: every 4th panel of a
+                // run starts a box (each lane finds its run: the nearest
+                // start at or below it)
+                const unsigned upto = starts & ((2u << lane) - 1u);
+                const int owner_lane = upto ? 31 - __clz(upto) : 0;
+                const int owner_row = __shfl_sync(0xffffffffu, run_row, owner_lane);
+                const int owner_len = __shfl_sync(0xffffffffu, run_len, owner_lane);
+                const int off = lane - owner_lane;   // panel index inside its run
+                if (in && off % 4 == 0) {
+                    run_row = owner_row + kChunk * off;
+                    run_len = min(4, owner_len - off);
+                } else {
+                    run_len = 0;
+                }
+            }
             for (int kb = 0; kb < kblocks; ++kb, ++iw) {
                 const int s = iw % kWStages;
                 const uint32_t round = iw / kWStages;
-                if (lane == 0) {
-                    if (round > 0) mbar_wait(&emptyw[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
-                    uint8_t *wsl = wring + s * kWSlot;
-                    if (jb.kind == 1) {
+                if (lane == 0 && round > 0) mbar_wait(&emptyw[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                __syncwarp();
+                uint8_t *wsl = wring + s * kWSlot;
+                if (jb.kind == 1) {
+                    if (lane == 0) {
                         mbar_expect_tx(&fullw[s], kWSlot);
                         tma_load_2d(wsl, &tm_w, &fullw[s], kb * kBK, jb.n * kBN);
-                    } else {
-                        mbar_expect_tx(&fullw[s], (jb.c1 - jb.c0) * kAPanelBytes);
-                        // consecutive rank panels of one adapter are consecutive
-                        // pool rows: one box of 16..64 rows per run
-                        for (int c = jb.c0; c < jb.c1;) {
-                            const int r0 = p.chunk_arow[c];
-                            int len = 1;
-                            while (len < 4 && c + len < jb.c1 && p.chunk_arow[c + len] == r0 + kChunk * len) ++len;
-                            const CUtensorMap *m = len == 1 ? &tm_a : len == 2 ? &tm_a32 : len == 3 ? &tm_a48 : &tm_a64;
-                            tma_load_2d(wsl + (c - jb.c0) * kAPanelBytes, m, &fullw[s], kb * kBK, r0);
-                            c += len;
-                        }
+                    }
+                } else {
+                    if (lane == 0) mbar_expect_tx(&fullw[s], (jb.c1 - jb.c0) * kAPanelBytes);
+                    __syncwarp();
+                    if (run_len > 0) {
+                        const CUtensorMap *m =
+                            run_len == 1 ? &tm_a : run_len == 2 ? &tm_a32 : run_len == 3 ? &tm_a48 : &tm_a64;
+                        tma_load_2d(wsl + lane * kAPanelBytes, m, &fullw[s], kb * kBK, run_row);
                     }
                 }
                 __syncwarp();
@@ -190,11 +224,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int nc = min(kPanelsPerStage, jb.c1 - cg);
                     if (lane == 0) mbar_expect_tx(&fullw[s], nc * (kSPanelBytes + kBPanelBytes));
                     __syncwarp();
+                    const int ci = cg - jb.c0 + lane;   // chunk index inside the tile
+                    const int brow_s = __shfl_sync(0xffffffffu, brow_l, ci & 31);
                     if (lane < nc) {
                         const int c = cg + lane;
+                        const int brow = ci < 32 ? brow_s : p.chunk_brow[c];
                         tma_load_2d(wsl + lane * kSPanelBytes, &tm_s, &fullw[s], 0, c * kBM);
                         tma_load_2d(wsl + kPanelsPerStage * kSPanelBytes + lane * kBPanelBytes, &tm_b, &fullw[s], 0,
-                                    p.chunk_brow[c] + jb.n * kBN);
+                                    brow + jb.n * kBN);
                     }
                     __syncwarp();
                 }
