@@ -51,16 +51,27 @@ constexpr int kPanelsPerStage = 2;               // expand step: 2 x (S 4 KB + B
 constexpr int kTcThreads = 320;   // 10 warps: TMA, MMA, 4 epilogue, 4 x loaders
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 256;
-constexpr size_t kTcSmemBytes = kXStages * kXSlot + kWStages * kWSlot + 1024 /*align*/ + 256 /*barriers*/;
+constexpr size_t kTcSmemBytes =
+    kXStages * kXSlot + kWStages * kWSlot + 1024 /*align*/ + 256 /*barriers*/ + 2 * kBN * 2 /*bias of two tiles*/;
+static_assert(kWStages * kWSlot == kBM * kBN * 4, "a split tile's fp32 partials fill the W ring exactly");
 
 struct Job {
     int kind;   // 0 shrink, 1 output
     int m, n, c0, c1;
+    int kb0, kb1;   // K blocks of this piece of the job
+    int part;       // kPartFull, or a piece of a split output tile: kPartHead (holds K block 0) / kPartTail
+    int slot;       // split tile: index of its partial-sum scratch
 };
+
+enum { kPartFull = 0, kPartHead = 1, kPartTail = 2 };
 
 __device__ __forceinline__ Job decode_job(int j, int n_sjobs, const TcParams &p)
 {
     Job jb;
+    jb.kb0 = 0;
+    jb.kb1 = p.mode == kModeExpand ? 0 : p.kblocks;
+    jb.part = kPartFull;
+    jb.slot = 0;
     if (j < n_sjobs) {
         jb.kind = 0;
         jb.m = p.sjob_tile[j];
@@ -82,6 +93,106 @@ __device__ __forceinline__ Job decode_job(int j, int n_sjobs, const TcParams &p)
     return jb;
 }
 
+// The q-th work item of CTA b (false past the last).  Without stream-K the
+// CTAs take jobs b, b + G, ...  With stream-K the whole waves are taken that
+// way, and the jobs of the last partial wave are shared out: its shrink jobs
+// whole (one per CTA, first CTAs), its output tiles as equal runs of K blocks
+// over the other CTAs.  A tile cut between CTAs has one head piece (K block
+// 0, last item of its CTA) and tail pieces (first items of the next CTAs):
+// tails add their partial sums to the tile's scratch and count themselves,
+// the head waits for them, applies the expand steps and writes y.
+struct SkPlan {
+    int waves, rs, t0, ro, gp;   // whole waves; tail shrink jobs; first tail tile; tail tiles; CTAs sharing them
+    int64_t wt;                  // K blocks of the tail tiles
+};
+
+__device__ __forceinline__ SkPlan sk_plan(int n_sjobs, int n_out, int G, int KB, bool streamk)
+{
+    SkPlan s;
+    const int total = n_sjobs + n_out;
+    // split only when the last wave would leave a quarter or more of the
+    // CTAs idle: otherwise the extra partial-sum epilogues cost more than
+    // the idle time they recover
+    const int rem = total % G;
+    streamk = streamk && rem != 0 && rem * 4 <= G * 3;
+    s.waves = streamk ? total / G : (total + G - 1) / G;
+    const int jf = s.waves * G;
+    s.rs = streamk ? max(0, n_sjobs - jf) : 0;
+    s.t0 = streamk ? max(0, jf - n_sjobs) : n_out;
+    s.ro = streamk ? n_out - s.t0 : 0;
+    s.gp = G - s.rs;
+    s.wt = static_cast<int64_t>(s.ro) * KB;
+    return s;
+}
+
+__device__ __forceinline__ bool get_item(int q, int b, int G, int n_sjobs, int n_out, const SkPlan &s,
+                                         const TcParams &p, Job &jb)
+{
+    const int total = n_sjobs + n_out;
+    if (q < s.waves) {
+        const int j = b + q * G;
+        if (j >= total) return false;
+        jb = decode_job(j, n_sjobs, p);
+        return true;
+    }
+    const int qt = q - s.waves;
+    if (b < s.rs) {   // a whole shrink job of the last wave
+        if (qt > 0) return false;
+        jb = decode_job(s.waves * G + b, n_sjobs, p);
+        return true;
+    }
+    if (s.ro <= 0) return false;
+    const int KB = p.kblocks, bb = b - s.rs;
+    const int64_t r0 = s.wt * bb / s.gp, r1 = s.wt * (bb + 1) / s.gp;
+    int64_t f = r0;
+    int t = static_cast<int>(f / KB);
+    for (int i = 0; i < qt && f < r1; ++i) {
+        ++t;
+        f = static_cast<int64_t>(t) * KB;
+    }
+    if (f >= r1) return false;
+    jb = decode_job(n_sjobs + s.t0 + t, n_sjobs, p);
+    jb.kb0 = static_cast<int>(f - static_cast<int64_t>(t) * KB);
+    jb.kb1 = static_cast<int>(min(r1, static_cast<int64_t>(t + 1) * KB) - static_cast<int64_t>(t) * KB);
+    jb.part = jb.kb0 > 0 ? kPartTail : (jb.kb1 < KB ? kPartHead : kPartFull);
+    jb.slot = t;
+    return true;
+}
+
+// Whether split tile t (one of CTA b's tail pieces) has a single tail piece:
+// the CTA before b holds its head, and no later CTA starts inside it.
+__device__ __forceinline__ bool sk_single_tail(int b, int t, const SkPlan &s, int KB)
+{
+    const int bb = b - s.rs;
+    const int64_t end = static_cast<int64_t>(t + 1) * KB, begin = static_cast<int64_t>(t) * KB;
+    const int64_t my_r0 = s.wt * bb / s.gp;
+    // my piece must start after the tile's first K block (I am a tail) and
+    // the head's CTA must be the previous non-empty one
+    int prev = bb - 1;
+    while (prev >= 0 && s.wt * prev / s.gp == s.wt * (prev + 1) / s.gp) --prev;
+    if (prev < 0 || s.wt * prev / s.gp > begin || my_r0 <= begin) return false;
+    for (int nb = bb + 1; nb < s.gp; ++nb) {
+        const int64_t r0 = s.wt * nb / s.gp, r1 = s.wt * (nb + 1) / s.gp;
+        if (r0 >= end) break;
+        if (r1 > r0) return false;   // another tail starts inside the tile
+    }
+    return true;
+}
+
+// Tail pieces of split tile t whose head piece is CTA b's (the non-empty
+// ranges of the next CTAs that start inside the tile).
+__device__ __forceinline__ int sk_tails(int b, int t, const SkPlan &s, int KB)
+{
+    int n = 0;
+    const int64_t end = static_cast<int64_t>(t + 1) * KB;
+    for (int bb = b - s.rs + 1; bb < s.gp; ++bb) {
+        const int64_t r0 = s.wt * bb / s.gp, r1 = s.wt * (bb + 1) / s.gp;
+        if (r0 >= end) break;
+        if (r1 > r0) ++n;
+    }
+    return n;
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
     lora_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                    const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -99,9 +210,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *emptyw = fullw + kWStages;
     uint64_t *acc_full = emptyw + kWStages;
     uint64_t *acc_empty = acc_full + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+    uint64_t *sk_bar = acc_empty + 2;   // stream-K head: the partial sums have landed in the W ring
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sk_bar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *last_flag = const_cast<int *>(abort_flag) + 1;
+    // bias of the output tile of each accumulator slot: [2][kBN] bf16 (16-byte aligned)
+    uint32_t *s_bias = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(fullx) + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *status = p.counters + CNT_STATUS;
@@ -119,6 +233,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&acc_full[a], 1);
             mbar_init(&acc_empty[a], 128);
         }
+        mbar_init(sk_bar, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -139,14 +254,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int n_sjobs = (p.mode == kModeExpand) ? 0 : p.hdr[HDR_NSJOBS];
     const int n_out = (p.mode == kModeShrink) ? 0 : p.num_mtiles * p.num_ntiles;
-    const int total = n_sjobs + n_out;
-    const int kblocks = (p.mode == kModeExpand) ? 0 : p.kblocks;
+    const SkPlan sk = sk_plan(n_sjobs, n_out, gridDim.x, p.kblocks, p.streamk != 0);
+    Job jb;
 
     if (warp == 0) {
         // ===================== TMA producer: W ring (W, A panels, S / B panels)
         uint32_t iw = 0;
-        for (int j = blockIdx.x; j < total; j += gridDim.x) {
-            const Job jb = decode_job(j, n_sjobs, p);
+        for (int q = 0; get_item(q, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, jb); ++q) {
             // shrink job: consecutive rank panels of one adapter are
             // consecutive pool rows, loaded as one box of 16..64 rows per run.
             // The runs are found once per job, one lane per chunk: lane c
@@ -184,7 +298,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     run_len = 0;
                 }
             }
-            for (int kb = 0; kb < kblocks; ++kb, ++iw) {
+            for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++iw) {
                 const int s = iw % kWStages;
                 const uint32_t round = iw / kWStages;
                 if (lane == 0 && round > 0) mbar_wait(&emptyw[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
@@ -206,7 +320,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 __syncwarp();
             }
-            if (jb.kind == 1 && jb.c1 > jb.c0) {
+            if (jb.kind == 1 && jb.c1 > jb.c0 && jb.part != kPartTail) {
                 if (p.mode == kModeLinear) {
                     if (lane == 0) {
                         wait_flag_geq(p.counters + CNT_FIXED + jb.m, p.tile_njobs[jb.m], abort_flag, status,
@@ -249,8 +363,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int chunk = lt & 7, rb = lt >> 3;
         const uint32_t swz = static_cast<uint32_t>((chunk ^ (rb & 7)) << 4);
         uint32_t ix = 0;
-        for (int j = blockIdx.x; j < total && kblocks > 0; j += gridDim.x) {
-            const Job jb = decode_job(j, n_sjobs, p);
+        for (int q = 0; get_item(q, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, jb); ++q) {
+            if (jb.kb1 <= jb.kb0) continue;
             const uint16_t *src[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -258,7 +372,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (pp >= p.M) pp = p.M - 1;
                 src[q] = p.x + static_cast<int64_t>(p.perm[pp]) * p.K + chunk * 8;
             }
-            for (int kb = 0; kb < kblocks; ++kb, ++ix) {
+            for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++ix) {
                 const int s = ix % kXStages;
                 const uint32_t round = ix / kXStages;
                 if (lane == 0 && round > 0) mbar_wait(&emptyx[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
@@ -273,9 +387,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         cp_async_wait_all();
     } else if (warp == 1) {
         // ===================== MMA issuer ====================================
-        uint32_t iw = 0, ix = 0, q = 0;
-        for (int j = blockIdx.x; j < total; j += gridDim.x, ++q) {
-            const Job jb = decode_job(j, n_sjobs, p);
+        uint32_t iw = 0, ix = 0;
+        for (int q = 0; get_item(q, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, jb); ++q) {
             const uint32_t slot = q & 1, use = q >> 1;
             if (use > 0) mbar_wait(&acc_empty[slot], (use - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
             tc_fence_after();
@@ -283,7 +396,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int n_mma = jb.kind == 0 ? (jb.c1 - jb.c0) * kChunk : kBN;
             const uint32_t idesc = umma_idesc_bf16(kBM, n_mma);
             uint32_t acc = 0;
-            for (int kb = 0; kb < kblocks; ++kb, ++iw, ++ix) {
+            for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++iw, ++ix) {
                 const int sw = iw % kWStages, sx = ix % kXStages;
                 mbar_wait(&fullx[sx], (ix / kXStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
                 mbar_wait(&fullw[sw], (iw / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
@@ -303,7 +416,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 __syncwarp();
             }
-            if (jb.kind == 1 && jb.c1 > jb.c0) {
+            if (jb.kind == 1 && jb.c1 > jb.c0 && jb.part != kPartTail) {
                 const uint32_t idesc_e = umma_idesc_bf16(kBM, kBN);
                 for (int cg = jb.c0; cg < jb.c1; cg += kPanelsPerStage, ++iw) {
                     const int sw = iw % kWStages;
@@ -331,10 +444,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int et = threadIdx.x - 64;   // 0..127
-        uint32_t q = 0;
-        for (int j = blockIdx.x; j < total; j += gridDim.x, ++q) {
-            const Job jb = decode_job(j, n_sjobs, p);
+        for (int q = 0; get_item(q, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, jb); ++q) {
             const uint32_t slot = q & 1, use = q >> 1;
+            uint32_t *tbias = s_bias + slot * (kBN / 2);   // [kBN / 2] bf16 pairs
+            const bool out_bias = jb.kind == 1 && jb.part != kPartTail && p.mode == kModeLinear && p.bias;
+            if (out_bias) {
+                // the tile's 256 bias values, once, while the MMA still runs
+                // (the barriers keep the previous tile's readers apart)
+                named_bar_sync(1, 128);
+                const int col = jb.n * kBN + 2 * et;
+                uint32_t bv = 0u;
+                if (col + 1 < p.N) bv = __ldg(reinterpret_cast<const uint32_t *>(p.bias + col));
+                else if (col < p.N) bv = static_cast<uint32_t>(__ldg(p.bias + col));
+                tbias[et] = bv;
+                named_bar_sync(1, 128);
+            }
             mbar_wait(&acc_full[slot], use & 1, abort_flag, status, LORA_DEV_TIMEOUT);
             tc_fence_after();
             const uint32_t tbase = tmem_base + slot * kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
@@ -382,10 +506,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     named_bar_sync(1, 128);
                     if (et == 0) red_release_gpu_add(p.counters + CNT_FIXED + jb.m, 1);
                 }
-            } else {
-                // ---- output tile: + bias, bf16, scatter to the original row ----
-                const int n0 = jb.n * kBN;
-                const bool lora_row = p.mode != kModeExpand || pp >= p.offsets[1];
+            } else if (jb.part == kPartTail) {
+                // ---- tail piece of a split tile: add my partial sums ----------
+                // scratch layout [col / 4][row][4]: a warp's float4 accesses
+                // cover 512 contiguous bytes.  The only tail of a tile stores
+                // its partials; several tails add theirs with atomics.
+                float4 *part = reinterpret_cast<float4 *>(p.sk_part) + static_cast<int64_t>(jb.slot) * (kBN / 4) * kBM;
+                const bool single = sk_single_tail(blockIdx.x, jb.slot, sk, p.kblocks);
                 for (int cc = 0; cc < kBN / 16; ++cc) {
                     uint32_t r[16];
                     tmem_ld16(tbase + cc * 16, r);
@@ -394,12 +521,65 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tc_fence_before();
                         mbar_arrive(&acc_empty[slot]);
                     }
-                    const int col = n0 + cc * 16;
-                    if (!valid || col >= p.N || !lora_row) continue;
-                    uint16_t *dst = p.y + static_cast<int64_t>(tok) * p.N + col;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 f4 = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                                      __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+                        if (single) __stcg(part + (cc * 4 + k) * kBM + row, f4);
+                        else atomicAdd(part + (cc * 4 + k) * kBM + row, f4);
+                    }
+                }
+                __threadfence();
+                named_bar_sync(1, 128);
+                if (et == 0) red_release_gpu_add(p.sk_cnt + jb.slot * kWinCntStride, 1);
+            } else {
+                // ---- output tile (whole, or the head piece of a split tile):
+                // + the tails' partial sums, + bias, bf16, scatter to the
+                // original row ----------------------------------------------
+                const int n0 = jb.n * kBN;
+                const bool lora_row = p.mode != kModeExpand || pp >= p.offsets[1];
+                const bool head = jb.part == kPartHead;
+                float4 *part = head ? reinterpret_cast<float4 *>(p.sk_part) + static_cast<int64_t>(jb.slot) * (kBN / 4) * kBM
+                                    : nullptr;
+                // the head is its CTA's last item: the W ring is idle now, and
+                // the summed partials (128 KB) come in by four bulk copies
+                const float4 *spart = reinterpret_cast<const float4 *>(wring);
+                if (head) {
+                    if (et == 0) {   // every tail piece has added its partial sums
+                        wait_flag_geq(p.sk_cnt + jb.slot * kWinCntStride, sk_tails(blockIdx.x, jb.slot, sk, p.kblocks),
+                                      abort_flag, status, LORA_DEV_TIMEOUT);
+                        fence_proxy_async_global();   // their atomics -> the bulk copies' reads
+                        mbar_expect_tx(sk_bar, kBM * kBN * 4);
+                        for (int i = 0; i < 4; ++i)
+                            bulk_load(wring + i * kWSlot, reinterpret_cast<const uint8_t *>(part) + i * kWSlot, kWSlot,
+                                      sk_bar);
+                    }
+                    mbar_wait(sk_bar, 0, abort_flag, status, LORA_DEV_TIMEOUT);
+                    // sums built by atomics: leave the scratch zeroed for the next call
+                    if (sk_tails(blockIdx.x, jb.slot, sk, p.kblocks) > 1) {
+#pragma unroll 8
+                        for (int i = 0; i < kBN / 4; ++i) __stcg(part + i * kBM + row, make_float4(0.f, 0.f, 0.f, 0.f));
+                    }
+                }
+                // one 16-column chunk: + partials, + bias (from shared memory) or
+                // the existing y (standalone expand), bf16, store to the row
+                auto emit = [&](int cc, const uint32_t (&r)[16]) {
                     float v[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
+                    if (head) {   // the summed partials, from shared memory
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float4 pv = spart[(cc * 4 + k) * kBM + row];
+                            v[4 * k] += pv.x;
+                            v[4 * k + 1] += pv.y;
+                            v[4 * k + 2] += pv.z;
+                            v[4 * k + 3] += pv.w;
+                        }
+                    }
+                    const int col = n0 + cc * 16;
+                    if (!valid || col >= p.N || !lora_row) return;
+                    uint16_t *dst = p.y + static_cast<int64_t>(tok) * p.N + col;
                     if (p.mode == kModeExpand) {
                         const uint4 *src = reinterpret_cast<const uint4 *>(dst);
 #pragma unroll
@@ -413,12 +593,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 v[8 * h + 2 * e + 1] += bf16_hi(w4[e]);
                             }
                         }
-                    } else if (p.bias) {
-                        const uint4 *bsrc = reinterpret_cast<const uint4 *>(p.bias + col);
+                    } else if (out_bias) {
+                        const uint4 *bsrc = reinterpret_cast<const uint4 *>(tbias + cc * 8);
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            if (col + 8 * h >= p.N) break;
-                            const uint4 u = __ldg(bsrc + h);
+                            const uint4 u = bsrc[h];
                             const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
@@ -433,6 +612,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (col + 8 < p.N)
                         o[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]),
                                           pack_bf16x2(v[12], v[13]), pack_bf16x2(v[14], v[15]));
+                };
+                // two chunks per TMEM wait
+                for (int cc = 0; cc < kBN / 16; cc += 2) {
+                    uint32_t r0[16], r1[16];
+                    tmem_ld16(tbase + cc * 16, r0);
+                    tmem_ld16(tbase + cc * 16 + 16, r1);
+                    tmem_ld_wait16(r0);
+                    tmem_regs_after_wait16(r1);
+                    if (cc + 2 == kBN / 16) {
+                        tc_fence_before();
+                        mbar_arrive(&acc_empty[slot]);
+                    }
+                    emit(cc, r0);
+                    emit(cc + 1, r1);
+                }
+                if (head) {   // all partials consumed: the counter is zero again for the next call
+                    named_bar_sync(1, 128);
+                    if (et == 0) p.sk_cnt[jb.slot * kWinCntStride] = 0;
                 }
             }
         }

@@ -34,6 +34,7 @@ constexpr int kSplitBN = 128;          // output features per tile (UMMA M)
 constexpr int kSplitMaxCtas = 1024;    // upper bound on the persistent grid
 constexpr int kStreamMaxTokens = 64;    // largest M served by the weight-streaming schedule
 constexpr int kWinCntStride = 32;       // ints per window counter pair (one 128-byte line)
+constexpr int kStreamKMaxTiles = 160;   // output tiles the tiled schedule may split along K in one call
 
 // plan header entries
 enum PlanHdr {
@@ -70,6 +71,8 @@ struct WsLayout {
     int32_t max_win_str;      // windows the stream schedule's sums and counters can hold (M <= 64)
     size_t s_scratch, s_scratch_bytes;
     size_t acc_out, acc_out_bytes, acc_shr, acc_shr_bytes;
+    size_t total_min;         // everything but the stream-K scratch
+    size_t sk_part, sk_cnt;   // stream-K partial sums / counters of the tiled schedule (M > 128)
     size_t total;
 };
 
@@ -103,6 +106,9 @@ struct TcParams {
     const int32_t *tile_chunk_off, *chunk_arow, *chunk_brow, *chunk_rng;
     const int32_t *sjob_tile, *sjob_c0, *sjob_c1, *tile_njobs;
     int32_t *counters;
+    int32_t streamk;           // split the last partial wave of output tiles along K
+    float *sk_part;            // fp32 [tiles][256/4][128][4]: summed partials of split tiles (zero at rest)
+    int32_t *sk_cnt;           // [tiles][kWinCntStride]: partials added per split tile (zero at rest)
 };
 
 struct SplitParams {

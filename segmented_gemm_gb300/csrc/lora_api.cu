@@ -166,6 +166,13 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
     L.s_scratch = take(L.s_scratch_bytes);
     L.acc_out = take(std::max<size_t>(L.acc_out_bytes, 16));
     L.acc_shr = take(std::max<size_t>(L.acc_shr_bytes, 16));
+    L.total_min = o;
+    // stream-K scratch of the tiled schedule: partial sums and counters of
+    // the split tiles (used only when the workspace is this large)
+    if (M > kSplitMaxTokens) {
+        L.sk_part = take(static_cast<size_t>(kStreamKMaxTiles) * kBM * kBN * 4);
+        L.sk_cnt = take(static_cast<size_t>(kStreamKMaxTiles) * kWinCntStride * 4);
+    }
     L.total = o;
     return L;
 }
@@ -262,7 +269,7 @@ static int prepare(const int32_t *ids, int64_t M, const lora_pool_t *pool, const
     if (!ws) return LORA_ERR_WORKSPACE;
     if (!device_supported()) return LORA_ERR_UNSUPPORTED;
     *L = make_ws_layout(M, pool->N, pool->num_adapters);
-    if (ws_bytes < L->total) return LORA_ERR_WORKSPACE;
+    if (ws_bytes < L->total_min) return LORA_ERR_WORKSPACE;
     if (segs) {
         if (segs->plan != ws || segs->M != M || segs->num_adapters != pool->num_adapters) return LORA_ERR_SEGMENTS;
         return LORA_OK;
@@ -322,11 +329,19 @@ static bool encode_pool_maps(TcMaps &m, const lora_pool_t *pool, const void *dum
 }
 
 static int run_tiled(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
-                     const lora_pool_t *pool, float scale, lora_bf16_t *y, void *ws, const WsLayout &L, int mode,
-                     float *s_out, int32_t s_cols, const float *s_in, cudaStream_t stream)
+                     const lora_pool_t *pool, float scale, lora_bf16_t *y, void *ws, size_t ws_bytes, const WsLayout &L,
+                     int mode, float *s_out, int32_t s_cols, const float *s_in, cudaStream_t stream)
 {
     TcParams p;
     fill_tc_params(p, L, ws, pool, M);
+    // stream-K for the last partial wave: the fused layer only, when the
+    // workspace holds the partial-sum scratch and the grid fits its tiles
+    const int sms_sk = num_sms_current_device();
+    if (mode == kModeLinear && L.sk_part && ws_bytes >= L.total && sms_sk <= kStreamKMaxTiles) {
+        p.streamk = 1;
+        p.sk_part = at<float>(ws, L.sk_part);
+        p.sk_cnt = at<int32_t>(ws, L.sk_cnt);
+    }
     p.mode = mode;
     p.scale = scale;
     p.bias = bias;
@@ -352,7 +367,8 @@ static int run_tiled(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, cons
     int64_t jobs = 0;
     if (mode != kModeShrink) jobs += static_cast<int64_t>(p.num_mtiles) * p.num_ntiles;
     if (mode != kModeExpand) jobs += L.max_sjobs;
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, jobs)));
+    // with stream-K the last partial wave is shared out over every SM
+    const int grid = p.streamk ? sms : static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, jobs)));
     return launch_tc(m, p, grid, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
@@ -545,7 +561,7 @@ int lora_build_segments(const int32_t *lora_id_map, int64_t M, const lora_pool_t
         int rc = check_pool(pool);
         if (rc) return rc;
         L = make_ws_layout(0, pool->N, pool->num_adapters);
-        if (!ws || ws_bytes < L.total) return LORA_ERR_WORKSPACE;
+        if (!ws || ws_bytes < L.total_min) return LORA_ERR_WORKSPACE;
         fill_segments(ws, L, 0, pool->num_adapters, out);
         return LORA_OK;
     }
@@ -578,7 +594,7 @@ int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const 
     }
     const bool splitk = path == LORA_PATH_SPLITK || (path == LORA_PATH_AUTO && M <= kSplitMaxTokens && lora_id_map);
     if (splitk) return run_splitk(x, M, W, bias, lora_id_map, pool, scale, y, ws, L, s);
-    return run_tiled(x, M, W, bias, pool, scale, y, ws, L, kModeLinear, nullptr, 0, nullptr, s);
+    return run_tiled(x, M, W, bias, pool, scale, y, ws, ws_bytes, L, kModeLinear, nullptr, 0, nullptr, s);
 }
 
 int lora_linear(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
@@ -605,7 +621,7 @@ int lora_shrink(const lora_bf16_t *x, int64_t M, const int32_t *lora_id_map, con
     if (cudaMemsetAsync(S, 0, static_cast<size_t>(M) * s_cols * sizeof(float), s) != cudaSuccess)
         return LORA_ERR_CUDA;
     if (pool->num_adapters == 0) return LORA_OK;
-    return run_tiled(x, M, nullptr, nullptr, pool, 1.0f, nullptr, ws, L, kModeShrink, S, s_cols, nullptr, s);
+    return run_tiled(x, M, nullptr, nullptr, pool, 1.0f, nullptr, ws, ws_bytes, L, kModeShrink, S, s_cols, nullptr, s);
 }
 
 int lora_expand(const float *S, int32_t s_cols, int64_t M, const int32_t *lora_id_map, const lora_pool_t *pool,
@@ -622,7 +638,7 @@ int lora_expand(const float *S, int32_t s_cols, int64_t M, const int32_t *lora_i
     int rc = prepare(lora_id_map, M, pool, segs, ws, ws_bytes, s, &L);
     if (rc) return rc;
     if (pool->num_adapters == 0) return LORA_OK;
-    return run_tiled(nullptr, M, nullptr, nullptr, pool, scale, y, ws, L, kModeExpand, nullptr, s_cols, S, s);
+    return run_tiled(nullptr, M, nullptr, nullptr, pool, scale, y, ws, ws_bytes, L, kModeExpand, nullptr, s_cols, S, s);
 }
 
 int lora_get_status(void *ws, lora_stream_t stream, int32_t *status)

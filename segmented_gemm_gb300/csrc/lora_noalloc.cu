@@ -52,9 +52,11 @@ extern "C" int lora_linear_noalloc(const lora_bf16_t *x, int64_t M, const lora_b
 {
     if (!pool) return LORA_ERR_NULL;
     if (M < 0 || pool->N <= 0 || pool->num_adapters < 0) return LORA_ERR_SHAPE;
-    const size_t need = lora_workspace_size(M, pool->N, pool->num_adapters);
-    if (need == 0) return LORA_ERR_SHAPE;
-    if (need > LORA_NOALLOC_SCRATCH_BYTES) return LORA_ERR_CAPACITY;
+    if (lora_workspace_size(M, pool->N, pool->num_adapters) == 0) return LORA_ERR_SHAPE;
+    // the minimal layout must fit; optional scratch beyond it is used only
+    // when it fits too
+    if (make_ws_layout(M, pool->N, pool->num_adapters).total_min > LORA_NOALLOC_SCRATCH_BYTES)
+        return LORA_ERR_CAPACITY;
     int rc = LORA_OK;
     void *ws = noalloc_scratch_address(&rc);
     if (rc != LORA_OK) return rc;
@@ -67,7 +69,13 @@ extern "C" int lora_linear_noalloc(const lora_bf16_t *x, int64_t M, const lora_b
                                       {L.wcnt, static_cast<size_t>(L.max_win_str) * kWinCntStride * 4},
                                       {L.acc_str, L.acc_str_bytes},
                                       {L.acc_out, L.acc_out_bytes},
-                                      {L.acc_shr, L.acc_shr_bytes}};
+                                      {L.acc_shr, L.acc_shr_bytes},
+                                      {L.sk_cnt, L.total <= LORA_NOALLOC_SCRATCH_BYTES && L.sk_part
+                                                     ? static_cast<size_t>(kStreamKMaxTiles) * kWinCntStride * 4
+                                                     : 0},
+                                      {L.sk_part, L.total <= LORA_NOALLOC_SCRATCH_BYTES && L.sk_part
+                                                      ? static_cast<size_t>(kStreamKMaxTiles) * kBM * kBN * 4
+                                                      : 0}};
     for (const auto &r : zero_regions)
         if (r[1] > 0 && cudaMemsetAsync(base + r[0], 0, r[1], s) != cudaSuccess) return LORA_ERR_CUDA;
     return lora_linear(x, M, W, bias, lora_id_map, pool, scale, nullptr, y, ws, LORA_NOALLOC_SCRATCH_BYTES, stream);

@@ -152,6 +152,16 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *m)
 }
 
 // 2-D tiled load of the map's box at (x = inner coordinate, y = row).
+// Plain bulk copy of `bytes` (multiple of 16, both addresses 16-byte
+// aligned) from global to shared memory, completing on an mbarrier.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, uint64_t *bar, int x, int y)
 {
     asm volatile(
@@ -288,6 +298,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
 
 // Wait for outstanding tcgen05.ld; the registers are threaded through so
 // no use of them can be scheduled before the wait.
+// Ties registers loaded by an earlier tcgen05.ld to a preceding wait::ld (an
+// ordered empty asm), so a second batch can share the first one's wait.
+__device__ __forceinline__ void tmem_regs_after_wait16(uint32_t (&r)[16])
+{
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]));
+}
 __device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16])
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;"

@@ -160,6 +160,25 @@ def test_linear_tiled_multi_tile(M, K, N, ranks, mode):
     assert_close(y, oracle.lora_linear(wl), what=f"M{M} K{K} N{N}")
 
 
+@pytest.mark.parametrize("M,K,N,ranks", [
+    (1280, 256, 2560, [16, 32, 64, 48] * 3),   # ~100 output tiles on the grid: split tiles with one tail each
+    (300, 320, 1032, [16, 64]),                # a few tiles over every CTA: many tails, summed by atomics
+])
+def test_linear_tiled_split_tiles_repeat(M, K, N, ranks):
+    """The tiled schedule's last partial wave split along K (partial sums in
+    the workspace), twice on one workspace: the scratch must be left clean."""
+    wl = workloads.make_custom(M, K, N, ranks, seed=M + 3 * N, id_mode="runs", p_base=0.1, scale=1.25)
+    dev = to_dev(wl)
+    ref = oracle.lora_linear(wl)
+    ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
+    for call in range(2):
+        y = torch.full((wl.M, wl.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        L.lora_linear(dev["x"], dev["W"], dev["bias"], dev["ids"], dev["pool"], wl.scale, ws, y=y,
+                      path=L.LORA_PATH_TILED)
+        assert L.lora_get_status(ws) == 0
+        assert_close(y, ref, what=f"split tiles M{M} N{N} call {call}")
+
+
 def test_linear_no_bias_and_prebuilt_segments():
     wl = workloads.make_custom(200, 256, 320, [16, 64, 32], seed=77, with_bias=False)
     dev = to_dev(wl)
