@@ -90,10 +90,20 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+# The source file each timed kernel is compiled from; a summary taken on an
+# older copy of that file, or of the headers every kernel includes, is stale.
+KERNEL_SOURCES = {
+    "lora_cluster_kernel": "fused_cluster.cu",
+    "lora_tc_kernel": "fused_tc.cu",
+    "lora_splitk_kernel": "fused_splitk.cu",
+    "seg_build_kernel": "seg_build.cu",
+}
+
+
+def kernel_source_hash(kernel: str):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "segmented_gemm_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in (KERNEL_SOURCES[kernel], "internal.h", "ptx.cuh"):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -107,7 +117,7 @@ def profiled_traffic(kernel: str, workload: str):
     txt = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
     h = re.search(r"source_hash:\s*([0-9a-f]+)", txt)
-    if not m or not h or h.group(1) != kernel_source_hash():
+    if not m or not h or h.group(1) != kernel_source_hash(kernel):
         return None
     return float(m.group(1))
 

@@ -143,9 +143,12 @@ int lora_pool_layout(int32_t num_adapters, const int32_t *true_rank, int32_t K, 
  * Bytes of device workspace needed by every call below for M tokens, output
  * width N and a pool of num_adapters adapters.  The workspace holds the
  * segment table, the tile work lists, the bf16 S scratch, split-K partial sums
- * and a status / counter block.  It must be zero-filled once before its
- * first use (lora_workspace_init does that); every call leaves the counter
- * block zeroed again.
+ * and a status / counter block; for M > 128 its last 20 MiB hold the partial
+ * sums the tiled schedule uses when it splits a mostly empty last wave of
+ * tiles along K (with less workspace than this, a call of that size still
+ * runs, without the split).  It must be zero-filled once before its first
+ * use (lora_workspace_init does that); every call leaves the parts that must
+ * start at zero zeroed again.
  */
 size_t lora_workspace_size(int64_t M, int32_t N, int32_t num_adapters);
 
@@ -222,8 +225,9 @@ int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const 
  * built internally).  The scratch is a file-scope device array of
  * LORA_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that
  * loads the library holds until the process exits; nothing is allocated or
- * freed.  A call whose lora_workspace_size(M, N, num_adapters) exceeds that
- * size returns LORA_ERR_CAPACITY and enqueues nothing.
+ * freed.  A call whose schedule needs more scratch than that returns
+ * LORA_ERR_CAPACITY and enqueues nothing (the tiled schedule's optional
+ * split-tile scratch is used only when it fits as well).
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
