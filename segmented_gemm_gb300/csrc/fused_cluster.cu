@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         named_bar_sync(kBarTmem, 192);
         tc_fence_after();
     }
-    pdl_launch_dependents();   // a dependent launch may start its prologue on the idle SMs
+    pdl_launch_dependents();   // a dependent launch (the segment builder) may start on an idle SM
     cluster_arrive_relaxed();  // my barriers are initialised; peers wait for this before any st.async
     const uint32_t tmem_base = warp < 6 ? *tmem_slot : 0u;
 

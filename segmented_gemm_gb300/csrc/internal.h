@@ -162,7 +162,7 @@ struct SegParams {
 };
 
 // ---- launchers (enqueue only; return the launch status) --------------------
-cudaError_t launch_seg_build(const SegParams &p, cudaStream_t stream);
+cudaError_t launch_seg_build(const SegParams &p, bool pdl, cudaStream_t stream);
 cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cudaStream_t stream);
 cudaError_t launch_s_prep(const float *S, int32_t s_cols, float scale, const TcParams &p, cudaStream_t stream);
 cudaError_t launch_splitk(const TcMaps &maps, const SplitParams &p, int grid, cudaStream_t stream);

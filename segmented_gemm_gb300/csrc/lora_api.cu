@@ -222,7 +222,7 @@ static void fill_segments(void *ws, const WsLayout &L, int64_t M, int32_t A, lor
 }
 
 static int enqueue_segments(const int32_t *ids, int64_t M, const lora_pool_t *pool, const WsLayout &L, void *ws,
-                            cudaStream_t stream)
+                            cudaStream_t stream, bool pdl = false)
 {
     SegParams p;
     p.ids = ids;
@@ -255,12 +255,13 @@ static int enqueue_segments(const int32_t *ids, int64_t M, const lora_pool_t *po
     p.dchunk_adapter = at<int32_t>(ws, L.dchunk_adapter);
     p.counters = at<int32_t>(ws, L.counters);
     p.n_counters = static_cast<int32_t>(L.n_counters);
-    return launch_seg_build(p, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+    return launch_seg_build(p, pdl, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
-// Validate the common arguments and make sure a segment table exists in ws.
+// Validate the common arguments and make sure a segment table exists in ws
+// (unless build is false: the caller enqueues it itself).
 static int prepare(const int32_t *ids, int64_t M, const lora_pool_t *pool, const lora_segments_t *segs, void *ws,
-                   size_t ws_bytes, cudaStream_t stream, WsLayout *L)
+                   size_t ws_bytes, cudaStream_t stream, WsLayout *L, bool build = true)
 {
     int rc = check_pool(pool);
     if (rc) return rc;
@@ -275,7 +276,7 @@ static int prepare(const int32_t *ids, int64_t M, const lora_pool_t *pool, const
         return LORA_OK;
     }
     if (!ids) return LORA_ERR_NULL;
-    return enqueue_segments(ids, M, pool, *L, ws, stream);
+    return build ? enqueue_segments(ids, M, pool, *L, ws, stream) : LORA_OK;
 }
 
 static void fill_tc_params(TcParams &p, const WsLayout &L, void *ws, const lora_pool_t *pool, int64_t M)
@@ -419,8 +420,9 @@ static int run_splitk(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, con
 
 // Weight-streaming schedule (M <= 64, K a multiple of 64): one cluster of C
 // CTAs per 128-feature output tile.  Returns -1 when this device / shape
-// cannot host it, so the caller falls back to split-K.  pdl: the segment
-// builder was enqueued right before this launch on the same stream.
+// cannot host it, so the caller falls back to split-K.  pdl: launch it as a
+// programmatic dependent of a segment builder enqueued right before it
+// (lora_linear enqueues the builder after it instead).
 static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
                        const int32_t *ids, const lora_pool_t *pool, float scale, lora_bf16_t *y, void *ws,
                        const WsLayout &L, bool pdl, cudaStream_t stream)
@@ -585,12 +587,18 @@ int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const 
     if ((path == LORA_PATH_SPLITK || path == LORA_PATH_STREAM) && !lora_id_map) return LORA_ERR_NULL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     WsLayout L;
-    int rc = prepare(lora_id_map, M, pool, segs, ws, ws_bytes, s, &L);
+    // The decode-sized schedule reads no segment table: a table this call
+    // builds is enqueued after it, as a programmatic dependent that runs on a
+    // free SM beside it.
+    const bool stream_path = path == LORA_PATH_STREAM || (path == LORA_PATH_AUTO && M <= kStreamMaxTokens && lora_id_map);
+    int rc = prepare(lora_id_map, M, pool, segs, ws, ws_bytes, s, &L, !stream_path);
     if (rc) return rc;
-    if (path == LORA_PATH_STREAM || (path == LORA_PATH_AUTO && M <= kStreamMaxTokens && lora_id_map)) {
-        const int rc2 = run_cluster(x, M, W, bias, lora_id_map, pool, scale, y, ws, L, segs == nullptr, s);
+    if (stream_path) {
+        const int rc2 = run_cluster(x, M, W, bias, lora_id_map, pool, scale, y, ws, L, false, s);
+        if (rc2 == LORA_OK && !segs) return enqueue_segments(lora_id_map, M, pool, L, ws, s, true);
         if (rc2 >= 0) return rc2;
         if (path == LORA_PATH_STREAM) return LORA_ERR_UNSUPPORTED;
+        if (!segs && (rc = enqueue_segments(lora_id_map, M, pool, L, ws, s))) return rc;
     }
     const bool splitk = path == LORA_PATH_SPLITK || (path == LORA_PATH_AUTO && M <= kSplitMaxTokens && lora_id_map);
     if (splitk) return run_splitk(x, M, W, bias, lora_id_map, pool, scale, y, ws, L, s);

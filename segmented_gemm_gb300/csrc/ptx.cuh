@@ -27,6 +27,13 @@ __device__ __forceinline__ void red_release_gpu_add(int32_t *p, int v)
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ void red_relaxed_gpu_add(int32_t *p, int v)
+{
+    asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ int atom_acq_rel_gpu_add(int32_t *p, int v)
 {
     int old;

@@ -98,11 +98,8 @@ __device__ void tile_group_scan(int a, int b, int *ws2, int *ea, int *eb, int *t
 
 __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
 {
-    // Let the fused kernel that follows start its prologue and weight stream
-    // now; it waits for this grid before reading anything built here.  (The
-    // wait is a no-op for an ordinary launch; it keeps the kernel correct
-    // should it ever be launched as a programmatic dependent itself.)
-    pdl_wait();
+    // Let a fused kernel that follows start its prologue and weight stream
+    // now; it waits for this grid before reading anything built here.
     pdl_launch_dependents();
 
     extern __shared__ int sm[];
@@ -369,6 +366,11 @@ __global__ void __launch_bounds__(kSegThreads, 1) seg_build_kernel(SegParams p)
             p.hdr[HDR_NSJOBS] = carry_j;
         }
     }
+    // Launched as the programmatic dependent of the decode-sized fused
+    // kernel (which reads none of these tables, and whose inputs this grid
+    // only reads), it runs beside that kernel and finishes only after it, so
+    // stream order holds for what follows.  A no-op for an ordinary launch.
+    if (threadIdx.x == 0) pdl_wait();
 }
 
 size_t seg_build_smem_bytes(int32_t A)
@@ -377,7 +379,7 @@ size_t seg_build_smem_bytes(int32_t A)
     return static_cast<size_t>(kSegWarps * (A + 1) + (A + 2) + 32 + 3 * A) * 4;
 }
 
-cudaError_t launch_seg_build(const SegParams &p, cudaStream_t stream)
+cudaError_t launch_seg_build(const SegParams &p, bool pdl, cudaStream_t stream)
 {
     const size_t smem = seg_build_smem_bytes(p.A);
     static int configured[64] = {0};
@@ -389,10 +391,21 @@ cudaError_t launch_seg_build(const SegParams &p, cudaStream_t stream)
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[dev] = 1;
     }
-    // an ordinary launch: measured faster than a programmatic dependent one
-    // here, whose waiting block delays the fused kernel's clusters
-    seg_build_kernel<<<1, kSegThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    // pdl: right after the decode-sized fused kernel, beside which it runs.
+    // Before a fused kernel it is an ordinary launch: a programmatic one
+    // there measured slower, its waiting block delaying the fused kernel's
+    // clusters.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kSegThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, seg_build_kernel, p);
 }
 
 }  // namespace lora
