@@ -47,13 +47,17 @@ constexpr int kWSlot = kBN * kBK * 2;         // 32 KB
 constexpr int kSPanelBytes = kBM * kChunk * 2;   // 4 KB  (128 rows x 16)
 constexpr int kBPanelBytes = kBN * kChunk * 2;   // 8 KB  (256 rows x 16)
 constexpr int kAPanelBytes = kChunk * kBK * 2;   // 2 KB  (16 rows x 64)
-constexpr int kPanelsPerStage = 2;               // expand step: 2 x (S 4 KB + B 8 KB) in one W slot
+constexpr int kPanelsPerStage = 2;               // expand step: 2 chunks x (2 S sets x 4 KB + B 8 KB) per W slot
+constexpr int kSAreaBytes = 2 * kPanelsPerStage * kSPanelBytes;   // S panels [set][chunk] at the slot's start
 constexpr int kTcThreads = 320;   // 10 warps: TMA, MMA, 4 epilogue, 4 x loaders
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 256;
+constexpr int kStageRow = kBN * 2 + 16;   // a staged output row: 512 bytes + 16 of padding
 constexpr size_t kTcSmemBytes =
     kXStages * kXSlot + kWStages * kWSlot + 1024 /*align*/ + 256 /*barriers*/ + 2 * kBN * 2 /*bias of two tiles*/;
 static_assert(kWStages * kWSlot == kBM * kBN * 4, "a split tile's fp32 partials fill the W ring exactly");
+static_assert(kBM * kStageRow <= kXStages * kXSlot, "a staged bf16 output tile fits in the x ring");
+static_assert(kSAreaBytes + kPanelsPerStage * kBPanelBytes <= kWSlot, "an expand stage fits in one W slot");
 
 struct Job {
     int kind;   // 0 shrink, 1 output
@@ -73,11 +77,16 @@ __device__ __forceinline__ Job decode_job(int j, int n_sjobs, const TcParams &p)
     jb.part = kPartFull;
     jb.slot = 0;
     if (j < n_sjobs) {
+        // shrink item j: K piece j % S of shrink job j / S
+        const int S = p.shrink_split, sj = j / S, h = j - sj * S;
         jb.kind = 0;
-        jb.m = p.sjob_tile[j];
+        jb.m = p.sjob_tile[sj];
         jb.n = 0;
-        jb.c0 = p.sjob_c0[j];
-        jb.c1 = p.sjob_c1[j];
+        jb.c0 = p.sjob_c0[sj];
+        jb.c1 = p.sjob_c1[sj];
+        jb.kb0 = (p.kblocks * h) / S;
+        jb.kb1 = (p.kblocks * (h + 1)) / S;
+        jb.slot = h;   // the S panel set it writes
         return jb;
     }
     const int t = j - n_sjobs;
@@ -104,9 +113,19 @@ __device__ __forceinline__ Job decode_job(int j, int n_sjobs, const TcParams &p)
 struct SkPlan {
     int waves, rs, t0, ro, gp;   // whole waves; tail shrink jobs; first tail tile; tail tiles; CTAs sharing them
     int64_t wt;                  // K blocks of the tail tiles
+    int64_t dk;                  // K blocks a CTA whose first item is a K piece of a shrink job is ahead by
+    int nsj;                     // such CTAs (the first nsj)
 };
 
-__device__ __forceinline__ SkPlan sk_plan(int n_sjobs, int n_out, int G, int KB, bool streamk)
+// First K block (in the tail tiles' K blocks laid end to end) of the range
+// of tail-sharing CTA bb: equal runs, plus dk more for each of the first nsj
+// CTAs, which end their whole waves early.
+__device__ __forceinline__ int64_t sk_start(const SkPlan &s, int bb)
+{
+    return ((s.wt - s.dk * s.nsj) * bb) / s.gp + s.dk * min(bb, s.nsj);
+}
+
+__device__ __forceinline__ SkPlan sk_plan(int n_sjobs, int n_out, int G, int KB, bool streamk, int split)
 {
     SkPlan s;
     const int total = n_sjobs + n_out;
@@ -122,6 +141,17 @@ __device__ __forceinline__ SkPlan sk_plan(int n_sjobs, int n_out, int G, int KB,
     s.ro = streamk ? n_out - s.t0 : 0;
     s.gp = G - s.rs;
     s.wt = static_cast<int64_t>(s.ro) * KB;
+    // the shrink items (K pieces of 1 / split) are the first wave's first
+    // items: those CTAs take the missing K blocks in the last wave
+    s.dk = 0;
+    s.nsj = 0;
+    if (streamk && split > 1 && s.rs == 0 && n_sjobs <= s.gp) {
+        const int64_t dk = KB - KB / split;
+        if (s.wt > dk * n_sjobs) {
+            s.dk = dk;
+            s.nsj = n_sjobs;
+        }
+    }
     return s;
 }
 
@@ -143,7 +173,7 @@ __device__ __forceinline__ bool get_item(int q, int b, int G, int n_sjobs, int n
     }
     if (s.ro <= 0) return false;
     const int KB = p.kblocks, bb = b - s.rs;
-    const int64_t r0 = s.wt * bb / s.gp, r1 = s.wt * (bb + 1) / s.gp;
+    const int64_t r0 = sk_start(s, bb), r1 = sk_start(s, bb + 1);
     int64_t f = r0;
     int t = static_cast<int>(f / KB);
     for (int i = 0; i < qt && f < r1; ++i) {
@@ -165,14 +195,14 @@ __device__ __forceinline__ bool sk_single_tail(int b, int t, const SkPlan &s, in
 {
     const int bb = b - s.rs;
     const int64_t end = static_cast<int64_t>(t + 1) * KB, begin = static_cast<int64_t>(t) * KB;
-    const int64_t my_r0 = s.wt * bb / s.gp;
+    const int64_t my_r0 = sk_start(s, bb);
     // my piece must start after the tile's first K block (I am a tail) and
     // the head's CTA must be the previous non-empty one
     int prev = bb - 1;
-    while (prev >= 0 && s.wt * prev / s.gp == s.wt * (prev + 1) / s.gp) --prev;
-    if (prev < 0 || s.wt * prev / s.gp > begin || my_r0 <= begin) return false;
+    while (prev >= 0 && sk_start(s, prev) == sk_start(s, prev + 1)) --prev;
+    if (prev < 0 || sk_start(s, prev) > begin || my_r0 <= begin) return false;
     for (int nb = bb + 1; nb < s.gp; ++nb) {
-        const int64_t r0 = s.wt * nb / s.gp, r1 = s.wt * (nb + 1) / s.gp;
+        const int64_t r0 = sk_start(s, nb), r1 = sk_start(s, nb + 1);
         if (r0 >= end) break;
         if (r1 > r0) return false;   // another tail starts inside the tile
     }
@@ -186,7 +216,7 @@ __device__ __forceinline__ int sk_tails(int b, int t, const SkPlan &s, int KB)
     int n = 0;
     const int64_t end = static_cast<int64_t>(t + 1) * KB;
     for (int bb = b - s.rs + 1; bb < s.gp; ++bb) {
-        const int64_t r0 = s.wt * bb / s.gp, r1 = s.wt * (bb + 1) / s.gp;
+        const int64_t r0 = sk_start(s, bb), r1 = sk_start(s, bb + 1);
         if (r0 >= end) break;
         if (r1 > r0) ++n;
     }
@@ -252,9 +282,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int n_sjobs = (p.mode == kModeExpand) ? 0 : p.hdr[HDR_NSJOBS];
+    // shrink items: every shrink job in p.shrink_split pieces along K
+    const int n_sjobs = (p.mode == kModeExpand) ? 0 : p.hdr[HDR_NSJOBS] * p.shrink_split;
     const int n_out = (p.mode == kModeShrink) ? 0 : p.num_mtiles * p.num_ntiles;
-    const SkPlan sk = sk_plan(n_sjobs, n_out, gridDim.x, p.kblocks, p.streamk != 0);
+    const SkPlan sk = sk_plan(n_sjobs, n_out, gridDim.x, p.kblocks, p.streamk != 0, p.shrink_split);
     Job jb;
 
     if (warp == 0) {
@@ -323,8 +354,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (jb.kind == 1 && jb.c1 > jb.c0 && jb.part != kPartTail) {
                 if (p.mode == kModeLinear) {
                     if (lane == 0) {
-                        wait_flag_geq(p.counters + CNT_FIXED + jb.m, p.tile_njobs[jb.m], abort_flag, status,
-                                      LORA_DEV_TIMEOUT);
+                        // every K piece of every shrink job of the tile
+                        wait_flag_geq(p.counters + CNT_FIXED + jb.m, p.tile_njobs[jb.m] * p.s_sets, abort_flag,
+                                      status, LORA_DEV_TIMEOUT);
                         fence_proxy_async_global();
                     }
                     __syncwarp();
@@ -334,18 +366,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t round = iw / kWStages;
                     if (lane == 0 && round > 0) mbar_wait(&emptyw[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
                     __syncwarp();
-                    uint8_t *wsl = wring + s * kWSlot;   // [S panels | B panels]
+                    uint8_t *wsl = wring + s * kWSlot;   // [S panels [set][chunk] | B panels [chunk]]
                     const int nc = min(kPanelsPerStage, jb.c1 - cg);
-                    if (lane == 0) mbar_expect_tx(&fullw[s], nc * (kSPanelBytes + kBPanelBytes));
+                    if (lane == 0) mbar_expect_tx(&fullw[s], nc * (p.s_sets * kSPanelBytes + kBPanelBytes));
                     __syncwarp();
                     const int ci = cg - jb.c0 + lane;   // chunk index inside the tile
                     const int brow_s = __shfl_sync(0xffffffffu, brow_l, ci & 31);
                     if (lane < nc) {
                         const int c = cg + lane;
                         const int brow = ci < 32 ? brow_s : p.chunk_brow[c];
-                        tma_load_2d(wsl + lane * kSPanelBytes, &tm_s, &fullw[s], 0, c * kBM);
-                        tma_load_2d(wsl + kPanelsPerStage * kSPanelBytes + lane * kBPanelBytes, &tm_b, &fullw[s], 0,
-                                    brow + jb.n * kBN);
+                        for (int h = 0; h < p.s_sets; ++h)
+                            tma_load_2d(wsl + (h * kPanelsPerStage + lane) * kSPanelBytes, &tm_s, &fullw[s], 0,
+                                        h * p.s_set_rows + c * kBM);
+                        tma_load_2d(wsl + kSAreaBytes + lane * kBPanelBytes, &tm_b, &fullw[s], 0, brow + jb.n * kBN);
                     }
                     __syncwarp();
                 }
@@ -424,13 +457,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc_fence_after();
                     if (lane == 0) {
                         const uint32_t sa = smem_u32(wring + sw * kWSlot);
-                        const uint32_t ba = sa + kPanelsPerStage * kSPanelBytes;
+                        const uint32_t ba = sa + kSAreaBytes;
                         const int nc = min(kPanelsPerStage, jb.c1 - cg);
-                        for (int i = 0; i < nc; ++i) {
-                            umma_bf16(d, umma_sdesc(sa + i * kSPanelBytes, 256, kSwizzle32),
-                                      umma_sdesc(ba + i * kBPanelBytes, 256, kSwizzle32), idesc_e, acc);
-                            acc = 1;
-                        }
+                        for (int i = 0; i < nc; ++i)
+                            for (int h = 0; h < p.s_sets; ++h) {   // (S_0 + S_1) B^T, set by set
+                                umma_bf16(d, umma_sdesc(sa + (h * kPanelsPerStage + i) * kSPanelBytes, 256, kSwizzle32),
+                                          umma_sdesc(ba + i * kBPanelBytes, 256, kSwizzle32), idesc_e, acc);
+                                acc = 1;
+                            }
                         umma_commit(&emptyw[sw]);
                     }
                     __syncwarp();
@@ -459,15 +493,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tbias[et] = bv;
                 named_bar_sync(1, 128);
             }
-            mbar_wait(&acc_full[slot], use & 1, abort_flag, status, LORA_DEV_TIMEOUT);
-            tc_fence_after();
-            const uint32_t tbase = tmem_base + slot * kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
+            // the row's original token, read while the MMA still runs
             const int64_t pp = static_cast<int64_t>(jb.m) * kBM + row;
             const bool valid = pp < p.M;
             const int tok = valid ? p.perm[pp] : 0;
+            const bool lora_row = p.mode != kModeExpand || pp >= p.offsets[1];
+            // the CTA's last item: both rings are idle, so an output tile is
+            // staged in the x ring (rows padded to 528 bytes: conflict-free)
+            // and each row goes out as one bulk copy, which writes whole
+            // lines instead of one 32-byte piece of 32 rows per warp store
+            Job nx;
+            const bool staged = p.mode == kModeLinear && jb.kind == 1 && jb.part != kPartTail &&
+                                !get_item(q + 1, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, nx);
+            mbar_wait(&acc_full[slot], use & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + slot * kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
 
             if (jb.kind == 0) {
                 // ---- S panels: mask to the row's own segment, scale, bf16 ----
+                // (panel set jb.slot: the K piece of the shrink job)
+                uint16_t *panels = p.s_panels + static_cast<int64_t>(jb.slot) * p.s_set_rows * kChunk;
                 for (int c = jb.c0; c < jb.c1; ++c) {
                     uint32_t r[16];
                     tmem_ld16(tbase + (c - jb.c0) * kChunk, r);
@@ -475,27 +520,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int32_t rng = p.chunk_rng[c];
                     const bool keep = valid && row >= rng_lo(rng) && row < rng_hi(rng);
                     if (p.mode == kModeLinear) {
-                        uint4 o0, o1;
                         const float sc = keep ? p.scale : 0.f;
-                        o0.x = pack_bf16x2(__uint_as_float(r[0]) * sc, __uint_as_float(r[1]) * sc);
-                        o0.y = pack_bf16x2(__uint_as_float(r[2]) * sc, __uint_as_float(r[3]) * sc);
-                        o0.z = pack_bf16x2(__uint_as_float(r[4]) * sc, __uint_as_float(r[5]) * sc);
-                        o0.w = pack_bf16x2(__uint_as_float(r[6]) * sc, __uint_as_float(r[7]) * sc);
-                        o1.x = pack_bf16x2(__uint_as_float(r[8]) * sc, __uint_as_float(r[9]) * sc);
-                        o1.y = pack_bf16x2(__uint_as_float(r[10]) * sc, __uint_as_float(r[11]) * sc);
-                        o1.z = pack_bf16x2(__uint_as_float(r[12]) * sc, __uint_as_float(r[13]) * sc);
-                        o1.w = pack_bf16x2(__uint_as_float(r[14]) * sc, __uint_as_float(r[15]) * sc);
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.s_panels + (static_cast<int64_t>(c) * kBM + row) * kChunk);
-                        dst[0] = o0;
-                        dst[1] = o1;
+                        uint32_t o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            o[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * sc, __uint_as_float(r[2 * e + 1]) * sc);
+                        uint4 *dst = reinterpret_cast<uint4 *>(panels + (static_cast<int64_t>(c) * kBM + row) * kChunk);
+                        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
                     } else if (keep) {
-                        // standalone shrink: fp32, unscaled, original row, panel columns
+                        // standalone shrink: fp32, unscaled, original row, panel
+                        // columns (the caller's S starts at zero: K pieces add)
                         float4 *dst = reinterpret_cast<float4 *>(p.s_out + static_cast<int64_t>(tok) * p.s_cols +
                                                                  rng_panel(rng) * kChunk);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                                 __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                        for (int v = 0; v < 4; ++v) {
+                            const float4 f4 = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                                          __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                            if (p.shrink_split > 1) atomicAdd(dst + v, f4);
+                            else dst[v] = f4;
+                        }
                     }
                 }
                 tc_fence_before();
@@ -513,21 +557,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // its partials; several tails add theirs with atomics.
                 float4 *part = reinterpret_cast<float4 *>(p.sk_part) + static_cast<int64_t>(jb.slot) * (kBN / 4) * kBM;
                 const bool single = sk_single_tail(blockIdx.x, jb.slot, sk, p.kblocks);
-                for (int cc = 0; cc < kBN / 16; ++cc) {
-                    uint32_t r[16];
-                    tmem_ld16(tbase + cc * 16, r);
-                    tmem_ld_wait16(r);
-                    if (cc == kBN / 16 - 1) {
+                // four 16-column TMEM loads per wait
+                for (int cc = 0; cc < kBN / 16; cc += 4) {
+                    uint32_t r[4][16];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) tmem_ld16(tbase + (cc + h) * 16, r[h]);
+                    tmem_ld_wait16(r[0]);
+#pragma unroll
+                    for (int h = 1; h < 4; ++h) tmem_regs_after_wait16(r[h]);
+                    if (cc + 4 == kBN / 16) {
                         tc_fence_before();
                         mbar_arrive(&acc_empty[slot]);
                     }
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float4 f4 = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                                      __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
-                        if (single) __stcg(part + (cc * 4 + k) * kBM + row, f4);
-                        else atomicAdd(part + (cc * 4 + k) * kBM + row, f4);
-                    }
+                    for (int h = 0; h < 4; ++h)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float4 f4 =
+                                make_float4(__uint_as_float(r[h][4 * k]), __uint_as_float(r[h][4 * k + 1]),
+                                            __uint_as_float(r[h][4 * k + 2]), __uint_as_float(r[h][4 * k + 3]));
+                            float4 *dst = part + ((cc + h) * 4 + k) * kBM + row;
+                            if (single) __stcg(dst, f4);
+                            else atomicAdd(dst, f4);
+                        }
                 }
                 __threadfence();
                 named_bar_sync(1, 128);
@@ -537,8 +589,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // + the tails' partial sums, + bias, bf16, scatter to the
                 // original row ----------------------------------------------
                 const int n0 = jb.n * kBN;
-                const bool lora_row = p.mode != kModeExpand || pp >= p.offsets[1];
                 const bool head = jb.part == kPartHead;
+                uint8_t *srow = xring + row * kStageRow;
                 float4 *part = head ? reinterpret_cast<float4 *>(p.sk_part) + static_cast<int64_t>(jb.slot) * (kBN / 4) * kBM
                                     : nullptr;
                 // the head is its CTA's last item: the W ring is idle now, and
@@ -555,11 +607,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                       sk_bar);
                     }
                     mbar_wait(sk_bar, 0, abort_flag, status, LORA_DEV_TIMEOUT);
-                    // sums built by atomics: leave the scratch zeroed for the next call
-                    if (sk_tails(blockIdx.x, jb.slot, sk, p.kblocks) > 1) {
-#pragma unroll 8
-                        for (int i = 0; i < kBN / 4; ++i) __stcg(part + i * kBM + row, make_float4(0.f, 0.f, 0.f, 0.f));
-                    }
                 }
                 // one 16-column chunk: + partials, + bias (from shared memory) or
                 // the existing y (standalone expand), bf16, store to the row
@@ -579,6 +626,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     const int col = n0 + cc * 16;
                     if (!valid || col >= p.N || !lora_row) return;
+                    if (staged) {
+                        const uint4 *bsrc = reinterpret_cast<const uint4 *>(tbias + cc * 8);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint4 u = out_bias ? bsrc[h] : make_uint4(0u, 0u, 0u, 0u);
+                            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+                            uint32_t o4[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                o4[e] = pack_bf16x2(v[8 * h + 2 * e] + bf16_lo(w4[e]), v[8 * h + 2 * e + 1] + bf16_hi(w4[e]));
+                            *reinterpret_cast<uint4 *>(srow + cc * 32 + h * 16) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+                        }
+                        return;
+                    }
                     uint16_t *dst = p.y + static_cast<int64_t>(tok) * p.N + col;
                     if (p.mode == kModeExpand) {
                         const uint4 *src = reinterpret_cast<const uint4 *>(dst);
@@ -613,22 +674,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         o[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]),
                                           pack_bf16x2(v[12], v[13]), pack_bf16x2(v[14], v[15]));
                 };
-                // two chunks per TMEM wait
-                for (int cc = 0; cc < kBN / 16; cc += 2) {
-                    uint32_t r0[16], r1[16];
-                    tmem_ld16(tbase + cc * 16, r0);
-                    tmem_ld16(tbase + cc * 16 + 16, r1);
-                    tmem_ld_wait16(r0);
-                    tmem_regs_after_wait16(r1);
-                    if (cc + 2 == kBN / 16) {
+                // four chunks per TMEM wait
+                for (int cc = 0; cc < kBN / 16; cc += 4) {
+                    uint32_t r[4][16];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) tmem_ld16(tbase + (cc + h) * 16, r[h]);
+                    tmem_ld_wait16(r[0]);
+#pragma unroll
+                    for (int h = 1; h < 4; ++h) tmem_regs_after_wait16(r[h]);
+                    if (cc + 4 == kBN / 16) {
                         tc_fence_before();
                         mbar_arrive(&acc_empty[slot]);
                     }
-                    emit(cc, r0);
-                    emit(cc + 1, r1);
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) emit(cc + h, r[h]);
+                }
+                if (staged && valid && lora_row && n0 < p.N) {
+                    fence_proxy_async_smem();   // my row's generic-proxy writes -> the bulk copy's reads
+                    bulk_store(p.y + static_cast<int64_t>(tok) * p.N + n0, srow,
+                               static_cast<uint32_t>(min(kBN, p.N - n0)) * 2);
+                    bulk_commit();
+                    bulk_wait_all();
                 }
                 if (head) {   // all partials consumed: the counter is zero again for the next call
                     named_bar_sync(1, 128);
+                    if (sk_tails(blockIdx.x, jb.slot, sk, p.kblocks) > 1) {
+                        // sums built by atomics: leave the scratch zeroed for
+                        // the next call, by bulk copies of a zeroed 32 KB
+                        // piece of the (now idle) W ring
+                        float4 *z = reinterpret_cast<float4 *>(wring);
+                        for (int i = et; i < kWSlot / 16; i += 128) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        fence_proxy_async_smem();
+                        named_bar_sync(1, 128);
+                        if (et == 0) {
+                            for (int i = 0; i < 4; ++i)
+                                bulk_store(reinterpret_cast<uint8_t *>(part) + i * kWSlot, wring, kWSlot);
+                            bulk_commit();
+                            bulk_wait_all();
+                        }
+                    }
                     if (et == 0) p.sk_cnt[jb.slot * kWinCntStride] = 0;
                 }
             }

@@ -81,6 +81,9 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A);
 
 // chunk_rng packing: rows [lo, hi) of the tile, rank panel p of the segment
 __host__ __device__ inline int32_t pack_rng(int lo, int hi, int p) { return lo | (hi << 8) | (p << 16); }
+// S panel sets the workspace holds for the tiled schedule: a shrink job is
+// split into two K halves (one set each) only for M > 128
+inline int tiled_s_sets(int64_t M) { return M > kSplitMaxTokens ? 2 : 1; }
 __host__ __device__ inline int rng_lo(int32_t v) { return v & 0xFF; }
 __host__ __device__ inline int rng_hi(int32_t v) { return (v >> 8) & 0xFF; }
 __host__ __device__ inline int rng_panel(int32_t v) { return (v >> 16) & 0xFF; }
@@ -100,13 +103,16 @@ struct TcParams {
     const uint16_t *bias;      // bf16 [N] or null
     const uint16_t *x;         // bf16 [M, K] (rows gathered by the loader warps)
     uint16_t *y;               // bf16 [M, N]
-    uint16_t *s_panels;        // bf16 [chunks][128][16]
+    uint16_t *s_panels;        // bf16 [sets][chunks][128][16]
     float *s_out;              // fp32 [M, s_cols] (shrink mode)
     const int32_t *perm, *offsets, *hdr;
     const int32_t *tile_chunk_off, *chunk_arow, *chunk_brow, *chunk_rng;
     const int32_t *sjob_tile, *sjob_c0, *sjob_c1, *tile_njobs;
     int32_t *counters;
     int32_t streamk;           // split the last partial wave of output tiles along K
+    int32_t shrink_split;      // K pieces per shrink job; piece h writes S panel set h
+    int32_t s_sets;            // S panel sets the expand steps add up (shrink_split, or 1 for expand)
+    int32_t s_set_rows;        // rows of one S panel set (chunks x 128)
     float *sk_part;            // fp32 [tiles][256/4][128][4]: summed partials of split tiles (zero at rest)
     int32_t *sk_cnt;           // [tiles][kWinCntStride]: partials added per split tile (zero at rest)
 };

@@ -125,7 +125,8 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
         split_s = static_cast<size_t>(L.max_dchunks) * T * kChunk * 2;
     }
     L.n_counters = CNT_FIXED + std::max<size_t>(L.num_mtiles, L.split_tiles) + 8;
-    const size_t tiled_s = static_cast<size_t>(L.max_chunks) * kBM * kChunk * 2;
+    // tiled schedule: S panels, one set per K piece of a shrink job (two for M > 128)
+    const size_t tiled_s = static_cast<size_t>(L.max_chunks) * kBM * kChunk * 2 * tiled_s_sets(M);
     L.s_scratch_bytes = std::max(tiled_s, split_s);
 
     size_t o = 0;
@@ -302,6 +303,16 @@ static void fill_tc_params(TcParams &p, const WsLayout &L, void *ws, const lora_
     p.sjob_c1 = at<int32_t>(ws, L.sjob_c1);
     p.tile_njobs = at<int32_t>(ws, L.tile_njobs);
     p.counters = at<int32_t>(ws, L.counters);
+    // two K halves per shrink job when each half keeps 8 K blocks or more
+    // and the output tiles fill at most four waves of the grid: the first
+    // wave of output tiles then finds S ready when its own K loops end (a
+    // wait that matters only while there are few waves).  Each half writes
+    // its own S panel set; the expand steps add both, (S_a + S_b) B^T =
+    // S_a B^T + S_b B^T, in the fp32 accumulator.
+    const int64_t n_out = static_cast<int64_t>(p.num_mtiles) * p.num_ntiles;
+    p.shrink_split = (tiled_s_sets(M) == 2 && p.kblocks >= 16 && n_out <= 4 * num_sms_current_device()) ? 2 : 1;
+    p.s_sets = p.shrink_split;
+    p.s_set_rows = L.max_chunks * kBM;
 }
 
 // Maps shared by the schedules: A pool (16-row boxes), B pool (16-col panels).
@@ -344,6 +355,7 @@ static int run_tiled(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, cons
         p.sk_cnt = at<int32_t>(ws, L.sk_cnt);
     }
     p.mode = mode;
+    if (mode == kModeExpand) p.s_sets = 1;   // the caller's S, prepared as one panel set
     p.scale = scale;
     p.bias = bias;
     p.x = x;
@@ -358,8 +370,8 @@ static int run_tiled(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, cons
     const void *wsrc = W ? static_cast<const void *>(W) : xsrc;
     if (!encode_2d(&m.w, wsrc, K, W ? N : 1, K * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ERR_CUDA;
     if (!encode_pool_maps(m, pool, p.s_panels, kBN)) return LORA_ERR_CUDA;
-    if (!encode_2d(&m.s, p.s_panels, kChunk, static_cast<uint64_t>(L.max_chunks) * kBM, kChunk * 2, kChunk, kBM,
-                   CU_TENSOR_MAP_SWIZZLE_32B))
+    if (!encode_2d(&m.s, p.s_panels, kChunk, static_cast<uint64_t>(L.max_chunks) * kBM * tiled_s_sets(M), kChunk * 2,
+                   kChunk, kBM, CU_TENSOR_MAP_SWIZZLE_32B))
         return LORA_ERR_CUDA;
     if (mode == kModeExpand) {
         if (launch_s_prep(s_in, s_cols, scale, p, stream) != cudaSuccess) return LORA_ERR_CUDA;
@@ -367,7 +379,7 @@ static int run_tiled(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, cons
     const int sms = num_sms_current_device();
     int64_t jobs = 0;
     if (mode != kModeShrink) jobs += static_cast<int64_t>(p.num_mtiles) * p.num_ntiles;
-    if (mode != kModeExpand) jobs += L.max_sjobs;
+    if (mode != kModeExpand) jobs += static_cast<int64_t>(L.max_sjobs) * p.shrink_split;
     // with stream-K the last partial wave is shared out over every SM
     const int grid = p.streamk ? sms : static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, jobs)));
     return launch_tc(m, p, grid, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;

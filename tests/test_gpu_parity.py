@@ -251,6 +251,24 @@ def test_host_errors():
     assert e.value.code == L.LORA_ERR_SHAPE
 
 
+
+def test_linear_tiled_split_shrink_weighted_waves_repeat():
+    """K >= 1024 with few waves: every shrink job runs as two K halves, each
+    writing its own S panel set that the expand steps add up, and the CTAs
+    that ran a half take more of the last wave's split tiles (160 output
+    tiles + 32 shrink halves on the grid).  Twice on one workspace."""
+    wl = workloads.make_custom(2048, 1024, 2560, [16, 32, 64, 48, 64, 16], seed=4242, id_mode="uniform",
+                               p_base=0.2, scale=0.8)
+    dev = to_dev(wl)
+    ref = oracle.lora_linear(wl)
+    ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
+    for call in range(2):
+        y = torch.full((wl.M, wl.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        L.lora_linear(dev["x"], dev["W"], dev["bias"], dev["ids"], dev["pool"], wl.scale, ws, y=y,
+                      path=L.LORA_PATH_TILED)
+        assert L.lora_get_status(ws) == 0
+        assert_close(y, ref, what=f"split shrink call {call}")
+
 # ---------------------------------------------------------------------------
 # full-size workloads: sampled rows against the oracle
 # ---------------------------------------------------------------------------
@@ -276,7 +294,8 @@ def test_config_full_size_sampled(name):
 
 @pytest.mark.parametrize("M,K,ranks,mode", [(64, 256, [8, 8, 16, 16], "uniform"),
                                             (300, 320, [16, 48, 64, 32], "runs"),
-                                            (257, 128, [64] * 20, "uniform")])
+                                            (257, 128, [64] * 20, "uniform"),
+                                            (300, 1024, [16, 64, 32], "uniform")])   # two K halves add into S
 def test_shrink(M, K, ranks, mode):
     wl = workloads.make_custom(M, K, 64, ranks, seed=M, id_mode=mode, p_base=0.2)
     dev = to_dev(wl)
