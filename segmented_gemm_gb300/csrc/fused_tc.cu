@@ -694,7 +694,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     bulk_store(p.y + static_cast<int64_t>(tok) * p.N + n0, srow,
                                static_cast<uint32_t>(min(kBN, p.N - n0)) * 2);
                     bulk_commit();
-                    bulk_wait_all();
+                    bulk_wait_read_all();   // the row is out of shared memory; y is written before the grid ends
                 }
                 if (head) {   // all partials consumed: the counter is zero again for the next call
                     named_bar_sync(1, 128);
@@ -710,7 +710,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             for (int i = 0; i < 4; ++i)
                                 bulk_store(reinterpret_cast<uint8_t *>(part) + i * kWSlot, wring, kWSlot);
                             bulk_commit();
-                            bulk_wait_all();
+                            bulk_wait_read_all();   // the zeros reach the scratch before the grid ends
                         }
                     }
                     if (et == 0) p.sk_cnt[jb.slot * kWinCntStride] = 0;
