@@ -205,6 +205,30 @@ def test_linear_repeated_calls_reuse_workspace():
         assert L.lora_get_status(ws) == 0
 
 
+@pytest.mark.parametrize("case", ["mix", "all_base", "four"])
+def test_stream_back_to_back_calls(case):
+    """Thirty decode-sized calls on one workspace with no host sync between
+    them: the window sums and counters a call uses must be back at zero when
+    the next one starts (a small pool shrunk whole, no LoRA token, and a
+    pool whose windows every token touches)."""
+    if case == "mix":
+        wl = workloads.make_config("decode")
+    elif case == "all_base":
+        wl = workloads.make_custom(32, 4096, 4096, [16, 32, 64] * 6, seed=21, id_mode="all_base")
+    else:
+        wl = workloads.make_custom(32, 4096, 4096, [64, 32, 16, 64], seed=3, p_base=0.0)
+    dev = to_dev(wl)
+    ref = oracle.lora_linear(wl)
+    ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
+    ys = [torch.full((wl.M, wl.N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(30)]
+    for y in ys:
+        L.lora_linear(dev["x"], dev["W"], dev["bias"], dev["ids"], dev["pool"], wl.scale, ws, y=y,
+                      path=L.LORA_PATH_STREAM)
+    assert L.lora_get_status(ws) == 0
+    for i in (0, 1, 14, 29):
+        assert_close(ys[i], ref, what=f"back to back {case} call {i}")
+
+
 def test_decode_walkthrough_shapes():
     """Page's decode walk-through: ids [0, 2, -1], K 4096, N 12288, ranks 16 / 32."""
     wl = workloads.make_custom(3, 4096, 12288, [16, 16, 32], seed=34, ids=[0, 2, -1])
