@@ -124,14 +124,17 @@ int oracle_build_segments(const int32_t *ids, int64_t M, int32_t num_adapters,
  *   base[t,n] = sum_k x[t,k] W[n,k] + bias[n]
  *   id -1:      y[t,n] = base[t,n]
  *   id i >= 0:  S[t,j] = sum_k x[t,k] A_i[j,k]              (j < r_i)
- *               y[t,n] = base[t,n] + scale * sum_j S[t,j] B_i[n,j]
+ *               y[t,n] = base[t,n] + scale * s_i * sum_j S[t,j] B_i[n,j]
+ * where s_i = adapter_scale[i] (1 when adapter_scale is NULL): an optional
+ * per-adapter factor on the LoRA term (this project's extension; the
+ * page's formula has one implicit scale of 1).
  * y is [nrows, N] fp64, row q holding token rows[q].
  */
 void oracle_lora_linear_rows(const uint16_t *x, int64_t M, int64_t K,
                              const uint16_t *W, int64_t N, const uint16_t *bias,
                              const int32_t *ids, int32_t num_adapters, const int32_t *rank,
                              const uint16_t *a_cat, const uint16_t *b_cat, double scale,
-                             const int64_t *rows, int64_t nrows, double *y)
+                             const double *adapter_scale, const int64_t *rows, int64_t nrows, double *y)
 {
     (void)M;
 #pragma omp parallel
@@ -161,11 +164,12 @@ void oracle_lora_linear_rows(const uint16_t *x, int64_t M, int64_t K,
                 for (int64_t k = 0; k < K; ++k) acc += xr[k] * bf16_to_f64(Ai[j * K + k]);
                 S[j] = acc;
             }
-            /* step 2 (§2.2): y += scale * S B_i^T */
+            /* step 2 (§2.2): y += scale * s_i * S B_i^T */
+            double si = adapter_scale ? adapter_scale[i] : 1.0;
             for (int64_t n = 0; n < N; ++n) {
                 double acc = 0.0;
                 for (int64_t j = 0; j < r; ++j) acc += S[j] * bf16_to_f64(Bi[n * r + j]);
-                yr[n] += scale * acc;
+                yr[n] += scale * si * acc;
             }
         }
         free(xr);
@@ -201,14 +205,15 @@ void oracle_shrink_rows(const uint16_t *x, int64_t M, int64_t K, const int32_t *
 
 /*
  * Step 2 alone (§2.2, §2.3 "added to the y_base rows"), given S:
- *   y[t,n] = y_in[t,n] + scale * sum_{j < r_id} S[t,j] B_id[n,j]   (id >= 0)
- *   y[t,n] = y_in[t,n]                                           (id == -1)
- * S is fp32 [M, s_cols] (the given input, widened exactly); y_in is bf16.
+ *   y[t,n] = y_in[t,n] + scale * s_id * sum_{j < r_id} S[t,j] B_id[n,j]   (id >= 0)
+ *   y[t,n] = y_in[t,n]                                                  (id == -1)
+ * S is fp32 [M, s_cols] (the given input, widened exactly); y_in is bf16;
+ * s_id as in oracle_lora_linear_rows.
  */
 void oracle_expand_rows(const float *S, int64_t s_cols, const uint16_t *y_in, int64_t N,
                         const int32_t *ids, int32_t num_adapters, const int32_t *rank,
-                        const uint16_t *b_cat, double scale, const int64_t *rows,
-                        int64_t nrows, double *y)
+                        const uint16_t *b_cat, double scale, const double *adapter_scale,
+                        const int64_t *rows, int64_t nrows, double *y)
 {
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t q = 0; q < nrows; ++q) {
@@ -219,11 +224,12 @@ void oracle_expand_rows(const float *S, int64_t s_cols, const uint16_t *y_in, in
         if (i < 0) continue;
         int64_t r = rank[i];
         const uint16_t *Bi = b_cat + b_start(rank, i, N);
+        double si = adapter_scale ? adapter_scale[i] : 1.0;
         for (int64_t n = 0; n < N; ++n) {
             double acc = 0.0;
             for (int64_t j = 0; j < r && j < s_cols; ++j)
                 acc += (double)S[t * s_cols + j] * bf16_to_f64(Bi[n * r + j]);
-            yr[n] += scale * acc;
+            yr[n] += scale * si * acc;
         }
     }
 }
@@ -236,8 +242,8 @@ void oracle_expand_rows(const float *S, int64_t s_cols, const uint16_t *y_in, in
 void oracle_lora_linear_elems(const uint16_t *x, int64_t K, const uint16_t *W, int64_t N,
                               const uint16_t *bias, const int32_t *ids, int32_t num_adapters,
                               const int32_t *rank, const uint16_t *a_cat, const uint16_t *b_cat,
-                              double scale, const int64_t *rows, const int64_t *cols, int64_t n,
-                              double *y)
+                              double scale, const double *adapter_scale, const int64_t *rows,
+                              const int64_t *cols, int64_t n, double *y)
 {
 #pragma omp parallel for schedule(dynamic, 16)
     for (int64_t q = 0; q < n; ++q) {
@@ -256,7 +262,7 @@ void oracle_lora_linear_elems(const uint16_t *x, int64_t K, const uint16_t *W, i
                 for (int64_t k = 0; k < K; ++k) s += bf16_to_f64(x[t * K + k]) * bf16_to_f64(Ai[j * K + k]);
                 lora += s * bf16_to_f64(Bi[c * r + j]);
             }
-            acc += scale * lora;
+            acc += scale * (adapter_scale ? adapter_scale[i] : 1.0) * lora;
         }
         y[q] = acc;
     }

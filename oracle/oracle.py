@@ -53,13 +53,13 @@ def _load():
         lib.oracle_build_segments.argtypes = [p, i64, i32, p, p, p, p, p, p, p, p]
         lib.oracle_lora_linear_rows.restype = None
         lib.oracle_lora_linear_rows.argtypes = [p, i64, i64, p, i64, p, p, i32, p, p, p, dbl,
-                                                p, i64, p]
+                                                p, p, i64, p]
         lib.oracle_shrink_rows.restype = None
         lib.oracle_shrink_rows.argtypes = [p, i64, i64, p, i32, p, p, p, i64, i64, p]
         lib.oracle_lora_linear_elems.restype = None
-        lib.oracle_lora_linear_elems.argtypes = [p, i64, p, i64, p, p, i32, p, p, p, dbl, p, p, i64, p]
+        lib.oracle_lora_linear_elems.argtypes = [p, i64, p, i64, p, p, i32, p, p, p, dbl, p, p, p, i64, p]
         lib.oracle_expand_rows.restype = None
-        lib.oracle_expand_rows.argtypes = [p, i64, p, i64, p, i32, p, p, dbl, p, i64, p]
+        lib.oracle_expand_rows.argtypes = [p, i64, p, i64, p, i32, p, p, dbl, p, p, i64, p]
         _lib = lib
     return _lib
 
@@ -82,6 +82,16 @@ def _bits(t: Optional[torch.Tensor]) -> Optional[np.ndarray]:
 
 def _ptr(a: Optional[np.ndarray]):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _adapter_scale(wl) -> Optional[np.ndarray]:
+    """fp64 per-adapter factors of the LoRA term, or None (all 1)."""
+    a = getattr(wl, "adapter_scale", None)
+    if a is None:
+        return None
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    assert a.shape == (len(wl.ranks),)
+    return a
 
 
 def _concat(mats: List[torch.Tensor], K_or_N: int) -> np.ndarray:
@@ -135,9 +145,10 @@ def lora_linear(wl, rows=None, scale: Optional[float] = None) -> np.ndarray:
     r, nrows = _rows_arg(rows, wl.M)
     y = np.zeros((nrows, wl.N), dtype=np.float64)
     s = wl.scale if scale is None else scale
+    asc = _adapter_scale(wl)
     lib.oracle_lora_linear_rows(_ptr(x), wl.M, wl.K, _ptr(W), wl.N, _ptr(bias), _ptr(ids),
                                 len(wl.ranks), _ptr(rk), _ptr(a_cat), _ptr(b_cat), float(s),
-                                _ptr(r), nrows, _ptr(y))
+                                _ptr(asc), _ptr(r), nrows, _ptr(y))
     return y
 
 
@@ -151,6 +162,7 @@ class Prepared:
         self.ids = np.ascontiguousarray(wl.ids.numpy().astype(np.int32))
         self.rk = np.ascontiguousarray(np.asarray(list(wl.ranks) or [0], dtype=np.int32))
         self.a_cat, self.b_cat = _concat(wl.A, wl.K), _concat(wl.B, wl.N)
+        self.asc = _adapter_scale(wl)
 
 
 def lora_linear_elems(prep: "Prepared", rows, cols, scale: Optional[float] = None) -> np.ndarray:
@@ -165,7 +177,8 @@ def lora_linear_elems(prep: "Prepared", rows, cols, scale: Optional[float] = Non
     s = wl.scale if scale is None else scale
     lib.oracle_lora_linear_elems(_ptr(prep.x), wl.K, _ptr(prep.W), wl.N, _ptr(prep.bias),
                                  _ptr(prep.ids), len(wl.ranks), _ptr(prep.rk), _ptr(prep.a_cat),
-                                 _ptr(prep.b_cat), float(s), _ptr(r), _ptr(c), r.size, _ptr(y))
+                                 _ptr(prep.b_cat), float(s), _ptr(prep.asc), _ptr(r), _ptr(c), r.size,
+                                 _ptr(y))
     return y
 
 
@@ -177,7 +190,7 @@ def lora_linear_rows_prepared(prep: "Prepared", rows) -> np.ndarray:
     y = np.zeros((nrows, wl.N), dtype=np.float64)
     lib.oracle_lora_linear_rows(_ptr(prep.x), wl.M, wl.K, _ptr(prep.W), wl.N, _ptr(prep.bias),
                                 _ptr(prep.ids), len(wl.ranks), _ptr(prep.rk), _ptr(prep.a_cat),
-                                _ptr(prep.b_cat), float(wl.scale), _ptr(r), nrows, _ptr(y))
+                                _ptr(prep.b_cat), float(wl.scale), _ptr(prep.asc), _ptr(r), nrows, _ptr(y))
     return y
 
 
@@ -207,7 +220,8 @@ def expand(wl, S: torch.Tensor, y_in: torch.Tensor, scale: Optional[float] = Non
     r, nrows = _rows_arg(rows, wl.M)
     y = np.zeros((nrows, wl.N), dtype=np.float64)
     s = wl.scale if scale is None else scale
+    asc = _adapter_scale(wl)
     lib.oracle_expand_rows(_ptr(S_np), S_np.shape[1], _ptr(yin), wl.N, _ptr(ids),
-                           len(wl.ranks), _ptr(rk), _ptr(b_cat), float(s), _ptr(r), nrows,
+                           len(wl.ranks), _ptr(rk), _ptr(b_cat), float(s), _ptr(asc), _ptr(r), nrows,
                            _ptr(y))
     return y

@@ -42,6 +42,8 @@ class Workload:
     scale: float
     seed: int = 0
     meta: dict = field(default_factory=dict)
+    # per-adapter factor on the LoRA term (e.g. alpha_i / r_i); None = 1 for all
+    adapter_scale: Optional[List[float]] = None
 
     @property
     def num_adapters(self) -> int:
@@ -189,13 +191,14 @@ def make_config(name_or_index, seed: Optional[int] = None) -> Workload:
 
 def make_custom(M: int, K: int, N: int, ranks: List[int], seed: int, ids=None,
                 id_mode: str = "uniform", p_base: float = 0.1, scale: float = 2.0,
-                with_bias: bool = True, w_std: float = 0.02) -> Workload:
+                with_bias: bool = True, w_std: float = 0.02, adapter_scale=None) -> Workload:
     """A free-form workload for edge cases.
 
     ``ids`` may be given explicitly; otherwise ``id_mode`` picks the structure:
     "uniform" (i.i.d. over adapters, then -1 with probability p_base),
     "runs" (contiguous runs of random length), "all_base" (every id -1),
-    "single" (every token uses adapter 0).
+    "single" (every token uses adapter 0).  ``adapter_scale`` is an optional
+    per-adapter factor on the LoRA term; "random" draws one from U(0.25, 2).
     """
     g = torch.Generator().manual_seed(seed)
     nA = len(ranks)
@@ -220,8 +223,11 @@ def make_custom(M: int, K: int, N: int, ranks: List[int], seed: int, ids=None,
         raise ValueError(id_mode)
     a_std = 1.0 / math.sqrt(K)
     x, W, bias, A, B = _draw_values(g, M, K, N, ranks, w_std, a_std, 0.02, 0.01, with_bias)
+    if isinstance(adapter_scale, str) and adapter_scale == "random":
+        adapter_scale = [float(v) for v in (torch.rand(nA, generator=g) * 1.75 + 0.25)]
     return Workload(name=f"custom_M{M}_K{K}_N{N}", M=M, K=K, N=N, ranks=list(ranks),
-                    ids=ids.to(torch.int32), x=x, W=W, bias=bias, A=A, B=B, scale=scale, seed=seed)
+                    ids=ids.to(torch.int32), x=x, W=W, bias=bias, A=A, B=B, scale=scale, seed=seed,
+                    adapter_scale=None if adapter_scale is None else [float(v) for v in adapter_scale])
 
 
 def random_fp32(shape, seed: int, std: float = 1.0) -> torch.Tensor:

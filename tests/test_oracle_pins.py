@@ -106,6 +106,29 @@ def test_single_adapter_equals_merged_weight(which):
     assert _rel_close(y, ref, 1e-10)
 
 
+@pytest.mark.parametrize("which", [0, 2])
+def test_single_adapter_with_factor_equals_merged_weight(which):
+    """Per-adapter factor s_i (for instance alpha_i / r_i): a batch where every
+    token uses adapter i equals x (W + scale * s_i * B_i A_i)^T + bias, with
+    the other adapters' different factors sitting in the table."""
+    wl = workloads.make_custom(20, 72, 40, [16, 8, 32], seed=41 + which, id_mode="single", scale=1.5,
+                               adapter_scale=[0.25, 4.0, 0.75])
+    wl.ids[:] = which
+    y = oracle.lora_linear(wl)
+    Wm = f64(wl.W) + wl.scale * wl.adapter_scale[which] * f64(wl.B[which]) @ f64(wl.A[which])
+    ref = f64(wl.x) @ Wm.T + f64(wl.bias)[None, :]
+    assert _rel_close(y, ref, 1e-10)
+
+
+def test_equal_factors_equal_a_global_scale():
+    """Every adapter with the same factor c is the same layer as scale * c."""
+    wl = workloads.make_custom(26, 64, 48, [16, 32, 8], seed=44, id_mode="uniform", p_base=0.2,
+                               scale=1.25, adapter_scale=[0.625] * 3)
+    y = oracle.lora_linear(wl)
+    wl.adapter_scale = None
+    assert _rel_close(y, oracle.lora_linear(wl, scale=1.25 * 0.625), 1e-12)
+
+
 def _brute(wl):
     """Per-token loop written out in Python, for tiny shapes only."""
     x, W, b = f64(wl.x), f64(wl.W), f64(wl.bias) if wl.bias is not None else None
@@ -119,16 +142,18 @@ def _brute(wl):
             if 0 <= i < len(wl.ranks):
                 A, B = f64(wl.A[i]), f64(wl.B[i])
                 S = [sum(x[t, k] * A[j, k] for k in range(wl.K)) for j in range(wl.ranks[i])]
-                v += wl.scale * sum(S[j] * B[n, j] for j in range(wl.ranks[i]))
+                si = 1.0 if wl.adapter_scale is None else wl.adapter_scale[i]
+                v += wl.scale * si * sum(S[j] * B[n, j] for j in range(wl.ranks[i]))
             out[t, n] = v
     return out
 
 
-@pytest.mark.parametrize("seed", [0, 1, 2])
-def test_per_token_brute_force(seed):
-    """§2.1 / §3.4: each token gets its own base row plus only its own adapter."""
+@pytest.mark.parametrize("seed,adapter_scale", [(0, None), (1, None), (2, None), (3, [0.5, 3.0, 1.25])])
+def test_per_token_brute_force(seed, adapter_scale):
+    """§2.1 / §3.4: each token gets its own base row plus only its own adapter
+    (and, when given, only its own adapter's factor on the LoRA term)."""
     wl = workloads.make_custom(8, 24, 16, [8, 16, 4], seed=seed, id_mode="uniform", p_base=0.3,
-                               scale=0.5 + seed)
+                               scale=0.5 + seed, adapter_scale=adapter_scale)
     wl.ids[0] = -1
     wl.ids[1] = 2
     wl.ids[2] = 9          # names no adapter: treated as base only
@@ -200,8 +225,10 @@ def test_shrink_matches_library_gemm():
         assert _rel_close(S[t], want)
 
 
-def test_expand_matches_library_gemm():
-    wl = workloads.make_custom(18, 40, 56, [16, 32], seed=22, id_mode="uniform", p_base=0.3)
+@pytest.mark.parametrize("adapter_scale", [None, [2.5, 0.4]])
+def test_expand_matches_library_gemm(adapter_scale):
+    wl = workloads.make_custom(18, 40, 56, [16, 32], seed=22, id_mode="uniform", p_base=0.3,
+                               adapter_scale=adapter_scale)
     S = workloads.random_fp32((wl.M, 32), seed=5)
     y_in = workloads.random_fp32((wl.M, wl.N), seed=6).to(torch.bfloat16)
     y = oracle.expand(wl, S, y_in, scale=1.5)
@@ -209,7 +236,8 @@ def test_expand_matches_library_gemm():
         i = int(wl.ids[t])
         want = f64(y_in[t])
         if i >= 0:
-            want = want + 1.5 * S[t, :wl.ranks[i]].double().numpy() @ f64(wl.B[i]).T
+            si = 1.0 if adapter_scale is None else adapter_scale[i]
+            want = want + 1.5 * si * S[t, :wl.ranks[i]].double().numpy() @ f64(wl.B[i]).T
         assert _rel_close(y[t], want)
 
 
