@@ -8,7 +8,11 @@
  * x is hidden_states [M, K], W the base weight [N, K] (nn.Linear layout), bias [N]
  * or none, lora_id_map [M] int32 with -1 meaning "base only" (§2.1), A_i [r_i, K]
  * and B_i [N, r_i] the adapter factors (§1.1), and the result is [M, N].
- * `scale` is one fp32 scalar per call (the page's formula has scale 1).
+ * `scale` is one fp32 scalar per call (the page's formula has scale 1).  A
+ * pool may also carry one fp32 factor s_i per adapter (for instance the usual
+ * alpha_i / r_i); adapter i's delta is then multiplied by scale * s_i.  This
+ * per-adapter factor is an extension of this library: the page applies one
+ * scale to every adapter, which is the case of a pool without factors.
  *
  * Conventions for every entry point
  *   - Pointers named "device" are CUDA device pointers; "host" ones are host
@@ -47,7 +51,7 @@ enum {
     LORA_OK = 0,
     LORA_ERR_NULL = 1,          /* a required pointer is NULL */
     LORA_ERR_SHAPE = 2,         /* negative M, K or N not positive multiples of 8, too many adapters */
-    LORA_ERR_ALIGN = 3,         /* a tensor base address is not 16-byte aligned */
+    LORA_ERR_ALIGN = 3,         /* a tensor base address is not 16-byte aligned (4 for adapter_scale) */
     LORA_ERR_RANK = 4,          /* a rank outside [1, 64], or max_rank not a padded rank */
     LORA_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than lora_workspace_size() */
     LORA_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch error, bad device) */
@@ -79,6 +83,11 @@ enum {
  *        sits at b_offset[i] + (j/16)*N*16 + n*16 + j%16 (columns >= true rank
  *        are zero).  b_offset[i] is a multiple of 16.
  * a_pool, b_pool, a_offset, b_offset, rank: DEVICE pointers, caller-owned.
+ * adapter_scale: DEVICE fp32 [num_adapters], adapter i's factor s_i on top of
+ *        the call's scale (4-byte aligned), or NULL for s_i = 1 everywhere.
+ *        Read by lora_linear and lora_expand (lora_shrink returns unscaled
+ *        S); a call that reads it needs its lora_id_map even when it is
+ *        given a prebuilt segment table.
  * a_elems / b_elems (host values) are the total element counts of the pools;
  * num_adapters, max_rank (largest rank[i]), K and N are host values.
  * lora_pool_layout() computes offsets, padded ranks and sizes for a set of
@@ -96,6 +105,7 @@ typedef struct {
     int32_t max_rank;
     int32_t K;
     int32_t N;
+    const float *adapter_scale;
 } lora_pool_t;
 
 /*
@@ -178,7 +188,8 @@ int lora_shrink(const lora_bf16_t *x, int64_t M, const int32_t *lora_id_map,
 
 /*
  * §2.2 second product alone, added into the output rows (§2.3):
- * y[t, :] += scale * S[t, :rank] B_{id[t]}^T for id >= 0; id -1 rows untouched.
+ * y[t, :] += scale * s_id * S[t, :rank] B_{id[t]}^T for id >= 0 (s_id: the
+ * pool's per-adapter factor, 1 without one); id -1 rows untouched.
  * S: DEVICE fp32 [M, s_cols] (s_cols >= pool->max_rank), original order.
  * y: DEVICE bf16 [M, pool->N], read and written (rounded once to bf16).
  */
@@ -188,7 +199,8 @@ int lora_expand(const float *S, int32_t s_cols, int64_t M, const int32_t *lora_i
 
 /*
  * The fused layer (§2.1 operator contract, §2.3 one dispatch for all
- * segments): y = x W^T + bias + scale * (x A_id^T) B_id^T per token.
+ * segments): y = x W^T + bias + scale * s_id * (x A_id^T) B_id^T per token
+ * (s_id: the pool's per-adapter factor, 1 without one).
  * x: DEVICE bf16 [M, K]; W: DEVICE bf16 [N, K]; bias: DEVICE bf16 [N] or NULL;
  * lora_id_map: DEVICE int32 [M]; y: DEVICE bf16 [M, N] (written, never read).
  * K and N are taken from the pool.  segs: a table built for lora_id_map and

@@ -76,6 +76,13 @@ struct StSeg {
     int arow;     // shrink: first A pool row of the window
 };
 
+// the barriers and tables that follow the reduction area fit kClMisc bytes
+static_assert((2 * kClMaxStages + kStMaxRegions + 1) * 8 + 10 * 4 + kSplitBN * 2 + 64 * 4 * 2 +
+                      kStMaxSegs * static_cast<int>(sizeof(StSeg)) + kStMaxWinCta * 4 * 3 + kStMaxWinCta * kStWin * 4 +
+                      kStMaxRuns * kStWin * 4 + (kStMaxWinAll / 32) * 4 * 2 + kStMaxWinList * 4 <=
+                  kClMisc,
+              "cluster kernel tables overflow their shared-memory area");
+
 __device__ __forceinline__ void tma_load_3d_st(void *dst, const CUtensorMap *m, uint64_t *bar, int x, int y, int z)
 {
     asm volatile(
@@ -192,7 +199,8 @@ __global__ void __launch_bounds__(kClThreads, 1)
     int *n_exp = ivars + 4;        // 1: segs[*n_segs] is my expand segment
     uint16_t *s_bias = reinterpret_cast<uint16_t *>(ivars + 10);   // [128] my output rows' bias (16-byte aligned)
     int *s_ids = reinterpret_cast<int *>(s_bias + kSplitBN);         // [64] token ids (-2 past M)
-    StSeg *segs = reinterpret_cast<StSeg *>(s_ids + 64);
+    float *s_tsc = reinterpret_cast<float *>(s_ids + 64);             // [64] token's LoRA scale (scale x factor)
+    StSeg *segs = reinterpret_cast<StSeg *>(s_tsc + 64);
     int *s_win_panel = reinterpret_cast<int *>(segs + kStMaxSegs);   // [kStMaxWinCta] first panel of my windows
     int *s_win_acc = s_win_panel + kStMaxWinCta;       // [kStMaxWinCta] window-sum / counter index of my windows
     int *s_win_info = s_win_acc + kStMaxWinCta;        // [kStMaxWinCta][8] adapter of each panel, -1 if absent
@@ -385,13 +393,13 @@ __global__ void __launch_bounds__(kClThreads, 1)
                             f[i][1] = __ldcg(src + 1);
                         }
                     }
-                    const float sc = p.scale;
 #pragma unroll
                     for (int i = 0; i < kMaxPer; ++i) {
                         const int pc = lt + 128 * i;
                         if (pc >= pieces) break;
                         const int j = pc / (T * 2), rem = pc - j * T * 2;
                         const int t = rem >> 1, c = rem & 1;
+                        const float sc = s_tsc[t];   // used only for tokens of the panel's adapter
                         const float4 f0 = f[i][0], f1 = f[i][1];
                         const uint4 o =
                             make_uint4(pack_bf16x2(f0.x * sc, f0.y * sc), pack_bf16x2(f0.z * sc, f0.w * sc),
@@ -520,8 +528,12 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const bool v0 = id0 >= 0 && id0 < p.A, v1 = id1 >= 0 && id1 < p.A;
             const int64_t ao0 = v0 ? p.a_offset[id0] : 0, ao1 = v1 ? p.a_offset[id1] : 0;
             const int rk0 = v0 ? p.rank[id0] : 0, rk1 = v1 ? p.rank[id1] : 0;
+            const bool fac = p.adapter_scale != nullptr;
+            const float f0 = fac && v0 ? p.adapter_scale[id0] : 1.f, f1 = fac && v1 ? p.adapter_scale[id1] : 1.f;
             s_ids[lane] = id0;
             s_ids[lane + 32] = id1;
+            s_tsc[lane] = p.scale * f0;
+            s_tsc[lane + 32] = p.scale * f1;
             const int pa0 = static_cast<int>(ao0 / p.K) / kChunk, np0 = v0 ? min(rk0 / kChunk, LORA_MAX_RANK / kChunk) : 0;
             const int pa1 = static_cast<int>(ao1 / p.K) / kChunk, np1 = v1 ? min(rk1 / kChunk, LORA_MAX_RANK / kChunk) : 0;
             // the windows the batch touches, ascending (s_wlist)

@@ -318,11 +318,12 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     const int gch = arow / kChunk;
                     if (gch < D) {
                         const int adapter = p.dchunk_adapter[gch];
+                        const float sc = p.adapter_scale ? p.scale * p.adapter_scale[adapter] : p.scale;
                         uint16_t *dst = p.s_panels + static_cast<int64_t>(gch) * T * kChunk + (arow % kChunk);
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const int t = c + e;
-                            const float v = (t < p.M && p.ids[t] == adapter) ? a[e] * p.scale : 0.f;
+                            const float v = (t < p.M && p.ids[t] == adapter) ? a[e] * sc : 0.f;
                             dst[static_cast<int64_t>(t) * kChunk] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFF);
                         }
                     }

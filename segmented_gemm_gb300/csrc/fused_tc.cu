@@ -498,6 +498,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool valid = pp < p.M;
             const int tok = valid ? p.perm[pp] : 0;
             const bool lora_row = p.mode != kModeExpand || pp >= p.offsets[1];
+            // the LoRA scale of my row: the call's scale times its adapter's
+            // factor (rows outside every segment are masked anyway)
+            float row_sc = p.scale;
+            if (p.adapter_scale && jb.kind == 0 && p.mode == kModeLinear && valid) {
+                const int id = p.ids[tok];
+                row_sc *= (id >= 0 && id < p.num_adapters) ? __ldg(p.adapter_scale + id) : 0.f;
+            }
             // the CTA's last item: both rings are idle, so an output tile is
             // staged in the x ring (rows padded to 528 bytes: conflict-free)
             // and each row goes out as one bulk copy, which writes whole
@@ -520,7 +527,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int32_t rng = p.chunk_rng[c];
                     const bool keep = valid && row >= rng_lo(rng) && row < rng_hi(rng);
                     if (p.mode == kModeLinear) {
-                        const float sc = keep ? p.scale : 0.f;
+                        const float sc = keep ? row_sc : 0.f;
                         uint32_t o[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
@@ -740,14 +747,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // Standalone expand: turn the caller's fp32 S [M, s_cols] (original token
 // order) into the kernel's bf16 S panels (permuted tile rows, each row masked
-// to its own segment's rank panels, multiplied by scale).  One CTA per token
-// tile, one thread per tile row.
+// to its own segment's rank panels, multiplied by scale and by its adapter's
+// factor).  One CTA per token tile, one thread per tile row.
 __global__ void __launch_bounds__(kBM) s_prep_kernel(const float *S, int32_t s_cols, float scale, TcParams p)
 {
     const int m = blockIdx.x, row = threadIdx.x;
     const int64_t pp = static_cast<int64_t>(m) * kBM + row;
     const bool valid = pp < p.M;
     const int tok = valid ? p.perm[pp] : 0;
+    if (p.adapter_scale && valid) {
+        const int id = p.ids[tok];
+        scale *= (id >= 0 && id < p.num_adapters) ? p.adapter_scale[id] : 0.f;
+    }
     for (int c = p.tile_chunk_off[m]; c < p.tile_chunk_off[m + 1]; ++c) {
         const int32_t rng = p.chunk_rng[c];
         const bool keep = valid && row >= rng_lo(rng) && row < rng_hi(rng);

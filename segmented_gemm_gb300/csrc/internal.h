@@ -100,6 +100,9 @@ struct TcParams {
     int64_t M;
     int32_t N, K, kblocks, num_mtiles, num_ntiles, group_m, mode, s_cols;
     float scale;
+    int32_t num_adapters;
+    const int32_t *ids;        // lora_id_map (original token order); read when adapter_scale is set
+    const float *adapter_scale;   // per-adapter factor on top of scale, or null (all 1)
     const uint16_t *bias;      // bf16 [N] or null
     const uint16_t *x;         // bf16 [M, K] (rows gathered by the loader warps)
     uint16_t *y;               // bf16 [M, N]
@@ -121,6 +124,7 @@ struct SplitParams {
     int64_t M;
     int32_t N, K, T_pad, kblocks, NT, stages, tmem_cols, A;
     float scale;
+    const float *adapter_scale;   // per-adapter factor on top of scale, or null (all 1)
     const uint16_t *bias;
     uint16_t *y;
     const int32_t *ids, *hdr, *dchunk_arow, *dchunk_brow, *dchunk_adapter;
@@ -139,6 +143,7 @@ struct ClusterParams {
     int64_t M;
     int32_t N, K, T_pad, C, NT, kblocks, stages, max_regions, max_win_str;
     float scale;
+    const float *adapter_scale;   // per-adapter factor on top of scale, or null (all 1)
     const uint16_t *bias;
     const uint16_t *x;         // bf16 [M, K] (read through the x tensor map)
     uint16_t *y;

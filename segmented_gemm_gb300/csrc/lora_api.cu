@@ -194,6 +194,7 @@ static int check_pool(const lora_pool_t *pool)
     if (pool->num_adapters > 0) {
         if (!pool->a_pool || !pool->b_pool || !pool->a_offset || !pool->b_offset || !pool->rank) return LORA_ERR_NULL;
         if (!aligned16(pool->a_pool) || !aligned16(pool->b_pool)) return LORA_ERR_ALIGN;
+        if (reinterpret_cast<uintptr_t>(pool->adapter_scale) & 3) return LORA_ERR_ALIGN;
         if (pool->max_rank < LORA_RANK_ALIGN || pool->max_rank > LORA_MAX_RANK || (pool->max_rank % LORA_RANK_ALIGN))
             return LORA_ERR_RANK;
         if (pool->a_elems <= 0 || pool->b_elems <= 0 || (pool->a_elems % pool->K) || (pool->b_elems % kChunk))
@@ -284,6 +285,8 @@ static void fill_tc_params(TcParams &p, const WsLayout &L, void *ws, const lora_
 {
     std::memset(&p, 0, sizeof p);
     p.M = M;
+    p.num_adapters = pool->num_adapters;
+    p.adapter_scale = pool->num_adapters ? pool->adapter_scale : nullptr;
     p.N = pool->N;
     p.K = pool->K;
     p.kblocks = (pool->K + kBK - 1) / kBK;
@@ -341,7 +344,7 @@ static bool encode_pool_maps(TcMaps &m, const lora_pool_t *pool, const void *dum
 }
 
 static int run_tiled(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
-                     const lora_pool_t *pool, float scale, lora_bf16_t *y, void *ws, size_t ws_bytes, const WsLayout &L,
+                     const int32_t *ids, const lora_pool_t *pool, float scale, lora_bf16_t *y, void *ws, size_t ws_bytes, const WsLayout &L,
                      int mode, float *s_out, int32_t s_cols, const float *s_in, cudaStream_t stream)
 {
     TcParams p;
@@ -355,6 +358,8 @@ static int run_tiled(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, cons
         p.sk_cnt = at<int32_t>(ws, L.sk_cnt);
     }
     p.mode = mode;
+    p.ids = ids;
+    if (mode == kModeShrink) p.adapter_scale = nullptr;   // S leaves unscaled
     if (mode == kModeExpand) p.s_sets = 1;   // the caller's S, prepared as one panel set
     p.scale = scale;
     p.bias = bias;
@@ -407,6 +412,7 @@ static int run_splitk(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, con
     if ((RTmax + G - 1) / G + 2 + (p.NT + G - 1) / G + 2 > splitk_max_runs()) return LORA_ERR_SHAPE;
     p.A = pool->num_adapters;
     p.scale = scale;
+    p.adapter_scale = pool->num_adapters ? pool->adapter_scale : nullptr;
     p.bias = bias;
     p.y = y;
     p.ids = ids;
@@ -497,6 +503,7 @@ static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, co
     // the unit list is then known at launch and the shrink can go first
     p.all_windows = p.windows_all <= L.max_win_str ? 1 : 0;
     p.scale = scale;
+    p.adapter_scale = pool->num_adapters ? pool->adapter_scale : nullptr;
     p.bias = bias;
     p.x = x;
     p.y = y;
@@ -597,6 +604,7 @@ int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const 
     if (path == LORA_PATH_SPLITK && M > kSplitMaxTokens) return LORA_ERR_SHAPE;
     if (path == LORA_PATH_STREAM && (M > kStreamMaxTokens || (pool && (pool->K % kBK)))) return LORA_ERR_SHAPE;
     if ((path == LORA_PATH_SPLITK || path == LORA_PATH_STREAM) && !lora_id_map) return LORA_ERR_NULL;
+    if (pool && pool->adapter_scale && !lora_id_map) return LORA_ERR_NULL;   // the factors are looked up by id
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     WsLayout L;
     // The decode-sized schedule reads no segment table: a table this call
@@ -614,7 +622,7 @@ int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const 
     }
     const bool splitk = path == LORA_PATH_SPLITK || (path == LORA_PATH_AUTO && M <= kSplitMaxTokens && lora_id_map);
     if (splitk) return run_splitk(x, M, W, bias, lora_id_map, pool, scale, y, ws, L, s);
-    return run_tiled(x, M, W, bias, pool, scale, y, ws, ws_bytes, L, kModeLinear, nullptr, 0, nullptr, s);
+    return run_tiled(x, M, W, bias, lora_id_map, pool, scale, y, ws, ws_bytes, L, kModeLinear, nullptr, 0, nullptr, s);
 }
 
 int lora_linear(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
@@ -641,7 +649,7 @@ int lora_shrink(const lora_bf16_t *x, int64_t M, const int32_t *lora_id_map, con
     if (cudaMemsetAsync(S, 0, static_cast<size_t>(M) * s_cols * sizeof(float), s) != cudaSuccess)
         return LORA_ERR_CUDA;
     if (pool->num_adapters == 0) return LORA_OK;
-    return run_tiled(x, M, nullptr, nullptr, pool, 1.0f, nullptr, ws, ws_bytes, L, kModeShrink, S, s_cols, nullptr, s);
+    return run_tiled(x, M, nullptr, nullptr, lora_id_map, pool, 1.0f, nullptr, ws, ws_bytes, L, kModeShrink, S, s_cols, nullptr, s);
 }
 
 int lora_expand(const float *S, int32_t s_cols, int64_t M, const int32_t *lora_id_map, const lora_pool_t *pool,
@@ -651,6 +659,7 @@ int lora_expand(const float *S, int32_t s_cols, int64_t M, const int32_t *lora_i
     if (M < 0) return LORA_ERR_SHAPE;
     if (M == 0) return check_pool(pool);
     if (!S || !y || !pool) return LORA_ERR_NULL;
+    if (pool->adapter_scale && !lora_id_map) return LORA_ERR_NULL;   // the factors are looked up by id
     if (!aligned16(S) || !aligned16(y)) return LORA_ERR_ALIGN;
     if (s_cols < std::max(pool->max_rank, 1)) return LORA_ERR_SHAPE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -658,7 +667,7 @@ int lora_expand(const float *S, int32_t s_cols, int64_t M, const int32_t *lora_i
     int rc = prepare(lora_id_map, M, pool, segs, ws, ws_bytes, s, &L);
     if (rc) return rc;
     if (pool->num_adapters == 0) return LORA_OK;
-    return run_tiled(nullptr, M, nullptr, nullptr, pool, scale, y, ws, ws_bytes, L, kModeExpand, nullptr, s_cols, S, s);
+    return run_tiled(nullptr, M, nullptr, nullptr, lora_id_map, pool, scale, y, ws, ws_bytes, L, kModeExpand, nullptr, s_cols, S, s);
 }
 
 int lora_get_status(void *ws, lora_stream_t stream, int32_t *status)

@@ -36,7 +36,7 @@ class lora_pool_t(ctypes.Structure):
                 ("a_offset", ctypes.c_void_p), ("b_offset", ctypes.c_void_p),
                 ("rank", ctypes.c_void_p), ("a_elems", ctypes.c_int64), ("b_elems", ctypes.c_int64),
                 ("num_adapters", ctypes.c_int32), ("max_rank", ctypes.c_int32),
-                ("K", ctypes.c_int32), ("N", ctypes.c_int32)]
+                ("K", ctypes.c_int32), ("N", ctypes.c_int32), ("adapter_scale", ctypes.c_void_p)]
 
 
 class lora_segments_t(ctypes.Structure):
@@ -136,15 +136,19 @@ class LoraPool:
     desc: lora_pool_t
     true_ranks: List[int]
     padded_ranks: List[int]
+    adapter_scale: Optional[torch.Tensor] = None   # fp32 [num_adapters] factors, or None (all 1)
 
     @property
     def num_adapters(self):
         return self.desc.num_adapters
 
 
-def build_pool(A: List[torch.Tensor], B: List[torch.Tensor], K: int, N: int, device="cuda") -> LoraPool:
+def build_pool(A: List[torch.Tensor], B: List[torch.Tensor], K: int, N: int, device="cuda",
+               adapter_scale: Optional[Sequence[float]] = None) -> LoraPool:
     """Arrange adapters A_i [r_i, K], B_i [N, r_i] into the pool layout of
-    include/lora.h (rank-grouped; A rows and B panels zero-padded to 16)."""
+    include/lora.h (rank-grouped; A rows and B panels zero-padded to 16).
+    ``adapter_scale``: optional per-adapter factors s_i (adapter i's delta is
+    multiplied by the call's scale times s_i)."""
     ranks = [int(a.shape[0]) for a in A]
     a_off, b_off, rpad, a_elems, b_elems = lora_pool_layout(ranks, K, N)
     bf = torch.bfloat16
@@ -161,9 +165,14 @@ def build_pool(A: List[torch.Tensor], B: List[torch.Tensor], K: int, N: int, dev
     a_offset = torch.tensor(a_off or [0], dtype=torch.int64, device=device)
     b_offset = torch.tensor(b_off or [0], dtype=torch.int64, device=device)
     rank = torch.tensor(rpad or [0], dtype=torch.int32, device=device)
+    asc = None
+    if adapter_scale is not None:
+        assert len(adapter_scale) == len(A)
+        asc = torch.tensor([float(v) for v in adapter_scale] or [1.0], dtype=torch.float32, device=device)
     desc = lora_pool_t(a_pool.data_ptr(), b_pool.data_ptr(), a_offset.data_ptr(), b_offset.data_ptr(),
-                       rank.data_ptr(), a_elems, b_elems, len(A), max(rpad) if rpad else 0, K, N)
-    return LoraPool(a_pool, b_pool, a_offset, b_offset, rank, desc, ranks, rpad)
+                       rank.data_ptr(), a_elems, b_elems, len(A), max(rpad) if rpad else 0, K, N,
+                       asc.data_ptr() if asc is not None else None)
+    return LoraPool(a_pool, b_pool, a_offset, b_offset, rank, desc, ranks, rpad, asc)
 
 
 # ---------------------------------------------------------------------------

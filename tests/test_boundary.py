@@ -76,3 +76,24 @@ def test_null_arguments_rejected_without_gpu(lib):
     assert rc == L.LORA_ERR_NULL
     rc = lib.lora_linear_ex(None, -1, None, None, None, None, ctypes.c_float(1.0), None, None, None, 0, None, 0)
     assert rc == L.LORA_ERR_SHAPE
+
+
+def _fake_pool(adapter_scale):
+    # addresses are never dereferenced: validation rejects the call first
+    return L.lora_pool_t(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 64 * 16, 64 * 16, 1, 16, 64, 64, adapter_scale)
+
+
+def test_adapter_factors_need_ids_and_alignment_without_gpu(lib):
+    f = ctypes.c_float(1.0)
+    # factors are looked up by token id: a prebuilt table alone is not enough
+    pool = _fake_pool(0x6000)
+    rc = lib.lora_linear_ex(0x7000, 4, 0x8000, None, None, ctypes.byref(pool), f, None, 0x9000, 0xA000, 1 << 20,
+                            None, 0)
+    assert rc == L.LORA_ERR_NULL
+    rc = lib.lora_expand(0x7000, 16, 4, None, ctypes.byref(pool), None, f, 0x9000, 0xA000, 1 << 20, None)
+    assert rc == L.LORA_ERR_NULL
+    # the fp32 factor table must be 4-byte aligned
+    pool = _fake_pool(0x6002)
+    rc = lib.lora_linear_ex(0x7000, 4, 0x8000, None, 0xB000, ctypes.byref(pool), f, None, 0x9000, 0xA000, 1 << 20,
+                            None, 0)
+    assert rc == L.LORA_ERR_ALIGN

@@ -21,7 +21,7 @@ TOL = 2e-2
 def to_dev(wl):
     d = "cuda"
     return dict(x=wl.x.to(d), W=wl.W.to(d), bias=None if wl.bias is None else wl.bias.to(d),
-                ids=wl.ids.to(d), pool=L.build_pool(wl.A, wl.B, wl.K, wl.N, d))
+                ids=wl.ids.to(d), pool=L.build_pool(wl.A, wl.B, wl.K, wl.N, d, adapter_scale=wl.adapter_scale))
 
 
 def rel_err(gpu, ref):
@@ -344,3 +344,73 @@ def test_expand(M, N, ranks, mode):
     assert_close(y, ref, what="expand")
     base_rows = (wl.ids < 0).nonzero().flatten()
     assert torch.equal(y[base_rows.to('cuda')].cpu(), y0[base_rows])    # -1 rows untouched
+
+
+# ---------------------------------------------------------------------------
+# per-adapter factors (adapter i's delta scaled by scale * s_i)
+# ---------------------------------------------------------------------------
+
+FACTOR_CASES = [
+    # M, K, N, ranks, paths
+    (7, 256, 384, [16, 32, 64, 16], (L.LORA_PATH_STREAM, L.LORA_PATH_SPLITK, L.LORA_PATH_TILED)),
+    (64, 512, 640, [64, 16, 32, 48, 16], (L.LORA_PATH_STREAM, L.LORA_PATH_SPLITK, L.LORA_PATH_TILED)),
+    (120, 320, 256, [32, 16, 64], (L.LORA_PATH_SPLITK, L.LORA_PATH_TILED)),
+    (700, 1024, 512, [16, 64, 32, 48, 16, 64], (L.LORA_PATH_TILED,)),   # K halves, split last wave
+]
+
+
+@pytest.mark.parametrize("M,K,N,ranks,paths", FACTOR_CASES)
+def test_linear_adapter_factors_every_path(M, K, N, ranks, paths):
+    factors = [0.25 + 0.5 * i for i in range(len(ranks))]
+    factors[1] = 0.0          # an adapter switched off by its factor
+    factors[-1] = -1.5        # and one with its delta reversed
+    wl = workloads.make_custom(M, K, N, ranks, seed=M + K, id_mode="uniform", p_base=0.15, scale=1.25,
+                               adapter_scale=factors)
+    wl.ids[0] = len(ranks) + 3    # an invalid id: base only, flagged, its factor never read
+    dev = to_dev(wl)
+    ref = oracle.lora_linear(wl)
+    for path in paths:
+        y, ws, status = run_linear(wl, dev, path)
+        assert status == L.LORA_DEV_BAD_ID
+        assert_close(y, ref, what=f"factors M{M} path={path}")
+
+
+def test_linear_adapter_factors_prebuilt_segments_and_decode_config():
+    """The decode-sized configuration with random factors, segments built
+    first, then two back-to-back calls on one workspace."""
+    base = workloads.make_config("decode")
+    wl = workloads.make_custom(base.M, base.K, base.N, base.ranks, seed=77, ids=base.ids.clone(),
+                               adapter_scale="random")
+    dev = to_dev(wl)
+    ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
+    rows = sample_rows(wl.M)
+    ref = oracle.lora_linear(wl, rows=rows)
+    segs = L.lora_build_segments(dev["ids"], dev["pool"], ws)
+    for call in range(2):
+        y = torch.full((wl.M, wl.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        L.lora_linear(dev["x"], dev["W"], dev["bias"], dev["ids"], dev["pool"], wl.scale, ws, y=y,
+                      segs=segs if call == 0 else None)
+        assert L.lora_get_status(ws) == 0
+        assert_close(y[rows], ref, what=f"decode factors call {call}")
+
+
+def test_expand_adapter_factors():
+    wl = workloads.make_custom(300, 64, 264, [16, 48, 64, 32], seed=5, id_mode="runs", p_base=0.2,
+                               adapter_scale=[2.0, 0.5, -0.75, 1.5])
+    dev = to_dev(wl)
+    ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
+    S = workloads.random_fp32((wl.M, 64), seed=13)
+    y0 = workloads.random_fp32((wl.M, wl.N), seed=14).to(torch.bfloat16)
+    y = y0.to("cuda")
+    L.lora_expand(S.to("cuda"), dev["ids"], dev["pool"], 1.25, y, ws)
+    assert_close(y, oracle.expand(wl, S, y0, scale=1.25), what="expand factors")
+
+
+def test_shrink_ignores_adapter_factors():
+    """S leaves the first product unscaled, factors or not."""
+    wl = workloads.make_custom(200, 256, 64, [16, 32, 64], seed=8, id_mode="uniform", adapter_scale=[3.0, 0.5, 2.0])
+    dev = to_dev(wl)
+    ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
+    S = torch.full((wl.M, 64), float("nan"), dtype=torch.float32, device="cuda")
+    L.lora_shrink(dev["x"], dev["ids"], dev["pool"], ws, S=S, s_cols=64)
+    assert_close(S, oracle.shrink(wl, 64), tol=1e-3, what="shrink with factors")
