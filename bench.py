@@ -266,34 +266,49 @@ def time_steps(fn, steps, warmup, stream, chunk=None, sampler=None, dist_barrier
     return e0.elapsed_time(e1)
 
 
-def run_config(name, L, device, steps, warmup, stream, sampler=None, dist_barrier=None, e2e=True):
+def run_config(name, L, device, steps, warmup, stream, sampler=None, dist_barrier=None, e2e=True,
+               static_weights=True, compare_plain=False):
+    """Time one configuration.  static_weights: the weights are loaded once
+    and never written by a kernel during the steps, so each call may start
+    streaming them before the previous call has finished
+    (LORA_FLAG_STATIC_WEIGHTS).  compare_plain: also time both legs without
+    the flag."""
     wl = workloads.make_config(name)
     nbytes, flops, n_present = algorithmic_work(wl)
     sets = build_sets(wl, L, device)
     ns = len(sets)
+    sw = static_weights
 
     def full_step(i):
         s = sets[i % ns]
-        L.lora_linear(s.x, s.W, s.bias, s.ids, s.pool, wl.scale, s.ws, y=s.y)
+        L.lora_linear(s.x, s.W, s.bias, s.ids, s.pool, wl.scale, s.ws, y=s.y, static_weights=sw)
 
     for s in sets:                          # prebuilt tables for the kernel-only timing
         s.segs = L.lora_build_segments(s.ids, s.pool, s.ws)
 
     def kernel_step(i):
         s = sets[i % ns]
-        L.lora_linear(s.x, s.W, s.bias, s.ids, s.pool, wl.scale, s.ws, y=s.y, segs=s.segs)
+        L.lora_linear(s.x, s.W, s.bias, s.ids, s.pool, wl.scale, s.ws, y=s.y, segs=s.segs, static_weights=sw)
 
     # the fused kernel alone (segment tables prebuilt): dominant-kernel duration
     kern_ms = time_steps(kernel_step, steps, warmup, stream) / steps
+    plain = None
+    if compare_plain:
+        sw = False
+        plain = {"kernel_us": round(time_steps(kernel_step, steps, warmup, stream) / steps * 1e3, 3)}
+    for s in sets:                          # the timed step also rebuilds its table
+        s.segs = None
+    if compare_plain:
+        plain["ms_per_step"] = round(time_steps(full_step, steps, warmup, stream) / steps, 6)
+        sw = static_weights
     if sampler:
         sampler.start()
     total_ms = time_steps(full_step, steps, warmup, stream, sampler=sampler, dist_barrier=dist_barrier)
     clocks = sampler.stop() if sampler else None
-    for s in sets:                          # the timed step also rebuilds its table
-        s.segs = None
     status = L.lora_get_status(sets[0].ws)
     res = dict(name=name, wl=wl, ms_per_step=total_ms / steps, kernel_ms=kern_ms, bytes=nbytes, flops=flops,
-               n_present=n_present, n_sets=ns, set_bytes=sets[0].nbytes(), status=status, clocks=clocks)
+               n_present=n_present, n_sets=ns, set_bytes=sets[0].nbytes(), status=status, clocks=clocks,
+               plain=plain)
     if e2e:
         res["e2e"] = run_e2e(wl, sets[0], L, device, min(steps, 5000), max(3, min(warmup, 50)), stream)
     return res
@@ -310,7 +325,7 @@ def run_e2e(wl, s, L, device, steps, warmup, stream):
     def step():
         dx.copy_(hx, non_blocking=True)
         dids.copy_(hids, non_blocking=True)
-        L.lora_linear(dx, s.W, s.bias, dids, s.pool, wl.scale, s.ws, y=s.y)
+        L.lora_linear(dx, s.W, s.bias, dids, s.pool, wl.scale, s.ws, y=s.y, static_weights=True)
         hy.copy_(s.y, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -375,7 +390,7 @@ def ours(args):
 
     sampler = ClockSampler(local)
     r = run_config(args.config, L, device, args.steps, args.warmup, stream, sampler=sampler,
-                   dist_barrier=barrier)
+                   dist_barrier=barrier, compare_plain=True)
     wl = r["wl"]
     def all_reduce_max(v):
         if not dist:
@@ -415,13 +430,16 @@ def ours(args):
                    "l2": f"rotating {r['n_sets']} input sets of {r['set_bytes'] / 1e6:.1f} MB "
                          f"({r['n_sets'] * r['set_bytes'] / 1e6:.0f} MB > L2)" if r["n_sets"] > 1 else
                          f"inputs {r['set_bytes'] / 1e6:.0f} MB > 4x L2",
-                   "timing": "CUDA graphs of whole steps (segment build + fused layer), CUDA events"},
+                   "timing": "CUDA graphs of whole steps (segment build + fused layer), CUDA events",
+                   "static_weights": "weights loaded once; each call may stream them before the previous "
+                                     "call ends (LORA_FLAG_STATIC_WEIGHTS)"},
         "roofline": roof,
         "tflops": round(r["flops"] / (ms * 1e-3) / 1e12, 2),
         "e2e": {k: r["e2e"][k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
         "gpu_launches": 2 * args.steps,
         "clocks": r["clocks"],
         "device_status": r["status"],
+        "without_static_weights": r["plain"],
     }
     if world == 1 and rank == 0 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(args.config)

@@ -221,7 +221,23 @@ enum {
     LORA_PATH_STREAM = 3        /* weight-streaming cluster schedule, M <= 64, K % 64 == 0 */
 };
 
-/* lora_linear with an explicit schedule (for tests and tuning). */
+/*
+ * Flags OR-ed into lora_linear_ex's `path` argument.
+ *
+ * LORA_FLAG_STATIC_WEIGHTS: W, bias and the adapter pool (A, B, offsets,
+ * ranks, factors) are not written by any kernel that can still be running
+ * when the call starts, i.e. by no kernel enqueued on `stream` since its last
+ * operation that is not a kernel launch (a copy, a memset, an event wait).
+ * Weights loaded once by copies and left alone during the steps qualify.
+ * The call may then start streaming weights before the kernel ahead of it on
+ * the stream has finished (a programmatic dependent launch); x, the ids, the
+ * workspace and y are still touched only after that kernel completes.  Today
+ * the decode-sized schedule (M <= 64) uses it; the others ignore it.
+ */
+#define LORA_FLAG_STATIC_WEIGHTS 0x100
+
+/* lora_linear with an explicit schedule (for tests and tuning); `path` is a
+ * LORA_PATH_* value, optionally OR-ed with LORA_FLAG_* bits. */
 int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
                    const int32_t *lora_id_map, const lora_pool_t *pool, float scale,
                    const lora_segments_t *segs, lora_bf16_t *y, void *ws, size_t ws_bytes,

@@ -238,8 +238,12 @@ __global__ void __launch_bounds__(kClThreads, 1)
     int32_t *ccnt = p.wcnt + kCntStride / 2;
 
     // ---- prologue: nothing in this kernel depends on the segment builder ------
+    // Launched as a programmatic dependent (early_weights), the kernel may
+    // start while the kernels ahead of it still run: until griddepcontrol.wait
+    // it touches only the weights (W, the A pool) and its own shared memory
+    // and TMEM; x, the ids, the workspace and y come after the wait.
     int id0 = -1, id1 = -1;   // warp 2: the ids of tokens lane, lane + 32 (inputs; loaded first)
-    if (warp == 2) {
+    if (warp == 2 && !p.early_weights) {
         id0 = lane < p.M ? p.ids[lane] : -2;
         id1 = lane + 32 < p.M ? p.ids[lane + 32] : -2;
     }
@@ -264,29 +268,33 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 const int U = p.windows_all * KU2;
                 const int u0 = (U * cta) / G, u1 = (U * (cta + 1)) / G;
                 int wi = u0 / KU2, ku = u0 - wi * KU2;
+                int kbs[kClMaxStages];
                 for (int i = 0; i < nfirst; ++i) {
                     uint8_t *wa = smem + i * slot_bytes;
                     mbar_expect_tx(&full[i], unit_tx);
-                    int kb;
                     if (u0 + i < u1) {
-                        kb = 2 * ku;
-                        tma_load_3d_st(wa, &tm_a3, &full[i], 0, kChunk * kStWin * wi, kb);
+                        kbs[i] = 2 * ku;
+                        tma_load_3d_st(wa, &tm_a3, &full[i], 0, kChunk * kStWin * wi, kbs[i]);
                         if (++ku == KU2) {
                             ku = 0;
                             ++wi;
                         }
                     } else {
-                        kb = 2 * (b0 + (u0 + i - u1));
-                        tma_load_3d_st(wa, &tm_w3, &full[i], 0, n0, kb);
+                        kbs[i] = 2 * (b0 + (u0 + i - u1));
+                        tma_load_3d_st(wa, &tm_w3, &full[i], 0, n0, kbs[i]);
                     }
-                    tma_load_3d_st(wa + kClWArea, &tm_x3, &full[i], 0, 0, kb);
                 }
+                pdl_wait();   // x may be written by the kernel ahead of this one
+                for (int i = 0; i < nfirst; ++i)
+                    tma_load_3d_st(smem + i * slot_bytes + kClWArea, &tm_x3, &full[i], 0, 0, kbs[i]);
             } else {
                 for (int i = 0; i < nfirst; ++i) {
                     mbar_expect_tx(&full[i], unit_tx);
                     tma_load_3d_st(smem + i * slot_bytes, &tm_w3, &full[i], 0, n0, 2 * (b0 + i));
-                    tma_load_3d_st(smem + i * slot_bytes + kClWArea, &tm_x3, &full[i], 0, 0, 2 * (b0 + i));
                 }
+                pdl_wait();
+                for (int i = 0; i < nfirst; ++i)
+                    tma_load_3d_st(smem + i * slot_bytes + kClWArea, &tm_x3, &full[i], 0, 0, 2 * (b0 + i));
             }
             tma_prefetch_map(&tm_a3);
             tma_prefetch_map(&tm_b3);
@@ -308,6 +316,14 @@ __global__ void __launch_bounds__(kClThreads, 1)
     pdl_launch_dependents();   // a dependent launch (the segment builder) may start on an idle SM
     cluster_arrive_relaxed();  // my barriers are initialised; peers wait for this before any st.async
     const uint32_t tmem_base = warp < 6 ? *tmem_slot : 0u;
+    // the kernels ahead of this one are complete and their writes visible
+    // before any thread reads an input other than the weights, touches the
+    // workspace or y, or starts a bounded wait
+    pdl_wait();
+    if (warp == 2 && p.early_weights) {
+        id0 = lane < p.M ? p.ids[lane] : -2;
+        id1 = lane + 32 < p.M ? p.ids[lane + 32] : -2;
+    }
 
     if (warp == 0) {
         // ===================== TMA producer: W, A and B boxes ================
@@ -706,9 +722,6 @@ __global__ void __launch_bounds__(kClThreads, 1)
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, 512);
     cluster_wait();            // no CTA leaves while a peer may still touch its shared memory
-    // when launched right after the segment builder as a programmatic
-    // dependent, finish only after it (stream order for what follows)
-    if (threadIdx.x == 0) pdl_wait();
 }
 
 int cluster_max_regions() { return kStMaxRegions; }

@@ -152,6 +152,7 @@ struct ClusterParams {
     const int32_t *rank;       // padded rank of each adapter
     int32_t A, windows_all;    // adapters; 128-row windows in the pool
     int32_t all_windows;       // process every window (known at launch) instead of the ones the batch touches
+    int32_t early_weights;     // launched as a programmatic dependent: weights are read before griddepcontrol.wait
     float *acc;                // fp32 [windows][T_pad][128]: per-window sums of S (zero at rest)
     int32_t *wcnt;             // [windows][kWinCntStride]: shrink arrivals at 0, consumer CTAs at 16 (zero at rest)
     int32_t *counters;

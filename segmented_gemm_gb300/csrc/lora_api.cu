@@ -439,8 +439,9 @@ static int run_splitk(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, con
 // Weight-streaming schedule (M <= 64, K a multiple of 64): one cluster of C
 // CTAs per 128-feature output tile.  Returns -1 when this device / shape
 // cannot host it, so the caller falls back to split-K.  pdl: launch it as a
-// programmatic dependent of a segment builder enqueued right before it
-// (lora_linear enqueues the builder after it instead).
+// programmatic dependent of whatever kernel precedes it on the stream; it
+// then streams its first weight boxes before that kernel has finished
+// (LORA_FLAG_STATIC_WEIGHTS).
 static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
                        const int32_t *ids, const lora_pool_t *pool, float scale, lora_bf16_t *y, void *ws,
                        const WsLayout &L, bool pdl, cudaStream_t stream)
@@ -502,6 +503,7 @@ static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, co
     // a pool no larger than what one batch could touch is processed whole:
     // the unit list is then known at launch and the shrink can go first
     p.all_windows = p.windows_all <= L.max_win_str ? 1 : 0;
+    p.early_weights = pdl ? 1 : 0;
     p.scale = scale;
     p.adapter_scale = pool->num_adapters ? pool->adapter_scale : nullptr;
     p.bias = bias;
@@ -600,6 +602,10 @@ int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const 
     if (M == 0) return check_pool(pool);
     if (!x || !W || !y) return LORA_ERR_NULL;
     if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (bias && !aligned16(bias))) return LORA_ERR_ALIGN;
+    const int32_t flags = path & ~0xFF;
+    path &= 0xFF;
+    if (flags & ~LORA_FLAG_STATIC_WEIGHTS) return LORA_ERR_SHAPE;
+    const bool static_weights = (flags & LORA_FLAG_STATIC_WEIGHTS) != 0;
     if (path < LORA_PATH_AUTO || path > LORA_PATH_STREAM) return LORA_ERR_SHAPE;
     if (path == LORA_PATH_SPLITK && M > kSplitMaxTokens) return LORA_ERR_SHAPE;
     if (path == LORA_PATH_STREAM && (M > kStreamMaxTokens || (pool && (pool->K % kBK)))) return LORA_ERR_SHAPE;
@@ -614,7 +620,7 @@ int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const 
     int rc = prepare(lora_id_map, M, pool, segs, ws, ws_bytes, s, &L, !stream_path);
     if (rc) return rc;
     if (stream_path) {
-        const int rc2 = run_cluster(x, M, W, bias, lora_id_map, pool, scale, y, ws, L, false, s);
+        const int rc2 = run_cluster(x, M, W, bias, lora_id_map, pool, scale, y, ws, L, static_weights, s);
         if (rc2 == LORA_OK && !segs) return enqueue_segments(lora_id_map, M, pool, L, ws, s, true);
         if (rc2 >= 0) return rc2;
         if (path == LORA_PATH_STREAM) return LORA_ERR_UNSUPPORTED;

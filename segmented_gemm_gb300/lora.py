@@ -24,6 +24,7 @@ LORA_ERR_CAPACITY = 9
 LORA_NOALLOC_SCRATCH_BYTES = 8 << 20
 LORA_DEV_BAD_ID, LORA_DEV_TIMEOUT = 1, 2
 LORA_PATH_AUTO, LORA_PATH_TILED, LORA_PATH_SPLITK, LORA_PATH_STREAM = 0, 1, 2, 3
+LORA_FLAG_STATIC_WEIGHTS = 0x100
 LORA_MAX_RANK, LORA_RANK_ALIGN, LORA_MAX_ADAPTERS = 64, 16, 1024
 
 EXPORTS = ("lora_pool_layout", "lora_workspace_size", "lora_workspace_init", "lora_build_segments",
@@ -229,15 +230,19 @@ def segments_to_host(segs: lora_segments_t, ws: Workspace, M: int, num_adapters:
 def lora_linear(x: torch.Tensor, W: torch.Tensor, bias: Optional[torch.Tensor], ids: torch.Tensor,
                 pool: LoraPool, scale: float, ws: Workspace, y: Optional[torch.Tensor] = None,
                 segs: Optional[lora_segments_t] = None, path: int = LORA_PATH_AUTO,
-                stream=None) -> torch.Tensor:
-    """y = x W^T + bias + scale * (x A_id^T) B_id^T per token (id -1: base only)."""
+                stream=None, static_weights: bool = False) -> torch.Tensor:
+    """y = x W^T + bias + scale * (x A_id^T) B_id^T per token (id -1: base only).
+
+    ``static_weights``: W, bias and the pool are written by no kernel that
+    can still run when the call starts (LORA_FLAG_STATIC_WEIGHTS), so the call
+    may start streaming them before the kernel ahead of it has finished."""
     M = x.shape[0]
     if y is None:
         y = torch.empty(M, W.shape[0], dtype=torch.bfloat16, device=x.device)
     _check(load_library().lora_linear_ex(
         _ptr(x), M, _ptr(W), _ptr(bias), _ptr(ids), ctypes.byref(pool.desc), float(scale),
         ctypes.byref(segs) if segs is not None else None, _ptr(y), ws.ptr, ws.nbytes,
-        _stream(stream), int(path)), "lora_linear")
+        _stream(stream), int(path) | (LORA_FLAG_STATIC_WEIGHTS if static_weights else 0)), "lora_linear")
     return y
 
 

@@ -6,6 +6,8 @@ accumulation, S rounded once to bf16 before the second product).
 Every output buffer is pre-filled with NaN so an element the kernels never
 write fails the comparison.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -414,3 +416,59 @@ def test_shrink_ignores_adapter_factors():
     S = torch.full((wl.M, 64), float("nan"), dtype=torch.float32, device="cuda")
     L.lora_shrink(dev["x"], dev["ids"], dev["pool"], ws, S=S, s_cols=64)
     assert_close(S, oracle.shrink(wl, 64), tol=1e-3, what="shrink with factors")
+
+
+# ---------------------------------------------------------------------------
+# LORA_FLAG_STATIC_WEIGHTS: weights streamed before the previous kernel ends
+# ---------------------------------------------------------------------------
+
+def test_static_weights_after_kernels_that_write_the_inputs():
+    """With the flag, the decode schedule may start streaming W and the pool
+    while the kernel ahead of it still runs; x and the ids must still be read
+    only after that kernel.  Every call here directly follows torch kernels
+    that write its x and ids (three input sets, six calls, one workspace),
+    run eagerly and then replayed from a CUDA graph."""
+    base = workloads.make_config("decode")
+    variants = [base]
+    for k in range(2):
+        g = torch.Generator().manual_seed(900 + k)
+        ids = torch.randint(-1, base.num_adapters, (base.M,), generator=g).to(torch.int32)
+        x = workloads.random_fp32((base.M, base.K), seed=910 + k).to(torch.bfloat16)
+        variants.append(dataclasses.replace(base, x=x, ids=ids))
+    refs = [oracle.lora_linear(v) for v in variants]
+    dev = to_dev(base)
+    src_x = [v.x.to("cuda") for v in variants]
+    src_ids = [v.ids.to("cuda") for v in variants]
+    xd, idd = torch.empty_like(src_x[0]), torch.empty_like(src_ids[0])
+    ws = L.Workspace(base.M, base.N, base.num_adapters)
+    ys = [torch.empty(base.M, base.N, dtype=torch.bfloat16, device="cuda") for _ in range(6)]
+
+    def calls():
+        for c in range(6):
+            v = c % 3
+            torch.mul(src_x[v], 1, out=xd)        # kernels that write this call's inputs
+            torch.add(src_ids[v], 0, out=idd)
+            L.lora_linear(xd, dev["W"], dev["bias"], idd, dev["pool"], base.scale, ws, y=ys[c],
+                          static_weights=True)
+
+    def check(what):
+        torch.cuda.synchronize()
+        assert L.lora_get_status(ws) == 0
+        for c in range(6):
+            assert_close(ys[c], refs[c % 3], what=f"{what} call {c}")
+            ys[c].fill_(float("nan"))
+
+    for y in ys:
+        y.fill_(float("nan"))
+    calls()
+    check("eager")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            calls()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        graph.replay()
+        check("graph")
