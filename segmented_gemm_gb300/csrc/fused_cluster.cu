@@ -40,6 +40,7 @@
 #include "internal.h"
 #include "lora.h"
 #include "ptx.cuh"
+#include "seg_build_body.cuh"
 
 namespace lora {
 
@@ -183,6 +184,17 @@ __global__ void __launch_bounds__(kClThreads, 1)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    if (blockIdx.x >= p.C * p.NT) {
+        // the extra cluster (p.build): its first CTA builds this call's
+        // segment table beside the weight stream, once the kernel ahead has
+        // finished with the workspace; the others have nothing to do
+        pdl_launch_dependents();
+        if (blockIdx.x == p.C * p.NT) {
+            pdl_wait();
+            SegBuild<kClThreads / 32>::run(p.seg, reinterpret_cast<int *>(smem));
+        }
+        return;
+    }
     const int T = p.T_pad;
     const int slot_bytes = kClWArea + T * 256;    // [W / A / B box | token operand]
     const uint32_t unit_tx = kClWArea + T * 256;   // a base / shrink unit: weight box + x box
@@ -211,7 +223,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     int *s_wlist = s_wpre + kStMaxWinAll / 32;         // [kStMaxWinList] windows touched, ascending
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int G = gridDim.x, cta = blockIdx.x;
+    const int G = p.C * p.NT, cta = blockIdx.x;   // the compute CTAs
     const int C = p.C;
     const int q = static_cast<int>(cluster_ctarank());
     const int n0 = (cta / C) * kSplitBN;
@@ -728,6 +740,7 @@ int cluster_max_regions() { return kStMaxRegions; }
 int cluster_max_runs() { return kStMaxRuns; }
 int cluster_max_win_cta() { return kStMaxWinCta; }
 int cluster_win() { return kStWin; }
+size_t cluster_build_smem_bytes(int32_t A) { return SegBuild<kClThreads / 32>::smem_bytes(A); }
 
 size_t cluster_smem_bytes(int T_pad, int stages)
 {
@@ -742,8 +755,8 @@ int cluster_stages(int T_pad)
     return s > 6 ? 6 : s;
 }
 
-// Largest cluster size in {8, 4, 2, 1} whose grid (C x NT CTAs, one per SM)
-// can be resident all at once; 0 when none can.
+// Largest cluster size in {8, 4, 2, 1} whose grid (C x (NT + 1) CTAs, one
+// per SM) can be resident all at once; 0 when none can.
 int cluster_pick_size(int NT, int T_pad, int sms)
 {
     const int stages = cluster_stages(T_pad);
@@ -758,10 +771,11 @@ int cluster_pick_size(int NT, int T_pad, int sms)
             return 0;
         if (dev < 64) configured[dev] = 1;
     }
+    // one cluster more than the output tiles: the segment builder's
     for (int C = 8; C >= 1; C >>= 1) {
-        if (C * NT > sms) continue;
+        if (C * (NT + 1) > sms) continue;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(C * NT);
+        cfg.gridDim = dim3(C * (NT + 1));
         cfg.blockDim = dim3(kClThreads);
         cfg.dynamicSmemBytes = smem;
         cudaLaunchAttribute attr[1];
@@ -776,18 +790,18 @@ int cluster_pick_size(int NT, int T_pad, int sms)
             cudaGetLastError();
             continue;
         }
-        if (nclusters >= NT) return C;
+        if (nclusters >= NT + 1) return C;
     }
     return 0;
 }
 
-// pdl: the launch directly follows this library's segment builder on the
-// same stream; the kernel's prologue (barriers, TMEM, the first weight
-// boxes, x, ids, bias) may then overlap the builder.
+// pdl: a programmatic dependent launch; the prologue (barriers, TMEM, the
+// first weight boxes) may then overlap the kernel ahead on the stream, and
+// everything else waits for it (griddepcontrol.wait).
 cudaError_t launch_cluster(const ClusterMaps &m, const ClusterParams &p, bool pdl, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.C * p.NT);
+    cfg.gridDim = dim3(p.C * (p.NT + (p.build ? 1 : 0)));
     cfg.blockDim = dim3(kClThreads);
     cfg.dynamicSmemBytes = cluster_smem_bytes(p.T_pad, p.stages);
     cfg.stream = stream;

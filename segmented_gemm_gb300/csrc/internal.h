@@ -134,6 +134,21 @@ struct SplitParams {
     int32_t *counters;
 };
 
+struct SegParams {
+    const int32_t *ids;
+    int64_t M;
+    int32_t A, K, N, num_mtiles;
+    const int32_t *rank;
+    const int64_t *a_offset;
+    const int64_t *b_offset;
+    int32_t *perm, *offsets, *seg_id, *seg_start, *seg_len, *seg_rank, *num_segments;
+    int32_t *hdr, *tile_chunk_off, *chunk_arow, *chunk_brow, *chunk_rng;
+    int32_t *sjob_tile, *sjob_c0, *sjob_c1, *tile_njobs;
+    int32_t *dchunk_arow, *dchunk_brow, *dchunk_adapter;
+    int32_t *counters;
+    int32_t n_counters;
+};
+
 struct ClusterMaps {
     CUtensorMap w3, a3, b3;    // W, A pool: {64, 128 rows, 2 K blocks}; B pool: {16, 128 rows, 8 panels}
     CUtensorMap x3;            // x: {64, T rows, 2 K blocks} (rows past M read as zeros)
@@ -153,25 +168,13 @@ struct ClusterParams {
     int32_t A, windows_all;    // adapters; 128-row windows in the pool
     int32_t all_windows;       // process every window (known at launch) instead of the ones the batch touches
     int32_t early_weights;     // launched as a programmatic dependent: weights are read before griddepcontrol.wait
+    int32_t build;             // one extra cluster, whose first CTA builds the segment table (seg)
+    SegParams seg;
     float *acc;                // fp32 [windows][T_pad][128]: per-window sums of S (zero at rest)
     int32_t *wcnt;             // [windows][kWinCntStride]: shrink arrivals at 0, consumer CTAs at 16 (zero at rest)
     int32_t *counters;
 };
 
-struct SegParams {
-    const int32_t *ids;
-    int64_t M;
-    int32_t A, K, N, num_mtiles;
-    const int32_t *rank;
-    const int64_t *a_offset;
-    const int64_t *b_offset;
-    int32_t *perm, *offsets, *seg_id, *seg_start, *seg_len, *seg_rank, *num_segments;
-    int32_t *hdr, *tile_chunk_off, *chunk_arow, *chunk_brow, *chunk_rng;
-    int32_t *sjob_tile, *sjob_c0, *sjob_c1, *tile_njobs;
-    int32_t *dchunk_arow, *dchunk_brow, *dchunk_adapter;
-    int32_t *counters;
-    int32_t n_counters;
-};
 
 // ---- launchers (enqueue only; return the launch status) --------------------
 cudaError_t launch_seg_build(const SegParams &p, bool pdl, cudaStream_t stream);
@@ -182,6 +185,8 @@ int splitk_stages(int T_pad);
 cudaError_t launch_cluster(const ClusterMaps &m, const ClusterParams &p, bool pdl, cudaStream_t stream);
 int cluster_pick_size(int NT, int T_pad, int sms);
 int cluster_stages(int T_pad);
+size_t cluster_smem_bytes(int T_pad, int stages);
+size_t cluster_build_smem_bytes(int32_t A);   // the segment build inside the decode kernel
 int cluster_max_regions();
 int cluster_max_runs();
 int cluster_max_win_cta();

@@ -223,10 +223,9 @@ static void fill_segments(void *ws, const WsLayout &L, int64_t M, int32_t A, lor
     out->reserved = 0;
 }
 
-static int enqueue_segments(const int32_t *ids, int64_t M, const lora_pool_t *pool, const WsLayout &L, void *ws,
-                            cudaStream_t stream, bool pdl = false)
+static void fill_seg_params(SegParams &p, const int32_t *ids, int64_t M, const lora_pool_t *pool, const WsLayout &L,
+                            void *ws)
 {
-    SegParams p;
     p.ids = ids;
     p.M = M;
     p.A = pool->num_adapters;
@@ -257,6 +256,13 @@ static int enqueue_segments(const int32_t *ids, int64_t M, const lora_pool_t *po
     p.dchunk_adapter = at<int32_t>(ws, L.dchunk_adapter);
     p.counters = at<int32_t>(ws, L.counters);
     p.n_counters = static_cast<int32_t>(L.n_counters);
+}
+
+static int enqueue_segments(const int32_t *ids, int64_t M, const lora_pool_t *pool, const WsLayout &L, void *ws,
+                            cudaStream_t stream, bool pdl = false)
+{
+    SegParams p;
+    fill_seg_params(p, ids, M, pool, L, ws);
     return launch_seg_build(p, pdl, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
@@ -441,10 +447,12 @@ static int run_splitk(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, con
 // cannot host it, so the caller falls back to split-K.  pdl: launch it as a
 // programmatic dependent of whatever kernel precedes it on the stream; it
 // then streams its first weight boxes before that kernel has finished
-// (LORA_FLAG_STATIC_WEIGHTS).
+// (LORA_FLAG_STATIC_WEIGHTS).  build: one more cluster, whose first CTA
+// builds the call's segment table in ws beside the weight stream (the
+// kernel itself reads no table).
 static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
                        const int32_t *ids, const lora_pool_t *pool, float scale, lora_bf16_t *y, void *ws,
-                       const WsLayout &L, bool pdl, cudaStream_t stream)
+                       const WsLayout &L, bool pdl, bool build, cudaStream_t stream)
 {
     if (M > kStreamMaxTokens || (pool->K % kBK) != 0) return -1;
     const int T = split_tpad(M);
@@ -504,6 +512,11 @@ static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, co
     // the unit list is then known at launch and the shrink can go first
     p.all_windows = p.windows_all <= L.max_win_str ? 1 : 0;
     p.early_weights = pdl ? 1 : 0;
+    if (build) {
+        if (cluster_build_smem_bytes(pool->num_adapters) + 1024 > cluster_smem_bytes(T, p.stages)) return -1;
+        p.build = 1;
+        fill_seg_params(p.seg, ids, M, pool, L, ws);
+    }
     p.scale = scale;
     p.adapter_scale = pool->num_adapters ? pool->adapter_scale : nullptr;
     p.bias = bias;
@@ -620,8 +633,7 @@ int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const 
     int rc = prepare(lora_id_map, M, pool, segs, ws, ws_bytes, s, &L, !stream_path);
     if (rc) return rc;
     if (stream_path) {
-        const int rc2 = run_cluster(x, M, W, bias, lora_id_map, pool, scale, y, ws, L, static_weights, s);
-        if (rc2 == LORA_OK && !segs) return enqueue_segments(lora_id_map, M, pool, L, ws, s, true);
+        const int rc2 = run_cluster(x, M, W, bias, lora_id_map, pool, scale, y, ws, L, static_weights, !segs, s);
         if (rc2 >= 0) return rc2;
         if (path == LORA_PATH_STREAM) return LORA_ERR_UNSUPPORTED;
         if (!segs && (rc = enqueue_segments(lora_id_map, M, pool, L, ws, s))) return rc;

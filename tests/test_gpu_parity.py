@@ -472,3 +472,45 @@ def test_static_weights_after_kernels_that_write_the_inputs():
     for _ in range(3):
         graph.replay()
         check("graph")
+
+
+# ---------------------------------------------------------------------------
+# the segment table a decode-sized call builds inside its own kernel
+# ---------------------------------------------------------------------------
+
+def _rebase(segs, ws_from, ws_to):
+    """The same table layout, pointing into another workspace of equal size."""
+    out = L.lora_segments_t()
+    d = ws_to.buf.data_ptr() - ws_from.buf.data_ptr()
+    for name in ("perm", "bucket_offsets", "seg_id", "seg_start", "seg_len", "seg_rank", "num_segments"):
+        setattr(out, name, getattr(segs, name) + d)
+    out.plan = ws_to.buf.data_ptr()
+    out.M, out.num_adapters = segs.M, segs.num_adapters
+    return out
+
+
+@pytest.mark.parametrize("static_weights", [False, True])
+def test_decode_call_builds_the_segment_table(static_weights):
+    """A decode-sized call given no table builds one in an extra CTA of its
+    own kernel, beside the weight stream.  The table it leaves in the
+    workspace equals the oracle's bit for bit, and the tiled schedule then
+    runs from it (its work lists included) to the oracle's output."""
+    wl = workloads.make_config("decode")
+    wl.ids[5] = wl.num_adapters + 2                  # flagged, bucketed as -1
+    dev = to_dev(wl)
+    ref = oracle.lora_linear(wl)
+    ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
+    y = torch.full((wl.M, wl.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    L.lora_linear(dev["x"], dev["W"], dev["bias"], dev["ids"], dev["pool"], wl.scale, ws, y=y,
+                  path=L.LORA_PATH_STREAM, static_weights=static_weights)
+    assert L.lora_get_status(ws) == L.LORA_DEV_BAD_ID
+    assert_close(y, ref, what="decode with in-kernel build")
+    ws2 = L.Workspace(wl.M, wl.N, wl.num_adapters)   # only for the table's addresses
+    segs = _rebase(L.lora_build_segments(dev["ids"], dev["pool"], ws2), ws2, ws)
+    del ws2
+    check_segments(wl, dev, ws, segs)
+    y2 = torch.full((wl.M, wl.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    L.lora_linear(dev["x"], dev["W"], dev["bias"], dev["ids"], dev["pool"], wl.scale, ws, y=y2, segs=segs,
+                  path=L.LORA_PATH_TILED)
+    assert L.lora_get_status(ws) == 0
+    assert_close(y2, ref, what="tiled from the in-kernel table")
