@@ -748,11 +748,14 @@ size_t cluster_smem_bytes(int T_pad, int stages)
            1024 + kClMisc;
 }
 
+// Ring depth: what fits, at most 3.  Deeper rings measured no faster: with
+// every CTA's boxes in flight the memory queues only grow, and each round
+// trip of the shrink-to-expand chain waits in them.
 int cluster_stages(int T_pad)
 {
     const size_t budget = 227 * 1024 - static_cast<size_t>(kSplitBN) * T_pad * 4 - 1024 - kClMisc;
     int s = static_cast<int>(budget / (kClWArea + T_pad * 256));
-    return s > 6 ? 6 : s;
+    return s > 3 ? 3 : s;
 }
 
 // Largest cluster size in {8, 4, 2, 1} whose grid (C x (NT + 1) CTAs, one
