@@ -106,10 +106,14 @@ __device__ __forceinline__ Job decode_job(int j, int n_sjobs, const TcParams &p)
 // CTAs take jobs b, b + G, ...  With stream-K the whole waves are taken that
 // way, and the jobs of the last partial wave are shared out: its shrink jobs
 // whole (one per CTA, first CTAs), its output tiles as equal runs of K blocks
-// over the other CTAs.  A tile cut between CTAs has one head piece (K block
-// 0, last item of its CTA) and tail pieces (first items of the next CTAs):
-// tails add their partial sums to the tile's scratch and count themselves,
-// the head waits for them, applies the expand steps and writes y.
+// over at most kSkPieces CTAs per tile.  A tile cut between CTAs has one head
+// piece (K block 0, last item of its CTA) and tail pieces (first items of the
+// next CTAs).  A CTA holds at most one tail piece: each tail stores its
+// partial sums in its CTA's own scratch slot and counts itself on the tile's
+// counter; the head waits for them, adds them, applies the expand steps and
+// writes y.  Nothing is added atomically, so the scratch needs no clearing.
+constexpr int kSkPieces = 4;   // CTAs per split tile, on average, at most
+
 struct SkPlan {
     int waves, rs, t0, ro, gp;   // whole waves; tail shrink jobs; first tail tile; tail tiles; CTAs sharing them
     int64_t wt;                  // K blocks of the tail tiles
@@ -139,7 +143,7 @@ __device__ __forceinline__ SkPlan sk_plan(int n_sjobs, int n_out, int G, int KB,
     s.rs = streamk ? max(0, n_sjobs - jf) : 0;
     s.t0 = streamk ? max(0, jf - n_sjobs) : n_out;
     s.ro = streamk ? n_out - s.t0 : 0;
-    s.gp = G - s.rs;
+    s.gp = min(G - s.rs, max(1, s.ro) * kSkPieces);
     s.wt = static_cast<int64_t>(s.ro) * KB;
     // the shrink items (K pieces of 1 / split) are the first wave's first
     // items: those CTAs take the missing K blocks in the last wave
@@ -171,7 +175,7 @@ __device__ __forceinline__ bool get_item(int q, int b, int G, int n_sjobs, int n
         jb = decode_job(s.waves * G + b, n_sjobs, p);
         return true;
     }
-    if (s.ro <= 0) return false;
+    if (s.ro <= 0 || b - s.rs >= s.gp) return false;
     const int KB = p.kblocks, bb = b - s.rs;
     const int64_t r0 = sk_start(s, bb), r1 = sk_start(s, bb + 1);
     int64_t f = r0;
@@ -189,29 +193,19 @@ __device__ __forceinline__ bool get_item(int q, int b, int G, int n_sjobs, int n
     return true;
 }
 
-// Whether split tile t (one of CTA b's tail pieces) has a single tail piece:
-// the CTA before b holds its head, and no later CTA starts inside it.
-__device__ __forceinline__ bool sk_single_tail(int b, int t, const SkPlan &s, int KB)
+// The tail pieces of split tile t whose head piece is CTA b are the next
+// non-empty tail-sharing CTAs that start inside the tile; a tail's scratch
+// slot is its tail-sharing CTA index.  sk_tail_count: how many there are.
+// sk_next_tail: the slot of the first tail after slot `after` (the head's
+// own index for the first one).
+__device__ __forceinline__ int sk_next_tail(int after, const SkPlan &s)
 {
-    const int bb = b - s.rs;
-    const int64_t end = static_cast<int64_t>(t + 1) * KB, begin = static_cast<int64_t>(t) * KB;
-    const int64_t my_r0 = sk_start(s, bb);
-    // my piece must start after the tile's first K block (I am a tail) and
-    // the head's CTA must be the previous non-empty one
-    int prev = bb - 1;
-    while (prev >= 0 && sk_start(s, prev) == sk_start(s, prev + 1)) --prev;
-    if (prev < 0 || sk_start(s, prev) > begin || my_r0 <= begin) return false;
-    for (int nb = bb + 1; nb < s.gp; ++nb) {
-        const int64_t r0 = sk_start(s, nb), r1 = sk_start(s, nb + 1);
-        if (r0 >= end) break;
-        if (r1 > r0) return false;   // another tail starts inside the tile
-    }
-    return true;
+    int bb = after + 1;
+    while (bb < s.gp && sk_start(s, bb + 1) == sk_start(s, bb)) ++bb;
+    return bb;
 }
 
-// Tail pieces of split tile t whose head piece is CTA b's (the non-empty
-// ranges of the next CTAs that start inside the tile).
-__device__ __forceinline__ int sk_tails(int b, int t, const SkPlan &s, int KB)
+__device__ __forceinline__ int sk_tail_count(int b, int t, const SkPlan &s, int KB)
 {
     int n = 0;
     const int64_t end = static_cast<int64_t>(t + 1) * KB;
@@ -243,7 +237,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *sk_bar = acc_empty + 2;   // stream-K head: the partial sums have landed in the W ring
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sk_bar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    int *last_flag = const_cast<int *>(abort_flag) + 1;
     // bias of the output tile of each accumulator slot: [2][kBN] bf16 (16-byte aligned)
     uint32_t *s_bias = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(fullx) + 256);
 
@@ -291,6 +284,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0) {
         // ===================== TMA producer: W ring (W, A panels, S / B panels)
         uint32_t iw = 0;
+        // The S-ready counter of token tile m is put back to zero by the last
+        // of its num_ntiles output tiles to pass the wait on it: each adds
+        // itself to a consumer counter right after the wait and reads the
+        // result one item later, so the round trip hides behind the loads.
+        int32_t *cons = p.counters + CNT_FIXED + p.num_mtiles;
+        int rst_m = -1, rst_old = 0;
+        auto settle = [&]() {
+            if (rst_m >= 0 && rst_old == p.num_ntiles - 1) {
+                p.counters[CNT_FIXED + rst_m] = 0;
+                cons[rst_m] = 0;
+            }
+            rst_m = -1;
+        };
         for (int q = 0; get_item(q, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, jb); ++q) {
             // shrink job: consecutive rank panels of one adapter are
             // consecutive pool rows, loaded as one box of 16..64 rows per run.
@@ -358,6 +364,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         wait_flag_geq(p.counters + CNT_FIXED + jb.m, p.tile_njobs[jb.m] * p.s_sets, abort_flag,
                                       status, LORA_DEV_TIMEOUT);
                         fence_proxy_async_global();
+                        settle();
+                        rst_old = atom_acq_rel_gpu_add(cons + jb.m, 1);
+                        rst_m = jb.m;
                     }
                     __syncwarp();
                 }
@@ -384,6 +393,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
         }
+        if (lane == 0) settle();
     } else if (warp >= 6) {
         // ===================== x loaders: permuted-row gather (cp.async) =====
         // Thread lt copies 16-byte chunk (lt % 8) of rows lt/8 + 16q, q < 8,
@@ -558,13 +568,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (et == 0) red_release_gpu_add(p.counters + CNT_FIXED + jb.m, 1);
                 }
             } else if (jb.part == kPartTail) {
-                // ---- tail piece of a split tile: add my partial sums ----------
-                // scratch layout [col / 4][row][4]: a warp's float4 accesses
-                // cover 512 contiguous bytes.  The only tail of a tile stores
-                // its partials; several tails add theirs with atomics.
-                float4 *part = reinterpret_cast<float4 *>(p.sk_part) + static_cast<int64_t>(jb.slot) * (kBN / 4) * kBM;
-                const bool single = sk_single_tail(blockIdx.x, jb.slot, sk, p.kblocks);
-                // four 16-column TMEM loads per wait
+                // ---- tail piece of a split tile: store my partial sums --------
+                // in my CTA's scratch slot, layout [col / 4][row][4]: a warp's
+                // float4 accesses cover 512 contiguous bytes
+                float4 *part = reinterpret_cast<float4 *>(p.sk_part) +
+                               static_cast<int64_t>(blockIdx.x - sk.rs) * (kBN / 4) * kBM;
+                // four 16-column TMEM loads per wait (one group at a time: the
+                // register budget holds no more)
+#pragma unroll 1
                 for (int cc = 0; cc < kBN / 16; cc += 4) {
                     uint32_t r[4][16];
 #pragma unroll
@@ -583,9 +594,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             const float4 f4 =
                                 make_float4(__uint_as_float(r[h][4 * k]), __uint_as_float(r[h][4 * k + 1]),
                                             __uint_as_float(r[h][4 * k + 2]), __uint_as_float(r[h][4 * k + 3]));
-                            float4 *dst = part + ((cc + h) * 4 + k) * kBM + row;
-                            if (single) __stcg(dst, f4);
-                            else atomicAdd(dst, f4);
+                            __stcg(part + ((cc + h) * 4 + k) * kBM + row, f4);
                         }
                 }
                 __threadfence();
@@ -598,22 +607,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int n0 = jb.n * kBN;
                 const bool head = jb.part == kPartHead;
                 uint8_t *srow = xring + row * kStageRow;
-                float4 *part = head ? reinterpret_cast<float4 *>(p.sk_part) + static_cast<int64_t>(jb.slot) * (kBN / 4) * kBM
-                                    : nullptr;
                 // the head is its CTA's last item: the W ring is idle now, and
-                // the summed partials (128 KB) come in by four bulk copies
+                // the first tail's partials (128 KB) come in by four bulk
+                // copies; further tails' are added from L2
                 const float4 *spart = reinterpret_cast<const float4 *>(wring);
+                int ntail = 0, tail0 = 0;
                 if (head) {
-                    if (et == 0) {   // every tail piece has added its partial sums
-                        wait_flag_geq(p.sk_cnt + jb.slot * kWinCntStride, sk_tails(blockIdx.x, jb.slot, sk, p.kblocks),
-                                      abort_flag, status, LORA_DEV_TIMEOUT);
-                        fence_proxy_async_global();   // their atomics -> the bulk copies' reads
+                    ntail = sk_tail_count(blockIdx.x, jb.slot, sk, p.kblocks);
+                    tail0 = sk_next_tail(blockIdx.x - sk.rs, sk);
+                    if (et == 0) {   // every tail piece has stored its partial sums
+                        wait_flag_geq(p.sk_cnt + jb.slot * kWinCntStride, ntail, abort_flag, status, LORA_DEV_TIMEOUT);
+                        fence_proxy_async_global();   // their stores -> the bulk copies' reads
                         mbar_expect_tx(sk_bar, kBM * kBN * 4);
-                        for (int i = 0; i < 4; ++i)
-                            bulk_load(wring + i * kWSlot, reinterpret_cast<const uint8_t *>(part) + i * kWSlot, kWSlot,
-                                      sk_bar);
+                        const uint8_t *src = reinterpret_cast<const uint8_t *>(p.sk_part) +
+                                             static_cast<int64_t>(tail0) * kBM * kBN * 4;
+                        for (int i = 0; i < 4; ++i) bulk_load(wring + i * kWSlot, src + i * kWSlot, kWSlot, sk_bar);
                     }
                     mbar_wait(sk_bar, 0, abort_flag, status, LORA_DEV_TIMEOUT);
+                    // further tails: each thread adds them into its own row of
+                    // the shared-memory copy, sixteen loads in flight at a time
+                    float4 *sp = reinterpret_cast<float4 *>(wring);
+                    for (int i = 1, ts = tail0; i < ntail; ++i) {
+                        ts = sk_next_tail(ts, sk);
+                        const float4 *xp =
+                            reinterpret_cast<const float4 *>(p.sk_part) + static_cast<int64_t>(ts) * (kBN / 4) * kBM;
+#pragma unroll 1
+                        for (int k0 = 0; k0 < kBN / 4; k0 += 16) {
+                            float4 b[16];
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) b[k] = __ldcg(xp + (k0 + k) * kBM + row);
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) {
+                                const float4 a = sp[(k0 + k) * kBM + row];
+                                sp[(k0 + k) * kBM + row] =
+                                    make_float4(a.x + b[k].x, a.y + b[k].y, a.z + b[k].z, a.w + b[k].w);
+                            }
+                        }
+                    }
                 }
                 // one 16-column chunk: + partials, + bias (from shared memory) or
                 // the existing y (standalone expand), bf16, store to the row
@@ -621,7 +651,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     float v[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
-                    if (head) {   // the summed partials, from shared memory
+                    if (head) {   // the tails' summed partials, from shared memory
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             const float4 pv = spart[(cc * 4 + k) * kBM + row];
@@ -703,25 +733,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     bulk_commit();
                     bulk_wait_read_all();   // the row is out of shared memory; y is written before the grid ends
                 }
-                if (head) {   // all partials consumed: the counter is zero again for the next call
-                    named_bar_sync(1, 128);
-                    if (sk_tails(blockIdx.x, jb.slot, sk, p.kblocks) > 1) {
-                        // sums built by atomics: leave the scratch zeroed for
-                        // the next call, by bulk copies of a zeroed 32 KB
-                        // piece of the (now idle) W ring
-                        float4 *z = reinterpret_cast<float4 *>(wring);
-                        for (int i = et; i < kWSlot / 16; i += 128) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        fence_proxy_async_smem();
-                        named_bar_sync(1, 128);
-                        if (et == 0) {
-                            for (int i = 0; i < 4; ++i)
-                                bulk_store(reinterpret_cast<uint8_t *>(part) + i * kWSlot, wring, kWSlot);
-                            bulk_commit();
-                            bulk_wait_read_all();   // the zeros reach the scratch before the grid ends
-                        }
-                    }
-                    if (et == 0) p.sk_cnt[jb.slot * kWinCntStride] = 0;
-                }
+                if (head && et == 0) p.sk_cnt[jb.slot * kWinCntStride] = 0;   // zero again for the next call
             }
         }
     }
@@ -731,18 +743,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
-    if (p.mode == kModeLinear) {
-        // the last CTA to finish clears the per-tile ready counters
-        if (threadIdx.x == 0) {
-            __threadfence();
-            *last_flag = (atom_acq_rel_gpu_add(p.counters + CNT_CTAS_DONE, 1) == static_cast<int>(gridDim.x) - 1);
-        }
-        __syncthreads();
-        if (*last_flag) {
-            for (int m = threadIdx.x; m < p.num_mtiles; m += blockDim.x) p.counters[CNT_FIXED + m] = 0;
-            if (threadIdx.x == 0) p.counters[CNT_CTAS_DONE] = 0;
-        }
-    }
 }
 
 // Standalone expand: turn the caller's fp32 S [M, s_cols] (original token

@@ -48,7 +48,6 @@ enum PlanHdr {
 // counter block entries (int32), zero between calls
 enum Counters {
     CNT_STATUS = 0,       // LORA_DEV_* bits
-    CNT_CTAS_DONE = 1,    // tiled schedule: CTAs finished
     CNT_SPLIT_DONE = 2,   // split-K: CTAs finished
     CNT_SPLIT_SREADY = 3, // split-K: shrink row tiles reduced
     CNT_FIXED = 8         // first per-tile counter
@@ -116,8 +115,8 @@ struct TcParams {
     int32_t shrink_split;      // K pieces per shrink job; piece h writes S panel set h
     int32_t s_sets;            // S panel sets the expand steps add up (shrink_split, or 1 for expand)
     int32_t s_set_rows;        // rows of one S panel set (chunks x 128)
-    float *sk_part;            // fp32 [tiles][256/4][128][4]: summed partials of split tiles (zero at rest)
-    int32_t *sk_cnt;           // [tiles][kWinCntStride]: partials added per split tile (zero at rest)
+    float *sk_part;            // fp32 [CTAs][256/4][128][4]: each tail piece's partial sums, in its CTA's slot
+    int32_t *sk_cnt;           // [tiles][kWinCntStride]: tail pieces stored per split tile (zero at rest)
 };
 
 struct SplitParams {

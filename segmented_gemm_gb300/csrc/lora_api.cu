@@ -124,7 +124,9 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
                                            static_cast<size_t>(2 * present + 2) * 32) * T * 4;
         split_s = static_cast<size_t>(L.max_dchunks) * T * kChunk * 2;
     }
-    L.n_counters = CNT_FIXED + std::max<size_t>(L.num_mtiles, L.split_tiles) + 8;
+    // per token tile: the tiled schedule's S-ready and consumer counters;
+    // per split-K tile: its arrival counter
+    L.n_counters = CNT_FIXED + std::max<size_t>(2 * L.num_mtiles, L.split_tiles) + 8;
     // tiled schedule: S panels, one set per K piece of a shrink job (two for M > 128)
     const size_t tiled_s = static_cast<size_t>(L.max_chunks) * kBM * kChunk * 2 * tiled_s_sets(M);
     L.s_scratch_bytes = std::max(tiled_s, split_s);

@@ -72,10 +72,7 @@ extern "C" int lora_linear_noalloc(const lora_bf16_t *x, int64_t M, const lora_b
                                       {L.acc_shr, L.acc_shr_bytes},
                                       {L.sk_cnt, L.total <= LORA_NOALLOC_SCRATCH_BYTES && L.sk_part
                                                      ? static_cast<size_t>(kStreamKMaxTiles) * kWinCntStride * 4
-                                                     : 0},
-                                      {L.sk_part, L.total <= LORA_NOALLOC_SCRATCH_BYTES && L.sk_part
-                                                      ? static_cast<size_t>(kStreamKMaxTiles) * kBM * kBN * 4
-                                                      : 0}};
+                                                     : 0}};
     for (const auto &r : zero_regions)
         if (r[1] > 0 && cudaMemsetAsync(base + r[0], 0, r[1], s) != cudaSuccess) return LORA_ERR_CUDA;
     return lora_linear(x, M, W, bias, lora_id_map, pool, scale, nullptr, y, ws, LORA_NOALLOC_SCRATCH_BYTES, stream);
