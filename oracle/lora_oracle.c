@@ -19,6 +19,9 @@
  *   §4.3  ranks padded to a multiple of 16 with zero rows / columns
  * The per-call scalar `scale` multiplying the LoRA term is this project's
  * reading (the page's formula has an implicit scale of 1).
+ * A merged output (Q|K|V, gate|up: one adapter pair per output slice, as a
+ * merged projection with LoRA needs it; the page's §3.3 names the merged QKV
+ * shape) is oracle_lora_linear_slices_rows, the same formula per slice.
  *
  * Adapter storage here is the oracle's own, deliberately naive layout:
  * adapter i's A_i [r_i, K] row-major starts right after A_{i-1}, and
@@ -265,5 +268,68 @@ void oracle_lora_linear_elems(const uint16_t *x, int64_t K, const uint16_t *W, i
             acc += scale * (adapter_scale ? adapter_scale[i] : 1.0) * lora;
         }
         y[q] = acc;
+    }
+}
+
+/*
+ * The layer with a merged output (Q|K|V, gate|up, ...): the output columns
+ * are cut into nslices slices [slice_start[s], slice_start[s+1]) and adapter
+ * i has one pair per slice, A_i^s [r_i, K] and B_i^s [N_s, r_i] with
+ * N_s = slice_start[s+1] - slice_start[s].  For a token of adapter i and an
+ * output column n of slice s:
+ *   y[t,n] = base[t,n] + scale * s_i * sum_j S^s[t,j] B_i^s[n - slice_start[s], j],
+ *   S^s[t,j] = sum_k x[t,k] A_i^s[j,k]
+ * a_cat holds A_i^s row-major, adapter-major then slice; b_cat holds B_i^s
+ * row-major, adapter-major then slice.  Rows as in oracle_lora_linear_rows.
+ */
+void oracle_lora_linear_slices_rows(const uint16_t *x, int64_t M, int64_t K,
+                                    const uint16_t *W, int64_t N, const uint16_t *bias,
+                                    const int32_t *ids, int32_t num_adapters, const int32_t *rank,
+                                    int32_t nslices, const int64_t *slice_start,
+                                    const uint16_t *a_cat, const uint16_t *b_cat, double scale,
+                                    const double *adapter_scale, const int64_t *rows, int64_t nrows, double *y)
+{
+    (void)M;
+#pragma omp parallel
+    {
+        double *xr = (double *)malloc((size_t)K * sizeof(double));
+        double *S = (double *)malloc(64 * 1024 * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t q = 0; q < nrows; ++q) {
+            int64_t t = rows ? rows[q] : q;
+            for (int64_t k = 0; k < K; ++k) xr[k] = bf16_to_f64(x[t * K + k]);
+            double *yr = y + q * N;
+            for (int64_t n = 0; n < N; ++n) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k) acc += xr[k] * bf16_to_f64(W[n * K + k]);
+                if (bias) acc += bf16_to_f64(bias[n]);
+                yr[n] = acc;
+            }
+            int32_t i = effective_id(ids[t], num_adapters);
+            if (i < 0) continue;
+            int64_t r = rank[i];
+            int64_t a0 = 0, b0 = 0;   /* adapter i's first element in a_cat / b_cat */
+            for (int32_t j = 0; j < i; ++j) {
+                a0 += (int64_t)nslices * rank[j] * K;
+                b0 += N * (int64_t)rank[j];
+            }
+            double si = adapter_scale ? adapter_scale[i] : 1.0;
+            for (int32_t s = 0; s < nslices; ++s) {
+                const uint16_t *As = a_cat + a0 + (int64_t)s * r * K;
+                const uint16_t *Bs = b_cat + b0 + slice_start[s] * r;
+                for (int64_t j = 0; j < r; ++j) {
+                    double acc = 0.0;
+                    for (int64_t k = 0; k < K; ++k) acc += xr[k] * bf16_to_f64(As[j * K + k]);
+                    S[j] = acc;
+                }
+                for (int64_t n = slice_start[s]; n < slice_start[s + 1]; ++n) {
+                    double acc = 0.0;
+                    for (int64_t j = 0; j < r; ++j) acc += S[j] * bf16_to_f64(Bs[(n - slice_start[s]) * r + j]);
+                    yr[n] += scale * si * acc;
+                }
+            }
+        }
+        free(xr);
+        free(S);
     }
 }

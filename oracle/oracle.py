@@ -58,6 +58,9 @@ def _load():
         lib.oracle_shrink_rows.argtypes = [p, i64, i64, p, i32, p, p, p, i64, i64, p]
         lib.oracle_lora_linear_elems.restype = None
         lib.oracle_lora_linear_elems.argtypes = [p, i64, p, i64, p, p, i32, p, p, p, dbl, p, p, p, i64, p]
+        lib.oracle_lora_linear_slices_rows.restype = None
+        lib.oracle_lora_linear_slices_rows.argtypes = [p, i64, i64, p, i64, p, p, i32, p, i32, p, p, p, dbl,
+                                                       p, p, i64, p]
         lib.oracle_expand_rows.restype = None
         lib.oracle_expand_rows.argtypes = [p, i64, p, i64, p, i32, p, p, dbl, p, p, i64, p]
         _lib = lib
@@ -136,7 +139,10 @@ def build_segments(ids, num_adapters: int, true_ranks: Sequence[int]):
 
 def lora_linear(wl, rows=None, scale: Optional[float] = None) -> np.ndarray:
     """fp64 layer output for a Workload-like object (fields x, W, bias, ids,
-    ranks, A, B, scale).  ``rows`` selects output rows; returns [len(rows), N]."""
+    ranks, A, B, scale; or slices, A_s, B_s for a merged output).  ``rows``
+    selects output rows; returns [len(rows), N]."""
+    if getattr(wl, "slices", None):
+        return _lora_linear_slices(wl, rows, scale)
     lib = _load()
     x, W, bias = _bits(wl.x), _bits(wl.W), _bits(wl.bias)
     ids = np.ascontiguousarray(wl.ids.numpy().astype(np.int32))
@@ -149,6 +155,25 @@ def lora_linear(wl, rows=None, scale: Optional[float] = None) -> np.ndarray:
     lib.oracle_lora_linear_rows(_ptr(x), wl.M, wl.K, _ptr(W), wl.N, _ptr(bias), _ptr(ids),
                                 len(wl.ranks), _ptr(rk), _ptr(a_cat), _ptr(b_cat), float(s),
                                 _ptr(asc), _ptr(r), nrows, _ptr(y))
+    return y
+
+
+def _lora_linear_slices(wl, rows, scale):
+    """Merged output: one A / B pair per output slice and adapter."""
+    lib = _load()
+    x, W, bias = _bits(wl.x), _bits(wl.W), _bits(wl.bias)
+    ids = np.ascontiguousarray(wl.ids.numpy().astype(np.int32))
+    rk = np.ascontiguousarray(np.asarray(list(wl.ranks) or [0], dtype=np.int32))
+    assert sum(wl.slices) == wl.N
+    starts = np.ascontiguousarray(np.concatenate([[0], np.cumsum(wl.slices)]).astype(np.int64))
+    a_cat = _concat([a for per in wl.A_s for a in per], wl.K)
+    b_cat = _concat([b for per in wl.B_s for b in per], wl.N)
+    r, nrows = _rows_arg(rows, wl.M)
+    y = np.zeros((nrows, wl.N), dtype=np.float64)
+    s = wl.scale if scale is None else scale
+    lib.oracle_lora_linear_slices_rows(_ptr(x), wl.M, wl.K, _ptr(W), wl.N, _ptr(bias), _ptr(ids), len(wl.ranks),
+                                       _ptr(rk), len(wl.slices), _ptr(starts), _ptr(a_cat), _ptr(b_cat), float(s),
+                                       _ptr(_adapter_scale(wl)), _ptr(r), nrows, _ptr(y))
     return y
 
 

@@ -44,6 +44,12 @@ class Workload:
     meta: dict = field(default_factory=dict)
     # per-adapter factor on the LoRA term (e.g. alpha_i / r_i); None = 1 for all
     adapter_scale: Optional[List[float]] = None
+    # merged output (e.g. Q|K|V): widths of the output slices (sum N); then each
+    # adapter has one pair per slice, A_s[i][s] bf16 [r_i, K] and
+    # B_s[i][s] bf16 [N_s, r_i], and A / B are None
+    slices: Optional[List[int]] = None
+    A_s: Optional[List[List[torch.Tensor]]] = None
+    B_s: Optional[List[List[torch.Tensor]]] = None
 
     @property
     def num_adapters(self) -> int:
@@ -228,6 +234,29 @@ def make_custom(M: int, K: int, N: int, ranks: List[int], seed: int, ids=None,
     return Workload(name=f"custom_M{M}_K{K}_N{N}", M=M, K=K, N=N, ranks=list(ranks),
                     ids=ids.to(torch.int32), x=x, W=W, bias=bias, A=A, B=B, scale=scale, seed=seed,
                     adapter_scale=None if adapter_scale is None else [float(v) for v in adapter_scale])
+
+
+def make_sliced(M: int, K: int, slices: List[int], ranks: List[int], seed: int, ids=None,
+                id_mode: str = "uniform", p_base: float = 0.1, scale: float = 2.0, with_bias: bool = True,
+                adapter_scale=None) -> Workload:
+    """A merged-output workload: output slices of widths ``slices`` (for a
+    merged QKV projection, [q, k, v]) and, per adapter, one A / B pair per
+    slice with the adapter's rank.  Ids and the base tensors are drawn as in
+    make_custom (same seed, same structure); A ~ N(0, 1/sqrt(K)),
+    B ~ N(0, 0.02)."""
+    N = int(sum(slices))
+    base = make_custom(M, K, N, ranks, seed, ids=ids, id_mode=id_mode, p_base=p_base, scale=scale,
+                       with_bias=with_bias, adapter_scale=adapter_scale)
+    g = torch.Generator().manual_seed(seed + 7919)
+    a_std = 1.0 / math.sqrt(K)
+    A_s, B_s = [], []
+    for r in ranks:
+        A_s.append([(torch.randn(r, K, generator=g) * a_std).to(torch.bfloat16) for _ in slices])
+        B_s.append([(torch.randn(n, r, generator=g) * 0.02).to(torch.bfloat16) for n in slices])
+    base.name = f"sliced_M{M}_K{K}_N{'+'.join(str(n) for n in slices)}"
+    base.A, base.B = None, None
+    base.slices, base.A_s, base.B_s = [int(n) for n in slices], A_s, B_s
+    return base
 
 
 def random_fp32(shape, seed: int, std: float = 1.0) -> torch.Tensor:

@@ -6,6 +6,7 @@ a brute-force Python loop on tiny inputs, a worked example printed on the
 page, or an invariant).  Source: "vLLM-Ascend dynamic LoRA"
 (pptc.cn/news/149022), sections cited per test.
 """
+import dataclasses
 import json
 import os
 
@@ -285,3 +286,84 @@ def test_element_samples_match_rows():
         assert abs(e[q] - want) <= 1e-11 * max(1.0, abs(want))
     full = oracle.lora_linear_rows_prepared(prep, list(range(wl.M)))
     assert np.allclose(e, full[rows, cols], rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# merged output (Q|K|V, gate|up): one adapter pair per output slice
+# ---------------------------------------------------------------------------
+
+def _one_slice_as_plain(wl):
+    """The same workload written as an ordinary (single-output) one."""
+    return dataclasses.replace(wl, slices=None, A=[a[0] for a in wl.A_s], B=[b[0] for b in wl.B_s],
+                               A_s=None, B_s=None)
+
+
+def test_single_slice_is_the_plain_layer():
+    wl = workloads.make_sliced(12, 48, [40], [16, 8, 32], seed=61, adapter_scale=[1.0, 0.5, 2.0])
+    assert _rel_close(oracle.lora_linear(wl), oracle.lora_linear(_one_slice_as_plain(wl)), 1e-13)
+
+
+@pytest.mark.parametrize("which", [0, 1])
+def test_sliced_single_adapter_equals_merged_weight(which):
+    """Every token uses adapter i: the merged output is x W'^T + bias with
+    W' = W whose slice-s rows get scale * s_i * B_i^s A_i^s added."""
+    wl = workloads.make_sliced(14, 56, [32, 16, 24], [16, 8], seed=62 + which, scale=1.5,
+                               adapter_scale=[0.5, 3.0])
+    wl.ids[:] = which
+    Wm = f64(wl.W).copy()
+    n0 = 0
+    for s, n in enumerate(wl.slices):
+        Wm[n0:n0 + n] += wl.scale * wl.adapter_scale[which] * f64(wl.B_s[which][s]) @ f64(wl.A_s[which][s])
+        n0 += n
+    ref = f64(wl.x) @ Wm.T + f64(wl.bias)[None, :]
+    assert _rel_close(oracle.lora_linear(wl), ref, 1e-10)
+
+
+def test_sliced_brute_force_per_element():
+    wl = workloads.make_sliced(6, 12, [4, 8, 4], [4, 8, 4], seed=64, id_mode="uniform", p_base=0.3)
+    x, W = f64(wl.x), f64(wl.W)
+    starts = [0, 4, 12, 16]
+    want = np.zeros((wl.M, wl.N))
+    for t in range(wl.M):
+        i = int(wl.ids[t])
+        for n in range(wl.N):
+            v = sum(x[t, k] * W[n, k] for k in range(wl.K)) + float(f64(wl.bias)[n])
+            if i >= 0:
+                s = max(q for q in range(3) if starts[q] <= n)
+                A, B = f64(wl.A_s[i][s]), f64(wl.B_s[i][s])
+                S = [sum(x[t, k] * A[j, k] for k in range(wl.K)) for j in range(wl.ranks[i])]
+                v += wl.scale * sum(S[j] * B[n - starts[s], j] for j in range(wl.ranks[i]))
+            want[t, n] = v
+    assert _rel_close(oracle.lora_linear(wl), want, 1e-12)
+
+
+def test_sliced_equals_stacked_block_diagonal_adapter():
+    """The representation the GPU pool uses: adapter i as one adapter of rank
+    S * r_i, its A the slices' A stacked and its B block-diagonal (slice s's
+    rows use only columns [s r_i, (s + 1) r_i))."""
+    wl = workloads.make_sliced(20, 64, [32, 16, 16], [16, 32], seed=65, adapter_scale=[2.0, 0.25])
+    A, B = [], []
+    for i, r in enumerate(wl.ranks):
+        A.append(torch.cat(wl.A_s[i], dim=0))
+        Bd = torch.zeros(wl.N, len(wl.slices) * r, dtype=torch.bfloat16)
+        n0 = 0
+        for s, n in enumerate(wl.slices):
+            Bd[n0:n0 + n, s * r:(s + 1) * r] = wl.B_s[i][s]
+            n0 += n
+        B.append(Bd)
+    stacked = dataclasses.replace(wl, slices=None, A_s=None, B_s=None, A=A, B=B,
+                                  ranks=[len(wl.slices) * r for r in wl.ranks])
+    assert _rel_close(oracle.lora_linear(wl), oracle.lora_linear(stacked), 1e-12)
+
+
+def test_a_slice_pair_touches_only_its_columns():
+    wl = workloads.make_sliced(16, 40, [24, 8, 16], [16], seed=66, id_mode="single")
+    y0 = oracle.lora_linear(wl)
+    wl.B_s[0][1] = (f64_t(wl.B_s[0][1]) * 3.0).to(torch.bfloat16)
+    y1 = oracle.lora_linear(wl)
+    changed = np.abs(y1 - y0).max(axis=0) > 0
+    assert not changed[:24].any() and not changed[32:].any() and changed[24:32].all()
+
+
+def f64_t(t):
+    return t.to(torch.float64)
