@@ -63,12 +63,15 @@ enum {
 /* Device-side status bits (returned through lora_get_status). */
 enum {
     LORA_DEV_BAD_ID = 1 << 0,   /* some id was < -1 or >= num_adapters (treated as -1) */
-    LORA_DEV_TIMEOUT = 1 << 1   /* a bounded wait gave up; that call's output is invalid */
+    LORA_DEV_TIMEOUT = 1 << 1,  /* a bounded wait gave up; that call's output is invalid */
+    LORA_DEV_BAD_POOL = 1 << 2  /* a rank is not a whole number of 16-wide panels per output slice */
 };
 
 #define LORA_MAX_RANK 64        /* largest padded rank */
 #define LORA_RANK_ALIGN 16      /* ranks are padded to a multiple of this (§4.3) */
 #define LORA_MAX_ADAPTERS 1024  /* largest num_adapters in one pool */
+#define LORA_MAX_SLICES 4       /* most output slices of a merged projection */
+#define LORA_SLICE_ALIGN 256    /* output slice boundaries are multiples of this */
 
 /*
  * Rank-grouped adapter pool (§2.1: all adapters of one rank stored in one
@@ -88,6 +91,20 @@ enum {
  *        Read by lora_linear and lora_expand (lora_shrink returns unscaled
  *        S); a call that reads it needs its lora_id_map even when it is
  *        given a prebuilt segment table.
+ * num_slices, slice_start (host values): a merged projection (Q|K|V,
+ *        gate|up) whose output columns are cut into num_slices slices
+ *        [slice_start[s], slice_start[s+1]), slice_start[0] = 0 and
+ *        slice_start[num_slices] = N, inner boundaries multiples of
+ *        LORA_SLICE_ALIGN; each adapter then has one A / B pair per slice
+ *        with one rank r_i.  The pool holds adapter i as one adapter of
+ *        rank num_slices * r_i (r_i padded to 16): A rows [s r_i, (s+1) r_i)
+ *        are slice s's A, and B is block-diagonal, B[n, j] = slice s's
+ *        B[n - slice_start[s], j - s r_i] for n in slice s and j in
+ *        [s r_i, (s+1) r_i), zero elsewhere.  The tiled schedule skips the
+ *        zero blocks; the decode-sized schedules read them.  num_slices 0 or
+ *        1: one output (slice_start unused).  lora_shrink returns the
+ *        stacked S (slice s in columns [s r_i, (s+1) r_i)); lora_expand takes
+ *        it in the same form.
  * a_elems / b_elems (host values) are the total element counts of the pools;
  * num_adapters, max_rank (largest rank[i]), K and N are host values.
  * lora_pool_layout() computes offsets, padded ranks and sizes for a set of
@@ -106,6 +123,8 @@ typedef struct {
     int32_t K;
     int32_t N;
     const float *adapter_scale;
+    int32_t num_slices;
+    int32_t slice_start[LORA_MAX_SLICES + 1];
 } lora_pool_t;
 
 /*
@@ -135,7 +154,7 @@ typedef struct {
     void *plan;                 /* internal: tile / chunk work lists */
     int64_t M;
     int32_t num_adapters;
-    int32_t reserved;
+    int32_t num_slices;         /* output slices of the pool it was built for (>= 1) */
 } lora_segments_t;
 
 /*

@@ -97,8 +97,12 @@ __device__ __forceinline__ Job decode_job(int j, int n_sjobs, const TcParams &p)
     jb.kind = 1;
     jb.m = m0 + r % gm;
     jb.n = r / gm;
-    jb.c0 = p.tile_chunk_off[jb.m];
-    jb.c1 = p.tile_chunk_off[jb.m + 1];
+    // the expand steps use the panels of the output slice holding tile n
+    int sl = 0;
+    for (int k = 1; k < p.num_slices; ++k)
+        if (jb.n * kBN >= p.slice_start[k]) sl = k;
+    jb.c0 = p.tile_chunk_off[jb.m * p.num_slices + sl];
+    jb.c1 = p.tile_chunk_off[jb.m * p.num_slices + sl + 1];
     return jb;
 }
 
@@ -759,7 +763,7 @@ __global__ void __launch_bounds__(kBM) s_prep_kernel(const float *S, int32_t s_c
         const int id = p.ids[tok];
         scale *= (id >= 0 && id < p.num_adapters) ? p.adapter_scale[id] : 0.f;
     }
-    for (int c = p.tile_chunk_off[m]; c < p.tile_chunk_off[m + 1]; ++c) {
+    for (int c = p.tile_chunk_off[m * p.num_slices]; c < p.tile_chunk_off[(m + 1) * p.num_slices]; ++c) {
         const int32_t rng = p.chunk_rng[c];
         const bool keep = valid && row >= rng_lo(rng) && row < rng_hi(rng);
         const float *src = S + static_cast<int64_t>(tok) * s_cols + rng_panel(rng) * kChunk;

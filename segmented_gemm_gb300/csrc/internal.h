@@ -19,6 +19,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "lora.h"
+
 namespace lora {
 
 // ---- tiled (token-tile x output-tile) schedule -----------------------------
@@ -100,6 +102,8 @@ struct TcParams {
     int32_t N, K, kblocks, num_mtiles, num_ntiles, group_m, mode, s_cols;
     float scale;
     int32_t num_adapters;
+    int32_t num_slices;        // output slices (>= 1); tile_chunk_off holds [tiles][slices] + 1 offsets
+    int32_t slice_start[LORA_MAX_SLICES + 1];   // first output column of each slice
     const int32_t *ids;        // lora_id_map (original token order); read when adapter_scale is set
     const float *adapter_scale;   // per-adapter factor on top of scale, or null (all 1)
     const uint16_t *bias;      // bf16 [N] or null
@@ -146,6 +150,7 @@ struct SegParams {
     int32_t *dchunk_arow, *dchunk_brow, *dchunk_adapter;
     int32_t *counters;
     int32_t n_counters;
+    int32_t num_slices;        // output slices of a merged projection (>= 1): tile chunk lists are slice-major
 };
 
 struct ClusterMaps {

@@ -146,7 +146,7 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
     L.seg_rank = take(static_cast<size_t>(std::max(A, 1)) * 4);
     L.num_segments = take(4);
     L.hdr = take(HDR_WORDS * 4);
-    L.tile_chunk_off = take(static_cast<size_t>(L.num_mtiles + 1) * 4);
+    L.tile_chunk_off = take((static_cast<size_t>(L.num_mtiles) * LORA_MAX_SLICES + 1) * 4);
     L.chunk_arow = take(static_cast<size_t>(L.max_chunks) * 4);
     L.chunk_brow = take(static_cast<size_t>(L.max_chunks) * 4);
     L.chunk_rng = take(static_cast<size_t>(L.max_chunks) * 4);
@@ -193,12 +193,23 @@ static int check_pool(const lora_pool_t *pool)
     if (!pool) return LORA_ERR_NULL;
     if (pool->K <= 0 || pool->N <= 0 || (pool->K % 8) || (pool->N % 8)) return LORA_ERR_SHAPE;
     if (pool->num_adapters < 0 || pool->num_adapters > LORA_MAX_ADAPTERS) return LORA_ERR_SHAPE;
+    if (pool->num_slices < 0 || pool->num_slices > LORA_MAX_SLICES) return LORA_ERR_SHAPE;
+    const int S = pool->num_slices;
+    if (S > 1) {
+        // a merged output: ordered slices covering [0, N), inner boundaries
+        // on output-tile edges
+        if (pool->slice_start[0] != 0 || pool->slice_start[S] != pool->N) return LORA_ERR_SHAPE;
+        for (int s = 1; s <= S; ++s)
+            if (pool->slice_start[s] <= pool->slice_start[s - 1] || (s < S && pool->slice_start[s] % LORA_SLICE_ALIGN))
+                return LORA_ERR_SHAPE;
+    }
     if (pool->num_adapters > 0) {
         if (!pool->a_pool || !pool->b_pool || !pool->a_offset || !pool->b_offset || !pool->rank) return LORA_ERR_NULL;
         if (!aligned16(pool->a_pool) || !aligned16(pool->b_pool)) return LORA_ERR_ALIGN;
         if (reinterpret_cast<uintptr_t>(pool->adapter_scale) & 3) return LORA_ERR_ALIGN;
         if (pool->max_rank < LORA_RANK_ALIGN || pool->max_rank > LORA_MAX_RANK || (pool->max_rank % LORA_RANK_ALIGN))
             return LORA_ERR_RANK;
+        if (S > 1 && pool->max_rank % (LORA_RANK_ALIGN * S)) return LORA_ERR_RANK;   // whole panels per slice
         if (pool->a_elems <= 0 || pool->b_elems <= 0 || (pool->a_elems % pool->K) || (pool->b_elems % kChunk))
             return LORA_ERR_SHAPE;
     }
@@ -210,7 +221,7 @@ struct Carve {
     int32_t *counters;
 };
 
-static void fill_segments(void *ws, const WsLayout &L, int64_t M, int32_t A, lora_segments_t *out)
+static void fill_segments(void *ws, const WsLayout &L, int64_t M, const lora_pool_t *pool, lora_segments_t *out)
 {
     out->perm = at<int32_t>(ws, L.perm);
     out->bucket_offsets = at<int32_t>(ws, L.offsets);
@@ -221,8 +232,8 @@ static void fill_segments(void *ws, const WsLayout &L, int64_t M, int32_t A, lor
     out->num_segments = at<int32_t>(ws, L.num_segments);
     out->plan = ws;
     out->M = M;
-    out->num_adapters = A;
-    out->reserved = 0;
+    out->num_adapters = pool->num_adapters;
+    out->num_slices = pool->num_slices > 1 ? pool->num_slices : 1;
 }
 
 static void fill_seg_params(SegParams &p, const int32_t *ids, int64_t M, const lora_pool_t *pool, const WsLayout &L,
@@ -258,6 +269,7 @@ static void fill_seg_params(SegParams &p, const int32_t *ids, int64_t M, const l
     p.dchunk_adapter = at<int32_t>(ws, L.dchunk_adapter);
     p.counters = at<int32_t>(ws, L.counters);
     p.n_counters = static_cast<int32_t>(L.n_counters);
+    p.num_slices = pool->num_slices > 1 ? pool->num_slices : 1;
 }
 
 static int enqueue_segments(const int32_t *ids, int64_t M, const lora_pool_t *pool, const WsLayout &L, void *ws,
@@ -282,7 +294,9 @@ static int prepare(const int32_t *ids, int64_t M, const lora_pool_t *pool, const
     *L = make_ws_layout(M, pool->N, pool->num_adapters);
     if (ws_bytes < L->total_min) return LORA_ERR_WORKSPACE;
     if (segs) {
-        if (segs->plan != ws || segs->M != M || segs->num_adapters != pool->num_adapters) return LORA_ERR_SEGMENTS;
+        if (segs->plan != ws || segs->M != M || segs->num_adapters != pool->num_adapters ||
+            segs->num_slices != (pool->num_slices > 1 ? pool->num_slices : 1))
+            return LORA_ERR_SEGMENTS;
         return LORA_OK;
     }
     if (!ids) return LORA_ERR_NULL;
@@ -295,6 +309,8 @@ static void fill_tc_params(TcParams &p, const WsLayout &L, void *ws, const lora_
     p.M = M;
     p.num_adapters = pool->num_adapters;
     p.adapter_scale = pool->num_adapters ? pool->adapter_scale : nullptr;
+    p.num_slices = pool->num_slices > 1 ? pool->num_slices : 1;
+    for (int s = 0; s <= LORA_MAX_SLICES; ++s) p.slice_start[s] = s <= p.num_slices && p.num_slices > 1 ? pool->slice_start[s] : 0;
     p.N = pool->N;
     p.K = pool->K;
     p.kblocks = (pool->K + kBK - 1) / kBK;
@@ -600,12 +616,12 @@ int lora_build_segments(const int32_t *lora_id_map, int64_t M, const lora_pool_t
         if (rc) return rc;
         L = make_ws_layout(0, pool->N, pool->num_adapters);
         if (!ws || ws_bytes < L.total_min) return LORA_ERR_WORKSPACE;
-        fill_segments(ws, L, 0, pool->num_adapters, out);
+        fill_segments(ws, L, 0, pool, out);
         return LORA_OK;
     }
     int rc = prepare(lora_id_map, M, pool, nullptr, ws, ws_bytes, static_cast<cudaStream_t>(stream), &L);
     if (rc) return rc;
-    fill_segments(ws, L, M, pool->num_adapters, out);
+    fill_segments(ws, L, M, pool, out);
     return LORA_OK;
 }
 

@@ -117,6 +117,7 @@ struct SegBuild {
     static __device__ void run(const SegParams &p, int *sm)
     {
         const int A = p.A, nb = A + 1;
+        const int nsl = p.num_slices > 1 ? p.num_slices : 1;   // output slices (merged projection)
         int *whist = sm;                          // [kSegWarps][nb]
         int *bsum = whist + kSegWarps * nb;       // [nb + 1] bucket offsets
         int *wsum = bsum + nb + 1;                // [32] scan scratch
@@ -138,6 +139,9 @@ struct SegBuild {
             s_rank[i] = p.rank[i];
             s_arow[i] = static_cast<int>(p.a_offset[i] / p.K);
             s_brow[i] = static_cast<int>(p.b_offset[i] / kChunk);
+            // a merged output needs every adapter's rank in whole 16-wide
+            // panels per slice
+            if (s_rank[i] % (kChunk * nsl) != 0) atomicOr(p.counters + CNT_STATUS, LORA_DEV_BAD_POOL);
         }
         __syncthreads();
 
@@ -262,7 +266,7 @@ struct SegBuild {
                 for (int b0 = bfirst; b0 <= A; b0 += 32) {
                     const int b = b0 + lane;
                     const bool in = b <= A && bsum[b] < hi;
-                    int nc = (in && bsum[b + 1] > bsum[b]) ? s_rank[b - 1] / kChunk : 0;
+                    int nc = (in && bsum[b + 1] > bsum[b]) ? s_rank[b - 1] / kChunk / nsl * nsl : 0;
     #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) nc += __shfl_xor_sync(0xffffffffu, nc, o);
                     nch += nc;
@@ -280,33 +284,35 @@ struct SegBuild {
                     cbase += t_nch[k];
                     jbase += t_nj[k];
                 }
+                // slice-major: the panels of output slice 0 of every segment,
+                // then slice 1's, ... (one slice unless the output is merged)
                 int c = cbase;
-                for (int b0 = bfirst; b0 <= A; b0 += 32) {
-                    const int b = b0 + lane;
-                    const bool in = b <= A && bsum[b] < hi;
-                    const bool live = in && bsum[b + 1] > bsum[b];
-                    const int nc = live ? s_rank[b - 1] / kChunk : 0;
-                    const int incl = warp_incl_scan(nc, lane);
-                    if (live) {
-                        const int64_t s0 = bsum[b], s1 = bsum[b + 1];
-                        const int rlo = static_cast<int>((s0 > lo ? s0 : lo) - lo);
-                        const int rhi = static_cast<int>((s1 < hi ? s1 : hi) - lo);
-                        const int i = b - 1;
-                        for (int q = 0; q < nc; ++q) {
-                            const int cc = c + incl - nc + q;
-                            p.chunk_arow[cc] = s_arow[i] + kChunk * q;
-                            p.chunk_brow[cc] = s_brow[i] + q * p.N;
-                            p.chunk_rng[cc] = pack_rng(rlo, rhi, q);
+                for (int sl = 0; sl < nsl; ++sl) {
+                    if (lane == 0) p.tile_chunk_off[m * nsl + sl] = c;
+                    for (int b0 = bfirst; b0 <= A; b0 += 32) {
+                        const int b = b0 + lane;
+                        const bool in = b <= A && bsum[b] < hi;
+                        const bool live = in && bsum[b + 1] > bsum[b];
+                        const int nc = live ? s_rank[b - 1] / kChunk / nsl : 0;   // panels per slice
+                        const int incl = warp_incl_scan(nc, lane);
+                        if (live) {
+                            const int64_t s0 = bsum[b], s1 = bsum[b + 1];
+                            const int rlo = static_cast<int>((s0 > lo ? s0 : lo) - lo);
+                            const int rhi = static_cast<int>((s1 < hi ? s1 : hi) - lo);
+                            const int i = b - 1;
+                            for (int qq = 0; qq < nc; ++qq) {
+                                const int cc = c + incl - nc + qq, q = sl * nc + qq;
+                                p.chunk_arow[cc] = s_arow[i] + kChunk * q;
+                                p.chunk_brow[cc] = s_brow[i] + q * p.N;
+                                p.chunk_rng[cc] = pack_rng(rlo, rhi, q);
+                            }
                         }
+                        c += __shfl_sync(0xffffffffu, incl, 31);
+                        if (__ballot_sync(0xffffffffu, in) != 0xffffffffu) break;
                     }
-                    c += __shfl_sync(0xffffffffu, incl, 31);
-                    if (__ballot_sync(0xffffffffu, in) != 0xffffffffu) break;
                 }
                 const int nj = t_nj[m];
-                if (lane == 0) {
-                    p.tile_chunk_off[m] = cbase;
-                    p.tile_njobs[m] = nj;
-                }
+                if (lane == 0) p.tile_njobs[m] = nj;
                 for (int q = lane; q < nj; q += 32) {
                     p.sjob_tile[jbase + q] = m;
                     p.sjob_c0[jbase + q] = cbase + kMaxShrinkChunks * q;
@@ -314,7 +320,7 @@ struct SegBuild {
                     p.sjob_c1[jbase + q] = c1 < cbase + nch ? c1 : cbase + nch;
                 }
                 if (m == p.num_mtiles - 1 && lane == 0) {
-                    p.tile_chunk_off[p.num_mtiles] = cbase + nch;
+                    p.tile_chunk_off[p.num_mtiles * nsl] = cbase + nch;
                     p.hdr[HDR_NCHUNKS] = cbase + nch;
                     p.hdr[HDR_NSJOBS] = jbase + nj;
                 }
@@ -340,7 +346,7 @@ struct SegBuild {
                     }
                     bfirst = L;
                     for (int b = bfirst; b <= A && bsum[b] < hi; ++b)
-                        if (bsum[b + 1] > bsum[b]) nch += s_rank[b - 1] / kChunk;
+                        if (bsum[b + 1] > bsum[b]) nch += s_rank[b - 1] / kChunk / nsl * nsl;
                 }
                 const int nj = (nch + kMaxShrinkChunks - 1) / kMaxShrinkChunks;
                 int exc, exj, totc, totj;
@@ -348,18 +354,21 @@ struct SegBuild {
                 if (m < p.num_mtiles) {
                     int c = carry_c + exc;
                     const int cfirst = c;
-                    p.tile_chunk_off[m] = c;
                     p.tile_njobs[m] = nj;
-                    for (int b = bfirst; b <= A && bsum[b] < hi; ++b) {
-                        const int64_t s0 = bsum[b], s1 = bsum[b + 1];
-                        if (s1 == s0) continue;
-                        const int rlo = static_cast<int>((s0 > lo ? s0 : lo) - lo);
-                        const int rhi = static_cast<int>((s1 < hi ? s1 : hi) - lo);
-                        const int i = b - 1;
-                        for (int q = 0; q < s_rank[i] / kChunk; ++q, ++c) {
-                            p.chunk_arow[c] = s_arow[i] + kChunk * q;
-                            p.chunk_brow[c] = s_brow[i] + q * p.N;
-                            p.chunk_rng[c] = pack_rng(rlo, rhi, q);
+                    for (int sl = 0; sl < nsl; ++sl) {   // slice-major, as above
+                        p.tile_chunk_off[m * nsl + sl] = c;
+                        for (int b = bfirst; b <= A && bsum[b] < hi; ++b) {
+                            const int64_t s0 = bsum[b], s1 = bsum[b + 1];
+                            if (s1 == s0) continue;
+                            const int rlo = static_cast<int>((s0 > lo ? s0 : lo) - lo);
+                            const int rhi = static_cast<int>((s1 < hi ? s1 : hi) - lo);
+                            const int i = b - 1;
+                            const int np = s_rank[i] / kChunk / nsl;
+                            for (int q = sl * np; q < (sl + 1) * np; ++q, ++c) {
+                                p.chunk_arow[c] = s_arow[i] + kChunk * q;
+                                p.chunk_brow[c] = s_brow[i] + q * p.N;
+                                p.chunk_rng[c] = pack_rng(rlo, rhi, q);
+                            }
                         }
                     }
                     const int j = carry_j + exj;
@@ -374,7 +383,7 @@ struct SegBuild {
                 carry_j += totj;
             }
             if (gt == 0) {
-                p.tile_chunk_off[p.num_mtiles] = carry_c;
+                p.tile_chunk_off[p.num_mtiles * nsl] = carry_c;
                 p.hdr[HDR_NCHUNKS] = carry_c;
                 p.hdr[HDR_NSJOBS] = carry_j;
             }

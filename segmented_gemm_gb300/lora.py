@@ -22,9 +22,10 @@ LORA_ERR_NULL, LORA_ERR_SHAPE, LORA_ERR_ALIGN, LORA_ERR_RANK = 1, 2, 3, 4
 LORA_ERR_WORKSPACE, LORA_ERR_CUDA, LORA_ERR_UNSUPPORTED, LORA_ERR_SEGMENTS = 5, 6, 7, 8
 LORA_ERR_CAPACITY = 9
 LORA_NOALLOC_SCRATCH_BYTES = 8 << 20
-LORA_DEV_BAD_ID, LORA_DEV_TIMEOUT = 1, 2
+LORA_DEV_BAD_ID, LORA_DEV_TIMEOUT, LORA_DEV_BAD_POOL = 1, 2, 4
 LORA_PATH_AUTO, LORA_PATH_TILED, LORA_PATH_SPLITK, LORA_PATH_STREAM = 0, 1, 2, 3
 LORA_FLAG_STATIC_WEIGHTS = 0x100
+LORA_MAX_SLICES = 4
 LORA_MAX_RANK, LORA_RANK_ALIGN, LORA_MAX_ADAPTERS = 64, 16, 1024
 
 EXPORTS = ("lora_pool_layout", "lora_workspace_size", "lora_workspace_init", "lora_build_segments",
@@ -37,7 +38,8 @@ class lora_pool_t(ctypes.Structure):
                 ("a_offset", ctypes.c_void_p), ("b_offset", ctypes.c_void_p),
                 ("rank", ctypes.c_void_p), ("a_elems", ctypes.c_int64), ("b_elems", ctypes.c_int64),
                 ("num_adapters", ctypes.c_int32), ("max_rank", ctypes.c_int32),
-                ("K", ctypes.c_int32), ("N", ctypes.c_int32), ("adapter_scale", ctypes.c_void_p)]
+                ("K", ctypes.c_int32), ("N", ctypes.c_int32), ("adapter_scale", ctypes.c_void_p),
+                ("num_slices", ctypes.c_int32), ("slice_start", ctypes.c_int32 * (LORA_MAX_SLICES + 1))]
 
 
 class lora_segments_t(ctypes.Structure):
@@ -45,7 +47,7 @@ class lora_segments_t(ctypes.Structure):
                 ("seg_id", ctypes.c_void_p), ("seg_start", ctypes.c_void_p),
                 ("seg_len", ctypes.c_void_p), ("seg_rank", ctypes.c_void_p),
                 ("num_segments", ctypes.c_void_p), ("plan", ctypes.c_void_p),
-                ("M", ctypes.c_int64), ("num_adapters", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("M", ctypes.c_int64), ("num_adapters", ctypes.c_int32), ("num_slices", ctypes.c_int32)]
 
 
 class LoraError(RuntimeError):
@@ -174,6 +176,35 @@ def build_pool(A: List[torch.Tensor], B: List[torch.Tensor], K: int, N: int, dev
                        rank.data_ptr(), a_elems, b_elems, len(A), max(rpad) if rpad else 0, K, N,
                        asc.data_ptr() if asc is not None else None)
     return LoraPool(a_pool, b_pool, a_offset, b_offset, rank, desc, ranks, rpad, asc)
+
+
+def build_pool_sliced(A_s: List[List[torch.Tensor]], B_s: List[List[torch.Tensor]], K: int, slices: Sequence[int],
+                      device="cuda", adapter_scale: Optional[Sequence[float]] = None) -> LoraPool:
+    """A merged-output pool (Q|K|V, gate|up): A_s[i][s] [r_i, K] and
+    B_s[i][s] [N_s, r_i] for output slices of widths ``slices``.  Adapter i is
+    stored as one adapter of rank S * ceil16(r_i): the slices' A stacked (each
+    padded to 16 rows) and a block-diagonal B (include/lora.h, lora_pool_t)."""
+    S, N = len(slices), int(sum(slices))
+    assert 1 <= S <= LORA_MAX_SLICES
+    starts = [0]
+    for n in slices:
+        starts.append(starts[-1] + int(n))
+    A, B = [], []
+    for a_list, b_list in zip(A_s, B_s):
+        r = int(a_list[0].shape[0])
+        rp = (r + 15) // 16 * 16
+        a = torch.zeros(S * rp, K, dtype=torch.bfloat16)
+        b = torch.zeros(N, S * rp, dtype=torch.bfloat16)
+        for s in range(S):
+            a[s * rp:s * rp + r] = a_list[s].to(torch.bfloat16)
+            b[starts[s]:starts[s + 1], s * rp:s * rp + r] = b_list[s].to(torch.bfloat16)
+        A.append(a)
+        B.append(b)
+    pool = build_pool(A, B, K, N, device, adapter_scale=adapter_scale)
+    pool.desc.num_slices = S
+    for s in range(S + 1):
+        pool.desc.slice_start[s] = starts[s]
+    return pool
 
 
 # ---------------------------------------------------------------------------

@@ -97,3 +97,25 @@ def test_adapter_factors_need_ids_and_alignment_without_gpu(lib):
     rc = lib.lora_linear_ex(0x7000, 4, 0x8000, None, 0xB000, ctypes.byref(pool), f, None, 0x9000, 0xA000, 1 << 20,
                             None, 0)
     assert rc == L.LORA_ERR_ALIGN
+
+
+def _fake_sliced_pool(starts, max_rank=48, num_slices=None):
+    pool = L.lora_pool_t(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 64 * 48, 768 * 48, 1, max_rank, 64, 768, None)
+    pool.num_slices = len(starts) - 1 if num_slices is None else num_slices
+    for s, v in enumerate(starts):
+        pool.slice_start[s] = v
+    return pool
+
+
+@pytest.mark.parametrize("starts,max_rank,code", [
+    ([0, 100, 768], 32, L.LORA_ERR_SHAPE),          # inner boundary off the 256-column grid
+    ([0, 512, 256, 768], 48, L.LORA_ERR_SHAPE),     # not increasing
+    ([0, 256, 512], 48, L.LORA_ERR_SHAPE),          # does not end at N
+    ([0, 256, 512, 768], 32, L.LORA_ERR_RANK),      # rank not whole panels per slice
+    ([0, 256, 512, 768, 768, 768], 48, L.LORA_ERR_SHAPE),   # more slices than LORA_MAX_SLICES
+])
+def test_sliced_pool_rejected_without_gpu(lib, starts, max_rank, code):
+    pool = _fake_sliced_pool(starts, max_rank) if len(starts) <= 5 else _fake_sliced_pool(starts[:5], max_rank, 5)
+    rc = lib.lora_linear_ex(0x7000, 4, 0x8000, None, 0xB000, ctypes.byref(pool), ctypes.c_float(1.0), None, 0x9000,
+                            0xA000, 1 << 20, None, 0)
+    assert rc == code

@@ -22,8 +22,12 @@ TOL = 2e-2
 
 def to_dev(wl):
     d = "cuda"
+    if wl.slices:
+        pool = L.build_pool_sliced(wl.A_s, wl.B_s, wl.K, wl.slices, d, adapter_scale=wl.adapter_scale)
+    else:
+        pool = L.build_pool(wl.A, wl.B, wl.K, wl.N, d, adapter_scale=wl.adapter_scale)
     return dict(x=wl.x.to(d), W=wl.W.to(d), bias=None if wl.bias is None else wl.bias.to(d),
-                ids=wl.ids.to(d), pool=L.build_pool(wl.A, wl.B, wl.K, wl.N, d, adapter_scale=wl.adapter_scale))
+                ids=wl.ids.to(d), pool=pool)
 
 
 def rel_err(gpu, ref):
@@ -485,7 +489,7 @@ def _rebase(segs, ws_from, ws_to):
     for name in ("perm", "bucket_offsets", "seg_id", "seg_start", "seg_len", "seg_rank", "num_segments"):
         setattr(out, name, getattr(segs, name) + d)
     out.plan = ws_to.buf.data_ptr()
-    out.M, out.num_adapters = segs.M, segs.num_adapters
+    out.M, out.num_adapters, out.num_slices = segs.M, segs.num_adapters, segs.num_slices
     return out
 
 
@@ -514,3 +518,70 @@ def test_decode_call_builds_the_segment_table(static_weights):
                   path=L.LORA_PATH_TILED)
     assert L.lora_get_status(ws) == 0
     assert_close(y2, ref, what="tiled from the in-kernel table")
+
+
+# ---------------------------------------------------------------------------
+# merged output (Q|K|V, gate|up): one adapter pair per output slice
+# ---------------------------------------------------------------------------
+
+SLICED_CASES = [
+    # M, K, slices, ranks, id_mode, paths
+    (300, 256, [256, 256, 512], [16, 8, 16, 4], "uniform", (L.LORA_PATH_TILED, L.LORA_PATH_AUTO)),
+    (1100, 512, [512, 512], [32, 16, 24], "runs", (L.LORA_PATH_TILED,)),
+    (257, 320, [256, 256, 256, 256], [16, 16], "uniform", (L.LORA_PATH_TILED,)),
+    (100, 256, [256, 256, 512], [16, 8, 16, 4], "uniform", (L.LORA_PATH_SPLITK, L.LORA_PATH_TILED)),
+    (20, 512, [512, 256, 256], [16, 4, 12], "uniform", (L.LORA_PATH_STREAM, L.LORA_PATH_SPLITK, L.LORA_PATH_TILED)),
+]
+
+
+@pytest.mark.parametrize("M,K,slices,ranks,mode,paths", SLICED_CASES)
+def test_linear_sliced_every_path(M, K, slices, ranks, mode, paths):
+    wl = workloads.make_sliced(M, K, slices, ranks, seed=M + K, id_mode=mode, p_base=0.15, scale=1.25,
+                               adapter_scale=[0.5 + 0.25 * i for i in range(len(ranks))])
+    dev = to_dev(wl)
+    ref = oracle.lora_linear(wl)
+    for path in paths:
+        y, ws, status = run_linear(wl, dev, path, prebuilt=(path == L.LORA_PATH_TILED))
+        assert status == 0
+        assert_close(y, ref, what=f"sliced M{M} slices={slices} path={path}")
+
+
+def test_sliced_qkv_shape_sampled():
+    """The merged QKV shape (M=2048, K=4096, slices 4096 | 1024 | 1024), eight
+    adapters of rank 16 per slice, shuffled Zipf-like ids: sampled rows."""
+    base = workloads.make_config("qkv")
+    wl = workloads.make_sliced(base.M, base.K, [4096, 1024, 1024], [16] * 8, seed=71, ids=base.ids.clone())
+    dev = to_dev(wl)
+    y, ws, status = run_linear(wl, dev)
+    assert status == 0
+    rows = sample_rows(wl.M, per_tile=2)
+    assert_close(y[rows], oracle.lora_linear(wl, rows=rows), what="sliced qkv")
+
+
+def test_sliced_table_must_match_its_pool():
+    """A segment table built for a one-output pool is refused with a merged
+    pool of the same adapters (its chunk lists are not slice-major)."""
+    wl = workloads.make_sliced(200, 256, [256, 256], [16, 16], seed=73)
+    dev = to_dev(wl)
+    plain = L.build_pool([torch.cat(a) for a in wl.A_s], [torch.zeros(wl.N, 32, dtype=torch.bfloat16)] * 2,
+                         wl.K, wl.N, "cuda")
+    ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
+    segs = L.lora_build_segments(dev["ids"], plain, ws)
+    y = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(L.LoraError) as e:
+        L.lora_linear(dev["x"], dev["W"], dev["bias"], dev["ids"], dev["pool"], wl.scale, ws, y=y, segs=segs)
+    assert e.value.code == L.LORA_ERR_SEGMENTS
+
+
+def test_sliced_rank_not_whole_panels_is_flagged():
+    """Ranks 48 and 16 with three slices: the largest rank splits into whole
+    panels, the other does not; the builder flags it (no fault)."""
+    wl = workloads.make_custom(64, 128, 768, [48, 16], seed=74)
+    dev = to_dev(wl)
+    pool = dev["pool"]
+    pool.desc.num_slices = 3
+    for s, v in enumerate([0, 256, 512, 768]):
+        pool.desc.slice_start[s] = v
+    ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
+    L.lora_build_segments(dev["ids"], pool, ws)
+    assert L.lora_get_status(ws) & L.LORA_DEV_BAD_POOL
