@@ -48,6 +48,18 @@ CONFIG_TEXT = {
     "qkv": "merged QKV: M=2048, K=4096, N=6144, 8 adapters rank 64, Zipf(1.1) ids shuffled, 20% base-only",
     "mlp_down": "MLP down: M=8192, K=12288, N=4096, 32 adapters U{16,32,64}, Zipf(1.1) requests, 20% base-only",
 }
+# extra sweep lines beside the configurations above
+SWEEP_EXTRA = {
+    "qkv_sliced": "merged QKV with one adapter pair per slice: the qkv config's M, K and ids, output slices "
+                  "4096 | 1024 | 1024, 8 adapters of rank 16 per slice",
+}
+
+
+def make_workload(name):
+    if name == "qkv_sliced":
+        base = workloads.make_config("qkv")
+        return workloads.make_sliced(base.M, base.K, [4096, 1024, 1024], [16] * 8, seed=1237, ids=base.ids.clone())
+    return workloads.make_config(name)
 
 
 def log(*a):
@@ -60,13 +72,15 @@ def log(*a):
 
 def algorithmic_work(wl):
     """Bytes: W, x, y, bias, ids and the A_i / B_i of distinct adapters
-    present at true rank.  Flops: 2MKN + sum over LoRA tokens 2 r (K + N)."""
+    present at true rank.  Flops: 2MKN + sum over LoRA tokens 2 r (K + N);
+    with S output slices each adapter has S pairs: 2 r (S K + N)."""
     ids = wl.ids
+    S = len(wl.slices) if getattr(wl, "slices", None) else 1
     present = sorted(set(int(i) for i in ids.tolist() if 0 <= i < wl.num_adapters))
-    adapter_elems = sum(wl.ranks[i] * (wl.K + wl.N) for i in present)
+    adapter_elems = sum(wl.ranks[i] * (S * wl.K + wl.N) for i in present)
     nbytes = 2 * (wl.N * wl.K + wl.M * wl.K + wl.M * wl.N + (wl.N if wl.bias is not None else 0)
                   + adapter_elems) + 4 * wl.M
-    lora_flops = sum(2 * wl.ranks[int(i)] * (wl.K + wl.N) for i in ids.tolist() if 0 <= i < wl.num_adapters)
+    lora_flops = sum(2 * wl.ranks[int(i)] * (S * wl.K + wl.N) for i in ids.tolist() if 0 <= i < wl.num_adapters)
     flops = 2 * wl.M * wl.K * wl.N + lora_flops
     return nbytes, flops, len(present)
 
@@ -202,7 +216,10 @@ class InputSet:
         self.W = wl.W.to(device)
         self.bias = None if wl.bias is None else wl.bias.to(device)
         self.ids = wl.ids.to(device)
-        self.pool = L.build_pool(wl.A, wl.B, wl.K, wl.N, device)
+        if getattr(wl, "slices", None):
+            self.pool = L.build_pool_sliced(wl.A_s, wl.B_s, wl.K, wl.slices, device)
+        else:
+            self.pool = L.build_pool(wl.A, wl.B, wl.K, wl.N, device)
         self.y = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device=device)
         self.ws = L.Workspace(wl.M, wl.N, wl.num_adapters, device)
         self.segs = None
@@ -273,7 +290,7 @@ def run_config(name, L, device, steps, warmup, stream, sampler=None, dist_barrie
     streaming them before the previous call has finished
     (LORA_FLAG_STATIC_WEIGHTS).  compare_plain: also time both legs without
     the flag."""
-    wl = workloads.make_config(name)
+    wl = make_workload(name)
     nbytes, flops, n_present = algorithmic_work(wl)
     sets = build_sets(wl, L, device)
     ns = len(sets)
@@ -447,12 +464,13 @@ def ours(args):
         out["cpu_baseline"] = cpu_baseline(args.config)
     if not args.no_sweep and rank == 0:
         sweep = {}
-        for name in ("prefill", "qkv", "mlp_down"):
+        for name in ("prefill", "qkv", "mlp_down", "qkv_sliced"):
             if name == args.config:
                 continue
             s = run_config(name, L, device, 30 if name == "mlp_down" else 100, 5, stream, e2e=False)
             kt = s["kernel_ms"] * 1e-3
             sweep[name] = {
+                **({"workload": SWEEP_EXTRA[name]} if name in SWEEP_EXTRA else {}),
                 "M": s["wl"].M, "tokens_per_s": round(s["wl"].M / (s["ms_per_step"] * 1e-3), 1),
                 "ms_per_step": round(s["ms_per_step"], 5), "kernel_us": round(s["kernel_ms"] * 1e3, 2),
                 "kernel_tflops": round(s["flops"] / kt / 1e12, 1),
