@@ -64,7 +64,8 @@ enum {
 enum {
     LORA_DEV_BAD_ID = 1 << 0,   /* some id was < -1 or >= num_adapters (treated as -1) */
     LORA_DEV_TIMEOUT = 1 << 1,  /* a bounded wait gave up; that call's output is invalid */
-    LORA_DEV_BAD_POOL = 1 << 2  /* a rank is not a whole number of 16-wide panels per output slice */
+    LORA_DEV_BAD_POOL = 1 << 2  /* pool layout the tables cannot describe: a rank not whole panels per
+                                   output slice, or a b_offset not whole [N, 16] panels */
 };
 
 #define LORA_MAX_RANK 64        /* largest padded rank */
@@ -84,7 +85,8 @@ enum {
  *   B_i  at b_pool + b_offset[i]: rank[i]/16 column panels, panel p being the
  *        [N, 16] row-major block B_i[:, 16p : 16p+16]; element (n, j) of B_i
  *        sits at b_offset[i] + (j/16)*N*16 + n*16 + j%16 (columns >= true rank
- *        are zero).  b_offset[i] is a multiple of 16.
+ *        are zero).  b_offset[i] is a whole number of [N, 16] panels (a
+ *        multiple of 16 N), as lora_pool_layout lays them out.
  * a_pool, b_pool, a_offset, b_offset, rank: DEVICE pointers, caller-owned.
  * adapter_scale: DEVICE fp32 [num_adapters], adapter i's factor s_i on top of
  *        the call's scale (4-byte aligned), or NULL for s_i = 1 everywhere.
@@ -186,10 +188,15 @@ int lora_workspace_init(void *ws, size_t ws_bytes, lora_stream_t stream);
 
 /*
  * §2.3 / §3.2: build the segment table for one step's lora_id_map (DEVICE
- * int32 [M]) against `pool` (its ranks).  One small kernel; the result can be
- * reused by every LoRA layer of the step that shares ids and ranks, as long
- * as the same workspace is passed to those calls.  *out (HOST struct) receives
- * device pointers into ws.
+ * int32 [M]) against `pool` (its ranks).  One small kernel; *out (HOST
+ * struct) receives device pointers into ws.  The table names pool rows in
+ * rank rows and whole [N, 16] B panels, so it serves every LoRA layer of the
+ * step whose pool holds the same adapters with the same ranks, laid out alike
+ * (lora_pool_layout of the same ranks) and sliced alike, whatever the
+ * layer's K and N (N <= 65536): pass it with the same workspace, sized with
+ * lora_workspace_size for the largest N.  A table that does not fit a call
+ * (another M, workspace, adapter count, slicing or workspace layout) is
+ * refused with LORA_ERR_SEGMENTS.
  */
 int lora_build_segments(const int32_t *lora_id_map, int64_t M, const lora_pool_t *pool,
                         lora_segments_t *out, void *ws, size_t ws_bytes, lora_stream_t stream);

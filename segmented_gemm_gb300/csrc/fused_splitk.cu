@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     if (lane == 0) mbar_expect_tx(&full[s], nch * (kSkBPanel + p.T_pad * kChunk * 2));
                     __syncwarp();
                     if (lane < nch) {
-                        tma_load_2d(as + lane * kSkBPanel, &tm_b, &full[s], 0, p.dchunk_brow[g0 + lane] + r.tile * kSplitBN);
+                        tma_load_2d(as + lane * kSkBPanel, &tm_b, &full[s], 0, p.dchunk_bpanel[g0 + lane] * p.N + r.tile * kSplitBN);
                         tma_load_2d(bs + lane * p.T_pad * kChunk * 2, &tm_s, &full[s], 0, (g0 + lane) * p.T_pad);
                     }
                 }

@@ -307,9 +307,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // The runs are found once per job, one lane per chunk: lane c
             // starts a run of run_len panels at pool row run_row, else 0.
             int run_row = 0, run_len = 0;
-            // output job: the B-pool row of each of the tile's first 32
-            // chunks, one lane per chunk, loaded now for the expand steps
-            const int brow_l = (jb.kind == 1 && jb.c0 + lane < jb.c1) ? p.chunk_brow[jb.c0 + lane] : 0;
+            // output job: the first B-pool row of the [N, 16] panel of each
+            // of the tile's first 32 chunks, one lane per chunk, loaded now
+            // for the expand steps
+            const int brow_l = (jb.kind == 1 && jb.c0 + lane < jb.c1) ? p.chunk_bpanel[jb.c0 + lane] * p.N : 0;
             if (jb.kind == 0) {
                 const int c = jb.c0 + lane;
                 const bool in = c < jb.c1;
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int brow_s = __shfl_sync(0xffffffffu, brow_l, ci & 31);
                     if (lane < nc) {
                         const int c = cg + lane;
-                        const int brow = ci < 32 ? brow_s : p.chunk_brow[c];
+                        const int brow = ci < 32 ? brow_s : p.chunk_bpanel[c] * p.N;
                         for (int h = 0; h < p.s_sets; ++h)
                             tma_load_2d(wsl + (h * kPanelsPerStage + lane) * kSPanelBytes, &tm_s, &fullw[s], 0,
                                         h * p.s_set_rows + c * kBM);

@@ -65,9 +65,9 @@ struct WsLayout {
     int32_t split_tiles;      // split-K output + shrink tiles (counter slots)
     size_t counters, n_counters;
     size_t perm, offsets, seg_id, seg_start, seg_len, seg_rank, num_segments;
-    size_t hdr, tile_chunk_off, chunk_arow, chunk_brow, chunk_rng;
+    size_t hdr, tile_chunk_off, chunk_arow, chunk_bpanel, chunk_rng;
     size_t sjob_tile, sjob_c0, sjob_c1, tile_njobs;
-    size_t dchunk_arow, dchunk_brow, dchunk_adapter;
+    size_t dchunk_arow, dchunk_bpanel, dchunk_adapter;
     size_t wcnt, acc_str, acc_str_bytes;
     int32_t max_win_str;      // windows the stream schedule's sums and counters can hold (M <= 64)
     size_t s_scratch, s_scratch_bytes;
@@ -112,7 +112,7 @@ struct TcParams {
     uint16_t *s_panels;        // bf16 [sets][chunks][128][16]
     float *s_out;              // fp32 [M, s_cols] (shrink mode)
     const int32_t *perm, *offsets, *hdr;
-    const int32_t *tile_chunk_off, *chunk_arow, *chunk_brow, *chunk_rng;
+    const int32_t *tile_chunk_off, *chunk_arow, *chunk_bpanel, *chunk_rng;
     const int32_t *sjob_tile, *sjob_c0, *sjob_c1, *tile_njobs;
     int32_t *counters;
     int32_t streamk;           // split the last partial wave of output tiles along K
@@ -130,7 +130,7 @@ struct SplitParams {
     const float *adapter_scale;   // per-adapter factor on top of scale, or null (all 1)
     const uint16_t *bias;
     uint16_t *y;
-    const int32_t *ids, *hdr, *dchunk_arow, *dchunk_brow, *dchunk_adapter;
+    const int32_t *ids, *hdr, *dchunk_arow, *dchunk_bpanel, *dchunk_adapter;
     uint16_t *s_panels;        // bf16 [chunks][T_pad][16]
     float *acc_out;            // fp32 [NT][128][T_pad], zero at rest
     float *acc_shr;            // fp32 [shrink tiles][128][T_pad], zero at rest
@@ -145,9 +145,9 @@ struct SegParams {
     const int64_t *a_offset;
     const int64_t *b_offset;
     int32_t *perm, *offsets, *seg_id, *seg_start, *seg_len, *seg_rank, *num_segments;
-    int32_t *hdr, *tile_chunk_off, *chunk_arow, *chunk_brow, *chunk_rng;
+    int32_t *hdr, *tile_chunk_off, *chunk_arow, *chunk_bpanel, *chunk_rng;
     int32_t *sjob_tile, *sjob_c0, *sjob_c1, *tile_njobs;
-    int32_t *dchunk_arow, *dchunk_brow, *dchunk_adapter;
+    int32_t *dchunk_arow, *dchunk_bpanel, *dchunk_adapter;
     int32_t *counters;
     int32_t n_counters;
     int32_t num_slices;        // output slices of a merged projection (>= 1): tile chunk lists are slice-major

@@ -125,8 +125,12 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
         split_s = static_cast<size_t>(L.max_dchunks) * T * kChunk * 2;
     }
     // per token tile: the tiled schedule's S-ready and consumer counters;
-    // per split-K tile: its arrival counter
-    L.n_counters = CNT_FIXED + std::max<size_t>(2 * L.num_mtiles, L.split_tiles) + 8;
+    // per split-K tile: its arrival counter.  Sized for N >= 65536 so that
+    // the regions after it (the segment table) sit at offsets that depend
+    // on M and A only: one table then serves layers of any K and N.
+    const int NT_cnt = (std::max<int32_t>(N, 65536) + kSplitBN - 1) / kSplitBN;
+    const size_t split_cnt = static_cast<size_t>(NT_cnt) + std::max<int>(RTmax, static_cast<int>(2 * present + 2));
+    L.n_counters = CNT_FIXED + std::max<size_t>(2 * L.num_mtiles, split_cnt) + 8;
     // tiled schedule: S panels, one set per K piece of a shrink job (two for M > 128)
     const size_t tiled_s = static_cast<size_t>(L.max_chunks) * kBM * kChunk * 2 * tiled_s_sets(M);
     L.s_scratch_bytes = std::max(tiled_s, split_s);
@@ -148,14 +152,14 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
     L.hdr = take(HDR_WORDS * 4);
     L.tile_chunk_off = take((static_cast<size_t>(L.num_mtiles) * LORA_MAX_SLICES + 1) * 4);
     L.chunk_arow = take(static_cast<size_t>(L.max_chunks) * 4);
-    L.chunk_brow = take(static_cast<size_t>(L.max_chunks) * 4);
+    L.chunk_bpanel = take(static_cast<size_t>(L.max_chunks) * 4);
     L.chunk_rng = take(static_cast<size_t>(L.max_chunks) * 4);
     L.sjob_tile = take(static_cast<size_t>(L.max_sjobs) * 4);
     L.sjob_c0 = take(static_cast<size_t>(L.max_sjobs) * 4);
     L.sjob_c1 = take(static_cast<size_t>(L.max_sjobs) * 4);
     L.tile_njobs = take(static_cast<size_t>(L.num_mtiles) * 4);
     L.dchunk_arow = take(static_cast<size_t>(L.max_dchunks) * 4);
-    L.dchunk_brow = take(static_cast<size_t>(L.max_dchunks) * 4);
+    L.dchunk_bpanel = take(static_cast<size_t>(L.max_dchunks) * 4);
     L.dchunk_adapter = take(static_cast<size_t>(L.max_dchunks) * 4);
     // stream schedule: windows of 8 pool panels.  An adapter's <= 4 panels
     // span at most 2 windows, so a batch touches <= 2 * min(A, M) of them.
@@ -258,14 +262,14 @@ static void fill_seg_params(SegParams &p, const int32_t *ids, int64_t M, const l
     p.hdr = at<int32_t>(ws, L.hdr);
     p.tile_chunk_off = at<int32_t>(ws, L.tile_chunk_off);
     p.chunk_arow = at<int32_t>(ws, L.chunk_arow);
-    p.chunk_brow = at<int32_t>(ws, L.chunk_brow);
+    p.chunk_bpanel = at<int32_t>(ws, L.chunk_bpanel);
     p.chunk_rng = at<int32_t>(ws, L.chunk_rng);
     p.sjob_tile = at<int32_t>(ws, L.sjob_tile);
     p.sjob_c0 = at<int32_t>(ws, L.sjob_c0);
     p.sjob_c1 = at<int32_t>(ws, L.sjob_c1);
     p.tile_njobs = at<int32_t>(ws, L.tile_njobs);
     p.dchunk_arow = at<int32_t>(ws, L.dchunk_arow);
-    p.dchunk_brow = at<int32_t>(ws, L.dchunk_brow);
+    p.dchunk_bpanel = at<int32_t>(ws, L.dchunk_bpanel);
     p.dchunk_adapter = at<int32_t>(ws, L.dchunk_adapter);
     p.counters = at<int32_t>(ws, L.counters);
     p.n_counters = static_cast<int32_t>(L.n_counters);
@@ -295,7 +299,7 @@ static int prepare(const int32_t *ids, int64_t M, const lora_pool_t *pool, const
     if (ws_bytes < L->total_min) return LORA_ERR_WORKSPACE;
     if (segs) {
         if (segs->plan != ws || segs->M != M || segs->num_adapters != pool->num_adapters ||
-            segs->num_slices != (pool->num_slices > 1 ? pool->num_slices : 1))
+            segs->num_slices != (pool->num_slices > 1 ? pool->num_slices : 1) || segs->perm != at<int32_t>(ws, L->perm))
             return LORA_ERR_SEGMENTS;
         return LORA_OK;
     }
@@ -323,7 +327,7 @@ static void fill_tc_params(TcParams &p, const WsLayout &L, void *ws, const lora_
     p.hdr = at<int32_t>(ws, L.hdr);
     p.tile_chunk_off = at<int32_t>(ws, L.tile_chunk_off);
     p.chunk_arow = at<int32_t>(ws, L.chunk_arow);
-    p.chunk_brow = at<int32_t>(ws, L.chunk_brow);
+    p.chunk_bpanel = at<int32_t>(ws, L.chunk_bpanel);
     p.chunk_rng = at<int32_t>(ws, L.chunk_rng);
     p.sjob_tile = at<int32_t>(ws, L.sjob_tile);
     p.sjob_c0 = at<int32_t>(ws, L.sjob_c0);
@@ -442,7 +446,7 @@ static int run_splitk(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, con
     p.ids = ids;
     p.hdr = at<int32_t>(ws, L.hdr);
     p.dchunk_arow = at<int32_t>(ws, L.dchunk_arow);
-    p.dchunk_brow = at<int32_t>(ws, L.dchunk_brow);
+    p.dchunk_bpanel = at<int32_t>(ws, L.dchunk_bpanel);
     p.dchunk_adapter = at<int32_t>(ws, L.dchunk_adapter);
     p.s_panels = at<uint16_t>(ws, L.s_scratch);
     p.acc_out = at<float>(ws, L.acc_out);

@@ -123,7 +123,7 @@ struct SegBuild {
         int *wsum = bsum + nb + 1;                // [32] scan scratch
         int *s_rank = wsum + 32;                  // [A] padded ranks
         int *s_arow = s_rank + A;                 // [A] first A pool row (a_offset / K)
-        int *s_brow = s_arow + A;                 // [A] b_offset / 16
+        int *s_bpan = s_arow + A;                 // [A] b_offset / (16 N): first [N, 16] B panel
         const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
         int32_t *status = p.counters + CNT_STATUS;
 
@@ -138,7 +138,10 @@ struct SegBuild {
         for (int i = tid; i < A; i += kSegThreads) {
             s_rank[i] = p.rank[i];
             s_arow[i] = static_cast<int>(p.a_offset[i] / p.K);
-            s_brow[i] = static_cast<int>(p.b_offset[i] / kChunk);
+            // B panels are counted in whole [N, 16] panels, so that the
+            // table does not depend on N (nor on K: A rows are rank rows)
+            s_bpan[i] = static_cast<int>(p.b_offset[i] / (static_cast<int64_t>(kChunk) * p.N));
+            if (p.b_offset[i] % (static_cast<int64_t>(kChunk) * p.N) != 0) atomicOr(p.counters + CNT_STATUS, LORA_DEV_BAD_POOL);
             // a merged output needs every adapter's rank in whole 16-wide
             // panels per slice
             if (s_rank[i] % (kChunk * nsl) != 0) atomicOr(p.counters + CNT_STATUS, LORA_DEV_BAD_POOL);
@@ -241,7 +244,7 @@ struct SegBuild {
                 const int c = n + incl - nc;
                 for (int q = 0; q < nc; ++q) {
                     p.dchunk_arow[c + q] = s_arow[i] + kChunk * q;
-                    p.dchunk_brow[c + q] = s_brow[i] + q * p.N;
+                    p.dchunk_bpanel[c + q] = s_bpan[i] + q;
                     p.dchunk_adapter[c + q] = i;
                 }
                 n += __shfl_sync(0xffffffffu, incl, 31);
@@ -303,7 +306,7 @@ struct SegBuild {
                             for (int qq = 0; qq < nc; ++qq) {
                                 const int cc = c + incl - nc + qq, q = sl * nc + qq;
                                 p.chunk_arow[cc] = s_arow[i] + kChunk * q;
-                                p.chunk_brow[cc] = s_brow[i] + q * p.N;
+                                p.chunk_bpanel[cc] = s_bpan[i] + q;
                                 p.chunk_rng[cc] = pack_rng(rlo, rhi, q);
                             }
                         }
@@ -366,7 +369,7 @@ struct SegBuild {
                             const int np = s_rank[i] / kChunk / nsl;
                             for (int q = sl * np; q < (sl + 1) * np; ++q, ++c) {
                                 p.chunk_arow[c] = s_arow[i] + kChunk * q;
-                                p.chunk_brow[c] = s_brow[i] + q * p.N;
+                                p.chunk_bpanel[c] = s_bpan[i] + q;
                                 p.chunk_rng[c] = pack_rng(rlo, rhi, q);
                             }
                         }

@@ -585,3 +585,28 @@ def test_sliced_rank_not_whole_panels_is_flagged():
     ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
     L.lora_build_segments(dev["ids"], pool, ws)
     assert L.lora_get_status(ws) & L.LORA_DEV_BAD_POOL
+
+
+# ---------------------------------------------------------------------------
+# one segment table for every layer of a step (§3.2)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M", [100, 700])
+def test_one_table_serves_layers_of_other_shapes(M):
+    """The table is built once, with the first layer's pool; the other layers
+    (other K and N, the same adapters and ranks, laid out alike) reuse it on
+    the same workspace, sized for the largest N.  M=100 runs the split-K
+    schedule, M=700 the tiled one."""
+    ranks = [16, 32, 64, 16, 48]
+    g = torch.Generator().manual_seed(M)
+    ids = torch.randint(-1, len(ranks), (M,), generator=g).to(torch.int32)
+    shapes = [(512, 768), (512, 256), (768, 512), (256, 1024)]   # (K, N) per layer
+    layers = [workloads.make_custom(M, K, N, ranks, seed=M + 10 * j, ids=ids.clone()) for j, (K, N) in enumerate(shapes)]
+    devs = [to_dev(wl) for wl in layers]
+    ws = L.Workspace(M, max(N for _, N in shapes), len(ranks))
+    segs = L.lora_build_segments(devs[0]["ids"], devs[0]["pool"], ws)
+    for j, (wl, dev) in enumerate(zip(layers, devs)):
+        y = torch.full((wl.M, wl.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        L.lora_linear(dev["x"], dev["W"], dev["bias"], dev["ids"], dev["pool"], wl.scale, ws, y=y, segs=segs)
+        assert L.lora_get_status(ws) == 0
+        assert_close(y, oracle.lora_linear(wl), what=f"layer {j} K{wl.K} N{wl.N} with the shared table")
