@@ -331,6 +331,43 @@ def run_config(name, L, device, steps, warmup, stream, sampler=None, dist_barrie
     return res
 
 
+LAYER_SHAPES = (("q", 4096, 4096), ("k", 4096, 1024), ("v", 4096, 1024), ("o", 4096, 4096))
+
+
+def run_layer_step(L, device, steps, warmup, stream):
+    """Four LoRA projections of one attention block (q, k, v, o: other N,
+    the same adapters) on the prefill config's ids, as one step: either one
+    segment table built for the step and passed to all four calls, or each
+    call building its own."""
+    base = workloads.make_config("prefill")
+    layers = [workloads.make_custom(base.M, K, N, base.ranks, seed=2000 + j, ids=base.ids.clone())
+              for j, (_, K, N) in enumerate(LAYER_SHAPES)]
+    nsets = 2
+    sets = [[InputSet(wl, L, device) for wl in layers] for _ in range(nsets)]
+    wss = [L.Workspace(base.M, max(n for _, _, n in LAYER_SHAPES), base.num_adapters, device) for _ in range(nsets)]
+    flops = sum(algorithmic_work(wl)[1] for wl in layers)
+
+    def shared(i):
+        st, ws = sets[i % nsets], wss[i % nsets]
+        segs = L.lora_build_segments(st[0].ids, st[0].pool, ws)
+        for wl, s in zip(layers, st):
+            L.lora_linear(s.x, s.W, s.bias, s.ids, s.pool, wl.scale, ws, y=s.y, segs=segs)
+
+    def separate(i):
+        st, ws = sets[i % nsets], wss[i % nsets]
+        for wl, s in zip(layers, st):
+            L.lora_linear(s.x, s.W, s.bias, s.ids, s.pool, wl.scale, ws, y=s.y)
+
+    ms_shared = time_steps(shared, steps, warmup, stream) / steps
+    ms_sep = time_steps(separate, steps, warmup, stream) / steps
+    status = L.lora_get_status(wss[0])
+    return {"workload": "q, k, v, o projections (K=4096; N=4096, 1024, 1024, 4096) on the prefill config's "
+                        "ids and adapters, one step = all four",
+            "M": base.M, "tokens_per_s": round(base.M / (ms_shared * 1e-3), 1),
+            "ms_per_step": round(ms_shared, 5), "ms_per_step_table_per_call": round(ms_sep, 5),
+            "tflops": round(flops / (ms_shared * 1e-3) / 1e12, 1), "device_status": status}
+
+
 def run_e2e(wl, s, L, device, steps, warmup, stream):
     """Same metric through the public API with host buffers: every step copies
     x and lora_id_map host->device (pinned) and reads y back."""
@@ -478,6 +515,8 @@ def ours(args):
                 "hbm_gbs": round(s["bytes"] / kt / 1e9, 1), "device_status": s["status"]}
             del s
             torch.cuda.empty_cache()
+        sweep["attention_block_prefill"] = run_layer_step(L, device, 100, 5, stream)
+        torch.cuda.empty_cache()
         out["sweep"] = sweep
     if rank == 0:
         print(json.dumps(out), flush=True)
