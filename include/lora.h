@@ -52,7 +52,7 @@ enum {
     LORA_ERR_NULL = 1,          /* a required pointer is NULL */
     LORA_ERR_SHAPE = 2,         /* negative M, K or N not positive multiples of 8, too many adapters */
     LORA_ERR_ALIGN = 3,         /* a tensor base address is not 16-byte aligned (4 for adapter_scale) */
-    LORA_ERR_RANK = 4,          /* a rank outside [1, 64], or max_rank not a padded rank */
+    LORA_ERR_RANK = 4,          /* a rank outside [1, LORA_MAX_RANK], or max_rank not a padded rank */
     LORA_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than lora_workspace_size() */
     LORA_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch error, bad device) */
     LORA_ERR_UNSUPPORTED = 7,   /* device is not sm_103 / sm_100 family or similar */
@@ -68,7 +68,7 @@ enum {
                                    output slice, or a b_offset not whole [N, 16] panels */
 };
 
-#define LORA_MAX_RANK 64        /* largest padded rank */
+#define LORA_MAX_RANK 128       /* largest padded rank */
 #define LORA_RANK_ALIGN 16      /* ranks are padded to a multiple of this (§4.3) */
 #define LORA_MAX_ADAPTERS 1024  /* largest num_adapters in one pool */
 #define LORA_MAX_SLICES 4       /* most output slices of a merged projection */
@@ -161,8 +161,8 @@ typedef struct {
 
 /*
  * Host helper: rank-grouped pool layout for `num_adapters` adapters with true
- * ranks `true_rank[i]` (host array, each in [1, 64]).  Adapters are grouped by
- * padded rank (16, 32, 48, 64) in that order, keeping id order inside a
+ * ranks `true_rank[i]` (host array, each in [1, LORA_MAX_RANK]).  Adapters are
+ * grouped by padded rank (16, 32, ..., 128) in that order, keeping id order inside a
  * group.  Writes (host arrays of num_adapters entries) a_offset, b_offset,
  * rank_padded, and *a_elems / *b_elems.  Returns LORA_ERR_RANK / _SHAPE / _NULL.
  */

@@ -109,10 +109,11 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
     L.N = N;
     L.A = A;
     L.num_mtiles = static_cast<int32_t>((M + kBM - 1) / kBM);
-    L.max_chunks = 4 * (A + L.num_mtiles) + 4;
+    constexpr int kMaxPanels = LORA_MAX_RANK / kChunk;   // rank panels of one adapter
+    L.max_chunks = kMaxPanels * (A + L.num_mtiles) + kMaxPanels;
     L.max_sjobs = L.num_mtiles + L.max_chunks / kMaxShrinkChunks + 1;
     const int64_t present = std::min<int64_t>(A, M);
-    L.max_dchunks = static_cast<int32_t>(4 * present + 4);
+    L.max_dchunks = static_cast<int32_t>(kMaxPanels * present + kMaxPanels);
     const int NT = (N + kSplitBN - 1) / kSplitBN;
     const int RTmax = (L.max_dchunks + 7) / 8;
     L.split_tiles = NT + std::max<int>(RTmax, static_cast<int>(2 * present + 2));
@@ -161,10 +162,10 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
     L.dchunk_arow = take(static_cast<size_t>(L.max_dchunks) * 4);
     L.dchunk_bpanel = take(static_cast<size_t>(L.max_dchunks) * 4);
     L.dchunk_adapter = take(static_cast<size_t>(L.max_dchunks) * 4);
-    // stream schedule: windows of 8 pool panels.  An adapter's <= 4 panels
+    // stream schedule: windows of 8 pool panels.  An adapter's <= 8 panels
     // span at most 2 windows, so a batch touches <= 2 * min(A, M) of them.
     L.max_win_str = M <= kStreamMaxTokens
-                        ? static_cast<int32_t>(std::min<int64_t>((4 * A + 7) / 8, 2 * present)) : 0;
+                        ? static_cast<int32_t>(std::min<int64_t>((kMaxPanels * A + 7) / 8, 2 * present)) : 0;
     L.wcnt = take(static_cast<size_t>(std::max(L.max_win_str, 1)) * kWinCntStride * 4);
     L.acc_str_bytes = M <= kStreamMaxTokens
                           ? static_cast<size_t>(std::max(L.max_win_str, 1)) * split_tpad(M) * kSplitBN * 4 : 16;
@@ -505,15 +506,17 @@ static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, co
     const int kblocks = pool->K / kBK;
     const int64_t KU2 = (kblocks + 1) / 2;
     const int max_regions = std::min(cluster_max_regions(), 512 / T);
-    // the shrink runs and expand windows of one CTA fit its on-chip tables
-    const int64_t u_cta = (static_cast<int64_t>(L.max_win_str) * KU2 + grid - 1) / grid;
-    const int64_t runs = (u_cta + KU2 - 1) / KU2 + 1;
-    if (runs > cluster_max_runs() || runs + 1 > max_regions) return -1;
-    if ((L.max_win_str + C - 1) / C > cluster_max_win_cta()) return -1;
-    if (static_cast<int64_t>(std::max(L.max_win_str, 1)) * KU2 * grid >= (int64_t(1) << 31)) return -1;   // 32-bit slicing
     const uint64_t panels =
         pool->num_adapters ? static_cast<uint64_t>(pool->b_elems / (static_cast<int64_t>(kChunk) * pool->N)) : 1;
     if ((panels + cluster_win() - 1) / cluster_win() > 512) return -1;   // the kernel's window bitmap
+    // windows the kernel can shrink: those a batch touches, at most all of the pool's
+    const int64_t wins = std::min<int64_t>(L.max_win_str, (panels + cluster_win() - 1) / cluster_win());
+    // the shrink runs and expand windows of one CTA fit its on-chip tables
+    const int64_t u_cta = (wins * KU2 + grid - 1) / grid;
+    const int64_t runs = (u_cta + KU2 - 1) / KU2 + 1;
+    if (runs > cluster_max_runs() || runs + 1 > max_regions) return -1;
+    if ((wins + C - 1) / C > cluster_max_win_cta()) return -1;
+    if (std::max<int64_t>(wins, 1) * KU2 * grid >= (int64_t(1) << 31)) return -1;   // 32-bit slicing
     ClusterParams p;
     std::memset(&p, 0, sizeof p);
     p.M = M;
@@ -579,7 +582,7 @@ int lora_pool_layout(int32_t num_adapters, const int32_t *true_rank, int32_t K, 
     if (num_adapters > 0 && (!true_rank || !a_offset || !b_offset || !rank_padded)) return LORA_ERR_NULL;
     for (int i = 0; i < num_adapters; ++i)
         if (true_rank[i] < 1 || true_rank[i] > LORA_MAX_RANK) return LORA_ERR_RANK;
-    // rank-grouped: padded rank 16, 32, 48, 64 in that order, id order inside
+    // rank-grouped: padded rank 16, 32, ..., 128 in that order, id order inside
     std::vector<int> order(num_adapters);
     for (int i = 0; i < num_adapters; ++i) order[i] = i;
     auto rp = [&](int i) { return ((true_rank[i] + LORA_RANK_ALIGN - 1) / LORA_RANK_ALIGN) * LORA_RANK_ALIGN; };
@@ -730,7 +733,7 @@ const char *lora_status_string(int code)
     case LORA_ERR_NULL: return "a required pointer is NULL";
     case LORA_ERR_SHAPE: return "invalid shape (M < 0, K or N not a positive multiple of 8, too many adapters)";
     case LORA_ERR_ALIGN: return "a tensor base address is not 16-byte aligned";
-    case LORA_ERR_RANK: return "a rank outside [1, 64] or max_rank not a multiple of 16";
+    case LORA_ERR_RANK: return "a rank outside [1, 128] or max_rank not a multiple of 16";
     case LORA_ERR_WORKSPACE: return "workspace missing or smaller than lora_workspace_size()";
     case LORA_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
     case LORA_ERR_UNSUPPORTED: return "the current device is not an sm_103 (GB300-class) GPU";

@@ -48,7 +48,7 @@ def test_pool_layout_rank_grouped(lib):
         assert b_off[y] == b_off[x] + rpad[x] * 1024
 
 
-@pytest.mark.parametrize("ranks,K,N,code", [([0], 64, 64, L.LORA_ERR_RANK), ([65], 64, 64, L.LORA_ERR_RANK),
+@pytest.mark.parametrize("ranks,K,N,code", [([0], 64, 64, L.LORA_ERR_RANK), ([129], 64, 64, L.LORA_ERR_RANK),
                                             ([16], 60, 64, L.LORA_ERR_SHAPE),
                                             ([16], 64, 0, L.LORA_ERR_SHAPE)])
 def test_pool_layout_errors(lib, ranks, K, N, code):
@@ -119,3 +119,9 @@ def test_sliced_pool_rejected_without_gpu(lib, starts, max_rank, code):
     rc = lib.lora_linear_ex(0x7000, 4, 0x8000, None, 0xB000, ctypes.byref(pool), ctypes.c_float(1.0), None, 0x9000,
                             0xA000, 1 << 20, None, 0)
     assert rc == code
+
+
+def test_pool_layout_accepts_rank_128(lib):
+    a_off, b_off, rpad, ae, be = L.lora_pool_layout([128, 100, 16], 256, 512)
+    assert rpad == [128, 112, 16]
+    assert ae == (128 + 112 + 16) * 256 and be == (128 + 112 + 16) * 512

@@ -610,3 +610,31 @@ def test_one_table_serves_layers_of_other_shapes(M):
         L.lora_linear(dev["x"], dev["W"], dev["bias"], dev["ids"], dev["pool"], wl.scale, ws, y=y, segs=segs)
         assert L.lora_get_status(ws) == 0
         assert_close(y, oracle.lora_linear(wl), what=f"layer {j} K{wl.K} N{wl.N} with the shared table")
+
+
+# ---------------------------------------------------------------------------
+# ranks above 64 (up to 128)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,paths", [(20, (L.LORA_PATH_STREAM, L.LORA_PATH_SPLITK, L.LORA_PATH_TILED)),
+                                     (100, (L.LORA_PATH_SPLITK, L.LORA_PATH_TILED)),
+                                     (700, (L.LORA_PATH_TILED,))])
+def test_linear_ranks_up_to_128_every_path(M, paths):
+    wl = workloads.make_custom(M, 512, 640, [128, 96, 16, 80, 128, 40], seed=M + 3, id_mode="uniform", p_base=0.1)
+    dev = to_dev(wl)
+    ref = oracle.lora_linear(wl)
+    for path in paths:
+        y, ws, status = run_linear(wl, dev, path)
+        assert status == 0
+        assert_close(y, ref, what=f"ranks to 128, M{M} path={path}")
+
+
+def test_sliced_rank_64_per_slice():
+    """A merged gate|up with rank 64 per slice: stacked rank 128."""
+    wl = workloads.make_sliced(300, 256, [512, 512], [64, 32, 64], seed=77, id_mode="runs")
+    dev = to_dev(wl)
+    ref = oracle.lora_linear(wl)
+    for path in (L.LORA_PATH_TILED, L.LORA_PATH_AUTO):
+        y, ws, status = run_linear(wl, dev, path)
+        assert status == 0
+        assert_close(y, ref, what=f"sliced rank 64 path={path}")
