@@ -333,3 +333,42 @@ void oracle_lora_linear_slices_rows(const uint16_t *x, int64_t M, int64_t K,
         free(S);
     }
 }
+
+/*
+ * Mixture-of-experts layer with grouped expert GEMMs (the pages' MoE section:
+ * route the tokens to their experts, one grouped matmul over all experts,
+ * then put the rows back and sum them with the routing weights):
+ *   y[t,n] = sum_{j < topk, e = expert[t,j] valid} weight[t,j] * sum_k x[t,k] W_e[n,k]
+ * expert ids outside [0, num_experts) contribute nothing.  W holds the
+ * experts' [N, K] weights one after another.  Rows as in
+ * oracle_lora_linear_rows.
+ */
+void oracle_moe_rows(const uint16_t *x, int64_t M, int64_t K, const uint16_t *W, int64_t N, int32_t num_experts,
+                     int32_t topk, const int32_t *expert, const float *weight, const int64_t *rows, int64_t nrows,
+                     double *y)
+{
+    (void)M;
+#pragma omp parallel
+    {
+        double *xr = (double *)malloc((size_t)K * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t q = 0; q < nrows; ++q) {
+            int64_t t = rows ? rows[q] : q;
+            for (int64_t k = 0; k < K; ++k) xr[k] = bf16_to_f64(x[t * K + k]);
+            double *yr = y + q * N;
+            for (int64_t n = 0; n < N; ++n) yr[n] = 0.0;
+            for (int32_t j = 0; j < topk; ++j) {
+                int32_t e = expert[t * topk + j];
+                if (e < 0 || e >= num_experts) continue;
+                double w = (double)weight[t * topk + j];
+                const uint16_t *We = W + (int64_t)e * N * K;
+                for (int64_t n = 0; n < N; ++n) {
+                    double acc = 0.0;
+                    for (int64_t k = 0; k < K; ++k) acc += xr[k] * bf16_to_f64(We[n * K + k]);
+                    yr[n] += w * acc;
+                }
+            }
+        }
+        free(xr);
+    }
+}

@@ -61,6 +61,8 @@ def _load():
         lib.oracle_lora_linear_slices_rows.restype = None
         lib.oracle_lora_linear_slices_rows.argtypes = [p, i64, i64, p, i64, p, p, i32, p, i32, p, p, p, dbl,
                                                        p, p, i64, p]
+        lib.oracle_moe_rows.restype = None
+        lib.oracle_moe_rows.argtypes = [p, i64, i64, p, i64, i32, i32, p, p, p, i64, p]
         lib.oracle_expand_rows.restype = None
         lib.oracle_expand_rows.argtypes = [p, i64, p, i64, p, i32, p, p, dbl, p, p, i64, p]
         _lib = lib
@@ -250,3 +252,29 @@ def expand(wl, S: torch.Tensor, y_in: torch.Tensor, scale: Optional[float] = Non
                            len(wl.ranks), _ptr(rk), _ptr(b_cat), float(s), _ptr(asc), _ptr(r), nrows,
                            _ptr(y))
     return y
+
+
+def moe(x: torch.Tensor, W: torch.Tensor, expert: torch.Tensor, weight: torch.Tensor, rows=None) -> np.ndarray:
+    """fp64 mixture-of-experts output: x bf16 [M, K], W bf16 [E, N, K],
+    expert int [M, topk] (ids outside [0, E) contribute nothing), weight
+    fp32 [M, topk].  Returns [len(rows), N]."""
+    lib = _load()
+    M, K = x.shape
+    E, N, _ = W.shape
+    topk = expert.shape[1]
+    xb, Wb = _bits(x.contiguous()), _bits(W.contiguous())
+    ex = np.ascontiguousarray(expert.numpy().astype(np.int32))
+    wt = np.ascontiguousarray(weight.numpy().astype(np.float32))
+    r, nrows = _rows_arg(rows, M)
+    y = np.zeros((nrows, N), dtype=np.float64)
+    lib.oracle_moe_rows(_ptr(xb), M, K, _ptr(Wb), N, E, topk, _ptr(ex), _ptr(wt), _ptr(r), nrows, _ptr(y))
+    return y
+
+
+def moe_routing(expert: torch.Tensor, num_experts: int):
+    """The routing of the (token, slot) pairs: pair p = t * topk + j sorted
+    stably by expert (the segment build over the pairs' expert ids), and the
+    number of pairs per expert."""
+    seg = build_segments(expert.reshape(-1).numpy(), num_experts, [16] * num_experts)
+    counts = np.diff(seg["bucket_offsets"])[1:]
+    return seg["perm"], seg["bucket_offsets"], counts

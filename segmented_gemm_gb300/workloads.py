@@ -259,6 +259,37 @@ def make_sliced(M: int, K: int, slices: List[int], ranks: List[int], seed: int, 
     return base
 
 
+@dataclass
+class MoeWorkload:
+    """Inputs of a mixture-of-experts layer (CPU tensors)."""
+
+    name: str
+    M: int
+    K: int
+    N: int
+    E: int
+    topk: int
+    x: torch.Tensor          # bf16 [M, K]
+    W: torch.Tensor          # bf16 [E, N, K]: expert e's weight, nn.Linear layout
+    expert: torch.Tensor     # int32 [M, topk]: the experts of each token (distinct)
+    weight: torch.Tensor     # fp32 [M, topk]: their routing weights (softmax over the chosen)
+    seed: int = 0
+
+
+def make_moe(M: int, K: int, N: int, E: int, topk: int, seed: int, skew: float = 0.0) -> MoeWorkload:
+    """Seeded MoE inputs: x ~ N(0, 1), W ~ N(0, 0.02), router logits ~ N(0, 1)
+    plus ``skew`` * (a per-expert bias ~ N(0, 1)) so that some experts are
+    busier; each token takes its topk largest logits and a softmax over them."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    W = (torch.randn(E, N, K, generator=g) * 0.02).to(torch.bfloat16)
+    logits = torch.randn(M, E, generator=g) + skew * torch.randn(1, E, generator=g)
+    top, idx = torch.topk(logits, topk, dim=1)
+    weight = torch.softmax(top, dim=1).to(torch.float32)
+    return MoeWorkload(name=f"moe_M{M}_K{K}_N{N}_E{E}_top{topk}", M=M, K=K, N=N, E=E, topk=topk, x=x, W=W,
+                       expert=idx.to(torch.int32).contiguous(), weight=weight.contiguous(), seed=seed)
+
+
 def random_fp32(shape, seed: int, std: float = 1.0) -> torch.Tensor:
     """A seeded fp32 tensor (used as the given S input of the expand step)."""
     g = torch.Generator().manual_seed(seed)

@@ -367,3 +367,54 @@ def test_a_slice_pair_touches_only_its_columns():
 
 def f64_t(t):
     return t.to(torch.float64)
+
+
+# ---------------------------------------------------------------------------
+# mixture-of-experts layer: routing, grouped expert GEMMs, weighted finalize
+# ---------------------------------------------------------------------------
+
+def test_moe_top1_unit_weight_is_the_grouped_gemm():
+    """topk 1 with weight 1: every token's row is x W_e^T of its expert,
+    computed here one expert group at a time with a library matmul."""
+    mw = workloads.make_moe(40, 48, 24, 5, 1, seed=81)
+    mw.weight[:] = 1.0
+    y = oracle.moe(mw.x, mw.W, mw.expert, mw.weight)
+    ref = np.zeros_like(y)
+    for e in range(mw.E):
+        rows = (mw.expert[:, 0] == e).nonzero().flatten().numpy()
+        if rows.size:
+            ref[rows] = f64(mw.x)[rows] @ f64(mw.W[e]).T
+    assert _rel_close(y, ref, 1e-12)
+
+
+def test_moe_brute_force():
+    mw = workloads.make_moe(5, 6, 4, 4, 2, seed=82)
+    mw.expert[1, 1] = 9          # an invalid expert contributes nothing
+    x, W = f64(mw.x), f64(mw.W)
+    want = np.zeros((mw.M, mw.N))
+    for t in range(mw.M):
+        for j in range(mw.topk):
+            e = int(mw.expert[t, j])
+            if not 0 <= e < mw.E:
+                continue
+            for n in range(mw.N):
+                want[t, n] += float(mw.weight[t, j]) * sum(x[t, k] * W[e, n, k] for k in range(mw.K))
+    assert _rel_close(oracle.moe(mw.x, mw.W, mw.expert, mw.weight), want, 1e-12)
+
+
+def test_moe_slot_order_and_weight_linearity():
+    mw = workloads.make_moe(30, 32, 16, 6, 3, seed=83)
+    y = oracle.moe(mw.x, mw.W, mw.expert, mw.weight)
+    perm = torch.tensor([2, 0, 1])
+    y_perm = oracle.moe(mw.x, mw.W, mw.expert[:, perm].contiguous(), mw.weight[:, perm].contiguous())
+    assert _rel_close(y, y_perm, 1e-13)
+    assert _rel_close(oracle.moe(mw.x, mw.W, mw.expert, mw.weight * 2.0), 2.0 * y, 1e-13)   # exact in fp32
+
+
+def test_moe_routing_is_a_stable_sort_of_the_pairs():
+    mw = workloads.make_moe(50, 8, 8, 7, 2, seed=84, skew=2.0)
+    perm, off, counts = oracle.moe_routing(mw.expert, mw.E)
+    flat = mw.expert.reshape(-1).tolist()
+    want = sorted(range(len(flat)), key=lambda p: (flat[p] + 1 if 0 <= flat[p] < mw.E else 0, p))
+    assert perm.tolist() == want
+    assert counts.tolist() == [flat.count(e) for e in range(mw.E)]
