@@ -299,6 +299,40 @@ int lora_linear_noalloc(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, c
                         lora_stream_t stream);
 
 /*
+ * Mixture of experts (the pages' MoE section: route the tokens to their
+ * experts, one grouped matmul over all experts, then put the rows back and
+ * sum them with the routing weights).  Not a LoRA layer: the same segment
+ * builder and tiled tensor-core kernel serve it.
+ *
+ *   y[t, :] = sum_{j < topk, e = expert[t, j] in [0, E)} weight[t, j] * x[t, :] W_e^T
+ *
+ * x: DEVICE bf16 [M, K]; W: DEVICE bf16 [E, N, K] (each expert's weight in
+ * nn.Linear layout, stacked); expert: DEVICE int32 [M, topk] (ids outside
+ * [0, E) contribute nothing); weight: DEVICE fp32 [M, topk]; out: DEVICE
+ * bf16 [M * topk, N], each (token, slot) pair's expert row x[t] W_e^T in pair
+ * order (rows of invalid pairs are not written); y: DEVICE bf16 [M, N].
+ * K and N multiples of 8, 1 <= topk <= E <= LORA_MAX_ADAPTERS.  ws: DEVICE,
+ * at least lora_moe_workspace_size(M, topk, E) bytes (no zero-fill needed).
+ *   lora_moe_route:    the stable sort of the pairs by expert (segment
+ *                      table over the pairs) and the padded expert order
+ *   lora_moe_gemm:     the grouped GEMM over the routed pairs (needs the
+ *                      routing of the same expert ids in ws)
+ *   lora_moe_finalize: the weighted sum of each token's rows
+ *   lora_moe:          the three in order
+ * Errors as for the other entry points.
+ */
+size_t lora_moe_workspace_size(int64_t M, int32_t topk, int32_t num_experts);
+int lora_moe_route(const int32_t *expert, int64_t M, int32_t topk, int32_t num_experts, void *ws, size_t ws_bytes,
+                   lora_stream_t stream);
+int lora_moe_gemm(const lora_bf16_t *x, int64_t M, int32_t K, const lora_bf16_t *W, int32_t N, int32_t num_experts,
+                  int32_t topk, lora_bf16_t *out, void *ws, size_t ws_bytes, lora_stream_t stream);
+int lora_moe_finalize(const lora_bf16_t *out, const int32_t *expert, const float *weight, int64_t M, int32_t topk,
+                      int32_t num_experts, int32_t N, lora_bf16_t *y, lora_stream_t stream);
+int lora_moe(const lora_bf16_t *x, int64_t M, int32_t K, const lora_bf16_t *W, int32_t N, const int32_t *expert,
+             const float *weight, int32_t num_experts, int32_t topk, lora_bf16_t *out, lora_bf16_t *y, void *ws,
+             size_t ws_bytes, lora_stream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the device status word of ws
  * into *status (a bitwise OR of LORA_DEV_* since the last read).
  */

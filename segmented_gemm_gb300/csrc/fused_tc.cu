@@ -69,7 +69,7 @@ struct Job {
 
 enum { kPartFull = 0, kPartHead = 1, kPartTail = 2 };
 
-__device__ __forceinline__ Job decode_job(int j, int n_sjobs, const TcParams &p)
+__device__ __forceinline__ Job decode_job(int j, int n_sjobs, const TcParams &p, int nmt)
 {
     Job jb;
     jb.kb0 = 0;
@@ -93,10 +93,14 @@ __device__ __forceinline__ Job decode_job(int j, int n_sjobs, const TcParams &p)
     const int per_group = p.group_m * p.num_ntiles;
     const int g = t / per_group, r = t - g * per_group;
     const int m0 = g * p.group_m;
-    const int gm = min(p.group_m, p.num_mtiles - m0);
+    const int gm = min(p.group_m, nmt - m0);
     jb.kind = 1;
     jb.m = m0 + r % gm;
     jb.n = r / gm;
+    if (p.mode == kModeMoe) {   // a plain GEMM tile: no expand steps
+        jb.c0 = jb.c1 = 0;
+        return jb;
+    }
     // the expand steps use the panels of the output slice holding tile n
     int sl = 0;
     for (int k = 1; k < p.num_slices; ++k)
@@ -119,6 +123,7 @@ __device__ __forceinline__ Job decode_job(int j, int n_sjobs, const TcParams &p)
 constexpr int kSkPieces = 4;   // CTAs per split tile, on average, at most
 
 struct SkPlan {
+    int nmt;                     // token tiles of this call (kModeMoe: the routing's count)
     int waves, rs, t0, ro, gp;   // whole waves; tail shrink jobs; first tail tile; tail tiles; CTAs sharing them
     int64_t wt;                  // K blocks of the tail tiles
     int64_t dk;                  // K blocks a CTA whose first item is a K piece of a shrink job is ahead by
@@ -170,13 +175,13 @@ __device__ __forceinline__ bool get_item(int q, int b, int G, int n_sjobs, int n
     if (q < s.waves) {
         const int j = b + q * G;
         if (j >= total) return false;
-        jb = decode_job(j, n_sjobs, p);
+        jb = decode_job(j, n_sjobs, p, s.nmt);
         return true;
     }
     const int qt = q - s.waves;
     if (b < s.rs) {   // a whole shrink job of the last wave
         if (qt > 0) return false;
-        jb = decode_job(s.waves * G + b, n_sjobs, p);
+        jb = decode_job(s.waves * G + b, n_sjobs, p, s.nmt);
         return true;
     }
     if (s.ro <= 0 || b - s.rs >= s.gp) return false;
@@ -189,7 +194,7 @@ __device__ __forceinline__ bool get_item(int q, int b, int G, int n_sjobs, int n
         f = static_cast<int64_t>(t) * KB;
     }
     if (f >= r1) return false;
-    jb = decode_job(n_sjobs + s.t0 + t, n_sjobs, p);
+    jb = decode_job(n_sjobs + s.t0 + t, n_sjobs, p, s.nmt);
     jb.kb0 = static_cast<int>(f - static_cast<int64_t>(t) * KB);
     jb.kb1 = static_cast<int>(min(r1, static_cast<int64_t>(t + 1) * KB) - static_cast<int64_t>(t) * KB);
     jb.part = jb.kb0 > 0 ? kPartTail : (jb.kb1 < KB ? kPartHead : kPartFull);
@@ -280,9 +285,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     // shrink items: every shrink job in p.shrink_split pieces along K
-    const int n_sjobs = (p.mode == kModeExpand) ? 0 : p.hdr[HDR_NSJOBS] * p.shrink_split;
-    const int n_out = (p.mode == kModeShrink) ? 0 : p.num_mtiles * p.num_ntiles;
-    const SkPlan sk = sk_plan(n_sjobs, n_out, gridDim.x, p.kblocks, p.streamk != 0, p.shrink_split);
+    const int nmt = p.mode == kModeMoe ? min(p.hdr[HDR_MOE_TILES], p.num_mtiles) : p.num_mtiles;
+    const int n_sjobs = (p.mode == kModeExpand || p.mode == kModeMoe) ? 0 : p.hdr[HDR_NSJOBS] * p.shrink_split;
+    const int n_out = (p.mode == kModeShrink) ? 0 : nmt * p.num_ntiles;
+    SkPlan sk = sk_plan(n_sjobs, n_out, gridDim.x, p.kblocks, p.streamk != 0, p.shrink_split);
+    sk.nmt = nmt;
     Job jb;
 
     if (warp == 0) {
@@ -311,6 +318,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // of the tile's first 32 chunks, one lane per chunk, loaded now
             // for the expand steps
             const int brow_l = (jb.kind == 1 && jb.c0 + lane < jb.c1) ? p.chunk_bpanel[jb.c0 + lane] * p.N : 0;
+            // kModeMoe: the tile's expert's rows of the stacked expert weights
+            const int w_row0 = (p.mode == kModeMoe && jb.kind == 1) ? p.mt_expert[jb.m] * p.N : 0;
             if (jb.kind == 0) {
                 const int c = jb.c0 + lane;
                 const bool in = c < jb.c1;
@@ -349,7 +358,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (jb.kind == 1) {
                     if (lane == 0) {
                         mbar_expect_tx(&fullw[s], kWSlot);
-                        tma_load_2d(wsl, &tm_w, &fullw[s], kb * kBK, jb.n * kBN);
+                        tma_load_2d(wsl, &tm_w, &fullw[s], kb * kBK, jb.n * kBN + w_row0);
                     }
                 } else {
                     if (lane == 0) mbar_expect_tx(&fullw[s], (jb.c1 - jb.c0) * kAPanelBytes);
@@ -418,7 +427,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int q = 0; q < 8; ++q) {
                 int64_t pp = static_cast<int64_t>(jb.m) * kBM + rb + 16 * q;
                 if (pp >= p.M) pp = p.M - 1;
-                src[q] = p.x + static_cast<int64_t>(p.perm[pp]) * p.K + chunk * 8;
+                int64_t row = p.perm[pp];
+                if (p.mode == kModeMoe) row = row >= 0 ? row / p.topk : 0;   // a pair's token; a gap reads row 0
+                src[q] = p.x + row * p.K + chunk * 8;
             }
             for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++ix) {
                 const int s = ix % kXStages;
@@ -510,7 +521,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             // the row's original token, read while the MMA still runs
             const int64_t pp = static_cast<int64_t>(jb.m) * kBM + row;
-            const bool valid = pp < p.M;
+            // kModeMoe: the output row is the pair itself (-1: a gap of the padded order)
+            const bool valid = pp < p.M && (p.mode != kModeMoe || p.perm[pp] >= 0);
             const int tok = valid ? p.perm[pp] : 0;
             const bool lora_row = p.mode != kModeExpand || pp >= p.offsets[1];
             // the LoRA scale of my row: the call's scale times its adapter's
@@ -525,7 +537,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // and each row goes out as one bulk copy, which writes whole
             // lines instead of one 32-byte piece of 32 rows per warp store
             Job nx;
-            const bool staged = p.mode == kModeLinear && jb.kind == 1 && jb.part != kPartTail &&
+            const bool staged = (p.mode == kModeLinear || p.mode == kModeMoe) && jb.kind == 1 && jb.part != kPartTail &&
                                 !get_item(q + 1, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, nx);
             mbar_wait(&acc_full[slot], use & 1, abort_flag, status, LORA_DEV_TIMEOUT);
             tc_fence_after();

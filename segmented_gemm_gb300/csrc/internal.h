@@ -44,6 +44,7 @@ enum PlanHdr {
     HDR_NSJOBS = 1,       // shrink jobs of the tiled schedule
     HDR_DCHUNKS = 2,      // chunks of the split-K schedule (adapters present)
     HDR_NSEG = 3,         // number of segments
+    HDR_MOE_TILES = 4,    // routing: 128-row tiles of the padded expert order
     HDR_WORDS = 16
 };
 
@@ -90,7 +91,9 @@ __host__ __device__ inline int rng_hi(int32_t v) { return (v >> 8) & 0xFF; }
 __host__ __device__ inline int rng_panel(int32_t v) { return (v >> 16) & 0xFF; }
 
 // ---- kernel parameter blocks ----------------------------------------------
-enum TcMode { kModeLinear = 0, kModeShrink = 1, kModeExpand = 2 };
+// kModeMoe: grouped expert GEMMs of a mixture-of-experts layer, over the
+// routing's padded expert order (perm = perm_pad; output rows are pairs)
+enum TcMode { kModeLinear = 0, kModeShrink = 1, kModeExpand = 2, kModeMoe = 3 };
 
 struct TcMaps {
     CUtensorMap x, w, a, b, s;
@@ -105,6 +108,8 @@ struct TcParams {
     int32_t num_slices;        // output slices (>= 1); tile_chunk_off holds [tiles][slices] + 1 offsets
     int32_t slice_start[LORA_MAX_SLICES + 1];   // first output column of each slice
     const int32_t *ids;        // lora_id_map (original token order); read when adapter_scale is set
+    int32_t topk;              // kModeMoe: pairs per token (a pair's token is pair / topk)
+    const int32_t *mt_expert;  // kModeMoe: the expert of each 128-row tile of the padded order
     const float *adapter_scale;   // per-adapter factor on top of scale, or null (all 1)
     const uint16_t *bias;      // bf16 [N] or null
     const uint16_t *x;         // bf16 [M, K] (rows gathered by the loader warps)
@@ -151,6 +156,12 @@ struct SegParams {
     int32_t *counters;
     int32_t n_counters;
     int32_t num_slices;        // output slices of a merged projection (>= 1): tile chunk lists are slice-major
+    // routing mode (mixture of experts): ids are the (token, slot) pairs'
+    // experts, no pool; besides perm, every expert's pairs are laid out from
+    // a fresh 128-row tile in perm_pad (-1 in the gaps), tile m holding
+    // expert mt_expert[m]
+    int32_t moe, max_mtiles;
+    int32_t *perm_pad, *mt_expert;
 };
 
 struct ClusterMaps {
@@ -183,6 +194,8 @@ struct ClusterParams {
 // ---- launchers (enqueue only; return the launch status) --------------------
 cudaError_t launch_seg_build(const SegParams &p, bool pdl, cudaStream_t stream);
 cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cudaStream_t stream);
+cudaError_t launch_moe_finalize(const uint16_t *out, const int32_t *expert, const float *weight, int64_t M, int topk,
+                                int E, int N, uint16_t *y, cudaStream_t stream);
 cudaError_t launch_s_prep(const float *S, int32_t s_cols, float scale, const TcParams &p, cudaStream_t stream);
 cudaError_t launch_splitk(const TcMaps &maps, const SplitParams &p, int grid, cudaStream_t stream);
 int splitk_stages(int T_pad);

@@ -275,6 +275,10 @@ static void fill_seg_params(SegParams &p, const int32_t *ids, int64_t M, const l
     p.counters = at<int32_t>(ws, L.counters);
     p.n_counters = static_cast<int32_t>(L.n_counters);
     p.num_slices = pool->num_slices > 1 ? pool->num_slices : 1;
+    p.moe = 0;
+    p.max_mtiles = 0;
+    p.perm_pad = nullptr;
+    p.mt_expert = nullptr;
 }
 
 static int enqueue_segments(const int32_t *ids, int64_t M, const lora_pool_t *pool, const WsLayout &L, void *ws,
@@ -571,7 +575,174 @@ static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, co
 
 using namespace lora;
 
+// ---- mixture of experts ----------------------------------------------------
+// Workspace of the routing and the grouped GEMM: the status / counter block,
+// the routing's perm, bucket offsets and segment table over the M * topk
+// (token, slot) pairs, then the padded expert order (each expert's pairs
+// from a fresh 128-row tile, -1 in the gaps) and each tile's expert.
+struct MoeLayout {
+    int64_t P;                 // pairs
+    int32_t E, max_mtiles;
+    size_t counters, n_counters, perm, offsets, seg_id, seg_start, seg_len, seg_rank, num_segments, hdr;
+    size_t perm_pad, mt_expert, total;
+};
+
+static MoeLayout make_moe_layout(int64_t M, int32_t topk, int32_t E)
+{
+    MoeLayout L;
+    std::memset(&L, 0, sizeof L);
+    L.P = M * topk;
+    L.E = E;
+    L.max_mtiles = static_cast<int32_t>((L.P + kBM - 1) / kBM + E);
+    L.n_counters = CNT_FIXED + 8;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align256(o + bytes);
+        return at;
+    };
+    L.counters = take(L.n_counters * 4);
+    L.perm = take(static_cast<size_t>(std::max<int64_t>(L.P, 1)) * 4);
+    L.offsets = take(static_cast<size_t>(E + 2) * 4);
+    L.seg_id = take(static_cast<size_t>(std::max(E, 1)) * 4);
+    L.seg_start = take(static_cast<size_t>(std::max(E, 1)) * 4);
+    L.seg_len = take(static_cast<size_t>(std::max(E, 1)) * 4);
+    L.seg_rank = take(static_cast<size_t>(std::max(E, 1)) * 4);
+    L.num_segments = take(4);
+    L.hdr = take(HDR_WORDS * 4);
+    L.perm_pad = take(static_cast<size_t>(L.max_mtiles) * kBM * 4);
+    L.mt_expert = take(static_cast<size_t>(L.max_mtiles) * 4);
+    L.total = o;
+    return L;
+}
+
+static int check_moe(int64_t M, int32_t K, int32_t N, int32_t E, int32_t topk)
+{
+    if (M < 0 || K <= 0 || N <= 0 || (K % 8) || (N % 8)) return LORA_ERR_SHAPE;
+    if (E <= 0 || E > LORA_MAX_ADAPTERS || topk <= 0 || topk > E) return LORA_ERR_SHAPE;
+    if (M * topk > (int64_t(1) << 31) - 2 * kBM * static_cast<int64_t>(E)) return LORA_ERR_SHAPE;
+    if (static_cast<int64_t>(E) * N >= (int64_t(1) << 31)) return LORA_ERR_SHAPE;   // stacked weight rows
+    return LORA_OK;
+}
+
 extern "C" {
+
+size_t lora_moe_workspace_size(int64_t M, int32_t topk, int32_t num_experts)
+{
+    if (M < 0 || topk <= 0 || num_experts <= 0) return 0;
+    return make_moe_layout(M, topk, num_experts).total;
+}
+
+int lora_moe_route(const int32_t *expert, int64_t M, int32_t topk, int32_t num_experts, void *ws, size_t ws_bytes,
+                   lora_stream_t stream)
+{
+    int rc = check_moe(M, 8, 8, num_experts, topk);
+    if (rc) return rc;
+    if (M == 0) return LORA_OK;
+    if (!expert) return LORA_ERR_NULL;
+    const MoeLayout L = make_moe_layout(M, topk, num_experts);
+    if (!ws || ws_bytes < L.total) return LORA_ERR_WORKSPACE;
+    if (!device_supported()) return LORA_ERR_UNSUPPORTED;
+    SegParams p;
+    std::memset(&p, 0, sizeof p);
+    p.ids = expert;
+    p.M = L.P;
+    p.A = num_experts;
+    p.K = 8;
+    p.N = 8;
+    p.perm = at<int32_t>(ws, L.perm);
+    p.offsets = at<int32_t>(ws, L.offsets);
+    p.seg_id = at<int32_t>(ws, L.seg_id);
+    p.seg_start = at<int32_t>(ws, L.seg_start);
+    p.seg_len = at<int32_t>(ws, L.seg_len);
+    p.seg_rank = at<int32_t>(ws, L.seg_rank);
+    p.num_segments = at<int32_t>(ws, L.num_segments);
+    p.hdr = at<int32_t>(ws, L.hdr);
+    p.counters = at<int32_t>(ws, L.counters);
+    p.n_counters = static_cast<int32_t>(L.n_counters);
+    p.num_slices = 1;
+    p.moe = 1;
+    p.max_mtiles = L.max_mtiles;
+    p.perm_pad = at<int32_t>(ws, L.perm_pad);
+    p.mt_expert = at<int32_t>(ws, L.mt_expert);
+    return launch_seg_build(p, false, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
+int lora_moe_gemm(const lora_bf16_t *x, int64_t M, int32_t K, const lora_bf16_t *W, int32_t N, int32_t num_experts,
+                  int32_t topk, lora_bf16_t *out, void *ws, size_t ws_bytes, lora_stream_t stream)
+{
+    int rc = check_moe(M, K, N, num_experts, topk);
+    if (rc) return rc;
+    if (M == 0) return LORA_OK;
+    if (!x || !W || !out) return LORA_ERR_NULL;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(out)) return LORA_ERR_ALIGN;
+    const MoeLayout L = make_moe_layout(M, topk, num_experts);
+    if (!ws || ws_bytes < L.total) return LORA_ERR_WORKSPACE;
+    if (!device_supported()) return LORA_ERR_UNSUPPORTED;
+    TcParams p;
+    std::memset(&p, 0, sizeof p);
+    p.M = static_cast<int64_t>(L.max_mtiles) * kBM;   // positions of the padded order
+    p.N = N;
+    p.K = K;
+    p.kblocks = (K + kBK - 1) / kBK;
+    p.num_mtiles = L.max_mtiles;                      // an upper bound: the kernel reads the routing's count
+    p.num_ntiles = (N + kBN - 1) / kBN;
+    p.group_m = 8;
+    p.mode = kModeMoe;
+    p.scale = 1.f;
+    p.num_slices = 1;
+    p.topk = topk;
+    p.x = x;
+    p.y = out;
+    p.perm = at<int32_t>(ws, L.perm_pad);
+    p.hdr = at<int32_t>(ws, L.hdr);
+    p.counters = at<int32_t>(ws, L.counters);
+    p.mt_expert = at<int32_t>(ws, L.mt_expert);
+    p.shrink_split = 1;
+    p.s_sets = 1;
+    TcMaps m;
+    const uint64_t Kq = K;
+    if (!encode_2d(&m.x, x, Kq, static_cast<uint64_t>(M), Kq * 2, kBK, 1, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ERR_CUDA;
+    // the experts' weights stacked: [E * N, K]
+    if (!encode_2d(&m.w, W, Kq, static_cast<uint64_t>(num_experts) * N, Kq * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return LORA_ERR_CUDA;
+    lora_pool_t none;
+    std::memset(&none, 0, sizeof none);
+    none.K = K;
+    none.N = N;
+    if (!encode_pool_maps(m, &none, W, kBN)) return LORA_ERR_CUDA;
+    if (!encode_2d(&m.s, W, kChunk, 1, kChunk * 2, kChunk, kBM, CU_TENSOR_MAP_SWIZZLE_32B)) return LORA_ERR_CUDA;
+    return launch_tc(m, p, num_sms_current_device(), static_cast<cudaStream_t>(stream)) == cudaSuccess ? LORA_OK
+                                                                                                       : LORA_ERR_CUDA;
+}
+
+int lora_moe_finalize(const lora_bf16_t *out, const int32_t *expert, const float *weight, int64_t M, int32_t topk,
+                      int32_t num_experts, int32_t N, lora_bf16_t *y, lora_stream_t stream)
+{
+    int rc = check_moe(M, 8, N, num_experts, topk);
+    if (rc) return rc;
+    if (M == 0) return LORA_OK;
+    if (!out || !expert || !weight || !y) return LORA_ERR_NULL;
+    if (!aligned16(out) || !aligned16(y)) return LORA_ERR_ALIGN;
+    if (!device_supported()) return LORA_ERR_UNSUPPORTED;
+    return launch_moe_finalize(out, expert, weight, M, topk, num_experts, N, y, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? LORA_OK
+               : LORA_ERR_CUDA;
+}
+
+int lora_moe(const lora_bf16_t *x, int64_t M, int32_t K, const lora_bf16_t *W, int32_t N, const int32_t *expert,
+             const float *weight, int32_t num_experts, int32_t topk, lora_bf16_t *out, lora_bf16_t *y, void *ws,
+             size_t ws_bytes, lora_stream_t stream)
+{
+    int rc = check_moe(M, K, N, num_experts, topk);
+    if (rc) return rc;
+    if (M == 0) return LORA_OK;
+    if (!x || !W || !out || !y || !expert || !weight) return LORA_ERR_NULL;
+    if ((rc = lora_moe_route(expert, M, topk, num_experts, ws, ws_bytes, stream))) return rc;
+    if ((rc = lora_moe_gemm(x, M, K, W, N, num_experts, topk, out, ws, ws_bytes, stream))) return rc;
+    return lora_moe_finalize(out, expert, weight, M, topk, num_experts, N, y, stream);
+}
 
 int lora_pool_layout(int32_t num_adapters, const int32_t *true_rank, int32_t K, int32_t N, int64_t *a_offset,
                      int64_t *b_offset, int32_t *rank_padded, int64_t *a_elems, int64_t *b_elems)

@@ -30,7 +30,8 @@ LORA_MAX_RANK, LORA_RANK_ALIGN, LORA_MAX_ADAPTERS = 64, 16, 1024
 
 EXPORTS = ("lora_pool_layout", "lora_workspace_size", "lora_workspace_init", "lora_build_segments",
            "lora_shrink", "lora_expand", "lora_linear", "lora_linear_ex", "lora_get_status",
-           "lora_status_string", "lora_linear_noalloc")
+           "lora_status_string", "lora_linear_noalloc", "lora_moe_workspace_size", "lora_moe_route",
+           "lora_moe_gemm", "lora_moe_finalize", "lora_moe")
 
 
 class lora_pool_t(ctypes.Structure):
@@ -82,6 +83,11 @@ def load_library():
         "lora_get_status": (ctypes.c_int, [P, P, P]),
         "lora_linear_noalloc": (ctypes.c_int, [P, I64, P, P, P, PP, F32, P, P]),
         "lora_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "lora_moe_workspace_size": (SZ, [I64, I32, I32]),
+        "lora_moe_route": (ctypes.c_int, [P, I64, I32, I32, P, SZ, P]),
+        "lora_moe_gemm": (ctypes.c_int, [P, I64, I32, P, I32, I32, I32, P, P, SZ, P]),
+        "lora_moe_finalize": (ctypes.c_int, [P, P, P, I64, I32, I32, I32, P, P]),
+        "lora_moe": (ctypes.c_int, [P, I64, I32, P, I32, P, P, I32, I32, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -321,3 +327,60 @@ def lora_get_status(ws: Workspace, stream=None) -> int:
     v = ctypes.c_int32()
     _check(load_library().lora_get_status(ws.ptr, _stream(stream), ctypes.byref(v)), "lora_get_status")
     return v.value
+
+
+# ---------------------------------------------------------------------------
+# mixture of experts
+# ---------------------------------------------------------------------------
+
+class MoeWorkspace:
+    """Device workspace of the MoE routing and grouped GEMM (no zero-fill needed)."""
+
+    def __init__(self, M: int, topk: int, num_experts: int, device="cuda"):
+        self.nbytes = int(load_library().lora_moe_workspace_size(M, topk, num_experts))
+        self.buf = torch.empty(max(self.nbytes, 256), dtype=torch.uint8, device=device)
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.buf.data_ptr())
+
+
+def lora_moe(x: torch.Tensor, W: torch.Tensor, expert: torch.Tensor, weight: torch.Tensor, ws: MoeWorkspace,
+             out: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y = sum_j weight[:, j] * x W_{expert[:, j]}^T: routing, grouped GEMM,
+    weighted finalize.  x bf16 [M, K], W bf16 [E, N, K], expert int32
+    [M, topk], weight fp32 [M, topk]; out (the pairs' rows) and y are made
+    when not given."""
+    M, K = x.shape
+    E, N, _ = W.shape
+    topk = expert.shape[1]
+    if out is None:
+        out = torch.empty(M * topk, N, dtype=torch.bfloat16, device=x.device)
+    if y is None:
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    _check(load_library().lora_moe(_ptr(x), M, K, _ptr(W), N, _ptr(expert), _ptr(weight), E, topk, _ptr(out),
+                                   _ptr(y), ws.ptr, ws.nbytes, _stream(stream)), "lora_moe")
+    return y
+
+
+def lora_moe_route(expert: torch.Tensor, num_experts: int, ws: MoeWorkspace, stream=None):
+    M, topk = expert.shape
+    _check(load_library().lora_moe_route(_ptr(expert), M, topk, num_experts, ws.ptr, ws.nbytes, _stream(stream)),
+           "lora_moe_route")
+
+
+def moe_routing_to_host(ws: MoeWorkspace, M: int, topk: int, num_experts: int):
+    """The routing's perm over the pairs and its bucket offsets (CPU int32)."""
+    P = M * topk
+    base = ws.buf
+
+    def grab(off, n):
+        return base[off:off + 4 * n].view(torch.int32).cpu()
+
+    def align(v):
+        return (v + 255) & ~255
+    # the layout of lora_moe_workspace_size: counter block (CNT_FIXED + 8 ints), perm, offsets
+    o_counters = 0
+    o_perm = align(o_counters + (8 + 8) * 4)
+    o_offsets = align(o_perm + max(P, 1) * 4)
+    return grab(o_perm, P), grab(o_offsets, num_experts + 2)

@@ -638,3 +638,41 @@ def test_sliced_rank_64_per_slice():
         y, ws, status = run_linear(wl, dev, path)
         assert status == 0
         assert_close(y, ref, what=f"sliced rank 64 path={path}")
+
+
+# ---------------------------------------------------------------------------
+# mixture of experts: routing (bit-exact), grouped GEMM + finalize
+# ---------------------------------------------------------------------------
+
+def run_moe(mw):
+    d = "cuda"
+    x, W = mw.x.to(d), mw.W.to(d)
+    ex, wt = mw.expert.to(d), mw.weight.to(d)
+    ws = L.MoeWorkspace(mw.M, mw.topk, mw.E)
+    out = torch.full((mw.M * mw.topk, mw.N), float("nan"), dtype=torch.bfloat16, device=d)
+    y = torch.full((mw.M, mw.N), float("nan"), dtype=torch.bfloat16, device=d)
+    L.lora_moe(x, W, ex, wt, ws, out=out, y=y)
+    return y, ws
+
+
+@pytest.mark.parametrize("M,K,N,E,topk,skew", [(1, 64, 64, 4, 1, 0.0), (37, 192, 136, 5, 2, 0.0),
+                                               (300, 512, 640, 16, 4, 1.5), (1000, 256, 264, 64, 8, 3.0),
+                                               (129, 128, 512, 3, 3, 0.0)])
+def test_moe_matches_oracle(M, K, N, E, topk, skew):
+    mw = workloads.make_moe(M, K, N, E, topk, seed=M + E, skew=skew)
+    if M > 3:
+        mw.expert[2, 0] = E + 5      # an invalid expert contributes nothing
+        mw.expert[3, topk - 1] = -1
+    y, ws = run_moe(mw)
+    assert assert_close(y, oracle.moe(mw.x, mw.W, mw.expert, mw.weight), what=f"moe M{M} E{E} top{topk}") is None
+    perm, off = L.moe_routing_to_host(ws, M, topk, E)
+    want_perm, want_off, _ = oracle.moe_routing(mw.expert, E)
+    assert np.array_equal(perm.numpy(), want_perm) and np.array_equal(off.numpy(), want_off)
+
+
+def test_moe_large_sampled_rows():
+    """M=2048 tokens, 64 experts, top-8, K=2048, N=1408: sampled rows."""
+    mw = workloads.make_moe(2048, 2048, 1408, 64, 8, seed=91, skew=1.0)
+    y, ws = run_moe(mw)
+    rows = sample_rows(mw.M, per_tile=2)
+    assert_close(y[rows], oracle.moe(mw.x, mw.W, mw.expert, mw.weight, rows=rows), what="moe large")
