@@ -368,6 +368,43 @@ def run_layer_step(L, device, steps, warmup, stream):
             "tflops": round(flops / (ms_shared * 1e-3) / 1e12, 1), "device_status": status}
 
 
+def run_moe_step(L, device, steps, warmup, stream, peaks):
+    """A mixture-of-experts layer's expert GEMM: routing + grouped GEMM +
+    weighted finalize through lora_moe, and the grouped GEMM alone."""
+    cfg = dict(M=2048, K=2048, N=1536, E=64, topk=8)
+    mw = workloads.make_moe(cfg["M"], cfg["K"], cfg["N"], cfg["E"], cfg["topk"], seed=4321, skew=1.0)
+    d = device
+    sets = []
+    for j in range(2):   # two weight sets: 800 MB > 4x L2
+        W = mw.W.to(d) if j == 0 else (mw.W.to(d) * 1.0)
+        sets.append(dict(x=mw.x.to(d), W=W, ex=mw.expert.to(d), wt=mw.weight.to(d),
+                         out=torch.empty(mw.M * mw.topk, mw.N, dtype=torch.bfloat16, device=d),
+                         y=torch.empty(mw.M, mw.N, dtype=torch.bfloat16, device=d),
+                         ws=L.MoeWorkspace(mw.M, mw.topk, mw.E, d)))
+    lib = L.load_library()
+
+    def whole(i):
+        s = sets[i % 2]
+        L.lora_moe(s["x"], s["W"], s["ex"], s["wt"], s["ws"], out=s["out"], y=s["y"])
+
+    def gemm(i):
+        s = sets[i % 2]
+        L._check(lib.lora_moe_gemm(L._ptr(s["x"]), mw.M, mw.K, L._ptr(s["W"]), mw.N, mw.E, mw.topk,
+                                   L._ptr(s["out"]), s["ws"].ptr, s["ws"].nbytes, L._stream(None)), "lora_moe_gemm")
+
+    whole(0)
+    whole(1)
+    torch.cuda.synchronize()
+    ms_whole = time_steps(whole, steps, warmup, stream) / steps
+    ms_gemm = time_steps(gemm, steps, warmup, stream) / steps
+    flops = 2 * mw.M * mw.topk * mw.K * mw.N
+    return {"workload": "mixture of experts: M=2048 tokens, K=2048, N=1536, 64 experts, top-8, skewed routing; "
+                        "routing + grouped GEMM + weighted finalize",
+            "M": mw.M, "tokens_per_s": round(mw.M / (ms_whole * 1e-3), 1), "ms_per_step": round(ms_whole, 5),
+            "gemm_us": round(ms_gemm * 1e3, 2), "gemm_tflops": round(flops / (ms_gemm * 1e-3) / 1e12, 1),
+            "tensor_frac": round(flops / (ms_gemm * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
+
+
 def run_e2e(wl, s, L, device, steps, warmup, stream):
     """Same metric through the public API with host buffers: every step copies
     x and lora_id_map host->device (pinned) and reads y back."""
@@ -516,6 +553,8 @@ def ours(args):
             del s
             torch.cuda.empty_cache()
         sweep["attention_block_prefill"] = run_layer_step(L, device, 100, 5, stream)
+        torch.cuda.empty_cache()
+        sweep["moe_experts"] = run_moe_step(L, device, 100, 5, stream, peaks)
         torch.cuda.empty_cache()
         out["sweep"] = sweep
     if rank == 0:

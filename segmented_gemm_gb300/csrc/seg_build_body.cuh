@@ -57,6 +57,7 @@ struct SegBuild {
     static constexpr int kTileWarp0 = 2;                 // first warp of the tile-list group
     static constexpr int kTileWarps = kSegWarps - kTileWarp0;
     static constexpr int kTileBar = 1;                   // named barrier of the tile-list group
+    static constexpr int kIdBatch = 8;                   // ids per lane loaded ahead of the histogram / scatter steps
     static_assert(kTileWarps >= 1 && 2 * kTileWarps <= 32 && kTileWarps <= 16,
                   "tile-list scan scratch lives in the 32-int wsum");
 
@@ -165,9 +166,16 @@ struct SegBuild {
                 if (lane == __ffs(peers) - 1) whist[w * nb + b] += __popc(peers);
             }
         };
-        for (int64_t base = t_begin; base < t_end; base += 32) {
-            const int64_t t = base + lane;
-            hist_step(t, t < t_end ? p.ids[t] : 0);
+        // eight ids per lane in flight, then the steps in token order
+        for (int64_t base = t_begin; base < t_end; base += 32 * kIdBatch) {
+            int idv[kIdBatch];
+#pragma unroll
+            for (int u = 0; u < kIdBatch; ++u) {
+                const int64_t t = base + 32 * u + lane;
+                idv[u] = t < t_end ? __ldg(p.ids + t) : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < kIdBatch; ++u) hist_step(base + 32 * u + lane, idv[u]);
         }
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(status, LORA_DEV_BAD_ID);
         __syncthreads();
@@ -237,9 +245,16 @@ struct SegBuild {
             if (act && lane == __ffs(peers) - 1) whist[w * nb + b] += __popc(peers);
             __syncwarp();
         };
-        for (int64_t base = t_begin; base < t_end; base += 32) {
-            const int64_t t = base + lane;
-            scatter_step(t, t < t_end ? p.ids[t] : 0);
+        // eight ids per lane in flight, then the steps in token order
+        for (int64_t base = t_begin; base < t_end; base += 32 * kIdBatch) {
+            int idv[kIdBatch];
+#pragma unroll
+            for (int u = 0; u < kIdBatch; ++u) {
+                const int64_t t = base + 32 * u + lane;
+                idv[u] = t < t_end ? __ldg(p.ids + t) : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < kIdBatch; ++u) scatter_step(base + 32 * u + lane, idv[u]);
         }
 
         // ---- phase 3b: one list per warp (group) ---------------------------------
