@@ -331,6 +331,8 @@ def run_config(name, L, device, steps, warmup, stream, sampler=None, dist_barrie
     return res
 
 
+SWEEP_LINES = ("prefill", "qkv", "mlp_down", "qkv_sliced", "attention_block_prefill", "moe_experts")
+
 LAYER_SHAPES = (("q", 4096, 4096), ("k", 4096, 1024), ("v", 4096, 1024), ("o", 4096, 4096))
 
 
@@ -538,8 +540,9 @@ def ours(args):
         out["cpu_baseline"] = cpu_baseline(args.config)
     if not args.no_sweep and rank == 0:
         sweep = {}
+        lines = set(args.sweep.split(","))
         for name in ("prefill", "qkv", "mlp_down", "qkv_sliced"):
-            if name == args.config:
+            if name == args.config or name not in lines:
                 continue
             s = run_config(name, L, device, 30 if name == "mlp_down" else 100, 5, stream, e2e=False)
             kt = s["kernel_ms"] * 1e-3
@@ -552,10 +555,12 @@ def ours(args):
                 "hbm_gbs": round(s["bytes"] / kt / 1e9, 1), "device_status": s["status"]}
             del s
             torch.cuda.empty_cache()
-        sweep["attention_block_prefill"] = run_layer_step(L, device, 100, 5, stream)
-        torch.cuda.empty_cache()
-        sweep["moe_experts"] = run_moe_step(L, device, 100, 5, stream, peaks)
-        torch.cuda.empty_cache()
+        if "attention_block_prefill" in lines:
+            sweep["attention_block_prefill"] = run_layer_step(L, device, 100, 5, stream)
+            torch.cuda.empty_cache()
+        if "moe_experts" in lines:
+            sweep["moe_experts"] = run_moe_step(L, device, 100, 5, stream, peaks)
+            torch.cuda.empty_cache()
         out["sweep"] = sweep
     if rank == 0:
         print(json.dumps(out), flush=True)
@@ -634,6 +639,8 @@ def main():
     ap.add_argument("--config", choices=list(CONFIG_TEXT), default="decode")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--sweep", default=",".join(SWEEP_LINES),
+                    help="comma-separated sweep lines to run (default: all of %s)" % ", ".join(SWEEP_LINES))
     ap.add_argument("--max-sets", type=int, default=None,
                     help="cap the rotating input sets (for small ncu captures; the L2 note in config says so)")
     args = ap.parse_args()
