@@ -301,8 +301,9 @@ int lora_linear_noalloc(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, c
 /*
  * Mixture of experts (the pages' MoE section: route the tokens to their
  * experts, one grouped matmul over all experts, then put the rows back and
- * sum them with the routing weights).  Not a LoRA layer: the same segment
- * builder and tiled tensor-core kernel serve it.
+ * sum them with the routing weights).  Not a LoRA layer: a stable bucket sort
+ * of the pairs like the segment build (two launches over chunks of the
+ * pairs) and the tiled tensor-core kernel serve it.
  *
  *   y[t, :] = sum_{j < topk, e = expert[t, j] in [0, E)} weight[t, j] * x[t, :] W_e^T
  *
@@ -312,7 +313,9 @@ int lora_linear_noalloc(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, c
  * bf16 [M * topk, N], each (token, slot) pair's expert row x[t] W_e^T in pair
  * order (rows of invalid pairs are not written); y: DEVICE bf16 [M, N].
  * K and N multiples of 8, 1 <= topk <= E <= LORA_MAX_ADAPTERS.  ws: DEVICE,
- * at least lora_moe_workspace_size(M, topk, E) bytes (no zero-fill needed).
+ * at least lora_moe_workspace_size(M, topk, E) bytes, zero-filled once before
+ * its first use (lora_workspace_init) so that its status word starts clear;
+ * the routing resets everything else it needs on every call.
  *   lora_moe_route:    the stable sort of the pairs by expert (segment
  *                      table over the pairs) and the padded expert order
  *   lora_moe_gemm:     the grouped GEMM over the routed pairs (needs the

@@ -156,12 +156,23 @@ struct SegParams {
     int32_t *counters;
     int32_t n_counters;
     int32_t num_slices;        // output slices of a merged projection (>= 1): tile chunk lists are slice-major
-    // routing mode (mixture of experts): ids are the (token, slot) pairs'
-    // experts, no pool; besides perm, every expert's pairs are laid out from
-    // a fresh 128-row tile in perm_pad (-1 in the gaps), tile m holding
-    // expert mt_expert[m]
-    int32_t moe, max_mtiles;
-    int32_t *perm_pad, *mt_expert;
+};
+
+// Mixture-of-experts routing: the (token, slot) pairs sorted stably by
+// expert (bucket 0: invalid ids, bucket e + 1: expert e), and each expert's
+// pairs laid out from a fresh 128-row tile of the padded order.
+constexpr int kRouteMaxChunks = 256;   // pair chunks (CTAs) of the routing, at most
+struct RouteParams {
+    const int32_t *expert;     // [P] each pair's expert
+    int64_t P;                 // pairs
+    int32_t E, nb;             // experts, buckets (E + 1)
+    int32_t chunk, nchunks;    // pairs per CTA (a multiple of 256), CTAs
+    int32_t max_mtiles;        // 128-row tiles the padded order has room for
+    int32_t n_counters;
+    int32_t *cnt;              // [nchunks][nb] bucket counts of each chunk
+    int32_t *perm, *offsets, *seg_id, *seg_start, *seg_len, *seg_rank, *num_segments, *hdr, *counters;
+    int32_t *perm_pad;         // [max_mtiles * 128] pair of each padded row, -1 in the gaps
+    int32_t *mt_expert;        // [max_mtiles] expert of each tile, -1 past the last
 };
 
 struct ClusterMaps {
@@ -193,6 +204,7 @@ struct ClusterParams {
 
 // ---- launchers (enqueue only; return the launch status) --------------------
 cudaError_t launch_seg_build(const SegParams &p, bool pdl, cudaStream_t stream);
+cudaError_t launch_moe_route(const RouteParams &p, cudaStream_t stream);
 cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cudaStream_t stream);
 cudaError_t launch_moe_finalize(const uint16_t *out, const int32_t *expert, const float *weight, int64_t M, int topk,
                                 int E, int N, uint16_t *y, cudaStream_t stream);

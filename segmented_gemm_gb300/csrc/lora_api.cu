@@ -275,10 +275,6 @@ static void fill_seg_params(SegParams &p, const int32_t *ids, int64_t M, const l
     p.counters = at<int32_t>(ws, L.counters);
     p.n_counters = static_cast<int32_t>(L.n_counters);
     p.num_slices = pool->num_slices > 1 ? pool->num_slices : 1;
-    p.moe = 0;
-    p.max_mtiles = 0;
-    p.perm_pad = nullptr;
-    p.mt_expert = nullptr;
 }
 
 static int enqueue_segments(const int32_t *ids, int64_t M, const lora_pool_t *pool, const WsLayout &L, void *ws,
@@ -579,12 +575,14 @@ using namespace lora;
 // Workspace of the routing and the grouped GEMM: the status / counter block,
 // the routing's perm, bucket offsets and segment table over the M * topk
 // (token, slot) pairs, then the padded expert order (each expert's pairs
-// from a fresh 128-row tile, -1 in the gaps) and each tile's expert.
+// from a fresh 128-row tile, -1 in the gaps), each tile's expert and the
+// routing's per-chunk bucket counts.
 struct MoeLayout {
     int64_t P;                 // pairs
     int32_t E, max_mtiles;
     size_t counters, n_counters, perm, offsets, seg_id, seg_start, seg_len, seg_rank, num_segments, hdr;
-    size_t perm_pad, mt_expert, total;
+    size_t perm_pad, mt_expert, route_cnt, total;
+    int32_t chunk, nchunks;    // the routing's pairs per CTA and CTAs
 };
 
 static MoeLayout make_moe_layout(int64_t M, int32_t topk, int32_t E)
@@ -612,6 +610,12 @@ static MoeLayout make_moe_layout(int64_t M, int32_t topk, int32_t E)
     L.hdr = take(HDR_WORDS * 4);
     L.perm_pad = take(static_cast<size_t>(L.max_mtiles) * kBM * 4);
     L.mt_expert = take(static_cast<size_t>(L.max_mtiles) * 4);
+    // the routing's chunks: 1024 pairs or more per CTA (a multiple of 256),
+    // at most kRouteMaxChunks of them, and their bucket counts
+    const int64_t per = (L.P + kRouteMaxChunks - 1) / kRouteMaxChunks;
+    L.chunk = static_cast<int32_t>(std::max<int64_t>(1024, (per + 255) / 256 * 256));
+    L.nchunks = static_cast<int32_t>(std::max<int64_t>(1, (L.P + L.chunk - 1) / L.chunk));
+    L.route_cnt = take(static_cast<size_t>(L.nchunks) * (E + 1) * 4);
     L.total = o;
     return L;
 }
@@ -643,13 +647,17 @@ int lora_moe_route(const int32_t *expert, int64_t M, int32_t topk, int32_t num_e
     const MoeLayout L = make_moe_layout(M, topk, num_experts);
     if (!ws || ws_bytes < L.total) return LORA_ERR_WORKSPACE;
     if (!device_supported()) return LORA_ERR_UNSUPPORTED;
-    SegParams p;
+    RouteParams p;
     std::memset(&p, 0, sizeof p);
-    p.ids = expert;
-    p.M = L.P;
-    p.A = num_experts;
-    p.K = 8;
-    p.N = 8;
+    p.expert = expert;
+    p.P = L.P;
+    p.E = num_experts;
+    p.nb = num_experts + 1;
+    p.chunk = L.chunk;
+    p.nchunks = L.nchunks;
+    p.max_mtiles = L.max_mtiles;
+    p.n_counters = static_cast<int32_t>(L.n_counters);
+    p.cnt = at<int32_t>(ws, L.route_cnt);
     p.perm = at<int32_t>(ws, L.perm);
     p.offsets = at<int32_t>(ws, L.offsets);
     p.seg_id = at<int32_t>(ws, L.seg_id);
@@ -659,13 +667,9 @@ int lora_moe_route(const int32_t *expert, int64_t M, int32_t topk, int32_t num_e
     p.num_segments = at<int32_t>(ws, L.num_segments);
     p.hdr = at<int32_t>(ws, L.hdr);
     p.counters = at<int32_t>(ws, L.counters);
-    p.n_counters = static_cast<int32_t>(L.n_counters);
-    p.num_slices = 1;
-    p.moe = 1;
-    p.max_mtiles = L.max_mtiles;
     p.perm_pad = at<int32_t>(ws, L.perm_pad);
     p.mt_expert = at<int32_t>(ws, L.mt_expert);
-    return launch_seg_build(p, false, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+    return launch_moe_route(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
 int lora_moe_gemm(const lora_bf16_t *x, int64_t M, int32_t K, const lora_bf16_t *W, int32_t N, int32_t num_experts,

@@ -125,7 +125,6 @@ struct SegBuild {
         int *s_rank = wsum + 32;                  // [A] padded ranks
         int *s_arow = s_rank + A;                 // [A] first A pool row (a_offset / K)
         int *s_bpan = s_arow + A;                 // [A] b_offset / (16 N): first [N, 16] B panel
-        int *pad_off = s_rank;                    // routing mode: [A + 2] first padded row of each bucket
         const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
         int32_t *status = p.counters + CNT_STATUS;
 
@@ -137,11 +136,7 @@ struct SegBuild {
         for (int i = tid; i < p.n_counters; i += kSegThreads)
             if (i != CNT_STATUS) p.counters[i] = 0;
         for (int i = tid; i < kSegWarps * nb; i += kSegThreads) whist[i] = 0;
-        if (p.moe) {   // routing: the padded order starts empty
-            for (int64_t i = tid; i < static_cast<int64_t>(p.max_mtiles) * kBM; i += kSegThreads) p.perm_pad[i] = -1;
-            for (int i = tid; i < p.max_mtiles; i += kSegThreads) p.mt_expert[i] = -1;
-        }
-        for (int i = tid; i < A && !p.moe; i += kSegThreads) {
+        for (int i = tid; i < A; i += kSegThreads) {
             s_rank[i] = p.rank[i];
             s_arow[i] = static_cast<int>(p.a_offset[i] / p.K);
             // B panels are counted in whole [N, 16] panels, so that the
@@ -203,27 +198,6 @@ struct SegBuild {
         if (tid == 0) bsum[nb] = carry;
         __syncthreads();
         for (int b = tid; b <= nb; b += kSegThreads) p.offsets[b] = bsum[b];
-        if (p.moe) {
-            // routing: each expert's pairs start a fresh 128-row tile of the
-            // padded order (one warp scans the experts' tile counts)
-            if (w == 0) {
-                int carry_t = 0;
-                for (int b0 = 1; b0 <= A; b0 += 32) {
-                    const int b = b0 + lane;
-                    const int tiles = b <= A ? (bsum[b + 1] - bsum[b] + kBM - 1) / kBM : 0;
-                    const int incl = warp_incl_scan(tiles, lane);
-                    const int first = carry_t + incl - tiles;
-                    if (b <= A) {
-                        pad_off[b] = first * kBM;
-                        for (int k = 0; k < tiles && first + k < p.max_mtiles; ++k) p.mt_expert[first + k] = b - 1;
-                    }
-                    carry_t += __shfl_sync(0xffffffffu, incl, 31);
-                }
-                if (lane == 0) p.hdr[HDR_MOE_TILES] = carry_t < p.max_mtiles ? carry_t : p.max_mtiles;
-            }
-            __syncthreads();
-        }
-
         // ---- phase 3a: stable scatter (every warp, its own tokens in order) ------
         auto scatter_step = [&](int64_t t, int id) {
             const bool act = t < t_end;
@@ -236,10 +210,6 @@ struct SegBuild {
                 const int below = __popc(peers & ((1u << lane) - 1u));
                 const int pos = whist[w * nb + b] + below;
                 p.perm[pos] = static_cast<int32_t>(t);
-                if (p.moe && b > 0) {
-                    const int64_t pp = pad_off[b] + (pos - bsum[b]);
-                    if (pp < static_cast<int64_t>(p.max_mtiles) * kBM) p.perm_pad[pp] = static_cast<int32_t>(t);
-                }
             }
             __syncwarp();
             if (act && lane == __ffs(peers) - 1) whist[w * nb + b] += __popc(peers);
@@ -259,31 +229,6 @@ struct SegBuild {
 
         // ---- phase 3b: one list per warp (group) ---------------------------------
         const unsigned lt_mask = (1u << lane) - 1u;
-        if (p.moe) {
-            // routing needs only the segment table (its per-expert counts):
-            // no pool, no chunk lists
-            if (w == 0) {
-                int n = 0;
-                for (int i0 = 0; i0 < A; i0 += 32) {
-                    const int i = i0 + lane;
-                    const int cnt = i < A ? bsum[i + 2] - bsum[i + 1] : 0;
-                    const unsigned m = __ballot_sync(0xffffffffu, cnt > 0);
-                    if (cnt > 0) {
-                        const int s = n + __popc(m & lt_mask);
-                        p.seg_id[s] = i;
-                        p.seg_start[s] = bsum[i + 1];
-                        p.seg_len[s] = cnt;
-                        p.seg_rank[s] = 0;
-                    }
-                    n += __popc(m);
-                }
-                if (lane == 0) {
-                    *p.num_segments = n;
-                    p.hdr[HDR_NSEG] = n;
-                }
-            }
-            return;
-        }
         if (w == 0) {
             // the segment table
             int n = 0;

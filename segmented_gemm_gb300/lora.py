@@ -334,11 +334,12 @@ def lora_get_status(ws: Workspace, stream=None) -> int:
 # ---------------------------------------------------------------------------
 
 class MoeWorkspace:
-    """Device workspace of the MoE routing and grouped GEMM (no zero-fill needed)."""
+    """Device workspace of the MoE routing and grouped GEMM, zero-filled once
+    (the status word starts clear; the routing resets the rest every call)."""
 
     def __init__(self, M: int, topk: int, num_experts: int, device="cuda"):
         self.nbytes = int(load_library().lora_moe_workspace_size(M, topk, num_experts))
-        self.buf = torch.empty(max(self.nbytes, 256), dtype=torch.uint8, device=device)
+        self.buf = torch.zeros(max(self.nbytes, 256), dtype=torch.uint8, device=device)
 
     @property
     def ptr(self):

@@ -670,6 +670,25 @@ def test_moe_matches_oracle(M, K, N, E, topk, skew):
     assert np.array_equal(perm.numpy(), want_perm) and np.array_equal(off.numpy(), want_off)
 
 
+@pytest.mark.parametrize("M,topk,E", [(40000, 8, 1024), (5000, 2, 7), (33, 8, 8)])
+def test_moe_routing_many_chunks(M, topk, E):
+    """The routing alone over many CTA chunks (320 K pairs: 250 chunks of
+    1280, so a warp's range is not a whole number of id batches), bit-exact
+    against the stable sort; ids outside [-1, E) set the device status."""
+    g = torch.Generator().manual_seed(M + E)
+    ex = torch.randint(-1, E, (M, topk), generator=g, dtype=torch.int32)
+    ex[0, 0] = E          # invalid: routed with the -1 pairs
+    ws = L.MoeWorkspace(M, topk, E)
+    L.lora_moe_route(ex.cuda(), E, ws)
+    perm, off = L.moe_routing_to_host(ws, M, topk, E)
+    want_perm, want_off, _ = oracle.moe_routing(ex, E)
+    assert np.array_equal(perm.numpy(), want_perm) and np.array_equal(off.numpy(), want_off)
+    assert L.lora_get_status(ws) & L.LORA_DEV_BAD_ID
+    ex[0, 0] = 0
+    L.lora_moe_route(ex.cuda(), E, ws)
+    assert L.lora_get_status(ws) == 0
+
+
 def test_moe_large_sampled_rows():
     """M=2048 tokens, 64 experts, top-8, K=2048, N=1408: sampled rows."""
     mw = workloads.make_moe(2048, 2048, 1408, 64, 8, seed=91, skew=1.0)
