@@ -40,8 +40,6 @@
 
 namespace lora {
 
-constexpr int kXStages = 6;                   // x ring (cp.async row gathers)
-constexpr int kWStages = 4;                   // W ring (TMA: W, A panels, S / B panels)
 constexpr int kXSlot = kBM * kBK * 2;         // 16 KB
 constexpr int kWSlot = kBN * kBK * 2;         // 32 KB
 constexpr int kSPanelBytes = kBM * kChunk * 2;   // 4 KB  (128 rows x 16)
@@ -53,10 +51,17 @@ constexpr int kTcThreads = 320;   // 10 warps: TMA, MMA, 4 epilogue, 4 x loaders
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 256;
 constexpr int kStageRow = kBN * 2 + 16;   // a staged output row: 512 bytes + 16 of padding
-constexpr size_t kTcSmemBytes =
-    kXStages * kXSlot + kWStages * kWSlot + 1024 /*align*/ + 256 /*barriers*/ + 2 * kBN * 2 /*bias of two tiles*/;
-static_assert(kWStages * kWSlot == kBM * kBN * 4, "a split tile's fp32 partials fill the W ring exactly");
-static_assert(kBM * kStageRow <= kXStages * kXSlot, "a staged bf16 output tile fits in the x ring");
+// The shared memory holds an x ring (cp.async row gathers, 16 KB slots) and
+// a W ring (TMA: W, A panels, S / B panels, 32 KB slots), split per mode:
+// the dense layer runs faster with 4 + 5 slots, the expert GEMM, whose x
+// rows are scattered pairs, with 6 + 4 (both measured on GB300).
+constexpr int kXStagesLinear = 4, kWStagesLinear = 5;
+constexpr int kXStagesMoe = 6, kWStagesMoe = 4;
+template <int kXStages, int kWStages>
+constexpr size_t tc_smem_bytes()
+{
+    return kXStages * kXSlot + kWStages * kWSlot + 1024 /*align*/ + 256 /*barriers*/ + 2 * kBN * 2 /*bias of two tiles*/;
+}
 static_assert(kSAreaBytes + kPanelsPerStage * kBPanelBytes <= kWSlot, "an expand stage fits in one W slot");
 
 struct Job {
@@ -226,6 +231,7 @@ __device__ __forceinline__ int sk_tail_count(int b, int t, const SkPlan &s, int 
     return n;
 }
 
+template <int kXStages, int kWStages>
 __global__ void __launch_bounds__(kTcThreads, 1)
     lora_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                    const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -233,6 +239,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                    const __grid_constant__ CUtensorMap tm_a48, const __grid_constant__ CUtensorMap tm_a64,
                    const TcParams p)
 {
+    static_assert(kWStages * kWSlot >= kBM * kBN * 4, "a split tile's fp32 partials fit in the W ring");
+    static_assert((2 * kXStages + 2 * kWStages + 5) * 8 + 8 <= 256, "barriers, TMEM address and abort flag fit");
+    static_assert(tc_smem_bytes<kXStages, kWStages>() <= 232448, "fits the opt-in shared memory of a CTA");
+    // the last item's bf16 output is staged in the idle x ring when it fits
+    constexpr bool kCanStage = kBM * kStageRow <= kXStages * kXSlot;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *xring = smem;                                  // kXStages x 16 KB
@@ -537,7 +548,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // and each row goes out as one bulk copy, which writes whole
             // lines instead of one 32-byte piece of 32 rows per warp store
             Job nx;
-            const bool staged = (p.mode == kModeLinear || p.mode == kModeMoe) && jb.kind == 1 && jb.part != kPartTail &&
+            const bool staged = kCanStage && (p.mode == kModeLinear || p.mode == kModeMoe) && jb.kind == 1 &&
+                                jb.part != kPartTail &&
                                 !get_item(q + 1, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, nx);
             mbar_wait(&acc_full[slot], use & 1, abort_flag, status, LORA_DEV_TIMEOUT);
             tc_fence_after();
@@ -796,20 +808,28 @@ cudaError_t launch_s_prep(const float *S, int32_t s_cols, float scale, const TcP
     return cudaGetLastError();
 }
 
-cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cudaStream_t stream)
+template <int kXStages, int kWStages>
+static cudaError_t launch_tc_split(const TcMaps &maps, const TcParams &p, int grid, cudaStream_t stream)
 {
+    constexpr size_t smem = tc_smem_bytes<kXStages, kWStages>();
     static int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(lora_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kTcSmemBytes));
+    if (dev >= 64 || !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(lora_tc_kernel<kXStages, kWStages>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        configured[dev] = 1;
+        if (dev < 64) configured[dev] = 1;
     }
-    lora_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, stream>>>(maps.x, maps.w, maps.a, maps.b, maps.s, maps.a32,
-                                                               maps.a48, maps.a64, p);
+    lora_tc_kernel<kXStages, kWStages><<<grid, kTcThreads, smem, stream>>>(maps.x, maps.w, maps.a, maps.b, maps.s,
+                                                                           maps.a32, maps.a48, maps.a64, p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cudaStream_t stream)
+{
+    if (p.mode == kModeMoe) return launch_tc_split<kXStagesMoe, kWStagesMoe>(maps, p, grid, stream);
+    return launch_tc_split<kXStagesLinear, kWStagesLinear>(maps, p, grid, stream);
 }
 
 }  // namespace lora
