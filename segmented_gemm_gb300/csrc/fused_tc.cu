@@ -119,13 +119,17 @@ __device__ __forceinline__ Job decode_job(int j, int n_sjobs, const TcParams &p,
 // CTAs take jobs b, b + G, ...  With stream-K the whole waves are taken that
 // way, and the jobs of the last partial wave are shared out: its shrink jobs
 // whole (one per CTA, first CTAs), its output tiles as equal runs of K blocks
-// over at most kSkPieces CTAs per tile.  A tile cut between CTAs has one head
+// over at most sk_pieces(KB) CTAs per tile.  A tile cut between CTAs has one head
 // piece (K block 0, last item of its CTA) and tail pieces (first items of the
 // next CTAs).  A CTA holds at most one tail piece: each tail stores its
 // partial sums in its CTA's own scratch slot and counts itself on the tile's
 // counter; the head waits for them, adds them, applies the expand steps and
 // writes y.  Nothing is added atomically, so the scratch needs no clearing.
-constexpr int kSkPieces = 4;   // CTAs per split tile, on average, at most
+// CTAs per split tile, on average, at most: pieces of about 32 K blocks or
+// more, 2 to 4 of them.  Shorter pieces cost more in the partial-sum handoff
+// than they save (measured: K = 4096 tiles run faster in 2 pieces than in 4,
+// K = 12288 tiles faster in 4 than in 2).
+__device__ __forceinline__ int sk_pieces(int KB) { return min(4, max(2, KB / 32)); }
 
 struct SkPlan {
     int nmt;                     // token tiles of this call (kModeMoe: the routing's count)
@@ -157,7 +161,7 @@ __device__ __forceinline__ SkPlan sk_plan(int n_sjobs, int n_out, int G, int KB,
     s.rs = streamk ? max(0, n_sjobs - jf) : 0;
     s.t0 = streamk ? max(0, jf - n_sjobs) : n_out;
     s.ro = streamk ? n_out - s.t0 : 0;
-    s.gp = min(G - s.rs, max(1, s.ro) * kSkPieces);
+    s.gp = min(G - s.rs, max(1, s.ro) * sk_pieces(KB));
     s.wt = static_cast<int64_t>(s.ro) * KB;
     // the shrink items (K pieces of 1 / split) are the first wave's first
     // items: those CTAs take the missing K blocks in the last wave
