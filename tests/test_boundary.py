@@ -125,3 +125,34 @@ def test_pool_layout_accepts_rank_128(lib):
     a_off, b_off, rpad, ae, be = L.lora_pool_layout([128, 100, 16], 256, 512)
     assert rpad == [128, 112, 16]
     assert ae == (128 + 112 + 16) * 256 and be == (128 + 112 + 16) * 512
+
+
+@pytest.mark.parametrize("M,topk,E", [(1, 1, 1), (37, 2, 5), (2048, 8, 64), (40000, 8, 1024)])
+def test_moe_workspace_holds_every_routing_region(lib, M, topk, E):
+    """The MoE workspace has room for what the routing and the grouped GEMM
+    write: perm over the pairs, bucket offsets, the segment table, the padded
+    expert order with each tile's expert, and the per-chunk bucket counts of
+    the routing (chunks of 1024 pairs or more, at most 256 of them)."""
+    def cdiv(a, b):
+        return -(-a // b)
+    P = M * topk
+    tiles = cdiv(P, 128) + E
+    chunk = max(1024, cdiv(cdiv(P, 256), 256) * 256)
+    nchunks = max(1, cdiv(P, chunk))
+    assert nchunks <= 256
+    need = 4 * (P + (E + 2) + 4 * E + 1 + tiles * 128 + tiles + nchunks * (E + 1))
+    size = lib.lora_moe_workspace_size(M, topk, E)
+    assert size >= need
+    assert lib.lora_moe_workspace_size(M, topk, E + 1) > size            # more experts, more room
+    assert lib.lora_moe_workspace_size(-1, topk, E) == 0
+    assert lib.lora_moe_workspace_size(M, 0, E) == 0
+
+
+def test_moe_host_errors_without_gpu(lib):
+    # shapes are checked before anything touches the device
+    assert lib.lora_moe_route(None, 4, 2, 0, None, 0, None) == L.LORA_ERR_SHAPE      # no experts
+    assert lib.lora_moe_route(None, 4, 3, 2, None, 0, None) == L.LORA_ERR_SHAPE      # topk > E
+    assert lib.lora_moe_route(None, 4, 2, 2000, None, 0, None) == L.LORA_ERR_SHAPE   # E > LORA_MAX_ADAPTERS
+    assert lib.lora_moe_route(None, 4, 2, 4, None, 0, None) == L.LORA_ERR_NULL
+    assert lib.lora_moe_route(None, 0, 2, 4, None, 0, None) == L.LORA_OK             # no tokens: nothing to do
+    assert lib.lora_moe_gemm(None, 4, 12, None, 64, 4, 2, None, None, 0, None) == L.LORA_ERR_SHAPE   # K % 8
