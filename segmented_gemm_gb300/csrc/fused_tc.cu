@@ -19,7 +19,7 @@
 // queued behind a waiting job: the grid cannot deadlock (every wait is also
 // bounded).
 //
-// Roles inside a CTA (192 threads):
+// Roles inside a CTA (320 threads):
 //   warp 0      TMA producer: W / A / B / S boxes by 2-D tiled loads
 //   warp 1      TMEM allocator and MMA issuer (one thread)
 //   warps 2..5  epilogue: tcgen05.ld -> registers -> global
@@ -28,8 +28,10 @@
 //               costs one LSU request per 16 bytes instead of one TMA
 //               instruction per four rows, which the TMA unit issues too
 //               slowly to feed the tensor core)
-// Smem: 4 stages x (16 KB x-slot + 32 KB w-slot), 128-byte swizzle for the
-// K-blocks of 64, 32-byte swizzle for the 16-wide rank panels.  TMEM: two
+// Smem: an x ring of 16 KB slots and a W ring of 32 KB slots, 224 KB in all
+// (4 + 5 slots for the dense layer, 6 + 4 for the expert GEMM), 128-byte
+// swizzle for the K-blocks of 64, 32-byte swizzle for the 16-wide rank
+// panels.  TMEM: two
 // 256-column fp32 accumulators so the epilogue of job j overlaps the
 // mainloop of job j+1.
 #include <cuda_runtime.h>
