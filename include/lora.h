@@ -299,7 +299,8 @@ int lora_linear_noalloc(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, c
                         lora_stream_t stream);
 
 /*
- * Mixture of experts (the pages' MoE section: route the tokens to their
+ * Mixture of experts (the page "Qwen3-MoE low-latency inference on Atlas A3",
+ * mokono.cn/news/2297686, its MoE section: route the tokens to their
  * experts, one grouped matmul over all experts, then put the rows back and
  * sum them with the routing weights).  Not a LoRA layer: a stable bucket sort
  * of the pairs like the segment build (two launches over chunks of the

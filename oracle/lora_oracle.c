@@ -335,7 +335,8 @@ void oracle_lora_linear_slices_rows(const uint16_t *x, int64_t M, int64_t K,
 }
 
 /*
- * Mixture-of-experts layer with grouped expert GEMMs (the pages' MoE section:
+ * Mixture-of-experts layer with grouped expert GEMMs (the page "Qwen3-MoE
+ * low-latency inference on Atlas A3", mokono.cn/news/2297686, its MoE section:
  * route the tokens to their experts, one grouped matmul over all experts,
  * then put the rows back and sum them with the routing weights):
  *   y[t,n] = sum_{j < topk, e = expert[t,j] valid} weight[t,j] * sum_k x[t,k] W_e[n,k]

@@ -1,4 +1,5 @@
-// Mixture of experts (the pages' MoE section): route the (token, slot)
+// Mixture of experts (the page "Qwen3-MoE low-latency inference on Atlas
+// A3", mokono.cn/news/2297686, its MoE section): route the (token, slot)
 // pairs to their experts, run the grouped expert matmul, then put every
 // token's rows back and sum them with the routing weights.  The grouped GEMM
 // is the tiled kernel in kModeMoe; this file holds the routing and the
