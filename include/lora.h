@@ -272,26 +272,31 @@ int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const 
 /*
  * lora_linear without a workspace, for callers that cannot allocate device
  * memory: an inference-engine hook or plugin that is handed no workspace and
- * may not call cudaMalloc while it runs, for example.  (The paper has no
- * counterpart; this is a convenience of this library.)
+ * may not call cudaMalloc while it runs, for example.  The paper this library
+ * follows (the page "vLLM-Ascend dynamic LoRA") has no counterpart to this
+ * entry point; it is a convenience of this library.
  *
  * Same arguments, layouts and result as lora_linear (segments are always
  * built internally).  The scratch is a file-scope device array of
  * LORA_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that
  * loads the library holds until the process exits; nothing is allocated or
- * freed.  A call whose schedule needs more scratch than that returns
- * LORA_ERR_CAPACITY and enqueues nothing (the tiled schedule's optional
- * split-tile scratch is used only when it fits as well).
+ * freed.  The call returns LORA_ERR_CAPACITY and enqueues nothing when the
+ * minimal workspace layout of (M, pool->N, pool->num_adapters) is larger
+ * than the array.  That minimal layout is lora_workspace_size() without the
+ * tiled schedule's optional 20 MiB split-tile scratch, which never fits: a
+ * call with M > 128 therefore runs the tiled schedule without splitting a
+ * partial last wave along K.  Every workload of up to 8192 tokens, N = 4096
+ * and 32 adapters fits (about 3 MiB).
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  All calls share the one array, which keeps the previous call's
  * contents: each call first clears (with cudaMemsetAsync on `stream`) the
- * parts that must start at zero.  Calls whose execution overlaps on the GPU
- * (other streams, other host threads) race on the array and must be avoided.
- * Device-detected problems (bad ids) are handled as in lora_linear, but the
- * status word is cleared by the next call and cannot be read through this
- * entry point.
+ * parts that must start at zero, the status word included.  Calls whose
+ * execution overlaps on the GPU (other streams, other host threads) race on
+ * the array and must be avoided.  Device-detected problems (bad ids) are
+ * handled as in lora_linear, but the status word is cleared by the next call
+ * and cannot be read through this entry point.
  */
 #define LORA_NOALLOC_SCRATCH_BYTES (8u << 20)   /* 8 MiB */
 int lora_linear_noalloc(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,

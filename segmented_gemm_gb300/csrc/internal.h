@@ -37,6 +37,7 @@ constexpr int kSplitMaxCtas = 1024;    // upper bound on the persistent grid
 constexpr int kStreamMaxTokens = 64;    // largest M served by the weight-streaming schedule
 constexpr int kWinCntStride = 32;       // ints per window counter pair (one 128-byte line)
 constexpr int kStreamKMaxTiles = 160;   // output tiles the tiled schedule may split along K in one call
+constexpr int64_t kMaxTokens = (int64_t(1) << 31) - kBM;   // largest M of one call (32-bit row indices)
 
 // plan header entries
 enum PlanHdr {
@@ -78,8 +79,11 @@ struct WsLayout {
     size_t total;
 };
 
-// Host+device: compute the layout for (M, N, A).
+// Host: compute the layout for (M, N, A); M <= kMaxTokens and
+// A <= LORA_MAX_ADAPTERS (callers check both first).
 WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A);
+// Host: validate a pool descriptor (LORA_OK or a LORA_ERR_* code).
+int check_pool(const lora_pool_t *pool);
 
 // chunk_rng packing: rows [lo, hi) of the tile, rank panel p of the segment
 __host__ __device__ inline int32_t pack_rng(int lo, int hi, int p) { return lo | (hi << 8) | (p << 16); }

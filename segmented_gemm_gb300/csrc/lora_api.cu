@@ -193,7 +193,7 @@ static T *at(void *ws, size_t off)
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-static int check_pool(const lora_pool_t *pool)
+int check_pool(const lora_pool_t *pool)
 {
     if (!pool) return LORA_ERR_NULL;
     if (pool->K <= 0 || pool->N <= 0 || (pool->K % 8) || (pool->N % 8)) return LORA_ERR_SHAPE;
@@ -293,7 +293,7 @@ static int prepare(const int32_t *ids, int64_t M, const lora_pool_t *pool, const
     int rc = check_pool(pool);
     if (rc) return rc;
     if (M < 0) return LORA_ERR_SHAPE;
-    if (M > (int64_t(1) << 31) - kBM) return LORA_ERR_SHAPE;
+    if (M > kMaxTokens) return LORA_ERR_SHAPE;
     if (!ws) return LORA_ERR_WORKSPACE;
     if (!device_supported()) return LORA_ERR_UNSUPPORTED;
     *L = make_ws_layout(M, pool->N, pool->num_adapters);
@@ -777,7 +777,7 @@ int lora_pool_layout(int32_t num_adapters, const int32_t *true_rank, int32_t K, 
 
 size_t lora_workspace_size(int64_t M, int32_t N, int32_t num_adapters)
 {
-    if (M < 0 || N <= 0 || num_adapters < 0) return 0;
+    if (M < 0 || M > kMaxTokens || N <= 0 || num_adapters < 0 || num_adapters > LORA_MAX_ADAPTERS) return 0;
     return make_ws_layout(M, N, num_adapters).total;
 }
 

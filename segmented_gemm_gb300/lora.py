@@ -26,7 +26,7 @@ LORA_DEV_BAD_ID, LORA_DEV_TIMEOUT, LORA_DEV_BAD_POOL = 1, 2, 4
 LORA_PATH_AUTO, LORA_PATH_TILED, LORA_PATH_SPLITK, LORA_PATH_STREAM = 0, 1, 2, 3
 LORA_FLAG_STATIC_WEIGHTS = 0x100
 LORA_MAX_SLICES = 4
-LORA_MAX_RANK, LORA_RANK_ALIGN, LORA_MAX_ADAPTERS = 64, 16, 1024
+LORA_MAX_RANK, LORA_RANK_ALIGN, LORA_MAX_ADAPTERS = 128, 16, 1024
 
 EXPORTS = ("lora_pool_layout", "lora_workspace_size", "lora_workspace_init", "lora_build_segments",
            "lora_shrink", "lora_expand", "lora_linear", "lora_linear_ex", "lora_get_status",

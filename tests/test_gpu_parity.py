@@ -195,12 +195,16 @@ def test_linear_no_bias_and_prebuilt_segments():
         assert_close(y, ref, what=f"no-bias path={path}")
 
 
-def test_linear_repeated_calls_reuse_workspace():
-    """Counters are left zeroed: the same workspace serves call after call."""
-    wl = workloads.make_custom(60, 256, 512, [16, 32, 64], seed=5, scale=2.0)
+@pytest.mark.parametrize("M,paths", [(60, "tiled,splitk,stream"), (96, "tiled,splitk"), (300, "tiled")])
+def test_linear_repeated_calls_reuse_workspace(M, paths):
+    """Counters are left zeroed: the same workspace serves call after call, on
+    every schedule that takes the batch size (M = 300 on the tiled schedule
+    with a full workspace, so a partial last wave is split along K)."""
+    wl = workloads.make_custom(M, 256, 512, [16, 32, 64], seed=5, scale=2.0)
     dev = to_dev(wl)
     ref = oracle.lora_linear(wl)
-    for path in (L.LORA_PATH_TILED, L.LORA_PATH_SPLITK, L.LORA_PATH_STREAM):
+    names = {"tiled": L.LORA_PATH_TILED, "splitk": L.LORA_PATH_SPLITK, "stream": L.LORA_PATH_STREAM}
+    for path in (names[n] for n in paths.split(",")):
         ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
         segs = L.lora_build_segments(dev["ids"], dev["pool"], ws)
         for _ in range(4):
