@@ -19,21 +19,25 @@
 //     adds its fp32 partial S of a window to the window's sum in L2 with
 //     atomics and releases the window's arrival counter;
 //   - expand units: one window of the B pool (8 panels x this tile's 128
-//     output rows).  The loader warps wait until the window's sum is
-//     complete, read it, keep for each token only the panels of its own
-//     adapter, scale, round to bf16 and stage it as the N operand.
+//     output rows) through the ring; the N operand is the window's S, which
+//     the loader warps stage in a small ring of their own: as soon as the
+//     window's sum is complete (early: every CTA shrinks first) they read
+//     it, keep for each token only the panels of its own adapter, scale and
+//     round it to bf16, while the weight stream goes on.
 // Order inside a CTA: the first units of its K part (issued before any
 // metadata is read, and, when the kernel follows the segment builder, before
 // the builder has finished), its shrink slice, the rest of its K part, its
 // share of the expand windows.  The last CTA to consume a window clears the
-// window's sum and counters, so they are zero again when the call ends.
+// window's sum and counters, so they are zero again when the call ends; the
+// loaders count their reads right after staging, so this also happens while
+// the weights still stream.
 // The C partial tiles are then pushed with st.async into the CTA that owns
 // each 128/C-row slice (distributed shared memory, mbarrier byte counting);
 // the owner sums them, adds the bias and writes y.
 // Roles (320 threads): warp 0 TMA producer (the weight box and the x box of
 // each unit, B windows), warp 1 TMEM allocator + MMA issuer, warps 2..5
 // epilogue (warp 2 also derives the metadata), warps 6..9 stage the S
-// operand of the expand units (load-convert-store).  All waits are bounded;
+// operand of the expand units (load-convert-store into the S ring).  All waits are bounded;
 // the host only launches the grid when every cluster can be resident at once.
 #include <cuda_runtime.h>
 
@@ -46,10 +50,11 @@ namespace lora {
 
 constexpr int kClThreads = 320;
 constexpr int kClWArea = 32 * 1024;        // one W / A / B box
-constexpr int kClMisc = 5120;              // barriers, segment list, window tables, bias
+constexpr int kClMisc = 8192;              // barriers, segment list, window tables, bias
 constexpr int kStMaxWinAll = 512;          // windows of the pool (bitmap of 16 words)
 constexpr int kStMaxWinList = 2 * kStreamMaxTokens;   // windows a batch can touch
 constexpr int kClMaxStages = 8;
+constexpr int kClMaxSRing = 4;             // S operand slots of the expand windows (one window each)
 constexpr int kStMaxSegs = 8;
 constexpr int kStMaxRegions = 16;
 constexpr int kStMaxRuns = 4;              // shrink runs (windows) of one CTA
@@ -59,11 +64,12 @@ constexpr int kBarMeta = 1;                // named barrier: metadata ready (eve
 constexpr int kBarMma = 2;                 // named barrier: metadata ready (MMA issuer + warp 2)
 constexpr int kBarLoad = 3;                // named barrier: the four loader warps
 constexpr int kBarEpi = 4;                 // named barrier: the four epilogue warps
-constexpr int kBarInit = 5;                // named barrier: ring barriers initialised (warp 0 -> loaders)
 constexpr int kBarTmem = 6;                // named barrier: TMEM allocated (warps 0..5; the loaders never read it)
-constexpr int kBarTables = 7;              // named barrier: panel tables ready (warp 2 -> producer, MMA, loaders)
+constexpr int kBarTables = 7;              // named barrier: expand windows ready (warp 2 -> producer, MMA)
 constexpr int kBarTablesEpi = 8;           // named barrier: panel tables ready (warp 2 -> the other epilogue warps)
-constexpr int kTablesThreads = kClThreads - 96;   // warp 2 + warps 0, 1, 6..9
+constexpr int kTablesThreads = 96;         // warps 0, 1, 2
+constexpr int kBarTablesLd = 9;            // named barrier: panel tables ready (warp 2 -> loaders)
+constexpr int kTablesLdThreads = 160;      // warp 2 + warps 6..9
 constexpr int kStFirst = 3;                // K units issued before the metadata is known
 constexpr int kMetaThreads = kClThreads - 32;
 
@@ -78,9 +84,10 @@ struct StSeg {
 };
 
 // the barriers and tables that follow the reduction area fit kClMisc bytes
-static_assert((2 * kClMaxStages + kStMaxRegions + 1) * 8 + 10 * 4 + kSplitBN * 2 + 64 * 4 * 2 +
+static_assert((2 * kClMaxStages + kStMaxRegions + 1 + 2 * kClMaxSRing) * 8 + 10 * 4 + kSplitBN * 2 + 64 * 4 * 2 +
                       kStMaxSegs * static_cast<int>(sizeof(StSeg)) + kStMaxWinCta * 4 * 3 + kStMaxWinCta * kStWin * 4 +
-                      kStMaxRuns * kStWin * 4 + (kStMaxWinAll / 32) * 4 * 2 + kStMaxWinList * 4 <=
+                      kStMaxRuns * kStWin * 4 + (kStMaxWinAll / 32) * 4 * 2 + kStMaxWinList * 4 +
+                      kStMaxWinCta * kStWin * 4 <=
                   kClMisc,
               "cluster kernel tables overflow their shared-memory area");
 
@@ -198,12 +205,17 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const int T = p.T_pad;
     const int slot_bytes = kClWArea + T * 256;    // [W / A / B box | token operand]
     const uint32_t unit_tx = kClWArea + T * 256;   // a base / shrink unit: weight box + x box
-    float *red = reinterpret_cast<float *>(smem + p.stages * slot_bytes);   // [C][128/C][T]
+    const int SR = p.s_ring;                      // S ring slots
+    const int sw_bytes = kStWin * T * 32;         // one window's S operand: [8 panels][T][16] bf16
+    uint8_t *sring = smem + p.stages * slot_bytes;
+    float *red = reinterpret_cast<float *>(sring + SR * sw_bytes);   // [C][128/C][T]
     uint64_t *full = reinterpret_cast<uint64_t *>(red + kSplitBN * T);
     uint64_t *empty = full + kClMaxStages;
     uint64_t *acc_full = empty + kClMaxStages;
     uint64_t *red_full = acc_full + kStMaxRegions;
-    int *ivars = reinterpret_cast<int *>(red_full + 1);
+    uint64_t *s_ready = red_full + 1;             // [kClMaxSRing] S slot staged (the 128 loader threads)
+    uint64_t *s_free = s_ready + kClMaxSRing;     // [kClMaxSRing] S slot read by its expand MMAs
+    int *ivars = reinterpret_cast<int *>(s_free + kClMaxSRing);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ivars);
     volatile int *abort_flag = ivars + 1;
     int *n_segs = ivars + 2;       // segments before the expand
@@ -218,6 +230,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     int *s_win_info = s_win_acc + kStMaxWinCta;        // [kStMaxWinCta][8] adapter of each panel, -1 if absent
     int *s_run_info = s_win_info + kStMaxWinCta * kStWin;   // [kStMaxRuns][8] the same for my shrink windows
     int *s_zero = s_run_info + kStMaxRuns * kStWin;    // [kStMaxWinCta] I am the window's last consumer
+    float *s_pan_fac = reinterpret_cast<float *>(s_zero + kStMaxWinCta);   // [kStMaxWinCta][8] owner's factor
     unsigned *s_wbits = reinterpret_cast<unsigned *>(s_zero + kStMaxWinCta);   // [16] windows touched
     int *s_wpre = reinterpret_cast<int *>(s_wbits + kStMaxWinAll / 32);       // [16] popcount prefix
     int *s_wlist = s_wpre + kStMaxWinAll / 32;         // [kStMaxWinList] windows touched, ascending
@@ -229,12 +242,16 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const int n0 = (cta / C) * kSplitBN;
     int32_t *status = p.counters + CNT_STATUS;
     const int KU2 = (p.kblocks + 1) / 2;          // K units of 2 K blocks
-    const int b0 = (KU2 * q) / C, b1 = (KU2 * (q + 1)) / C;
-    const int rpo = kSplitBN / C;                 // output rows owned by each CTA of the cluster
-    // all_windows: every window of the pool is processed, so the unit list
-    // is known at launch and the shrink goes first; otherwise warp 2 finds
-    // the windows the batch touches and the first units are base units
+    // allw: every window of the pool is shrunk and expanded, so the unit
+    // list is known at launch and the shrink goes first; otherwise warp 2
+    // finds the windows the batch touches and the first units are base units
     const bool allw = p.all_windows != 0;
+    // my base K units: an equal share of the tile's K (evening the shares
+    // out by the CTAs' shrink and expand units was measured slower: the
+    // expand windows wait on S, not on bandwidth)
+    const int b0 = (KU2 * q) / C, b1 = (KU2 * (q + 1)) / C;
+
+    const int rpo = kSplitBN / C;                 // output rows owned by each CTA of the cluster
     int nfirst;   // units issued in the prologue (no metadata needed)
     if (allw) {
         const int U = p.windows_all * KU2;
@@ -254,16 +271,24 @@ __global__ void __launch_bounds__(kClThreads, 1)
     // start while the kernels ahead of it still run: until griddepcontrol.wait
     // it touches only the weights (W, the A pool) and its own shared memory
     // and TMEM; x, the ids, the workspace and y come after the wait.
-    int id0 = -1, id1 = -1;   // warp 2: the ids of tokens lane, lane + 32 (inputs; loaded first)
-    if (warp == 2 && !p.early_weights) {
+    // the warp that builds the token tables: warp 2 when the batch decides
+    // which windows are shrunk, else loader warp 6 (the epilogue warps then
+    // need no table before the shrink runs)
+    const int meta_warp = allw ? 6 : 2;
+    int id0 = -1, id1 = -1;   // meta_warp: the ids of tokens lane, lane + 32 (inputs; loaded first)
+    if (warp == meta_warp && !p.early_weights) {
         id0 = lane < p.M ? p.ids[lane] : -2;
         id1 = lane + 32 < p.M ? p.ids[lane + 32] : -2;
     }
     if (warp == 0) {
         // one barrier per lane
         if (lane < p.stages) {
-            mbar_init(&full[lane], 1 + 128);   // producer's expect_tx arrive + one arrive per loader thread
+            mbar_init(&full[lane], 1);   // the producer's expect_tx arrive (every operand comes by TMA)
             mbar_init(&empty[lane], 1);
+        }
+        if (lane < SR) {
+            mbar_init(&s_ready[lane], 128);
+            mbar_init(&s_free[lane], 1);
         }
         if (lane < kStMaxRegions) mbar_init(&acc_full[lane], 1);
         if (lane == 0) {
@@ -273,32 +298,24 @@ __global__ void __launch_bounds__(kClThreads, 1)
         }
         fence_mbarrier_init();
         __syncwarp();
-        named_bar_arrive(kBarInit, 160);   // the loaders may arrive on the ring barriers now
         if (lane == 0) {
             if (allw) {
                 // the first units: my shrink units (window, K unit), then base
                 const int U = p.windows_all * KU2;
                 const int u0 = (U * cta) / G, u1 = (U * (cta + 1)) / G;
-                int wi = u0 / KU2, ku = u0 - wi * KU2;
-                int kbs[kClMaxStages];
                 for (int i = 0; i < nfirst; ++i) {
                     uint8_t *wa = smem + i * slot_bytes;
+                    const int u = u0 + i;
                     mbar_expect_tx(&full[i], unit_tx);
-                    if (u0 + i < u1) {
-                        kbs[i] = 2 * ku;
-                        tma_load_3d_st(wa, &tm_a3, &full[i], 0, kChunk * kStWin * wi, kbs[i]);
-                        if (++ku == KU2) {
-                            ku = 0;
-                            ++wi;
-                        }
-                    } else {
-                        kbs[i] = 2 * (b0 + (u0 + i - u1));
-                        tma_load_3d_st(wa, &tm_w3, &full[i], 0, n0, kbs[i]);
-                    }
+                    if (u < u1) tma_load_3d_st(wa, &tm_a3, &full[i], 0, kChunk * kStWin * (u / KU2), 2 * (u % KU2));
+                    else tma_load_3d_st(wa, &tm_w3, &full[i], 0, n0, 2 * (b0 + (u - u1)));
                 }
                 pdl_wait();   // x may be written by the kernel ahead of this one
-                for (int i = 0; i < nfirst; ++i)
-                    tma_load_3d_st(smem + i * slot_bytes + kClWArea, &tm_x3, &full[i], 0, 0, kbs[i]);
+                for (int i = 0; i < nfirst; ++i) {
+                    const int u = u0 + i;
+                    tma_load_3d_st(smem + i * slot_bytes + kClWArea, &tm_x3, &full[i], 0, 0,
+                                   u < u1 ? 2 * (u % KU2) : 2 * (b0 + (u - u1)));
+                }
             } else {
                 for (int i = 0; i < nfirst; ++i) {
                     mbar_expect_tx(&full[i], unit_tx);
@@ -316,14 +333,52 @@ __global__ void __launch_bounds__(kClThreads, 1)
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
-    if (warp >= 6) {   // the first units need no token-side staging
-        named_bar_sync(kBarInit, 160);
-        for (int i = 0; i < nfirst; ++i) mbar_arrive(&full[i]);
-    }
     if (warp < 6) {
         tc_fence_before();
         named_bar_sync(kBarTmem, 192);
         tc_fence_after();
+    }
+    // the bias of the rows this CTA finishes (a weight: read before the wait),
+    // held in registers until the shrink runs are released
+    uint4 bias_reg = make_uint4(0u, 0u, 0u, 0u);
+    const bool bias_thread = threadIdx.x >= 160 && threadIdx.x < 160 + rpo / 8;
+    if (bias_thread && p.bias && n0 + q * rpo + 8 * (threadIdx.x - 160) < p.N)
+        bias_reg = __ldg(reinterpret_cast<const uint4 *>(p.bias + n0 + q * rpo + 8 * (threadIdx.x - 160)));
+    if (allw && warp == meta_warp) {
+        // The owner of each pool panel of my expand windows and its factor:
+        // the pool table is a weight, so this is read before the wait.  Only
+        // the ids are left for after it.
+        const int wa0 = (p.windows_all * q) / C;
+        const int wa1 = min((p.windows_all * (q + 1)) / C, wa0 + kStMaxWinCta);
+        const int plo = kStWin * wa0, phi = kStWin * wa1;
+        for (int k = lane; k < phi - plo; k += 32) {
+            s_win_info[k] = -1;
+            s_pan_fac[k] = 1.f;
+        }
+        __syncwarp();
+        for (int i0 = 0; i0 < p.A; i0 += 8 * 32) {
+            int64_t ao[8];
+            int rk[8];
+            float fa[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {   // all loads first
+                const int i = i0 + 32 * j + lane;
+                ao[j] = i < p.A ? p.a_offset[i] : 0;
+                rk[j] = i < p.A ? p.rank[i] : 0;
+                fa[j] = i < p.A && p.adapter_scale ? p.adapter_scale[i] : 1.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = i0 + 32 * j + lane;
+                if (i >= p.A) continue;
+                const int pa = static_cast<int>(ao[j] / p.K) / kChunk, np = min(rk[j] / kChunk, LORA_MAX_RANK / kChunk);
+                for (int pp = max(pa, plo); pp < min(pa + np, phi); ++pp) {
+                    s_win_info[pp - plo] = i;
+                    s_pan_fac[pp - plo] = fa[j];
+                }
+            }
+        }
+        __syncwarp();
     }
     pdl_launch_dependents();   // a dependent launch (the segment builder) may start on an idle SM
     cluster_arrive_relaxed();  // my barriers are initialised; peers wait for this before any st.async
@@ -332,7 +387,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     // before any thread reads an input other than the weights, touches the
     // workspace or y, or starts a bounded wait
     pdl_wait();
-    if (warp == 2 && p.early_weights) {
+    if (warp == meta_warp && p.early_weights) {
         id0 = lane < p.M ? p.ids[lane] : -2;
         id1 = lane + 32 < p.M ? p.ids[lane + 32] : -2;
     }
@@ -348,10 +403,11 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 if (!*n_exp) break;
             }
             const StSeg sg = segs[si];
-            for (int u = sg.a; u < sg.b; ++u, ++it) {
-                if (it < static_cast<uint32_t>(nfirst)) continue;   // issued in the prologue
-                const int s = it % p.stages;
-                const uint32_t round = it / p.stages;
+            for (int u = sg.a; u < sg.b; ++u) {
+                const uint32_t iu = it++;
+                if (iu < static_cast<uint32_t>(nfirst)) continue;   // issued in the prologue
+                const int s = iu % p.stages;
+                const uint32_t round = iu / p.stages;
                 if (lane == 0) {
                     if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
                     uint8_t *wa = smem + s * slot_bytes;
@@ -370,91 +426,94 @@ __global__ void __launch_bounds__(kClThreads, 1)
         }
     } else if (warp >= 6) {
         // ===================== loaders: the S operand of the expand ==========
+        // Each expand window's S is staged into slot w % SR of the S ring as
+        // soon as the window's sum is complete.  Every CTA shrinks before it
+        // streams its base units, so the sums are complete long before the
+        // expand units' B boxes arrive: the staging overlaps the weight
+        // stream.  A slot is reused only after the MMAs of the window it
+        // held have read it.
         const int lt = threadIdx.x - 192;
         named_bar_sync(kBarMeta, kMetaThreads);
-        const int nk = *n_segs;
-        int ew0 = 0, ew1 = 0;   // my expand windows
-        uint32_t it = 0;
-        for (int si = 0; si <= nk; ++si) {
-            if (si == nk) {   // the expand windows, once the tables are ready
-                named_bar_sync(kBarTables, kTablesThreads);   // s_win_*, s_ids
-                if (!*n_exp) break;
-                ew0 = segs[si].a;
-                ew1 = segs[si].b;
-                // every window of my share must be complete: one lane per
-                // window waits, so the checks overlap
-                for (int k = ew0 + lane; k < ew1; k += 32)
-                    wait_flag_geq(wcnt + s_win_acc[k - ew0] * kCntStride, KU2, abort_flag, status, LORA_DEV_TIMEOUT);
-                __syncwarp();
-            }
-            const StSeg sg = segs[si];
-            for (int u = sg.a; u < sg.b; ++u, ++it) {
-                if (it < static_cast<uint32_t>(nfirst)) continue;   // arrived in the prologue
-                const int s = it % p.stages;
-                const uint32_t round = it / p.stages;
-                if (lane == 0 && round > 0) mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
-                __syncwarp();
-                uint8_t *xa = smem + s * slot_bytes + kClWArea;
-                if (sg.kind != kStExpand) {
-                    mbar_arrive(&full[s]);   // x arrives by TMA with the weight box
-                } else {
-                    // S panels [8][T rows][16], 32-byte swizzle (chunk c of
-                    // row t at t*32 + (c ^ ((t >> 2) & 1))*16); pieces of 8
-                    // ranks (panel j, token t, half c); all loads of a thread
-                    // are issued before the first conversion
-                    const int *info = s_win_info + (u - sg.a) * kStWin;
-                    const float *wsum = p.acc + static_cast<int64_t>(s_win_acc[u - sg.a]) * T * kSplitBN;
-                    const int pieces = kStWin * T * 2;           // <= 1024 for T <= 64
-                    constexpr int kMaxPer = kStWin * kStreamMaxTokens * 2 / 128;
-                    float4 f[kMaxPer][2];
-                    bool use[kMaxPer];
+        named_bar_sync(kBarTablesLd, kTablesLdThreads);   // s_win_*; and s_ids, s_tsc unless every window is shrunk
+        const int ew0 = *n_exp ? segs[*n_segs].a : 0;
+        const int ew1 = *n_exp ? segs[*n_segs].b : 0;
+        if (allw && warp == meta_warp) {
+            // each token's adapter (the panel table was built before the
+            // wait); an id outside [0, A) matches no panel
+            s_ids[lane] = id0;
+            s_ids[lane + 32] = id1;
+            __syncwarp();
+        }
+        // every window of my share must be complete: one lane per window
+        // waits, so the checks overlap
+        for (int k = ew0 + lane; k < ew1; k += 32)
+            wait_flag_geq(wcnt + s_win_acc[k - ew0] * kCntStride, KU2, abort_flag, status, LORA_DEV_TIMEOUT);
+        __syncwarp();
+        if (allw) named_bar_sync(kBarLoad, 128);   // warp 6's token table
+        for (int w = 0; w < ew1 - ew0; ++w) {
+            const int r = w % SR;
+            const uint32_t round = w / SR;
+            if (lane == 0 && round > 0) mbar_wait(&s_free[r], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+            __syncwarp();
+            uint8_t *xa = sring + r * sw_bytes;
+            // S panels [8][T rows][16], 32-byte swizzle (chunk c of row t at
+            // t*32 + (c ^ ((t >> 2) & 1))*16); pieces of 8 ranks (panel j,
+            // token t, half c); all loads of a thread are issued before the
+            // first conversion
+            const int *info = s_win_info + w * kStWin;
+            const float *wsum = p.acc + static_cast<int64_t>(s_win_acc[w]) * T * kSplitBN;
+            const int pieces = kStWin * T * 2;           // <= 1024 for T <= 64
+            constexpr int kMaxPer = kStWin * kStreamMaxTokens * 2 / 128;
+            float4 f[kMaxPer][2];
+            bool use[kMaxPer];
 #pragma unroll
-                    for (int i = 0; i < kMaxPer; ++i) {
-                        const int pc = lt + 128 * i;
-                        const int j = pc / (T * 2), rem = pc - j * T * 2;
-                        const int t = rem >> 1, c = rem & 1;
-                        use[i] = pc < pieces && info[j] >= 0 && s_ids[t] == info[j];
-                        f[i][0] = f[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (use[i]) {
-                            const float4 *src = reinterpret_cast<const float4 *>(wsum + t * kSplitBN + j * 16 + c * 8);
-                            f[i][0] = __ldcg(src);
-                            f[i][1] = __ldcg(src + 1);
-                        }
-                    }
-#pragma unroll
-                    for (int i = 0; i < kMaxPer; ++i) {
-                        const int pc = lt + 128 * i;
-                        if (pc >= pieces) break;
-                        const int j = pc / (T * 2), rem = pc - j * T * 2;
-                        const int t = rem >> 1, c = rem & 1;
-                        const float sc = s_tsc[t];   // used only for tokens of the panel's adapter
-                        const float4 f0 = f[i][0], f1 = f[i][1];
-                        const uint4 o =
-                            make_uint4(pack_bf16x2(f0.x * sc, f0.y * sc), pack_bf16x2(f0.z * sc, f0.w * sc),
-                                       pack_bf16x2(f1.x * sc, f1.y * sc), pack_bf16x2(f1.z * sc, f1.w * sc));
-                        *reinterpret_cast<uint4 *>(xa + j * T * 32 + t * 32 + ((c ^ ((t >> 2) & 1)) << 4)) = o;
-                    }
-                    fence_proxy_async_smem();   // generic-proxy stores -> tensor core reads
-                    mbar_arrive(&full[s]);
+            for (int i = 0; i < kMaxPer; ++i) {
+                const int pc = lt + 128 * i;
+                const int j = pc / (T * 2), rem = pc - j * T * 2;
+                const int t = rem >> 1, c = rem & 1;
+                use[i] = pc < pieces && info[j] >= 0 && s_ids[t] == info[j];
+                f[i][0] = f[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (use[i]) {
+                    const float4 *src = reinterpret_cast<const float4 *>(wsum + t * kSplitBN + j * 16 + c * 8);
+                    f[i][0] = __ldcg(src);
+                    f[i][1] = __ldcg(src + 1);
                 }
             }
-        }
-        if (ew1 > ew0) {
-            // my reads of the window sums are done: count myself as a
-            // consumer; the last of the NT consumers of a window clears it
-            named_bar_sync(kBarLoad, 128);
-            if (lt == 0)
-                for (int k = ew0; k < ew1; ++k)
-                    s_zero[k - ew0] = atom_acq_rel_gpu_add(ccnt + s_win_acc[k - ew0] * kCntStride, 1) == p.NT - 1;
-            named_bar_sync(kBarLoad, 128);
-            for (int k = ew0; k < ew1; ++k) {
-                if (!s_zero[k - ew0]) continue;
-                const int ai = s_win_acc[k - ew0];
-                float4 *wsum = reinterpret_cast<float4 *>(p.acc + static_cast<int64_t>(ai) * T * kSplitBN);
-                for (int i = lt; i < T * kSplitBN / 4; i += 128) wsum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (lt == 0) {
-                    wcnt[ai * kCntStride] = 0;
-                    ccnt[ai * kCntStride] = 0;
+#pragma unroll
+            for (int i = 0; i < kMaxPer; ++i) {
+                const int pc = lt + 128 * i;
+                if (pc >= pieces) break;
+                const int j = pc / (T * 2), rem = pc - j * T * 2;
+                const int t = rem >> 1, c = rem & 1;
+                // used only for tokens of the panel's adapter: the call's
+                // scale times that adapter's factor
+                const float sc = allw ? p.scale * s_pan_fac[w * kStWin + j] : s_tsc[t];
+                const float4 f0 = f[i][0], f1 = f[i][1];
+                const uint4 o = make_uint4(pack_bf16x2(f0.x * sc, f0.y * sc), pack_bf16x2(f0.z * sc, f0.w * sc),
+                                           pack_bf16x2(f1.x * sc, f1.y * sc), pack_bf16x2(f1.z * sc, f1.w * sc));
+                *reinterpret_cast<uint4 *>(xa + j * T * 32 + t * 32 + ((c ^ ((t >> 2) & 1)) << 4)) = o;
+            }
+            fence_proxy_async_smem();   // generic-proxy stores -> tensor core reads
+            mbar_arrive(&s_ready[r]);
+            if (w + 1 == min(ew1 - ew0, SR) || (w >= SR && w + 1 == ew1 - ew0)) {
+                // the sums of windows [.., w] are read (all of my windows
+                // once the ring has held them all): count myself as their
+                // consumer; the last of the NT consumers of a window clears it
+                const int c0 = w < SR ? 0 : SR, c1 = w + 1;
+                named_bar_sync(kBarLoad, 128);
+                if (lt == 0)
+                    for (int k = c0; k < c1; ++k)
+                        s_zero[k] = atom_acq_rel_gpu_add(ccnt + s_win_acc[k] * kCntStride, 1) == p.NT - 1;
+                named_bar_sync(kBarLoad, 128);
+                for (int k = c0; k < c1; ++k) {
+                    if (!s_zero[k]) continue;
+                    const int ai = s_win_acc[k];
+                    float4 *ws4 = reinterpret_cast<float4 *>(p.acc + static_cast<int64_t>(ai) * T * kSplitBN);
+                    for (int i = lt; i < T * kSplitBN / 4; i += 128) ws4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (lt == 0) {
+                        wcnt[ai * kCntStride] = 0;
+                        ccnt[ai * kCntStride] = 0;
+                    }
                 }
             }
         }
@@ -498,18 +557,21 @@ __global__ void __launch_bounds__(kClThreads, 1)
             }
             const StSeg sg = segs[si];
             const uint32_t d = tmem_base + sg.region * T;
-            for (int u = sg.a; u < sg.b; ++u, ++it) {
+            for (int u = sg.a; u < sg.b; ++u) {
                 if (sg.kind != kStExpand) {
-                    mma_kunit(it, d, sg.region);
+                    mma_kunit(it++, d, sg.region);
                     continue;
                 }
-                const int s = it % p.stages;
+                // the window's B box through the ring, its S in slot r of the S ring
+                const int w = u - sg.a, r = w % SR;
+                const int s = static_cast<int>(it % p.stages);
                 mbar_wait(&full[s], (it / p.stages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                mbar_wait(&s_ready[r], (w / SR) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
                 fence_proxy_async_smem();   // the S operand arrived through the generic proxy
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t wa = smem_u32(smem + s * slot_bytes);
-                    const uint32_t xa = wa + kClWArea;
+                    const uint32_t xa = smem_u32(sring + r * sw_bytes);
                     uint32_t acc = started & 1;
                     for (int j = 0; j < kStWin; ++j) {
                         umma_bf16(d, umma_sdesc(wa + j * kSplitBN * kChunk * 2, 256, kSwizzle32),
@@ -517,7 +579,9 @@ __global__ void __launch_bounds__(kClThreads, 1)
                         acc = 1;
                     }
                     umma_commit(&empty[s]);
+                    umma_commit(&s_free[r]);
                 }
+                ++it;
                 started |= 1u;
                 __syncwarp();
             }
@@ -533,25 +597,38 @@ __global__ void __launch_bounds__(kClThreads, 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int et = threadIdx.x - 64;
-        if (threadIdx.x >= 160 && threadIdx.x < 160 + rpo / 8) {   // bias of the rows this CTA finishes
-            const int k = threadIdx.x - 160;
-            const int n = n0 + q * rpo + 8 * k;
-            uint4 b = make_uint4(0u, 0u, 0u, 0u);
-            if (p.bias && n < p.N) b = __ldg(reinterpret_cast<const uint4 *>(p.bias + n));
-            reinterpret_cast<uint4 *>(s_bias)[k] = b;
-        }
         if (warp == 2) {
             // ---- metadata --------------------------------------------------
             SegPlan pl;
             if (allw) {
-                // every window is shrunk: the list before the expand is known now
+                // every window of the pool is shrunk and expanded: the whole
+                // unit list is known at launch, and the shrink runs need no
+                // token table (loader warp 6 builds the one the S staging uses)
                 pl = plan_segments(segs, lane == 0, p.windows_all, KU2, G, cta, b0, b1, 0, p.max_regions, nullptr,
                                    true);
-                if (lane == 0) *n_segs = pl.n;
+                const int w0 = (p.windows_all * q) / C, w1 = (p.windows_all * (q + 1)) / C;
+                const int wend = min(w1, w0 + kStMaxWinCta);
+                for (int k = w0 + lane; k < wend; k += 32) {
+                    s_win_panel[k - w0] = kStWin * k;
+                    s_win_acc[k - w0] = k;
+                }
+                if (lane == 0) {
+                    *n_segs = pl.n;
+                    segs[pl.n] = {kStExpand, w0, wend, 0, 0, 0};
+                    *n_exp = w1 > w0;
+                    *out_empty = (b1 == b0 && w1 == w0);
+                    if (!pl.ok || w1 - w0 > kStMaxWinCta) {   // the host rules both out
+                        atomicOr(status, LORA_DEV_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                }
                 __syncwarp();
                 named_bar_arrive(kBarMma, 64);
                 named_bar_arrive(kBarMeta, kMetaThreads);
-            }
+                named_bar_arrive(kBarTablesEpi, 128);
+                named_bar_arrive(kBarTables, kTablesThreads);
+                named_bar_arrive(kBarTablesLd, kTablesLdThreads);
+            } else {
             // tokens' adapters: pool panels [pa, pa + np), windows pa/8 ..
             const bool v0 = id0 >= 0 && id0 < p.A, v1 = id1 >= 0 && id1 < p.A;
             const int64_t ao0 = v0 ? p.a_offset[id0] : 0, ao1 = v1 ? p.a_offset[id1] : 0;
@@ -587,14 +664,12 @@ __global__ void __launch_bounds__(kClThreads, 1)
             if (lane < kStMaxWinAll / 32) s_wpre[lane] = incl - cnt;
             for (unsigned b = bits, k = incl - cnt; b; b &= b - 1, ++k) s_wlist[k] = 32 * lane + __ffs(b) - 1;
             __syncwarp();
-            if (!allw) {
-                // only the touched windows are shrunk, named by their list index
-                pl = plan_segments(segs, lane == 0, NT_, KU2, G, cta, b0, b1, nfirst, p.max_regions, s_wlist, false);
-                if (lane == 0) *n_segs = pl.n;
-                __syncwarp();
-                named_bar_arrive(kBarMma, 64);
-                named_bar_arrive(kBarMeta, kMetaThreads);   // the producer may issue the shrink boxes now
-            }
+            // only the touched windows are shrunk, named by their list index
+            pl = plan_segments(segs, lane == 0, NT_, KU2, G, cta, b0, b1, nfirst, p.max_regions, s_wlist, false);
+            if (lane == 0) *n_segs = pl.n;
+            __syncwarp();
+            named_bar_arrive(kBarMma, 64);
+            named_bar_arrive(kBarMeta, kMetaThreads);   // the producer may issue the shrink boxes now
             if (!pl.ok && lane == 0) {
                 atomicOr(status, LORA_DEV_TIMEOUT);
                 *abort_flag = 1;
@@ -608,7 +683,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const int wend = min(w1, w0 + kStMaxWinCta);
             for (int k = w0 + lane; k < wend; k += 32) {
                 s_win_panel[k - w0] = kStWin * s_wlist[k];
-                s_win_acc[k - w0] = allw ? s_wlist[k] : k;   // sums are kept per shrunk window
+                s_win_acc[k - w0] = k;   // sums are kept per shrunk window
             }
             for (int k = lane; k < (wend - w0) * kStWin; k += 32) s_win_info[k] = -1;
             s_run_info[lane] = -1;   // kStMaxRuns x kStWin = 32 entries
@@ -626,10 +701,9 @@ __global__ void __launch_bounds__(kClThreads, 1)
                     const int lo = max(pa, kStWin * wv), hi = min(pa + np, kStWin * wv + kStWin);
                     if (pos >= w0 && pos < wend)
                         for (int pp = lo; pp < hi; ++pp) s_win_info[(pos - w0) * kStWin + pp - kStWin * wv] = id;
-                    const int rw = allw ? wv : pos;   // how shrink runs name this window
 #pragma unroll
                     for (int r = 0; r < kStMaxRuns; ++r)
-                        if (pl.run_w[r] == rw)
+                        if (pl.run_w[r] == pos)
                             for (int pp = lo; pp < hi; ++pp) s_run_info[r * kStWin + pp - kStWin * wv] = id;
                 }
             };
@@ -638,6 +712,8 @@ __global__ void __launch_bounds__(kClThreads, 1)
             __syncwarp();
             named_bar_arrive(kBarTablesEpi, 128);
             named_bar_arrive(kBarTables, kTablesThreads);
+            named_bar_arrive(kBarTablesLd, kTablesLdThreads);
+            }
         } else {
             named_bar_sync(kBarMeta, kMetaThreads);
             named_bar_sync(kBarTablesEpi, 128);   // s_run_info, s_wbits
@@ -650,7 +726,10 @@ __global__ void __launch_bounds__(kClThreads, 1)
             mbar_wait(&acc_full[sg.region], 0, abort_flag, status, LORA_DEV_TIMEOUT);
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + sg.region * T;
-            const bool live = s_run_info[run * kStWin + row / kChunk] >= 0;   // panel of an adapter present
+            // the rows of every panel go into the sum when every window is
+            // expanded (the S staging keeps each token's own panels); else
+            // only the panels of an adapter present
+            const bool live = allw || s_run_info[run * kStWin + row / kChunk] >= 0;
             float *dst = p.acc + static_cast<int64_t>(sg.w) * T * kSplitBN + row;
             for (int c = 0; c < T; c += 16) {
                 uint32_t v[16];
@@ -662,15 +741,13 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 }
             }
             // one release for the whole run, after all four warps' additions:
-            // the window is complete once its KU2 units have arrived.  A
-            // window no token touches (shrunk only because every window is)
-            // keeps its sum and counter at zero.
+            // the window is complete once its KU2 units have arrived (every
+            // shrunk window is expanded, so its consumers clear it again)
             named_bar_sync(kBarEpi, 128);
-            const int pw = allw ? sg.w : s_wlist[sg.w];
-            const bool touched = (s_wbits[pw >> 5] >> (pw & 31)) & 1u;
-            if (et == 0 && touched) red_release_gpu_add(wcnt + sg.w * kCntStride, sg.b - sg.a);
+            if (et == 0) red_release_gpu_add(wcnt + sg.w * kCntStride, sg.b - sg.a);
             ++run;
         }
+        if (bias_thread) reinterpret_cast<uint4 *>(s_bias)[threadIdx.x - 160] = bias_reg;
         // ---- output tile: push my partial rows to their owners ----------------
         mbar_wait(&acc_full[0], 0, abort_flag, status, LORA_DEV_TIMEOUT);
         tc_fence_after();
@@ -742,20 +819,31 @@ int cluster_max_win_cta() { return kStMaxWinCta; }
 int cluster_win() { return kStWin; }
 size_t cluster_build_smem_bytes(int32_t A) { return SegBuild<kClThreads / 32>::smem_bytes(A); }
 
-size_t cluster_smem_bytes(int T_pad, int stages)
+size_t cluster_smem_bytes(int T_pad, int stages, int s_ring)
 {
-    return static_cast<size_t>(stages) * (kClWArea + T_pad * 256) + static_cast<size_t>(kSplitBN) * T_pad * 4 +
-           1024 + kClMisc;
+    return static_cast<size_t>(stages) * (kClWArea + T_pad * 256) + static_cast<size_t>(s_ring) * kStWin * T_pad * 32 +
+           static_cast<size_t>(kSplitBN) * T_pad * 4 + 1024 + kClMisc;
 }
 
-// Ring depth: what fits, at most 3.  Deeper rings measured no faster: with
-// every CTA's boxes in flight the memory queues only grow, and each round
-// trip of the shrink-to-expand chain waits in them.
+// Ring depth: what fits beside two S slots, at most 3.  Deeper rings
+// measured no faster: with every CTA's boxes in flight the memory queues
+// only grow.
 int cluster_stages(int T_pad)
 {
-    const size_t budget = 227 * 1024 - static_cast<size_t>(kSplitBN) * T_pad * 4 - 1024 - kClMisc;
+    const size_t budget = 227 * 1024 - static_cast<size_t>(kSplitBN) * T_pad * 4 - 1024 - kClMisc -
+                          2 * static_cast<size_t>(kStWin) * T_pad * 32;
     int s = static_cast<int>(budget / (kClWArea + T_pad * 256));
     return s > 3 ? 3 : s;
+}
+
+// S ring slots: what fits beside the weight ring, 2 to kClMaxSRing (0 if
+// not even two fit).
+int cluster_s_ring(int T_pad, int stages)
+{
+    const size_t cap = 227 * 1024;
+    const size_t used = cluster_smem_bytes(T_pad, stages, 0);
+    const int n = used >= cap ? 0 : static_cast<int>((cap - used) / (static_cast<size_t>(kStWin) * T_pad * 32));
+    return n < 2 ? 0 : (n > kClMaxSRing ? kClMaxSRing : n);
 }
 
 // Largest cluster size in {8, 4, 2, 1} whose grid (C x (NT + 1) CTAs, one
@@ -763,8 +851,9 @@ int cluster_stages(int T_pad)
 int cluster_pick_size(int NT, int T_pad, int sms)
 {
     const int stages = cluster_stages(T_pad);
-    if (stages < 2) return 0;
-    const size_t smem = cluster_smem_bytes(T_pad, stages);
+    const int s_ring = cluster_s_ring(T_pad, stages);
+    if (stages < 2 || s_ring < 2) return 0;
+    const size_t smem = cluster_smem_bytes(T_pad, stages, s_ring);
     static int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -806,7 +895,7 @@ cudaError_t launch_cluster(const ClusterMaps &m, const ClusterParams &p, bool pd
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.C * (p.NT + (p.build ? 1 : 0)));
     cfg.blockDim = dim3(kClThreads);
-    cfg.dynamicSmemBytes = cluster_smem_bytes(p.T_pad, p.stages);
+    cfg.dynamicSmemBytes = cluster_smem_bytes(p.T_pad, p.stages, p.s_ring);
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;

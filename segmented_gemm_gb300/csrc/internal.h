@@ -187,6 +187,7 @@ struct ClusterMaps {
 struct ClusterParams {
     int64_t M;
     int32_t N, K, T_pad, C, NT, kblocks, stages, max_regions, max_win_str;
+    int32_t s_ring;            // S operand slots of the expand windows (2..4)
     float scale;
     const float *adapter_scale;   // per-adapter factor on top of scale, or null (all 1)
     const uint16_t *bias;
@@ -218,7 +219,8 @@ int splitk_stages(int T_pad);
 cudaError_t launch_cluster(const ClusterMaps &m, const ClusterParams &p, bool pdl, cudaStream_t stream);
 int cluster_pick_size(int NT, int T_pad, int sms);
 int cluster_stages(int T_pad);
-size_t cluster_smem_bytes(int T_pad, int stages);
+size_t cluster_smem_bytes(int T_pad, int stages, int s_ring);
+int cluster_s_ring(int T_pad, int stages);
 size_t cluster_build_smem_bytes(int32_t A);   // the segment build inside the decode kernel
 int cluster_max_regions();
 int cluster_max_runs();

@@ -527,6 +527,7 @@ static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, co
     p.NT = NT;
     p.kblocks = kblocks;
     p.stages = cluster_stages(T);
+    p.s_ring = cluster_s_ring(T, p.stages);
     p.max_regions = max_regions;
     p.max_win_str = L.max_win_str;
     p.A = pool->num_adapters;
@@ -538,7 +539,7 @@ static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, co
     p.all_windows = p.windows_all <= L.max_win_str ? 1 : 0;
     p.early_weights = pdl ? 1 : 0;
     if (build) {
-        if (cluster_build_smem_bytes(pool->num_adapters) + 1024 > cluster_smem_bytes(T, p.stages)) return -1;
+        if (cluster_build_smem_bytes(pool->num_adapters) + 1024 > cluster_smem_bytes(T, p.stages, p.s_ring)) return -1;
         p.build = 1;
         fill_seg_params(p.seg, ids, M, pool, L, ws);
     }
