@@ -65,11 +65,12 @@ constexpr int kBarMma = 2;                 // named barrier: metadata ready (MMA
 constexpr int kBarLoad = 3;                // named barrier: the four loader warps
 constexpr int kBarEpi = 4;                 // named barrier: the four epilogue warps
 constexpr int kBarTmem = 6;                // named barrier: TMEM allocated (warps 0..5; the loaders never read it)
-constexpr int kBarTables = 7;              // named barrier: expand windows ready (warp 2 -> producer, MMA)
+constexpr int kBarTables = 7;              // named barrier: expand windows ready (table warp -> producer, MMA)
 constexpr int kBarTablesEpi = 8;           // named barrier: panel tables ready (warp 2 -> the other epilogue warps)
-constexpr int kTablesThreads = 96;         // warps 0, 1, 2
+constexpr int kTablesThreads = 96;         // warps 0, 1 and the table warp (2, or 6 when every window is processed)
 constexpr int kBarTablesLd = 9;            // named barrier: panel tables ready (warp 2 -> loaders)
 constexpr int kTablesLdThreads = 160;      // warp 2 + warps 6..9
+constexpr int kBarTouch = 10;              // named barrier: expand windows' touched flags (warp 6 -> epilogue)
 constexpr int kStFirst = 3;                // K units issued before the metadata is known
 constexpr int kMetaThreads = kClThreads - 32;
 
@@ -87,7 +88,7 @@ struct StSeg {
 static_assert((2 * kClMaxStages + kStMaxRegions + 1 + 2 * kClMaxSRing) * 8 + 10 * 4 + kSplitBN * 2 + 64 * 4 * 2 +
                       kStMaxSegs * static_cast<int>(sizeof(StSeg)) + kStMaxWinCta * 4 * 3 + kStMaxWinCta * kStWin * 4 +
                       kStMaxRuns * kStWin * 4 + (kStMaxWinAll / 32) * 4 * 2 + kStMaxWinList * 4 +
-                      kStMaxWinCta * kStWin * 4 <=
+                      kStMaxWinCta * kStWin * 4 + kStMaxWinCta * 4 <=
                   kClMisc,
               "cluster kernel tables overflow their shared-memory area");
 
@@ -219,7 +220,6 @@ __global__ void __launch_bounds__(kClThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ivars);
     volatile int *abort_flag = ivars + 1;
     int *n_segs = ivars + 2;       // segments before the expand
-    int *out_empty = ivars + 3;
     int *n_exp = ivars + 4;        // 1: segs[*n_segs] is my expand segment
     uint16_t *s_bias = reinterpret_cast<uint16_t *>(ivars + 10);   // [128] my output rows' bias (16-byte aligned)
     int *s_ids = reinterpret_cast<int *>(s_bias + kSplitBN);         // [64] token ids (-2 past M)
@@ -231,6 +231,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     int *s_run_info = s_win_info + kStMaxWinCta * kStWin;   // [kStMaxRuns][8] the same for my shrink windows
     int *s_zero = s_run_info + kStMaxRuns * kStWin;    // [kStMaxWinCta] I am the window's last consumer
     float *s_pan_fac = reinterpret_cast<float *>(s_zero + kStMaxWinCta);   // [kStMaxWinCta][8] owner's factor
+    int *s_win_touch = reinterpret_cast<int *>(s_pan_fac + kStMaxWinCta * kStWin);   // [kStMaxWinCta] a token uses it
     unsigned *s_wbits = reinterpret_cast<unsigned *>(s_zero + kStMaxWinCta);   // [16] windows touched
     int *s_wpre = reinterpret_cast<int *>(s_wbits + kStMaxWinAll / 32);       // [16] popcount prefix
     int *s_wlist = s_wpre + kStMaxWinAll / 32;         // [kStMaxWinList] windows touched, ascending
@@ -404,6 +405,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             }
             const StSeg sg = segs[si];
             for (int u = sg.a; u < sg.b; ++u) {
+                if (sg.kind == kStExpand && !s_win_touch[u - sg.a]) continue;   // no token uses the window
                 const uint32_t iu = it++;
                 if (iu < static_cast<uint32_t>(nfirst)) continue;   // issued in the prologue
                 const int s = iu % p.stages;
@@ -442,7 +444,18 @@ __global__ void __launch_bounds__(kClThreads, 1)
             // wait); an id outside [0, A) matches no panel
             s_ids[lane] = id0;
             s_ids[lane + 32] = id1;
+            for (int k = lane; k < ew1 - ew0; k += 32) s_win_touch[k] = 0;
             __syncwarp();
+            // a window is expanded only if some token's adapter owns one of its panels
+            for (int k = lane; k < (ew1 - ew0) * kStWin; k += 32) {
+                const int owner = s_win_info[k];
+                bool hit = false;
+                for (int t = 0; t < 64 && owner >= 0 && !hit; ++t) hit = s_ids[t] == owner;
+                if (hit) s_win_touch[k / kStWin] = 1;
+            }
+            __syncwarp();
+            named_bar_arrive(kBarTables, kTablesThreads);   // producer and MMA: which windows to expand
+            named_bar_arrive(kBarTouch, 160);                // epilogue: whether my output tile gets any MMA
         }
         // every window of my share must be complete: one lane per window
         // waits, so the checks overlap
@@ -450,11 +463,39 @@ __global__ void __launch_bounds__(kClThreads, 1)
             wait_flag_geq(wcnt + s_win_acc[k - ew0] * kCntStride, KU2, abort_flag, status, LORA_DEV_TIMEOUT);
         __syncwarp();
         if (allw) named_bar_sync(kBarLoad, 128);   // warp 6's token table
-        for (int w = 0; w < ew1 - ew0; ++w) {
-            const int r = w % SR;
-            const uint32_t round = w / SR;
+        // my reads of the sums of windows [counted, hi) are done (or a
+        // window no token uses needs no read): count myself as their
+        // consumer; the last of the NT consumers of a window clears it
+        int counted = 0;
+        auto count_upto = [&](int hi) {
+            if (hi <= counted) return;
+            named_bar_sync(kBarLoad, 128);
+            if (lt == 0)
+                for (int k = counted; k < hi; ++k)
+                    s_zero[k] = atom_acq_rel_gpu_add(ccnt + s_win_acc[k] * kCntStride, 1) == p.NT - 1;
+            named_bar_sync(kBarLoad, 128);
+            for (int k = counted; k < hi; ++k) {
+                if (!s_zero[k]) continue;
+                const int ai = s_win_acc[k];
+                float4 *ws4 = reinterpret_cast<float4 *>(p.acc + static_cast<int64_t>(ai) * T * kSplitBN);
+                for (int i = lt; i < T * kSplitBN / 4; i += 128) ws4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (lt == 0) {
+                    wcnt[ai * kCntStride] = 0;
+                    ccnt[ai * kCntStride] = 0;
+                }
+            }
+            counted = hi;
+        };
+        // the windows some token uses, staged in S ring slot wt % SR (wt:
+        // their index among those windows, as the MMA issuer counts them)
+        for (int w = 0, wt = 0; w < ew1 - ew0; ++w) {
+            if (!s_win_touch[w]) continue;
+            const int r = wt % SR;
+            const uint32_t round = wt / SR;
+            if (round > 0) count_upto(w);   // before waiting for a slot: the windows before w are read
             if (lane == 0 && round > 0) mbar_wait(&s_free[r], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
             __syncwarp();
+            ++wt;
             uint8_t *xa = sring + r * sw_bytes;
             // S panels [8][T rows][16], 32-byte swizzle (chunk c of row t at
             // t*32 + (c ^ ((t >> 2) & 1))*16); pieces of 8 ranks (panel j,
@@ -495,28 +536,8 @@ __global__ void __launch_bounds__(kClThreads, 1)
             }
             fence_proxy_async_smem();   // generic-proxy stores -> tensor core reads
             mbar_arrive(&s_ready[r]);
-            if (w + 1 == min(ew1 - ew0, SR) || (w >= SR && w + 1 == ew1 - ew0)) {
-                // the sums of windows [.., w] are read (all of my windows
-                // once the ring has held them all): count myself as their
-                // consumer; the last of the NT consumers of a window clears it
-                const int c0 = w < SR ? 0 : SR, c1 = w + 1;
-                named_bar_sync(kBarLoad, 128);
-                if (lt == 0)
-                    for (int k = c0; k < c1; ++k)
-                        s_zero[k] = atom_acq_rel_gpu_add(ccnt + s_win_acc[k] * kCntStride, 1) == p.NT - 1;
-                named_bar_sync(kBarLoad, 128);
-                for (int k = c0; k < c1; ++k) {
-                    if (!s_zero[k]) continue;
-                    const int ai = s_win_acc[k];
-                    float4 *ws4 = reinterpret_cast<float4 *>(p.acc + static_cast<int64_t>(ai) * T * kSplitBN);
-                    for (int i = lt; i < T * kSplitBN / 4; i += 128) ws4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (lt == 0) {
-                        wcnt[ai * kCntStride] = 0;
-                        ccnt[ai * kCntStride] = 0;
-                    }
-                }
-            }
         }
+        count_upto(ew1 - ew0);
     } else if (warp == 1) {
         // ===================== MMA issuer ====================================
         uint32_t started = 0;   // bit r: region r holds a partial sum
@@ -550,6 +571,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         }
         named_bar_sync(kBarMma, 64);
         const int nk = *n_segs;
+        int wt = 0;   // expand windows issued so far
         for (int si = si0; si <= nk; ++si) {
             if (si == nk) {   // the expand windows, once the tables are ready
                 named_bar_sync(kBarTables, kTablesThreads);
@@ -562,8 +584,10 @@ __global__ void __launch_bounds__(kClThreads, 1)
                     mma_kunit(it++, d, sg.region);
                     continue;
                 }
-                // the window's B box through the ring, its S in slot r of the S ring
-                const int w = u - sg.a, r = w % SR;
+                // the window's B box through the ring, its S in slot r of the
+                // S ring (windows no token uses are skipped: wt counts the others)
+                if (!s_win_touch[u - sg.a]) continue;
+                const int w = wt++, r = w % SR;
                 const int s = static_cast<int>(it % p.stages);
                 mbar_wait(&full[s], (it / p.stages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
                 mbar_wait(&s_ready[r], (w / SR) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
@@ -616,7 +640,6 @@ __global__ void __launch_bounds__(kClThreads, 1)
                     *n_segs = pl.n;
                     segs[pl.n] = {kStExpand, w0, wend, 0, 0, 0};
                     *n_exp = w1 > w0;
-                    *out_empty = (b1 == b0 && w1 == w0);
                     if (!pl.ok || w1 - w0 > kStMaxWinCta) {   // the host rules both out
                         atomicOr(status, LORA_DEV_TIMEOUT);
                         *abort_flag = 1;
@@ -626,8 +649,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 named_bar_arrive(kBarMma, 64);
                 named_bar_arrive(kBarMeta, kMetaThreads);
                 named_bar_arrive(kBarTablesEpi, 128);
-                named_bar_arrive(kBarTables, kTablesThreads);
-                named_bar_arrive(kBarTablesLd, kTablesLdThreads);
+                named_bar_arrive(kBarTablesLd, kTablesLdThreads);   // kBarTables: warp 6, once it knows the ids
             } else {
             // tokens' adapters: pool panels [pa, pa + np), windows pa/8 ..
             const bool v0 = id0 >= 0 && id0 < p.A, v1 = id1 >= 0 && id1 < p.A;
@@ -686,11 +708,11 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 s_win_acc[k - w0] = k;   // sums are kept per shrunk window
             }
             for (int k = lane; k < (wend - w0) * kStWin; k += 32) s_win_info[k] = -1;
+            for (int k = lane; k < wend - w0; k += 32) s_win_touch[k] = 1;   // only touched windows are listed
             s_run_info[lane] = -1;   // kStMaxRuns x kStWin = 32 entries
             if (lane == 0) {
                 segs[pl.n] = {kStExpand, w0, wend, 0, 0, 0};
                 *n_exp = w1 > w0;
-                *out_empty = (b1 == b0 && w1 == w0);
             }
             __syncwarp();
             // the adapter owning each panel of my windows (absent panels stay -1)
@@ -751,7 +773,13 @@ __global__ void __launch_bounds__(kClThreads, 1)
         // ---- output tile: push my partial rows to their owners ----------------
         mbar_wait(&acc_full[0], 0, abort_flag, status, LORA_DEV_TIMEOUT);
         tc_fence_after();
-        const bool empty_run = *out_empty;   // nothing accumulated: send zeros
+        // nothing accumulated (no base units and no expand window a token
+        // uses): send zeros
+        named_bar_sync(kBarTouch, allw ? 160 : 128);   // the touched flags (warp 6, or warp 2 before kBarTablesEpi)
+        bool any_touch = false;
+        if (*n_exp)
+            for (int k = 0; k < segs[*n_segs].b - segs[*n_segs].a; ++k) any_touch = any_touch || s_win_touch[k];
+        const bool empty_run = b1 == b0 && !any_touch;
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
         cluster_wait();        // every peer's receive barrier is initialised
         const int owner = row / rpo;
