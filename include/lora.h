@@ -239,6 +239,48 @@ int lora_linear(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lor
                 const lora_segments_t *segs, lora_bf16_t *y, void *ws, size_t ws_bytes,
                 lora_stream_t stream);
 
+/*
+ * Several LoRA layers of one step in ONE launch (page "vLLM-Ascend dynamic
+ * LoRA", §1.2 end: a model runs many LoRA linears per layer and the
+ * per-operator dispatch multiplies; §3.2: one lora_id_map and one segment
+ * table per step serve every LoRA layer).  Each layer is
+ *     y_l = x_l W_l^T + bias_l + scale_l * s_{l,id} * (x_l A_{l,id}^T) B_{l,id}^T
+ * with the step's one lora_id_map; the layers may differ in K, N, weights,
+ * inputs, outputs, scale, factors and slice boundaries, but their pools must
+ * hold the same adapters with the same ranks, laid out alike (lora_pool_layout
+ * of the same true ranks, each for its own K and N) and cut into the same
+ * number of output slices.  The host checks what it can see of that (adapter
+ * count, max_rank, pool row and panel counts, slice count) and returns
+ * LORA_ERR_SHAPE otherwise.
+ *
+ * The tiled tensor-core schedule runs all layers in one persistent launch:
+ * its work list holds every layer's shrink jobs, then every layer's output
+ * tiles, so one layer's last partial wave overlaps the next layer's tiles.
+ * Without a prebuilt table a segment build launch goes first, as for
+ * lora_linear.
+ *
+ * layers: HOST array of num_layers (1..LORA_MAX_LAYERS) descriptors.
+ * lora_id_map: DEVICE int32 [M] (needed unless segs is given and no pool
+ * has per-adapter factors).  segs: a table built by lora_build_segments
+ * for layer 0's pool in this ws, or NULL.  ws: DEVICE, at least
+ * lora_layers_workspace_size(M, largest N, num_adapters, num_layers) bytes,
+ * zero-filled once (lora_workspace_init); it also holds the table.
+ * Accumulation and rounding as for lora_linear; M == 0 is a no-op.
+ */
+#define LORA_MAX_LAYERS 8
+typedef struct {
+    const lora_bf16_t *x;       /* DEVICE bf16 [M, pool->K] */
+    const lora_bf16_t *W;       /* DEVICE bf16 [pool->N, pool->K] */
+    const lora_bf16_t *bias;    /* DEVICE bf16 [pool->N] or NULL */
+    const lora_pool_t *pool;    /* HOST descriptor of the layer's adapter pool */
+    float scale;                /* the layer's LoRA scale */
+    lora_bf16_t *y;             /* DEVICE bf16 [M, pool->N], written */
+} lora_layer_t;
+
+size_t lora_layers_workspace_size(int64_t M, int32_t max_N, int32_t num_adapters, int32_t num_layers);
+int lora_linear_layers(const lora_layer_t *layers, int32_t num_layers, int64_t M, const int32_t *lora_id_map,
+                       const lora_segments_t *segs, void *ws, size_t ws_bytes, lora_stream_t stream);
+
 /* Schedules of lora_linear_ex (the automatic choice picks by M). */
 enum {
     LORA_PATH_AUTO = 0,

@@ -68,6 +68,7 @@ static_assert(kSAreaBytes + kPanelsPerStage * kBPanelBytes <= kWSlot, "an expand
 
 struct Job {
     int kind;   // 0 shrink, 1 output
+    int layer;  // the layer of the launch it belongs to
     int m, n, c0, c1;
     int kb0, kb1;   // K blocks of this piece of the job
     int part;       // kPartFull, or a piece of a split output tile: kPartHead (holds K block 0) / kPartTail
@@ -76,28 +77,40 @@ struct Job {
 
 enum { kPartFull = 0, kPartHead = 1, kPartTail = 2 };
 
+// Item j of the launch: the n_sjobs shrink items of every layer (each
+// layer's list alike: the layers share one table), then every layer's
+// output tiles.
 __device__ __forceinline__ Job decode_job(int j, int n_sjobs, const TcParams &p, int nmt)
 {
     Job jb;
-    jb.kb0 = 0;
-    jb.kb1 = p.mode == kModeExpand ? 0 : p.kblocks;
     jb.part = kPartFull;
     jb.slot = 0;
+    const int nsl = n_sjobs / p.num_layers;   // shrink items of one layer
     if (j < n_sjobs) {
-        // shrink item j: K piece j % S of shrink job j / S
-        const int S = p.shrink_split, sj = j / S, h = j - sj * S;
+        // shrink item j: K piece jl % S of shrink job jl / S of its layer
+        jb.layer = j / nsl;
+        const int jl = j - jb.layer * nsl;
+        const int S = p.shrink_split, sj = jl / S, h = jl - sj * S;
+        const int kb = p.layer[jb.layer].kblocks;
         jb.kind = 0;
         jb.m = p.sjob_tile[sj];
         jb.n = 0;
         jb.c0 = p.sjob_c0[sj];
         jb.c1 = p.sjob_c1[sj];
-        jb.kb0 = (p.kblocks * h) / S;
-        jb.kb1 = (p.kblocks * (h + 1)) / S;
+        jb.kb0 = (kb * h) / S;
+        jb.kb1 = (kb * (h + 1)) / S;
         jb.slot = h;   // the S panel set it writes
         return jb;
     }
-    const int t = j - n_sjobs;
-    const int per_group = p.group_m * p.num_ntiles;
+    int t = j - n_sjobs;
+    int l = 0;
+    while (l + 1 < p.num_layers && t >= p.layer[l + 1].tile0) ++l;
+    const TcLayer &Ly = p.layer[l];
+    t -= Ly.tile0;
+    jb.layer = l;
+    jb.kb0 = 0;
+    jb.kb1 = p.mode == kModeExpand ? 0 : Ly.kblocks;
+    const int per_group = p.group_m * Ly.num_ntiles;
     const int g = t / per_group, r = t - g * per_group;
     const int m0 = g * p.group_m;
     const int gm = min(p.group_m, nmt - m0);
@@ -111,7 +124,7 @@ __device__ __forceinline__ Job decode_job(int j, int n_sjobs, const TcParams &p,
     // the expand steps use the panels of the output slice holding tile n
     int sl = 0;
     for (int k = 1; k < p.num_slices; ++k)
-        if (jb.n * kBN >= p.slice_start[k]) sl = k;
+        if (jb.n * kBN >= Ly.slice_start[k]) sl = k;
     jb.c0 = p.tile_chunk_off[jb.m * p.num_slices + sl];
     jb.c1 = p.tile_chunk_off[jb.m * p.num_slices + sl + 1];
     return jb;
@@ -196,7 +209,7 @@ __device__ __forceinline__ bool get_item(int q, int b, int G, int n_sjobs, int n
         return true;
     }
     if (s.ro <= 0 || b - s.rs >= s.gp) return false;
-    const int KB = p.kblocks, bb = b - s.rs;
+    const int KB = p.layer[0].kblocks, bb = b - s.rs;   // stream-K: one layer
     const int64_t r0 = sk_start(s, bb), r1 = sk_start(s, bb + 1);
     int64_t f = r0;
     int t = static_cast<int>(f / KB);
@@ -238,13 +251,10 @@ __device__ __forceinline__ int sk_tail_count(int b, int t, const SkPlan &s, int 
 }
 
 template <int kXStages, int kWStages>
-__global__ void __launch_bounds__(kTcThreads, 1)
-    lora_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                   const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_a32,
-                   const __grid_constant__ CUtensorMap tm_a48, const __grid_constant__ CUtensorMap tm_a64,
-                   const TcParams p)
+__global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_constant__ TcArgs args)
 {
+    const TcParams &p = args.p;
+    const CUtensorMap &tm_s = args.s;
     static_assert(kWStages * kWSlot >= kBM * kBN * 4, "a split tile's fp32 partials fit in the W ring");
     static_assert((2 * kXStages + 2 * kWStages + 5) * 8 + 8 <= 256, "barriers, TMEM address and abort flag fit");
     static_assert(tc_smem_bytes<kXStages, kWStages>() <= 232448, "fits the opt-in shared memory of a CTA");
@@ -287,9 +297,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_mbarrier_init();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&tm_w);
-        tma_prefetch_map(&tm_a);
-        tma_prefetch_map(&tm_b);
+        tma_prefetch_map(&args.maps[0].w);
+        tma_prefetch_map(&args.maps[0].a);
+        tma_prefetch_map(&args.maps[0].b);
         tma_prefetch_map(&tm_s);
     }
     if (warp == 1) {
@@ -303,29 +313,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     // shrink items: every shrink job in p.shrink_split pieces along K
     const int nmt = p.mode == kModeMoe ? min(p.hdr[HDR_MOE_TILES], p.num_mtiles) : p.num_mtiles;
-    const int n_sjobs = (p.mode == kModeExpand || p.mode == kModeMoe) ? 0 : p.hdr[HDR_NSJOBS] * p.shrink_split;
-    const int n_out = (p.mode == kModeShrink) ? 0 : nmt * p.num_ntiles;
-    SkPlan sk = sk_plan(n_sjobs, n_out, gridDim.x, p.kblocks, p.streamk != 0, p.shrink_split);
+    const int n_sjobs =
+        (p.mode == kModeExpand || p.mode == kModeMoe) ? 0 : p.hdr[HDR_NSJOBS] * p.shrink_split * p.num_layers;
+    int n_out = 0;   // output tiles of every layer
+    if (p.mode != kModeShrink)
+        for (int l = 0; l < p.num_layers; ++l) n_out += nmt * p.layer[l].num_ntiles;
+    SkPlan sk = sk_plan(n_sjobs, n_out, gridDim.x, p.layer[0].kblocks, p.streamk != 0, p.shrink_split);
     sk.nmt = nmt;
     Job jb;
 
     if (warp == 0) {
         // ===================== TMA producer: W ring (W, A panels, S / B panels)
         uint32_t iw = 0;
-        // The S-ready counter of token tile m is put back to zero by the last
-        // of its num_ntiles output tiles to pass the wait on it: each adds
-        // itself to a consumer counter right after the wait and reads the
-        // result one item later, so the round trip hides behind the loads.
-        int32_t *cons = p.counters + CNT_FIXED + p.num_mtiles;
-        int rst_m = -1, rst_old = 0;
+        // The S-ready counter of (layer, token tile m) is put back to zero by
+        // the last of the layer's num_ntiles output tiles of row m to pass
+        // the wait on it: each adds itself to a consumer counter right after
+        // the wait and reads the result one item later, so the round trip
+        // hides behind the loads.
+        int32_t *cons = p.counters + CNT_FIXED + p.num_layers * p.num_mtiles;
+        int rst_m = -1, rst_old = 0, rst_nt = 0;   // counter index, consumers before me, the layer's tiles per row
         auto settle = [&]() {
-            if (rst_m >= 0 && rst_old == p.num_ntiles - 1) {
+            if (rst_m >= 0 && rst_old == rst_nt - 1) {
                 p.counters[CNT_FIXED + rst_m] = 0;
                 cons[rst_m] = 0;
             }
             rst_m = -1;
         };
         for (int q = 0; get_item(q, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, jb); ++q) {
+            const TcLayer &Ly = p.layer[jb.layer];
+            const TcLayerMaps &mp = args.maps[jb.layer];
             // shrink job: consecutive rank panels of one adapter are
             // consecutive pool rows, loaded as one box of 16..64 rows per run.
             // The runs are found once per job, one lane per chunk: lane c
@@ -334,9 +350,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // output job: the first B-pool row of the [N, 16] panel of each
             // of the tile's first 32 chunks, one lane per chunk, loaded now
             // for the expand steps
-            const int brow_l = (jb.kind == 1 && jb.c0 + lane < jb.c1) ? p.chunk_bpanel[jb.c0 + lane] * p.N : 0;
+            const int brow_l = (jb.kind == 1 && jb.c0 + lane < jb.c1) ? p.chunk_bpanel[jb.c0 + lane] * Ly.N : 0;
             // kModeMoe: the tile's expert's rows of the stacked expert weights
-            const int w_row0 = (p.mode == kModeMoe && jb.kind == 1) ? p.mt_expert[jb.m] * p.N : 0;
+            const int w_row0 = (p.mode == kModeMoe && jb.kind == 1) ? p.mt_expert[jb.m] * Ly.N : 0;
             if (jb.kind == 0) {
                 const int c = jb.c0 + lane;
                 const bool in = c < jb.c1;
@@ -375,14 +391,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (jb.kind == 1) {
                     if (lane == 0) {
                         mbar_expect_tx(&fullw[s], kWSlot);
-                        tma_load_2d(wsl, &tm_w, &fullw[s], kb * kBK, jb.n * kBN + w_row0);
+                        tma_load_2d(wsl, &mp.w, &fullw[s], kb * kBK, jb.n * kBN + w_row0);
                     }
                 } else {
                     if (lane == 0) mbar_expect_tx(&fullw[s], (jb.c1 - jb.c0) * kAPanelBytes);
                     __syncwarp();
                     if (run_len > 0) {
                         const CUtensorMap *m =
-                            run_len == 1 ? &tm_a : run_len == 2 ? &tm_a32 : run_len == 3 ? &tm_a48 : &tm_a64;
+                            run_len == 1 ? &mp.a : run_len == 2 ? &mp.a32 : run_len == 3 ? &mp.a48 : &mp.a64;
                         tma_load_2d(wsl + lane * kAPanelBytes, m, &fullw[s], kb * kBK, run_row);
                     }
                 }
@@ -391,13 +407,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (jb.kind == 1 && jb.c1 > jb.c0 && jb.part != kPartTail) {
                 if (p.mode == kModeLinear) {
                     if (lane == 0) {
-                        // every K piece of every shrink job of the tile
-                        wait_flag_geq(p.counters + CNT_FIXED + jb.m, p.tile_njobs[jb.m] * p.s_sets, abort_flag,
-                                      status, LORA_DEV_TIMEOUT);
+                        // every K piece of every shrink job of the tile (this layer's)
+                        const int ci = jb.layer * p.num_mtiles + jb.m;
+                        wait_flag_geq(p.counters + CNT_FIXED + ci, p.tile_njobs[jb.m] * p.s_sets, abort_flag, status,
+                                      LORA_DEV_TIMEOUT);
                         fence_proxy_async_global();
                         settle();
-                        rst_old = atom_acq_rel_gpu_add(cons + jb.m, 1);
-                        rst_m = jb.m;
+                        rst_old = atom_acq_rel_gpu_add(cons + ci, 1);
+                        rst_m = ci;
+                        rst_nt = Ly.num_ntiles;
                     }
                     __syncwarp();
                 }
@@ -414,11 +432,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int brow_s = __shfl_sync(0xffffffffu, brow_l, ci & 31);
                     if (lane < nc) {
                         const int c = cg + lane;
-                        const int brow = ci < 32 ? brow_s : p.chunk_bpanel[c] * p.N;
+                        const int brow = ci < 32 ? brow_s : p.chunk_bpanel[c] * Ly.N;
                         for (int h = 0; h < p.s_sets; ++h)
                             tma_load_2d(wsl + (h * kPanelsPerStage + lane) * kSPanelBytes, &tm_s, &fullw[s], 0,
-                                        h * p.s_set_rows + c * kBM);
-                        tma_load_2d(wsl + kSAreaBytes + lane * kBPanelBytes, &tm_b, &fullw[s], 0, brow + jb.n * kBN);
+                                        (jb.layer * p.s_sets + h) * p.s_set_rows + c * kBM);
+                        tma_load_2d(wsl + kSAreaBytes + lane * kBPanelBytes, &mp.b, &fullw[s], 0, brow + jb.n * kBN);
                     }
                     __syncwarp();
                 }
@@ -439,6 +457,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t ix = 0;
         for (int q = 0; get_item(q, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, jb); ++q) {
             if (jb.kb1 <= jb.kb0) continue;
+            const TcLayer &Ly = p.layer[jb.layer];
             const uint16_t *src[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -446,7 +465,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (pp >= p.M) pp = p.M - 1;
                 int64_t row = p.perm[pp];
                 if (p.mode == kModeMoe) row = row >= 0 ? row / p.topk : 0;   // a pair's token; a gap reads row 0
-                src[q] = p.x + row * p.K + chunk * 8;
+                src[q] = Ly.x + row * Ly.K + chunk * 8;
             }
             for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++ix) {
                 const int s = ix % kXStages;
@@ -454,7 +473,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (lane == 0 && round > 0) mbar_wait(&emptyx[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
                 __syncwarp();
                 uint8_t *xs = xring + s * kXSlot + swz;
-                const uint32_t nbytes = (kb * kBK + chunk * 8 < p.K) ? 16u : 0u;
+                const uint32_t nbytes = (kb * kBK + chunk * 8 < Ly.K) ? 16u : 0u;
 #pragma unroll
                 for (int q = 0; q < 8; ++q) cp_async16(xs + (rb + 16 * q) * 128, src[q] + kb * kBK, nbytes);
                 cp_async_mbar_arrive_noinc(&fullx[s]);
@@ -522,17 +541,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int row = quad * 32 + lane;
         const int et = threadIdx.x - 64;   // 0..127
         for (int q = 0; get_item(q, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, jb); ++q) {
+            const TcLayer &Ly = p.layer[jb.layer];
             const uint32_t slot = q & 1, use = q >> 1;
             uint32_t *tbias = s_bias + slot * (kBN / 2);   // [kBN / 2] bf16 pairs
-            const bool out_bias = jb.kind == 1 && jb.part != kPartTail && p.mode == kModeLinear && p.bias;
+            const bool out_bias = jb.kind == 1 && jb.part != kPartTail && p.mode == kModeLinear && Ly.bias;
             if (out_bias) {
                 // the tile's 256 bias values, once, while the MMA still runs
                 // (the barriers keep the previous tile's readers apart)
                 named_bar_sync(1, 128);
                 const int col = jb.n * kBN + 2 * et;
                 uint32_t bv = 0u;
-                if (col + 1 < p.N) bv = __ldg(reinterpret_cast<const uint32_t *>(p.bias + col));
-                else if (col < p.N) bv = static_cast<uint32_t>(__ldg(p.bias + col));
+                if (col + 1 < Ly.N) bv = __ldg(reinterpret_cast<const uint32_t *>(Ly.bias + col));
+                else if (col < Ly.N) bv = static_cast<uint32_t>(__ldg(Ly.bias + col));
                 tbias[et] = bv;
                 named_bar_sync(1, 128);
             }
@@ -544,10 +564,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool lora_row = p.mode != kModeExpand || pp >= p.offsets[1];
             // the LoRA scale of my row: the call's scale times its adapter's
             // factor (rows outside every segment are masked anyway)
-            float row_sc = p.scale;
-            if (p.adapter_scale && jb.kind == 0 && p.mode == kModeLinear && valid) {
+            float row_sc = Ly.scale;
+            if (Ly.adapter_scale && jb.kind == 0 && p.mode == kModeLinear && valid) {
                 const int id = p.ids[tok];
-                row_sc *= (id >= 0 && id < p.num_adapters) ? __ldg(p.adapter_scale + id) : 0.f;
+                row_sc *= (id >= 0 && id < p.num_adapters) ? __ldg(Ly.adapter_scale + id) : 0.f;
             }
             // the CTA's last item: both rings are idle, so an output tile is
             // staged in the x ring (rows padded to 528 bytes: conflict-free)
@@ -563,8 +583,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
             if (jb.kind == 0) {
                 // ---- S panels: mask to the row's own segment, scale, bf16 ----
-                // (panel set jb.slot: the K piece of the shrink job)
-                uint16_t *panels = p.s_panels + static_cast<int64_t>(jb.slot) * p.s_set_rows * kChunk;
+                // (panel set jb.slot of the layer: the K piece of the shrink job)
+                uint16_t *panels =
+                    p.s_panels + static_cast<int64_t>(jb.layer * p.s_sets + jb.slot) * p.s_set_rows * kChunk;
                 for (int c = jb.c0; c < jb.c1; ++c) {
                     uint32_t r[16];
                     tmem_ld16(tbase + (c - jb.c0) * kChunk, r);
@@ -600,7 +621,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     fence_proxy_async_global();
                     __threadfence();
                     named_bar_sync(1, 128);
-                    if (et == 0) red_release_gpu_add(p.counters + CNT_FIXED + jb.m, 1);
+                    if (et == 0) red_release_gpu_add(p.counters + CNT_FIXED + jb.layer * p.num_mtiles + jb.m, 1);
                 }
             } else if (jb.part == kPartTail) {
                 // ---- tail piece of a split tile: store my partial sums --------
@@ -648,7 +669,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const float4 *spart = reinterpret_cast<const float4 *>(wring);
                 int ntail = 0, tail0 = 0;
                 if (head) {
-                    ntail = sk_tail_count(blockIdx.x, jb.slot, sk, p.kblocks);
+                    ntail = sk_tail_count(blockIdx.x, jb.slot, sk, Ly.kblocks);
                     tail0 = sk_next_tail(blockIdx.x - sk.rs, sk);
                     if (et == 0) {   // every tail piece has stored its partial sums
                         wait_flag_geq(p.sk_cnt + jb.slot * kWinCntStride, ntail, abort_flag, status, LORA_DEV_TIMEOUT);
@@ -697,7 +718,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                     }
                     const int col = n0 + cc * 16;
-                    if (!valid || col >= p.N || !lora_row) return;
+                    if (!valid || col >= Ly.N || !lora_row) return;
                     if (staged) {
                         const uint4 *bsrc = reinterpret_cast<const uint4 *>(tbias + cc * 8);
 #pragma unroll
@@ -712,12 +733,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         return;
                     }
-                    uint16_t *dst = p.y + static_cast<int64_t>(tok) * p.N + col;
+                    uint16_t *dst = Ly.y + static_cast<int64_t>(tok) * Ly.N + col;
                     if (p.mode == kModeExpand) {
                         const uint4 *src = reinterpret_cast<const uint4 *>(dst);
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            if (col + 8 * h >= p.N) break;
+                            if (col + 8 * h >= Ly.N) break;
                             const uint4 u = src[h];
                             const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -742,7 +763,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     uint4 *o = reinterpret_cast<uint4 *>(dst);
                     o[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                                       pack_bf16x2(v[6], v[7]));
-                    if (col + 8 < p.N)
+                    if (col + 8 < Ly.N)
                         o[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]),
                                           pack_bf16x2(v[12], v[13]), pack_bf16x2(v[14], v[15]));
                 };
@@ -761,10 +782,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int h = 0; h < 4; ++h) emit(cc + h, r[h]);
                 }
-                if (staged && valid && lora_row && n0 < p.N) {
+                if (staged && valid && lora_row && n0 < Ly.N) {
                     fence_proxy_async_smem();   // my row's generic-proxy writes -> the bulk copy's reads
-                    bulk_store(p.y + static_cast<int64_t>(tok) * p.N + n0, srow,
-                               static_cast<uint32_t>(min(kBN, p.N - n0)) * 2);
+                    bulk_store(Ly.y + static_cast<int64_t>(tok) * Ly.N + n0, srow,
+                               static_cast<uint32_t>(min(kBN, Ly.N - n0)) * 2);
                     bulk_commit();
                     bulk_wait_read_all();   // the row is out of shared memory; y is written before the grid ends
                 }
@@ -790,9 +811,9 @@ __global__ void __launch_bounds__(kBM) s_prep_kernel(const float *S, int32_t s_c
     const int64_t pp = static_cast<int64_t>(m) * kBM + row;
     const bool valid = pp < p.M;
     const int tok = valid ? p.perm[pp] : 0;
-    if (p.adapter_scale && valid) {
+    if (p.layer[0].adapter_scale && valid) {
         const int id = p.ids[tok];
-        scale *= (id >= 0 && id < p.num_adapters) ? p.adapter_scale[id] : 0.f;
+        scale *= (id >= 0 && id < p.num_adapters) ? p.layer[0].adapter_scale[id] : 0.f;
     }
     for (int c = p.tile_chunk_off[m * p.num_slices]; c < p.tile_chunk_off[(m + 1) * p.num_slices]; ++c) {
         const int32_t rng = p.chunk_rng[c];
@@ -815,7 +836,7 @@ cudaError_t launch_s_prep(const float *S, int32_t s_cols, float scale, const TcP
 }
 
 template <int kXStages, int kWStages>
-static cudaError_t launch_tc_split(const TcMaps &maps, const TcParams &p, int grid, cudaStream_t stream)
+static cudaError_t launch_tc_split(const TcArgs &args, int grid, cudaStream_t stream)
 {
     constexpr size_t smem = tc_smem_bytes<kXStages, kWStages>();
     static int configured[64] = {0};
@@ -827,15 +848,14 @@ static cudaError_t launch_tc_split(const TcMaps &maps, const TcParams &p, int gr
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[dev] = 1;
     }
-    lora_tc_kernel<kXStages, kWStages><<<grid, kTcThreads, smem, stream>>>(maps.x, maps.w, maps.a, maps.b, maps.s,
-                                                                           maps.a32, maps.a48, maps.a64, p);
+    lora_tc_kernel<kXStages, kWStages><<<grid, kTcThreads, smem, stream>>>(args);
     return cudaGetLastError();
 }
 
-cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cudaStream_t stream)
+cudaError_t launch_tc(const TcArgs &args, int grid, cudaStream_t stream)
 {
-    if (p.mode == kModeMoe) return launch_tc_split<kXStagesMoe, kWStagesMoe>(maps, p, grid, stream);
-    return launch_tc_split<kXStagesLinear, kWStagesLinear>(maps, p, grid, stream);
+    if (args.p.mode == kModeMoe) return launch_tc_split<kXStagesMoe, kWStagesMoe>(args, grid, stream);
+    return launch_tc_split<kXStagesLinear, kWStagesLinear>(args, grid, stream);
 }
 
 }  // namespace lora

@@ -104,32 +104,57 @@ struct TcMaps {
     CUtensorMap a32, a48, a64;   // A pool with 32 / 48 / 64-row boxes (a: 16 rows)
 };
 
-struct TcParams {
-    int64_t M;
-    int32_t N, K, kblocks, num_mtiles, num_ntiles, group_m, mode, s_cols;
-    float scale;
-    int32_t num_adapters;
-    int32_t num_slices;        // output slices (>= 1); tile_chunk_off holds [tiles][slices] + 1 offsets
+// One layer of a tiled launch.  A launch covers up to kMaxLayers layers that
+// share one segment table (the same M, ids, adapters, ranks and slicing;
+// each its own K, N, weights and output); its work list runs every layer's
+// shrink items, then every layer's output tiles.
+constexpr int kMaxLayers = LORA_MAX_LAYERS;
+struct TcLayer {
+    int32_t N, K, kblocks, num_ntiles;
     int32_t slice_start[LORA_MAX_SLICES + 1];   // first output column of each slice
-    const int32_t *ids;        // lora_id_map (original token order); read when adapter_scale is set
-    int32_t topk;              // kModeMoe: pairs per token (a pair's token is pair / topk)
-    const int32_t *mt_expert;  // kModeMoe: the expert of each 128-row tile of the padded order
+    float scale;
     const float *adapter_scale;   // per-adapter factor on top of scale, or null (all 1)
     const uint16_t *bias;      // bf16 [N] or null
     const uint16_t *x;         // bf16 [M, K] (rows gathered by the loader warps)
     uint16_t *y;               // bf16 [M, N]
-    uint16_t *s_panels;        // bf16 [sets][chunks][128][16]
+    int32_t tile0;             // the layer's first output tile in the launch's list of output tiles
+};
+
+struct TcLayerMaps {
+    CUtensorMap x, w, a, b;
+    CUtensorMap a32, a48, a64;   // A pool with 32 / 48 / 64-row boxes (a: 16 rows)
+};
+
+struct TcParams {
+    int64_t M;
+    int32_t num_mtiles, group_m, mode, s_cols;
+    int32_t num_adapters;
+    int32_t num_slices;        // output slices (>= 1); tile_chunk_off holds [tiles][slices] + 1 offsets
+    int32_t num_layers;        // layers of this launch (1..kMaxLayers)
+    const int32_t *ids;        // lora_id_map (original token order); read when adapter_scale is set
+    int32_t topk;              // kModeMoe: pairs per token (a pair's token is pair / topk)
+    const int32_t *mt_expert;  // kModeMoe: the expert of each 128-row tile of the padded order
+    uint16_t *s_panels;        // bf16 [layers][sets][chunks][128][16]
     float *s_out;              // fp32 [M, s_cols] (shrink mode)
     const int32_t *perm, *offsets, *hdr;
     const int32_t *tile_chunk_off, *chunk_arow, *chunk_bpanel, *chunk_rng;
     const int32_t *sjob_tile, *sjob_c0, *sjob_c1, *tile_njobs;
-    int32_t *counters;
-    int32_t streamk;           // split the last partial wave of output tiles along K
+    int32_t *counters;         // S-ready counters [layers][tiles] at CNT_FIXED, their consumers after them
+    int32_t streamk;           // split the last partial wave of output tiles along K (one layer only)
     int32_t shrink_split;      // K pieces per shrink job; piece h writes S panel set h
     int32_t s_sets;            // S panel sets the expand steps add up (shrink_split, or 1 for expand)
     int32_t s_set_rows;        // rows of one S panel set (chunks x 128)
     float *sk_part;            // fp32 [CTAs][256/4][128][4]: each tail piece's partial sums, in its CTA's slot
     int32_t *sk_cnt;           // [tiles][kWinCntStride]: tail pieces stored per split tile (zero at rest)
+    TcLayer layer[kMaxLayers];
+};
+
+// Everything a tiled launch takes: each layer's tensor maps, the map of the
+// S panel scratch and the parameters (one __grid_constant__ argument).
+struct TcArgs {
+    TcLayerMaps maps[kMaxLayers];
+    CUtensorMap s;
+    TcParams p;
 };
 
 struct SplitParams {
@@ -210,7 +235,7 @@ struct ClusterParams {
 // ---- launchers (enqueue only; return the launch status) --------------------
 cudaError_t launch_seg_build(const SegParams &p, bool pdl, cudaStream_t stream);
 cudaError_t launch_moe_route(const RouteParams &p, cudaStream_t stream);
-cudaError_t launch_tc(const TcMaps &maps, const TcParams &p, int grid, cudaStream_t stream);
+cudaError_t launch_tc(const TcArgs &args, int grid, cudaStream_t stream);
 cudaError_t launch_moe_finalize(const uint16_t *out, const int32_t *expert, const float *weight, int64_t M, int topk,
                                 int E, int N, uint16_t *y, cudaStream_t stream);
 cudaError_t launch_s_prep(const float *S, int32_t s_cols, float scale, const TcParams &p, cudaStream_t stream);

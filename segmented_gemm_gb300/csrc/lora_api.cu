@@ -125,13 +125,14 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
                                            static_cast<size_t>(2 * present + 2) * 32) * T * 4;
         split_s = static_cast<size_t>(L.max_dchunks) * T * kChunk * 2;
     }
-    // per token tile: the tiled schedule's S-ready and consumer counters;
-    // per split-K tile: its arrival counter.  Sized for N >= 65536 so that
+    // per (layer, token tile): the tiled schedule's S-ready and consumer
+    // counters, for up to kMaxLayers layers of one launch; per split-K
+    // tile: its arrival counter.  Sized for N >= 65536 so that
     // the regions after it (the segment table) sit at offsets that depend
     // on M and A only: one table then serves layers of any K and N.
     const int NT_cnt = (std::max<int32_t>(N, 65536) + kSplitBN - 1) / kSplitBN;
     const size_t split_cnt = static_cast<size_t>(NT_cnt) + std::max<int>(RTmax, static_cast<int>(2 * present + 2));
-    L.n_counters = CNT_FIXED + std::max<size_t>(2 * L.num_mtiles, split_cnt) + 8;
+    L.n_counters = CNT_FIXED + std::max<size_t>(2 * static_cast<size_t>(kMaxLayers) * L.num_mtiles, split_cnt) + 8;
     // tiled schedule: S panels, one set per K piece of a shrink job (two for M > 128)
     const size_t tiled_s = static_cast<size_t>(L.max_chunks) * kBM * kChunk * 2 * tiled_s_sets(M);
     L.s_scratch_bytes = std::max(tiled_s, split_s);
@@ -308,21 +309,19 @@ static int prepare(const int32_t *ids, int64_t M, const lora_pool_t *pool, const
     return build ? enqueue_segments(ids, M, pool, *L, ws, stream) : LORA_OK;
 }
 
-static void fill_tc_params(TcParams &p, const WsLayout &L, void *ws, const lora_pool_t *pool, int64_t M)
+// The shared part of a tiled launch's parameters (the table, the workspace,
+// the S panel scratch at s_panels); the layers are filled by run_tiled.
+static void fill_tc_params(TcParams &p, const WsLayout &L, void *ws, const lora_pool_t *pool, int64_t M,
+                           uint16_t *s_panels)
 {
     std::memset(&p, 0, sizeof p);
     p.M = M;
     p.num_adapters = pool->num_adapters;
-    p.adapter_scale = pool->num_adapters ? pool->adapter_scale : nullptr;
     p.num_slices = pool->num_slices > 1 ? pool->num_slices : 1;
-    for (int s = 0; s <= LORA_MAX_SLICES; ++s) p.slice_start[s] = s <= p.num_slices && p.num_slices > 1 ? pool->slice_start[s] : 0;
-    p.N = pool->N;
-    p.K = pool->K;
-    p.kblocks = (pool->K + kBK - 1) / kBK;
+    p.num_layers = 1;
     p.num_mtiles = L.num_mtiles;
-    p.num_ntiles = (pool->N + kBN - 1) / kBN;
     p.group_m = 8;
-    p.s_panels = at<uint16_t>(ws, L.s_scratch);
+    p.s_panels = s_panels;
     p.perm = at<int32_t>(ws, L.perm);
     p.offsets = at<int32_t>(ws, L.offsets);
     p.hdr = at<int32_t>(ws, L.hdr);
@@ -335,20 +334,32 @@ static void fill_tc_params(TcParams &p, const WsLayout &L, void *ws, const lora_
     p.sjob_c1 = at<int32_t>(ws, L.sjob_c1);
     p.tile_njobs = at<int32_t>(ws, L.tile_njobs);
     p.counters = at<int32_t>(ws, L.counters);
-    // two K halves per shrink job when each half keeps 8 K blocks or more
-    // and the output tiles fill at most four waves of the grid: the first
-    // wave of output tiles then finds S ready when its own K loops end (a
-    // wait that matters only while there are few waves).  Each half writes
-    // its own S panel set; the expand steps add both, (S_a + S_b) B^T =
-    // S_a B^T + S_b B^T, in the fp32 accumulator.
-    const int64_t n_out = static_cast<int64_t>(p.num_mtiles) * p.num_ntiles;
-    p.shrink_split = (tiled_s_sets(M) == 2 && p.kblocks >= 16 && n_out <= 4 * num_sms_current_device()) ? 2 : 1;
-    p.s_sets = p.shrink_split;
+    p.shrink_split = 1;
+    p.s_sets = 1;
     p.s_set_rows = L.max_chunks * kBM;
 }
 
+// Layer l of a tiled launch.
+static void fill_tc_layer(TcLayer &Ly, const lora_pool_t *pool, const lora_bf16_t *x, const lora_bf16_t *bias,
+                          float scale, lora_bf16_t *y)
+{
+    std::memset(&Ly, 0, sizeof Ly);
+    Ly.N = pool->N;
+    Ly.K = pool->K;
+    Ly.kblocks = (pool->K + kBK - 1) / kBK;
+    Ly.num_ntiles = (pool->N + kBN - 1) / kBN;
+    const int S = pool->num_slices > 1 ? pool->num_slices : 1;
+    for (int s = 0; s <= LORA_MAX_SLICES; ++s) Ly.slice_start[s] = s <= S && S > 1 ? pool->slice_start[s] : 0;
+    Ly.scale = scale;
+    Ly.adapter_scale = pool->num_adapters ? pool->adapter_scale : nullptr;
+    Ly.bias = bias;
+    Ly.x = x;
+    Ly.y = y;
+}
+
 // Maps shared by the schedules: A pool (16-row boxes), B pool (16-col panels).
-static bool encode_pool_maps(TcMaps &m, const lora_pool_t *pool, const void *dummy, uint32_t b_rows_box)
+template <typename Maps>
+static bool encode_pool_maps(Maps &m, const lora_pool_t *pool, const void *dummy, uint32_t b_rows_box)
 {
     const uint64_t K = pool->K;
     if (pool->num_adapters > 0) {
@@ -372,51 +383,94 @@ static bool encode_pool_maps(TcMaps &m, const lora_pool_t *pool, const void *dum
     return true;
 }
 
-static int run_tiled(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
-                     const int32_t *ids, const lora_pool_t *pool, float scale, lora_bf16_t *y, void *ws, size_t ws_bytes, const WsLayout &L,
-                     int mode, float *s_out, int32_t s_cols, const float *s_in, cudaStream_t stream)
+// One layer of a tiled launch as the caller gives it.
+struct LayerCall {
+    const lora_bf16_t *x, *W, *bias;
+    const lora_pool_t *pool;
+    float scale;
+    lora_bf16_t *y;
+};
+
+// The tiled schedule over nl layers that share the segment table in ws:
+// one launch whose work list runs every layer's shrink items, then every
+// layer's output tiles.  The layers' S panel sets start at s_panels
+// (nl x tiled_s_sets(M) sets).  Stream-K (splitting a partial last wave
+// along K) is used by one-layer fused calls only.
+static int run_tiled(const LayerCall *lc, int nl, int64_t M, const int32_t *ids, void *ws, size_t ws_bytes,
+                     const WsLayout &L, int mode, float *s_out, int32_t s_cols, const float *s_in, uint16_t *s_panels,
+                     cudaStream_t stream)
 {
-    TcParams p;
-    fill_tc_params(p, L, ws, pool, M);
+    TcArgs a;
+    std::memset(&a, 0, sizeof a);
+    TcParams &p = a.p;
+    fill_tc_params(p, L, ws, lc[0].pool, M, s_panels);
+    p.num_layers = nl;
+    const int sms = num_sms_current_device();
+    int64_t n_out = 0;
+    bool long_k = true;
+    for (int l = 0; l < nl; ++l) {
+        fill_tc_layer(p.layer[l], lc[l].pool, lc[l].x, lc[l].bias, lc[l].scale, lc[l].y);
+        p.layer[l].tile0 = static_cast<int32_t>(n_out);
+        n_out += static_cast<int64_t>(p.num_mtiles) * p.layer[l].num_ntiles;
+        long_k = long_k && p.layer[l].kblocks >= 16;
+    }
+    // two K halves per shrink job when each half keeps 8 K blocks or more
+    // and the output tiles fill at most four waves of the grid: the first
+    // wave of output tiles then finds S ready when its own K loops end (a
+    // wait that matters only while there are few waves).  Each half writes
+    // its own S panel set; the expand steps add both, (S_a + S_b) B^T =
+    // S_a B^T + S_b B^T, in the fp32 accumulator.
+    p.shrink_split = (tiled_s_sets(M) == 2 && long_k && n_out <= 4 * sms) ? 2 : 1;
+    p.s_sets = p.shrink_split;
     // stream-K for the last partial wave: the fused layer only, when the
     // workspace holds the partial-sum scratch and the grid fits its tiles
-    const int sms_sk = num_sms_current_device();
-    if (mode == kModeLinear && L.sk_part && ws_bytes >= L.total && sms_sk <= kStreamKMaxTiles) {
+    if (mode == kModeLinear && nl == 1 && L.sk_part && ws_bytes >= L.total && sms <= kStreamKMaxTiles) {
         p.streamk = 1;
         p.sk_part = at<float>(ws, L.sk_part);
         p.sk_cnt = at<int32_t>(ws, L.sk_cnt);
     }
     p.mode = mode;
     p.ids = ids;
-    if (mode == kModeShrink) p.adapter_scale = nullptr;   // S leaves unscaled
+    if (mode == kModeShrink) p.layer[0].adapter_scale = nullptr;   // S leaves unscaled
     if (mode == kModeExpand) p.s_sets = 1;   // the caller's S, prepared as one panel set
-    p.scale = scale;
-    p.bias = bias;
-    p.x = x;
-    p.y = y;
     p.s_out = s_out;
     p.s_cols = s_cols;
-    const uint64_t K = pool->K, N = pool->N;
-    TcMaps m;
-    const void *xsrc = x ? static_cast<const void *>(x) : static_cast<const void *>(p.s_panels);
-    const uint64_t xrows = x ? static_cast<uint64_t>(M) : 1;
-    if (!encode_2d(&m.x, xsrc, K, xrows, K * 2, kBK, 1, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ERR_CUDA;
-    const void *wsrc = W ? static_cast<const void *>(W) : xsrc;
-    if (!encode_2d(&m.w, wsrc, K, W ? N : 1, K * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ERR_CUDA;
-    if (!encode_pool_maps(m, pool, p.s_panels, kBN)) return LORA_ERR_CUDA;
-    if (!encode_2d(&m.s, p.s_panels, kChunk, static_cast<uint64_t>(L.max_chunks) * kBM * tiled_s_sets(M), kChunk * 2,
-                   kChunk, kBM, CU_TENSOR_MAP_SWIZZLE_32B))
+    for (int l = 0; l < nl; ++l) {
+        const lora_pool_t *pool = lc[l].pool;
+        const uint64_t K = pool->K, N = pool->N;
+        TcLayerMaps &m = a.maps[l];
+        const void *xsrc = lc[l].x ? static_cast<const void *>(lc[l].x) : static_cast<const void *>(s_panels);
+        const uint64_t xrows = lc[l].x ? static_cast<uint64_t>(M) : 1;
+        if (!encode_2d(&m.x, xsrc, K, xrows, K * 2, kBK, 1, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ERR_CUDA;
+        const void *wsrc = lc[l].W ? static_cast<const void *>(lc[l].W) : xsrc;
+        if (!encode_2d(&m.w, wsrc, K, lc[l].W ? N : 1, K * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B))
+            return LORA_ERR_CUDA;
+        if (!encode_pool_maps(m, pool, s_panels, kBN)) return LORA_ERR_CUDA;
+    }
+    const uint64_t s_rows = static_cast<uint64_t>(nl) * tiled_s_sets(M) * L.max_chunks * kBM;
+    if (!encode_2d(&a.s, s_panels, kChunk, s_rows, kChunk * 2, kChunk, kBM, CU_TENSOR_MAP_SWIZZLE_32B))
         return LORA_ERR_CUDA;
     if (mode == kModeExpand) {
-        if (launch_s_prep(s_in, s_cols, scale, p, stream) != cudaSuccess) return LORA_ERR_CUDA;
+        if (launch_s_prep(s_in, s_cols, lc[0].scale, p, stream) != cudaSuccess) return LORA_ERR_CUDA;
     }
-    const int sms = num_sms_current_device();
     int64_t jobs = 0;
-    if (mode != kModeShrink) jobs += static_cast<int64_t>(p.num_mtiles) * p.num_ntiles;
-    if (mode != kModeExpand) jobs += static_cast<int64_t>(L.max_sjobs) * p.shrink_split;
+    if (mode != kModeShrink) jobs += n_out;
+    if (mode != kModeExpand) jobs += static_cast<int64_t>(L.max_sjobs) * p.shrink_split * nl;
     // with stream-K the last partial wave is shared out over every SM
     const int grid = p.streamk ? sms : static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(sms, jobs)));
-    return launch_tc(m, p, grid, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+    return launch_tc(a, grid, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
+// One layer (lora_linear, lora_shrink, lora_expand), S panels in the
+// workspace's own scratch.
+static int run_tiled(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
+                     const int32_t *ids, const lora_pool_t *pool, float scale, lora_bf16_t *y, void *ws,
+                     size_t ws_bytes, const WsLayout &L, int mode, float *s_out, int32_t s_cols, const float *s_in,
+                     cudaStream_t stream)
+{
+    const LayerCall lc = {x, W, bias, pool, scale, y};
+    return run_tiled(&lc, 1, M, ids, ws, ws_bytes, L, mode, s_out, s_cols, s_in, at<uint16_t>(ws, L.s_scratch),
+                     stream);
 }
 
 static int run_splitk(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
@@ -684,28 +738,30 @@ int lora_moe_gemm(const lora_bf16_t *x, int64_t M, int32_t K, const lora_bf16_t 
     const MoeLayout L = make_moe_layout(M, topk, num_experts);
     if (!ws || ws_bytes < L.total) return LORA_ERR_WORKSPACE;
     if (!device_supported()) return LORA_ERR_UNSUPPORTED;
-    TcParams p;
-    std::memset(&p, 0, sizeof p);
+    TcArgs a;
+    std::memset(&a, 0, sizeof a);
+    TcParams &p = a.p;
     p.M = static_cast<int64_t>(L.max_mtiles) * kBM;   // positions of the padded order
-    p.N = N;
-    p.K = K;
-    p.kblocks = (K + kBK - 1) / kBK;
     p.num_mtiles = L.max_mtiles;                      // an upper bound: the kernel reads the routing's count
-    p.num_ntiles = (N + kBN - 1) / kBN;
+    p.num_layers = 1;
+    p.layer[0].N = N;
+    p.layer[0].K = K;
+    p.layer[0].kblocks = (K + kBK - 1) / kBK;
+    p.layer[0].num_ntiles = (N + kBN - 1) / kBN;
+    p.layer[0].scale = 1.f;
+    p.layer[0].x = x;
+    p.layer[0].y = out;
     p.group_m = 8;
     p.mode = kModeMoe;
-    p.scale = 1.f;
     p.num_slices = 1;
     p.topk = topk;
-    p.x = x;
-    p.y = out;
     p.perm = at<int32_t>(ws, L.perm_pad);
     p.hdr = at<int32_t>(ws, L.hdr);
     p.counters = at<int32_t>(ws, L.counters);
     p.mt_expert = at<int32_t>(ws, L.mt_expert);
     p.shrink_split = 1;
     p.s_sets = 1;
-    TcMaps m;
+    TcLayerMaps &m = a.maps[0];
     const uint64_t Kq = K;
     if (!encode_2d(&m.x, x, Kq, static_cast<uint64_t>(M), Kq * 2, kBK, 1, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ERR_CUDA;
     // the experts' weights stacked: [E * N, K]
@@ -716,9 +772,9 @@ int lora_moe_gemm(const lora_bf16_t *x, int64_t M, int32_t K, const lora_bf16_t 
     none.K = K;
     none.N = N;
     if (!encode_pool_maps(m, &none, W, kBN)) return LORA_ERR_CUDA;
-    if (!encode_2d(&m.s, W, kChunk, 1, kChunk * 2, kChunk, kBM, CU_TENSOR_MAP_SWIZZLE_32B)) return LORA_ERR_CUDA;
-    return launch_tc(m, p, num_sms_current_device(), static_cast<cudaStream_t>(stream)) == cudaSuccess ? LORA_OK
-                                                                                                       : LORA_ERR_CUDA;
+    if (!encode_2d(&a.s, W, kChunk, 1, kChunk * 2, kChunk, kBM, CU_TENSOR_MAP_SWIZZLE_32B)) return LORA_ERR_CUDA;
+    return launch_tc(a, num_sms_current_device(), static_cast<cudaStream_t>(stream)) == cudaSuccess ? LORA_OK
+                                                                                                    : LORA_ERR_CUDA;
 }
 
 int lora_moe_finalize(const lora_bf16_t *out, const int32_t *expert, const float *weight, int64_t M, int32_t topk,
@@ -849,6 +905,74 @@ int lora_linear(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lor
                 lora_bf16_t *y, void *ws, size_t ws_bytes, lora_stream_t stream)
 {
     return lora_linear_ex(x, M, W, bias, lora_id_map, pool, scale, segs, y, ws, ws_bytes, stream, LORA_PATH_AUTO);
+}
+
+// ---- several layers in one launch -------------------------------------------
+// Workspace of lora_linear_layers: the one-layer layout for the largest N
+// (everything but the stream-K scratch), then the S panel sets of every layer.
+static size_t layers_s_offset(const WsLayout &L) { return (L.total_min + 1023) & ~size_t(1023); }
+static size_t layers_s_bytes(const WsLayout &L, int nl)
+{
+    return static_cast<size_t>(nl) * tiled_s_sets(L.M) * L.max_chunks * kBM * kChunk * 2;
+}
+
+size_t lora_layers_workspace_size(int64_t M, int32_t max_N, int32_t num_adapters, int32_t num_layers)
+{
+    if (M < 0 || M > kMaxTokens || max_N <= 0 || num_adapters < 0 || num_adapters > LORA_MAX_ADAPTERS) return 0;
+    if (num_layers < 1 || num_layers > LORA_MAX_LAYERS) return 0;
+    const WsLayout L = make_ws_layout(M, max_N, num_adapters);
+    return layers_s_offset(L) + layers_s_bytes(L, num_layers);
+}
+
+int lora_linear_layers(const lora_layer_t *layers, int32_t num_layers, int64_t M, const int32_t *lora_id_map,
+                       const lora_segments_t *segs, void *ws, size_t ws_bytes, lora_stream_t stream)
+{
+    if (!layers) return LORA_ERR_NULL;
+    if (num_layers < 1 || num_layers > LORA_MAX_LAYERS || M < 0 || M > kMaxTokens) return LORA_ERR_SHAPE;
+    // every layer: a valid pool holding the same adapters with the same
+    // ranks and slicing as layer 0's (what one segment table can describe)
+    const lora_pool_t *p0 = layers[0].pool;
+    int32_t max_N = 0;
+    bool factors = false;
+    for (int l = 0; l < num_layers; ++l) {
+        const lora_pool_t *pl = layers[l].pool;
+        int rc = check_pool(pl);
+        if (rc) return rc;
+        if (pl->num_adapters != p0->num_adapters || pl->max_rank != p0->max_rank ||
+            (pl->num_slices > 1 ? pl->num_slices : 1) != (p0->num_slices > 1 ? p0->num_slices : 1))
+            return LORA_ERR_SHAPE;
+        if (pl->num_adapters &&
+            (pl->a_elems / pl->K != p0->a_elems / p0->K || pl->b_elems / pl->N != p0->b_elems / p0->N))
+            return LORA_ERR_SHAPE;
+        max_N = std::max(max_N, pl->N);
+        factors = factors || (pl->num_adapters && pl->adapter_scale);
+    }
+    if (M == 0) return LORA_OK;
+    for (int l = 0; l < num_layers; ++l) {
+        const lora_layer_t &ly = layers[l];
+        if (!ly.x || !ly.W || !ly.y) return LORA_ERR_NULL;
+        if (!aligned16(ly.x) || !aligned16(ly.W) || !aligned16(ly.y) || (ly.bias && !aligned16(ly.bias)))
+            return LORA_ERR_ALIGN;
+    }
+    if ((!segs || factors) && !lora_id_map) return LORA_ERR_NULL;   // the table is built from it; factors look it up
+    if (!ws) return LORA_ERR_WORKSPACE;
+    if (!device_supported()) return LORA_ERR_UNSUPPORTED;
+    const WsLayout L = make_ws_layout(M, max_N, p0->num_adapters);
+    if (ws_bytes < layers_s_offset(L) + layers_s_bytes(L, num_layers)) return LORA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (segs) {
+        if (segs->plan != ws || segs->M != M || segs->num_adapters != p0->num_adapters ||
+            segs->num_slices != (p0->num_slices > 1 ? p0->num_slices : 1) || segs->perm != at<int32_t>(ws, L.perm))
+            return LORA_ERR_SEGMENTS;
+    } else {
+        int rc = enqueue_segments(lora_id_map, M, p0, L, ws, s);
+        if (rc) return rc;
+    }
+    LayerCall lc[LORA_MAX_LAYERS];
+    for (int l = 0; l < num_layers; ++l)
+        lc[l] = {layers[l].x, layers[l].W, layers[l].bias, layers[l].pool, layers[l].scale, layers[l].y};
+    return run_tiled(lc, num_layers, M, lora_id_map, ws, ws_bytes, L, kModeLinear, nullptr, 0, nullptr,
+                     at<uint16_t>(ws, layers_s_offset(L)), s);
 }
 
 int lora_shrink(const lora_bf16_t *x, int64_t M, const int32_t *lora_id_map, const lora_pool_t *pool,

@@ -26,12 +26,13 @@ LORA_DEV_BAD_ID, LORA_DEV_TIMEOUT, LORA_DEV_BAD_POOL = 1, 2, 4
 LORA_PATH_AUTO, LORA_PATH_TILED, LORA_PATH_SPLITK, LORA_PATH_STREAM = 0, 1, 2, 3
 LORA_FLAG_STATIC_WEIGHTS = 0x100
 LORA_MAX_SLICES = 4
+LORA_MAX_LAYERS = 8
 LORA_MAX_RANK, LORA_RANK_ALIGN, LORA_MAX_ADAPTERS = 128, 16, 1024
 
 EXPORTS = ("lora_pool_layout", "lora_workspace_size", "lora_workspace_init", "lora_build_segments",
            "lora_shrink", "lora_expand", "lora_linear", "lora_linear_ex", "lora_get_status",
            "lora_status_string", "lora_linear_noalloc", "lora_moe_workspace_size", "lora_moe_route",
-           "lora_moe_gemm", "lora_moe_finalize", "lora_moe")
+           "lora_moe_gemm", "lora_moe_finalize", "lora_moe", "lora_layers_workspace_size", "lora_linear_layers")
 
 
 class lora_pool_t(ctypes.Structure):
@@ -49,6 +50,11 @@ class lora_segments_t(ctypes.Structure):
                 ("seg_len", ctypes.c_void_p), ("seg_rank", ctypes.c_void_p),
                 ("num_segments", ctypes.c_void_p), ("plan", ctypes.c_void_p),
                 ("M", ctypes.c_int64), ("num_adapters", ctypes.c_int32), ("num_slices", ctypes.c_int32)]
+
+
+class lora_layer_t(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("W", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("pool", ctypes.c_void_p), ("scale", ctypes.c_float), ("y", ctypes.c_void_p)]
 
 
 class LoraError(RuntimeError):
@@ -88,6 +94,8 @@ def load_library():
         "lora_moe_gemm": (ctypes.c_int, [P, I64, I32, P, I32, I32, I32, P, P, SZ, P]),
         "lora_moe_finalize": (ctypes.c_int, [P, P, P, I64, I32, I32, I32, P, P]),
         "lora_moe": (ctypes.c_int, [P, I64, I32, P, I32, P, P, I32, I32, P, P, P, SZ, P]),
+        "lora_layers_workspace_size": (SZ, [I64, I32, I32, I32]),
+        "lora_linear_layers": (ctypes.c_int, [P, I32, I64, P, PS, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -281,6 +289,43 @@ def lora_linear(x: torch.Tensor, W: torch.Tensor, bias: Optional[torch.Tensor], 
         ctypes.byref(segs) if segs is not None else None, _ptr(y), ws.ptr, ws.nbytes,
         _stream(stream), int(path) | (LORA_FLAG_STATIC_WEIGHTS if static_weights else 0)), "lora_linear")
     return y
+
+
+def lora_layers_workspace_size(M: int, max_N: int, num_adapters: int, num_layers: int) -> int:
+    return int(load_library().lora_layers_workspace_size(M, max_N, num_adapters, num_layers))
+
+
+class LayersWorkspace(Workspace):
+    """A zero-initialised device workspace for lora_linear_layers."""
+
+    def __init__(self, M: int, max_N: int, num_adapters: int, num_layers: int, device="cuda"):
+        self.nbytes = lora_layers_workspace_size(M, max_N, num_adapters, num_layers)
+        self.buf = torch.zeros(max(self.nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def lora_linear_layers(layers: Sequence[tuple], ids: torch.Tensor, ws: Workspace,
+                       segs: Optional[lora_segments_t] = None, stream=None) -> List[torch.Tensor]:
+    """Several LoRA layers of one step in one launch.  ``layers``: tuples
+    (x, W, bias, pool, scale) or (x, W, bias, pool, scale, y); returns the
+    outputs y_l = x_l W_l^T + bias_l + scale_l (x_l A_id^T) B_id^T."""
+    n = len(layers)
+    arr = (lora_layer_t * max(n, 1))()
+    outs, keep = [], []
+    for i, ly in enumerate(layers):
+        x, W, bias, pool, scale = ly[:5]
+        y = ly[5] if len(ly) > 5 and ly[5] is not None else torch.empty(x.shape[0], W.shape[0],
+                                                                        dtype=torch.bfloat16, device=x.device)
+        arr[i].x, arr[i].W = x.data_ptr(), W.data_ptr()
+        arr[i].bias = None if bias is None else bias.data_ptr()
+        arr[i].pool = ctypes.addressof(pool.desc)
+        arr[i].scale = float(scale)
+        arr[i].y = y.data_ptr()
+        outs.append(y)
+        keep.append(pool)
+    M = layers[0][0].shape[0] if n else 0
+    _check(load_library().lora_linear_layers(arr, n, M, _ptr(ids), ctypes.byref(segs) if segs is not None else None,
+                                             ws.ptr, ws.nbytes, _stream(stream)), "lora_linear_layers")
+    return outs
 
 
 def lora_shrink(x: torch.Tensor, ids: torch.Tensor, pool: LoraPool, ws: Workspace,
