@@ -26,7 +26,14 @@
  * Adapter storage here is the oracle's own, deliberately naive layout:
  * adapter i's A_i [r_i, K] row-major starts right after A_{i-1}, and
  * B_i [N, r_i] row-major starts right after B_{i-1}, using TRUE ranks.
+ *
+ * Adapters may also be given as 8-bit floats (e4m3) with one fp64 dequant
+ * factor per adapter and factor: A_i = a_deq_i * e4m3(a), B_i = b_deq_i *
+ * e4m3(b) (the *_e4m3 functions; this project's extension, the page stores
+ * adapters in the model's own precision).  The 8-bit codes are decoded
+ * exactly from the format's definition (oracle_e4m3_to_f64).
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -371,5 +378,118 @@ void oracle_moe_rows(const uint16_t *x, int64_t M, int64_t K, const uint16_t *W,
             }
         }
         free(xr);
+    }
+}
+
+/*
+ * e4m3, the 8-bit float with 1 sign bit, 4 exponent bits (bias 7) and 3
+ * mantissa bits, no infinities (OCP 8-bit floating point, "E4M3"):
+ *   exponent field e = 0:      (-1)^s * (m / 8) * 2^-6          (subnormal)
+ *   e = 1..15:                 (-1)^s * (1 + m / 8) * 2^(e - 7)
+ *   e = 15 with m = 7:         NaN (the largest finite value is 448)
+ */
+double oracle_e4m3_to_f64(uint8_t v)
+{
+    int s = v >> 7, e = (v >> 3) & 15, m = v & 7;
+    if (e == 15 && m == 7) return NAN;
+    double mag = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+/*
+ * oracle_lora_linear_rows with e4m3 adapters: the same layer, with
+ *   A_i[j,k] = deq[2i] * e4m3(a8_i[j,k]),  B_i[n,j] = deq[2i+1] * e4m3(b8_i[n,j])
+ * (a8_cat / b8_cat in the oracle's concatenated true-rank layout, one byte
+ * per element; deq: [num_adapters][2] fp64).
+ */
+void oracle_lora_linear_rows_e4m3(const uint16_t *x, int64_t M, int64_t K,
+                                  const uint16_t *W, int64_t N, const uint16_t *bias,
+                                  const int32_t *ids, int32_t num_adapters, const int32_t *rank,
+                                  const uint8_t *a8_cat, const uint8_t *b8_cat, const double *deq, double scale,
+                                  const double *adapter_scale, const int64_t *rows, int64_t nrows, double *y)
+{
+    (void)M;
+#pragma omp parallel
+    {
+        double *xr = (double *)malloc((size_t)K * sizeof(double));
+        double *S = (double *)malloc(64 * 1024 * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t q = 0; q < nrows; ++q) {
+            int64_t t = rows ? rows[q] : q;
+            for (int64_t k = 0; k < K; ++k) xr[k] = bf16_to_f64(x[t * K + k]);
+            double *yr = y + q * N;
+            for (int64_t n = 0; n < N; ++n) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k) acc += xr[k] * bf16_to_f64(W[n * K + k]);
+                if (bias) acc += bf16_to_f64(bias[n]);
+                yr[n] = acc;
+            }
+            int32_t i = effective_id(ids[t], num_adapters);
+            if (i < 0) continue;
+            int64_t r = rank[i];
+            const uint8_t *Ai = a8_cat + a_start(rank, i, K);
+            const uint8_t *Bi = b8_cat + b_start(rank, i, N);
+            for (int64_t j = 0; j < r; ++j) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k) acc += xr[k] * (deq[2 * i] * oracle_e4m3_to_f64(Ai[j * K + k]));
+                S[j] = acc;
+            }
+            double si = adapter_scale ? adapter_scale[i] : 1.0;
+            for (int64_t n = 0; n < N; ++n) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < r; ++j) acc += S[j] * (deq[2 * i + 1] * oracle_e4m3_to_f64(Bi[n * r + j]));
+                yr[n] += scale * si * acc;
+            }
+        }
+        free(xr);
+        free(S);
+    }
+}
+
+/* oracle_shrink_rows with e4m3 adapters (A_i as in oracle_lora_linear_rows_e4m3). */
+void oracle_shrink_rows_e4m3(const uint16_t *x, int64_t M, int64_t K, const int32_t *ids,
+                             int32_t num_adapters, const int32_t *rank, const uint8_t *a8_cat, const double *deq,
+                             const int64_t *rows, int64_t nrows, int64_t s_cols, double *S)
+{
+    (void)M;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t q = 0; q < nrows; ++q) {
+        int64_t t = rows ? rows[q] : q;
+        double *Sr = S + q * s_cols;
+        for (int64_t j = 0; j < s_cols; ++j) Sr[j] = 0.0;
+        int32_t i = effective_id(ids[t], num_adapters);
+        if (i < 0) continue;
+        const uint8_t *Ai = a8_cat + a_start(rank, i, K);
+        for (int64_t j = 0; j < rank[i] && j < s_cols; ++j) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += bf16_to_f64(x[t * K + k]) * (deq[2 * i] * oracle_e4m3_to_f64(Ai[j * K + k]));
+            Sr[j] = acc;
+        }
+    }
+}
+
+/* oracle_expand_rows with e4m3 adapters (B_i as in oracle_lora_linear_rows_e4m3). */
+void oracle_expand_rows_e4m3(const float *S, int64_t s_cols, const uint16_t *y_in, int64_t N,
+                             const int32_t *ids, int32_t num_adapters, const int32_t *rank,
+                             const uint8_t *b8_cat, const double *deq, double scale, const double *adapter_scale,
+                             const int64_t *rows, int64_t nrows, double *y)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t q = 0; q < nrows; ++q) {
+        int64_t t = rows ? rows[q] : q;
+        double *yr = y + q * N;
+        for (int64_t n = 0; n < N; ++n) yr[n] = bf16_to_f64(y_in[t * N + n]);
+        int32_t i = effective_id(ids[t], num_adapters);
+        if (i < 0) continue;
+        int64_t r = rank[i];
+        const uint8_t *Bi = b8_cat + b_start(rank, i, N);
+        double si = adapter_scale ? adapter_scale[i] : 1.0;
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < r && j < s_cols; ++j)
+                acc += (double)S[t * s_cols + j] * (deq[2 * i + 1] * oracle_e4m3_to_f64(Bi[n * r + j]));
+            yr[n] += scale * si * acc;
+        }
     }
 }

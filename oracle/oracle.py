@@ -65,6 +65,14 @@ def _load():
         lib.oracle_moe_rows.argtypes = [p, i64, i64, p, i64, i32, i32, p, p, p, i64, p]
         lib.oracle_expand_rows.restype = None
         lib.oracle_expand_rows.argtypes = [p, i64, p, i64, p, i32, p, p, dbl, p, p, i64, p]
+        lib.oracle_e4m3_to_f64.restype = dbl
+        lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_lora_linear_rows_e4m3.restype = None
+        lib.oracle_lora_linear_rows_e4m3.argtypes = [p, i64, i64, p, i64, p, p, i32, p, p, p, p, dbl, p, p, i64, p]
+        lib.oracle_shrink_rows_e4m3.restype = None
+        lib.oracle_shrink_rows_e4m3.argtypes = [p, i64, i64, p, i32, p, p, p, p, i64, i64, p]
+        lib.oracle_expand_rows_e4m3.restype = None
+        lib.oracle_expand_rows_e4m3.argtypes = [p, i64, p, i64, p, i32, p, p, p, dbl, p, p, i64, p]
         _lib = lib
     return _lib
 
@@ -97,6 +105,24 @@ def _adapter_scale(wl) -> Optional[np.ndarray]:
     a = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
     assert a.shape == (len(wl.ranks),)
     return a
+
+
+def _codes(mats: List[torch.Tensor]) -> np.ndarray:
+    """e4m3 codes (uint8 tensors) concatenated in the oracle's layout."""
+    if not mats:
+        return np.zeros(1, dtype=np.uint8)
+    return np.ascontiguousarray(torch.cat([m.reshape(-1) for m in mats]).numpy().astype(np.uint8))
+
+
+def _deq(wl) -> np.ndarray:
+    """fp64 [num_adapters][2] dequant factors (A, B) of an e4m3 workload."""
+    d = np.ascontiguousarray(np.asarray(wl.deq or [(1.0, 1.0)], dtype=np.float64).reshape(-1))
+    return d
+
+
+def e4m3_to_f64(code: int) -> float:
+    """The oracle's decode of one e4m3 code."""
+    return float(_load().oracle_e4m3_to_f64(int(code) & 0xFF))
 
 
 def _concat(mats: List[torch.Tensor], K_or_N: int) -> np.ndarray:
@@ -145,6 +171,8 @@ def lora_linear(wl, rows=None, scale: Optional[float] = None) -> np.ndarray:
     selects output rows; returns [len(rows), N]."""
     if getattr(wl, "slices", None):
         return _lora_linear_slices(wl, rows, scale)
+    if getattr(wl, "A8", None) is not None:
+        return _lora_linear_e4m3(wl, rows, scale)
     lib = _load()
     x, W, bias = _bits(wl.x), _bits(wl.W), _bits(wl.bias)
     ids = np.ascontiguousarray(wl.ids.numpy().astype(np.int32))
@@ -157,6 +185,22 @@ def lora_linear(wl, rows=None, scale: Optional[float] = None) -> np.ndarray:
     lib.oracle_lora_linear_rows(_ptr(x), wl.M, wl.K, _ptr(W), wl.N, _ptr(bias), _ptr(ids),
                                 len(wl.ranks), _ptr(rk), _ptr(a_cat), _ptr(b_cat), float(s),
                                 _ptr(asc), _ptr(r), nrows, _ptr(y))
+    return y
+
+
+def _lora_linear_e4m3(wl, rows, scale):
+    """e4m3 adapters: A_i = deq_a,i e4m3(A8_i), B_i = deq_b,i e4m3(B8_i)."""
+    lib = _load()
+    x, W, bias = _bits(wl.x), _bits(wl.W), _bits(wl.bias)
+    ids = np.ascontiguousarray(wl.ids.numpy().astype(np.int32))
+    rk = np.ascontiguousarray(np.asarray(list(wl.ranks) or [0], dtype=np.int32))
+    a8, b8, deq = _codes(wl.A8), _codes(wl.B8), _deq(wl)
+    r, nrows = _rows_arg(rows, wl.M)
+    y = np.zeros((nrows, wl.N), dtype=np.float64)
+    s = wl.scale if scale is None else scale
+    lib.oracle_lora_linear_rows_e4m3(_ptr(x), wl.M, wl.K, _ptr(W), wl.N, _ptr(bias), _ptr(ids), len(wl.ranks),
+                                     _ptr(rk), _ptr(a8), _ptr(b8), _ptr(deq), float(s), _ptr(_adapter_scale(wl)),
+                                     _ptr(r), nrows, _ptr(y))
     return y
 
 
@@ -227,9 +271,13 @@ def shrink(wl, s_cols: int, rows=None) -> np.ndarray:
     x = _bits(wl.x)
     ids = np.ascontiguousarray(wl.ids.numpy().astype(np.int32))
     rk = np.ascontiguousarray(np.asarray(list(wl.ranks) or [0], dtype=np.int32))
-    a_cat = _concat(wl.A, wl.K)
     r, nrows = _rows_arg(rows, wl.M)
     S = np.zeros((nrows, s_cols), dtype=np.float64)
+    if getattr(wl, "A8", None) is not None:
+        lib.oracle_shrink_rows_e4m3(_ptr(x), wl.M, wl.K, _ptr(ids), len(wl.ranks), _ptr(rk), _ptr(_codes(wl.A8)),
+                                    _ptr(_deq(wl)), _ptr(r), nrows, s_cols, _ptr(S))
+        return S
+    a_cat = _concat(wl.A, wl.K)
     lib.oracle_shrink_rows(_ptr(x), wl.M, wl.K, _ptr(ids), len(wl.ranks), _ptr(rk),
                            _ptr(a_cat), _ptr(r), nrows, s_cols, _ptr(S))
     return S
@@ -243,11 +291,16 @@ def expand(wl, S: torch.Tensor, y_in: torch.Tensor, scale: Optional[float] = Non
     yin = _bits(y_in)
     ids = np.ascontiguousarray(wl.ids.numpy().astype(np.int32))
     rk = np.ascontiguousarray(np.asarray(list(wl.ranks) or [0], dtype=np.int32))
-    b_cat = _concat(wl.B, wl.N)
     r, nrows = _rows_arg(rows, wl.M)
     y = np.zeros((nrows, wl.N), dtype=np.float64)
     s = wl.scale if scale is None else scale
     asc = _adapter_scale(wl)
+    if getattr(wl, "A8", None) is not None:
+        lib.oracle_expand_rows_e4m3(_ptr(S_np), S_np.shape[1], _ptr(yin), wl.N, _ptr(ids), len(wl.ranks), _ptr(rk),
+                                    _ptr(_codes(wl.B8)), _ptr(_deq(wl)), float(s), _ptr(asc), _ptr(r), nrows,
+                                    _ptr(y))
+        return y
+    b_cat = _concat(wl.B, wl.N)
     lib.oracle_expand_rows(_ptr(S_np), S_np.shape[1], _ptr(yin), wl.N, _ptr(ids),
                            len(wl.ranks), _ptr(rk), _ptr(b_cat), float(s), _ptr(asc), _ptr(r), nrows,
                            _ptr(y))

@@ -15,6 +15,7 @@ Notation: ``N(0, s)`` means a normal distribution with standard deviation s.
 """
 from __future__ import annotations
 
+import dataclasses
 import math
 from dataclasses import dataclass, field
 from typing import List, Optional
@@ -50,6 +51,12 @@ class Workload:
     slices: Optional[List[int]] = None
     A_s: Optional[List[List[torch.Tensor]]] = None
     B_s: Optional[List[List[torch.Tensor]]] = None
+    # e4m3 adapters: codes A8[i] uint8 [r_i, K], B8[i] uint8 [N, r_i] and
+    # dequant factors deq[i] = (a, b); adapter i is then A_i = a * e4m3(A8[i]),
+    # B_i = b * e4m3(B8[i]), and A / B are None
+    A8: Optional[List[torch.Tensor]] = None
+    B8: Optional[List[torch.Tensor]] = None
+    deq: Optional[List[tuple]] = None
 
     @property
     def num_adapters(self) -> int:
@@ -294,3 +301,19 @@ def random_fp32(shape, seed: int, std: float = 1.0) -> torch.Tensor:
     """A seeded fp32 tensor (used as the given S input of the expand step)."""
     g = torch.Generator().manual_seed(seed)
     return torch.randn(*shape, generator=g, dtype=torch.float32) * std
+
+
+def to_e4m3(wl: Workload) -> Workload:
+    """The same workload with its adapters stored as e4m3 codes: per adapter
+    and factor, a dequant factor d = max|value| / 448 (the largest e4m3
+    magnitude) and codes e4m3(value / d), round to nearest even (torch's
+    float8_e4m3fn cast).  This is input preparation: the oracle decodes the
+    codes itself, and the layer is defined by codes and factors."""
+    A8, B8, deq = [], [], []
+    for a, b in zip(wl.A, wl.B):
+        da = float(a.float().abs().max()) / 448.0 or 1.0
+        db = float(b.float().abs().max()) / 448.0 or 1.0
+        A8.append((a.float() / da).to(torch.float8_e4m3fn).view(torch.uint8).contiguous())
+        B8.append((b.float() / db).to(torch.float8_e4m3fn).view(torch.uint8).contiguous())
+        deq.append((da, db))
+    return dataclasses.replace(wl, A=None, B=None, A8=A8, B8=B8, deq=deq, name=wl.name + "_e4m3")

@@ -418,3 +418,93 @@ def test_moe_routing_is_a_stable_sort_of_the_pairs():
     want = sorted(range(len(flat)), key=lambda p: (flat[p] + 1 if 0 <= flat[p] < mw.E else 0, p))
     assert perm.tolist() == want
     assert counts.tolist() == [flat.count(e) for e in range(mw.E)]
+
+
+# ---------------------------------------------------------------------------
+# e4m3 adapters (8-bit codes with one dequant factor per adapter and factor)
+# ---------------------------------------------------------------------------
+
+def test_e4m3_decode_spec_values():
+    """Values the e4m3 format fixes: bias 7, 3 mantissa bits, no infinities;
+    the smallest subnormal is 2^-9, the smallest normal 2^-6, the largest
+    finite magnitude 448 (0x7E); S.1111.111 is NaN."""
+    table = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x30: 0.5, 0x38: 1.0,
+             0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x77: 240.0, 0x78: 256.0, 0x7E: 448.0,
+             0x80: -0.0, 0xB8: -1.0, 0xFE: -448.0}
+    for code, v in table.items():
+        assert oracle.e4m3_to_f64(code) == v, hex(code)
+    assert np.isnan(oracle.e4m3_to_f64(0x7F)) and np.isnan(oracle.e4m3_to_f64(0xFF))
+    assert np.signbit(oracle.e4m3_to_f64(0x80))
+
+
+def test_e4m3_codes_are_ordered_and_symmetric():
+    """The 127 non-negative finite codes increase strictly with the code,
+    and each negative code is the mirror of its positive one."""
+    pos = [oracle.e4m3_to_f64(c) for c in range(0x7F)]
+    assert all(b > a for a, b in zip(pos, pos[1:]))
+    for c in range(1, 0x7F):
+        assert oracle.e4m3_to_f64(c | 0x80) == -pos[c]
+
+
+def _bf16_twin(wl8):
+    """The bf16 workload holding e4m3 adapters decoded with unit factors
+    (every e4m3 value is exact in bf16)."""
+    def dec(codes):
+        v = np.vectorize(oracle.e4m3_to_f64)(codes.numpy().astype(np.int64))
+        return torch.tensor(v, dtype=torch.float64).to(torch.bfloat16)
+    return dataclasses.replace(wl8, A=[dec(a) for a in wl8.A8], B=[dec(b) for b in wl8.B8], A8=None, B8=None,
+                               deq=None)
+
+
+def test_e4m3_unit_factors_equal_the_bf16_oracle():
+    """An e4m3 pool with unit dequant factors is the bf16 pool of the same
+    values: the two oracle paths agree bit for bit."""
+    wl8 = workloads.to_e4m3(workloads.make_custom(12, 64, 48, [16, 32, 8], seed=71, p_base=0.2))
+    wl8 = dataclasses.replace(wl8, deq=[(1.0, 1.0)] * 3)
+    assert np.array_equal(oracle.lora_linear(wl8), oracle.lora_linear(_bf16_twin(wl8)))
+
+
+def test_e4m3_factors_scale_the_delta():
+    """The LoRA term is linear in each dequant factor: doubling every A
+    factor and halving every B factor changes nothing; doubling every A
+    factor equals doubling the call's scale."""
+    wl8 = workloads.to_e4m3(workloads.make_custom(10, 96, 64, [16, 48], seed=73, p_base=0.0))
+    ref = oracle.lora_linear(wl8)
+    same = dataclasses.replace(wl8, deq=[(2 * a, b / 2) for a, b in wl8.deq])
+    np.testing.assert_allclose(oracle.lora_linear(same), ref, rtol=1e-12, atol=1e-12)
+    dbl = dataclasses.replace(wl8, deq=[(2 * a, b) for a, b in wl8.deq])
+    np.testing.assert_allclose(oracle.lora_linear(dbl), oracle.lora_linear(wl8, scale=2 * wl8.scale),
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_e4m3_per_token_brute_force():
+    """Plain Python per token, with A and B factors that differ (a swapped
+    factor or a wrong code offset fails)."""
+    wl8 = workloads.to_e4m3(workloads.make_custom(7, 24, 20, [16, 32, 16], seed=79, p_base=0.2,
+                                                  adapter_scale="random"))
+    dec = np.vectorize(oracle.e4m3_to_f64)
+    x = wl8.x.double().numpy()
+    W = wl8.W.double().numpy()
+    bias = wl8.bias.double().numpy()
+    y = x @ W.T + bias
+    for t in range(wl8.M):
+        i = int(wl8.ids[t])
+        if i < 0:
+            continue
+        a, b = wl8.deq[i]
+        A = a * dec(wl8.A8[i].numpy().astype(np.int64))
+        B = b * dec(wl8.B8[i].numpy().astype(np.int64))
+        y[t] += wl8.scale * wl8.adapter_scale[i] * ((x[t] @ A.T) @ B.T)
+    np.testing.assert_allclose(oracle.lora_linear(wl8), y, rtol=1e-11, atol=1e-12)
+
+
+def test_e4m3_linear_is_shrink_then_expand():
+    """The two steps with e4m3 adapters (A's factor in the shrink, B's in
+    the expand) give the fused layer's LoRA term; S passes through fp32."""
+    wl8 = workloads.to_e4m3(workloads.make_custom(9, 64, 32, [16, 32], seed=83, p_base=0.2))
+    S = oracle.shrink(wl8, 32)
+    base = dataclasses.replace(wl8, ids=torch.full_like(wl8.ids, -1))
+    delta = oracle.lora_linear(wl8) - oracle.lora_linear(base)
+    zero = torch.zeros(wl8.M, wl8.N, dtype=torch.bfloat16)
+    got = oracle.expand(wl8, torch.tensor(S, dtype=torch.float32), zero)
+    np.testing.assert_allclose(got, delta, rtol=1e-5, atol=1e-6)
