@@ -107,6 +107,25 @@ enum {
  *        1: one output (slice_start unused).  lora_shrink returns the
  *        stacked S (slice s in columns [s r_i, (s+1) r_i)); lora_expand takes
  *        it in the same form.
+ * adapter_type (host value): LORA_ADAPTER_BF16 (0, the layout above) or
+ *        LORA_ADAPTER_E4M3: a_pool and b_pool then hold one byte per element,
+ *        the 8-bit float e4m3 (1 sign, 4 exponent bits with bias 7, 3
+ *        mantissa bits; largest finite 448), in the same layout and at the
+ *        same element offsets, and adapter i is A_i = dequant[2i] * A8_i,
+ *        B_i = dequant[2i+1] * B8_i.  The 8-bit codes are widened to bf16
+ *        exactly (every e4m3 value is a bf16 value); the factors join the
+ *        per-adapter factor that scales S before its one bf16 rounding
+ *        (lora_shrink applies A's factor, lora_expand B's).  This storage is
+ *        an extension of this library; the page stores adapters in the
+ *        model's precision.
+ * dequant: e4m3 pools: DEVICE fp32 [num_adapters][2] (A factor, B factor).
+ * widened: e4m3 pools: DEVICE bf16 scratch of a_elems + b_elems elements
+ *        (16-byte aligned).  The decode-sized schedule (M <= 64) reads the
+ *        8-bit pool directly; the others (and lora_shrink / lora_expand)
+ *        first widen the adapters a batch uses into this scratch, at the
+ *        same offsets.  One scratch can serve every pool of a step (sized
+ *        for the largest) when the calls run one after another on a
+ *        stream.  NULL: those calls return LORA_ERR_NULL.
  * a_elems / b_elems (host values) are the total element counts of the pools;
  * num_adapters, max_rank (largest rank[i]), K and N are host values.
  * lora_pool_layout() computes offsets, padded ranks and sizes for a set of
@@ -127,7 +146,13 @@ typedef struct {
     const float *adapter_scale;
     int32_t num_slices;
     int32_t slice_start[LORA_MAX_SLICES + 1];
+    int32_t adapter_type;
+    const float *dequant;
+    lora_bf16_t *widened;
 } lora_pool_t;
+
+#define LORA_ADAPTER_BF16 0
+#define LORA_ADAPTER_E4M3 1
 
 /*
  * Segment table (§2.3): a stable bucket sort of the tokens by lora_id.

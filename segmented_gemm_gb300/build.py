@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "liblora.so")
 
 SOURCES = ["lora_api.cu", "seg_build.cu", "fused_tc.cu", "fused_splitk.cu", "fused_cluster.cu",
-           "lora_noalloc.cu", "moe.cu"]
+           "lora_noalloc.cu", "moe.cu", "widen.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

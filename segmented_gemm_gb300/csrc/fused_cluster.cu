@@ -55,6 +55,8 @@ constexpr int kStMaxWinAll = 512;          // windows of the pool (bitmap of 16 
 constexpr int kStMaxWinList = 2 * kStreamMaxTokens;   // windows a batch can touch
 constexpr int kClMaxStages = 8;
 constexpr int kClMaxSRing = 4;             // S operand slots of the expand windows (one window each)
+constexpr int kFp8Box = 16 * 1024;         // an e4m3 A or B box; it lands in the upper half of the weight area
+constexpr int kBarConv = 11;               // named barrier: the epilogue warps' loads of an e4m3 B box are done
 constexpr int kStMaxSegs = 8;
 constexpr int kStMaxRegions = 16;
 constexpr int kStMaxRuns = 4;              // shrink runs (windows) of one CTA
@@ -85,7 +87,7 @@ struct StSeg {
 };
 
 // the barriers and tables that follow the reduction area fit kClMisc bytes
-static_assert((2 * kClMaxStages + kStMaxRegions + 1 + 2 * kClMaxSRing) * 8 + 10 * 4 + kSplitBN * 2 + 64 * 4 * 2 +
+static_assert((4 * kClMaxStages + kStMaxRegions + 1 + 2 * kClMaxSRing) * 8 + 10 * 4 + kSplitBN * 2 + 64 * 4 * 2 +
                       kStMaxSegs * static_cast<int>(sizeof(StSeg)) + kStMaxWinCta * 4 * 3 + kStMaxWinCta * kStWin * 4 +
                       kStMaxRuns * kStWin * 4 + (kStMaxWinAll / 32) * 4 * 2 + kStMaxWinList * 4 +
                       kStMaxWinCta * kStWin * 4 + kStMaxWinCta * 4 <=
@@ -216,7 +218,17 @@ __global__ void __launch_bounds__(kClThreads, 1)
     uint64_t *red_full = acc_full + kStMaxRegions;
     uint64_t *s_ready = red_full + 1;             // [kClMaxSRing] S slot staged (the 128 loader threads)
     uint64_t *s_free = s_ready + kClMaxSRing;     // [kClMaxSRing] S slot read by its expand MMAs
-    int *ivars = reinterpret_cast<int *>(s_free + kClMaxSRing);
+    // e4m3 pools: the ic-th 8-bit box (in ring order) has landed on
+    // codes[ic % stages] and is widened on conv[ic % stages].  The boxes get
+    // barriers of their own (not the ring's full[]) because the epilogue
+    // warps that widen them skip the base units in between: waiting on a
+    // ring slot two phases ahead would see the parity of an older phase.
+    // Here the waiters walk the 8-bit boxes in order, and the producer
+    // issues box ic + stages only after the MMA issuer has consumed box ic
+    // (its ring slot comes free later), so no phase is ever skipped.
+    uint64_t *conv = s_free + kClMaxSRing;        // [stages]
+    uint64_t *codes = conv + kClMaxStages;        // [stages]
+    int *ivars = reinterpret_cast<int *>(codes + kClMaxStages);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ivars);
     volatile int *abort_flag = ivars + 1;
     int *n_segs = ivars + 2;       // segments before the expand
@@ -291,6 +303,10 @@ __global__ void __launch_bounds__(kClThreads, 1)
             mbar_init(&s_ready[lane], 128);
             mbar_init(&s_free[lane], 1);
         }
+        if (lane < p.stages) {
+            mbar_init(&conv[lane], 128);   // the four epilogue warps widen each 8-bit box
+            mbar_init(&codes[lane], 1);    // the producer's expect_tx arrive
+        }
         if (lane < kStMaxRegions) mbar_init(&acc_full[lane], 1);
         if (lane == 0) {
             mbar_init(red_full, 1);
@@ -307,9 +323,16 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 for (int i = 0; i < nfirst; ++i) {
                     uint8_t *wa = smem + i * slot_bytes;
                     const int u = u0 + i;
-                    mbar_expect_tx(&full[i], unit_tx);
-                    if (u < u1) tma_load_3d_st(wa, &tm_a3, &full[i], 0, kChunk * kStWin * (u / KU2), 2 * (u % KU2));
-                    else tma_load_3d_st(wa, &tm_w3, &full[i], 0, n0, 2 * (b0 + (u - u1)));
+                    if (u < u1 && p.fp8) {   // 8-bit A codes (the i-th 8-bit box), widened by the epilogue warps
+                        mbar_expect_tx(&full[i], T * 256);
+                        mbar_expect_tx(&codes[i % p.stages], kFp8Box);
+                        tma_load_2d(wa + kFp8Box, &tm_a3, &codes[i % p.stages], 2 * kBK * (u % KU2),
+                                    kChunk * kStWin * (u / KU2));
+                    } else {
+                        mbar_expect_tx(&full[i], unit_tx);
+                        if (u < u1) tma_load_3d_st(wa, &tm_a3, &full[i], 0, kChunk * kStWin * (u / KU2), 2 * (u % KU2));
+                        else tma_load_3d_st(wa, &tm_w3, &full[i], 0, n0, 2 * (b0 + (u - u1)));
+                    }
                 }
                 pdl_wait();   // x may be written by the kernel ahead of this one
                 for (int i = 0; i < nfirst; ++i) {
@@ -367,6 +390,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 ao[j] = i < p.A ? p.a_offset[i] : 0;
                 rk[j] = i < p.A ? p.rank[i] : 0;
                 fa[j] = i < p.A && p.adapter_scale ? p.adapter_scale[i] : 1.f;
+                if (p.fp8 && i < p.A) fa[j] *= p.dequant[2 * i] * p.dequant[2 * i + 1];   // e4m3: A and B factors
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -398,6 +422,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         named_bar_sync(kBarMeta, kMetaThreads);
         const int nk = *n_segs;
         uint32_t it = 0;
+        uint32_t ic = 0;   // e4m3: 8-bit boxes in ring order (the prologue's included)
         for (int si = 0; si <= nk; ++si) {
             if (si == nk) {   // the expand windows, once the tables are ready
                 named_bar_sync(kBarTables, kTablesThreads);
@@ -407,15 +432,26 @@ __global__ void __launch_bounds__(kClThreads, 1)
             for (int u = sg.a; u < sg.b; ++u) {
                 if (sg.kind == kStExpand && !s_win_touch[u - sg.a]) continue;   // no token uses the window
                 const uint32_t iu = it++;
+                const uint32_t icu = p.fp8 && sg.kind != kStBase ? ic++ : 0;   // its index among the 8-bit boxes
                 if (iu < static_cast<uint32_t>(nfirst)) continue;   // issued in the prologue
                 const int s = iu % p.stages;
                 const uint32_t round = iu / p.stages;
                 if (lane == 0) {
                     if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
                     uint8_t *wa = smem + s * slot_bytes;
-                    if (sg.kind == kStExpand) {
+                    uint64_t *cb = &codes[icu % p.stages];
+                    if (sg.kind == kStExpand && p.fp8) {   // 8-bit B codes; the slot carries nothing else
+                        mbar_arrive(&full[s]);
+                        mbar_expect_tx(cb, kFp8Box);
+                        tma_load_3d_st(wa + kFp8Box, &tm_b3, cb, 0, n0, s_win_panel[u - sg.a]);
+                    } else if (sg.kind == kStExpand) {
                         mbar_expect_tx(&full[s], kClWArea);
                         tma_load_3d_st(wa, &tm_b3, &full[s], 0, n0, s_win_panel[u - sg.a]);
+                    } else if (sg.kind == kStShrink && p.fp8) {   // 8-bit A codes; the x box on the slot
+                        mbar_expect_tx(&full[s], T * 256);
+                        mbar_expect_tx(cb, kFp8Box);
+                        tma_load_2d(wa + kFp8Box, &tm_a3, cb, 2 * kBK * u, sg.arow);
+                        tma_load_3d_st(wa + kClWArea, &tm_x3, &full[s], 0, 0, 2 * u);
                     } else {
                         mbar_expect_tx(&full[s], unit_tx);
                         if (sg.kind == kStShrink) tma_load_3d_st(wa, &tm_a3, &full[s], 0, sg.arow, 2 * u);
@@ -541,10 +577,17 @@ __global__ void __launch_bounds__(kClThreads, 1)
     } else if (warp == 1) {
         // ===================== MMA issuer ====================================
         uint32_t started = 0;   // bit r: region r holds a partial sum
+        uint32_t ic = 0;        // e4m3: 8-bit units consumed (their widening is signalled on conv[ic % stages])
         const uint32_t idesc = umma_idesc_bf16(kSplitBN, T);
-        auto mma_kunit = [&](uint32_t it, uint32_t d, int region) {
+        auto wait_widened = [&]() {
+            mbar_wait(&conv[ic % p.stages], (ic / p.stages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+            ++ic;
+            fence_proxy_async_smem();   // the widened operand was written through the generic proxy
+        };
+        auto mma_kunit = [&](uint32_t it, uint32_t d, int region, bool widened) {
             const int s = it % p.stages;
             mbar_wait(&full[s], (it / p.stages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+            if (widened) wait_widened();
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t wa = smem_u32(smem + s * slot_bytes);
@@ -566,7 +609,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         uint32_t it = 0;
         int si0 = 0;
         if (!allw) {   // the first base units are known before the metadata
-            for (; it < static_cast<uint32_t>(nfirst); ++it) mma_kunit(it, tmem_base, 0);
+            for (; it < static_cast<uint32_t>(nfirst); ++it) mma_kunit(it, tmem_base, 0, false);
             si0 = 1;
         }
         named_bar_sync(kBarMma, 64);
@@ -581,7 +624,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const uint32_t d = tmem_base + sg.region * T;
             for (int u = sg.a; u < sg.b; ++u) {
                 if (sg.kind != kStExpand) {
-                    mma_kunit(it++, d, sg.region);
+                    mma_kunit(it++, d, sg.region, p.fp8 && sg.kind == kStShrink);
                     continue;
                 }
                 // the window's B box through the ring, its S in slot r of the
@@ -590,6 +633,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 const int w = wt++, r = w % SR;
                 const int s = static_cast<int>(it % p.stages);
                 mbar_wait(&full[s], (it / p.stages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                if (p.fp8) wait_widened();
                 mbar_wait(&s_ready[r], (w / SR) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
                 fence_proxy_async_smem();   // the S operand arrived through the generic proxy
                 tc_fence_after();
@@ -656,7 +700,11 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const int64_t ao0 = v0 ? p.a_offset[id0] : 0, ao1 = v1 ? p.a_offset[id1] : 0;
             const int rk0 = v0 ? p.rank[id0] : 0, rk1 = v1 ? p.rank[id1] : 0;
             const bool fac = p.adapter_scale != nullptr;
-            const float f0 = fac && v0 ? p.adapter_scale[id0] : 1.f, f1 = fac && v1 ? p.adapter_scale[id1] : 1.f;
+            float f0 = fac && v0 ? p.adapter_scale[id0] : 1.f, f1 = fac && v1 ? p.adapter_scale[id1] : 1.f;
+            if (p.fp8) {   // e4m3: A and B factors
+                if (v0) f0 *= p.dequant[2 * id0] * p.dequant[2 * id0 + 1];
+                if (v1) f1 *= p.dequant[2 * id1] * p.dequant[2 * id1 + 1];
+            }
             s_ids[lane] = id0;
             s_ids[lane + 32] = id1;
             s_tsc[lane] = p.scale * f0;
@@ -742,9 +790,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         }
         const int ns = *n_segs;
         // ---- shrink runs: add my partial window sums, then release ------------
-        for (int si = 0, run = 0; si < ns; ++si) {
-            const StSeg sg = segs[si];
-            if (sg.kind != kStShrink) continue;
+        auto shrink_run = [&](const StSeg &sg, int run) {
             mbar_wait(&acc_full[sg.region], 0, abort_flag, status, LORA_DEV_TIMEOUT);
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + sg.region * T;
@@ -767,15 +813,81 @@ __global__ void __launch_bounds__(kClThreads, 1)
             // shrunk window is expanded, so its consumers clear it again)
             named_bar_sync(kBarEpi, 128);
             if (et == 0) red_release_gpu_add(wcnt + sg.w * kCntStride, sg.b - sg.a);
-            ++run;
+        };
+        // e4m3 pool: the 8-bit box of ring unit iu (the cic-th 8-bit box)
+        // sits in the upper half of its slot's weight area once codes[] says
+        // so; widen it in place to the bf16 operand the MMA reads (the bf16
+        // box's layout)
+        uint32_t cit = 0, cic = 0;   // ring units and 8-bit units walked, as the producer and the MMA count them
+        auto widen_unit = [&](uint32_t iu, bool b_box) {
+            const int s = iu % p.stages;
+            mbar_wait(&codes[cic % p.stages], (cic / p.stages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+            uint8_t *wa = smem + s * slot_bytes;
+            const uint8_t *box = wa + kFp8Box;
+            uint4 c[8];
+            if (!b_box) {
+                // A: box row et (128 K codes) -> row et of K blocks 0 and 1,
+                // 128-byte swizzle (16-byte chunk q at (q ^ (row & 7)) * 16);
+                // only this thread reads the row it overwrites
+#pragma unroll
+                for (int h = 0; h < 8; ++h) c[h] = reinterpret_cast<const uint4 *>(box + et * 128)[h];
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    uint32_t o[8];
+                    e4m3x16_to_bf16(c[h], o);
+                    uint8_t *rowp = wa + (h >> 2) * (kSplitBN * kBK * 2) + et * 128;
+                    const int q = 2 * (h & 3);
+                    *reinterpret_cast<uint4 *>(rowp + ((q ^ (et & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4 *>(rowp + (((q + 1) ^ (et & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+            } else {
+                // B: row et of each of the 8 panels (16 codes) -> 32-byte rows,
+                // 32-byte swizzle (chunk q at (q ^ ((row >> 2) & 1)) * 16); the
+                // stores overwrite other threads' codes, so all loads go first
+#pragma unroll
+                for (int j = 0; j < kStWin; ++j) c[j] = *reinterpret_cast<const uint4 *>(box + j * 2048 + et * 16);
+                named_bar_sync(kBarConv, 128);
+                const int sw = (et >> 2) & 1;
+#pragma unroll
+                for (int j = 0; j < kStWin; ++j) {
+                    uint32_t o[8];
+                    e4m3x16_to_bf16(c[j], o);
+                    uint8_t *rowp = wa + j * (kSplitBN * kChunk * 2) + et * 32;
+                    *reinterpret_cast<uint4 *>(rowp + (sw << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4 *>(rowp + ((1 ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+            }
+            fence_proxy_async_smem();   // generic-proxy stores -> the tensor core's reads
+            mbar_arrive(&conv[cic % p.stages]);
+            ++cic;
+        };
+        if (p.fp8) {
+            // walk the units in ring order: each shrink run's boxes are widened
+            // before its sums are read
+            for (int si = 0, run = 0; si < ns; ++si) {
+                const StSeg sg = segs[si];
+                for (int u = sg.a; u < sg.b; ++u) {
+                    const uint32_t iu = cit++;
+                    if (sg.kind == kStShrink) widen_unit(iu, false);
+                }
+                if (sg.kind == kStShrink) shrink_run(sg, run++);
+            }
+        } else {
+            for (int si = 0, run = 0; si < ns; ++si)
+                if (segs[si].kind == kStShrink) shrink_run(segs[si], run++);
         }
         if (bias_thread) reinterpret_cast<uint4 *>(s_bias)[threadIdx.x - 160] = bias_reg;
+        named_bar_sync(kBarTouch, allw ? 160 : 128);   // the touched flags (warp 6, or warp 2 before kBarTablesEpi)
+        if (p.fp8 && *n_exp) {   // the B boxes of the expand windows some token uses
+            const StSeg sg = segs[ns];
+            for (int u = sg.a; u < sg.b; ++u)
+                if (s_win_touch[u - sg.a]) widen_unit(cit++, true);
+        }
         // ---- output tile: push my partial rows to their owners ----------------
         mbar_wait(&acc_full[0], 0, abort_flag, status, LORA_DEV_TIMEOUT);
         tc_fence_after();
         // nothing accumulated (no base units and no expand window a token
         // uses): send zeros
-        named_bar_sync(kBarTouch, allw ? 160 : 128);   // the touched flags (warp 6, or warp 2 before kBarTablesEpi)
         bool any_touch = false;
         if (*n_exp)
             for (int k = 0; k < segs[*n_segs].b - segs[*n_segs].a; ++k) any_touch = any_touch || s_win_touch[k];

@@ -563,9 +563,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
             const int tok = valid ? p.perm[pp] : 0;
             const bool lora_row = p.mode != kModeExpand || pp >= p.offsets[1];
             // the LoRA scale of my row: the call's scale times its adapter's
-            // factor (rows outside every segment are masked anyway)
-            float row_sc = Ly.scale;
-            if (Ly.adapter_scale && jb.kind == 0 && p.mode == kModeLinear && valid) {
+            // factor (rows outside every segment are masked anyway); the
+            // standalone shrink applies the factor alone (an e4m3 pool's A
+            // factor; no factor for a bf16 pool: S leaves unscaled)
+            float row_sc = p.mode == kModeShrink ? 1.f : Ly.scale;
+            if (Ly.adapter_scale && jb.kind == 0 && (p.mode == kModeLinear || p.mode == kModeShrink) && valid) {
                 const int id = p.ids[tok];
                 row_sc *= (id >= 0 && id < p.num_adapters) ? __ldg(Ly.adapter_scale + id) : 0.f;
             }
@@ -608,8 +610,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                                                                  rng_panel(rng) * kChunk);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
-                            const float4 f4 = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                                          __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                            const float4 f4 = make_float4(
+                                __uint_as_float(r[4 * v]) * row_sc, __uint_as_float(r[4 * v + 1]) * row_sc,
+                                __uint_as_float(r[4 * v + 2]) * row_sc, __uint_as_float(r[4 * v + 3]) * row_sc);
                             if (p.shrink_split > 1) atomicAdd(dst + v, f4);
                             else dst[v] = f4;
                         }

@@ -74,6 +74,7 @@ struct WsLayout {
     int32_t max_win_str;      // windows the stream schedule's sums and counters can hold (M <= 64)
     size_t s_scratch, s_scratch_bytes;
     size_t acc_out, acc_out_bytes, acc_shr, acc_shr_bytes;
+    size_t fac;               // e4m3 pools: each layer's per-adapter factors for a call, fp32 [kMaxLayers][A]
     size_t total_min;         // everything but the stream-K scratch
     size_t sk_part, sk_cnt;   // stream-K partial sums / counters of the tiled schedule (M > 128)
     size_t total;
@@ -213,6 +214,8 @@ struct ClusterParams {
     int64_t M;
     int32_t N, K, T_pad, C, NT, kblocks, stages, max_regions, max_win_str;
     int32_t s_ring;            // S operand slots of the expand windows (2..4)
+    int32_t fp8;               // e4m3 pool: A and B boxes arrive as 8-bit codes and are widened in the kernel
+    const float *dequant;      // e4m3 pool: [A][2] dequant factors of A and B
     float scale;
     const float *adapter_scale;   // per-adapter factor on top of scale, or null (all 1)
     const uint16_t *bias;
@@ -232,7 +235,22 @@ struct ClusterParams {
 };
 
 
+// e4m3 pools: widening the adapters a batch uses into the pool's bf16
+// scratch (same offsets) and the call's per-adapter factors
+enum WidenMode { kWidenFused = 0, kWidenShrink = 1, kWidenExpand = 2 };
+struct WidenParams {
+    const uint8_t *a8, *b8;    // the e4m3 pools
+    uint16_t *aw, *bw;         // their bf16 twins in the scratch
+    const int64_t *a_off, *b_off;
+    const int32_t *rank;
+    int32_t K, N, A, parts, mode;
+    const int32_t *seg_id, *num_segments;   // the batch's segment table
+    const float *dequant, *adapter_scale;
+    float *fac;                // fused: s_i da_i db_i; shrink: da_i; expand: s_i db_i
+};
+
 // ---- launchers (enqueue only; return the launch status) --------------------
+cudaError_t launch_widen(const WidenParams &p, int max_segments, cudaStream_t stream);
 cudaError_t launch_seg_build(const SegParams &p, bool pdl, cudaStream_t stream);
 cudaError_t launch_moe_route(const RouteParams &p, cudaStream_t stream);
 cudaError_t launch_tc(const TcArgs &args, int grid, cudaStream_t stream);

@@ -66,7 +66,8 @@ static EncodeTiledFn encoder()
 
 // 2-D bf16 map: `inner` elements per row, `rows` rows, row pitch in bytes.
 static bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t pitch,
-                      uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw)
+                      uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw,
+                      CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)
 {
     EncodeTiledFn fn = encoder();
     if (!fn) return false;
@@ -74,14 +75,15 @@ static bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t
     cuuint64_t strides[1] = {pitch};
     cuuint32_t box[2] = {box_inner, box_rows};
     cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 3-D bf16 map: dims {d0, d1, d2}, byte strides of dims 1 and 2.
 static bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
-                      uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle sw)
+                      uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle sw,
+                      CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)
 {
     EncodeTiledFn fn = encoder();
     if (!fn) return false;
@@ -89,7 +91,7 @@ static bool encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1
     cuuint64_t strides[2] = {s1, s2};
     cuuint32_t box[3] = {b0, b1, b2};
     cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -175,6 +177,7 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
     L.s_scratch = take(L.s_scratch_bytes);
     L.acc_out = take(std::max<size_t>(L.acc_out_bytes, 16));
     L.acc_shr = take(std::max<size_t>(L.acc_shr_bytes, 16));
+    L.fac = take(static_cast<size_t>(kMaxLayers) * std::max(A, 1) * 4);
     L.total_min = o;
     // stream-K scratch of the tiled schedule: partial sums and counters of
     // the split tiles (used only when the workspace is this large)
@@ -213,6 +216,11 @@ int check_pool(const lora_pool_t *pool)
         if (!pool->a_pool || !pool->b_pool || !pool->a_offset || !pool->b_offset || !pool->rank) return LORA_ERR_NULL;
         if (!aligned16(pool->a_pool) || !aligned16(pool->b_pool)) return LORA_ERR_ALIGN;
         if (reinterpret_cast<uintptr_t>(pool->adapter_scale) & 3) return LORA_ERR_ALIGN;
+        if (pool->adapter_type != LORA_ADAPTER_BF16 && pool->adapter_type != LORA_ADAPTER_E4M3) return LORA_ERR_SHAPE;
+        if (pool->adapter_type == LORA_ADAPTER_E4M3) {
+            if (!pool->dequant) return LORA_ERR_NULL;
+            if ((reinterpret_cast<uintptr_t>(pool->dequant) & 3) || !aligned16(pool->widened)) return LORA_ERR_ALIGN;
+        }
         if (pool->max_rank < LORA_RANK_ALIGN || pool->max_rank > LORA_MAX_RANK || (pool->max_rank % LORA_RANK_ALIGN))
             return LORA_ERR_RANK;
         if (S > 1 && pool->max_rank % (LORA_RANK_ALIGN * S)) return LORA_ERR_RANK;   // whole panels per slice
@@ -383,6 +391,46 @@ static bool encode_pool_maps(Maps &m, const lora_pool_t *pool, const void *dummy
     return true;
 }
 
+// e4m3 pools: enqueue the widening of the adapters the table in ws names
+// into the pool's bf16 scratch, with this call's per-adapter factors
+// (mode: kWiden*) in factor row `slot` of the workspace, and describe the
+// widened pool in *out.  bf16 pools: *out is the pool itself.
+static int widen_pool(const lora_pool_t *pool, const WsLayout &L, void *ws, int mode, int slot, cudaStream_t stream,
+                      lora_pool_t *out)
+{
+    *out = *pool;
+    if (pool->adapter_type != LORA_ADAPTER_E4M3 || pool->num_adapters == 0) return LORA_OK;
+    if (!pool->widened) return LORA_ERR_NULL;
+    WidenParams w;
+    std::memset(&w, 0, sizeof w);
+    w.a8 = reinterpret_cast<const uint8_t *>(pool->a_pool);
+    w.b8 = reinterpret_cast<const uint8_t *>(pool->b_pool);
+    w.aw = pool->widened;
+    w.bw = pool->widened + pool->a_elems;
+    w.a_off = pool->a_offset;
+    w.b_off = pool->b_offset;
+    w.rank = pool->rank;
+    w.K = pool->K;
+    w.N = pool->N;
+    w.A = pool->num_adapters;
+    const int max_seg = static_cast<int>(std::min<int64_t>(pool->num_adapters, std::max<int64_t>(L.M, 1)));
+    w.parts = std::max(1, 2 * num_sms_current_device() / std::max(1, max_seg));
+    w.mode = mode;
+    w.seg_id = at<int32_t>(ws, L.seg_id);
+    w.num_segments = at<int32_t>(ws, L.num_segments);
+    w.dequant = pool->dequant;
+    w.adapter_scale = pool->adapter_scale;
+    w.fac = at<float>(ws, L.fac) + static_cast<size_t>(slot) * std::max(pool->num_adapters, 1);
+    if (launch_widen(w, max_seg, stream) != cudaSuccess) return LORA_ERR_CUDA;
+    out->a_pool = pool->widened;
+    out->b_pool = pool->widened + pool->a_elems;
+    out->adapter_type = LORA_ADAPTER_BF16;
+    out->adapter_scale = w.fac;
+    out->dequant = nullptr;
+    out->widened = nullptr;
+    return LORA_OK;
+}
+
 // One layer of a tiled launch as the caller gives it.
 struct LayerCall {
     const lora_bf16_t *x, *W, *bias;
@@ -431,7 +479,8 @@ static int run_tiled(const LayerCall *lc, int nl, int64_t M, const int32_t *ids,
     }
     p.mode = mode;
     p.ids = ids;
-    if (mode == kModeShrink) p.layer[0].adapter_scale = nullptr;   // S leaves unscaled
+    // shrink mode: the pool's factor is what S is multiplied by (the caller
+    // passes none for a bf16 pool: S leaves unscaled; an e4m3 pool's A factor)
     if (mode == kModeExpand) p.s_sets = 1;   // the caller's S, prepared as one panel set
     p.s_out = s_out;
     p.s_cols = s_cols;
@@ -599,6 +648,8 @@ static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, co
     }
     p.scale = scale;
     p.adapter_scale = pool->num_adapters ? pool->adapter_scale : nullptr;
+    p.fp8 = pool->num_adapters && pool->adapter_type == LORA_ADAPTER_E4M3 ? 1 : 0;
+    p.dequant = p.fp8 ? pool->dequant : nullptr;
     p.bias = bias;
     p.x = x;
     p.y = y;
@@ -614,11 +665,22 @@ static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, co
         return LORA_ERR_CUDA;
     const void *apool = pool->num_adapters ? static_cast<const void *>(pool->a_pool) : static_cast<const void *>(W);
     const uint64_t arows = pool->num_adapters ? static_cast<uint64_t>(pool->a_elems / pool->K) : 1;
-    if (!encode_3d(&m.a3, apool, kBK, arows, KB, K * 2, kBK * 2, kBK, kSplitBN, 2, s128)) return LORA_ERR_CUDA;
     const void *bpool = pool->num_adapters ? static_cast<const void *>(pool->b_pool) : static_cast<const void *>(W);
-
-    if (!encode_3d(&m.b3, bpool, kChunk, N, panels, kChunk * 2, N * kChunk * 2, kChunk, kSplitBN, cluster_win(), s32))
-        return LORA_ERR_CUDA;
+    if (p.fp8) {
+        // e4m3 pools, one byte per element: a shrink unit's A box is 128
+        // rows x 128 K codes, an expand window's B box 8 panels x 128 rows x
+        // 16 codes (16 KB each, unswizzled); the kernel widens them in place
+        const CUtensorMapSwizzle s0 = CU_TENSOR_MAP_SWIZZLE_NONE;
+        const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        if (!encode_2d(&m.a3, apool, K, arows, K, 2 * kBK, kSplitBN, s0, u8)) return LORA_ERR_CUDA;
+        if (!encode_3d(&m.b3, bpool, kChunk, N, panels, kChunk, N * kChunk, kChunk, kSplitBN, cluster_win(), s0, u8))
+            return LORA_ERR_CUDA;
+    } else {
+        if (!encode_3d(&m.a3, apool, kBK, arows, KB, K * 2, kBK * 2, kBK, kSplitBN, 2, s128)) return LORA_ERR_CUDA;
+        if (!encode_3d(&m.b3, bpool, kChunk, N, panels, kChunk * 2, N * kChunk * 2, kChunk, kSplitBN, cluster_win(),
+                       s32))
+            return LORA_ERR_CUDA;
+    }
     return launch_cluster(m, p, pdl, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
@@ -895,9 +957,11 @@ int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const 
         if (path == LORA_PATH_STREAM) return LORA_ERR_UNSUPPORTED;
         if (!segs && (rc = enqueue_segments(lora_id_map, M, pool, L, ws, s))) return rc;
     }
+    lora_pool_t wpool;   // e4m3: the widened pool
+    if ((rc = widen_pool(pool, L, ws, kWidenFused, 0, s, &wpool))) return rc;
     const bool splitk = path == LORA_PATH_SPLITK || (path == LORA_PATH_AUTO && M <= kSplitMaxTokens && lora_id_map);
-    if (splitk) return run_splitk(x, M, W, bias, lora_id_map, pool, scale, y, ws, L, s);
-    return run_tiled(x, M, W, bias, lora_id_map, pool, scale, y, ws, ws_bytes, L, kModeLinear, nullptr, 0, nullptr, s);
+    if (splitk) return run_splitk(x, M, W, bias, lora_id_map, &wpool, scale, y, ws, L, s);
+    return run_tiled(x, M, W, bias, lora_id_map, &wpool, scale, y, ws, ws_bytes, L, kModeLinear, nullptr, 0, nullptr, s);
 }
 
 int lora_linear(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
@@ -969,8 +1033,12 @@ int lora_linear_layers(const lora_layer_t *layers, int32_t num_layers, int64_t M
         if (rc) return rc;
     }
     LayerCall lc[LORA_MAX_LAYERS];
-    for (int l = 0; l < num_layers; ++l)
-        lc[l] = {layers[l].x, layers[l].W, layers[l].bias, layers[l].pool, layers[l].scale, layers[l].y};
+    lora_pool_t wpool[LORA_MAX_LAYERS];   // e4m3 layers: their widened pools
+    for (int l = 0; l < num_layers; ++l) {
+        int rc = widen_pool(layers[l].pool, L, ws, kWidenFused, l, s, &wpool[l]);
+        if (rc) return rc;
+        lc[l] = {layers[l].x, layers[l].W, layers[l].bias, &wpool[l], layers[l].scale, layers[l].y};
+    }
     return run_tiled(lc, num_layers, M, lora_id_map, ws, ws_bytes, L, kModeLinear, nullptr, 0, nullptr,
                      at<uint16_t>(ws, layers_s_offset(L)), s);
 }
@@ -992,7 +1060,10 @@ int lora_shrink(const lora_bf16_t *x, int64_t M, const int32_t *lora_id_map, con
     if (cudaMemsetAsync(S, 0, static_cast<size_t>(M) * s_cols * sizeof(float), s) != cudaSuccess)
         return LORA_ERR_CUDA;
     if (pool->num_adapters == 0) return LORA_OK;
-    return run_tiled(x, M, nullptr, nullptr, lora_id_map, pool, 1.0f, nullptr, ws, ws_bytes, L, kModeShrink, S, s_cols, nullptr, s);
+    lora_pool_t wpool;   // bf16: S unscaled; e4m3: the widened pool, S times A's factor
+    if ((rc = widen_pool(pool, L, ws, kWidenShrink, 0, s, &wpool))) return rc;
+    if (pool->adapter_type != LORA_ADAPTER_E4M3) wpool.adapter_scale = nullptr;
+    return run_tiled(x, M, nullptr, nullptr, lora_id_map, &wpool, 1.0f, nullptr, ws, ws_bytes, L, kModeShrink, S, s_cols, nullptr, s);
 }
 
 int lora_expand(const float *S, int32_t s_cols, int64_t M, const int32_t *lora_id_map, const lora_pool_t *pool,
@@ -1010,7 +1081,9 @@ int lora_expand(const float *S, int32_t s_cols, int64_t M, const int32_t *lora_i
     int rc = prepare(lora_id_map, M, pool, segs, ws, ws_bytes, s, &L);
     if (rc) return rc;
     if (pool->num_adapters == 0) return LORA_OK;
-    return run_tiled(nullptr, M, nullptr, nullptr, lora_id_map, pool, scale, y, ws, ws_bytes, L, kModeExpand, nullptr, s_cols, S, s);
+    lora_pool_t wpool;   // e4m3: the widened pool, the factor times B's factor
+    if ((rc = widen_pool(pool, L, ws, kWidenExpand, 0, s, &wpool))) return rc;
+    return run_tiled(nullptr, M, nullptr, nullptr, lora_id_map, &wpool, scale, y, ws, ws_bytes, L, kModeExpand, nullptr, s_cols, S, s);
 }
 
 int lora_get_status(void *ws, lora_stream_t stream, int32_t *status)

@@ -359,6 +359,29 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
+// Two e4m3 codes (low byte first) -> two bf16 values (low half first).
+// Every e4m3 value is an f16 and a bf16 value: the widening is exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t codes)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
+    float lo, hi;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"(static_cast<uint16_t>(h2 & 0xFFFFu)));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(static_cast<uint16_t>(h2 >> 16)));
+    return pack_bf16x2(lo, hi);
+}
+
+// 16 e4m3 codes (one uint4) -> 16 bf16 values (o[0..3]: codes 0..7, o[4..7]: codes 8..15).
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 c, uint32_t (&o)[8])
+{
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        o[2 * k] = e4m3x2_to_bf16x2(static_cast<uint16_t>(w[k] & 0xFFFFu));
+        o[2 * k + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(w[k] >> 16));
+    }
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 

@@ -26,6 +26,7 @@ LORA_DEV_BAD_ID, LORA_DEV_TIMEOUT, LORA_DEV_BAD_POOL = 1, 2, 4
 LORA_PATH_AUTO, LORA_PATH_TILED, LORA_PATH_SPLITK, LORA_PATH_STREAM = 0, 1, 2, 3
 LORA_FLAG_STATIC_WEIGHTS = 0x100
 LORA_MAX_SLICES = 4
+LORA_ADAPTER_BF16, LORA_ADAPTER_E4M3 = 0, 1
 LORA_MAX_LAYERS = 8
 LORA_MAX_RANK, LORA_RANK_ALIGN, LORA_MAX_ADAPTERS = 128, 16, 1024
 
@@ -41,7 +42,8 @@ class lora_pool_t(ctypes.Structure):
                 ("rank", ctypes.c_void_p), ("a_elems", ctypes.c_int64), ("b_elems", ctypes.c_int64),
                 ("num_adapters", ctypes.c_int32), ("max_rank", ctypes.c_int32),
                 ("K", ctypes.c_int32), ("N", ctypes.c_int32), ("adapter_scale", ctypes.c_void_p),
-                ("num_slices", ctypes.c_int32), ("slice_start", ctypes.c_int32 * (LORA_MAX_SLICES + 1))]
+                ("num_slices", ctypes.c_int32), ("slice_start", ctypes.c_int32 * (LORA_MAX_SLICES + 1)),
+                ("adapter_type", ctypes.c_int32), ("dequant", ctypes.c_void_p), ("widened", ctypes.c_void_p)]
 
 
 class lora_segments_t(ctypes.Structure):
@@ -154,6 +156,8 @@ class LoraPool:
     true_ranks: List[int]
     padded_ranks: List[int]
     adapter_scale: Optional[torch.Tensor] = None   # fp32 [num_adapters] factors, or None (all 1)
+    dequant: Optional[torch.Tensor] = None         # e4m3 pools: fp32 [num_adapters][2]
+    widened: Optional[torch.Tensor] = None         # e4m3 pools: bf16 scratch [a_elems + b_elems]
 
     @property
     def num_adapters(self):
@@ -190,6 +194,42 @@ def build_pool(A: List[torch.Tensor], B: List[torch.Tensor], K: int, N: int, dev
                        rank.data_ptr(), a_elems, b_elems, len(A), max(rpad) if rpad else 0, K, N,
                        asc.data_ptr() if asc is not None else None)
     return LoraPool(a_pool, b_pool, a_offset, b_offset, rank, desc, ranks, rpad, asc)
+
+
+def build_pool_e4m3(A8: List[torch.Tensor], B8: List[torch.Tensor], deq: Sequence[tuple], K: int, N: int,
+                    device="cuda", adapter_scale: Optional[Sequence[float]] = None,
+                    widened: bool = True) -> LoraPool:
+    """An e4m3 pool: codes A8_i uint8 [r_i, K] and B8_i uint8 [N, r_i] in the
+    layout of build_pool (one byte per element), dequant factors deq[i] =
+    (a, b), and (``widened``) the bf16 scratch the schedules for more than
+    64 tokens widen the used adapters into."""
+    ranks = [int(a.shape[0]) for a in A8]
+    a_off, b_off, rpad, a_elems, b_elems = lora_pool_layout(ranks, K, N)
+    u8 = torch.uint8
+    a_pool = torch.zeros(max(a_elems, 16), dtype=u8, device=device)
+    b_pool = torch.zeros(max(b_elems, 16), dtype=u8, device=device)
+    for i, (a, b) in enumerate(zip(A8, B8)):
+        r, rp = ranks[i], rpad[i]
+        assert a.shape == (r, K) and b.shape == (N, r) and a.dtype == u8 and b.dtype == u8
+        a_pool[a_off[i]:a_off[i] + r * K] = a.to(device).reshape(-1)
+        bp = torch.zeros(N, rp, dtype=u8, device=device)
+        bp[:, :r] = b.to(device)
+        b_pool[b_off[i]:b_off[i] + rp * N] = bp.reshape(N, rp // 16, 16).permute(1, 0, 2).contiguous().reshape(-1)
+    a_offset = torch.tensor(a_off or [0], dtype=torch.int64, device=device)
+    b_offset = torch.tensor(b_off or [0], dtype=torch.int64, device=device)
+    rank = torch.tensor(rpad or [0], dtype=torch.int32, device=device)
+    asc = None
+    if adapter_scale is not None:
+        asc = torch.tensor([float(v) for v in adapter_scale] or [1.0], dtype=torch.float32, device=device)
+    dq = torch.tensor([float(v) for pair in deq for v in pair] or [1.0, 1.0], dtype=torch.float32, device=device)
+    wid = torch.zeros(max(a_elems + b_elems, 8), dtype=torch.bfloat16, device=device) if widened else None
+    desc = lora_pool_t(a_pool.data_ptr(), b_pool.data_ptr(), a_offset.data_ptr(), b_offset.data_ptr(),
+                       rank.data_ptr(), a_elems, b_elems, len(A8), max(rpad) if rpad else 0, K, N,
+                       asc.data_ptr() if asc is not None else None)
+    desc.adapter_type = LORA_ADAPTER_E4M3
+    desc.dequant = dq.data_ptr()
+    desc.widened = wid.data_ptr() if wid is not None else None
+    return LoraPool(a_pool, b_pool, a_offset, b_offset, rank, desc, ranks, rpad, asc, dq, wid)
 
 
 def build_pool_sliced(A_s: List[List[torch.Tensor]], B_s: List[List[torch.Tensor]], K: int, slices: Sequence[int],
