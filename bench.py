@@ -52,10 +52,14 @@ CONFIG_TEXT = {
 SWEEP_EXTRA = {
     "qkv_sliced": "merged QKV with one adapter pair per slice: the qkv config's M, K and ids, output slices "
                   "4096 | 1024 | 1024, 8 adapters of rank 16 per slice",
+    "decode_e4m3": "the decode step with its adapters stored as e4m3 codes (one byte per element) and one "
+                   "dequant factor per adapter and factor; the same x, W, bias and ids",
 }
 
 
 def make_workload(name):
+    if name == "decode_e4m3":
+        return workloads.to_e4m3(workloads.make_config("decode"))
     if name == "qkv_sliced":
         base = workloads.make_config("qkv")
         return workloads.make_sliced(base.M, base.K, [4096, 1024, 1024], [16] * 8, seed=1237, ids=base.ids.clone())
@@ -78,8 +82,9 @@ def algorithmic_work(wl):
     S = len(wl.slices) if getattr(wl, "slices", None) else 1
     present = sorted(set(int(i) for i in ids.tolist() if 0 <= i < wl.num_adapters))
     adapter_elems = sum(wl.ranks[i] * (S * wl.K + wl.N) for i in present)
-    nbytes = 2 * (wl.N * wl.K + wl.M * wl.K + wl.M * wl.N + (wl.N if wl.bias is not None else 0)
-                  + adapter_elems) + 4 * wl.M
+    adapter_bytes = adapter_elems * (1 if getattr(wl, "A8", None) is not None else 2)   # e4m3: one byte each
+    nbytes = 2 * (wl.N * wl.K + wl.M * wl.K + wl.M * wl.N + (wl.N if wl.bias is not None else 0)) \
+        + adapter_bytes + 4 * wl.M
     lora_flops = sum(2 * wl.ranks[int(i)] * (S * wl.K + wl.N) for i in ids.tolist() if 0 <= i < wl.num_adapters)
     flops = 2 * wl.M * wl.K * wl.N + lora_flops
     return nbytes, flops, len(present)
@@ -218,6 +223,8 @@ class InputSet:
         self.ids = wl.ids.to(device)
         if getattr(wl, "slices", None):
             self.pool = L.build_pool_sliced(wl.A_s, wl.B_s, wl.K, wl.slices, device)
+        elif getattr(wl, "A8", None) is not None:
+            self.pool = L.build_pool_e4m3(wl.A8, wl.B8, wl.deq, wl.K, wl.N, device, widened=wl.M > 64)
         else:
             self.pool = L.build_pool(wl.A, wl.B, wl.K, wl.N, device)
         self.y = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device=device)
@@ -350,7 +357,7 @@ def run_config(name, L, device, steps, warmup, stream, sampler=None, dist_barrie
     return res
 
 
-SWEEP_LINES = ("prefill", "qkv", "mlp_down", "qkv_sliced", "attention_block_prefill", "moe_experts")
+SWEEP_LINES = ("prefill", "qkv", "mlp_down", "qkv_sliced", "decode_e4m3", "attention_block_prefill", "moe_experts")
 
 LAYER_SHAPES = (("q", 4096, 4096), ("k", 4096, 1024), ("v", 4096, 1024), ("o", 4096, 4096))
 
@@ -679,11 +686,12 @@ def ours(args):
     if not args.no_sweep and rank == 0:
         sweep = {}
         lines = set(args.sweep.split(","))
-        for name in ("prefill", "qkv", "mlp_down", "qkv_sliced"):
+        for name in ("prefill", "qkv", "mlp_down", "qkv_sliced", "decode_e4m3"):
             if name == args.config or name not in lines:
                 continue
             samp = ClockSampler(local)
-            s = run_config(name, L, device, 30 if name == "mlp_down" else 100, 5, stream, e2e=False, sampler=samp)
+            nsteps = 30 if name == "mlp_down" else 2000 if name == "decode_e4m3" else 100
+            s = run_config(name, L, device, nsteps, 5 if nsteps < 1000 else 100, stream, e2e=False, sampler=samp)
             kt = s["kernel_ms"] * 1e-3
             sk = dominant_kernel(s["wl"])
             sweep[name] = {

@@ -62,7 +62,7 @@ constexpr int kStMaxRegions = 16;
 constexpr int kStMaxRuns = 4;              // shrink runs (windows) of one CTA
 constexpr int kStWin = 8;                  // rank panels per window
 constexpr int kStMaxWinCta = 64;           // expand windows of one CTA
-constexpr int kBarMeta = 1;                // named barrier: metadata ready (every warp but the MMA issuer)
+constexpr int kBarMeta = 1;                // named barrier: metadata ready (the producer and the epilogue warps)
 constexpr int kBarMma = 2;                 // named barrier: metadata ready (MMA issuer + warp 2)
 constexpr int kBarLoad = 3;                // named barrier: the four loader warps
 constexpr int kBarEpi = 4;                 // named barrier: the four epilogue warps
@@ -74,7 +74,7 @@ constexpr int kBarTablesLd = 9;            // named barrier: panel tables ready 
 constexpr int kTablesLdThreads = 160;      // warp 2 + warps 6..9
 constexpr int kBarTouch = 10;              // named barrier: expand windows' touched flags (warp 6 -> epilogue)
 constexpr int kStFirst = 3;                // K units issued before the metadata is known
-constexpr int kMetaThreads = kClThreads - 32;
+constexpr int kMetaThreads = 160;   // warps 0 and 2..5 (the loaders learn of the plan through kBarTablesLd)
 
 enum StKind { kStBase = 0, kStShrink = 1, kStExpand = 2 };
 
@@ -471,8 +471,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         // stream.  A slot is reused only after the MMAs of the window it
         // held have read it.
         const int lt = threadIdx.x - 192;
-        named_bar_sync(kBarMeta, kMetaThreads);
-        named_bar_sync(kBarTablesLd, kTablesLdThreads);   // s_win_*; and s_ids, s_tsc unless every window is shrunk
+        named_bar_sync(kBarTablesLd, kTablesLdThreads);   // the plan (written before it) and the tables   // s_win_*; and s_ids, s_tsc unless every window is shrunk
         const int ew0 = *n_exp ? segs[*n_segs].a : 0;
         const int ew1 = *n_exp ? segs[*n_segs].b : 0;
         if (allw && warp == meta_warp) {
@@ -828,17 +827,21 @@ __global__ void __launch_bounds__(kClThreads, 1)
             if (!b_box) {
                 // A: box row et (128 K codes) -> row et of K blocks 0 and 1,
                 // 128-byte swizzle (16-byte chunk q at (q ^ (row & 7)) * 16);
-                // only this thread reads the row it overwrites
+                // only this thread reads the row it overwrites.  Step h
+                // reads the row's 16-code group h ^ (et & 7), so the eight
+                // threads of a quarter warp read eight different banks.
+                const int rot = et & 7;
 #pragma unroll
-                for (int h = 0; h < 8; ++h) c[h] = reinterpret_cast<const uint4 *>(box + et * 128)[h];
+                for (int h = 0; h < 8; ++h) c[h] = reinterpret_cast<const uint4 *>(box + et * 128)[h ^ rot];
 #pragma unroll
                 for (int h = 0; h < 8; ++h) {
+                    const int g = h ^ rot;   // the 16-code group in c[h]: K block g >> 2, chunks 2 (g & 3) and + 1
                     uint32_t o[8];
                     e4m3x16_to_bf16(c[h], o);
-                    uint8_t *rowp = wa + (h >> 2) * (kSplitBN * kBK * 2) + et * 128;
-                    const int q = 2 * (h & 3);
-                    *reinterpret_cast<uint4 *>(rowp + ((q ^ (et & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                    *reinterpret_cast<uint4 *>(rowp + (((q + 1) ^ (et & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+                    uint8_t *rowp = wa + (g >> 2) * (kSplitBN * kBK * 2) + et * 128;
+                    const int q = 2 * (g & 3);
+                    *reinterpret_cast<uint4 *>(rowp + ((q ^ rot) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4 *>(rowp + (((q + 1) ^ rot) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
                 }
             } else {
                 // B: row et of each of the 8 panels (16 codes) -> 32-byte rows,

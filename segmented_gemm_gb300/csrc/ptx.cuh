@@ -359,16 +359,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
-// Two e4m3 codes (low byte first) -> two bf16 values (low half first).
-// Every e4m3 value is an f16 and a bf16 value: the widening is exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t codes)
+// e4m3 codes -> bf16, exactly.  An e4m3 code s.eeee.mmm shifted into bf16
+// bit positions (sign to bit 15, eeeemmm to bits 10..4) is the bf16 value
+// (-1)^s (1.mmm) 2^(e - 127) for e > 0, and (-1)^s (m / 8) 2^-126 for e = 0
+// (a bf16 subnormal); both are the e4m3 value times 2^-120.  One bf16
+// multiply by 2^120 (exact: at most 4 significant bits) rebases the
+// exponent, subnormals included.  The NaN codes (eeee.mmm all ones) become
+// the bf16 NaN.
+__device__ __forceinline__ uint32_t e4m3_pair_to_bf16x2(uint32_t p)   // codes in bits 0..7 and 16..23
 {
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
-    float lo, hi;
-    asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"(static_cast<uint16_t>(h2 & 0xFFFFu)));
-    asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(static_cast<uint16_t>(h2 >> 16)));
-    return pack_bf16x2(lo, hi);
+    const uint32_t em = p & 0x007F007Fu;
+    const uint32_t t = (em << 4) | ((p & 0x00800080u) << 8);
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x7B807B80u));   // x 2^120 in both halves
+    // em + 1 carries into bit 7 of a half only where em is 0x7F (a NaN code)
+    const uint32_t nan = (((em + 0x00010001u) & 0x00800080u) >> 7) * 0xFFFFu;
+    return (r & ~nan) | (0x7FC07FC0u & nan);
 }
 
 // 16 e4m3 codes (one uint4) -> 16 bf16 values (o[0..3]: codes 0..7, o[4..7]: codes 8..15).
@@ -377,8 +383,8 @@ __device__ __forceinline__ void e4m3x16_to_bf16(const uint4 c, uint32_t (&o)[8])
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        o[2 * k] = e4m3x2_to_bf16x2(static_cast<uint16_t>(w[k] & 0xFFFFu));
-        o[2 * k + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(w[k] >> 16));
+        o[2 * k] = e4m3_pair_to_bf16x2(__byte_perm(w[k], 0u, 0x4140));       // codes 4k, 4k + 1
+        o[2 * k + 1] = e4m3_pair_to_bf16x2(__byte_perm(w[k], 0u, 0x4342));   // codes 4k + 2, 4k + 3
     }
 }
 

@@ -127,3 +127,32 @@ def test_e4m3_widening_needs_its_scratch():
     with pytest.raises(L.LoraError) as e:
         L.lora_linear(dev["x"], dev["W"], dev["bias"], dev["ids"], dev["pool"], wl8.scale, ws)
     assert e.value.code == L.LORA_ERR_NULL
+
+
+@pytest.mark.parametrize("path", [L.LORA_PATH_STREAM, L.LORA_PATH_SPLITK, L.LORA_PATH_TILED])
+def test_e4m3_every_code_is_widened_exactly(path):
+    """Every finite e4m3 code, read back exactly through a schedule: x is
+    one-hot (token t selects K column t), A's first 16 columns hold the 256
+    codes (A[j, k] = code 16 j + k), B is the identity (code 0x38 = 1.0),
+    factors are 1 and W is zero, so y[t, n] = A[n, t] with no rounding
+    anywhere.  Compared with the oracle's decode, bit for bit."""
+    M, K, N, r = 16, 256, 16, 16
+    codes = torch.arange(256, dtype=torch.int64).reshape(16, 16)
+    codes[(codes & 0x7F) == 0x7F] = 0          # the two NaN codes
+    A8 = torch.zeros(r, K, dtype=torch.uint8)
+    A8[:, :16] = codes.to(torch.uint8)
+    B8 = torch.zeros(N, r, dtype=torch.uint8)
+    B8[torch.arange(N), torch.arange(N)] = 0x38
+    pool = L.build_pool_e4m3([A8], [B8], [(1.0, 1.0)], K, N, "cuda")
+    x = torch.zeros(M, K, dtype=torch.bfloat16)
+    x[torch.arange(M), torch.arange(M)] = 1.0
+    W = torch.zeros(N, K, dtype=torch.bfloat16)
+    ids = torch.zeros(M, dtype=torch.int32)
+    ws = L.Workspace(M, N, 1)
+    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    L.lora_linear(x.cuda(), W.cuda(), None, ids.cuda(), pool, 1.0, ws, y=y, path=path)
+    assert L.lora_get_status(ws) == 0
+    want = torch.tensor([[oracle.e4m3_to_f64(int(codes[n, t])) for n in range(N)] for t in range(M)],
+                        dtype=torch.float64)
+    got = y.double().cpu()
+    assert torch.equal(got, want), f"path {path}: {int((got != want).sum())} codes differ"
