@@ -414,6 +414,19 @@ int lora_moe(const lora_bf16_t *x, int64_t M, int32_t K, const lora_bf16_t *W, i
  */
 int lora_get_status(void *ws, lora_stream_t stream, int32_t *status);
 
+/*
+ * Test knob for the bounded waits of the tiled schedule's kernel (the one
+ * lora_linear runs for M > 128, lora_linear_layers, lora_shrink,
+ * lora_expand and lora_moe_gemm use): each wait gives up after `cycles` SM
+ * clock cycles, sets LORA_DEV_TIMEOUT and lets the kernel run to its end.
+ * cycles = 0 restores the default (2e9 cycles, about one second).  A budget
+ * shorter than a healthy wait reports timeouts on healthy calls, so this is
+ * for exercising the timeout path, not for production.  Process-wide; read
+ * when a call is enqueued.  Returns LORA_ERR_SHAPE for cycles < 0.  The
+ * method has no counterpart: it is part of this library's failure detection.
+ */
+int lora_set_wait_budget(int64_t cycles);
+
 /* Static text for a LORA_ERR_* code. */
 const char *lora_status_string(int code);
 

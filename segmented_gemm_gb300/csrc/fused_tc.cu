@@ -278,6 +278,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *status = p.counters + CNT_STATUS;
+    const long long wait = p.wait_cycles;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kXStages; ++s) {
@@ -385,7 +386,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
             for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++iw) {
                 const int s = iw % kWStages;
                 const uint32_t round = iw / kWStages;
-                if (lane == 0 && round > 0) mbar_wait(&emptyw[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                if (lane == 0 && round > 0) mbar_wait(&emptyw[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                 __syncwarp();
                 uint8_t *wsl = wring + s * kWSlot;
                 if (jb.kind == 1) {
@@ -410,7 +411,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                         // every K piece of every shrink job of the tile (this layer's)
                         const int ci = jb.layer * p.num_mtiles + jb.m;
                         wait_flag_geq(p.counters + CNT_FIXED + ci, p.tile_njobs[jb.m] * p.s_sets, abort_flag, status,
-                                      LORA_DEV_TIMEOUT);
+                                      LORA_DEV_TIMEOUT, wait);
                         fence_proxy_async_global();
                         settle();
                         rst_old = atom_acq_rel_gpu_add(cons + ci, 1);
@@ -422,7 +423,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                 for (int cg = jb.c0; cg < jb.c1; cg += kPanelsPerStage, ++iw) {
                     const int s = iw % kWStages;
                     const uint32_t round = iw / kWStages;
-                    if (lane == 0 && round > 0) mbar_wait(&emptyw[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                    if (lane == 0 && round > 0) mbar_wait(&emptyw[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                     __syncwarp();
                     uint8_t *wsl = wring + s * kWSlot;   // [S panels [set][chunk] | B panels [chunk]]
                     const int nc = min(kPanelsPerStage, jb.c1 - cg);
@@ -442,7 +443,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                 }
             }
         }
-        if (lane == 0) settle();
+        if (lane == 0) {
+            settle();
+            // every load this warp issued has landed before the CTA ends (after
+            // a timeout the MMA may have stopped waiting for some): the last
+            // phase of each W slot
+            for (uint32_t i = iw > kWStages ? iw - kWStages : 0; i < iw; ++i)
+                mbar_wait(&fullw[i % kWStages], (i / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+        }
     } else if (warp >= 6) {
         // ===================== x loaders: permuted-row gather (cp.async) =====
         // Thread lt copies 16-byte chunk (lt % 8) of rows lt/8 + 16q, q < 8,
@@ -470,7 +478,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
             for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++ix) {
                 const int s = ix % kXStages;
                 const uint32_t round = ix / kXStages;
-                if (lane == 0 && round > 0) mbar_wait(&emptyx[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                if (lane == 0 && round > 0) mbar_wait(&emptyx[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                 __syncwarp();
                 uint8_t *xs = xring + s * kXSlot + swz;
                 const uint32_t nbytes = (kb * kBK + chunk * 8 < Ly.K) ? 16u : 0u;
@@ -483,9 +491,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
     } else if (warp == 1) {
         // ===================== MMA issuer ====================================
         uint32_t iw = 0, ix = 0;
+        int last_q = -1;
         for (int q = 0; get_item(q, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, jb); ++q) {
             const uint32_t slot = q & 1, use = q >> 1;
-            if (use > 0) mbar_wait(&acc_empty[slot], (use - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+            if (use > 0) mbar_wait(&acc_empty[slot], (use - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
             tc_fence_after();
             const uint32_t d = tmem_base + slot * kAccCols;
             const int n_mma = jb.kind == 0 ? (jb.c1 - jb.c0) * kChunk : kBN;
@@ -493,8 +502,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
             uint32_t acc = 0;
             for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++iw, ++ix) {
                 const int sw = iw % kWStages, sx = ix % kXStages;
-                mbar_wait(&fullx[sx], (ix / kXStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
-                mbar_wait(&fullw[sw], (iw / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                mbar_wait(&fullx[sx], (ix / kXStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+                mbar_wait(&fullw[sw], (iw / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                 fence_proxy_async_smem();   // x arrived through the generic proxy (cp.async)
                 tc_fence_after();
                 if (lane == 0) {
@@ -515,7 +524,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                 const uint32_t idesc_e = umma_idesc_bf16(kBM, kBN);
                 for (int cg = jb.c0; cg < jb.c1; cg += kPanelsPerStage, ++iw) {
                     const int sw = iw % kWStages;
-                    mbar_wait(&fullw[sw], (iw / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                    mbar_wait(&fullw[sw], (iw / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                     tc_fence_after();
                     if (lane == 0) {
                         const uint32_t sa = smem_u32(wring + sw * kWSlot);
@@ -534,7 +543,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
             }
             if (lane == 0) umma_commit(&acc_full[slot]);
             __syncwarp();
+            last_q = q;
         }
+        // the last commit covers every MMA this thread issued: they are done
+        // before the tensor memory is freed, even if the epilogue stopped
+        // waiting for them after a timeout
+        if (lane == 0 && last_q >= 0)
+            mbar_wait(&acc_full[last_q & 1], (last_q >> 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+        __syncwarp();
     } else if (warp >= 2) {
         // ===================== epilogue (warps 2..5) =========================
         const int quad = warp & 3;
@@ -579,7 +595,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
             const bool staged = kCanStage && (p.mode == kModeLinear || p.mode == kModeMoe) && jb.kind == 1 &&
                                 jb.part != kPartTail &&
                                 !get_item(q + 1, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, nx);
-            mbar_wait(&acc_full[slot], use & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+            mbar_wait(&acc_full[slot], use & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
             tc_fence_after();
             const uint32_t tbase = tmem_base + slot * kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
 
@@ -675,14 +691,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                     ntail = sk_tail_count(blockIdx.x, jb.slot, sk, Ly.kblocks);
                     tail0 = sk_next_tail(blockIdx.x - sk.rs, sk);
                     if (et == 0) {   // every tail piece has stored its partial sums
-                        wait_flag_geq(p.sk_cnt + jb.slot * kWinCntStride, ntail, abort_flag, status, LORA_DEV_TIMEOUT);
+                        wait_flag_geq(p.sk_cnt + jb.slot * kWinCntStride, ntail, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                         fence_proxy_async_global();   // their stores -> the bulk copies' reads
                         mbar_expect_tx(sk_bar, kBM * kBN * 4);
                         const uint8_t *src = reinterpret_cast<const uint8_t *>(p.sk_part) +
                                              static_cast<int64_t>(tail0) * kBM * kBN * 4;
                         for (int i = 0; i < 4; ++i) bulk_load(wring + i * kWSlot, src + i * kWSlot, kWSlot, sk_bar);
                     }
-                    mbar_wait(sk_bar, 0, abort_flag, status, LORA_DEV_TIMEOUT);
+                    mbar_wait(sk_bar, 0, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                     // further tails: each thread adds them into its own row of
                     // the shared-memory copy, sixteen loads in flight at a time
                     float4 *sp = reinterpret_cast<float4 *>(wring);
@@ -792,7 +808,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                     bulk_commit();
                     bulk_wait_read_all();   // the row is out of shared memory; y is written before the grid ends
                 }
-                if (head && et == 0) p.sk_cnt[jb.slot * kWinCntStride] = 0;   // zero again for the next call
+                if (head && et == 0) {
+                    p.sk_cnt[jb.slot * kWinCntStride] = 0;   // zero again for the next call
+                    // the partial sums' bulk copies have landed before the CTA
+                    // ends, even if the wait above gave up after a timeout
+                    mbar_wait(sk_bar, 0, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+                }
             }
         }
     }

@@ -57,6 +57,11 @@ enum Counters {
     CNT_FIXED = 8         // first per-tile counter
 };
 
+// long budget of the tiled kernel's bounded waits (SM clock cycles), set by
+// lora_set_wait_budget; read when a tiled launch is enqueued
+constexpr int64_t kDefaultWaitCycles = 2000000000ll;
+int64_t tc_wait_cycles();
+
 struct WsLayout {
     int64_t M;
     int32_t N, A;
@@ -147,6 +152,7 @@ struct TcParams {
     int32_t s_set_rows;        // rows of one S panel set (chunks x 128)
     float *sk_part;            // fp32 [CTAs][256/4][128][4]: each tail piece's partial sums, in its CTA's slot
     int32_t *sk_cnt;           // [tiles][kWinCntStride]: tail pieces stored per split tile (zero at rest)
+    int64_t wait_cycles;       // long budget of the kernel's bounded waits, in SM clock cycles
     TcLayer layer[kMaxLayers];
 };
 

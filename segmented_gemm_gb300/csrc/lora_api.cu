@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -317,6 +318,10 @@ static int prepare(const int32_t *ids, int64_t M, const lora_pool_t *pool, const
     return build ? enqueue_segments(ids, M, pool, *L, ws, stream) : LORA_OK;
 }
 
+static std::atomic<int64_t> g_wait_cycles{kDefaultWaitCycles};
+
+int64_t tc_wait_cycles() { return g_wait_cycles.load(std::memory_order_relaxed); }
+
 // The shared part of a tiled launch's parameters (the table, the workspace,
 // the S panel scratch at s_panels); the layers are filled by run_tiled.
 static void fill_tc_params(TcParams &p, const WsLayout &L, void *ws, const lora_pool_t *pool, int64_t M,
@@ -343,6 +348,7 @@ static void fill_tc_params(TcParams &p, const WsLayout &L, void *ws, const lora_
     p.tile_njobs = at<int32_t>(ws, L.tile_njobs);
     p.counters = at<int32_t>(ws, L.counters);
     p.shrink_split = 1;
+    p.wait_cycles = tc_wait_cycles();
     p.s_sets = 1;
     p.s_set_rows = L.max_chunks * kBM;
 }
@@ -822,6 +828,7 @@ int lora_moe_gemm(const lora_bf16_t *x, int64_t M, int32_t K, const lora_bf16_t 
     p.counters = at<int32_t>(ws, L.counters);
     p.mt_expert = at<int32_t>(ws, L.mt_expert);
     p.shrink_split = 1;
+    p.wait_cycles = tc_wait_cycles();
     p.s_sets = 1;
     TcLayerMaps &m = a.maps[0];
     const uint64_t Kq = K;
@@ -1084,6 +1091,13 @@ int lora_expand(const float *S, int32_t s_cols, int64_t M, const int32_t *lora_i
     lora_pool_t wpool;   // e4m3: the widened pool, the factor times B's factor
     if ((rc = widen_pool(pool, L, ws, kWidenExpand, 0, s, &wpool))) return rc;
     return run_tiled(nullptr, M, nullptr, nullptr, lora_id_map, &wpool, scale, y, ws, ws_bytes, L, kModeExpand, nullptr, s_cols, S, s);
+}
+
+int lora_set_wait_budget(int64_t cycles)
+{
+    if (cycles < 0) return LORA_ERR_SHAPE;
+    g_wait_cycles.store(cycles ? cycles : kDefaultWaitCycles, std::memory_order_relaxed);
+    return LORA_OK;
 }
 
 int lora_get_status(void *ws, lora_stream_t stream, int32_t *status)

@@ -109,18 +109,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 // Cycle budgets of the bounded waits: a healthy wait ends in microseconds;
 // the long budget (~1 s at 2 GHz) only runs out when something is broken,
 // after which every later wait of the CTA uses the short budget so the
-// kernel drains quickly instead of hanging.
+// kernel drains quickly instead of hanging.  A kernel may pass a shorter
+// long budget of its own (the tiled kernel takes it from its parameters).
 constexpr long long kWaitLong = 2000000000ll;
 constexpr long long kWaitShort = 200000ll;
+
+__device__ __forceinline__ long long wait_budget(volatile int *abort, long long budget)
+{
+    return *abort ? (budget < kWaitShort ? budget : kWaitShort) : budget;
+}
 
 // Wait for completion of the phase with the given parity.  Returns false
 // (and raises *abort + the device status bit) when the budget runs out.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          int32_t *status, int32_t timeout_bit)
+                                          int32_t *status, int32_t timeout_bit, long long long_budget = kWaitLong)
 {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
-    const long long budget = *abort ? kWaitShort : kWaitLong;
+    const long long budget = wait_budget(abort, long_budget);
     const long long t0 = clock64();
     while (!mbar_try_wait(a, parity)) {
         if (clock64() - t0 > budget) {
@@ -134,10 +140,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 
 // Spin (bounded) until *flag >= target with acquire semantics.
 __device__ __forceinline__ bool wait_flag_geq(const int32_t *flag, int target, volatile int *abort,
-                                              int32_t *status, int32_t timeout_bit)
+                                              int32_t *status, int32_t timeout_bit, long long long_budget = kWaitLong)
 {
     if (ld_acquire_gpu(flag) >= target) return true;
-    const long long budget = *abort ? kWaitShort : kWaitLong;
+    const long long budget = wait_budget(abort, long_budget);
     const long long t0 = clock64();
     while (ld_acquire_gpu(flag) < target) {
         if (clock64() - t0 > budget) {

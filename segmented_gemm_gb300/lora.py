@@ -33,7 +33,8 @@ LORA_MAX_RANK, LORA_RANK_ALIGN, LORA_MAX_ADAPTERS = 128, 16, 1024
 EXPORTS = ("lora_pool_layout", "lora_workspace_size", "lora_workspace_init", "lora_build_segments",
            "lora_shrink", "lora_expand", "lora_linear", "lora_linear_ex", "lora_get_status",
            "lora_status_string", "lora_linear_noalloc", "lora_moe_workspace_size", "lora_moe_route",
-           "lora_moe_gemm", "lora_moe_finalize", "lora_moe", "lora_layers_workspace_size", "lora_linear_layers")
+           "lora_moe_gemm", "lora_moe_finalize", "lora_moe", "lora_layers_workspace_size", "lora_linear_layers",
+           "lora_set_wait_budget")
 
 
 class lora_pool_t(ctypes.Structure):
@@ -98,6 +99,7 @@ def load_library():
         "lora_moe": (ctypes.c_int, [P, I64, I32, P, I32, P, P, I32, I32, P, P, P, SZ, P]),
         "lora_layers_workspace_size": (SZ, [I64, I32, I32, I32]),
         "lora_linear_layers": (ctypes.c_int, [P, I32, I64, P, PS, P, SZ, P]),
+        "lora_set_wait_budget": (ctypes.c_int, [I64]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -406,6 +408,12 @@ def lora_linear_noalloc(x: torch.Tensor, W: torch.Tensor, bias: Optional[torch.T
         _ptr(x), M, _ptr(W), _ptr(bias), _ptr(ids), ctypes.byref(pool.desc), float(scale), _ptr(y),
         _stream(stream)), "lora_linear_noalloc")
     return y
+
+
+def lora_set_wait_budget(cycles: int):
+    """Test knob: the tiled kernel's bounded waits give up after ``cycles``
+    SM clock cycles (0: the default, about one second)."""
+    _check(load_library().lora_set_wait_budget(int(cycles)), "lora_set_wait_budget")
 
 
 def lora_get_status(ws: Workspace, stream=None) -> int:

@@ -156,3 +156,9 @@ def test_moe_host_errors_without_gpu(lib):
     assert lib.lora_moe_route(None, 4, 2, 4, None, 0, None) == L.LORA_ERR_NULL
     assert lib.lora_moe_route(None, 0, 2, 4, None, 0, None) == L.LORA_OK             # no tokens: nothing to do
     assert lib.lora_moe_gemm(None, 4, 12, None, 64, 4, 2, None, None, 0, None) == L.LORA_ERR_SHAPE   # K % 8
+
+
+def test_wait_budget_knob_validates(lib):
+    assert lib.lora_set_wait_budget(-1) == L.LORA_ERR_SHAPE
+    assert lib.lora_set_wait_budget(1_000_000) == L.LORA_OK
+    assert lib.lora_set_wait_budget(0) == L.LORA_OK   # back to the default
