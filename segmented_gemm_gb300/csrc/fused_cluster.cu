@@ -103,36 +103,12 @@ __device__ __forceinline__ void tma_load_3d_st(void *dst, const CUtensorMap *m, 
         : "memory");
 }
 
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-
 __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint32_t remote_bar)
 {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
                      remote_addr),
                  "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
                  : "memory");
-}
-
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
-// Arrive without release semantics: used once the barriers a peer will
-// touch have been published with fence.mbarrier_init (a release arrive
-// would also wait for this thread's outstanding memory operations).
-__device__ __forceinline__ void cluster_arrive_relaxed()
-{
-    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
-
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
 }
 
 // Unit list of one CTA before its expand windows.  Shrink runs are the
@@ -436,8 +412,20 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 if (iu < static_cast<uint32_t>(nfirst)) continue;   // issued in the prologue
                 const int s = iu % p.stages;
                 const uint32_t round = iu / p.stages;
-                if (lane == 0) {
-                    if (round > 0) mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                // A slot's barriers get the unit's arrives only once their
+                // previous phases have completed (immediate in a healthy run:
+                // the MMA waited for them before freeing the slot), so an
+                // arrive always opens a new phase, also after a timeout let a
+                // wait go early; a unit whose slot never comes free is skipped.
+                bool ok = true;
+                if (lane == 0 && round > 0) {
+                    mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                    ok = mbar_wait(&full[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                }
+                if (lane == 0 && ok && p.fp8 && sg.kind != kStBase && icu >= static_cast<uint32_t>(p.stages))
+                    ok = mbar_wait(&codes[icu % p.stages], (icu / p.stages - 1) & 1, abort_flag, status,
+                                   LORA_DEV_TIMEOUT);
+                if (lane == 0 && ok) {
                     uint8_t *wa = smem + s * slot_bytes;
                     uint64_t *cb = &codes[icu % p.stages];
                     if (sg.kind == kStExpand && p.fp8) {   // 8-bit B codes; the slot carries nothing else

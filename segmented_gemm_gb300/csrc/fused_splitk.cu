@@ -173,8 +173,16 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 }
                 const int s = it % p.stages;
                 const uint32_t round = it / p.stages;
-                if (lane == 0 && round > 0) mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
-                __syncwarp();
+                // the slot's full barrier gets this stage's arrive only once its
+                // previous phase has completed (immediate in a healthy run), so
+                // the arrive opens a new phase also after a timeout let a wait
+                // go early; a stage whose slot never comes free is skipped
+                int ok = 1;
+                if (lane == 0 && round > 0) {
+                    mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                    ok = mbar_wait(&full[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                }
+                if (!__shfl_sync(0xffffffffu, ok, 0)) continue;
                 uint8_t *as = smem + s * stage_bytes;
                 uint8_t *bs = as + kSkASlot;
                 if (r.list == 0) {
