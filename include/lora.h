@@ -365,7 +365,7 @@ int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const 
  * handled as in lora_linear, but the status word is cleared by the next call
  * and cannot be read through this entry point.
  */
-#define LORA_NOALLOC_SCRATCH_BYTES (16u << 20)   /* 16 MiB */
+#define LORA_NOALLOC_SCRATCH_BYTES (8u << 20)   /* 8 MiB */
 int lora_linear_noalloc(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,
                         const int32_t *lora_id_map, const lora_pool_t *pool, float scale, lora_bf16_t *y,
                         lora_stream_t stream);

@@ -36,8 +36,6 @@
 // mainloop of job j+1.
 #include <cuda_runtime.h>
 
-#include <algorithm>
-
 #include "internal.h"
 #include "lora.h"
 #include "ptx.cuh"
@@ -61,29 +59,12 @@ constexpr int kStageRow = kBN * 2 + 16;   // a staged output row: 512 bytes + 16
 // rows are scattered pairs, with 6 + 4 (both measured on GB300).
 constexpr int kXStagesLinear = 4, kWStagesLinear = 5;
 constexpr int kXStagesMoe = 6, kWStagesMoe = 4;
-// CTA pairs: a CTA loads half of each W tile (128 rows, 16 KB) and half of
-// each chunk's B panel (128 rows, 4 KB), so a W slot of 16 KB holds a W
-// half-tile, half of a shrink job's panels, or an expand stage of one chunk
-// (S panels of two sets 8 KB + a B half 4 KB).  The same 224 KB then holds
-// 6 x slots and 8 W slots: the deeper rings cover the extra hop each K step
-// takes through the odd CTA's forwarder.
-constexpr int kWSlotPair = 16 * 1024;
-constexpr int kBPanelBytesPair = kBM * kChunk * 2;   // 4 KB (128 rows x 16)
-constexpr int kPanelsPerStagePair = 1;
-constexpr int kXStagesPair = 6, kWStagesPair = 8;
-constexpr int kBarArea = 512;                        // mbarriers, TMEM address, abort flag
-constexpr int kSkChunk = kBM * kBN * 4 / 4;          // a split tile's partial sums come in as 4 copies of 32 KB
-template <int kXStages, int kWStages, bool kPair>
+template <int kXStages, int kWStages>
 constexpr size_t tc_smem_bytes()
 {
-    return kXStages * kXSlot + kWStages * (kPair ? kWSlotPair : kWSlot) + 1024 /*align*/ + kBarArea +
-           2 * kBN * 2 /*bias of two tiles*/;
+    return kXStages * kXSlot + kWStages * kWSlot + 1024 /*align*/ + 256 /*barriers*/ + 2 * kBN * 2 /*bias of two tiles*/;
 }
 static_assert(kSAreaBytes + kPanelsPerStage * kBPanelBytes <= kWSlot, "an expand stage fits in one W slot");
-static_assert(2 * kPanelsPerStagePair * kSPanelBytes + kPanelsPerStagePair * kBPanelBytesPair <= kWSlotPair,
-              "a pair's expand stage fits");
-static_assert(kBM * kBK * 2 <= kWSlotPair && kMaxShrinkChunks / 2 * kAPanelBytes <= kWSlotPair,
-              "a W half-tile and half of a shrink job's panels fit in a pair's W slot");
 
 struct Job {
     int kind;   // 0 shrink, 1 output
@@ -269,68 +250,48 @@ __device__ __forceinline__ int sk_tail_count(int b, int t, const SkPlan &s, int 
     return n;
 }
 
-template <int kXStages, int kWStages, bool kPair>
+template <int kXStages, int kWStages>
 __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_constant__ TcArgs args)
 {
     const TcParams &p = args.p;
     const CUtensorMap &tm_s = args.s;
-    constexpr int kWSl = kPair ? kWSlotPair : kWSlot;                  // W ring slot
-    constexpr int kBPanel = kPair ? kBPanelBytesPair : kBPanelBytes;   // a CTA's B panel of one chunk
-    constexpr int kTileRows = kPair ? kPairRows : kBM;                 // token rows of a tile
-    constexpr int kPPS = kPair ? kPanelsPerStagePair : kPanelsPerStage;   // chunks per expand stage
-    constexpr int kSArea = 2 * kPPS * kSPanelBytes;                   // S panels [set][chunk] of a stage
-    constexpr int kShare = kPair ? 2 : 1;                              // CTAs working on one tile
-    static_assert(kWStages * kWSl >= kBM * kBN * 4, "a split tile's fp32 partials fit in the W ring");
-    static_assert((2 * kXStages + 3 * kWStages + 5) * 8 + 8 <= kBarArea, "barriers, TMEM address and abort flag fit");
-    static_assert(tc_smem_bytes<kXStages, kWStages, kPair>() <= 232448, "fits the opt-in shared memory of a CTA");
+    static_assert(kWStages * kWSlot >= kBM * kBN * 4, "a split tile's fp32 partials fit in the W ring");
+    static_assert((2 * kXStages + 2 * kWStages + 5) * 8 + 8 <= 256, "barriers, TMEM address and abort flag fit");
+    static_assert(tc_smem_bytes<kXStages, kWStages>() <= 232448, "fits the opt-in shared memory of a CTA");
     // the last item's bf16 output is staged in the idle x ring when it fits
     constexpr bool kCanStage = kBM * kStageRow <= kXStages * kXSlot;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *xring = smem;                                  // kXStages x 16 KB
-    uint8_t *wring = smem + kXStages * kXSlot;              // kWStages x kWSl
-    uint64_t *fullx = reinterpret_cast<uint64_t *>(wring + kWStages * kWSl);
+    uint8_t *wring = smem + kXStages * kXSlot;              // kWStages x 32 KB
+    uint64_t *fullx = reinterpret_cast<uint64_t *>(wring + kWStages * kWSlot);
     uint64_t *emptyx = fullx + kXStages;
     uint64_t *fullw = emptyx + kXStages;
     uint64_t *emptyw = fullw + kWStages;
-    uint64_t *peerw = emptyw + kWStages;   // a pair's even CTA: the odd CTA's x and W slots of a stage have landed
-    uint64_t *acc_full = peerw + kWStages;
+    uint64_t *acc_full = emptyw + kWStages;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *sk_bar = acc_empty + 2;   // stream-K head: the partial sums have landed in the W ring
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sk_bar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     // bias of the output tile of each accumulator slot: [2][kBN] bf16 (16-byte aligned)
-    uint32_t *s_bias = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(fullx) + kBarArea);
+    uint32_t *s_bias = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(fullx) + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *status = p.counters + CNT_STATUS;
     const long long wait = p.wait_cycles;
-    // CTA pairs: the work list is dealt out per pair (both CTAs run the same
-    // items); rank 0 issues the pair's MMAs, each CTA holds rows row0.. of a
-    // token tile and W rows row0.. of a W tile
-    const int rank = kPair ? static_cast<int>(cluster_ctarank()) : 0;
-    const int unit = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const int units = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-    const int row0 = rank * kBM;
-    const bool issuer = !kPair || rank == 0;
 
     if (threadIdx.x == 0) {
-        // the issuing CTA of a pair counts one more arrive on its accumulator
-        // barriers (the peer's epilogue, passed on by the peer's warp 1); the
-        // peer's stages arrive on peerw, which carries no transaction bytes
-        const uint32_t peer = kPair && issuer ? 1u : 0u;
         for (int s = 0; s < kXStages; ++s) {
-            mbar_init(&fullx[s], 128);   // one cp.async-completion arrive per loader thread
+            mbar_init(&fullx[s], 128);    // one cp.async-completion arrive per loader thread
             mbar_init(&emptyx[s], 1);
         }
         for (int s = 0; s < kWStages; ++s) {
-            mbar_init(&fullw[s], 1);   // the producer's expect_tx arrive
+            mbar_init(&fullw[s], 1);      // the producer's expect_tx arrive
             mbar_init(&emptyw[s], 1);
-            mbar_init(&peerw[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], 128 + peer);
+            mbar_init(&acc_empty[a], 128);
         }
         mbar_init(sk_bar, 1);
         *abort_flag = 0;
@@ -343,21 +304,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
         tma_prefetch_map(&tm_s);
     }
     if (warp == 1) {
-        if constexpr (kPair) {
-            tmem_alloc_pair(tmem_slot, kTmemCols);
-            tmem_relinquish_pair();
-        } else {
-            tmem_alloc(tmem_slot, kTmemCols);
-            tmem_relinquish();
-        }
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
     }
     tc_fence_before();
-    if constexpr (kPair) {   // both CTAs' barriers exist before either CTA's arrives reach them
-        cluster_arrive();
-        cluster_wait();
-    } else {
-        __syncthreads();
-    }
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -368,7 +319,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
     int n_out = 0;   // output tiles of every layer
     if (p.mode != kModeShrink)
         for (int l = 0; l < p.num_layers; ++l) n_out += nmt * p.layer[l].num_ntiles;
-    SkPlan sk = sk_plan(n_sjobs, n_out, units, p.layer[0].kblocks, p.streamk != 0, p.shrink_split);
+    SkPlan sk = sk_plan(n_sjobs, n_out, gridDim.x, p.layer[0].kblocks, p.streamk != 0, p.shrink_split);
     sk.nmt = nmt;
     Job jb;
 
@@ -376,10 +327,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
         // ===================== TMA producer: W ring (W, A panels, S / B panels)
         uint32_t iw = 0;
         // The S-ready counter of (layer, token tile m) is put back to zero by
-        // the last of the layer's num_ntiles output tiles of row m (times the
-        // CTAs of a pair) to pass the wait on it: each adds itself to a
-        // consumer counter right after the wait and reads the result one item
-        // later, so the round trip hides behind the loads.
+        // the last of the layer's num_ntiles output tiles of row m to pass
+        // the wait on it: each adds itself to a consumer counter right after
+        // the wait and reads the result one item later, so the round trip
+        // hides behind the loads.
         int32_t *cons = p.counters + CNT_FIXED + p.num_layers * p.num_mtiles;
         int rst_m = -1, rst_old = 0, rst_nt = 0;   // counter index, consumers before me, the layer's tiles per row
         auto settle = [&]() {
@@ -403,26 +354,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
             }
             return __shfl_sync(0xffffffffu, ok, 0) != 0;
         };
-        for (int q = 0; get_item(q, unit, units, n_sjobs, n_out, sk, p, jb); ++q) {
+        for (int q = 0; get_item(q, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, jb); ++q) {
             const TcLayer &Ly = p.layer[jb.layer];
             const TcLayerMaps &mp = args.maps[jb.layer];
             // shrink job: consecutive rank panels of one adapter are
             // consecutive pool rows, loaded as one box of 16..64 rows per run.
             // The runs are found once per job, one lane per chunk: lane c
             // starts a run of run_len panels at pool row run_row, else 0.
-            // A pair splits the job's panels [c0, c1): the even CTA loads the
-            // first half (rounded up), the odd CTA the rest and, when their
-            // number is odd, the last panel once more (its columns are unused)
-            // so both halves of the MMA's B have the same height.
             int run_row = 0, run_len = 0;
-            int sc0 = jb.c0, sc1 = jb.c1, npan = jb.c1 - jb.c0;   // my panels, and how many I load
-            if constexpr (kPair) {
-                npan = (jb.c1 - jb.c0 + 1) >> 1;
-                sc0 = min(jb.c0 + rank * npan, jb.c1);
-                sc1 = min(sc0 + npan, jb.c1);
-            }
-            const int pad_row =
-                (kPair && jb.kind == 0 && lane == npan - 1 && sc0 + lane >= sc1) ? p.chunk_arow[jb.c1 - 1] : -1;
             // output job: the first B-pool row of the [N, 16] panel of each
             // of the tile's first 32 chunks, one lane per chunk, loaded now
             // for the expand steps
@@ -430,8 +369,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
             // kModeMoe: the tile's expert's rows of the stacked expert weights
             const int w_row0 = (p.mode == kModeMoe && jb.kind == 1) ? p.mt_expert[jb.m] * Ly.N : 0;
             if (jb.kind == 0) {
-                const int c = sc0 + lane;
-                const bool in = c < sc1;
+                const int c = jb.c0 + lane;
+                const bool in = c < jb.c1;
                 const int r = in ? p.chunk_arow[c] : -1;
                 const int prev = __shfl_up_sync(0xffffffffu, r, 1);
                 const bool start = in && (lane == 0 || prev != r - kChunk);
@@ -439,7 +378,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                 if (start) {
                     // up to the next start or the end of the job, at most 4 panels
                     const unsigned later = starts & ~((2u << lane) - 1u);
-                    const int next = later ? __ffs(later) - 1 : sc1 - sc0;
+                    const int next = later ? __ffs(later) - 1 : jb.c1 - jb.c0;
                     run_row = r;
                     run_len = next - lane;
                 }
@@ -461,21 +400,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
             for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++iw) {
                 const int s = iw % kWStages;
                 if (!slot_free(s, iw / kWStages)) continue;
-                uint8_t *wsl = wring + s * kWSl;
+                uint8_t *wsl = wring + s * kWSlot;
                 if (jb.kind == 1) {
-                    if (lane == 0) {   // the tile's W rows (a pair: this CTA's half)
-                        mbar_expect_tx(&fullw[s], kBN / kShare * kBK * 2);
-                        tma_load_2d(wsl, &mp.w, &fullw[s], kb * kBK, jb.n * kBN + row0 + w_row0);
+                    if (lane == 0) {
+                        mbar_expect_tx(&fullw[s], kWSlot);
+                        tma_load_2d(wsl, &mp.w, &fullw[s], kb * kBK, jb.n * kBN + w_row0);
                     }
                 } else {
-                    if (lane == 0) mbar_expect_tx(&fullw[s], npan * kAPanelBytes);
+                    if (lane == 0) mbar_expect_tx(&fullw[s], (jb.c1 - jb.c0) * kAPanelBytes);
                     __syncwarp();
                     if (run_len > 0) {
                         const CUtensorMap *m =
                             run_len == 1 ? &mp.a : run_len == 2 ? &mp.a32 : run_len == 3 ? &mp.a48 : &mp.a64;
                         tma_load_2d(wsl + lane * kAPanelBytes, m, &fullw[s], kb * kBK, run_row);
                     }
-                    if (pad_row >= 0) tma_load_2d(wsl + lane * kAPanelBytes, &mp.a, &fullw[s], kb * kBK, pad_row);
                 }
                 __syncwarp();
             }
@@ -483,35 +421,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                 if (p.mode == kModeLinear) {
                     if (lane == 0) {
                         // every K piece of every shrink job of the tile (this layer's)
-                        // (a pair: both CTAs' epilogues count each piece)
                         const int ci = jb.layer * p.num_mtiles + jb.m;
-                        wait_flag_geq(p.counters + CNT_FIXED + ci, p.tile_njobs[jb.m] * p.s_sets * kShare, abort_flag,
-                                      status, LORA_DEV_TIMEOUT, wait);
+                        wait_flag_geq(p.counters + CNT_FIXED + ci, p.tile_njobs[jb.m] * p.s_sets, abort_flag, status,
+                                      LORA_DEV_TIMEOUT, wait);
                         fence_proxy_async_global();
                         settle();
                         rst_old = atom_acq_rel_gpu_add(cons + ci, 1);
                         rst_m = ci;
-                        rst_nt = Ly.num_ntiles * kShare;
+                        rst_nt = Ly.num_ntiles;
                     }
                     __syncwarp();
                 }
-                for (int cg = jb.c0; cg < jb.c1; cg += kPPS, ++iw) {
+                for (int cg = jb.c0; cg < jb.c1; cg += kPanelsPerStage, ++iw) {
                     const int s = iw % kWStages;
                     if (!slot_free(s, iw / kWStages)) continue;
-                    uint8_t *wsl = wring + s * kWSl;   // [S panels [set][chunk] | B panels [chunk]]
-                    const int nc = min(kPPS, jb.c1 - cg);
-                    if (lane == 0) mbar_expect_tx(&fullw[s], nc * (p.s_sets * kSPanelBytes + kBPanel));
+                    uint8_t *wsl = wring + s * kWSlot;   // [S panels [set][chunk] | B panels [chunk]]
+                    const int nc = min(kPanelsPerStage, jb.c1 - cg);
+                    if (lane == 0) mbar_expect_tx(&fullw[s], nc * (p.s_sets * kSPanelBytes + kBPanelBytes));
                     __syncwarp();
                     const int ci = cg - jb.c0 + lane;   // chunk index inside the tile
                     const int brow_s = __shfl_sync(0xffffffffu, brow_l, ci & 31);
                     if (lane < nc) {
-                        // my rows of the S panels, my half of the B panel's rows (a pair)
                         const int c = cg + lane;
                         const int brow = ci < 32 ? brow_s : p.chunk_bpanel[c] * Ly.N;
                         for (int h = 0; h < p.s_sets; ++h)
-                            tma_load_2d(wsl + (h * kPPS + lane) * kSPanelBytes, &tm_s, &fullw[s], 0,
-                                        (jb.layer * p.s_sets + h) * p.s_set_rows + c * kTileRows + row0);
-                        tma_load_2d(wsl + kSArea + lane * kBPanel, &mp.b, &fullw[s], 0, brow + jb.n * kBN + row0);
+                            tma_load_2d(wsl + (h * kPanelsPerStage + lane) * kSPanelBytes, &tm_s, &fullw[s], 0,
+                                        (jb.layer * p.s_sets + h) * p.s_set_rows + c * kBM);
+                        tma_load_2d(wsl + kSAreaBytes + lane * kBPanelBytes, &mp.b, &fullw[s], 0, brow + jb.n * kBN);
                     }
                     __syncwarp();
                 }
@@ -537,13 +473,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
         const int chunk = lt & 7, rb = lt >> 3;
         const uint32_t swz = static_cast<uint32_t>((chunk ^ (rb & 7)) << 4);
         uint32_t ix = 0;
-        for (int q = 0; get_item(q, unit, units, n_sjobs, n_out, sk, p, jb); ++q) {
+        for (int q = 0; get_item(q, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, jb); ++q) {
             if (jb.kb1 <= jb.kb0) continue;
             const TcLayer &Ly = p.layer[jb.layer];
             const uint16_t *src[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-                int64_t pp = static_cast<int64_t>(jb.m) * kTileRows + row0 + rb + 16 * q;
+                int64_t pp = static_cast<int64_t>(jb.m) * kBM + rb + 16 * q;
                 if (pp >= p.M) pp = p.M - 1;
                 int64_t row = p.perm[pp];
                 if (p.mode == kModeMoe) row = row >= 0 ? row / p.topk : 0;   // a pair's token; a gap reads row 0
@@ -562,77 +498,60 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
             }
         }
         cp_async_wait_all();
-    } else if (warp == 1 && issuer) {
+    } else if (warp == 1) {
         // ===================== MMA issuer ====================================
-        // (a pair: the even CTA's thread issues MMAs over both CTAs' halves,
-        // and its commits arrive on the barrier of that name in both CTAs)
-        auto mma = [&](uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-            if constexpr (kPair) umma_bf16_pair(d, adesc, bdesc, idesc, acc);
-            else umma_bf16(d, adesc, bdesc, idesc, acc);
-        };
-        auto commit = [&](uint64_t *bar) {
-            if constexpr (kPair) umma_commit_pair(bar, 3);
-            else umma_commit(bar);
-        };
         uint32_t iw = 0, ix = 0;
         int last_q = -1;
-        for (int q = 0; get_item(q, unit, units, n_sjobs, n_out, sk, p, jb); ++q) {
+        for (int q = 0; get_item(q, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, jb); ++q) {
             const uint32_t slot = q & 1, use = q >> 1;
-            if (use > 0) mbar_wait<kPair>(&acc_empty[slot], (use - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+            if (use > 0) mbar_wait(&acc_empty[slot], (use - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
             tc_fence_after();
             const uint32_t d = tmem_base + slot * kAccCols;
-            // a shrink job's B: 16 rows per panel (a pair: two halves of
-            // (c1 - c0 + 1) / 2 panels each)
-            const int n_mma =
-                jb.kind == 0 ? (kPair ? 2 * kChunk * ((jb.c1 - jb.c0 + 1) >> 1) : (jb.c1 - jb.c0) * kChunk) : kBN;
-            const uint32_t idesc = umma_idesc_bf16(kTileRows, n_mma);
+            const int n_mma = jb.kind == 0 ? (jb.c1 - jb.c0) * kChunk : kBN;
+            const uint32_t idesc = umma_idesc_bf16(kBM, n_mma);
             uint32_t acc = 0;
             for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++iw, ++ix) {
                 const int sw = iw % kWStages, sx = ix % kXStages;
                 mbar_wait(&fullx[sx], (ix / kXStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                 mbar_wait(&fullw[sw], (iw / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
-                if constexpr (kPair)   // the odd CTA's x and W slots of this K step
-                    mbar_wait(&peerw[sw], (iw / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                 fence_proxy_async_smem();   // x arrived through the generic proxy (cp.async)
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t xa = smem_u32(xring + sx * kXSlot);
-                    const uint32_t wa = smem_u32(wring + sw * kWSl);
+                    const uint32_t wa = smem_u32(wring + sw * kWSlot);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
-                        mma(d, umma_sdesc(xa + kk * 32, 1024, kSwizzle128), umma_sdesc(wa + kk * 32, 1024, kSwizzle128),
-                            idesc, acc);
+                        umma_bf16(d, umma_sdesc(xa + kk * 32, 1024, kSwizzle128),
+                                  umma_sdesc(wa + kk * 32, 1024, kSwizzle128), idesc, acc);
                         acc = 1;
                     }
-                    commit(&emptyx[sx]);
-                    commit(&emptyw[sw]);
+                    umma_commit(&emptyx[sx]);
+                    umma_commit(&emptyw[sw]);
                 }
                 __syncwarp();
             }
             if (jb.kind == 1 && jb.c1 > jb.c0 && jb.part != kPartTail) {
-                const uint32_t idesc_e = umma_idesc_bf16(kTileRows, kBN);
-                for (int cg = jb.c0; cg < jb.c1; cg += kPPS, ++iw) {
+                const uint32_t idesc_e = umma_idesc_bf16(kBM, kBN);
+                for (int cg = jb.c0; cg < jb.c1; cg += kPanelsPerStage, ++iw) {
                     const int sw = iw % kWStages;
                     mbar_wait(&fullw[sw], (iw / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
-                    if constexpr (kPair)
-                        mbar_wait(&peerw[sw], (iw / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t sa = smem_u32(wring + sw * kWSl);
-                        const uint32_t ba = sa + kSArea;
-                        const int nc = min(kPPS, jb.c1 - cg);
+                        const uint32_t sa = smem_u32(wring + sw * kWSlot);
+                        const uint32_t ba = sa + kSAreaBytes;
+                        const int nc = min(kPanelsPerStage, jb.c1 - cg);
                         for (int i = 0; i < nc; ++i)
                             for (int h = 0; h < p.s_sets; ++h) {   // (S_0 + S_1) B^T, set by set
-                                mma(d, umma_sdesc(sa + (h * kPPS + i) * kSPanelBytes, 256, kSwizzle32),
-                                    umma_sdesc(ba + i * kBPanel, 256, kSwizzle32), idesc_e, acc);
+                                umma_bf16(d, umma_sdesc(sa + (h * kPanelsPerStage + i) * kSPanelBytes, 256, kSwizzle32),
+                                          umma_sdesc(ba + i * kBPanelBytes, 256, kSwizzle32), idesc_e, acc);
                                 acc = 1;
                             }
-                        commit(&emptyw[sw]);
+                        umma_commit(&emptyw[sw]);
                     }
                     __syncwarp();
                 }
             }
-            if (lane == 0) commit(&acc_full[slot]);
+            if (lane == 0) umma_commit(&acc_full[slot]);
             __syncwarp();
             last_q = q;
         }
@@ -642,51 +561,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
         if (lane == 0 && last_q >= 0)
             mbar_wait(&acc_full[last_q & 1], (last_q >> 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
         __syncwarp();
-    } else if (warp == 1) {
-        // ===================== odd CTA of a pair: forwarder ==================
-        // The even CTA's MMA reads this CTA's halves of A and B and writes
-        // this CTA's half of D: each K step whose x and W slots have landed
-        // here, each expand stage, and each accumulator this CTA's epilogue
-        // has read out, is passed on to the even CTA (one arrive on its peerw
-        // barrier of the stage's W slot, or on its accumulator barrier), in
-        // the order its MMA thread waits on them.  The stages' arrives are
-        // relaxed: the copies they
-        // announce have completed (and the x rows are fenced for the tensor
-        // core's proxy first); a release would make each arrive wait for the
-        // one before it to be performed.
-        const uint32_t lead_peerw = mapa_shared(smem_u32(peerw), 0);
-        const uint32_t lead_acc_empty = mapa_shared(smem_u32(acc_empty), 0);
-        uint32_t iw = 0, ix = 0;
-        for (int q = 0; get_item(q, unit, units, n_sjobs, n_out, sk, p, jb); ++q) {
-            const uint32_t slot = q & 1, use = q >> 1;
-            if (use > 0) {
-                mbar_wait(&acc_empty[slot], (use - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
-                if (lane == 0) mbar_arrive_remote(lead_acc_empty + slot * 8);
-                __syncwarp();
-            }
-            for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++iw, ++ix) {
-                const int sw = iw % kWStages, sx = ix % kXStages;
-                mbar_wait(&fullx[sx], (ix / kXStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
-                mbar_wait(&fullw[sw], (iw / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
-                fence_proxy_async_smem();   // the x rows (generic proxy) before the tensor core reads them
-                if (lane == 0) mbar_arrive_remote_relaxed(lead_peerw + sw * 8);
-                __syncwarp();
-            }
-            if (jb.kind == 1 && jb.c1 > jb.c0 && jb.part != kPartTail) {
-                for (int cg = jb.c0; cg < jb.c1; cg += kPPS, ++iw) {
-                    const int sw = iw % kWStages;
-                    mbar_wait(&fullw[sw], (iw / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
-                    if (lane == 0) mbar_arrive_remote_relaxed(lead_peerw + sw * 8);
-                    __syncwarp();
-                }
-            }
-        }
     } else if (warp >= 2) {
         // ===================== epilogue (warps 2..5) =========================
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int et = threadIdx.x - 64;   // 0..127
-        for (int q = 0; get_item(q, unit, units, n_sjobs, n_out, sk, p, jb); ++q) {
+        for (int q = 0; get_item(q, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, jb); ++q) {
             const TcLayer &Ly = p.layer[jb.layer];
             const uint32_t slot = q & 1, use = q >> 1;
             uint32_t *tbias = s_bias + slot * (kBN / 2);   // [kBN / 2] bf16 pairs
@@ -703,7 +583,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                 named_bar_sync(1, 128);
             }
             // the row's original token, read while the MMA still runs
-            const int64_t pp = static_cast<int64_t>(jb.m) * kTileRows + row0 + row;
+            const int64_t pp = static_cast<int64_t>(jb.m) * kBM + row;
             // kModeMoe: the output row is the pair itself (-1: a gap of the padded order)
             const bool valid = pp < p.M && (p.mode != kModeMoe || p.perm[pp] >= 0);
             const int tok = valid ? p.perm[pp] : 0;
@@ -724,7 +604,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
             Job nx;
             const bool staged = kCanStage && (p.mode == kModeLinear || p.mode == kModeMoe) && jb.kind == 1 &&
                                 jb.part != kPartTail &&
-                                !get_item(q + 1, unit, units, n_sjobs, n_out, sk, p, nx);
+                                !get_item(q + 1, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, nx);
             mbar_wait(&acc_full[slot], use & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
             tc_fence_after();
             const uint32_t tbase = tmem_base + slot * kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
@@ -739,15 +619,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                     tmem_ld16(tbase + (c - jb.c0) * kChunk, r);
                     tmem_ld_wait16(r);
                     const int32_t rng = p.chunk_rng[c];
-                    const bool keep = valid && row0 + row >= rng_lo(rng) && row0 + row < rng_hi(rng);
+                    const bool keep = valid && row >= rng_lo(rng) && row < rng_hi(rng);
                     if (p.mode == kModeLinear) {
                         const float sc = keep ? row_sc : 0.f;
                         uint32_t o[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
                             o[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * sc, __uint_as_float(r[2 * e + 1]) * sc);
-                        uint4 *dst = reinterpret_cast<uint4 *>(
-                            panels + (static_cast<int64_t>(c) * kTileRows + row0 + row) * kChunk);
+                        uint4 *dst = reinterpret_cast<uint4 *>(panels + (static_cast<int64_t>(c) * kBM + row) * kChunk);
                         dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
                         dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
                     } else if (keep) {
@@ -778,7 +657,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                 // in my CTA's scratch slot, layout [col / 4][row][4]: a warp's
                 // float4 accesses cover 512 contiguous bytes
                 float4 *part = reinterpret_cast<float4 *>(p.sk_part) +
-                               static_cast<int64_t>((unit - sk.rs) * kShare + rank) * (kBN / 4) * kBM;
+                               static_cast<int64_t>(blockIdx.x - sk.rs) * (kBN / 4) * kBM;
                 // four 16-column TMEM loads per wait (one group at a time: the
                 // register budget holds no more)
 #pragma unroll 1
@@ -805,7 +684,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                 }
                 __threadfence();
                 named_bar_sync(1, 128);
-                if (et == 0) red_release_gpu_add(p.sk_cnt + (jb.slot * kShare + rank) * kWinCntStride, 1);
+                if (et == 0) red_release_gpu_add(p.sk_cnt + jb.slot * kWinCntStride, 1);
             } else {
                 // ---- output tile (whole, or the head piece of a split tile):
                 // + the tails' partial sums, + bias, bf16, scatter to the
@@ -819,17 +698,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                 const float4 *spart = reinterpret_cast<const float4 *>(wring);
                 int ntail = 0, tail0 = 0;
                 if (head) {
-                    ntail = sk_tail_count(unit, jb.slot, sk, Ly.kblocks);
-                    tail0 = sk_next_tail(unit - sk.rs, sk);
-                    if (et == 0) {   // every tail piece has stored its partial sums (a pair: my rows' CTAs)
-                        wait_flag_geq(p.sk_cnt + (jb.slot * kShare + rank) * kWinCntStride, ntail, abort_flag, status,
-                                      LORA_DEV_TIMEOUT, wait);
+                    ntail = sk_tail_count(blockIdx.x, jb.slot, sk, Ly.kblocks);
+                    tail0 = sk_next_tail(blockIdx.x - sk.rs, sk);
+                    if (et == 0) {   // every tail piece has stored its partial sums
+                        wait_flag_geq(p.sk_cnt + jb.slot * kWinCntStride, ntail, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                         fence_proxy_async_global();   // their stores -> the bulk copies' reads
                         mbar_expect_tx(sk_bar, kBM * kBN * 4);
                         const uint8_t *src = reinterpret_cast<const uint8_t *>(p.sk_part) +
-                                             static_cast<int64_t>(tail0 * kShare + rank) * kBM * kBN * 4;
-                        for (int i = 0; i < 4; ++i)
-                            bulk_load(wring + i * kSkChunk, src + i * kSkChunk, kSkChunk, sk_bar);
+                                             static_cast<int64_t>(tail0) * kBM * kBN * 4;
+                        for (int i = 0; i < 4; ++i) bulk_load(wring + i * kWSlot, src + i * kWSlot, kWSlot, sk_bar);
                     }
                     mbar_wait(sk_bar, 0, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                     // further tails: each thread adds them into its own row of
@@ -837,8 +714,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                     float4 *sp = reinterpret_cast<float4 *>(wring);
                     for (int i = 1, ts = tail0; i < ntail; ++i) {
                         ts = sk_next_tail(ts, sk);
-                        const float4 *xp = reinterpret_cast<const float4 *>(p.sk_part) +
-                                           static_cast<int64_t>(ts * kShare + rank) * (kBN / 4) * kBM;
+                        const float4 *xp =
+                            reinterpret_cast<const float4 *>(p.sk_part) + static_cast<int64_t>(ts) * (kBN / 4) * kBM;
 #pragma unroll 1
                         for (int k0 = 0; k0 < kBN / 4; k0 += 16) {
                             float4 b[16];
@@ -942,7 +819,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                     bulk_wait_read_all();   // the row is out of shared memory; y is written before the grid ends
                 }
                 if (head && et == 0) {
-                    p.sk_cnt[(jb.slot * kShare + rank) * kWinCntStride] = 0;   // zero again for the next call
+                    p.sk_cnt[jb.slot * kWinCntStride] = 0;   // zero again for the next call
                     // the partial sums' bulk copies have landed before the CTA
                     // ends, even if the wait above gave up after a timeout
                     mbar_wait(sk_bar, 0, abort_flag, status, LORA_DEV_TIMEOUT, wait);
@@ -952,30 +829,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
     }
 
     // ---- teardown ---------------------------------------------------------
-    // (a pair: neither CTA ends while the other may still arrive on its
-    // barriers or the even CTA's MMAs may still write its tensor memory)
     tc_fence_before();
-    if constexpr (kPair) {
-        cluster_arrive();
-        cluster_wait();
-    } else {
-        __syncthreads();
-    }
+    __syncthreads();
     tc_fence_after();
-    if (warp == 1) {
-        if constexpr (kPair) tmem_dealloc_pair(tmem_base, kTmemCols);
-        else tmem_dealloc(tmem_base, kTmemCols);
-    }
+    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
 // Standalone expand: turn the caller's fp32 S [M, s_cols] (original token
 // order) into the kernel's bf16 S panels (permuted tile rows, each row masked
 // to its own segment's rank panels, multiplied by scale and by its adapter's
 // factor).  One CTA per token tile, one thread per tile row.
-__global__ void __launch_bounds__(kPairRows) s_prep_kernel(const float *S, int32_t s_cols, float scale, TcParams p)
+__global__ void __launch_bounds__(kBM) s_prep_kernel(const float *S, int32_t s_cols, float scale, TcParams p)
 {
     const int m = blockIdx.x, row = threadIdx.x;
-    const int64_t pp = static_cast<int64_t>(m) * p.tile_rows + row;
+    const int64_t pp = static_cast<int64_t>(m) * kBM + row;
     const bool valid = pp < p.M;
     const int tok = valid ? p.perm[pp] : 0;
     if (p.layer[0].adapter_scale && valid) {
@@ -990,7 +857,7 @@ __global__ void __launch_bounds__(kPairRows) s_prep_kernel(const float *S, int32
 #pragma unroll
         for (int e = 0; e < 8; ++e)
             w[e] = keep ? pack_bf16x2(src[2 * e] * scale, src[2 * e + 1] * scale) : 0u;
-        uint4 *dst = reinterpret_cast<uint4 *>(p.s_panels + (static_cast<int64_t>(c) * p.tile_rows + row) * kChunk);
+        uint4 *dst = reinterpret_cast<uint4 *>(p.s_panels + (static_cast<int64_t>(c) * kBM + row) * kChunk);
         dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
         dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
     }
@@ -998,66 +865,30 @@ __global__ void __launch_bounds__(kPairRows) s_prep_kernel(const float *S, int32
 
 cudaError_t launch_s_prep(const float *S, int32_t s_cols, float scale, const TcParams &p, cudaStream_t stream)
 {
-    s_prep_kernel<<<p.num_mtiles, p.tile_rows, 0, stream>>>(S, s_cols, scale, p);
+    s_prep_kernel<<<p.num_mtiles, kBM, 0, stream>>>(S, s_cols, scale, p);
     return cudaGetLastError();
 }
 
 template <int kXStages, int kWStages>
 static cudaError_t launch_tc_split(const TcArgs &args, int grid, cudaStream_t stream)
 {
-    constexpr size_t smem = tc_smem_bytes<kXStages, kWStages, false>();
+    constexpr size_t smem = tc_smem_bytes<kXStages, kWStages>();
     static int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 64 || !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(lora_tc_kernel<kXStages, kWStages, false>,
+        cudaError_t e = cudaFuncSetAttribute(lora_tc_kernel<kXStages, kWStages>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[dev] = 1;
     }
-    lora_tc_kernel<kXStages, kWStages, false><<<grid, kTcThreads, smem, stream>>>(args);
+    lora_tc_kernel<kXStages, kWStages><<<grid, kTcThreads, smem, stream>>>(args);
     return cudaGetLastError();
-}
-
-// CTA pairs: 2-CTA clusters, at most as many as the device holds at once
-// (every CTA of the persistent grid must be resident: output tiles wait on
-// shrink jobs that other CTAs run).  `pairs`: the pairs the work list wants.
-static cudaError_t launch_tc_pair(const TcArgs &args, int pairs, cudaStream_t stream)
-{
-    constexpr size_t smem = tc_smem_bytes<kXStagesPair, kWStagesPair, true>();
-    auto *kern = lora_tc_kernel<kXStagesPair, kWStagesPair, true>;
-    static int max_pairs[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int limit = dev < 64 ? max_pairs[dev] : 0;
-    if (limit == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        cfg.gridDim = dim3(2);
-        e = cudaOccupancyMaxActiveClusters(&limit, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        if (limit < 1) return cudaErrorInvalidConfiguration;
-        if (dev < 64) max_pairs[dev] = limit;
-    }
-    cfg.gridDim = dim3(2 * std::max(1, std::min(limit, pairs)));
-    return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
 cudaError_t launch_tc(const TcArgs &args, int grid, cudaStream_t stream)
 {
     if (args.p.mode == kModeMoe) return launch_tc_split<kXStagesMoe, kWStagesMoe>(args, grid, stream);
-    if (args.p.tile_rows == kPairRows) return launch_tc_pair(args, grid, stream);
     return launch_tc_split<kXStagesLinear, kWStagesLinear>(args, grid, stream);
 }
 

@@ -37,11 +37,6 @@ constexpr int kSplitMaxCtas = 1024;    // upper bound on the persistent grid
 constexpr int kStreamMaxTokens = 64;    // largest M served by the weight-streaming schedule
 constexpr int kWinCntStride = 32;       // ints per window counter pair (one 128-byte line)
 constexpr int kStreamKMaxTiles = 160;   // output tiles the tiled schedule may split along K in one call
-// From this many tokens on, the tiled schedule runs on CTA pairs: its token
-// tiles are 256 rows, each CTA of a pair gathering 128 of them and loading
-// half of every W tile, and one pair MMA (M = 256) covers both halves
-constexpr int64_t kPairMinTokens = 512;
-constexpr int kPairRows = 2 * kBM;
 constexpr int64_t kMaxTokens = (int64_t(1) << 31) - kBM;   // largest M of one call (32-bit row indices)
 
 // plan header entries
@@ -70,8 +65,7 @@ int64_t tc_wait_cycles();
 struct WsLayout {
     int64_t M;
     int32_t N, A;
-    int32_t tile_rows;        // token tile of the tiled schedule: kBM, or kPairRows from kPairMinTokens on
-    int32_t num_mtiles;       // ceil(M / tile_rows)
+    int32_t num_mtiles;       // ceil(M / kBM)
     int32_t max_chunks;       // tiled-schedule chunk capacity
     int32_t max_sjobs;        // shrink-job capacity
     int32_t max_dchunks;      // split-K chunk capacity
@@ -97,15 +91,14 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A);
 // Host: validate a pool descriptor (LORA_OK or a LORA_ERR_* code).
 int check_pool(const lora_pool_t *pool);
 
-// chunk_rng packing: rows [lo, hi) of the tile (up to 256 rows), rank panel p
-// of the segment
-__host__ __device__ inline int32_t pack_rng(int lo, int hi, int p) { return lo | (hi << 9) | (p << 18); }
+// chunk_rng packing: rows [lo, hi) of the tile, rank panel p of the segment
+__host__ __device__ inline int32_t pack_rng(int lo, int hi, int p) { return lo | (hi << 8) | (p << 16); }
 // S panel sets the workspace holds for the tiled schedule: a shrink job is
 // split into two K halves (one set each) only for M > 128
 inline int tiled_s_sets(int64_t M) { return M > kSplitMaxTokens ? 2 : 1; }
-__host__ __device__ inline int rng_lo(int32_t v) { return v & 0x1FF; }
-__host__ __device__ inline int rng_hi(int32_t v) { return (v >> 9) & 0x1FF; }
-__host__ __device__ inline int rng_panel(int32_t v) { return (v >> 18) & 0xFF; }
+__host__ __device__ inline int rng_lo(int32_t v) { return v & 0xFF; }
+__host__ __device__ inline int rng_hi(int32_t v) { return (v >> 8) & 0xFF; }
+__host__ __device__ inline int rng_panel(int32_t v) { return (v >> 16) & 0xFF; }
 
 // ---- kernel parameter blocks ----------------------------------------------
 // kModeMoe: grouped expert GEMMs of a mixture-of-experts layer, over the
@@ -160,7 +153,6 @@ struct TcParams {
     float *sk_part;            // fp32 [CTAs][256/4][128][4]: each tail piece's partial sums, in its CTA's slot
     int32_t *sk_cnt;           // [tiles][kWinCntStride]: tail pieces stored per split tile (zero at rest)
     int64_t wait_cycles;       // long budget of the kernel's bounded waits, in SM clock cycles
-    int32_t tile_rows;         // rows of a token tile (kPairRows: the CTA-pair kernel)
     TcLayer layer[kMaxLayers];
 };
 
@@ -190,7 +182,6 @@ struct SegParams {
     const int32_t *ids;
     int64_t M;
     int32_t A, K, N, num_mtiles;
-    int32_t tile_rows;         // rows of a token tile of the tiled schedule's tables
     const int32_t *rank;
     const int64_t *a_offset;
     const int64_t *b_offset;
@@ -268,8 +259,6 @@ struct WidenParams {
 cudaError_t launch_widen(const WidenParams &p, int max_segments, cudaStream_t stream);
 cudaError_t launch_seg_build(const SegParams &p, bool pdl, cudaStream_t stream);
 cudaError_t launch_moe_route(const RouteParams &p, cudaStream_t stream);
-// grid: the CTAs (for p.tile_rows == kPairRows: the CTA pairs) the work list
-// wants; capped by what the device holds at once
 cudaError_t launch_tc(const TcArgs &args, int grid, cudaStream_t stream);
 cudaError_t launch_moe_finalize(const uint16_t *out, const int32_t *expert, const float *weight, int64_t M, int topk,
                                 int E, int N, uint16_t *y, cudaStream_t stream);

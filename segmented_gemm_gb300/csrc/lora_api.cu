@@ -111,8 +111,7 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
     L.M = M;
     L.N = N;
     L.A = A;
-    L.tile_rows = M >= kPairMinTokens ? kPairRows : kBM;
-    L.num_mtiles = static_cast<int32_t>((M + L.tile_rows - 1) / L.tile_rows);
+    L.num_mtiles = static_cast<int32_t>((M + kBM - 1) / kBM);
     constexpr int kMaxPanels = LORA_MAX_RANK / kChunk;   // rank panels of one adapter
     L.max_chunks = kMaxPanels * (A + L.num_mtiles) + kMaxPanels;
     L.max_sjobs = L.num_mtiles + L.max_chunks / kMaxShrinkChunks + 1;
@@ -138,7 +137,7 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
     const size_t split_cnt = static_cast<size_t>(NT_cnt) + std::max<int>(RTmax, static_cast<int>(2 * present + 2));
     L.n_counters = CNT_FIXED + std::max<size_t>(2 * static_cast<size_t>(kMaxLayers) * L.num_mtiles, split_cnt) + 8;
     // tiled schedule: S panels, one set per K piece of a shrink job (two for M > 128)
-    const size_t tiled_s = static_cast<size_t>(L.max_chunks) * L.tile_rows * kChunk * 2 * tiled_s_sets(M);
+    const size_t tiled_s = static_cast<size_t>(L.max_chunks) * kBM * kChunk * 2 * tiled_s_sets(M);
     L.s_scratch_bytes = std::max(tiled_s, split_s);
 
     size_t o = 0;
@@ -185,7 +184,7 @@ WsLayout make_ws_layout(int64_t M, int32_t N, int32_t A)
     // the split tiles (used only when the workspace is this large)
     if (M > kSplitMaxTokens) {
         L.sk_part = take(static_cast<size_t>(kStreamKMaxTiles) * kBM * kBN * 4);
-        L.sk_cnt = take(static_cast<size_t>(kStreamKMaxTiles) * 2 * kWinCntStride * 4);   // [tiles][CTA of a pair]
+        L.sk_cnt = take(static_cast<size_t>(kStreamKMaxTiles) * kWinCntStride * 4);
     }
     L.total = o;
     return L;
@@ -261,7 +260,6 @@ static void fill_seg_params(SegParams &p, const int32_t *ids, int64_t M, const l
     p.K = pool->K;
     p.N = pool->N;
     p.num_mtiles = L.num_mtiles;
-    p.tile_rows = L.tile_rows;
     p.rank = pool->rank;
     p.a_offset = pool->a_offset;
     p.b_offset = pool->b_offset;
@@ -335,7 +333,6 @@ static void fill_tc_params(TcParams &p, const WsLayout &L, void *ws, const lora_
     p.num_slices = pool->num_slices > 1 ? pool->num_slices : 1;
     p.num_layers = 1;
     p.num_mtiles = L.num_mtiles;
-    p.tile_rows = L.tile_rows;
     p.group_m = 8;
     p.s_panels = s_panels;
     p.perm = at<int32_t>(ws, L.perm);
@@ -353,7 +350,7 @@ static void fill_tc_params(TcParams &p, const WsLayout &L, void *ws, const lora_
     p.shrink_split = 1;
     p.wait_cycles = tc_wait_cycles();
     p.s_sets = 1;
-    p.s_set_rows = L.max_chunks * L.tile_rows;
+    p.s_set_rows = L.max_chunks * kBM;
 }
 
 // Layer l of a tiled launch.
@@ -500,14 +497,12 @@ static int run_tiled(const LayerCall *lc, int nl, int64_t M, const int32_t *ids,
         const void *xsrc = lc[l].x ? static_cast<const void *>(lc[l].x) : static_cast<const void *>(s_panels);
         const uint64_t xrows = lc[l].x ? static_cast<uint64_t>(M) : 1;
         if (!encode_2d(&m.x, xsrc, K, xrows, K * 2, kBK, 1, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ERR_CUDA;
-        // a CTA pair: each CTA loads half of every W tile and B panel
-        const uint32_t n_box = L.tile_rows == kPairRows ? kBN / 2 : kBN;
         const void *wsrc = lc[l].W ? static_cast<const void *>(lc[l].W) : xsrc;
-        if (!encode_2d(&m.w, wsrc, K, lc[l].W ? N : 1, K * 2, kBK, n_box, CU_TENSOR_MAP_SWIZZLE_128B))
+        if (!encode_2d(&m.w, wsrc, K, lc[l].W ? N : 1, K * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B))
             return LORA_ERR_CUDA;
-        if (!encode_pool_maps(m, pool, s_panels, n_box)) return LORA_ERR_CUDA;
+        if (!encode_pool_maps(m, pool, s_panels, kBN)) return LORA_ERR_CUDA;
     }
-    const uint64_t s_rows = static_cast<uint64_t>(nl) * tiled_s_sets(M) * L.max_chunks * L.tile_rows;
+    const uint64_t s_rows = static_cast<uint64_t>(nl) * tiled_s_sets(M) * L.max_chunks * kBM;
     if (!encode_2d(&a.s, s_panels, kChunk, s_rows, kChunk * 2, kChunk, kBM, CU_TENSOR_MAP_SWIZZLE_32B))
         return LORA_ERR_CUDA;
     if (mode == kModeExpand) {
@@ -816,7 +811,6 @@ int lora_moe_gemm(const lora_bf16_t *x, int64_t M, int32_t K, const lora_bf16_t 
     TcParams &p = a.p;
     p.M = static_cast<int64_t>(L.max_mtiles) * kBM;   // positions of the padded order
     p.num_mtiles = L.max_mtiles;                      // an upper bound: the kernel reads the routing's count
-    p.tile_rows = kBM;
     p.num_layers = 1;
     p.layer[0].N = N;
     p.layer[0].K = K;
@@ -990,7 +984,7 @@ int lora_linear(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lor
 static size_t layers_s_offset(const WsLayout &L) { return (L.total_min + 1023) & ~size_t(1023); }
 static size_t layers_s_bytes(const WsLayout &L, int nl)
 {
-    return static_cast<size_t>(nl) * tiled_s_sets(L.M) * L.max_chunks * L.tile_rows * kChunk * 2;
+    return static_cast<size_t>(nl) * tiled_s_sets(L.M) * L.max_chunks * kBM * kChunk * 2;
 }
 
 size_t lora_layers_workspace_size(int64_t M, int32_t max_N, int32_t num_adapters, int32_t num_layers)

@@ -106,22 +106,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// The same with cluster-scope acquire: for a barrier that another CTA of the
-// cluster arrives on (its release then covers what that CTA wrote before).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-
 // Cycle budgets of the bounded waits: a healthy wait ends in microseconds;
 // the long budget (~1 s at 2 GHz) only runs out when something is broken,
 // after which every later wait of the CTA uses the short budget so the
@@ -137,16 +121,14 @@ __device__ __forceinline__ long long wait_budget(volatile int *abort, long long 
 
 // Wait for completion of the phase with the given parity.  Returns false
 // (and raises *abort + the device status bit) when the budget runs out.
-template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           int32_t *status, int32_t timeout_bit, long long long_budget = kWaitLong)
 {
     const uint32_t a = smem_u32(bar);
-    auto ready = [&]() { return kCluster ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity); };
-    if (ready()) return true;
+    if (mbar_try_wait(a, parity)) return true;
     const long long budget = wait_budget(abort, long_budget);
     const long long t0 = clock64();
-    while (!ready()) {
+    while (!mbar_try_wait(a, parity)) {
         if (clock64() - t0 > budget) {
             *abort = 1;
             atomicOr(status, timeout_bit);
@@ -172,50 +154,6 @@ __device__ __forceinline__ bool wait_flag_geq(const int32_t *flag, int target, v
         __nanosleep(64);
     }
     return true;
-}
-
-// ---------------------------------------------------------------------------
-// clusters
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
-// Arrive without release semantics: used once the barriers a peer will
-// touch have been published with fence.mbarrier_init (a release arrive
-// would also wait for this thread's outstanding memory operations).
-__device__ __forceinline__ void cluster_arrive_relaxed()
-{
-    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
-
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-
-// Arrive once on the mbarrier at shared::cluster address `cluster_bar` (a
-// barrier of any CTA of the cluster, from mapa_shared), releasing this
-// thread's earlier memory operations to the cluster.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
-}
-
-// The same without release semantics: for a signal that what it announces
-// has completed (a copy this thread saw land), where a release would also
-// wait for this thread's earlier remote arrives to be performed.
-__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar)
-{
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -357,53 +295,6 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
-}
-
-// ---- CTA pairs (cta_group::2): the two CTAs of a 2-CTA cluster share one
-// MMA.  The even CTA issues it; each CTA holds its half of A (M / 2 rows)
-// and of B (N / 2 rows) at the same shared-memory address, and its half of
-// D (M / 2 lanes x N columns) in its own tensor memory at the same address.
-// Every tcgen05 instruction of a kernel uses the same cta_group.
-
-// One warp of EACH CTA of the pair executes these together.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols)
-{
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
-                 "r"(ncols)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_relinquish_pair()
-{
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
-{
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// D (+)= A B^T over the pair (issued by one thread of the even CTA).
-__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                               uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrive once on the barrier at this shared-memory offset in every CTA of
-// `cta_mask` when the pair MMAs this thread issued so far complete.
-__device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
 }
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.

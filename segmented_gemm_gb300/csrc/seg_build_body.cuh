@@ -21,7 +21,7 @@
 //                           adapter bucket, ascending id)
 //              warp 1       split-K chunk list (rank panels of adapters present)
 //              warps 2..W-1 tiled-schedule chunk lists and shrink jobs: one
-//                           warp per token tile of 128 or 256 rows (a lane per adapter
+//                           warp per 128-token tile (a lane per adapter
 //                           bucket) when there are at most W-2 tiles, else
 //                           one thread per tile
 // Bucket 0 holds id -1, bucket i+1 adapter i; ids outside [-1, A) are
@@ -273,8 +273,8 @@ struct SegBuild {
             int64_t lo = 0, hi = 0;
             int bfirst = A + 1, nch = 0;
             if (m < p.num_mtiles) {
-                lo = static_cast<int64_t>(m) * p.tile_rows;
-                hi = lo + p.tile_rows < p.M ? lo + p.tile_rows : p.M;
+                lo = static_cast<int64_t>(m) * kBM;
+                hi = lo + kBM < p.M ? lo + kBM : p.M;
                 int L = 1, R = A + 1;   // first adapter bucket that ends past lo
                 while (L < R) {
                     const int mid = (L + R) >> 1;
@@ -344,7 +344,7 @@ struct SegBuild {
                 }
             }
         } else {
-            // tiled schedule, many tiles: per token tile of the permuted
+            // tiled schedule, many tiles: per 128-token tile of the permuted
             // order (one thread each), the rank panels of the segments it
             // intersects (ascending adapter), and its shrink jobs of
             // <= kMaxShrinkChunks panels
@@ -355,8 +355,8 @@ struct SegBuild {
                 int nch = 0, bfirst = 1;
                 int64_t lo = 0, hi = 0;
                 if (m < p.num_mtiles) {
-                    lo = static_cast<int64_t>(m) * p.tile_rows;
-                    hi = lo + p.tile_rows < p.M ? lo + p.tile_rows : p.M;
+                    lo = static_cast<int64_t>(m) * kBM;
+                    hi = lo + kBM < p.M ? lo + kBM : p.M;
                     int L = 1, R = A + 1;   // first adapter bucket that ends past lo
                     while (L < R) {
                         const int mid = (L + R) >> 1;

@@ -21,7 +21,7 @@ LORA_OK = 0
 LORA_ERR_NULL, LORA_ERR_SHAPE, LORA_ERR_ALIGN, LORA_ERR_RANK = 1, 2, 3, 4
 LORA_ERR_WORKSPACE, LORA_ERR_CUDA, LORA_ERR_UNSUPPORTED, LORA_ERR_SEGMENTS = 5, 6, 7, 8
 LORA_ERR_CAPACITY = 9
-LORA_NOALLOC_SCRATCH_BYTES = 16 << 20
+LORA_NOALLOC_SCRATCH_BYTES = 8 << 20
 LORA_DEV_BAD_ID, LORA_DEV_TIMEOUT, LORA_DEV_BAD_POOL = 1, 2, 4
 LORA_PATH_AUTO, LORA_PATH_TILED, LORA_PATH_SPLITK, LORA_PATH_STREAM = 0, 1, 2, 3
 LORA_FLAG_STATIC_WEIGHTS = 0x100

@@ -1,12 +1,9 @@
-"""Parity of the tiled schedule on CTA pairs (from 512 tokens on) with the
-fp64 oracle: 256-row token tiles, each CTA of a pair gathering 128 rows and
-loading half of every W tile and B panel, one pair MMA per step.
-
-Cases aimed at what the pair adds: the token count at which the pairs take
-over, a last token tile whose odd CTA has few or no rows, shrink jobs with an
-odd number of rank panels (the odd CTA loads one panel twice), stream-K on
-pairs twice on one workspace, merged slices, several layers in one launch,
-the standalone products and e4m3 pools.  Bar: |gpu - oracle| <=
+"""Parity of the tiled schedule at a few hundred to a thousand tokens with the
+fp64 oracle: several token tiles, a ragged last tile, shrink jobs with odd
+and large numbers of rank panels, stream-K (the last partial wave split
+along K) twice on one workspace, a prebuilt table reused call after call
+with per-adapter factors, invalid ids, merged slices, several layers in one
+launch, the standalone products and e4m3 pools.  Bar: |gpu - oracle| <=
 2e-2 (1 + |oracle|), outputs NaN-prefilled.
 """
 import numpy as np
@@ -49,9 +46,8 @@ def linear(wl, dev, ws=None, path=L.LORA_PATH_AUTO, segs=None):
 
 
 @pytest.mark.parametrize("M", [511, 512, 600, 700, 1000])
-def test_pairs_take_over_and_ragged_last_tile(M):
-    """511: one CTA per tile; 512 on: pairs.  600: the last 256-row tile has
-    88 rows (its odd CTA none); 700: 188 (the odd CTA 60)."""
+def test_tiled_ragged_last_tile(M):
+    """Token counts around 512 and ragged last tiles (600: 88 rows; 700: 60)."""
     wl = workloads.make_custom(M, 384, 768, [16, 48, 64, 32, 16], seed=900 + M, p_base=0.1, scale=0.75)
     dev = to_dev(wl)
     y, status = linear(wl, dev)
@@ -63,7 +59,7 @@ def test_pairs_take_over_and_ragged_last_tile(M):
                                         ([64] * 6, "uniform"),             # 24 panels a tile: jobs of 16 + 8
                                         ([16] * 19, "uniform"),            # 19 panels: 16 + 3
                                         ([32], "single")])
-def test_pair_shrink_jobs_with_odd_panel_counts(ranks, mode):
+def test_tiled_shrink_jobs_with_odd_panel_counts(ranks, mode):
     wl = workloads.make_custom(768, 256, 512, ranks, seed=len(ranks) * 7, id_mode=mode, p_base=0.05)
     dev = to_dev(wl)
     y, status = linear(wl, dev, path=L.LORA_PATH_TILED)
@@ -71,9 +67,9 @@ def test_pair_shrink_jobs_with_odd_panel_counts(ranks, mode):
     assert_close(y, oracle.lora_linear(wl), what=f"ranks {ranks}")
 
 
-def test_pair_stream_k_twice_on_one_workspace():
-    """Fewer pair tiles than pairs: the output tiles are split along K over
-    pairs (each CTA of a tail pair stores its rows' partial sums); the scratch
+def test_tiled_stream_k_twice_on_one_workspace():
+    """Fewer output tiles than CTAs: the tiles are split along K (each tail
+    piece stores its partial sums in its CTA's scratch slot); the scratch
     and counters must be clean for the second call."""
     wl = workloads.make_custom(1024, 1024, 2048, [16, 32, 64, 48] * 2, seed=931, id_mode="runs", p_base=0.1)
     dev = to_dev(wl)
@@ -85,7 +81,7 @@ def test_pair_stream_k_twice_on_one_workspace():
         assert_close(y, ref, what=f"stream-K call {call}")
 
 
-def test_pair_prebuilt_table_repeated_calls_adapter_factors():
+def test_tiled_prebuilt_table_repeated_calls_adapter_factors():
     wl = workloads.make_custom(900, 512, 640, [64, 16, 32, 48, 16, 64], seed=941, p_base=0.2,
                                adapter_scale="random", scale=1.5)
     dev = to_dev(wl)
@@ -98,7 +94,7 @@ def test_pair_prebuilt_table_repeated_calls_adapter_factors():
         assert_close(y, ref, what=f"prebuilt call {call}")
 
 
-def test_pair_all_base_and_bad_ids():
+def test_tiled_all_base_and_bad_ids():
     wl = workloads.make_custom(640, 256, 512, [16, 32], seed=951, id_mode="all_base")
     dev = to_dev(wl)
     y, status = linear(wl, dev)
@@ -115,7 +111,7 @@ def test_pair_all_base_and_bad_ids():
     assert_close(y, oracle.lora_linear(wl), what="bad ids")
 
 
-def test_pair_sliced_output():
+def test_tiled_sliced_output():
     wl = workloads.make_sliced(1024, 512, [512, 256, 256], [16, 32, 16], seed=961, p_base=0.15)
     dev = to_dev(wl)
     y, status = linear(wl, dev)
@@ -123,7 +119,7 @@ def test_pair_sliced_output():
     assert_close(y, oracle.lora_linear(wl), what="sliced")
 
 
-def test_pair_layers_one_launch():
+def test_tiled_layers_one_launch():
     M = 800
     base = workloads.make_custom(M, 256, 256, [16, 32, 64], seed=971)
     wls = [workloads.make_custom(M, K, N, [16, 32, 64], seed=972 + j, ids=base.ids.clone(), scale=1.0 + 0.5 * j)
@@ -137,7 +133,7 @@ def test_pair_layers_one_launch():
         assert_close(y, oracle.lora_linear(wl), what=f"layer {j}")
 
 
-def test_pair_shrink_and_expand_alone():
+def test_tiled_shrink_and_expand_alone():
     wl = workloads.make_custom(900, 1024, 520, [16, 48, 64, 32], seed=981, id_mode="runs", p_base=0.2)
     dev = to_dev(wl)
     ws = L.Workspace(wl.M, wl.N, wl.num_adapters)
@@ -153,10 +149,10 @@ def test_pair_shrink_and_expand_alone():
     assert torch.equal(y[base_rows.to("cuda")].cpu(), y0[base_rows])
 
 
-def test_pair_e4m3_pool():
+def test_tiled_e4m3_pool():
     wl8 = workloads.to_e4m3(workloads.make_custom(700, 512, 384, [16, 32, 64, 48, 16], seed=991, p_base=0.15,
                                                   adapter_scale="random"))
     dev = to_dev(wl8)
     y, status = linear(wl8, dev)
     assert status == 0
-    assert_close(y, oracle.lora_linear(wl8), what="e4m3 pairs")
+    assert_close(y, oracle.lora_linear(wl8), what="e4m3")
