@@ -28,12 +28,11 @@
 //               costs one LSU request per 16 bytes instead of one TMA
 //               instruction per four rows, which the TMA unit issues too
 //               slowly to feed the tensor core)
-// Smem: an x ring of 16 KB slots and a W ring of 32 KB slots, 224 KB in all
-// (4 + 5 slots for the dense layer, 6 + 4 for the expert GEMM), 128-byte
-// swizzle for the K-blocks of 64, 32-byte swizzle for the 16-wide rank
-// panels.  TMEM: two
-// 256-column fp32 accumulators so the epilogue of job j overlaps the
-// mainloop of job j+1.
+// Smem: one ring of 4 stages, each a 16 KB x slot and a 32 KB W slot under
+// one full and one empty barrier (192 KB), 128-byte swizzle for the K-blocks
+// of 64, 32-byte swizzle for the 16-wide rank panels.  TMEM: two 256-column
+// fp32 accumulators so the epilogue of job j overlaps the mainloop of job
+// j+1.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -53,16 +52,19 @@ constexpr int kTcThreads = 320;   // 10 warps: TMA, MMA, 4 epilogue, 4 x loaders
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 256;
 constexpr int kStageRow = kBN * 2 + 16;   // a staged output row: 512 bytes + 16 of padding
-// The shared memory holds an x ring (cp.async row gathers, 16 KB slots) and
-// a W ring (TMA: W, A panels, S / B panels, 32 KB slots), split per mode:
-// the dense layer runs faster with 4 + 5 slots, the expert GEMM, whose x
-// rows are scattered pairs, with 6 + 4 (both measured on GB300).
-constexpr int kXStagesLinear = 4, kWStagesLinear = 5;
-constexpr int kXStagesMoe = 6, kWStagesMoe = 4;
-template <int kXStages, int kWStages>
+// The shared memory holds one ring of stages.  A stage is an x slot (the
+// loader warps' cp.async row gathers, 16 KB) and a W slot (the producer's
+// TMA boxes: W, A panels, or S and B panels, 32 KB) with ONE full barrier,
+// which counts the 128 loader threads' copies and the W slot's bytes, and
+// one empty barrier.  The MMA thread, whose loop bounds the K steps (the
+// tensor pipe queues few MMAs, so every wait and commit between a step's
+// MMAs shows), then waits once and commits once per K step.  An expand
+// stage has no x rows: its producer arrives for the loader threads.
+constexpr int kStages = 4;   // 4 x 48 KB
+template <int kStg>
 constexpr size_t tc_smem_bytes()
 {
-    return kXStages * kXSlot + kWStages * kWSlot + 1024 /*align*/ + 256 /*barriers*/ + 2 * kBN * 2 /*bias of two tiles*/;
+    return kStg * (kXSlot + kWSlot) + 1024 /*align*/ + 256 /*barriers*/ + 2 * kBN * 2 /*bias of two tiles*/;
 }
 static_assert(kSAreaBytes + kPanelsPerStage * kBPanelBytes <= kWSlot, "an expand stage fits in one W slot");
 
@@ -76,6 +78,16 @@ struct Job {
 };
 
 enum { kPartFull = 0, kPartHead = 1, kPartTail = 2 };
+
+// The ring stages of an item after its K steps: its expand steps,
+// kPanelsPerStage chunks a stage (an output tile, or the head piece of a
+// split one, whose token tile has chunks).  Every role steps through them.
+__device__ __forceinline__ int expand_stages(const Job &jb)
+{
+    return (jb.kind == 1 && jb.c1 > jb.c0 && jb.part != kPartTail)
+               ? (jb.c1 - jb.c0 + kPanelsPerStage - 1) / kPanelsPerStage
+               : 0;
+}
 
 // Item j of the launch: the n_sjobs shrink items of every layer (each
 // layer's list alike: the layers share one table), then every layer's
@@ -250,44 +262,38 @@ __device__ __forceinline__ int sk_tail_count(int b, int t, const SkPlan &s, int 
     return n;
 }
 
-template <int kXStages, int kWStages>
+template <int kStg>
 __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_constant__ TcArgs args)
 {
     const TcParams &p = args.p;
     const CUtensorMap &tm_s = args.s;
-    static_assert(kWStages * kWSlot >= kBM * kBN * 4, "a split tile's fp32 partials fit in the W ring");
-    static_assert((2 * kXStages + 2 * kWStages + 5) * 8 + 8 <= 256, "barriers, TMEM address and abort flag fit");
-    static_assert(tc_smem_bytes<kXStages, kWStages>() <= 232448, "fits the opt-in shared memory of a CTA");
-    // the last item's bf16 output is staged in the idle x ring when it fits
-    constexpr bool kCanStage = kBM * kStageRow <= kXStages * kXSlot;
+    static_assert(kStg * kWSlot >= kBM * kBN * 4, "a split tile's fp32 partials fit in the W slots");
+    static_assert((2 * kStg + 5) * 8 + 8 <= 256, "barriers, TMEM address and abort flag fit");
+    static_assert(tc_smem_bytes<kStg>() <= 232448, "fits the opt-in shared memory of a CTA");
+    // the last item's bf16 output is staged in the idle x slots when it fits
+    constexpr bool kCanStage = kBM * kStageRow <= kStg * kXSlot;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *xring = smem;                                  // kXStages x 16 KB
-    uint8_t *wring = smem + kXStages * kXSlot;              // kWStages x 32 KB
-    uint64_t *fullx = reinterpret_cast<uint64_t *>(wring + kWStages * kWSlot);
-    uint64_t *emptyx = fullx + kXStages;
-    uint64_t *fullw = emptyx + kXStages;
-    uint64_t *emptyw = fullw + kWStages;
-    uint64_t *acc_full = emptyw + kWStages;
+    uint8_t *xring = smem;                                  // the stages' x slots, kStg x 16 KB
+    uint8_t *wring = smem + kStg * kXSlot;                  // their W slots, kStg x 32 KB
+    uint64_t *full = reinterpret_cast<uint64_t *>(wring + kStg * kWSlot);
+    uint64_t *empty = full + kStg;
+    uint64_t *acc_full = empty + kStg;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *sk_bar = acc_empty + 2;   // stream-K head: the partial sums have landed in the W ring
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sk_bar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     // bias of the output tile of each accumulator slot: [2][kBN] bf16 (16-byte aligned)
-    uint32_t *s_bias = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(fullx) + 256);
+    uint32_t *s_bias = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(full) + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *status = p.counters + CNT_STATUS;
     const long long wait = p.wait_cycles;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kXStages; ++s) {
-            mbar_init(&fullx[s], 128);    // one cp.async-completion arrive per loader thread
-            mbar_init(&emptyx[s], 1);
-        }
-        for (int s = 0; s < kWStages; ++s) {
-            mbar_init(&fullw[s], 1);      // the producer's expect_tx arrive
-            mbar_init(&emptyw[s], 1);
+        for (int s = 0; s < kStg; ++s) {
+            mbar_init(&full[s], 128 + 1);   // a cp.async-completion arrive per loader thread, the producer's expect_tx
+            mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
@@ -324,8 +330,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
     Job jb;
 
     if (warp == 0) {
-        // ===================== TMA producer: W ring (W, A panels, S / B panels)
-        uint32_t iw = 0;
+        // ===================== TMA producer: W slots (W, A panels, S / B panels)
+        uint32_t it = 0;
         // The S-ready counter of (layer, token tile m) is put back to zero by
         // the last of the layer's num_ntiles output tiles of row m to pass
         // the wait on it: each adds itself to a consumer counter right after
@@ -340,17 +346,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
             }
             rst_m = -1;
         };
-        // A W slot is refilled only once the MMA has freed it AND its previous
-        // phase has completed, so the expect_tx arrive always opens a new
-        // phase.  In a healthy run the second wait returns at once (the MMA
-        // waited for that phase before freeing the slot); after a timeout let
-        // a wait go early it keeps a second arrive off a phase that still
-        // waits for bytes.  A stage whose slot never comes free is skipped.
+        // A stage is refilled only once the MMA has freed it AND its full
+        // barrier's previous phase has completed, so this stage's arrives
+        // always open a new phase.  In a healthy run the second wait returns
+        // at once (the MMA waited for that phase before freeing the stage);
+        // after a timeout let a wait go early it keeps an arrive off a phase
+        // that still waits for bytes.  A stage that never comes free is
+        // skipped.  (The loader warps guard their arrives the same way.)
         auto slot_free = [&](int s, uint32_t round) -> bool {
             int ok = 1;
             if (lane == 0 && round > 0) {
-                mbar_wait(&emptyw[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
-                ok = mbar_wait(&fullw[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+                mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+                ok = mbar_wait(&full[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
             }
             return __shfl_sync(0xffffffffu, ok, 0) != 0;
         };
@@ -397,22 +404,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                     run_len = 0;
                 }
             }
-            for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++iw) {
-                const int s = iw % kWStages;
-                if (!slot_free(s, iw / kWStages)) continue;
+            for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++it) {
+                const int s = it % kStg;
+                if (!slot_free(s, it / kStg)) continue;
                 uint8_t *wsl = wring + s * kWSlot;
                 if (jb.kind == 1) {
                     if (lane == 0) {
-                        mbar_expect_tx(&fullw[s], kWSlot);
-                        tma_load_2d(wsl, &mp.w, &fullw[s], kb * kBK, jb.n * kBN + w_row0);
+                        mbar_expect_tx(&full[s], kWSlot);
+                        tma_load_2d(wsl, &mp.w, &full[s], kb * kBK, jb.n * kBN + w_row0);
                     }
                 } else {
-                    if (lane == 0) mbar_expect_tx(&fullw[s], (jb.c1 - jb.c0) * kAPanelBytes);
+                    if (lane == 0) mbar_expect_tx(&full[s], (jb.c1 - jb.c0) * kAPanelBytes);
                     __syncwarp();
                     if (run_len > 0) {
                         const CUtensorMap *m =
                             run_len == 1 ? &mp.a : run_len == 2 ? &mp.a32 : run_len == 3 ? &mp.a48 : &mp.a64;
-                        tma_load_2d(wsl + lane * kAPanelBytes, m, &fullw[s], kb * kBK, run_row);
+                        tma_load_2d(wsl + lane * kAPanelBytes, m, &full[s], kb * kBK, run_row);
                     }
                 }
                 __syncwarp();
@@ -432,12 +439,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                     }
                     __syncwarp();
                 }
-                for (int cg = jb.c0; cg < jb.c1; cg += kPanelsPerStage, ++iw) {
-                    const int s = iw % kWStages;
-                    if (!slot_free(s, iw / kWStages)) continue;
+                for (int cg = jb.c0; cg < jb.c1; cg += kPanelsPerStage, ++it) {
+                    const int s = it % kStg;
+                    if (!slot_free(s, it / kStg)) continue;
                     uint8_t *wsl = wring + s * kWSlot;   // [S panels [set][chunk] | B panels [chunk]]
                     const int nc = min(kPanelsPerStage, jb.c1 - cg);
-                    if (lane == 0) mbar_expect_tx(&fullw[s], nc * (p.s_sets * kSPanelBytes + kBPanelBytes));
+                    if (lane == 0) {   // the stage has no x rows: arrive for the loader threads too
+                        mbar_expect_tx(&full[s], nc * (p.s_sets * kSPanelBytes + kBPanelBytes));
+                        mbar_arrive_n(&full[s], 128);
+                    }
                     __syncwarp();
                     const int ci = cg - jb.c0 + lane;   // chunk index inside the tile
                     const int brow_s = __shfl_sync(0xffffffffu, brow_l, ci & 31);
@@ -445,9 +455,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                         const int c = cg + lane;
                         const int brow = ci < 32 ? brow_s : p.chunk_bpanel[c] * Ly.N;
                         for (int h = 0; h < p.s_sets; ++h)
-                            tma_load_2d(wsl + (h * kPanelsPerStage + lane) * kSPanelBytes, &tm_s, &fullw[s], 0,
+                            tma_load_2d(wsl + (h * kPanelsPerStage + lane) * kSPanelBytes, &tm_s, &full[s], 0,
                                         (jb.layer * p.s_sets + h) * p.s_set_rows + c * kBM);
-                        tma_load_2d(wsl + kSAreaBytes + lane * kBPanelBytes, &mp.b, &fullw[s], 0, brow + jb.n * kBN);
+                        tma_load_2d(wsl + kSAreaBytes + lane * kBPanelBytes, &mp.b, &full[s], 0, brow + jb.n * kBN);
                     }
                     __syncwarp();
                 }
@@ -457,24 +467,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
             settle();
             // every load this warp issued has landed before the CTA ends (after
             // a timeout the MMA may have stopped waiting for some): the last
-            // phase of each W slot
-            for (uint32_t i = iw > kWStages ? iw - kWStages : 0; i < iw; ++i)
-                mbar_wait(&fullw[i % kWStages], (i / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+            // phase of each stage
+            for (uint32_t i = it > kStg ? it - kStg : 0; i < it; ++i)
+                mbar_wait(&full[i % kStg], (i / kStg) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
         }
     } else if (warp >= 6) {
         // ===================== x loaders: permuted-row gather (cp.async) =====
         // Thread lt copies 16-byte chunk (lt % 8) of rows lt/8 + 16q, q < 8,
         // into the 128-byte-swizzled x slot; a warp instruction covers four
         // whole 128-byte row segments.  Completion is tracked by the hardware
-        // (cp.async.mbarrier.arrive.noinc), so all kXStages slots stay in
-        // flight; the MMA thread fences the generic-proxy writes for the
-        // tensor core's async-proxy reads after its wait.
+        // (cp.async.mbarrier.arrive.noinc on the stage's full barrier), so
+        // every stage stays in flight; the MMA thread fences the
+        // generic-proxy writes for the tensor core's async-proxy reads after
+        // its wait.  The loaders step over expand stages (no x rows).
         const int lt = threadIdx.x - 192;
         const int chunk = lt & 7, rb = lt >> 3;
         const uint32_t swz = static_cast<uint32_t>((chunk ^ (rb & 7)) << 4);
-        uint32_t ix = 0;
+        uint32_t it = 0;
         for (int q = 0; get_item(q, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, jb); ++q) {
-            if (jb.kb1 <= jb.kb0) continue;
+            if (jb.kb1 <= jb.kb0) {
+                it += expand_stages(jb);
+                continue;
+            }
             const TcLayer &Ly = p.layer[jb.layer];
             const uint16_t *src[8];
 #pragma unroll
@@ -485,22 +499,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                 if (p.mode == kModeMoe) row = row >= 0 ? row / p.topk : 0;   // a pair's token; a gap reads row 0
                 src[q] = Ly.x + row * Ly.K + chunk * 8;
             }
-            for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++ix) {
-                const int s = ix % kXStages;
-                const uint32_t round = ix / kXStages;
-                if (lane == 0 && round > 0) mbar_wait(&emptyx[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
-                __syncwarp();
+            for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++it) {
+                const int s = it % kStg;
+                const uint32_t round = it / kStg;
+                int ok = 1;   // as the producer's slot_free: the full barrier's previous phase has completed
+                if (lane == 0 && round > 0) {
+                    mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+                    ok = mbar_wait(&full[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+                }
+                if (!__shfl_sync(0xffffffffu, ok, 0)) continue;
                 uint8_t *xs = xring + s * kXSlot + swz;
                 const uint32_t nbytes = (kb * kBK + chunk * 8 < Ly.K) ? 16u : 0u;
 #pragma unroll
                 for (int q = 0; q < 8; ++q) cp_async16(xs + (rb + 16 * q) * 128, src[q] + kb * kBK, nbytes);
-                cp_async_mbar_arrive_noinc(&fullx[s]);
+                cp_async_mbar_arrive_noinc(&full[s]);
             }
+            it += expand_stages(jb);
         }
         cp_async_wait_all();
     } else if (warp == 1) {
         // ===================== MMA issuer ====================================
-        uint32_t iw = 0, ix = 0;
+        uint32_t it = 0;
         int last_q = -1;
         for (int q = 0; get_item(q, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, jb); ++q) {
             const uint32_t slot = q & 1, use = q >> 1;
@@ -510,34 +529,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
             const int n_mma = jb.kind == 0 ? (jb.c1 - jb.c0) * kChunk : kBN;
             const uint32_t idesc = umma_idesc_bf16(kBM, n_mma);
             uint32_t acc = 0;
-            for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++iw, ++ix) {
-                const int sw = iw % kWStages, sx = ix % kXStages;
-                mbar_wait(&fullx[sx], (ix / kXStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
-                mbar_wait(&fullw[sw], (iw / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+            for (int kb = jb.kb0; kb < jb.kb1; ++kb, ++it) {
+                const int s = it % kStg;
+                mbar_wait(&full[s], (it / kStg) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                 fence_proxy_async_smem();   // x arrived through the generic proxy (cp.async)
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t xa = smem_u32(xring + sx * kXSlot);
-                    const uint32_t wa = smem_u32(wring + sw * kWSlot);
+                    const uint32_t xa = smem_u32(xring + s * kXSlot);
+                    const uint32_t wa = smem_u32(wring + s * kWSlot);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         umma_bf16(d, umma_sdesc(xa + kk * 32, 1024, kSwizzle128),
                                   umma_sdesc(wa + kk * 32, 1024, kSwizzle128), idesc, acc);
                         acc = 1;
                     }
-                    umma_commit(&emptyx[sx]);
-                    umma_commit(&emptyw[sw]);
+                    umma_commit(&empty[s]);
                 }
                 __syncwarp();
             }
             if (jb.kind == 1 && jb.c1 > jb.c0 && jb.part != kPartTail) {
                 const uint32_t idesc_e = umma_idesc_bf16(kBM, kBN);
-                for (int cg = jb.c0; cg < jb.c1; cg += kPanelsPerStage, ++iw) {
-                    const int sw = iw % kWStages;
-                    mbar_wait(&fullw[sw], (iw / kWStages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+                for (int cg = jb.c0; cg < jb.c1; cg += kPanelsPerStage, ++it) {
+                    const int s = it % kStg;
+                    mbar_wait(&full[s], (it / kStg) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t sa = smem_u32(wring + sw * kWSlot);
+                        const uint32_t sa = smem_u32(wring + s * kWSlot);
                         const uint32_t ba = sa + kSAreaBytes;
                         const int nc = min(kPanelsPerStage, jb.c1 - cg);
                         for (int i = 0; i < nc; ++i)
@@ -546,7 +563,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                                           umma_sdesc(ba + i * kBPanelBytes, 256, kSwizzle32), idesc_e, acc);
                                 acc = 1;
                             }
-                        umma_commit(&emptyw[sw]);
+                        umma_commit(&empty[s]);
                     }
                     __syncwarp();
                 }
@@ -869,27 +886,26 @@ cudaError_t launch_s_prep(const float *S, int32_t s_cols, float scale, const TcP
     return cudaGetLastError();
 }
 
-template <int kXStages, int kWStages>
+template <int kStg>
 static cudaError_t launch_tc_split(const TcArgs &args, int grid, cudaStream_t stream)
 {
-    constexpr size_t smem = tc_smem_bytes<kXStages, kWStages>();
+    constexpr size_t smem = tc_smem_bytes<kStg>();
     static int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 64 || !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(lora_tc_kernel<kXStages, kWStages>,
+        cudaError_t e = cudaFuncSetAttribute(lora_tc_kernel<kStg>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[dev] = 1;
     }
-    lora_tc_kernel<kXStages, kWStages><<<grid, kTcThreads, smem, stream>>>(args);
+    lora_tc_kernel<kStg><<<grid, kTcThreads, smem, stream>>>(args);
     return cudaGetLastError();
 }
 
 cudaError_t launch_tc(const TcArgs &args, int grid, cudaStream_t stream)
 {
-    if (args.p.mode == kModeMoe) return launch_tc_split<kXStagesMoe, kWStagesMoe>(args, grid, stream);
-    return launch_tc_split<kXStagesLinear, kWStagesLinear>(args, grid, stream);
+    return launch_tc_split<kStages>(args, grid, stream);
 }
 
 }  // namespace lora
