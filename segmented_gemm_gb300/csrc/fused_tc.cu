@@ -519,6 +519,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
         cp_async_wait_all();
     } else if (warp == 1) {
         // ===================== MMA issuer ====================================
+        // The K steps' operand descriptors: those of slot 0, advanced by the
+        // slot's and the 16-wide K step's byte offsets (>> 4) in the start
+        // address field (shared-memory offsets stay inside its 14 bits).
+        const uint64_t xdesc0 = umma_sdesc(smem_u32(xring), 1024, kSwizzle128);
+        const uint64_t wdesc0 = umma_sdesc(smem_u32(wring), 1024, kSwizzle128);
         uint32_t it = 0;
         int last_q = -1;
         for (int q = 0; get_item(q, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, jb); ++q) {
@@ -535,12 +540,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                 fence_proxy_async_smem();   // x arrived through the generic proxy (cp.async)
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t xa = smem_u32(xring + s * kXSlot);
-                    const uint32_t wa = smem_u32(wring + s * kWSlot);
+                    const uint64_t xd = xdesc0 + static_cast<uint64_t>((s * kXSlot) >> 4);
+                    const uint64_t wd = wdesc0 + static_cast<uint64_t>((s * kWSlot) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        umma_bf16(d, umma_sdesc(xa + kk * 32, 1024, kSwizzle128),
-                                  umma_sdesc(wa + kk * 32, 1024, kSwizzle128), idesc, acc);
+                    for (int kk = 0; kk < kBK / 16; ++kk) {   // 16 K columns of bf16 = 32 bytes
+                        umma_bf16(d, xd + 2 * kk, wd + 2 * kk, idesc, acc);
                         acc = 1;
                     }
                     umma_commit(&empty[s]);
