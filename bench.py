@@ -38,6 +38,10 @@ import torch  # noqa: E402
 from segmented_gemm_gb300 import workloads  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
+# nominal peaks of a GB300, printed beside the measured ones (the fractions
+# that the roofline reports are of the measured peaks)
+NOMINAL_HBM_GBS = 7900.0
+NOMINAL_BF16_TFLOPS = 2250.0
 MAX_SETS = None          # --max-sets: cap the rotating input sets (small profiler captures)
 METRIC = "multi-LoRA linear tokens/s; % of HBM / bf16 tensor roofline, M=32..8192"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -334,6 +338,17 @@ def run_config(name, L, device, steps, warmup, stream, sampler=None, dist_barrie
     # the fused kernel alone (segment tables prebuilt): dominant-kernel duration
     kern_ms = time_steps(kernel_step, steps, warmup, stream) / steps
     iso_kern_ms = time_isolated(kernel_step, 200, stream)
+
+    # reference: the base GEMM alone (x W^T + bias, no LoRA term) by cuBLAS
+    # through PyTorch, on the same rotating inputs, timed the same way
+    def base_step(i):
+        s = sets[i % ns]
+        if s.bias is not None:
+            torch.addmm(s.bias, s.x, s.W.t(), out=s.y)
+        else:
+            torch.mm(s.x, s.W.t(), out=s.y)
+
+    base_ms = time_steps(base_step, steps, warmup, stream) / steps
     plain = None
     if compare_plain:
         sw = False
@@ -351,7 +366,7 @@ def run_config(name, L, device, steps, warmup, stream, sampler=None, dist_barrie
     status = L.lora_get_status(sets[0].ws)
     res = dict(name=name, wl=wl, ms_per_step=total_ms / steps, kernel_ms=kern_ms, bytes=nbytes, flops=flops,
                n_present=n_present, n_sets=ns, set_bytes=sets[0].nbytes(), status=status, clocks=clocks,
-               plain=plain, iso_kernel_ms=iso_kern_ms, iso_step_ms=iso_step_ms)
+               plain=plain, iso_kernel_ms=iso_kern_ms, iso_step_ms=iso_step_ms, base_ms=base_ms)
     if e2e:
         res["e2e"] = run_e2e(wl, sets, L, device, min(steps, 5000), max(3, min(warmup, 50)), stream)
     return res
@@ -602,10 +617,10 @@ def roofline(r, wl, kname, config, peaks, peak_kind):
                   "graphs, CUDA events on the launching stream")
     hbm_bound = wl.M <= 128
     if hbm_bound:
-        work, peak, unit, scale = r["bytes"], peaks["hbm_gbs"], "GB/s", 1e9
+        work, peak, unit, scale, nominal = r["bytes"], peaks["hbm_gbs"], "GB/s", 1e9, NOMINAL_HBM_GBS
         roof = {"bound": "hbm"}
     else:
-        work, peak, unit, scale = r["flops"], peaks["bf16_tflops"], "TFLOP/s", 1e12
+        work, peak, unit, scale, nominal = r["flops"], peaks["bf16_tflops"], "TFLOP/s", 1e12, NOMINAL_BF16_TFLOPS
         roof = {"bound": "tensor"}
     achieved = work / (kern_ms * 1e-3) / scale
     iso = work / (iso_ms * 1e-3) / scale
@@ -614,6 +629,7 @@ def roofline(r, wl, kname, config, peaks, peak_kind):
                  "kernel_us": round(kern_ms * 1e3, 3), "kernel_time_method": method,
                  "isolated_us": round(iso_ms * 1e3, 3), "isolated_achieved": round(iso, 1),
                  "isolated_frac": round(iso / peak, 4),
+                 "nominal_peak": nominal, "frac_of_nominal": round(achieved / nominal, 4),
                  "isolated_method": "median of 200 single calls, each after a device synchronize (idle GPU), "
                                     "CUDA events on the launching stream around the one call; the launch's own "
                                     "start-up is included and nothing overlaps it",
@@ -680,6 +696,9 @@ def ours(args):
         "clocks": r["clocks"],
         "device_status": r["status"],
         "without_static_weights": r["plain"],
+        "torch_base_only": {"us": round(r["base_ms"] * 1e3, 3),
+                            "method": "cuBLAS through torch.addmm: x W^T + bias alone (no LoRA term) on the same "
+                                      "rotating inputs, back to back in CUDA graphs, CUDA events"},
     }
     if world == 1 and rank == 0 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(args.config)
@@ -702,6 +721,7 @@ def ours(args):
                 "tensor_frac": round(s["flops"] / kt / 1e12 / peaks["bf16_tflops"], 4),
                 "hbm_gbs": round(s["bytes"] / kt / 1e9, 1),
                 "roofline": roofline(s, s["wl"], sk, name, peaks, peak_kind),
+                "torch_base_only_us": round(s["base_ms"] * 1e3, 2),
                 "clocks": s["clocks"], "device_status": s["status"]}
             del s
             torch.cuda.empty_cache()
