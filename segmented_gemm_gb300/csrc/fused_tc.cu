@@ -289,6 +289,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *status = p.counters + CNT_STATUS;
     const long long wait = p.wait_cycles;
+    // A programmatic dependent launch: the kernel after this one may place
+    // its CTAs on the SMs this grid's CTAs leave, and this grid's CTAs run
+    // their prologue while the kernel ahead of them ends (below).
+    pdl_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStg; ++s) {
@@ -317,6 +321,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Nothing before this point reads or writes global memory that another
+    // kernel produces or consumes: wait for the kernel ahead (its tables,
+    // counters, S and outputs) before the first such access.
+    pdl_wait();
 
     // shrink items: every shrink job in p.shrink_split pieces along K
     const int nmt = p.mode == kModeMoe ? min(p.hdr[HDR_MOE_TILES], p.num_mtiles) : p.num_mtiles;
@@ -903,8 +911,19 @@ static cudaError_t launch_tc_split(const TcArgs &args, int grid, cudaStream_t st
         if (e != cudaSuccess) return e;
         if (dev < 64) configured[dev] = 1;
     }
-    lora_tc_kernel<kStg><<<grid, kTcThreads, smem, stream>>>(args);
-    return cudaGetLastError();
+    // a programmatic dependent launch: the CTAs start their prologue as the
+    // kernel ahead releases SMs, and wait for it before touching its data
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, lora_tc_kernel<kStg>, args);
 }
 
 cudaError_t launch_tc(const TcArgs &args, int grid, cudaStream_t stream)
