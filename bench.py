@@ -18,6 +18,7 @@ project): rank 0 only, each step a bounded element sample of the workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -58,12 +59,17 @@ SWEEP_EXTRA = {
                   "4096 | 1024 | 1024, 8 adapters of rank 16 per slice",
     "decode_e4m3": "the decode step with its adapters stored as e4m3 codes (one byte per element) and one "
                    "dequant factor per adapter and factor; the same x, W, bias and ids",
+    "decode_all_base": "the decode step with every id -1 (no LoRA token): the bare weight stream of the decode "
+                       "kernel; the same x, W, bias and pool",
 }
 
 
 def make_workload(name):
     if name == "decode_e4m3":
         return workloads.to_e4m3(workloads.make_config("decode"))
+    if name == "decode_all_base":
+        base = workloads.make_config("decode")
+        return dataclasses.replace(base, ids=torch.full_like(base.ids, -1))
     if name == "qkv_sliced":
         base = workloads.make_config("qkv")
         return workloads.make_sliced(base.M, base.K, [4096, 1024, 1024], [16] * 8, seed=1237, ids=base.ids.clone())
@@ -372,7 +378,8 @@ def run_config(name, L, device, steps, warmup, stream, sampler=None, dist_barrie
     return res
 
 
-SWEEP_LINES = ("prefill", "qkv", "mlp_down", "qkv_sliced", "decode_e4m3", "attention_block_prefill", "moe_experts")
+SWEEP_LINES = ("prefill", "qkv", "mlp_down", "qkv_sliced", "decode_e4m3", "decode_all_base", "attention_block_prefill",
+               "moe_experts")
 
 LAYER_SHAPES = (("q", 4096, 4096), ("k", 4096, 1024), ("v", 4096, 1024), ("o", 4096, 4096))
 
@@ -705,11 +712,11 @@ def ours(args):
     if not args.no_sweep and rank == 0:
         sweep = {}
         lines = set(args.sweep.split(","))
-        for name in ("prefill", "qkv", "mlp_down", "qkv_sliced", "decode_e4m3"):
+        for name in ("prefill", "qkv", "mlp_down", "qkv_sliced", "decode_e4m3", "decode_all_base"):
             if name == args.config or name not in lines:
                 continue
             samp = ClockSampler(local)
-            nsteps = 30 if name == "mlp_down" else 2000 if name == "decode_e4m3" else 100
+            nsteps = 30 if name == "mlp_down" else 2000 if name.startswith("decode") else 100
             s = run_config(name, L, device, nsteps, 5 if nsteps < 1000 else 100, stream, e2e=False, sampler=samp)
             kt = s["kernel_ms"] * 1e-3
             sk = dominant_kernel(s["wl"])
