@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, cta = blockIdx.x;
     int32_t *status = p.counters + CNT_STATUS;
+    const long long wait = p.wait_cycles;
 
     const int D = p.hdr[HDR_DCHUNKS];               // rank panels of the adapters present
     const int RT = (D + 7) / 8;                     // shrink tiles (8 panels = 128 rows)
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 const bool expand = r.list == 1 && k >= p.kblocks;
                 if (expand && !s_ready) {
                     if (lane == 0) {
-                        wait_flag_geq(p.counters + CNT_SPLIT_SREADY, RT, abort_flag, status, LORA_DEV_TIMEOUT);
+                        wait_flag_geq(p.counters + CNT_SPLIT_SREADY, RT, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                         fence_proxy_async_global();
                     }
                     __syncwarp();
@@ -179,8 +180,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 // go early; a stage whose slot never comes free is skipped
                 int ok = 1;
                 if (lane == 0 && round > 0) {
-                    mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
-                    ok = mbar_wait(&full[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                    mbar_wait(&empty[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+                    ok = mbar_wait(&full[s], (round - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                 }
                 if (!__shfl_sync(0xffffffffu, ok, 0)) continue;
                 uint8_t *as = smem + s * stage_bytes;
@@ -218,6 +219,13 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 __syncwarp();
             }
         }
+        // every load this warp issued has landed before the CTA ends (after a
+        // timeout the MMA may have stopped waiting for some): the last phase
+        // of each stage
+        if (lane == 0)
+            for (uint32_t i = it > static_cast<uint32_t>(p.stages) ? it - p.stages : 0; i < it; ++i)
+                mbar_wait(&full[i % p.stages], (i / p.stages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+        __syncwarp();
     } else if (warp == 1) {
         // ===================== MMA issuer ====================================
         uint32_t it = 0;
@@ -225,14 +233,14 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         for (int ri = 0; ri < nr; ++ri) {
             const Run r = runs[ri];
             const uint32_t slot = ri & 1, use = ri >> 1;
-            if (use > 0) mbar_wait(&acc_empty[slot], (use - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+            if (use > 0) mbar_wait(&acc_empty[slot], (use - 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
             tc_fence_after();
             const uint32_t d = tmem_base + slot * p.T_pad;
             uint32_t acc = 0;
             for (int k = r.u0; k < r.u1; ++k, ++it) {
                 const bool expand = r.list == 1 && k >= p.kblocks;
                 const int s = it % p.stages;
-                mbar_wait(&full[s], (it / p.stages) & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+                mbar_wait(&full[s], (it / p.stages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t aa = smem_u32(smem + s * stage_bytes);
@@ -259,6 +267,12 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             if (lane == 0) umma_commit(&acc_full[slot]);
             __syncwarp();
         }
+        // the last commit covers every MMA this thread issued: they are done
+        // before the tensor memory is freed, even if the epilogue stopped
+        // waiting for them after a timeout
+        if (lane == 0 && nr > 0)
+            mbar_wait(&acc_full[(nr - 1) & 1], ((nr - 1) >> 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+        __syncwarp();
     } else {
         // ===================== epilogue: accumulate, finish tiles =============
         const int quad = warp & 3;
@@ -268,7 +282,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         for (int ri = 0; ri < nr; ++ri) {
             const Run r = runs[ri];
             const uint32_t slot = ri & 1, use = ri >> 1;
-            mbar_wait(&acc_full[slot], use & 1, abort_flag, status, LORA_DEV_TIMEOUT);
+            mbar_wait(&acc_full[slot], use & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
             tc_fence_after();
             const uint32_t tbase = tmem_base + slot * T + (static_cast<uint32_t>(quad * 32) << 16);
             const bool is_out = r.list == 1;

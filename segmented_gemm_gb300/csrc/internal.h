@@ -57,8 +57,8 @@ enum Counters {
     CNT_FIXED = 8         // first per-tile counter
 };
 
-// long budget of the tiled kernel's bounded waits (SM clock cycles), set by
-// lora_set_wait_budget; read when a tiled launch is enqueued
+// long budget of the tiled and split-K kernels' bounded waits (SM clock
+// cycles), set by lora_set_wait_budget; read when a launch is enqueued
 constexpr int64_t kDefaultWaitCycles = 2000000000ll;
 int64_t tc_wait_cycles();
 
@@ -176,6 +176,7 @@ struct SplitParams {
     float *acc_out;            // fp32 [NT][128][T_pad], zero at rest
     float *acc_shr;            // fp32 [shrink tiles][128][T_pad], zero at rest
     int32_t *counters;
+    int64_t wait_cycles;       // long budget of the kernel's bounded waits, in SM clock cycles
 };
 
 struct SegParams {

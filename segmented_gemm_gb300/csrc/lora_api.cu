@@ -562,6 +562,7 @@ static int run_splitk(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, con
     p.acc_out = at<float>(ws, L.acc_out);
     p.acc_shr = at<float>(ws, L.acc_shr);
     p.counters = at<int32_t>(ws, L.counters);
+    p.wait_cycles = tc_wait_cycles();
     const uint64_t K = pool->K, N = pool->N;
     TcMaps m;
     if (!encode_2d(&m.x, x, K, static_cast<uint64_t>(M), K * 2, kBK, T, CU_TENSOR_MAP_SWIZZLE_128B))
