@@ -219,12 +219,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 __syncwarp();
             }
         }
-        // every load this warp issued has landed before the CTA ends (after a
-        // timeout the MMA may have stopped waiting for some): the last phase
-        // of each stage
-        if (lane == 0)
-            for (uint32_t i = it > static_cast<uint32_t>(p.stages) ? it - p.stages : 0; i < it; ++i)
-                mbar_wait(&full[i % p.stages], (i / p.stages) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+        if (lane == 0) n_runs[1] = static_cast<int>(it);   // for the teardown: the stages issued
         __syncwarp();
     } else if (warp == 1) {
         // ===================== MMA issuer ====================================
@@ -267,11 +262,6 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             if (lane == 0) umma_commit(&acc_full[slot]);
             __syncwarp();
         }
-        // the last commit covers every MMA this thread issued: they are done
-        // before the tensor memory is freed, even if the epilogue stopped
-        // waiting for them after a timeout
-        if (lane == 0 && nr > 0)
-            mbar_wait(&acc_full[(nr - 1) & 1], ((nr - 1) >> 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
         __syncwarp();
     } else {
         // ===================== epilogue: accumulate, finish tiles =============
@@ -365,6 +355,23 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // After a timeout let a wait of this CTA go early, its loads and MMAs
+    // still in flight are waited for (bounded) before the tensor memory is
+    // freed and the CTA ends: the last phase of each stage and the last
+    // commit, which covers every MMA.  In a healthy run every one of them has
+    // been waited for already.
+    if (*abort_flag) {
+        if (warp == 0 && lane == 0) {
+            const uint32_t it = static_cast<uint32_t>(n_runs[1]), ns = static_cast<uint32_t>(p.stages);
+            for (uint32_t i = it > ns ? it - ns : 0; i < it; ++i)
+                mbar_wait(&full[i % ns], (i / ns) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+        }
+        if (warp == 1 && lane == 0 && nr > 0)
+            mbar_wait(&acc_full[(nr - 1) & 1], ((nr - 1) >> 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
     if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
     if (threadIdx.x == 0) {
         __threadfence();

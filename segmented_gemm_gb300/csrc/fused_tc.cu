@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
     const TcParams &p = args.p;
     const CUtensorMap &tm_s = args.s;
     static_assert(kStg * kWSlot >= kBM * kBN * 4, "a split tile's fp32 partials fit in the W slots");
-    static_assert((2 * kStg + 5) * 8 + 8 <= 256, "barriers, TMEM address and abort flag fit");
+    static_assert((2 * kStg + 5) * 8 + 16 <= 256, "barriers, TMEM address, abort flag and drain counts fit");
     static_assert(tc_smem_bytes<kStg>() <= 232448, "fits the opt-in shared memory of a CTA");
     // the last item's bf16 output is staged in the idle x slots when it fits
     constexpr bool kCanStage = kBM * kStageRow <= kStg * kXSlot;
@@ -283,6 +283,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
     uint64_t *sk_bar = acc_empty + 2;   // stream-K head: the partial sums have landed in the W ring
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sk_bar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *drain = const_cast<int *>(abort_flag) + 1;   // for the teardown: [0] stages issued, [1] the last item
     // bias of the output tile of each accumulator slot: [2][kBN] bf16 (16-byte aligned)
     uint32_t *s_bias = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(full) + 256);
 
@@ -473,11 +474,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
         }
         if (lane == 0) {
             settle();
-            // every load this warp issued has landed before the CTA ends (after
-            // a timeout the MMA may have stopped waiting for some): the last
-            // phase of each stage
-            for (uint32_t i = it > kStg ? it - kStg : 0; i < it; ++i)
-                mbar_wait(&full[i % kStg], (i / kStg) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+            drain[0] = static_cast<int>(it);
         }
     } else if (warp >= 6) {
         // ===================== x loaders: permuted-row gather (cp.async) =====
@@ -584,11 +581,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
             __syncwarp();
             last_q = q;
         }
-        // the last commit covers every MMA this thread issued: they are done
-        // before the tensor memory is freed, even if the epilogue stopped
-        // waiting for them after a timeout
-        if (lane == 0 && last_q >= 0)
-            mbar_wait(&acc_full[last_q & 1], (last_q >> 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+        if (lane == 0) drain[1] = last_q;
         __syncwarp();
     } else if (warp >= 2) {
         // ===================== epilogue (warps 2..5) =========================
@@ -861,6 +854,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // After a timeout let a wait of this CTA go early, its loads and MMAs
+    // still in flight are waited for (bounded) before the tensor memory is
+    // freed and the CTA ends: the last phase of each stage (the producer's
+    // bytes and the loader warps' copies) and the last commit, which covers
+    // every MMA.  In a healthy run every one of them has been waited for.
+    if (*abort_flag) {
+        if (warp == 0 && lane == 0) {
+            const uint32_t it = static_cast<uint32_t>(drain[0]);
+            for (uint32_t i = it > kStg ? it - kStg : 0; i < it; ++i)
+                mbar_wait(&full[i % kStg], (i / kStg) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+        }
+        if (warp == 1 && lane == 0 && drain[1] >= 0)
+            mbar_wait(&acc_full[drain[1] & 1], (drain[1] >> 1) & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
     if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
