@@ -64,8 +64,11 @@ enum {
 enum {
     LORA_DEV_BAD_ID = 1 << 0,   /* some id was < -1 or >= num_adapters (treated as -1) */
     LORA_DEV_TIMEOUT = 1 << 1,  /* a bounded wait gave up; that call's output is invalid */
-    LORA_DEV_BAD_POOL = 1 << 2  /* pool layout the tables cannot describe: a rank not whole panels per
+    LORA_DEV_BAD_POOL = 1 << 2, /* pool layout the tables cannot describe: a rank not whole panels per
                                    output slice, or a b_offset not whole [N, 16] panels */
+    LORA_DEV_CHECK = 1 << 3     /* a segment table failed lora_check_segments, or (library built with
+                                   LORA_DEBUG) a kernel met a table-derived index out of range and
+                                   skipped that access; the call's output is invalid */
 };
 
 #define LORA_MAX_RANK 128       /* largest padded rank */
@@ -225,6 +228,26 @@ int lora_workspace_init(void *ws, size_t ws_bytes, lora_stream_t stream);
  */
 int lora_build_segments(const int32_t *lora_id_map, int64_t M, const lora_pool_t *pool,
                         lora_segments_t *out, void *ws, size_t ws_bytes, lora_stream_t stream);
+
+/*
+ * §2.3 / §2.4: check, on the device, a segment table held in ws against the
+ * lora_id_map (DEVICE int32 [M]) and pool it was built for.  One small
+ * kernel that writes nothing but the status word: LORA_DEV_CHECK (read with
+ * lora_get_status) when the bucket widths differ from the counts of the ids
+ * (the segment sums), perm is not the stable order of the tokens by bucket,
+ * the segment list is not the adapters present with their starts, lengths
+ * and padded ranks, or a tile / chunk work list is out of range.  segs: the
+ * table, as lora_build_segments returned it (checked against ws, M and the
+ * pool like a prebuilt table: LORA_ERR_SEGMENTS).  M = 0 is a no-op.
+ *
+ * Debug build: the library compiled with LORA_DEBUG (liblora_debug.so, the
+ * same exports) runs this check after every table it builds, and its fused
+ * kernels test each table-derived row index before they use it (a bad one
+ * sets LORA_DEV_CHECK and the access is skipped).  The normal build has
+ * neither cost.
+ */
+int lora_check_segments(const int32_t *lora_id_map, int64_t M, const lora_pool_t *pool,
+                        const lora_segments_t *segs, void *ws, size_t ws_bytes, lora_stream_t stream);
 
 /*
  * §2.2 first product alone: S[t, j] = sum_k x[t,k] A_{id[t]}[j,k] for

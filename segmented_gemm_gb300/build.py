@@ -1,9 +1,12 @@
 """Compile liblora.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
 Each translation unit is compiled in parallel, then linked into
-``segmented_gemm_gb300/liblora.so``.  The CUDA runtime is linked statically
-so the library only needs the driver at run time.  Usage:
-``python -m segmented_gemm_gb300.build [--force] [--verbose]``.
+``segmented_gemm_gb300/liblora.so``; the same sources compiled with
+``-DLORA_DEBUG`` (segment-table checks before every use, kernels that test
+table-derived row indices) are linked into ``liblora_debug.so`` beside it.
+The CUDA runtime is linked statically so the library only needs the driver
+at run time.  Usage: ``python -m segmented_gemm_gb300.build [--force]
+[--verbose]``.
 """
 from __future__ import annotations
 
@@ -19,9 +22,11 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "liblora.so")
+DEBUG_LIB_PATH = os.path.join(PKG, "liblora_debug.so")
 
 SOURCES = ["lora_api.cu", "seg_build.cu", "fused_tc.cu", "fused_splitk.cu", "fused_cluster.cu",
-           "lora_noalloc.cu", "moe.cu", "widen.cu"]
+           "lora_noalloc.cu", "moe.cu", "widen.cu", "seg_check.cu"]
+VARIANTS = ((LIB_PATH, "", []), (DEBUG_LIB_PATH, "debug", ["-DLORA_DEBUG"]))
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -46,18 +51,24 @@ def _stale(obj: str, src: str) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    """Compile both variants (all translation units in one pool) and link
+    each library whose objects changed; returns the normal library's path."""
     nvcc = _nvcc()
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
                      "--expt-relaxed-constexpr"]
     if verbose:
         common += ["-Xptxas", "-v"]
-    jobs = []
-    for src in SOURCES:
-        s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        if force or _stale(o, s):
-            jobs.append([nvcc, "-c", s, "-o", o] + common)
+    jobs, objs, relink = [], {}, {}
+    for lib, sub, defs in VARIANTS:
+        odir = os.path.join(BUILD_DIR, sub) if sub else BUILD_DIR
+        os.makedirs(odir, exist_ok=True)
+        objs[lib] = [os.path.join(odir, s.replace(".cu", ".o")) for s in SOURCES]
+        relink[lib] = force or not os.path.exists(lib)
+        for src, o in zip(SOURCES, objs[lib]):
+            s = os.path.join(CSRC, src)
+            if force or _stale(o, s):
+                jobs.append([nvcc, "-c", s, "-o", o] + common + defs)
+                relink[lib] = True
 
     def run(cmd):
         r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
@@ -69,15 +80,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
                 sys.stdout.write(out)
             if rc:
                 raise RuntimeError(f"nvcc failed ({rc}) for {cmd[2]}")
-    objs = [os.path.join(BUILD_DIR, s.replace(".cu", ".o")) for s in SOURCES]
-    if force or jobs or not os.path.exists(LIB_PATH):
-        tmp = LIB_PATH + f".tmp{os.getpid()}"
-        cmd = [nvcc, "-shared", "-o", tmp] + objs + ARCH + ["-Xcompiler", "-fPIC"]
+    for lib, _, _ in VARIANTS:
+        if not relink[lib]:
+            continue
+        tmp = lib + f".tmp{os.getpid()}"
+        cmd = [nvcc, "-shared", "-o", tmp] + objs[lib] + ARCH + ["-Xcompiler", "-fPIC"]
         r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
         if r.returncode:
             sys.stdout.write(r.stdout)
             raise RuntimeError("nvcc link failed")
-        os.replace(tmp, LIB_PATH)
+        os.replace(tmp, lib)
     return LIB_PATH
 
 

@@ -96,7 +96,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     int32_t *status = p.counters + CNT_STATUS;
     const long long wait = p.wait_cycles;
 
-    const int D = p.hdr[HDR_DCHUNKS];               // rank panels of the adapters present
+    // rank panels of the adapters present (LORA_DEBUG build: none when the
+    // segment table failed its check; the base product alone is computed)
+    const int D = kDebugChecks && p.hdr[HDR_CHECK] != 0 ? 0 : p.hdr[HDR_DCHUNKS];
     const int RT = (D + 7) / 8;                     // shrink tiles (8 panels = 128 rows)
     const int EU = (D + 3) / 4;                     // expand units per output tile
     const ListGeo g_shr = {static_cast<int64_t>(RT) * p.kblocks, p.kblocks};

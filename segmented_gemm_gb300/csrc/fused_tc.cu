@@ -328,11 +328,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
     pdl_wait();
 
     // shrink items: every shrink job in p.shrink_split pieces along K
+    // LORA_DEBUG build: a segment table that failed its check leaves every
+    // CTA's work list empty (every CTA reads the same verdict)
+    const bool table_bad = kDebugChecks && p.mode != kModeMoe && p.hdr[HDR_CHECK] != 0;
     const int nmt = p.mode == kModeMoe ? min(p.hdr[HDR_MOE_TILES], p.num_mtiles) : p.num_mtiles;
-    const int n_sjobs =
-        (p.mode == kModeExpand || p.mode == kModeMoe) ? 0 : p.hdr[HDR_NSJOBS] * p.shrink_split * p.num_layers;
+    const int n_sjobs = (p.mode == kModeExpand || p.mode == kModeMoe || table_bad)
+                            ? 0 : p.hdr[HDR_NSJOBS] * p.shrink_split * p.num_layers;
     int n_out = 0;   // output tiles of every layer
-    if (p.mode != kModeShrink)
+    if (p.mode != kModeShrink && !table_bad)
         for (int l = 0; l < p.num_layers; ++l) n_out += nmt * p.layer[l].num_ntiles;
     SkPlan sk = sk_plan(n_sjobs, n_out, gridDim.x, p.layer[0].kblocks, p.streamk != 0, p.shrink_split);
     sk.nmt = nmt;
@@ -501,6 +504,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                 int64_t pp = static_cast<int64_t>(jb.m) * kBM + rb + 16 * q;
                 if (pp >= p.M) pp = p.M - 1;
                 int64_t row = p.perm[pp];
+                if (kDebugChecks && !debug_index_ok(row >= (p.mode == kModeMoe ? -1 : 0) && row < p.out_rows, status))
+                    row = 0;
                 if (p.mode == kModeMoe) row = row >= 0 ? row / p.topk : 0;   // a pair's token; a gap reads row 0
                 src[q] = Ly.x + row * Ly.K + chunk * 8;
             }
@@ -607,8 +612,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
             // the row's original token, read while the MMA still runs
             const int64_t pp = static_cast<int64_t>(jb.m) * kBM + row;
             // kModeMoe: the output row is the pair itself (-1: a gap of the padded order)
-            const bool valid = pp < p.M && (p.mode != kModeMoe || p.perm[pp] >= 0);
-            const int tok = valid ? p.perm[pp] : 0;
+            bool valid = pp < p.M && (p.mode != kModeMoe || p.perm[pp] >= 0);
+            int tok = valid ? p.perm[pp] : 0;
+            if (kDebugChecks && valid && !debug_index_ok(tok >= 0 && tok < p.out_rows, status)) {
+                valid = false;   // this row is neither read by id nor stored
+                tok = 0;
+            }
             const bool lora_row = p.mode != kModeExpand || pp >= p.offsets[1];
             // the LoRA scale of my row: the call's scale times its adapter's
             // factor (rows outside every segment are masked anyway); the
@@ -881,6 +890,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
 __global__ void __launch_bounds__(kBM) s_prep_kernel(const float *S, int32_t s_cols, float scale, TcParams p)
 {
     const int m = blockIdx.x, row = threadIdx.x;
+    if (kDebugChecks && p.hdr[HDR_CHECK] != 0) return;   // LORA_DEBUG: the table failed its check
     const int64_t pp = static_cast<int64_t>(m) * kBM + row;
     const bool valid = pp < p.M;
     const int tok = valid ? p.perm[pp] : 0;

@@ -46,6 +46,7 @@ enum PlanHdr {
     HDR_DCHUNKS = 2,      // chunks of the split-K schedule (adapters present)
     HDR_NSEG = 3,         // number of segments
     HDR_MOE_TILES = 4,    // routing: 128-row tiles of the padded expert order
+    HDR_CHECK = 5,        // the table checker's verdict on this table: 0 consistent, 1 not
     HDR_WORDS = 16
 };
 
@@ -61,6 +62,21 @@ enum Counters {
 // cycles), set by lora_set_wait_budget; read when a launch is enqueued
 constexpr int64_t kDefaultWaitCycles = 2000000000ll;
 int64_t tc_wait_cycles();
+
+// Checks compiled into the LORA_DEBUG build only: an index that a kernel
+// derives from the segment table is tested before it is used; a bad one
+// sets LORA_DEV_CHECK and the access is skipped.  In the normal build the
+// condition is not evaluated.
+#ifdef LORA_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+__device__ __forceinline__ bool debug_index_ok(bool ok, int32_t *status)
+{
+    if (!ok) atomicOr(status, LORA_DEV_CHECK);
+    return ok;
+}
 
 struct WsLayout {
     int64_t M;
@@ -139,6 +155,7 @@ struct TcParams {
     int32_t num_layers;        // layers of this launch (1..kMaxLayers)
     const int32_t *ids;        // lora_id_map (original token order); read when adapter_scale is set
     int32_t topk;              // kModeMoe: pairs per token (a pair's token is pair / topk)
+    int64_t out_rows;          // rows a perm entry may name: M (kModeMoe: the pairs, M * topk)
     const int32_t *mt_expert;  // kModeMoe: the expert of each 128-row tile of the padded order
     uint16_t *s_panels;        // bf16 [layers][sets][chunks][128][16]
     float *s_out;              // fp32 [M, s_cols] (shrink mode)
@@ -193,6 +210,15 @@ struct SegParams {
     int32_t *counters;
     int32_t n_counters;
     int32_t num_slices;        // output slices of a merged projection (>= 1): tile chunk lists are slice-major
+};
+
+// The table checker (seg_check.cu): the builder's parameters plus the
+// workspace's capacities and the pool's extent.
+struct SegCheckParams {
+    SegParams s;
+    int32_t max_chunks, max_sjobs, max_dchunks;
+    int64_t a_rows;            // rows of the A pool (a_elems / K)
+    int64_t b_panels;          // [N, 16] panels of the B pool (b_elems / (16 N))
 };
 
 // Mixture-of-experts routing: the (token, slot) pairs sorted stably by
@@ -259,6 +285,7 @@ struct WidenParams {
 // ---- launchers (enqueue only; return the launch status) --------------------
 cudaError_t launch_widen(const WidenParams &p, int max_segments, cudaStream_t stream);
 cudaError_t launch_seg_build(const SegParams &p, bool pdl, cudaStream_t stream);
+cudaError_t launch_seg_check(const SegCheckParams &q, cudaStream_t stream);
 cudaError_t launch_moe_route(const RouteParams &p, cudaStream_t stream);
 cudaError_t launch_tc(const TcArgs &args, int grid, cudaStream_t stream);
 cudaError_t launch_moe_finalize(const uint16_t *out, const int32_t *expert, const float *weight, int64_t M, int topk,

@@ -287,12 +287,28 @@ static void fill_seg_params(SegParams &p, const int32_t *ids, int64_t M, const l
     p.num_slices = pool->num_slices > 1 ? pool->num_slices : 1;
 }
 
+// The table checker over the table in ws (lora_check_segments; after every
+// table build in the LORA_DEBUG build).
+static int enqueue_check(const int32_t *ids, int64_t M, const lora_pool_t *pool, const WsLayout &L, void *ws,
+                         cudaStream_t stream)
+{
+    SegCheckParams q;
+    fill_seg_params(q.s, ids, M, pool, L, ws);
+    q.max_chunks = L.max_chunks;
+    q.max_sjobs = L.max_sjobs;
+    q.max_dchunks = L.max_dchunks;
+    q.a_rows = pool->num_adapters ? pool->a_elems / pool->K : 0;
+    q.b_panels = pool->num_adapters ? pool->b_elems / (static_cast<int64_t>(kChunk) * pool->N) : 0;
+    return launch_seg_check(q, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
 static int enqueue_segments(const int32_t *ids, int64_t M, const lora_pool_t *pool, const WsLayout &L, void *ws,
                             cudaStream_t stream, bool pdl = false)
 {
     SegParams p;
     fill_seg_params(p, ids, M, pool, L, ws);
-    return launch_seg_build(p, pdl, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+    if (launch_seg_build(p, pdl, stream) != cudaSuccess) return LORA_ERR_CUDA;
+    return kDebugChecks ? enqueue_check(ids, M, pool, L, ws, stream) : LORA_OK;
 }
 
 // Validate the common arguments and make sure a segment table exists in ws
@@ -312,7 +328,8 @@ static int prepare(const int32_t *ids, int64_t M, const lora_pool_t *pool, const
         if (segs->plan != ws || segs->M != M || segs->num_adapters != pool->num_adapters ||
             segs->num_slices != (pool->num_slices > 1 ? pool->num_slices : 1) || segs->perm != at<int32_t>(ws, L->perm))
             return LORA_ERR_SEGMENTS;
-        return LORA_OK;
+        // the LORA_DEBUG build checks a prebuilt table before it is used
+        return kDebugChecks && ids ? enqueue_check(ids, M, pool, *L, ws, stream) : LORA_OK;
     }
     if (!ids) return LORA_ERR_NULL;
     return build ? enqueue_segments(ids, M, pool, *L, ws, stream) : LORA_OK;
@@ -329,6 +346,7 @@ static void fill_tc_params(TcParams &p, const WsLayout &L, void *ws, const lora_
 {
     std::memset(&p, 0, sizeof p);
     p.M = M;
+    p.out_rows = M;
     p.num_adapters = pool->num_adapters;
     p.num_slices = pool->num_slices > 1 ? pool->num_slices : 1;
     p.num_layers = 1;
@@ -688,7 +706,9 @@ static int run_cluster(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, co
                        s32))
             return LORA_ERR_CUDA;
     }
-    return launch_cluster(m, p, pdl, stream) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+    if (launch_cluster(m, p, pdl, stream) != cudaSuccess) return LORA_ERR_CUDA;
+    // the table this launch built, checked once the launch is complete
+    return kDebugChecks && build ? enqueue_check(ids, M, pool, L, ws, stream) : LORA_OK;
 }
 
 }  // namespace lora
@@ -824,6 +844,7 @@ int lora_moe_gemm(const lora_bf16_t *x, int64_t M, int32_t K, const lora_bf16_t 
     p.mode = kModeMoe;
     p.num_slices = 1;
     p.topk = topk;
+    p.out_rows = M * static_cast<int64_t>(topk);   // perm_pad names pairs (or -1)
     p.perm = at<int32_t>(ws, L.perm_pad);
     p.hdr = at<int32_t>(ws, L.hdr);
     p.counters = at<int32_t>(ws, L.counters);
@@ -932,6 +953,20 @@ int lora_build_segments(const int32_t *lora_id_map, int64_t M, const lora_pool_t
     if (rc) return rc;
     fill_segments(ws, L, M, pool, out);
     return LORA_OK;
+}
+
+int lora_check_segments(const int32_t *lora_id_map, int64_t M, const lora_pool_t *pool, const lora_segments_t *segs,
+                        void *ws, size_t ws_bytes, lora_stream_t stream)
+{
+    if (!segs) return LORA_ERR_NULL;
+    if (M < 0) return LORA_ERR_SHAPE;
+    if (M == 0) return check_pool(pool);
+    if (!lora_id_map) return LORA_ERR_NULL;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsLayout L;
+    const int rc = prepare(lora_id_map, M, pool, segs, ws, ws_bytes, s, &L);
+    if (rc) return rc;
+    return enqueue_check(lora_id_map, M, pool, L, ws, s);
 }
 
 int lora_linear_ex(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, const lora_bf16_t *bias,

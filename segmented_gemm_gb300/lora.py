@@ -16,13 +16,14 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "liblora.so")
+DEBUG_LIB_PATH = os.path.join(_PKG, "liblora_debug.so")   # built with LORA_DEBUG: table checks before every use
 
 LORA_OK = 0
 LORA_ERR_NULL, LORA_ERR_SHAPE, LORA_ERR_ALIGN, LORA_ERR_RANK = 1, 2, 3, 4
 LORA_ERR_WORKSPACE, LORA_ERR_CUDA, LORA_ERR_UNSUPPORTED, LORA_ERR_SEGMENTS = 5, 6, 7, 8
 LORA_ERR_CAPACITY = 9
 LORA_NOALLOC_SCRATCH_BYTES = 8 << 20
-LORA_DEV_BAD_ID, LORA_DEV_TIMEOUT, LORA_DEV_BAD_POOL = 1, 2, 4
+LORA_DEV_BAD_ID, LORA_DEV_TIMEOUT, LORA_DEV_BAD_POOL, LORA_DEV_CHECK = 1, 2, 4, 8
 LORA_PATH_AUTO, LORA_PATH_TILED, LORA_PATH_SPLITK, LORA_PATH_STREAM = 0, 1, 2, 3
 LORA_FLAG_STATIC_WEIGHTS = 0x100
 LORA_MAX_SLICES = 4
@@ -34,7 +35,7 @@ EXPORTS = ("lora_pool_layout", "lora_workspace_size", "lora_workspace_init", "lo
            "lora_shrink", "lora_expand", "lora_linear", "lora_linear_ex", "lora_get_status",
            "lora_status_string", "lora_linear_noalloc", "lora_moe_workspace_size", "lora_moe_route",
            "lora_moe_gemm", "lora_moe_finalize", "lora_moe", "lora_layers_workspace_size", "lora_linear_layers",
-           "lora_set_wait_budget")
+           "lora_set_wait_budget", "lora_check_segments")
 
 
 class lora_pool_t(ctypes.Structure):
@@ -66,17 +67,26 @@ class LoraError(RuntimeError):
         self.code = code
 
 
-_lib = None
+_libs = {}
+_active = LIB_PATH
+
+
+def use_debug_library(debug: bool):
+    """Route every later call through liblora_debug.so (True) or liblora.so
+    (False).  Both may be loaded at once; workspaces and pools serve either."""
+    global _active
+    _active = DEBUG_LIB_PATH if debug else LIB_PATH
 
 
 def load_library():
-    """Load liblora.so; raises if it has not been built."""
-    global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"liblora.so is not built ({LIB_PATH}); run __graft_entry__.build()")
-    lib = ctypes.CDLL(LIB_PATH)
+    """Load the active library (liblora.so unless use_debug_library(True));
+    raises if it has not been built."""
+    path = _active
+    if path in _libs:
+        return _libs[path]
+    if not os.path.exists(path):
+        raise RuntimeError(f"{os.path.basename(path)} is not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
     P, I32, I64, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
     PP = ctypes.POINTER(lora_pool_t)
     PS = ctypes.POINTER(lora_segments_t)
@@ -100,12 +110,13 @@ def load_library():
         "lora_layers_workspace_size": (SZ, [I64, I32, I32, I32]),
         "lora_linear_layers": (ctypes.c_int, [P, I32, I64, P, PS, P, SZ, P]),
         "lora_set_wait_budget": (ctypes.c_int, [I64]),
+        "lora_check_segments": (ctypes.c_int, [P, I64, PP, PS, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
         f.restype = res
         f.argtypes = args
-    _lib = lib
+    _libs[path] = lib
     return lib
 
 
@@ -293,6 +304,13 @@ def lora_build_segments(ids: torch.Tensor, pool: LoraPool, ws: Workspace, stream
                                               ctypes.byref(out), ws.ptr, ws.nbytes, _stream(stream)),
            "lora_build_segments")
     return out
+
+
+def lora_check_segments(ids: torch.Tensor, pool: LoraPool, ws: Workspace, segs: lora_segments_t, stream=None):
+    """Enqueue the device check of the table in ws; its verdict is the
+    LORA_DEV_CHECK bit of lora_get_status."""
+    _check(load_library().lora_check_segments(_ptr(ids), ids.numel(), ctypes.byref(pool.desc), ctypes.byref(segs),
+                                              ws.ptr, ws.nbytes, _stream(stream)), "lora_check_segments")
 
 
 def segments_to_host(segs: lora_segments_t, ws: Workspace, M: int, num_adapters: int) -> dict:

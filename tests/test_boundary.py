@@ -162,3 +162,30 @@ def test_wait_budget_knob_validates(lib):
     assert lib.lora_set_wait_budget(-1) == L.LORA_ERR_SHAPE
     assert lib.lora_set_wait_budget(1_000_000) == L.LORA_OK
     assert lib.lora_set_wait_budget(0) == L.LORA_OK   # back to the default
+
+
+def test_debug_library_exports_the_same_symbols(lib):
+    """liblora_debug.so (the sources built with LORA_DEBUG) is the same ABI."""
+    assert os.path.exists(L.DEBUG_LIB_PATH), "build() makes both libraries"
+    dbg = ctypes.CDLL(L.DEBUG_LIB_PATH)
+    for n in L.EXPORTS:
+        assert hasattr(dbg, n), n
+
+
+def test_device_status_bits_match_the_header():
+    src = open(os.path.join(ROOT, "include", "lora.h")).read()
+    bits = {m.group(1): 1 << int(m.group(2)) for m in re.finditer(r"\b(LORA_DEV_[A-Z_]+)\s*=\s*1\s*<<\s*(\d+)", src)}
+    assert set(bits) == {"LORA_DEV_BAD_ID", "LORA_DEV_TIMEOUT", "LORA_DEV_BAD_POOL", "LORA_DEV_CHECK"}
+    for name, v in bits.items():
+        assert getattr(L, name) == v, name
+
+
+def test_check_segments_host_errors_without_gpu(lib):
+    seg = L.lora_segments_t()
+    pool = _fake_pool(None)
+    F = lib.lora_check_segments
+    assert F(0x1000, 64, ctypes.byref(pool), None, 0x2000, 1 << 20, None) == L.LORA_ERR_NULL   # no table
+    assert F(0x1000, -1, ctypes.byref(pool), ctypes.byref(seg), 0x2000, 1 << 20, None) == L.LORA_ERR_SHAPE
+    assert F(None, 64, ctypes.byref(pool), ctypes.byref(seg), 0x2000, 1 << 20, None) == L.LORA_ERR_NULL   # no ids
+    assert F(0x1000, 0, ctypes.byref(pool), ctypes.byref(seg), 0x2000, 1 << 20, None) == L.LORA_OK   # M = 0: no-op
+    assert F(0x1000, 0, None, ctypes.byref(seg), 0x2000, 1 << 20, None) == L.LORA_ERR_NULL
