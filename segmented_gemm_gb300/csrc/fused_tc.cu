@@ -51,7 +51,6 @@ constexpr int kSAreaBytes = 2 * kPanelsPerStage * kSPanelBytes;   // S panels [s
 constexpr int kTcThreads = 320;   // 10 warps: TMA, MMA, 4 epilogue, 4 x loaders
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 256;
-constexpr int kStageRow = kBN * 2 + 16;   // a staged output row: 512 bytes + 16 of padding
 // The shared memory holds one ring of stages.  A stage is an x slot (the
 // loader warps' cp.async row gathers, 16 KB) and a W slot (the producer's
 // TMA boxes: W, A panels, or S and B panels, 32 KB) with ONE full barrier,
@@ -270,8 +269,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
     static_assert(kStg * kWSlot >= kBM * kBN * 4, "a split tile's fp32 partials fit in the W slots");
     static_assert((2 * kStg + 5) * 8 + 16 <= 256, "barriers, TMEM address, abort flag and drain counts fit");
     static_assert(tc_smem_bytes<kStg>() <= 232448, "fits the opt-in shared memory of a CTA");
-    // the last item's bf16 output is staged in the idle x slots when it fits
-    constexpr bool kCanStage = kBM * kStageRow <= kStg * kXSlot;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *xring = smem;                                  // the stages' x slots, kStg x 16 KB
@@ -628,14 +625,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                 const int id = p.ids[tok];
                 row_sc *= (id >= 0 && id < p.num_adapters) ? __ldg(Ly.adapter_scale + id) : 0.f;
             }
-            // the CTA's last item: both rings are idle, so an output tile is
-            // staged in the x ring (rows padded to 528 bytes: conflict-free)
-            // and each row goes out as one bulk copy, which writes whole
-            // lines instead of one 32-byte piece of 32 rows per warp store
-            Job nx;
-            const bool staged = kCanStage && (p.mode == kModeLinear || p.mode == kModeMoe) && jb.kind == 1 &&
-                                jb.part != kPartTail &&
-                                !get_item(q + 1, blockIdx.x, gridDim.x, n_sjobs, n_out, sk, p, nx);
             mbar_wait(&acc_full[slot], use & 1, abort_flag, status, LORA_DEV_TIMEOUT, wait);
             tc_fence_after();
             const uint32_t tbase = tmem_base + slot * kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
@@ -722,7 +711,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                 // original row ----------------------------------------------
                 const int n0 = jb.n * kBN;
                 const bool head = jb.part == kPartHead;
-                uint8_t *srow = xring + row * kStageRow;
                 // the head is its CTA's last item: the W ring is idle now, and
                 // the first tail's partials (128 KB) come in by four bulk
                 // copies; further tails' are added from L2
@@ -779,20 +767,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                     }
                     const int col = n0 + cc * 16;
                     if (!valid || col >= Ly.N || !lora_row) return;
-                    if (staged) {
-                        const uint4 *bsrc = reinterpret_cast<const uint4 *>(tbias + cc * 8);
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint4 u = out_bias ? bsrc[h] : make_uint4(0u, 0u, 0u, 0u);
-                            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-                            uint32_t o4[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                o4[e] = pack_bf16x2(v[8 * h + 2 * e] + bf16_lo(w4[e]), v[8 * h + 2 * e + 1] + bf16_hi(w4[e]));
-                            *reinterpret_cast<uint4 *>(srow + cc * 32 + h * 16) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-                        }
-                        return;
-                    }
                     uint16_t *dst = Ly.y + static_cast<int64_t>(tok) * Ly.N + col;
                     if (p.mode == kModeExpand) {
                         const uint4 *src = reinterpret_cast<const uint4 *>(dst);
@@ -841,13 +815,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                     }
 #pragma unroll
                     for (int h = 0; h < 4; ++h) emit(cc + h, r[h]);
-                }
-                if (staged && valid && lora_row && n0 < Ly.N) {
-                    fence_proxy_async_smem();   // my row's generic-proxy writes -> the bulk copy's reads
-                    bulk_store(Ly.y + static_cast<int64_t>(tok) * Ly.N + n0, srow,
-                               static_cast<uint32_t>(min(kBN, Ly.N - n0)) * 2);
-                    bulk_commit();
-                    bulk_wait_read_all();   // the row is out of shared memory; y is written before the grid ends
                 }
                 if (head && et == 0) {
                     p.sk_cnt[jb.slot * kWinCntStride] = 0;   // zero again for the next call
