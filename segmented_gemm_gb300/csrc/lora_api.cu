@@ -840,7 +840,11 @@ int lora_moe_gemm(const lora_bf16_t *x, int64_t M, int32_t K, const lora_bf16_t 
     p.layer[0].scale = 1.f;
     p.layer[0].x = x;
     p.layer[0].y = out;
-    p.group_m = 8;
+    // one group of every token tile: the tiles that use one expert's weight
+    // tile (its token tiles, for one column tile) are consecutive in the work
+    // list and run in the same wave, so each weight tile is read from HBM
+    // once (groups of 8 measured 168 us per grouped GEMM, one group 157 us)
+    p.group_m = L.max_mtiles;
     p.mode = kModeMoe;
     p.num_slices = 1;
     p.topk = topk;
