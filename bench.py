@@ -120,7 +120,8 @@ def load_peaks():
 
 
 # The source file each timed kernel is compiled from; a summary taken on an
-# older copy of that file, or of the headers every kernel includes, is stale.
+# older copy of that file's code, or of the headers every kernel includes, is
+# stale (comments do not count).
 KERNEL_SOURCES = {   # the sources each kernel is compiled from (besides internal.h and ptx.cuh)
     "lora_cluster_kernel": ("fused_cluster.cu", "seg_build_body.cuh"),
     "lora_tc_kernel": ("fused_tc.cu",),
@@ -129,11 +130,36 @@ KERNEL_SOURCES = {   # the sources each kernel is compiled from (besides interna
 }
 
 
+def code_only(src: str) -> str:
+    """C/CUDA source without its comments and blank lines: an edit of a
+    comment leaves a kernel's measurements standing."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":                      # a string or character literal, kept whole
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            i = src.find("\n", i)
+            i = n if i < 0 else i
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (ln.rstrip() for ln in "".join(out).split("\n"))
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def kernel_source_hash(kernel: str):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "segmented_gemm_gb300", "csrc")
     for f in KERNEL_SOURCES[kernel] + ("internal.h", "ptx.cuh"):
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(code_only(open(os.path.join(csrc, f)).read()).encode())
     return h.hexdigest()[:16]
 
 

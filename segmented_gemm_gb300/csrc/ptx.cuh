@@ -170,7 +170,6 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *m)
     asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
 }
 
-// 2-D tiled load of the map's box at (x = inner coordinate, y = row).
 // Plain bulk copy of `bytes` (multiple of 16, both addresses 16-byte
 // aligned) from global to shared memory, completing on an mbarrier.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
@@ -181,6 +180,7 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                  : "memory");
 }
 
+// 2-D tiled load of the map's box at (x = inner coordinate, y = row).
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, uint64_t *bar, int x, int y)
 {
     asm volatile(
