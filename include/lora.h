@@ -418,11 +418,20 @@ int lora_linear_noalloc(const lora_bf16_t *x, int64_t M, const lora_bf16_t *W, c
  *                      routing of the same expert ids in ws)
  *   lora_moe_finalize: the weighted sum of each token's rows
  *   lora_moe:          the three in order
+ *   lora_moe_check_route: a device check of the routing in ws against the
+ *                      expert ids it was made from (bucket widths, perm
+ *                      stable and complete, the segment table, the padded
+ *                      order and each tile's expert): LORA_DEV_CHECK when
+ *                      they disagree.  The LORA_DEBUG build runs it after
+ *                      every routing, and its grouped GEMM leaves its work
+ *                      list empty on a routing that failed.
  * Errors as for the other entry points.
  */
 size_t lora_moe_workspace_size(int64_t M, int32_t topk, int32_t num_experts);
 int lora_moe_route(const int32_t *expert, int64_t M, int32_t topk, int32_t num_experts, void *ws, size_t ws_bytes,
                    lora_stream_t stream);
+int lora_moe_check_route(const int32_t *expert, int64_t M, int32_t topk, int32_t num_experts, void *ws,
+                         size_t ws_bytes, lora_stream_t stream);
 int lora_moe_gemm(const lora_bf16_t *x, int64_t M, int32_t K, const lora_bf16_t *W, int32_t N, int32_t num_experts,
                   int32_t topk, lora_bf16_t *out, void *ws, size_t ws_bytes, lora_stream_t stream);
 int lora_moe_finalize(const lora_bf16_t *out, const int32_t *expert, const float *weight, int64_t M, int32_t topk,

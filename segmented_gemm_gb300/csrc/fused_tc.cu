@@ -325,9 +325,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
     pdl_wait();
 
     // shrink items: every shrink job in p.shrink_split pieces along K
-    // LORA_DEBUG build: a segment table that failed its check leaves every
-    // CTA's work list empty (every CTA reads the same verdict)
-    const bool table_bad = kDebugChecks && p.mode != kModeMoe && p.hdr[HDR_CHECK] != 0;
+    // LORA_DEBUG build: a segment table (or an expert routing) that failed
+    // its check leaves every CTA's work list empty (every CTA reads the same
+    // verdict)
+    const bool table_bad = kDebugChecks && p.hdr[HDR_CHECK] != 0;
     const int nmt = p.mode == kModeMoe ? min(p.hdr[HDR_MOE_TILES], p.num_mtiles) : p.num_mtiles;
     const int n_sjobs = (p.mode == kModeExpand || p.mode == kModeMoe || table_bad)
                             ? 0 : p.hdr[HDR_NSJOBS] * p.shrink_split * p.num_layers;

@@ -286,6 +286,7 @@ struct WidenParams {
 cudaError_t launch_widen(const WidenParams &p, int max_segments, cudaStream_t stream);
 cudaError_t launch_seg_build(const SegParams &p, bool pdl, cudaStream_t stream);
 cudaError_t launch_seg_check(const SegCheckParams &q, cudaStream_t stream);
+cudaError_t launch_moe_route_check(const RouteParams &p, cudaStream_t stream);
 cudaError_t launch_moe_route(const RouteParams &p, cudaStream_t stream);
 cudaError_t launch_tc(const TcArgs &args, int grid, cudaStream_t stream);
 cudaError_t launch_moe_finalize(const uint16_t *out, const int32_t *expert, const float *weight, int64_t M, int topk,

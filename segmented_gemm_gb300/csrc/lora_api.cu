@@ -781,22 +781,15 @@ size_t lora_moe_workspace_size(int64_t M, int32_t topk, int32_t num_experts)
     return make_moe_layout(M, topk, num_experts).total;
 }
 
-int lora_moe_route(const int32_t *expert, int64_t M, int32_t topk, int32_t num_experts, void *ws, size_t ws_bytes,
-                   lora_stream_t stream)
+// The routing's parameters over the workspace ws of layout L.
+static RouteParams route_params(const int32_t *expert, const MoeLayout &L, void *ws)
 {
-    int rc = check_moe(M, 8, 8, num_experts, topk);
-    if (rc) return rc;
-    if (M == 0) return LORA_OK;
-    if (!expert) return LORA_ERR_NULL;
-    const MoeLayout L = make_moe_layout(M, topk, num_experts);
-    if (!ws || ws_bytes < L.total) return LORA_ERR_WORKSPACE;
-    if (!device_supported()) return LORA_ERR_UNSUPPORTED;
     RouteParams p;
     std::memset(&p, 0, sizeof p);
     p.expert = expert;
     p.P = L.P;
-    p.E = num_experts;
-    p.nb = num_experts + 1;
+    p.E = L.E;
+    p.nb = L.E + 1;
     p.chunk = L.chunk;
     p.nchunks = L.nchunks;
     p.max_mtiles = L.max_mtiles;
@@ -813,7 +806,45 @@ int lora_moe_route(const int32_t *expert, int64_t M, int32_t topk, int32_t num_e
     p.counters = at<int32_t>(ws, L.counters);
     p.perm_pad = at<int32_t>(ws, L.perm_pad);
     p.mt_expert = at<int32_t>(ws, L.mt_expert);
-    return launch_moe_route(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+    return p;
+}
+
+// Shared validation of the routing calls; *L receives the layout.
+static int route_prepare(const int32_t *expert, int64_t M, int32_t topk, int32_t num_experts, void *ws,
+                         size_t ws_bytes, MoeLayout *L)
+{
+    int rc = check_moe(M, 8, 8, num_experts, topk);
+    if (rc) return rc;
+    if (M == 0) return LORA_OK;
+    if (!expert) return LORA_ERR_NULL;
+    *L = make_moe_layout(M, topk, num_experts);
+    if (!ws || ws_bytes < L->total) return LORA_ERR_WORKSPACE;
+    if (!device_supported()) return LORA_ERR_UNSUPPORTED;
+    return LORA_OK;
+}
+
+int lora_moe_route(const int32_t *expert, int64_t M, int32_t topk, int32_t num_experts, void *ws, size_t ws_bytes,
+                   lora_stream_t stream)
+{
+    MoeLayout L;
+    const int rc = route_prepare(expert, M, topk, num_experts, ws, ws_bytes, &L);
+    if (rc || M == 0) return rc;
+    const RouteParams p = route_params(expert, L, ws);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (launch_moe_route(p, s) != cudaSuccess) return LORA_ERR_CUDA;
+    // the LORA_DEBUG build checks every routing it makes
+    return kDebugChecks && launch_moe_route_check(p, s) != cudaSuccess ? LORA_ERR_CUDA : LORA_OK;
+}
+
+int lora_moe_check_route(const int32_t *expert, int64_t M, int32_t topk, int32_t num_experts, void *ws,
+                         size_t ws_bytes, lora_stream_t stream)
+{
+    MoeLayout L;
+    const int rc = route_prepare(expert, M, topk, num_experts, ws, ws_bytes, &L);
+    if (rc || M == 0) return rc;
+    return launch_moe_route_check(route_params(expert, L, ws), static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? LORA_OK
+               : LORA_ERR_CUDA;
 }
 
 int lora_moe_gemm(const lora_bf16_t *x, int64_t M, int32_t K, const lora_bf16_t *W, int32_t N, int32_t num_experts,

@@ -149,6 +149,113 @@ __global__ void __launch_bounds__(kCheckThreads) seg_check_kernel(const SegCheck
     }
 }
 
+// The routing of a mixture-of-experts layer ("Qwen3-MoE low-latency
+// inference on Atlas A3", its MoE section: the (token, slot) pairs sorted by
+// expert before the grouped matmul), checked against the pairs' experts the
+// same way: bucket widths against the counts (bucket 0: ids outside [0, E)),
+// perm a stable permutation by bucket, one segment per expert with pairs,
+// and the padded order: each expert's pairs, in perm's order, from a fresh
+// 128-row tile, -1 in the gaps, each tile's expert, the tile count.
+__global__ void __launch_bounds__(kCheckThreads) moe_route_check_kernel(const RouteParams p)
+{
+    __shared__ int s_off[LORA_MAX_ADAPTERS + 2];
+    __shared__ int s_cnt[LORA_MAX_ADAPTERS + 1];
+    __shared__ int s_padt[LORA_MAX_ADAPTERS + 2];   // first padded tile of each expert (index e + 1: bucket)
+    __shared__ int s_present;
+    const int E = p.E, nb = E + 1, tid = threadIdx.x;
+    const int64_t P = p.P;
+    bool bad = false;
+    for (int b = tid; b < nb; b += kCheckThreads) s_cnt[b] = 0;
+    for (int b = tid; b <= nb; b += kCheckThreads) s_off[b] = p.offsets[b];
+    if (tid == 0) s_present = 0;
+    __syncthreads();
+    for (int64_t t = tid; t < P; t += kCheckThreads) atomicAdd(&s_cnt[check_bucket(p.expert[t], E)], 1);
+    __syncthreads();
+    if (tid == 0) {
+        bad |= s_off[0] != 0;
+        int tiles = 0;   // the padded order's tiles, expert by expert
+        for (int b = 1; b < nb; ++b) {
+            s_padt[b] = tiles;
+            tiles += (s_cnt[b] + kBM - 1) / kBM;
+        }
+        s_padt[nb] = tiles;
+        bad |= tiles > p.max_mtiles || p.hdr[HDR_MOE_TILES] != tiles;
+    }
+    for (int b = tid; b < nb; b += kCheckThreads) {
+        if (s_off[b + 1] - s_off[b] != s_cnt[b]) bad = true;
+        if (b >= 1 && s_cnt[b] > 0) atomicAdd(&s_present, 1);
+    }
+    const bool offs_bad = __syncthreads_or(bad) != 0;
+
+    for (int64_t j = tid; j < P; j += kCheckThreads) {
+        const int t = p.perm[j];
+        if (t < 0 || t >= P) {
+            bad = true;
+            continue;
+        }
+        if (offs_bad) continue;
+        int lo = 0, hi = nb - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_off[mid] <= j) lo = mid;
+            else hi = mid - 1;
+        }
+        if (check_bucket(p.expert[t], E) != lo) bad = true;
+        if (j + 1 < s_off[lo + 1] && p.perm[j + 1] <= t) bad = true;
+    }
+
+    const int n = *p.num_segments;
+    if (tid == 0 && (n < 0 || n > E || n != s_present || p.hdr[HDR_NSEG] != n)) bad = true;
+    for (int s = tid; s < ((n >= 0 && n <= E) ? n : 0); s += kCheckThreads) {
+        const int id = p.seg_id[s];
+        if (id < 0 || id >= E) {
+            bad = true;
+            continue;
+        }
+        if (s > 0 && p.seg_id[s - 1] >= id) bad = true;
+        if (p.seg_len[s] != s_cnt[id + 1] || p.seg_len[s] <= 0 || p.seg_rank[s] != 0) bad = true;
+        if (!offs_bad && p.seg_start[s] != s_off[id + 1]) bad = true;
+    }
+
+    // the padded order (its capacity: max_mtiles tiles of 128 rows)
+    if (!offs_bad) {
+        const int64_t npad = static_cast<int64_t>(p.max_mtiles) * kBM;
+        const int tiles = s_padt[nb];
+        for (int64_t i = tid; i < npad; i += kCheckThreads) {
+            const int m = static_cast<int>(i / kBM);
+            int want = -1;
+            if (m < tiles) {
+                int lo = 1, hi = nb - 1;   // the expert whose tiles hold m: the last b with s_padt[b] <= m
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (s_padt[mid] <= m) lo = mid;
+                    else hi = mid - 1;
+                }
+                const int64_t k = i - static_cast<int64_t>(s_padt[lo]) * kBM;
+                if (k < s_cnt[lo]) {
+                    const int64_t j = s_off[lo] + k;   // its position in perm
+                    want = (j >= 0 && j < P) ? p.perm[j] : -2;
+                }
+                if (i % kBM == 0 && p.mt_expert[m] != lo - 1) bad = true;
+            } else if (i % kBM == 0 && p.mt_expert[m] != -1) {
+                bad = true;
+            }
+            if (p.perm_pad[i] != want) bad = true;
+        }
+    }
+    const bool any_bad = __syncthreads_or(bad) != 0;
+    if (tid == 0) {
+        p.hdr[HDR_CHECK] = any_bad ? 1 : 0;
+        if (any_bad) atomicOr(p.counters + CNT_STATUS, LORA_DEV_CHECK);
+    }
+}
+
+cudaError_t launch_moe_route_check(const RouteParams &p, cudaStream_t stream)
+{
+    moe_route_check_kernel<<<1, kCheckThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_seg_check(const SegCheckParams &q, cudaStream_t stream)
 {
     seg_check_kernel<<<1, kCheckThreads, 0, stream>>>(q);

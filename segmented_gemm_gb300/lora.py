@@ -35,7 +35,7 @@ EXPORTS = ("lora_pool_layout", "lora_workspace_size", "lora_workspace_init", "lo
            "lora_shrink", "lora_expand", "lora_linear", "lora_linear_ex", "lora_get_status",
            "lora_status_string", "lora_linear_noalloc", "lora_moe_workspace_size", "lora_moe_route",
            "lora_moe_gemm", "lora_moe_finalize", "lora_moe", "lora_layers_workspace_size", "lora_linear_layers",
-           "lora_set_wait_budget", "lora_check_segments")
+           "lora_set_wait_budget", "lora_check_segments", "lora_moe_check_route")
 
 
 class lora_pool_t(ctypes.Structure):
@@ -111,6 +111,7 @@ def load_library():
         "lora_linear_layers": (ctypes.c_int, [P, I32, I64, P, PS, P, SZ, P]),
         "lora_set_wait_budget": (ctypes.c_int, [I64]),
         "lora_check_segments": (ctypes.c_int, [P, I64, PP, PS, P, SZ, P]),
+        "lora_moe_check_route": (ctypes.c_int, [P, I64, I32, I32, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -481,6 +482,40 @@ def lora_moe_route(expert: torch.Tensor, num_experts: int, ws: MoeWorkspace, str
            "lora_moe_route")
 
 
+def lora_moe_gemm(x: torch.Tensor, W: torch.Tensor, topk: int, ws: MoeWorkspace, out: torch.Tensor, stream=None):
+    """The grouped GEMM alone over the routing in ws: out [M * topk, N] bf16,
+    each routed pair's row x[t] W_e^T (rows of dropped slots untouched)."""
+    M, K = x.shape
+    E, N, _ = W.shape
+    _check(load_library().lora_moe_gemm(_ptr(x), M, K, _ptr(W), N, E, topk, _ptr(out), ws.ptr, ws.nbytes,
+                                         _stream(stream)), "lora_moe_gemm")
+
+
+def lora_moe_check_route(expert: torch.Tensor, num_experts: int, ws: MoeWorkspace, stream=None):
+    """Enqueue the device check of the routing in ws against expert int32
+    [M, topk]; its verdict is the LORA_DEV_CHECK bit of lora_get_status."""
+    M, topk = expert.shape
+    _check(load_library().lora_moe_check_route(_ptr(expert), M, topk, num_experts, ws.ptr, ws.nbytes,
+                                               _stream(stream)), "lora_moe_check_route")
+
+
+def moe_routing_layout(M: int, topk: int, num_experts: int) -> dict:
+    """Byte offsets of the routing's arrays in a MoE workspace, in the order
+    lora_moe_workspace_size lays them out (each region 256-byte aligned)."""
+    P, E = M * topk, num_experts
+    max_mtiles = (P + 127) // 128 + E
+    sizes = [("counters", (8 + 8) * 4), ("perm", max(P, 1) * 4), ("offsets", (E + 2) * 4),
+             ("seg_id", max(E, 1) * 4), ("seg_start", max(E, 1) * 4), ("seg_len", max(E, 1) * 4),
+             ("seg_rank", max(E, 1) * 4), ("num_segments", 4), ("hdr", 16 * 4), ("perm_pad", max_mtiles * 128 * 4),
+             ("mt_expert", max_mtiles * 4)]
+    out, o = {}, 0
+    for name, n in sizes:
+        out[name] = o
+        o = (o + n + 255) & ~255
+    out["max_mtiles"] = max_mtiles
+    return out
+
+
 def moe_routing_to_host(ws: MoeWorkspace, M: int, topk: int, num_experts: int):
     """The routing's perm over the pairs and its bucket offsets (CPU int32)."""
     P = M * topk
@@ -489,10 +524,5 @@ def moe_routing_to_host(ws: MoeWorkspace, M: int, topk: int, num_experts: int):
     def grab(off, n):
         return base[off:off + 4 * n].view(torch.int32).cpu()
 
-    def align(v):
-        return (v + 255) & ~255
-    # the layout of lora_moe_workspace_size: counter block (CNT_FIXED + 8 ints), perm, offsets
-    o_counters = 0
-    o_perm = align(o_counters + (8 + 8) * 4)
-    o_offsets = align(o_perm + max(P, 1) * 4)
-    return grab(o_perm, P), grab(o_offsets, num_experts + 2)
+    lay = moe_routing_layout(M, topk, num_experts)
+    return grab(lay["perm"], P), grab(lay["offsets"], num_experts + 2)

@@ -189,3 +189,24 @@ def test_check_segments_host_errors_without_gpu(lib):
     assert F(None, 64, ctypes.byref(pool), ctypes.byref(seg), 0x2000, 1 << 20, None) == L.LORA_ERR_NULL   # no ids
     assert F(0x1000, 0, ctypes.byref(pool), ctypes.byref(seg), 0x2000, 1 << 20, None) == L.LORA_OK   # M = 0: no-op
     assert F(0x1000, 0, None, ctypes.byref(seg), 0x2000, 1 << 20, None) == L.LORA_ERR_NULL
+
+
+@pytest.mark.parametrize("M,topk,E", [(1, 1, 1), (37, 2, 5), (2048, 8, 64), (40000, 8, 1024)])
+def test_moe_layout_mirror_fits_the_workspace(lib, M, topk, E):
+    """The binding's mirror of the routing's layout (the arrays the tests
+    read and edit) ends inside the workspace the library sizes."""
+    lay = L.moe_routing_layout(M, topk, E)
+    order = ["counters", "perm", "offsets", "seg_id", "seg_start", "seg_len", "seg_rank", "num_segments", "hdr",
+             "perm_pad", "mt_expert"]
+    offs = [lay[k] for k in order]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    assert lay["mt_expert"] + 4 * lay["max_mtiles"] <= lib.lora_moe_workspace_size(M, topk, E)
+
+
+def test_moe_check_route_host_errors_without_gpu(lib):
+    F = lib.lora_moe_check_route
+    assert F(None, 4, 2, 0, None, 0, None) == L.LORA_ERR_SHAPE      # no experts
+    assert F(None, 4, 3, 2, None, 0, None) == L.LORA_ERR_SHAPE      # topk > E
+    assert F(None, 4, 2, 4, None, 0, None) == L.LORA_ERR_NULL       # no expert ids
+    assert F(None, 0, 2, 4, None, 0, None) == L.LORA_OK             # no tokens: nothing to check
+    assert F(0x1000, 4, 2, 4, None, 0, None) == L.LORA_ERR_WORKSPACE

@@ -11,8 +11,12 @@ work lists derived from it) and sets LORA_DEV_CHECK when they disagree.
   edit is undone.  The checker reads only inside the table's arrays (every
   index it follows is range-checked first), so these edits run safely.
 
+lora_moe_check_route does the same for the routing of a mixture-of-experts
+layer (the pairs sorted stably by expert, the padded expert order, each
+tile's expert), with the same two kinds of tests.
+
 liblora_debug.so runs the checker on every table before a fused kernel
-uses it:
+uses it, and on every routing it makes:
 - on valid inputs it matches the oracle on every schedule and never raises
   LORA_DEV_CHECK;
 - given a prebuilt table whose perm names a token past M, it flags the
@@ -284,3 +288,104 @@ def test_debug_library_refuses_a_table_whose_perm_leaves_the_batch(debug_lib):
                           path=path)
         assert L.lora_get_status(ws) == 0
         assert_close(y, oracle.lora_linear(wl), f"M={M} after a fresh build")
+
+
+# ---- the routing of a mixture-of-experts layer ----------------------------------
+
+def _route(M, topk, E, seed, skew=0.0, invalid=False):
+    mw = workloads.make_moe(M, 64, 64, E, topk, seed=seed, skew=skew)
+    ex = mw.expert.clone()
+    if invalid and M > 3:
+        ex[1, 0] = E + 3       # outside [0, E): routed with the dropped slots
+        ex[2, topk - 1] = -1   # a dropped slot
+    return mw, ex
+
+
+ROUTES = [(1, 1, 1, 0.0), (37, 2, 5, 0.0), (300, 4, 16, 2.0), (2048, 8, 64, 1.0), (5000, 2, 7, 0.0),
+          (777, 8, 300, 0.5)]
+
+
+@pytest.mark.parametrize("M,topk,E,skew", ROUTES)
+def test_route_checker_accepts_every_routing(M, topk, E, skew):
+    for invalid in (False, True):
+        _, ex = _route(M, topk, E, seed=M + E, skew=skew, invalid=invalid)
+        ws = L.MoeWorkspace(M, topk, E)
+        L.lora_moe_route(ex.cuda(), E, ws)
+        first = L.lora_get_status(ws)
+        assert first == (L.LORA_DEV_BAD_ID if invalid and M > 3 else 0)
+        L.lora_moe_check_route(ex.cuda(), E, ws)
+        assert L.lora_get_status(ws) == 0, f"M={M} E={E} invalid={invalid}"
+
+
+def test_route_checker_flags_each_edit_and_passes_once_undone():
+    M, topk, E = 300, 4, 16
+    _, ex = _route(M, topk, E, seed=661, skew=2.0, invalid=True)
+    exd = ex.cuda()
+    ws = L.MoeWorkspace(M, topk, E)
+    L.lora_moe_route(exd, E, ws)
+    L.lora_get_status(ws)
+    lay = L.moe_routing_layout(M, topk, E)
+    perm, off = (t.tolist() for t in L.moe_routing_to_host(ws, M, topk, E))
+    P = M * topk
+
+    def word(name, i):
+        o = lay[name] + 4 * i
+        return ws.buf[o:o + 4].view(torch.int32)
+
+    busy = max(range(1, E + 1), key=lambda b: off[b + 1] - off[b])   # the busiest expert's bucket
+    j = off[busy]
+    other = next(b for b in range(1, E + 1) if b != busy and off[b + 1] > off[b])
+    tiles = int(word("hdr", 4).item())   # the padded order's tile count
+    pad_first = int(word("perm_pad", 0).item())
+    edits = [
+        ("perm past the pairs", [("perm", 3, P + 5)]),
+        ("perm repeats a pair", [("perm", j + 1, perm[j])]),
+        ("perm swaps pairs of two experts", [("perm", j, perm[off[other]]), ("perm", off[other], perm[j])]),
+        ("a bucket offset moved", [("offsets", busy, off[busy] + 1)]),
+        ("a padded row names another pair", [("perm_pad", 0, pad_first + 1 if pad_first + 1 < P else 0)]),
+        ("a row past the last tile holds a pair", [("perm_pad", tiles * 128 + 5, 0)]),
+        ("a tile's expert", [("mt_expert", 0, int(word("mt_expert", 0).item()) + 1)]),
+        ("a tile past the last has an expert", [("mt_expert", tiles, 0)]),
+        ("the tile count", [("hdr", 4, tiles + 1)]),
+        ("a segment length", [("seg_len", 0, int(word("seg_len", 0).item()) + 1)]),
+        ("the segment count", [("num_segments", 0, int(word("num_segments", 0).item()) - 1)]),
+    ]
+    assert tiles < lay["max_mtiles"]
+    for name, edit in edits:
+        saved = []
+        for arr, i, v in edit:
+            w = word(arr, i)
+            saved.append((w, w.clone()))
+            w.fill_(v)
+        L.lora_moe_check_route(exd, E, ws)
+        status = L.lora_get_status(ws)
+        for w, old in reversed(saved):
+            w.copy_(old)
+        assert status & L.LORA_DEV_CHECK, f"{name}: not flagged (status {status})"
+        L.lora_moe_check_route(exd, E, ws)
+        assert L.lora_get_status(ws) == 0, f"{name}: still flagged once undone"
+
+
+def test_debug_library_refuses_a_routing_that_failed_its_check(debug_lib):
+    """The debug build checks the routing it makes (the layer matches the
+    oracle, no alarm).  A routing edited afterwards and checked again is
+    flagged, and the grouped GEMM then leaves its output untouched; routing
+    afresh works again."""
+    M, topk, E = 300, 4, 16
+    mw = workloads.make_moe(M, 256, 192, E, topk, seed=671, skew=1.0)
+    x, W, ex, wt = mw.x.cuda(), mw.W.cuda(), mw.expert.cuda(), mw.weight.cuda()
+    ws = L.MoeWorkspace(M, topk, E)
+    y = L.lora_moe(x, W, ex, wt, ws)
+    assert L.lora_get_status(ws) == 0
+    assert_close(y, oracle.moe(mw.x, mw.W, mw.expert, mw.weight), "moe through the debug build")
+    lay = L.moe_routing_layout(M, topk, E)
+    ws.buf[lay["perm_pad"]:lay["perm_pad"] + 4].view(torch.int32).fill_(M * topk + 100)   # a pair past the batch
+    L.lora_moe_check_route(ex, E, ws)
+    out = torch.full((M * topk, 192), float("nan"), dtype=torch.bfloat16, device="cuda")
+    L.lora_moe_gemm(x, W, topk, ws, out)
+    status = L.lora_get_status(ws)
+    assert status & L.LORA_DEV_CHECK, f"status {status}"
+    assert torch.isnan(out.float()).all(), "the grouped GEMM ran on a routing that failed its check"
+    y2 = L.lora_moe(x, W, ex, wt, ws)   # routes afresh
+    assert L.lora_get_status(ws) == 0
+    assert_close(y2, oracle.moe(mw.x, mw.W, mw.expert, mw.weight), "moe after routing afresh")
