@@ -345,12 +345,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
         // The S-ready counter of (layer, token tile m) is put back to zero by
         // the last of the layer's num_ntiles output tiles of row m to pass
         // the wait on it: each adds itself to a consumer counter right after
-        // the wait and reads the result one item later, so the round trip
-        // hides behind the loads.
+        // the wait (a release: its read of the counter comes first) and reads
+        // the result one item later, so the round trip hides behind the
+        // loads; the last one takes an acquire fence before the reset, which
+        // orders the reset after every consumer's read.
         int32_t *cons = p.counters + CNT_FIXED + p.num_layers * p.num_mtiles;
         int rst_m = -1, rst_old = 0, rst_nt = 0;   // counter index, consumers before me, the layer's tiles per row
         auto settle = [&]() {
             if (rst_m >= 0 && rst_old == rst_nt - 1) {
+                fence_acq_rel_gpu();
                 p.counters[CNT_FIXED + rst_m] = 0;
                 cons[rst_m] = 0;
             }
@@ -443,7 +446,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) lora_tc_kernel(const __grid_con
                                       LORA_DEV_TIMEOUT, wait);
                         fence_proxy_async_global();
                         settle();
-                        rst_old = atom_acq_rel_gpu_add(cons + ci, 1);
+                        rst_old = atom_release_gpu_add(cons + ci, 1);
                         rst_m = ci;
                         rst_nt = Ly.num_ntiles;
                     }

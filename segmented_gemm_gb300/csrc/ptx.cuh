@@ -34,6 +34,15 @@ __device__ __forceinline__ void red_relaxed_gpu_add(int32_t *p, int v)
 
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// Release only: the thread's earlier accesses are ordered before the add,
+// and nothing after it waits for the result.
+__device__ __forceinline__ int atom_release_gpu_add(int32_t *p, int v)
+{
+    int old;
+    asm volatile("atom.release.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ int atom_acq_rel_gpu_add(int32_t *p, int v)
 {
     int old;
