@@ -1106,6 +1106,11 @@ int lora_linear_layers(const lora_layer_t *layers, int32_t num_layers, int64_t M
         if (segs->plan != ws || segs->M != M || segs->num_adapters != p0->num_adapters ||
             segs->num_slices != (p0->num_slices > 1 ? p0->num_slices : 1) || segs->perm != at<int32_t>(ws, L.perm))
             return LORA_ERR_SEGMENTS;
+        // the LORA_DEBUG build checks a prebuilt table before it is used
+        if (kDebugChecks && lora_id_map) {
+            int rc = enqueue_check(lora_id_map, M, p0, L, ws, s);
+            if (rc) return rc;
+        }
     } else {
         int rc = enqueue_segments(lora_id_map, M, p0, L, ws, s);
         if (rc) return rc;

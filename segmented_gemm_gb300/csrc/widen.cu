@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(256) widen_kernel(const WidenParams p)
     const int seg = blockIdx.x / p.parts, part = blockIdx.x - seg * p.parts;
     if (seg >= *p.num_segments) return;
     const int i = p.seg_id[seg];
+    if (kDebugChecks && (i < 0 || i >= p.A)) return;   // LORA_DEBUG: a table the checker has flagged
     const int64_t na = static_cast<int64_t>(p.rank[i]) * p.K / 16;   // 16-code groups (padded rows are zero)
     const int64_t nb = static_cast<int64_t>(p.rank[i]) * p.N / 16;
     const uint8_t *a8 = p.a8 + p.a_off[i];

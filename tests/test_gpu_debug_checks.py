@@ -290,6 +290,34 @@ def test_debug_library_refuses_a_table_whose_perm_leaves_the_batch(debug_lib):
         assert_close(y, oracle.lora_linear(wl), f"M={M} after a fresh build")
 
 
+def test_debug_library_refuses_a_bad_prebuilt_table_for_several_layers(debug_lib):
+    """lora_linear_layers with a prebuilt table: the debug build checks it
+    first, and a perm entry past M leaves every layer's output untouched."""
+    M = 300
+    base = workloads.make_custom(M, 256, 256, [16, 32, 64], seed=681)
+    wls = [workloads.make_custom(M, K, N, [16, 32, 64], seed=682 + j, ids=base.ids.clone())
+           for j, (K, N) in enumerate([(256, 512), (384, 256)])]
+    devs = [to_dev(w) for w in wls]
+    ids = devs[0]["ids"]
+    ws = L.LayersWorkspace(M, 512, 3, len(wls))
+    segs = L.lora_build_segments(ids, devs[0]["pool"], ws)
+    assert L.lora_get_status(ws) == 0
+    ys = [torch.full((M, w.N), float("nan"), dtype=torch.bfloat16, device="cuda") for w in wls]
+    layers = [(d["x"], d["W"], d["bias"], d["pool"], w.scale, y) for w, d, y in zip(wls, devs, ys)]
+    L.lora_linear_layers(layers, ids, ws, segs=segs)
+    assert L.lora_get_status(ws) == 0
+    for j, (w, y) in enumerate(zip(wls, ys)):
+        assert_close(y, oracle.lora_linear(w), f"layer {j}, prebuilt table")
+    _word(ws, segs.perm, 7).fill_(M + 1000)
+    for y in ys:
+        y.fill_(float("nan"))
+    L.lora_linear_layers(layers, ids, ws, segs=segs)
+    status = L.lora_get_status(ws)
+    assert status & L.LORA_DEV_CHECK, f"status {status}"
+    for j, y in enumerate(ys):
+        assert torch.isnan(y.float()).all(), f"layer {j} was written from a refused table"
+
+
 # ---- the routing of a mixture-of-experts layer ----------------------------------
 
 def _route(M, topk, E, seed, skew=0.0, invalid=False):
