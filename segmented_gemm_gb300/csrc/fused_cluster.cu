@@ -36,7 +36,8 @@
 // the owner sums them, adds the bias and writes y.
 // Roles (320 threads): warp 0 TMA producer (the weight box and the x box of
 // each unit, B windows), warp 1 TMEM allocator + MMA issuer, warps 2..5
-// epilogue (warp 2 also derives the metadata), warps 6..9 stage the S
+// epilogue (warp 2 also derives the metadata, warp 3 pulls the B windows
+// into L2 as soon as they are known), warps 6..9 stage the S
 // operand of the expand units (load-convert-store into the S ring).  All waits are bounded;
 // the host only launches the grid when every cluster can be resident at once.
 #include <cuda_runtime.h>
@@ -93,6 +94,14 @@ static_assert((4 * kClMaxStages + kStMaxRegions + 1 + 2 * kClMaxSRing) * 8 + 10 
                       kStMaxWinCta * kStWin * 4 + kStMaxWinCta * 4 <=
                   kClMisc,
               "cluster kernel tables overflow their shared-memory area");
+
+// Pull one box of a 3-D tensor map into L2 (no shared-memory destination,
+// nothing to wait for).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *m, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(m), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
 
 __device__ __forceinline__ void tma_load_3d_st(void *dst, const CUtensorMap *m, uint64_t *bar, int x, int y, int z)
 {
@@ -800,6 +809,13 @@ __global__ void __launch_bounds__(kClThreads, 1)
             named_bar_sync(kBarTablesEpi, 128);   // s_run_info, s_wbits
         }
         const int ns = *n_segs;
+        // The B boxes of my expand windows into L2 now (a prefetch through the
+        // tensor map: the box the producer loads after the weight stream), so
+        // that load finds them there instead of waiting on HBM.  The pool is
+        // a weight; L2 is coherent, so this is safe before the programmatic
+        // wait too.
+        if (warp == 3 && *n_exp)
+            for (int w = lane; w < segs[ns].b - segs[ns].a; w += 32) tma_prefetch_3d(&tm_b3, 0, n0, s_win_panel[w]);
         // ---- shrink runs: add my partial window sums, then release ------------
         auto shrink_run = [&](const StSeg &sg, int run) {
             mbar_wait(&acc_full[sg.region], 0, abort_flag, status, LORA_DEV_TIMEOUT);
