@@ -57,7 +57,9 @@ enum {
     LORA_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch error, bad device) */
     LORA_ERR_UNSUPPORTED = 7,   /* device is not sm_103 / sm_100 family or similar */
     LORA_ERR_SEGMENTS = 8,      /* a prebuilt segment table does not match this call */
-    LORA_ERR_CAPACITY = 9       /* the problem needs more scratch than lora_linear_noalloc holds */
+    LORA_ERR_CAPACITY = 9,      /* the problem needs more scratch than lora_linear_noalloc holds */
+    LORA_ERR_ACCESS = 10        /* memory the current device cannot access (pageable host memory,
+                                   another device's memory) */
 };
 
 /* Device-side status bits (returned through lora_get_status). */
@@ -276,8 +278,11 @@ int lora_expand(const float *S, int32_t s_cols, int64_t M, const int32_t *lora_i
  * segments): y = x W^T + bias + scale * s_id * (x A_id^T) B_id^T per token
  * (s_id: the pool's per-adapter factor, 1 without one).
  * x: DEVICE bf16 [M, K]; W: DEVICE bf16 [N, K]; bias: DEVICE bf16 [N] or NULL;
- * lora_id_map: DEVICE int32 [M]; y: DEVICE bf16 [M, N] (written, never read).
- * K and N are taken from the pool.  segs: a table built for lora_id_map and
+ * lora_id_map: DEVICE int32 [M]; y: bf16 [M, N] (written, never read) in
+ * device memory or in pinned host memory through its device address
+ * (lora_device_pointer): the kernels write y with plain 16-byte stores, which
+ * reach host memory over the board's host link.  K and N are taken from the
+ * pool.  segs: a table built for lora_id_map and
  * this pool's ranks, or NULL to build one in ws first.  Accumulation is fp32;
  * S is rounded to bf16 once after scaling, the output once at the end.
  * M == 0 is a no-op.  A call whose ids are all -1 runs the base GEMM only.
@@ -459,6 +464,39 @@ int lora_get_status(void *ws, lora_stream_t stream, int32_t *status);
  * method has no counterpart: it is part of this library's failure detection.
  */
 int lora_set_wait_budget(int64_t cycles);
+
+/*
+ * Moving a step's inputs and outputs across the host link with the SMs.
+ *
+ * lora_device_pointer: the address a kernel on the current device uses for
+ * ptr.  That is ptr itself for this device's memory or managed memory, and
+ * the mapped alias for pinned host memory.  Returns LORA_ERR_ACCESS for
+ * pageable host memory, another device's memory or an unknown pointer, and
+ * LORA_ERR_NULL for a NULL argument.
+ *
+ * lora_copy_async: copies n <= LORA_MAX_COPIES buffers (dst[i] <- src[i],
+ * bytes[i] each) in one small kernel on `stream`: each side may be device
+ * memory or pinned host memory (given by its host address), so a step's
+ * host-to-device inputs move without a copy-engine transfer.  Addresses and
+ * sizes must be multiples of 16 bytes (LORA_ERR_ALIGN), sizes >= 0
+ * (LORA_ERR_SHAPE); a zero-byte entry is skipped; LORA_ERR_ACCESS as above.
+ * The kernel is a programmatic dependent launch: it starts while the kernel
+ * ahead of it finishes, waits for that kernel (griddepcontrol.wait) before
+ * it reads or writes any byte, and lets the launch behind it start its
+ * prologue at once.  Buffers must not overlap.  The copy is ordered on
+ * `stream` like any kernel; the host sees a host-side destination once the
+ * stream has been synchronised.  This is plumbing around the layer, not a
+ * step of the method.
+ */
+#define LORA_MAX_COPIES 4
+typedef struct {
+    void *dst;
+    const void *src;
+    int64_t bytes;
+} lora_copy_t;
+
+int lora_device_pointer(const void *ptr, void **dev_ptr);
+int lora_copy_async(const lora_copy_t *copies, int32_t n, lora_stream_t stream);
 
 /* Static text for a LORA_ERR_* code. */
 const char *lora_status_string(int code);

@@ -1202,6 +1202,7 @@ const char *lora_status_string(int code)
     case LORA_ERR_UNSUPPORTED: return "the current device is not an sm_103 (GB300-class) GPU";
     case LORA_ERR_SEGMENTS: return "the segment table was built for another call (M, pool or workspace differ)";
     case LORA_ERR_CAPACITY: return "the problem needs more scratch than lora_linear_noalloc holds (LORA_NOALLOC_SCRATCH_BYTES)";
+    case LORA_ERR_ACCESS: return "memory the current device cannot access (pageable host memory or another device's)";
     default: return "unknown status";
     }
 }

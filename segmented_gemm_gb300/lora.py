@@ -21,7 +21,8 @@ DEBUG_LIB_PATH = os.path.join(_PKG, "liblora_debug.so")   # built with LORA_DEBU
 LORA_OK = 0
 LORA_ERR_NULL, LORA_ERR_SHAPE, LORA_ERR_ALIGN, LORA_ERR_RANK = 1, 2, 3, 4
 LORA_ERR_WORKSPACE, LORA_ERR_CUDA, LORA_ERR_UNSUPPORTED, LORA_ERR_SEGMENTS = 5, 6, 7, 8
-LORA_ERR_CAPACITY = 9
+LORA_ERR_CAPACITY, LORA_ERR_ACCESS = 9, 10
+LORA_MAX_COPIES = 4
 LORA_NOALLOC_SCRATCH_BYTES = 8 << 20
 LORA_DEV_BAD_ID, LORA_DEV_TIMEOUT, LORA_DEV_BAD_POOL, LORA_DEV_CHECK = 1, 2, 4, 8
 LORA_PATH_AUTO, LORA_PATH_TILED, LORA_PATH_SPLITK, LORA_PATH_STREAM = 0, 1, 2, 3
@@ -35,7 +36,8 @@ EXPORTS = ("lora_pool_layout", "lora_workspace_size", "lora_workspace_init", "lo
            "lora_shrink", "lora_expand", "lora_linear", "lora_linear_ex", "lora_get_status",
            "lora_status_string", "lora_linear_noalloc", "lora_moe_workspace_size", "lora_moe_route",
            "lora_moe_gemm", "lora_moe_finalize", "lora_moe", "lora_layers_workspace_size", "lora_linear_layers",
-           "lora_set_wait_budget", "lora_check_segments", "lora_moe_check_route")
+           "lora_set_wait_budget", "lora_check_segments", "lora_moe_check_route", "lora_device_pointer",
+           "lora_copy_async")
 
 
 class lora_pool_t(ctypes.Structure):
@@ -54,6 +56,10 @@ class lora_segments_t(ctypes.Structure):
                 ("seg_len", ctypes.c_void_p), ("seg_rank", ctypes.c_void_p),
                 ("num_segments", ctypes.c_void_p), ("plan", ctypes.c_void_p),
                 ("M", ctypes.c_int64), ("num_adapters", ctypes.c_int32), ("num_slices", ctypes.c_int32)]
+
+
+class lora_copy_t(ctypes.Structure):
+    _fields_ = [("dst", ctypes.c_void_p), ("src", ctypes.c_void_p), ("bytes", ctypes.c_int64)]
 
 
 class lora_layer_t(ctypes.Structure):
@@ -112,6 +118,8 @@ def load_library():
         "lora_set_wait_budget": (ctypes.c_int, [I64]),
         "lora_check_segments": (ctypes.c_int, [P, I64, PP, PS, P, SZ, P]),
         "lora_moe_check_route": (ctypes.c_int, [P, I64, I32, I32, P, SZ, P]),
+        "lora_device_pointer": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_void_p)]),
+        "lora_copy_async": (ctypes.c_int, [ctypes.POINTER(lora_copy_t), I32, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -138,6 +146,37 @@ def _stream(stream=None):
     if stream is None:
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def device_pointer(t: torch.Tensor) -> int:
+    """The address kernels on the current device use for t's storage: its
+    own for device memory, the mapped alias for pinned host memory
+    (LoraError LORA_ERR_ACCESS for pageable host memory)."""
+    out = ctypes.c_void_p()
+    _check(load_library().lora_device_pointer(ctypes.c_void_p(t.data_ptr()), ctypes.byref(out)),
+           "lora_device_pointer")
+    return int(out.value)
+
+
+def _out_ptr(t: torch.Tensor):
+    """An output the kernels write with plain stores: device memory, or a
+    pinned host tensor through its device address."""
+    return ctypes.c_void_p(t.data_ptr() if t.is_cuda else device_pointer(t))
+
+
+def copy_async(pairs: Sequence[tuple], stream=None):
+    """dst <- src for up to LORA_MAX_COPIES (dst, src) tensor pairs of equal
+    byte size, in one kernel on ``stream`` (lora_copy_async): each side
+    contiguous, on the device or in pinned host memory."""
+    if len(pairs) > LORA_MAX_COPIES:
+        raise ValueError(f"at most {LORA_MAX_COPIES} copies per call")
+    arr = (lora_copy_t * max(len(pairs), 1))()
+    for i, (dst, src) in enumerate(pairs):
+        nb = dst.numel() * dst.element_size()
+        if src.numel() * src.element_size() != nb or not dst.is_contiguous() or not src.is_contiguous():
+            raise ValueError("copy_async: contiguous tensors of equal byte size")
+        arr[i].dst, arr[i].src, arr[i].bytes = dst.data_ptr(), src.data_ptr(), nb
+    _check(load_library().lora_copy_async(arr, len(pairs), _stream(stream)), "lora_copy_async")
 
 
 # ---------------------------------------------------------------------------
@@ -341,13 +380,14 @@ def lora_linear(x: torch.Tensor, W: torch.Tensor, bias: Optional[torch.Tensor], 
 
     ``static_weights``: W, bias and the pool are written by no kernel that
     can still run when the call starts (LORA_FLAG_STATIC_WEIGHTS), so the call
-    may start streaming them before the kernel ahead of it has finished."""
+    may start streaming them before the kernel ahead of it has finished.
+    ``y`` may be a pinned host tensor: the kernels store into it directly."""
     M = x.shape[0]
     if y is None:
         y = torch.empty(M, W.shape[0], dtype=torch.bfloat16, device=x.device)
     _check(load_library().lora_linear_ex(
         _ptr(x), M, _ptr(W), _ptr(bias), _ptr(ids), ctypes.byref(pool.desc), float(scale),
-        ctypes.byref(segs) if segs is not None else None, _ptr(y), ws.ptr, ws.nbytes,
+        ctypes.byref(segs) if segs is not None else None, _out_ptr(y), ws.ptr, ws.nbytes,
         _stream(stream), int(path) | (LORA_FLAG_STATIC_WEIGHTS if static_weights else 0)), "lora_linear")
     return y
 

@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from segmented_gemm_gb300 import lora as L
 
@@ -65,7 +66,7 @@ def test_workspace_size_monotone(lib):
 
 
 def test_status_strings(lib):
-    for c in range(10):
+    for c in range(11):
         assert L.status_string(c)
     assert "unknown" in L.status_string(99)
 
@@ -210,3 +211,45 @@ def test_moe_check_route_host_errors_without_gpu(lib):
     assert F(None, 4, 2, 4, None, 0, None) == L.LORA_ERR_NULL       # no expert ids
     assert F(None, 0, 2, 4, None, 0, None) == L.LORA_OK             # no tokens: nothing to check
     assert F(0x1000, 4, 2, 4, None, 0, None) == L.LORA_ERR_WORKSPACE
+
+
+def test_error_codes_and_copy_limit_match_the_header():
+    src = open(os.path.join(ROOT, "include", "lora.h")).read()
+    codes = {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(LORA_ERR_[A-Z_]+)\s*=\s*(\d+)", src)}
+    assert len(codes) == 10
+    for name, v in codes.items():
+        assert getattr(L, name) == v, name
+    assert int(re.search(r"#define LORA_MAX_COPIES (\d+)", src).group(1)) == L.LORA_MAX_COPIES
+    assert "access" in L.status_string(L.LORA_ERR_ACCESS)
+
+
+def test_copy_async_host_errors_without_gpu(lib):
+    # every check here returns before the library asks the driver anything
+    C = L.lora_copy_t
+    assert lib.lora_copy_async(None, 0, None) == L.LORA_OK
+    assert lib.lora_copy_async(None, 1, None) == L.LORA_ERR_NULL
+    assert lib.lora_copy_async((C * 5)(), 5, None) == L.LORA_ERR_SHAPE
+    assert lib.lora_copy_async((C * 1)(), -1, None) == L.LORA_ERR_SHAPE
+    one = (C * 1)()
+    one[0].dst, one[0].src, one[0].bytes = 0x1000, 0x2000, -16
+    assert lib.lora_copy_async(one, 1, None) == L.LORA_ERR_SHAPE
+    one[0].bytes = 0                                   # an empty entry is skipped
+    assert lib.lora_copy_async(one, 1, None) == L.LORA_OK
+    one[0].dst, one[0].bytes = None, 64
+    assert lib.lora_copy_async(one, 1, None) == L.LORA_ERR_NULL
+    for dst, src, nb in ((0x1008, 0x2000, 64), (0x1000, 0x2004, 64), (0x1000, 0x2000, 40)):
+        one[0].dst, one[0].src, one[0].bytes = dst, src, nb
+        assert lib.lora_copy_async(one, 1, None) == L.LORA_ERR_ALIGN, (dst, src, nb)
+    out = ctypes.c_void_p()
+    assert lib.lora_device_pointer(None, ctypes.byref(out)) == L.LORA_ERR_NULL
+    assert lib.lora_device_pointer(ctypes.c_void_p(0x1000), None) == L.LORA_ERR_NULL
+
+
+def test_copy_async_binding_checks_its_pairs():
+    a, b = torch.zeros(8), torch.zeros(4)
+    with pytest.raises(ValueError):
+        L.copy_async([(a, b)])                         # sizes differ
+    with pytest.raises(ValueError):
+        L.copy_async([(a, a)] * (L.LORA_MAX_COPIES + 1))
+    with pytest.raises(ValueError):
+        L.copy_async([(a[::2], b)])                    # not contiguous
