@@ -127,6 +127,7 @@ KERNEL_SOURCES = {   # the sources each kernel is compiled from (besides interna
     "lora_tc_kernel": ("fused_tc.cu",),
     "lora_splitk_kernel": ("fused_splitk.cu",),
     "seg_build_kernel": ("seg_build.cu", "seg_build_body.cuh"),
+    "moe_pair_kernel": ("moe_pair.cu", "moe_pair.h"),
 }
 
 
@@ -489,11 +490,20 @@ def run_moe_step(L, device, steps, warmup, stream, peaks):
     ms_whole = time_steps(whole, steps, warmup, stream) / steps
     ms_gemm = time_steps(gemm, steps, warmup, stream) / steps
     flops = 2 * mw.M * mw.topk * mw.K * mw.N
+    tflops = flops / (ms_gemm * 1e-3) / 1e12
     return {"workload": "mixture of experts: M=2048 tokens, K=2048, N=1536, 64 experts, top-8, skewed routing; "
                         "routing + grouped GEMM + weighted finalize",
             "M": mw.M, "tokens_per_s": round(mw.M / (ms_whole * 1e-3), 1), "ms_per_step": round(ms_whole, 5),
-            "gemm_us": round(ms_gemm * 1e3, 2), "gemm_tflops": round(flops / (ms_gemm * 1e-3) / 1e12, 1),
-            "tensor_frac": round(flops / (ms_gemm * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
+            "gemm_us": round(ms_gemm * 1e3, 2), "gemm_tflops": round(tflops, 1),
+            "tensor_frac": round(tflops / peaks["bf16_tflops"], 4),
+            # the grouped GEMM (two token tiles of an expert per work item)
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(tflops / peaks["bf16_tflops"], 4),
+                         "traffic": profiled_traffic("moe_pair_kernel", "moe"), "kernel": "moe_pair_kernel",
+                         "kernel_us": round(ms_gemm * 1e3, 3),
+                         "kernel_time_method": "lora_moe_gemm alone, back to back in CUDA graphs over two weight "
+                                               "sets, CUDA events on the launching stream",
+                         "algorithmic_flops": flops}}
 
 
 def run_e2e(wl, sets, L, device, steps, warmup, stream):

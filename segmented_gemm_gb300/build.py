@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(PKG, "liblora.so")
 DEBUG_LIB_PATH = os.path.join(PKG, "liblora_debug.so")
 
 SOURCES = ["lora_api.cu", "seg_build.cu", "fused_tc.cu", "fused_splitk.cu", "fused_cluster.cu",
-           "lora_noalloc.cu", "moe.cu", "widen.cu", "seg_check.cu", "stage.cu"]
+           "lora_noalloc.cu", "moe.cu", "widen.cu", "seg_check.cu", "stage.cu", "moe_pair.cu"]
 VARIANTS = ((LIB_PATH, "", []), (DEBUG_LIB_PATH, "debug", ["-DLORA_DEBUG"]))
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -12,6 +12,7 @@
 #include <vector>
 
 #include "internal.h"
+#include "moe_pair.h"
 #include "lora.h"
 
 namespace lora {
@@ -858,6 +859,29 @@ int lora_moe_gemm(const lora_bf16_t *x, int64_t M, int32_t K, const lora_bf16_t 
     const MoeLayout L = make_moe_layout(M, topk, num_experts);
     if (!ws || ws_bytes < L.total) return LORA_ERR_WORKSPACE;
     if (!device_supported()) return LORA_ERR_UNSUPPORTED;
+    const uint64_t Kq = K;
+    if (L.max_mtiles <= kMoePairMaxTiles) {
+        // two token tiles of an expert per work item (moe_pair.cu)
+        CUtensorMap w;
+        if (!encode_2d(&w, W, Kq, static_cast<uint64_t>(num_experts) * N, Kq * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B))
+            return LORA_ERR_CUDA;
+        MoePairParams mp;
+        mp.x = x;
+        mp.out = out;
+        mp.perm_pad = at<int32_t>(ws, L.perm_pad);
+        mp.mt_expert = at<int32_t>(ws, L.mt_expert);
+        mp.hdr = at<int32_t>(ws, L.hdr);
+        mp.status = at<int32_t>(ws, L.counters) + CNT_STATUS;
+        mp.out_rows = M * static_cast<int64_t>(topk);
+        mp.K = K;
+        mp.N = N;
+        mp.topk = topk;
+        mp.kblocks = (K + kBK - 1) / kBK;
+        mp.num_ntiles = (N + kBN - 1) / kBN;
+        mp.max_mtiles = L.max_mtiles;
+        mp.wait_cycles = tc_wait_cycles();
+        return launch_moe_pair(w, mp, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+    }
     TcArgs a;
     std::memset(&a, 0, sizeof a);
     TcParams &p = a.p;
@@ -888,7 +912,6 @@ int lora_moe_gemm(const lora_bf16_t *x, int64_t M, int32_t K, const lora_bf16_t 
     p.wait_cycles = tc_wait_cycles();
     p.s_sets = 1;
     TcLayerMaps &m = a.maps[0];
-    const uint64_t Kq = K;
     if (!encode_2d(&m.x, x, Kq, static_cast<uint64_t>(M), Kq * 2, kBK, 1, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ERR_CUDA;
     // the experts' weights stacked: [E * N, K]
     if (!encode_2d(&m.w, W, Kq, static_cast<uint64_t>(num_experts) * N, Kq * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B))
