@@ -453,9 +453,10 @@ int lora_get_status(void *ws, lora_stream_t stream, int32_t *status);
 
 /*
  * Test knob for the bounded waits of the tiled schedule's kernel (the one
- * lora_linear runs for M > 128, lora_linear_layers, lora_shrink,
- * lora_expand and lora_moe_gemm use) and of the split-K schedule's (64 < M
- * <= 128): each wait gives up after `cycles` SM clock cycles, sets
+ * lora_linear runs for M > 128, lora_linear_layers, lora_shrink and
+ * lora_expand use), of lora_moe_gemm's grouped expert kernel and of the
+ * split-K schedule's (64 < M <= 128): each wait gives up after `cycles` SM
+ * clock cycles, sets
  * LORA_DEV_TIMEOUT and lets the kernel run to its end.
  * cycles = 0 restores the default (2e9 cycles, about one second).  A budget
  * shorter than a healthy wait reports timeouts on healthy calls, so this is

@@ -2,7 +2,8 @@
 // A3", mokono.cn/news/2297686, its MoE section): route the (token, slot)
 // pairs to their experts, run the grouped expert matmul, then put every
 // token's rows back and sum them with the routing weights.  The grouped GEMM
-// is the tiled kernel in kModeMoe; this file holds the routing and the
+// is moe_pair.cu's kernel (the tiled kernel in kModeMoe for routings of more
+// token tiles than its item list holds); this file holds the routing and the
 // weighted finalize.
 //
 // Routing, in two launches over chunks of the pairs (one CTA per chunk):
