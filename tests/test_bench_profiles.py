@@ -2,6 +2,7 @@
 sources it was taken on: the hash covers the code, not its comments, and a
 summary whose hash differs yields no traffic figure."""
 import os
+import re
 import sys
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -52,3 +53,21 @@ def test_a_summary_on_other_sources_gives_no_traffic(tmp_path, monkeypatch):
     (prof / "lora_tc_kernel_prefill.md").write_text("traffic_bytes_per_launch: 1234\nsource_hash: 0000000000000000\n")
     assert bench.profiled_traffic("lora_tc_kernel", "prefill") is None
     assert bench.profiled_traffic("lora_tc_kernel", "qkv") is None   # no summary at all
+
+
+def test_committed_summaries_name_a_known_kernel_and_their_command():
+    """Every ncu summary under profiles/ gives the command that made it (ncu
+    with --clock-control none), a source hash, and, for a single kernel's
+    capture, its DRAM traffic per launch under the kernel's own name."""
+    prof = os.path.join(ROOT, "profiles")
+    names = sorted(f for f in os.listdir(prof) if f.endswith(".md"))
+    assert names
+    for f in names:
+        txt = open(os.path.join(prof, f)).read()
+        assert "ncu " in txt and "--clock-control none" in txt, f
+        assert re.search(r"^source_hash: [0-9a-f]{16}$", txt, re.M), f
+        if f.startswith("launches_"):
+            continue
+        kernel = next((k for k in bench.KERNEL_SOURCES if f.startswith(k + "_")), None)
+        assert kernel is not None, f
+        assert re.search(r"^traffic_bytes_per_launch: \d+$", txt, re.M), f
